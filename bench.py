@@ -1,0 +1,368 @@
+"""Benchmark of the KDA hot path on GB300.
+
+Default (one GPU): the single-sequence prefill workload (B=1, H=32, T=8192,
+dk=dv=128, bf16 inputs, fp32 state, chunk 64) timed through the C ABI, plus
+the batched decode workload (256 sequences x 32 heads, fp32 128x128 states,
+1000 consecutive steps).  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+--impl reference times the CPU oracle (fp64, the machine's host cores) on a
+bounded sample of the same workload and metric.
+Under torchrun (N > 1) every rank runs its own copy of the workload (the
+(sequence, head) units are independent: weak scaling, no collective on the
+data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (H=32,d=128) and decode state GB/s vs roofline, 1 GB300"
+PREFILL_WL = "prefill_8k"
+DECODE_WL = "decode_256"
+# algorithmic work per unit (derivation in the design doc)
+PREFILL_BYTES_PER_TOKEN_HEAD = 4 * 128 * 2 + 2 + 128 * 2      # q,k,v,g + b in, o out (bf16)
+INTRA_FLOP_PER_CHUNK_HEAD = 4 * 2 * 64 * 64 * 128              # A_kk, A_qk, W, U~ (dense)
+INTER_FLOP_PER_CHUNK_HEAD = 2 * 64 * 128 * 128 * 2 + 2 * 64 * 64 * 128 + 2 * 128 * 64 * 128
+DECODE_STATE_BYTES_PER_HEAD = 2 * 128 * 128 * 4                # read + write fp32 state
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() in ("active", "1"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def flush_l2(buf):
+    buf.zero_()
+
+
+def bench_prefill(torch, kda, W, steps, warmup, dev):
+    w = W.WORKLOADS[PREFILL_WL]
+    inp = W.prefill_inputs(w, device=dev, gen_device=dev)
+    T = sum(inp["lens"])
+    p = kda.Prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["b"], inp["cu_seqlens"],
+                    host_cu_seqlens=inp["cu_seqlens"].cpu())
+    nph = kda.PREFILL_PHASES
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)]
+    ev_handles = (kda.c_vp * (nph + 1))(*[e.cuda_event for e in ev])
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > L2 (129 MB)
+    for _ in range(warmup):
+        flush_l2(flush)
+        p.run()
+    torch.cuda.synchronize()
+    p.args.phase_events = kda.ctypes.cast(ev_handles, kda.c_vp)
+    step_ms, phase_ms = [], [[] for _ in range(nph)]
+    for _ in range(steps):
+        flush_l2(flush)
+        p.run(stream)
+        ev[-1].synchronize()
+        step_ms.append(ev[0].elapsed_time(ev[-1]))
+        for i in range(nph):
+            phase_ms[i].append(ev[i].elapsed_time(ev[i + 1]))
+    p.args.phase_events = None
+    torch.cuda.synchronize()
+    assert p.device_status() == 0
+    n_chunks = (T + 63) // 64
+    return dict(T=T, H=w.H, step_ms=step_ms, phase_ms=phase_ms, n_chunks=n_chunks,
+                launches_per_step=4, workload=w)
+
+
+def bench_decode(torch, kda, W, steps, warmup, dev):
+    dw = W.DECODE_WORKLOADS[DECODE_WL]
+    n = steps + warmup
+    inp = W.decode_inputs(dw, steps=n, device=dev, gen_device=dev)
+    state = inp["state"]
+    o = torch.empty(dw.batch, dw.H, dw.dv, dtype=torch.bfloat16, device=dev)
+    args = [[inp[x][s] for x in "qkvgb"] for s in range(n)]
+    for s in range(warmup):
+        kda.kda_decode_step(*args[s], state, o)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(warmup, n):
+        kda.kda_decode_step(*args[s], state, o)
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    heads = dw.batch * dw.H
+    return dict(ms_per_step=ms, heads=heads, batch=dw.batch, steps=steps, workload=dw)
+
+
+def bench_e2e(torch, kda, W, steps, warmup, dev):
+    w = W.WORKLOADS[PREFILL_WL]
+    inp = W.prefill_inputs(w)  # host tensors
+    host = {x: inp[x].pin_memory() for x in "qkvgb"}
+    cu = inp["cu_seqlens"]
+    T = sum(inp["lens"])
+    h2d = sum(host[x].numel() * host[x].element_size() for x in "qkvgb") + cu.numel() * 8
+    d2h = T * w.H * w.dv * 2 + w.n_seqs * w.H * w.dk * w.dv * 4
+    for _ in range(warmup):
+        kda.prefill_host(host["q"], host["k"], host["v"], host["g"], host["b"], cu, device=dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        kda.prefill_host(host["q"], host["k"], host["v"], host["g"], host["b"], cu, device=dev)
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    return dict(value=T / dt, unit="tokens/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                ms_per_step=dt * 1e3)
+
+
+def cpu_baseline(seconds_budget=20.0):
+    """The oracle, as it stands, on a bounded sample of the prefill workload:
+    all T=8192 tokens of the first heads that fit the time budget."""
+    import oracle
+    from linear_attention_serving_delta_gb300 import workloads as W
+    w = W.WORKLOADS[PREFILL_WL]
+    inp = W.prefill_inputs(w)
+    f = lambda t: t.float().numpy()
+    q, k, v, g, b = (f(inp[x]) for x in "qkvgb")
+    cu = inp["cu_seqlens"].numpy()
+    cores = oracle.max_threads()
+    heads = min(w.H, max(cores, 1))
+    t0 = time.perf_counter()
+    oracle.prefill(q, k, v, g, b, cu, heads=(0, heads))
+    dt = time.perf_counter() - t0
+    if dt < seconds_budget / 4 and heads < w.H:
+        heads = w.H
+        t0 = time.perf_counter()
+        oracle.prefill(q, k, v, g, b, cu, heads=(0, heads))
+        dt = time.perf_counter() - t0
+    T = sum(inp["lens"])
+    # tokens/s at H=32: token-heads per second / 32
+    value = T * heads / w.H / dt
+    return {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"prefill_8k, all {T} tokens of {heads}/{w.H} heads, fp64, {dt:.2f} s"}
+
+
+def gpu_arm(a):
+    import torch
+    import torch.distributed as dist
+    from linear_attention_serving_delta_gb300 import kda
+    from linear_attention_serving_delta_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+    kda.lib()
+    pk = peaks()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    with ClockSampler(local) as clk:
+        pre = bench_prefill(torch, kda, W, a.steps, a.warmup, dev)
+        barrier()
+        dec = bench_decode(torch, kda, W, a.decode_steps, max(3, a.warmup), dev)
+        barrier()
+    step_ms = sum(pre["step_ms"]) / len(pre["step_ms"])
+    dec_ms = dec["ms_per_step"]
+    if world > 1:
+        t = torch.tensor([step_ms, dec_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, dec_ms = t.tolist()
+    e2e = bench_e2e(torch, kda, W, max(1, min(a.steps, 5)), 1, dev) if rank == 0 else None
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    T, H = pre["T"], pre["H"]
+    value = world * T / (step_ms * 1e-3)
+    ph = [sum(x) / len(x) for x in pre["phase_ms"]]
+    names = ["plan", "intra_chunk", "inter_chunk"]
+    kernels = {n: {"ms": m, "share": m / max(sum(ph), 1e-12)} for n, m in zip(names, ph)}
+    chunk_heads = pre["n_chunks"] * H
+    intra_tflops = INTRA_FLOP_PER_CHUNK_HEAD * chunk_heads / (ph[1] * 1e-3) / 1e12
+    inter_tflops = INTER_FLOP_PER_CHUNK_HEAD * chunk_heads / (ph[2] * 1e-3) / 1e12
+    prefill_gbs = PREFILL_BYTES_PER_TOKEN_HEAD * T * H / (step_ms * 1e-3) / 1e9
+    kernels["intra_chunk"]["achieved_tflops"] = intra_tflops
+    kernels["inter_chunk"]["achieved_tflops"] = inter_tflops
+    kernels["inter_chunk"]["us_per_chunk_step"] = ph[2] * 1e3 / pre["n_chunks"]
+    dom = max(range(3), key=lambda i: ph[i])
+    if names[dom] == "intra_chunk":
+        roof = {"kernel": "intra_chunk", "bound": "tensor", "achieved": intra_tflops,
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": intra_tflops / pk["bf16_tflops"], "traffic": None}
+    else:
+        # the serial inter-chunk kernel: its algorithmic FLOPs against the tensor peak
+        roof = {"kernel": names[dom], "bound": "tensor", "achieved": inter_tflops,
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": inter_tflops / pk["bf16_tflops"], "traffic": None}
+    roof["peak_source"] = pk["source"]
+    dec_gbs = DECODE_STATE_BYTES_PER_HEAD * dec["heads"] / (dec_ms * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": W.WORKLOADS[PREFILL_WL].description,
+                   "global_batch": world, "seq_len": T, "heads": H, "dk": 128, "dv": 128,
+                   "chunk": 64, "parallelism": f"replicas{world}",
+                   "l2": "512 MB buffer written between timed steps (inputs 268 MB > L2)",
+                   "decode_workload": W.DECODE_WORKLOADS[DECODE_WL].description},
+        "roofline": roof,
+        "prefill_hbm": {"achieved": prefill_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": prefill_gbs / pk["hbm_gbs"],
+                        "algorithmic_bytes_per_token_head": PREFILL_BYTES_PER_TOKEN_HEAD},
+        "decode": {"state_gbs": dec_gbs, "us_per_step": dec_ms * 1e3,
+                   "tokens_per_s": world * dec["batch"] / (dec_ms * 1e-3),
+                   "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": pk["hbm_gbs"],
+                                "unit": "GB/s", "frac": dec_gbs / pk["hbm_gbs"],
+                                "traffic": None, "peak_source": pk["source"]},
+                   "steps": dec["steps"]},
+        "kernels": kernels,
+        "e2e": {"value": e2e["value"], "unit": e2e["unit"],
+                "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+                "ms_per_step": e2e["ms_per_step"]},
+        "gpu_launches": pre["launches_per_step"] * a.steps + dec["steps"],
+        "clocks": clk.summary(),
+    }
+    if not a.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- reference arm
+def reference_arm(a):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from linear_attention_serving_delta_gb300 import workloads as W
+    oracle.build()
+    w = W.WORKLOADS[PREFILL_WL]
+    inp = W.prefill_inputs(w)
+    f = lambda t: t.float().numpy()
+    q, k, v, g, b = (f(inp[x]) for x in "qkvgb")
+    cu = inp["cu_seqlens"].numpy()
+    T = sum(inp["lens"])
+    cores = oracle.max_threads()
+    heads = min(w.H, max(1, cores))       # one head per core: a bounded sample per step
+    for _ in range(a.warmup):
+        oracle.prefill(q, k, v, g, b, cu, heads=(0, heads))
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        oracle.prefill(q, k, v, g, b, cu, heads=(0, heads))
+    dt = (time.perf_counter() - t0) / a.steps
+    value = T * heads / w.H / dt
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+           "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": a.steps,
+           "warmup": a.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": w.description, "global_batch": 1, "seq_len": T,
+                      "heads_per_step": heads, "parallelism": "cpu-oracle"},
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                            "sample": f"all {T} tokens of {heads}/{w.H} heads per step"},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        a.warmup = 3
+    if a.impl == "reference":
+        reference_arm(a)
+    else:
+        gpu_arm(a)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+/*
+ * kda.h -- C ABI of libkda, a GB300 (sm_103a) library for the Kimi Delta
+ * Attention (KDA) recurrence.
+ *
+ * The operation.  Each attention head keeps one fixed-size fp32 state
+ * S in R^{dk x dv}.  For every token t of a sequence:
+ *
+ *     q^ = q_t / max(|q_t|, 1e-6)           k^ = k_t / max(|k_t|, 1e-6)
+ *     alpha_t = exp(-softplus(g_t))  (per key channel, dk values)
+ *     beta_t  = sigmoid(b_t)         (one value per token and head)
+ *     S_t = (I - beta_t k^ k^T) Diag(alpha_t) S_{t-1} + beta_t k^ v_t^T
+ *     o_t = scale * S_t^T q^
+ *
+ *   - "From KV Cache to Depth Attention: The Bottlenecks Kimi K3 Had to
+ *     Break", Technical Details: the state predicts the value from its
+ *     memory and writes back only the difference; alpha is retention, beta
+ *     update strength, and each feature channel has its own timescale.
+ *   - "Kimi K3: The Manos, The Mythos, The Legendos", bullet list: delta
+ *     rule plus a forget gate made diagonal; L2-normalised queries and keys;
+ *     FlashKDA's chunked unrolling gives linear prefill and constant-cost
+ *     decode.  Its Context section: the serving engine keeps state snapshots
+ *     at prompt boundaries so that later requests can resume from them.
+ *
+ * Conventions shared by every call.
+ *   - Every tensor is caller-owned device memory, row-major and contiguous,
+ *     token-major: q, k, g [T, H, dk]; v, o [T, H, dv]; b [T, H]; states
+ *     [.., H, dk, dv] fp32.  The library allocates nothing and keeps no
+ *     mutable global state; calls from several host threads are safe.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream).  Arguments are validated on the host before any
+ *     launch; on an error nothing is launched and the status says why.
+ *   - Values that live on the device (cu_seqlens, boundary positions, slot
+ *     indices) are checked by the kernels: a malformed value raises a flag
+ *     in the workspace status word (see kda_prefill_device_status) and the
+ *     affected sequence is skipped; no kernel traps.
+ *   - Outputs must not alias inputs; snapshots, initial and final states must
+ *     not overlap one another.
+ *   - No C++ exception crosses this boundary.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1, /* null pointer, bad size, inconsistent argument  */
+  KDA_ERR_UNSUPPORTED = 2, /* head size or dtype this build does not cover   */
+  KDA_ERR_WORKSPACE = 3,   /* workspace missing, too small or misaligned     */
+  KDA_ERR_CUDA = 4,        /* a CUDA launch or query failed                  */
+  KDA_ERR_TIMEOUT = 5,     /* a bounded device-side wait expired             */
+  KDA_ERR_DEVICE_DATA = 6  /* a device-side index array was malformed        */
+} kda_status_t;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
+
+/* Chunk length of the chunked prefill (tokens). */
+#define KDA_CHUNK 64
+
+/*
+ * Prefill over packed variable-length sequences.
+ *
+ * Sequence s holds packed tokens [cu_seqlens[s], cu_seqlens[s+1]).  Each
+ * (sequence, head) starts from initial_state (or zeros), runs the
+ * recurrence over its tokens, writes o for every token, its final state and
+ * the snapshots it owns.
+ *
+ * Snapshot positions (seq-relative token counts p, the state after p tokens,
+ * as in "Kimi K3: The Manos, The Mythos, The Legendos", Context) of sequence
+ * s are the sorted, de-duplicated union of
+ *   { p : p % snapshot_interval == 0, 0 < p <= len }   (if interval > 0)
+ *   boundary_pos[cu_boundaries[s] .. cu_boundaries[s+1])  (if given)
+ * Snapshot j of sequence s goes to snapshots[cu_snapshots[s] + j].
+ * kda_snapshot_plan() computes cu_snapshots on the host.
+ */
+typedef struct {
+  int32_t num_seqs;            /* N >= 1                                          */
+  int32_t num_heads;           /* H >= 1                                          */
+  int32_t dk, dv;              /* each in {16, 32, 64, 128}                       */
+  int64_t total_tokens;        /* T = cu_seqlens[N]; host-known upper bound, >= 0 */
+  const int64_t* cu_seqlens;   /* device [N+1], cu[0] = 0, non-decreasing         */
+  kda_dtype_t in_dtype;        /* dtype of q, k, v, g, b and of o                 */
+  const void* q;               /* device [T, H, dk]                               */
+  const void* k;               /* device [T, H, dk]                               */
+  const void* v;               /* device [T, H, dv]                               */
+  const void* g;               /* device [T, H, dk], decay logit                  */
+  const void* b;               /* device [T, H], update logit                     */
+  float scale;                 /* o = scale * S^T q^; 1.0 is the plain recurrence */
+  const float* initial_state;  /* device [N, H, dk, dv] or NULL (zeros)           */
+  void* o;                     /* device [T, H, dv], in_dtype                     */
+  float* final_state;          /* device [N, H, dk, dv] or NULL                   */
+  int64_t snapshot_interval;   /* 0 = off, else a positive multiple of KDA_CHUNK  */
+  const int64_t* boundary_pos; /* device, per sequence strictly increasing in [1, len], or NULL */
+  const int64_t* cu_boundaries;/* device [N+1] offsets into boundary_pos (NULL iff boundary_pos is) */
+  int64_t num_boundaries;      /* host-known total entries of boundary_pos (0 if NULL) */
+  const int64_t* cu_snapshots; /* device [N+1] snapshot slot offsets, or NULL if no snapshots */
+  float* snapshots;            /* device [num_snapshots, H, dk, dv] or NULL       */
+  int64_t num_snapshots;       /* host-known rows of `snapshots`; a slot at or past
+                                  it is not written and raises status flag 2     */
+  void* const* phase_events;   /* NULL, or KDA_PREFILL_PHASES + 1 cudaEvent_t the call
+                                  records on `stream` before the first phase and after
+                                  each phase (chunk planning, intra-chunk,
+                                  inter-chunk), for per-kernel timing             */
+} kda_prefill_args;
+
+/* Number of timed phases of kda_prefill (see phase_events). */
+#define KDA_PREFILL_PHASES 3
+
+/* Bytes of device workspace kda_prefill needs for these arguments (reads
+ * only host-side fields).  Returns 0 if the arguments are invalid. */
+size_t kda_prefill_workspace_size(const kda_prefill_args* args);
+
+/* Runs the prefill.  ws: device buffer of at least
+ * kda_prefill_workspace_size(args) bytes, 256-byte aligned, owned by the
+ * caller and not used by another call in flight.  The path is chosen by the
+ * arguments: bf16 inputs with dk = dv = 128 run on the tcgen05 tensor-core
+ * kernels; every other supported shape runs on fp32 CUDA-core kernels. */
+kda_status_t kda_prefill(const kda_prefill_args* args, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* Copies the workspace status word of the last kda_prefill that used `ws`
+ * to *out (host), synchronising `stream`.  0 = clean; otherwise a bitwise OR
+ * of 1 (malformed cu_seqlens), 2 (malformed boundary positions), 4 (chunk
+ * table overflow), 8 (bounded wait expired). */
+kda_status_t kda_prefill_device_status(const void* ws, int32_t* out, void* stream);
+
+/* Host helper: snapshot slot offsets.  From host copies of cu_seqlens [n+1],
+ * the interval and the boundary positions (may be NULL), fills
+ * cu_snapshots_out [n+1] and returns the total number of snapshots, or -1 on
+ * invalid input (boundaries not strictly increasing inside [1, len]). */
+int64_t kda_snapshot_plan(const int64_t* h_cu_seqlens, int32_t n, int64_t interval,
+                          const int64_t* h_boundary_pos, const int64_t* h_cu_boundaries,
+                          int64_t* h_cu_snapshots_out);
+
+/*
+ * One decode step for a batch of independent rows ("constant decode": a
+ * single-token advance of each fixed-size state).  Row r advances the state
+ * in pool slot state_slots[r] (slot r if state_slots is NULL; a negative
+ * slot skips the row and leaves its o untouched) by its one token and
+ * writes o.  The state is read once and written once, in place.
+ */
+typedef struct {
+  int32_t batch;               /* B >= 0 rows                                     */
+  int32_t num_heads;           /* H                                               */
+  int32_t dk, dv;              /* each in {16, 32, 64, 128}                       */
+  int32_t num_slots;           /* rows of the state pool                          */
+  kda_dtype_t in_dtype;        /* dtype of q, k, v, g, b and of o                 */
+  float scale;
+  const void* q;               /* device [B, H, dk]                               */
+  const void* k;               /* device [B, H, dk]                               */
+  const void* v;               /* device [B, H, dv]                               */
+  const void* g;               /* device [B, H, dk]                               */
+  const void* b;               /* device [B, H]                                   */
+  float* state;                /* device pool [num_slots, H, dk, dv], in place    */
+  const int32_t* state_slots;  /* device [B] or NULL; two rows must not share a slot */
+  void* o;                     /* device [B, H, dv]                               */
+} kda_decode_args;
+
+kda_status_t kda_decode_step(const kda_decode_args* args, void* stream);
+
+/*
+ * The preparation step on its own: for every token and head, q^ and k^
+ * (L2-normalised), beta = sigmoid(b), and G, the running sum of
+ * log alpha = -softplus(g) restarted at the start of each chunk of
+ * KDA_CHUNK tokens of each sequence (chunks counted from the sequence
+ * start).  kda_prefill performs the same step inside its intra-chunk kernel;
+ * this entry exposes it.  Outputs are fp32: qhat, khat, G [T, H, dk];
+ * beta [T, H].  Needs no workspace.
+ */
+typedef struct {
+  int32_t num_seqs, num_heads, dk;
+  int64_t total_tokens;
+  const int64_t* cu_seqlens;   /* device [N+1]                                    */
+  kda_dtype_t in_dtype;
+  const void* q;
+  const void* k;
+  const void* g;
+  const void* b;
+  float* qhat;                 /* device [T, H, dk]                               */
+  float* khat;                 /* device [T, H, dk]                               */
+  float* G;                    /* device [T, H, dk]                               */
+  float* beta;                 /* device [T, H]                                   */
+} kda_prep_args;
+
+kda_status_t kda_prep(const kda_prep_args* args, void* stream);
+
+/* Static description of a status code. */
+const char* kda_status_string(kda_status_t status);
+
+/* Library version string. */
+const char* kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

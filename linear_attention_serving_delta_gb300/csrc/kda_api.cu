@@ -1,0 +1,215 @@
+// kda_api.cu -- the extern "C" entry points of libkda: argument validation,
+// workspace layout and kernel launches.  Declarations and contracts are in
+// include/kda.h.
+#include <new>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+bool head_size_ok(int32_t d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool dtype_ok(kda_dtype_t t) { return t == KDA_F32 || t == KDA_BF16; }
+
+bool use_tensor_cores(const kda_prefill_args* a) {
+  return kHaveTensorCorePath && a->in_dtype == KDA_BF16 && a->dk == 128 && a->dv == 128;
+}
+
+kda_status_t validate_prefill(const kda_prefill_args* a) {
+  if (!a) return KDA_ERR_INVALID_ARG;
+  if (a->num_seqs < 1 || a->num_heads < 1 || a->total_tokens < 0) return KDA_ERR_INVALID_ARG;
+  if (!dtype_ok(a->in_dtype)) return KDA_ERR_INVALID_ARG;
+  if (!head_size_ok(a->dk) || !head_size_ok(a->dv)) return KDA_ERR_UNSUPPORTED;
+  if (!a->cu_seqlens) return KDA_ERR_INVALID_ARG;
+  if (a->total_tokens > 0 && (!a->q || !a->k || !a->v || !a->g || !a->b || !a->o))
+    return KDA_ERR_INVALID_ARG;
+  if (a->snapshot_interval < 0 || a->snapshot_interval % KDA_CHUNK != 0) return KDA_ERR_INVALID_ARG;
+  if ((a->boundary_pos == nullptr) != (a->cu_boundaries == nullptr)) return KDA_ERR_INVALID_ARG;
+  if (a->num_boundaries < 0 || (!a->boundary_pos && a->num_boundaries != 0))
+    return KDA_ERR_INVALID_ARG;
+  if ((a->snapshots == nullptr) != (a->cu_snapshots == nullptr)) return KDA_ERR_INVALID_ARG;
+  if (a->num_snapshots < 0 || (a->snapshots && a->num_snapshots == 0)) return KDA_ERR_INVALID_ARG;
+  // sizes whose products must stay inside the index types used by the kernels
+  if (a->total_tokens > ((int64_t)1 << 40)) return KDA_ERR_UNSUPPORTED;
+  return KDA_OK;
+}
+
+WsLayout prefill_layout(const kda_prefill_args* a) {
+  WsLayout L;
+  const int64_t N = a->num_seqs, nb = a->num_boundaries;
+  L.max_chunks = (a->total_tokens + kChunk - 1) / kChunk + N + nb;
+  L.rec_bytes = use_tensor_cores(a) ? tc_record_bytes()
+                                    : SimtRec::floats(a->dk, a->dv) * sizeof(float);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  L.status = take(sizeof(int32_t) * 4);
+  L.meta = take(sizeof(PlanMeta));
+  L.seq_len = 0;
+  L.seq_seg_begin = take(sizeof(int64_t) * (N + 1));
+  L.seq_chunk_begin = take(sizeof(int64_t) * (N + 1));
+  L.bnd_nonaligned = take(sizeof(int32_t) * (nb + N + 1));
+  L.bnd_nonmult = take(sizeof(int32_t) * (nb + N + 1));
+  L.seq_aux = take(sizeof(int64_t) * 3 * N);  // seq_len [N] + seq_bnd [2N]
+  L.chunks = take(sizeof(Chunk) * (size_t)L.max_chunks);
+  L.inter = take(L.rec_bytes * (size_t)L.max_chunks * (size_t)a->num_heads);
+  L.total = off;
+  return L;
+}
+
+kda_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+size_t kda_prefill_workspace_size(const kda_prefill_args* args) {
+  if (validate_prefill(args) != KDA_OK) return 0;
+  return prefill_layout(args).total;
+}
+
+kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, void* stream_) {
+  kda_status_t st = validate_prefill(a);
+  if (st != KDA_OK) return st;
+  const WsLayout L = prefill_layout(a);
+  if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255) != 0)
+    return KDA_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  char* w = static_cast<char*>(ws);
+
+  PlanParams pp{};
+  pp.num_seqs = a->num_seqs;
+  pp.total_tokens = a->total_tokens;
+  pp.cu_seqlens = a->cu_seqlens;
+  pp.snapshot_interval = a->snapshot_interval;
+  pp.boundary_pos = a->boundary_pos;
+  pp.cu_boundaries = a->cu_boundaries;
+  pp.num_boundaries = a->num_boundaries;
+  pp.cu_snapshots = a->cu_snapshots;
+  pp.num_snapshots = a->snapshots ? a->num_snapshots : 0;
+  pp.max_chunks = L.max_chunks;
+  pp.status = reinterpret_cast<int32_t*>(w + L.status);
+  pp.meta = reinterpret_cast<PlanMeta*>(w + L.meta);
+  pp.seq_seg_begin = reinterpret_cast<int64_t*>(w + L.seq_seg_begin);
+  pp.seq_chunk_begin = reinterpret_cast<int64_t*>(w + L.seq_chunk_begin);
+  pp.bnd_nonaligned = reinterpret_cast<int32_t*>(w + L.bnd_nonaligned);
+  pp.bnd_nonmult = reinterpret_cast<int32_t*>(w + L.bnd_nonmult);
+  pp.seq_len = reinterpret_cast<int64_t*>(w + L.seq_aux);
+  pp.seq_bnd = pp.seq_len + a->num_seqs;
+  pp.chunks = reinterpret_cast<Chunk*>(w + L.chunks);
+
+  cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(a->phase_events);
+  auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
+
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w + L.status, 0, 256, stream);
+  if (e == cudaSuccess) e = launch_plan(pp, stream);
+  if (e == cudaSuccess) e = mark(1);
+  if (e != cudaSuccess) return KDA_ERR_CUDA;
+
+  ChunkParams cp{};
+  cp.num_seqs = a->num_seqs;
+  cp.H = a->num_heads;
+  cp.dk = a->dk;
+  cp.dv = a->dv;
+  cp.max_chunks = L.max_chunks;
+  cp.q = a->q;
+  cp.k = a->k;
+  cp.v = a->v;
+  cp.g = a->g;
+  cp.b = a->b;
+  cp.scale = a->scale;
+  cp.initial_state = a->initial_state;
+  cp.o = a->o;
+  cp.final_state = a->final_state;
+  cp.snapshots = a->snapshots;
+  cp.status = pp.status;
+  cp.meta = pp.meta;
+  cp.seq_chunk_begin = pp.seq_chunk_begin;
+  cp.chunks = pp.chunks;
+  cp.inter = reinterpret_cast<float*>(w + L.inter);
+  cp.rec_floats = L.rec_bytes / sizeof(float);
+  e = use_tensor_cores(a) ? launch_tc_prefill(cp, stream, ev ? ev[2] : nullptr)
+                          : launch_simt_prefill(cp, a->in_dtype, stream, ev ? ev[2] : nullptr);
+  if (e == cudaSuccess) e = mark(3);
+  return from_cuda(e);
+}
+
+kda_status_t kda_prefill_device_status(const void* ws, int32_t* out, void* stream_) {
+  if (!ws || !out) return KDA_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return KDA_ERR_CUDA;
+  *out = v;
+  return KDA_OK;
+}
+
+int64_t kda_snapshot_plan(const int64_t* h_cu, int32_t n, int64_t interval,
+                          const int64_t* h_bpos, const int64_t* h_cub, int64_t* out) {
+  if (!h_cu || !out || n < 1 || interval < 0) return -1;
+  if ((h_bpos == nullptr) != (h_cub == nullptr)) return -1;
+  out[0] = 0;
+  for (int32_t s = 0; s < n; ++s) {
+    const int64_t len = h_cu[s + 1] - h_cu[s];
+    if (len < 0) return -1;
+    int64_t cnt = interval > 0 ? len / interval : 0;
+    if (h_bpos) {
+      for (int64_t i = h_cub[s]; i < h_cub[s + 1]; ++i) {
+        const int64_t x = h_bpos[i];
+        if (x < 1 || x > len || (i > h_cub[s] && x <= h_bpos[i - 1])) return -1;
+        if (interval <= 0 || x % interval != 0) ++cnt;
+      }
+    }
+    out[s + 1] = out[s] + cnt;
+  }
+  return out[n];
+}
+
+kda_status_t kda_decode_step(const kda_decode_args* a, void* stream) {
+  if (!a) return KDA_ERR_INVALID_ARG;
+  if (a->batch < 0 || a->num_heads < 1 || a->num_slots < 0) return KDA_ERR_INVALID_ARG;
+  if (!dtype_ok(a->in_dtype)) return KDA_ERR_INVALID_ARG;
+  if (!head_size_ok(a->dk) || !head_size_ok(a->dv)) return KDA_ERR_UNSUPPORTED;
+  if (a->batch == 0) return KDA_OK;
+  if (!a->q || !a->k || !a->v || !a->g || !a->b || !a->state || !a->o) return KDA_ERR_INVALID_ARG;
+  if (!a->state_slots && a->num_slots < a->batch) return KDA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(a->state) & 15) != 0) return KDA_ERR_INVALID_ARG;
+  return from_cuda(launch_decode(*a, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status_t kda_prep(const kda_prep_args* a, void* stream) {
+  if (!a) return KDA_ERR_INVALID_ARG;
+  if (a->num_seqs < 1 || a->num_heads < 1 || a->total_tokens < 0) return KDA_ERR_INVALID_ARG;
+  if (!dtype_ok(a->in_dtype)) return KDA_ERR_INVALID_ARG;
+  if (!head_size_ok(a->dk)) return KDA_ERR_UNSUPPORTED;
+  if (!a->cu_seqlens) return KDA_ERR_INVALID_ARG;
+  if (a->total_tokens > 0 &&
+      (!a->q || !a->k || !a->g || !a->b || !a->qhat || !a->khat || !a->G || !a->beta))
+    return KDA_ERR_INVALID_ARG;
+  return from_cuda(launch_prep(*a, static_cast<cudaStream_t>(stream)));
+}
+
+const char* kda_status_string(kda_status_t s) {
+  switch (s) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported head size or dtype";
+    case KDA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case KDA_ERR_CUDA: return "CUDA launch or query failed";
+    case KDA_ERR_TIMEOUT: return "bounded device wait expired";
+    case KDA_ERR_DEVICE_DATA: return "malformed device-side index data";
+  }
+  return "unknown status";
+}
+
+const char* kda_version(void) { return "libkda 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// kda_internal.cuh -- parameter blocks and launcher declarations shared by the
+// translation units of libkda (not part of the public ABI).
+#pragma once
+
+#include "kda_common.cuh"
+
+namespace kda {
+
+struct PlanParams {
+  int32_t num_seqs;
+  int64_t total_tokens;
+  const int64_t* cu_seqlens;
+  int64_t snapshot_interval;
+  const int64_t* boundary_pos;
+  const int64_t* cu_boundaries;
+  int64_t num_boundaries;
+  const int64_t* cu_snapshots;
+  int64_t num_snapshots;
+  int64_t max_chunks;
+  // workspace outputs
+  int32_t* status;
+  PlanMeta* meta;
+  int64_t* seq_len;         // [N]
+  int64_t* seq_seg_begin;   // [N+1]
+  int64_t* seq_chunk_begin; // [N+1]
+  int64_t* seq_bnd;         // [2N] usable boundary range per sequence
+  int32_t* bnd_nonaligned;  // [num_boundaries + N]
+  int32_t* bnd_nonmult;     // [num_boundaries + N]
+  Chunk* chunks;            // [max_chunks]
+};
+
+// Everything the intra-chunk and inter-chunk kernels read.
+struct ChunkParams {
+  int32_t num_seqs, H, dk, dv;
+  int64_t max_chunks;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* g;
+  const void* b;
+  float scale;
+  const float* initial_state;
+  void* o;
+  float* final_state;
+  float* snapshots;
+  // workspace
+  int32_t* status;
+  const PlanMeta* meta;
+  const int64_t* seq_chunk_begin;
+  const Chunk* chunks;
+  float* inter;     // [max_chunks][H] records
+  size_t rec_floats;
+};
+
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
+
+// fp32 CUDA-core path (any supported dk, dv; f32 or bf16 inputs)
+// `mid` (may be null) is recorded on the stream between the intra-chunk and
+// the inter-chunk kernels.
+cudaError_t launch_simt_prefill(const ChunkParams& p, kda_dtype_t dt, cudaStream_t stream,
+                                cudaEvent_t mid);
+
+// tcgen05 tensor-core path (bf16 inputs, dk = dv = 128)
+extern const bool kHaveTensorCorePath;
+size_t tc_record_bytes();
+cudaError_t launch_tc_prefill(const ChunkParams& p, cudaStream_t stream, cudaEvent_t mid);
+
+cudaError_t launch_decode(const kda_decode_args& a, cudaStream_t stream);
+cudaError_t launch_prep(const kda_prep_args& a, cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,208 @@
+// kda_plan.cu -- builds the chunk table of a prefill call on the device.
+//
+// The chunked prefill ("Kimi K3: The Manos, The Mythos, The Legendos":
+// FlashKDA unrolls the recurrence in chunks) needs the sequence cut into
+// runs of at most KDA_CHUNK tokens.  Cut points of sequence s are the
+// multiples of KDA_CHUNK, every boundary position (snapshots must fall on a
+// chunk end, as the snapshot of a prompt boundary is the state after its last
+// token, same page, Context) and the sequence end.  Snapshot interval
+// multiples are multiples of KDA_CHUNK and need no extra cut.
+//
+// Two launches, no host synchronisation:
+//   plan_sequences (one CTA): validates cu_seqlens and boundaries, counts the
+//     aligned segments and chunks per sequence, prefix-sums them.
+//   plan_fill (grid over aligned segments): writes the chunk entries.
+#include "kda_internal.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+__device__ __forceinline__ int64_t lower_bound_i64(const int64_t* a, int64_t lo, int64_t hi,
+                                                   int64_t x) {
+  while (lo < hi) {
+    int64_t mid = (lo + hi) >> 1;
+    if (a[mid] < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int64_t upper_bound_i64(const int64_t* a, int64_t lo, int64_t hi,
+                                                   int64_t x) {
+  while (lo < hi) {
+    int64_t mid = (lo + hi) >> 1;
+    if (a[mid] <= x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// Block-wide exclusive scan of one value per thread; `total` receives the sum.
+__device__ int64_t block_exclusive_scan(int64_t x, int64_t* sh, int64_t& total) {
+  const int tid = threadIdx.x;
+  sh[tid] = x;
+  __syncthreads();
+  for (int off = 1; off < kPlanThreads; off <<= 1) {
+    int64_t y = tid >= off ? sh[tid - off] : 0;
+    __syncthreads();
+    sh[tid] += y;
+    __syncthreads();
+  }
+  const int64_t incl = sh[tid];
+  total = sh[kPlanThreads - 1];
+  __syncthreads();  // every thread has read before sh is reused
+  return incl - x;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+plan_sequences(PlanParams p) {
+  __shared__ int64_t sh[kPlanThreads];
+  const int tid = threadIdx.x;
+  int32_t flags = 0;
+  int64_t seg_carry = 0, chunk_carry = 0;
+  for (int32_t base = 0; base < p.num_seqs; base += kPlanThreads) {
+    const int32_t s = base + tid;
+    int64_t nseg = 0, nchunk = 0;
+    if (s < p.num_seqs) {
+      int64_t c0 = p.cu_seqlens[s], c1 = p.cu_seqlens[s + 1];
+      int64_t len = c1 - c0;
+      bool ok = (c0 >= 0) && (len >= 0) && (c1 <= p.total_tokens) && (s > 0 || c0 == 0);
+      if (!ok) { flags |= kFlagBadSeqlens; len = 0; }
+      int64_t b0 = 0, b1 = 0;
+      if (p.boundary_pos) {
+        b0 = p.cu_boundaries[s];
+        b1 = p.cu_boundaries[s + 1];
+        bool bok = b0 >= 0 && b1 >= b0 && b1 <= p.num_boundaries;
+        for (int64_t i = b0; bok && i < b1; ++i) {
+          int64_t x = p.boundary_pos[i];
+          if (x < 1 || x > len || (i > b0 && x <= p.boundary_pos[i - 1])) bok = false;
+        }
+        if (!bok) { flags |= kFlagBadBoundaries; b0 = b1 = 0; }
+      }
+      // empty range (b0 == b1): the prefix arrays are neither written nor read
+      p.seq_bnd[2 * s] = b0;
+      p.seq_bnd[2 * s + 1] = b1;
+      // prefix counts of non-aligned boundaries (they add a cut) and of
+      // boundaries that are not interval multiples (they add a snapshot);
+      // entry i + s for i in [b0, b1] (the +s keeps sequences apart)
+      int32_t na = 0, nm = 0;
+      int64_t extra = 0;
+      if (b1 > b0) {
+        for (int64_t i = b0; i < b1; ++i) {
+          p.bnd_nonaligned[i + s] = na;
+          p.bnd_nonmult[i + s] = nm;
+          const int64_t x = p.boundary_pos[i];
+          if (x % kChunk != 0) { ++na; if (x < len) ++extra; }
+          if (p.snapshot_interval <= 0 || x % p.snapshot_interval != 0) ++nm;
+        }
+        p.bnd_nonaligned[b1 + s] = na;
+        p.bnd_nonmult[b1 + s] = nm;
+      }
+      nseg = (len + kChunk - 1) / kChunk;
+      nchunk = nseg + extra;
+      p.seq_len[s] = len;
+    }
+    int64_t seg_total = 0, ch_total = 0;
+    const int64_t seg_ex = block_exclusive_scan(nseg, sh, seg_total);
+    const int64_t ch_ex = block_exclusive_scan(nchunk, sh, ch_total);
+    if (s < p.num_seqs) {
+      p.seq_seg_begin[s] = seg_carry + seg_ex;
+      p.seq_chunk_begin[s] = chunk_carry + ch_ex;
+    }
+    seg_carry += seg_total;
+    chunk_carry += ch_total;
+  }
+  // reduce flags
+  __shared__ int32_t shf;
+  if (tid == 0) shf = 0;
+  __syncthreads();
+  if (flags) atomicOr(&shf, flags);
+  __syncthreads();
+  if (tid == 0) {
+    int32_t f = shf;
+    int64_t total = chunk_carry;
+    if (total > p.max_chunks) { f |= kFlagChunkOverflow; total = 0; }
+    p.seq_seg_begin[p.num_seqs] = seg_carry;
+    p.seq_chunk_begin[p.num_seqs] = chunk_carry;
+    p.meta->total_chunks = total;
+    if (f) atomicOr(p.status, f);
+  }
+}
+
+__global__ void plan_fill(PlanParams p, int64_t max_segs) {
+  const int64_t gidx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gidx >= max_segs) return;
+  if (p.meta->total_chunks == 0) return;
+  const int64_t total_segs = p.seq_seg_begin[p.num_seqs];
+  if (gidx >= total_segs) return;
+  // sequence owning this aligned segment: largest s with seg_begin[s] <= gidx
+  int32_t lo = 0, hi = p.num_seqs - 1;
+  while (lo < hi) {
+    int32_t mid = (lo + hi + 1) >> 1;
+    if (p.seq_seg_begin[mid] <= gidx) lo = mid; else hi = mid - 1;
+  }
+  const int32_t s = lo;
+  const int64_t m = gidx - p.seq_seg_begin[s];
+  const int64_t len = p.seq_len[s];
+  const int64_t tok_base = p.cu_seqlens[s];
+  const int64_t b0 = p.seq_bnd[2 * s], b1 = p.seq_bnd[2 * s + 1];
+  const bool has_b = p.boundary_pos != nullptr && b1 > b0;
+  const int64_t seg0 = m * kChunk;
+  const int64_t seg1 = seg0 + kChunk < len ? seg0 + kChunk : len;
+  int64_t j = has_b ? lower_bound_i64(p.boundary_pos, b0, b1, seg0 + 1) : 0;
+  int64_t ci = p.seq_chunk_begin[s] + m + (has_b ? p.bnd_nonaligned[j + s] : 0);
+  const int64_t snap_lo = p.cu_snapshots ? p.cu_snapshots[s] : 0;
+  const int64_t snap_hi = p.cu_snapshots ? p.cu_snapshots[s + 1] : 0;
+  int64_t start = seg0;
+  int32_t bad = 0;
+  while (start < seg1) {
+    int64_t end = seg1;
+    if (has_b && j < b1 && p.boundary_pos[j] < seg1) end = p.boundary_pos[j];
+    // snapshot slot of the state after `end` tokens
+    int32_t slot = -1;
+    if (p.cu_snapshots) {
+      bool is_mult = p.snapshot_interval > 0 && end % p.snapshot_interval == 0;
+      int64_t jb = has_b ? upper_bound_i64(p.boundary_pos, b0, b1, end) : 0;
+      bool is_bnd = has_b && jb > b0 && p.boundary_pos[jb - 1] == end;
+      if (is_mult || is_bnd) {
+        int64_t rank = (p.snapshot_interval > 0 ? end / p.snapshot_interval : 0) +
+                       (has_b ? p.bnd_nonmult[jb + s] : 0) - 1;
+        int64_t sl = snap_lo + rank;
+        if (sl >= snap_lo && sl < snap_hi && sl < p.num_snapshots) slot = (int32_t)sl; else bad = 1;
+      }
+    }
+    if (ci < p.max_chunks) {
+      Chunk c;
+      c.tok0 = tok_base + start;
+      c.seq = s;
+      c.len = (int32_t)(end - start);
+      c.snap_slot = slot;
+      c.flags = (start == 0 ? kChunkFirst : 0) | (end == len ? kChunkLast : 0);
+      c.pad = 0;
+      p.chunks[ci] = c;
+    }
+    ++ci;
+    if (has_b && j < b1 && p.boundary_pos[j] == end) ++j;
+    start = end;
+  }
+  if (bad) atomicOr(p.status, kFlagBadBoundaries);
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
+  plan_sequences<<<1, kPlanThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t max_segs = (p.total_tokens + kChunk - 1) / kChunk + p.num_seqs;
+  if (max_segs > 0) {
+    const int threads = 256;
+    const int64_t blocks = (max_segs + threads - 1) / threads;
+    plan_fill<<<(unsigned)blocks, threads, 0, stream>>>(p, max_segs);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace kda

@@ -1,0 +1,340 @@
+"""Python binding of libkda (include/kda.h): argument marshalling only.
+
+Every step of the KDA path runs in the library's CUDA kernels; PyTorch only
+provides device memory, streams and the host<->device copies of the
+end-to-end helper.  There is no CPU fallback: if libkda.so has not been
+built, or no CUDA device is present, the calls raise.
+
+The names follow the C ABI: ``kda_prefill``, ``kda_prefill_workspace_size``,
+``kda_prefill_device_status``, ``kda_snapshot_plan``, ``kda_decode_step``,
+``kda_prep``, ``kda_status_string``.  ``prefill`` and ``prefill_host`` are
+conveniences that allocate outputs and workspace with torch and call
+``kda_prefill``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
+
+KDA_OK = 0
+KDA_F32, KDA_BF16 = 0, 1
+CHUNK = 64
+PREFILL_PHASES = 3  # chunk planning, intra-chunk, inter-chunk
+_STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED",
+                 3: "KDA_ERR_WORKSPACE", 4: "KDA_ERR_CUDA", 5: "KDA_ERR_TIMEOUT",
+                 6: "KDA_ERR_DEVICE_DATA"}
+EXPORTED = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_device_status",
+            "kda_snapshot_plan", "kda_decode_step", "kda_prep", "kda_status_string",
+            "kda_version")
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_STATUS_NAMES.get(status, status)} "
+                         f"({kda_status_string(status)})")
+
+
+c_i32, c_i64, c_f32, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+
+
+class PrefillArgs(ctypes.Structure):
+    _fields_ = [("num_seqs", c_i32), ("num_heads", c_i32), ("dk", c_i32), ("dv", c_i32),
+                ("total_tokens", c_i64), ("cu_seqlens", c_vp), ("in_dtype", ctypes.c_int),
+                ("q", c_vp), ("k", c_vp), ("v", c_vp), ("g", c_vp), ("b", c_vp),
+                ("scale", c_f32), ("initial_state", c_vp), ("o", c_vp), ("final_state", c_vp),
+                ("snapshot_interval", c_i64), ("boundary_pos", c_vp), ("cu_boundaries", c_vp),
+                ("num_boundaries", c_i64), ("cu_snapshots", c_vp), ("snapshots", c_vp),
+                ("num_snapshots", c_i64), ("phase_events", c_vp)]
+
+
+class DecodeArgs(ctypes.Structure):
+    _fields_ = [("batch", c_i32), ("num_heads", c_i32), ("dk", c_i32), ("dv", c_i32),
+                ("num_slots", c_i32), ("in_dtype", ctypes.c_int), ("scale", c_f32),
+                ("q", c_vp), ("k", c_vp), ("v", c_vp), ("g", c_vp), ("b", c_vp),
+                ("state", c_vp), ("state_slots", c_vp), ("o", c_vp)]
+
+
+class PrepArgs(ctypes.Structure):
+    _fields_ = [("num_seqs", c_i32), ("num_heads", c_i32), ("dk", c_i32),
+                ("total_tokens", c_i64), ("cu_seqlens", c_vp), ("in_dtype", ctypes.c_int),
+                ("q", c_vp), ("k", c_vp), ("g", c_vp), ("b", c_vp), ("qhat", c_vp),
+                ("khat", c_vp), ("G", c_vp), ("beta", c_vp)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libkda.so; raises if it was not built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libkda.so not built ({LIB_PATH}); run "
+                                   "`python -m linear_attention_serving_delta_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            L.kda_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs)]
+            L.kda_prefill_workspace_size.restype = ctypes.c_size_t
+            L.kda_prefill.argtypes = [ctypes.POINTER(PrefillArgs), c_vp, ctypes.c_size_t, c_vp]
+            L.kda_prefill.restype = ctypes.c_int
+            L.kda_prefill_device_status.argtypes = [c_vp, ctypes.POINTER(c_i32), c_vp]
+            L.kda_prefill_device_status.restype = ctypes.c_int
+            L.kda_snapshot_plan.argtypes = [c_vp, c_i32, c_i64, c_vp, c_vp, c_vp]
+            L.kda_snapshot_plan.restype = c_i64
+            L.kda_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), c_vp]
+            L.kda_decode_step.restype = ctypes.c_int
+            L.kda_prep.argtypes = [ctypes.POINTER(PrepArgs), c_vp]
+            L.kda_prep.restype = ctypes.c_int
+            L.kda_status_string.argtypes = [ctypes.c_int]
+            L.kda_status_string.restype = ctypes.c_char_p
+            L.kda_version.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def kda_status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+def kda_version() -> str:
+    return lib().kda_version().decode()
+
+
+# ----------------------------------------------------------------- marshalling helpers
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return KDA_F32
+    if t == torch.bfloat16:
+        return KDA_BF16
+    raise TypeError(f"unsupported input dtype {t} (float32 or bfloat16)")
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name: str = "") -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int, what: str):
+    if status != KDA_OK:
+        raise KdaError(status, what)
+
+
+def make_prefill_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=None,
+                      final_state=None, snapshot_interval=0, boundary_pos=None,
+                      cu_boundaries=None, cu_snapshots=None, snapshots=None) -> PrefillArgs:
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    for name, t, shp in (("k", k, (T, H, dk)), ("g", g, (T, H, dk)), ("v", v, (T, H, dv)),
+                         ("b", b, (T, H)), ("o", o, (T, H, dv))):
+        if tuple(t.shape) != shp:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shp}")
+    a = PrefillArgs()
+    a.num_seqs = cu_seqlens.numel() - 1
+    a.num_heads, a.dk, a.dv, a.total_tokens = H, dk, dv, T
+    a.cu_seqlens = _ptr(cu_seqlens, torch.int64, "cu_seqlens")
+    a.in_dtype = _dtype_code(dt)
+    a.q, a.k, a.v = _ptr(q, dt, "q"), _ptr(k, dt, "k"), _ptr(v, dt, "v")
+    a.g, a.b, a.o = _ptr(g, dt, "g"), _ptr(b, dt, "b"), _ptr(o, dt, "o")
+    a.scale = float(scale)
+    a.initial_state = _ptr(initial_state, torch.float32, "initial_state")
+    a.final_state = _ptr(final_state, torch.float32, "final_state")
+    a.snapshot_interval = int(snapshot_interval)
+    a.boundary_pos = _ptr(boundary_pos, torch.int64, "boundary_pos")
+    a.cu_boundaries = _ptr(cu_boundaries, torch.int64, "cu_boundaries")
+    a.num_boundaries = 0 if boundary_pos is None else boundary_pos.numel()
+    a.cu_snapshots = _ptr(cu_snapshots, torch.int64, "cu_snapshots")
+    a.snapshots = _ptr(snapshots, torch.float32, "snapshots")
+    a.num_snapshots = 0 if snapshots is None else snapshots.shape[0]
+    return a
+
+
+# ----------------------------------------------------------------- the C entry points
+def kda_prefill_workspace_size(args: PrefillArgs) -> int:
+    return int(lib().kda_prefill_workspace_size(ctypes.byref(args)))
+
+
+def kda_prefill(args: PrefillArgs, workspace: torch.Tensor, stream=None) -> None:
+    """Launches the prefill described by ``args`` (see make_prefill_args)."""
+    ws = _ptr(workspace, torch.uint8, "workspace")
+    _check(lib().kda_prefill(ctypes.byref(args), ws, workspace.numel(), _stream(stream)),
+           "kda_prefill")
+
+
+def kda_prefill_device_status(workspace: torch.Tensor, stream=None) -> int:
+    out = c_i32(0)
+    _check(lib().kda_prefill_device_status(_ptr(workspace, name="workspace"), ctypes.byref(out),
+                                           _stream(stream)), "kda_prefill_device_status")
+    return int(out.value)
+
+
+def kda_snapshot_plan(cu_seqlens, interval: int, boundary_pos=None, cu_boundaries=None):
+    """Host helper: (cu_snapshots int64 [N+1] numpy, n_snap)."""
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens.cpu() if torch.is_tensor(cu_seqlens)
+                                         else cu_seqlens, dtype=np.int64))
+    n = cu.shape[0] - 1
+    out = np.zeros(n + 1, dtype=np.int64)
+    bp = cb = None
+    if boundary_pos is not None:
+        bp = np.ascontiguousarray(np.asarray(boundary_pos.cpu() if torch.is_tensor(boundary_pos)
+                                             else boundary_pos, dtype=np.int64))
+        cb = np.ascontiguousarray(np.asarray(cu_boundaries.cpu() if torch.is_tensor(cu_boundaries)
+                                             else cu_boundaries, dtype=np.int64))
+    n_snap = lib().kda_snapshot_plan(cu.ctypes.data, n, int(interval),
+                                     None if bp is None else bp.ctypes.data,
+                                     None if cb is None else cb.ctypes.data, out.ctypes.data)
+    if n_snap < 0:
+        raise ValueError("kda_snapshot_plan: invalid sequence lengths or boundary positions")
+    return out, int(n_snap)
+
+
+def kda_decode_step(q, k, v, g, b, state, o, state_slots=None, scale=1.0, stream=None) -> None:
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    a = DecodeArgs()
+    a.batch, a.num_heads, a.dk, a.dv = B, H, dk, dv
+    a.num_slots = state.shape[0]
+    if tuple(state.shape[1:]) != (H, dk, dv):
+        raise ValueError(f"state has shape {tuple(state.shape)}, expected [slots, {H}, {dk}, {dv}]")
+    a.in_dtype = _dtype_code(dt)
+    a.scale = float(scale)
+    a.q, a.k, a.v = _ptr(q, dt, "q"), _ptr(k, dt, "k"), _ptr(v, dt, "v")
+    a.g, a.b, a.o = _ptr(g, dt, "g"), _ptr(b, dt, "b"), _ptr(o, dt, "o")
+    a.state = _ptr(state, torch.float32, "state")
+    a.state_slots = _ptr(state_slots, torch.int32, "state_slots")
+    _check(lib().kda_decode_step(ctypes.byref(a), _stream(stream)), "kda_decode_step")
+
+
+def kda_prep(q, k, g, b, cu_seqlens, qhat, khat, G, beta, stream=None) -> None:
+    T, H, dk = q.shape
+    dt = q.dtype
+    a = PrepArgs()
+    a.num_seqs, a.num_heads, a.dk, a.total_tokens = cu_seqlens.numel() - 1, H, dk, T
+    a.cu_seqlens = _ptr(cu_seqlens, torch.int64, "cu_seqlens")
+    a.in_dtype = _dtype_code(dt)
+    a.q, a.k, a.g, a.b = _ptr(q, dt, "q"), _ptr(k, dt, "k"), _ptr(g, dt, "g"), _ptr(b, dt, "b")
+    a.qhat, a.khat = _ptr(qhat, torch.float32, "qhat"), _ptr(khat, torch.float32, "khat")
+    a.G, a.beta = _ptr(G, torch.float32, "G"), _ptr(beta, torch.float32, "beta")
+    _check(lib().kda_prep(ctypes.byref(a), _stream(stream)), "kda_prep")
+
+
+# ----------------------------------------------------------------- conveniences
+class Prefill:
+    """A planned prefill call: outputs, workspace and snapshot slots are
+    allocated once (torch device memory); ``run()`` only launches kernels.
+
+    Host copies of cu_seqlens (and boundaries) are needed to size the
+    snapshot buffer; pass them as ``lens`` to avoid a device->host read."""
+
+    def __init__(self, q, k, v, g, b, cu_seqlens, *, scale=1.0, initial_state=None,
+                 snapshot_interval=0, boundary_pos=None, cu_boundaries=None,
+                 want_final=True, host_cu_seqlens=None, host_boundary_pos=None,
+                 host_cu_boundaries=None):
+        dev = q.device
+        T, H, dk = q.shape
+        dv = v.shape[-1]
+        N = cu_seqlens.numel() - 1
+        self.o = torch.empty(T, H, dv, dtype=q.dtype, device=dev)
+        self.final_state = (torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
+                            if want_final else None)
+        self.cu_snapshots = self.snapshots = None
+        self.n_snap = 0
+        if snapshot_interval > 0 or boundary_pos is not None:
+            hcu = cu_seqlens.cpu() if host_cu_seqlens is None else host_cu_seqlens
+            hbp = (None if boundary_pos is None else
+                   (boundary_pos.cpu() if host_boundary_pos is None else host_boundary_pos))
+            hcb = (None if cu_boundaries is None else
+                   (cu_boundaries.cpu() if host_cu_boundaries is None else host_cu_boundaries))
+            cs, n_snap = kda_snapshot_plan(hcu, snapshot_interval, hbp, hcb)
+            self.n_snap = n_snap
+            self.cu_snapshots = torch.from_numpy(cs).to(dev)
+            self.snapshots = torch.empty(max(n_snap, 1), H, dk, dv, dtype=torch.float32,
+                                         device=dev)
+        self.args = make_prefill_args(
+            q, k, v, g, b, cu_seqlens, self.o, scale=scale, initial_state=initial_state,
+            final_state=self.final_state, snapshot_interval=snapshot_interval,
+            boundary_pos=boundary_pos, cu_boundaries=cu_boundaries,
+            cu_snapshots=self.cu_snapshots, snapshots=self.snapshots)
+        nbytes = kda_prefill_workspace_size(self.args)
+        if nbytes == 0:
+            raise ValueError("kda_prefill_workspace_size rejected the arguments")
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self._keep = (q, k, v, g, b, cu_seqlens, initial_state, boundary_pos, cu_boundaries)
+
+    def run(self, stream=None):
+        kda_prefill(self.args, self.workspace, stream)
+        return self
+
+    def device_status(self, stream=None) -> int:
+        return kda_prefill_device_status(self.workspace, stream)
+
+    @property
+    def snapshot_view(self):
+        return None if self.snapshots is None else self.snapshots[: self.n_snap]
+
+
+def prefill(q, k, v, g, b, cu_seqlens, **kw):
+    """Allocates, runs and returns (o, final_state, snapshots) on the device."""
+    p = Prefill(q, k, v, g, b, cu_seqlens, **kw).run()
+    return p.o, p.final_state, p.snapshot_view
+
+
+def prefill_host(q, k, v, g, b, cu_seqlens, *, device="cuda", stream=None, **kw):
+    """End-to-end prefill from host tensors: copies the inputs (pinned host
+    memory is copied asynchronously) to the device, runs kda_prefill, and
+    copies o and the final state back.  Returns host (o, final_state)."""
+    s = torch.cuda.current_stream() if stream is None else stream
+    with torch.cuda.stream(s):
+        dq, dk_, dv_, dg, db = (t.to(device, non_blocking=True) for t in (q, k, v, g, b))
+        dcu = cu_seqlens.to(device, non_blocking=True)
+        init = kw.pop("initial_state", None)
+        dinit = None if init is None else init.to(device, non_blocking=True)
+        p = Prefill(dq, dk_, dv_, dg, db, dcu, initial_state=dinit,
+                    host_cu_seqlens=cu_seqlens, **kw).run(s)
+        o = torch.empty(p.o.shape, dtype=p.o.dtype, pin_memory=True)
+        o.copy_(p.o, non_blocking=True)
+        fs = torch.empty(p.final_state.shape, dtype=torch.float32, pin_memory=True)
+        fs.copy_(p.final_state, non_blocking=True)
+    s.synchronize()
+    return o, fs
+
+
+def decode_step(q, k, v, g, b, state, state_slots=None, scale=1.0, o=None, stream=None):
+    if o is None:
+        o = torch.empty(q.shape[0], q.shape[1], v.shape[-1], dtype=q.dtype, device=q.device)
+    kda_decode_step(q, k, v, g, b, state, o, state_slots=state_slots, scale=scale, stream=stream)
+    return o
+
+
+def prep(q, k, g, b, cu_seqlens, stream=None):
+    T, H, dk = q.shape
+    f = dict(dtype=torch.float32, device=q.device)
+    qhat, khat, G = (torch.empty(T, H, dk, **f) for _ in range(3))
+    beta = torch.empty(T, H, **f)
+    kda_prep(q, k, g, b, cu_seqlens, qhat, khat, G, beta, stream=stream)
+    return qhat, khat, G, beta

@@ -1,0 +1,171 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+* libkda.so builds for sm_103a and loads;
+* it exports every function include/kda.h declares;
+* the ctypes structures of the binding have the C layout (sizes and offsets
+  from a C program compiled against kda.h);
+* argument validation rejects bad arguments before any launch;
+* the host snapshot plan agrees with the oracle's definition of the
+  snapshot positions.
+"""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def kda():
+    from linear_attention_serving_delta_gb300 import build, kda as binding
+    build.build()
+    binding.lib()
+    return binding
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_function(kda):
+    names = declared_functions()
+    assert len(names) >= 8
+    L = kda.lib()
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in kda.h but not exported"
+    assert set(names) == set(kda.EXPORTED)
+    out = subprocess.run(["nm", "-D", "--defined-only", kda.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    for n in names:
+        assert re.search(rf"\bT {n}\b", out), f"{n} not a defined text symbol"
+
+
+def test_struct_layouts_match_c(kda, tmp_path):
+    prog = r'''
+#include <stdio.h>
+#include <stddef.h>
+#include "kda.h"
+#define F(T, m) printf(#T "." #m " %zu\n", offsetof(T, m));
+int main(void) {
+  printf("kda_prefill_args %zu\n", sizeof(kda_prefill_args));
+  printf("kda_decode_args %zu\n", sizeof(kda_decode_args));
+  printf("kda_prep_args %zu\n", sizeof(kda_prep_args));
+  F(kda_prefill_args, cu_seqlens) F(kda_prefill_args, in_dtype) F(kda_prefill_args, q)
+  F(kda_prefill_args, scale) F(kda_prefill_args, initial_state)
+  F(kda_prefill_args, snapshot_interval) F(kda_prefill_args, num_boundaries)
+  F(kda_prefill_args, snapshots) F(kda_prefill_args, num_snapshots)
+  F(kda_prefill_args, phase_events)
+  F(kda_decode_args, scale) F(kda_decode_args, q) F(kda_decode_args, state_slots)
+  F(kda_decode_args, o)
+  F(kda_prep_args, total_tokens) F(kda_prep_args, in_dtype) F(kda_prep_args, beta)
+  return 0;
+}
+'''
+    c = tmp_path / "layout.c"
+    c.write_text(prog)
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.dirname(HEADER), str(c), "-o", str(exe)], check=True)
+    lines = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = dict(l.rsplit(" ", 1) for l in lines if l)
+    structs = {"kda_prefill_args": kda.PrefillArgs, "kda_decode_args": kda.DecodeArgs,
+               "kda_prep_args": kda.PrepArgs}
+    for key, val in got.items():
+        if "." in key:
+            s, m = key.split(".")
+            assert getattr(structs[s], m).offset == int(val), key
+        else:
+            assert ctypes.sizeof(structs[key]) == int(val), key
+
+
+def _args(kda, **over):
+    a = kda.PrefillArgs()
+    a.num_seqs, a.num_heads, a.dk, a.dv, a.total_tokens = 1, 2, 16, 16, 64
+    a.cu_seqlens = 0x1000
+    a.in_dtype = kda.KDA_F32
+    a.q = a.k = a.v = a.g = a.b = a.o = 0x2000
+    a.scale = 1.0
+    for k_, v_ in over.items():
+        setattr(a, k_, v_)
+    return a
+
+
+def test_workspace_size_and_validation(kda):
+    L = kda.lib()
+    good = _args(kda)
+    ws = L.kda_prefill_workspace_size(ctypes.byref(good))
+    assert ws > 0 and ws % 256 == 0
+    # invalid arguments: size query returns 0 and the call returns a status, no launch
+    for bad, code in [(dict(dk=24), 2), (dict(dv=256), 2), (dict(num_seqs=0), 1),
+                      (dict(cu_seqlens=None), 1), (dict(q=None), 1),
+                      (dict(snapshot_interval=100), 1), (dict(snapshot_interval=-64), 1),
+                      (dict(boundary_pos=0x3000), 1), (dict(snapshots=0x3000), 1),
+                      (dict(in_dtype=7), 1), (dict(total_tokens=-1), 1)]:
+        a = _args(kda, **bad)
+        assert L.kda_prefill_workspace_size(ctypes.byref(a)) == 0, bad
+        assert L.kda_prefill(ctypes.byref(a), 0x4000, 1 << 30, None) == code, bad
+    # workspace too small / missing / misaligned
+    assert L.kda_prefill(ctypes.byref(good), None, ws, None) == 3
+    assert L.kda_prefill(ctypes.byref(good), 0x4000, ws - 256, None) == 3
+    assert L.kda_prefill(ctypes.byref(good), 0x4010, ws, None) == 3
+    # the workspace grows with tokens, sequences and boundaries
+    big = _args(kda, total_tokens=8192)
+    assert L.kda_prefill_workspace_size(ctypes.byref(big)) > ws
+    assert L.kda_prefill(None, 0x4000, ws, None) == 1
+    assert kda.kda_status_string(3).startswith("workspace")
+
+
+def test_decode_and_prep_validation(kda):
+    L = kda.lib()
+    d = kda.DecodeArgs()
+    d.batch, d.num_heads, d.dk, d.dv, d.num_slots = 0, 1, 128, 128, 0
+    assert L.kda_decode_step(ctypes.byref(d), None) == 0          # empty batch: nothing to do
+    d.batch, d.num_slots = 4, 4
+    assert L.kda_decode_step(ctypes.byref(d), None) == 1          # null pointers
+    d.q = d.k = d.v = d.g = d.b = d.o = 0x2000
+    d.state = 0x3008                                               # misaligned state
+    assert L.kda_decode_step(ctypes.byref(d), None) == 1
+    d.state = 0x3000
+    d.num_slots = 2                                                # pool smaller than batch
+    assert L.kda_decode_step(ctypes.byref(d), None) == 1
+    d.dk = 96
+    assert L.kda_decode_step(ctypes.byref(d), None) == 2
+    p = kda.PrepArgs()
+    p.num_seqs, p.num_heads, p.dk, p.total_tokens = 1, 1, 20, 4
+    assert L.kda_prep(ctypes.byref(p), None) == 2
+    assert L.kda_decode_step(None, None) == 1
+    assert L.kda_prep(None, None) == 1
+
+
+def test_snapshot_plan_matches_oracle_definition(kda, oracle_mod):
+    rng = np.random.default_rng(5)
+    for trial in range(20):
+        n = int(rng.integers(1, 6))
+        lens = rng.integers(0, 300, size=n)
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        interval = int(rng.choice([0, 64, 128]))
+        bpos, cub = [], [0]
+        for L in lens:
+            k = int(rng.integers(0, 4)) if L > 0 else 0
+            pts = sorted(set(int(x) for x in rng.integers(1, L + 1, size=k))) if L > 0 else []
+            bpos += pts
+            cub.append(len(bpos))
+        use_b = bool(rng.integers(0, 2))
+        bp = np.array(bpos, np.int64) if use_b else None
+        cb = np.array(cub, np.int64) if use_b else None
+        cs, n_snap = kda.kda_snapshot_plan(cu, interval, bp, cb)
+        pos, cs_ref = oracle_mod.snapshot_positions(lens, interval, bp, cb)
+        assert list(cs) == list(cs_ref)
+        assert n_snap == len(pos)
+    with pytest.raises(ValueError):
+        kda.kda_snapshot_plan([0, 10], 0, [5, 5], [0, 2])      # not strictly increasing
+    with pytest.raises(ValueError):
+        kda.kda_snapshot_plan([0, 10], 0, [11], [0, 1])        # beyond the sequence

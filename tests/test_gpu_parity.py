@@ -1,0 +1,245 @@
+"""CUDA path vs the fp64 CPU oracle, element by element, on seeded inputs.
+
+Tolerances (relative Frobenius error, on o, final states and snapshots):
+1e-5 where inputs are fp32, 5e-3 where inputs are bf16 (state fp32).  Every
+call goes through the C ABI (ctypes binding).
+"""
+import numpy as np
+import pytest
+import torch
+
+from linear_attention_serving_delta_gb300 import kda
+from linear_attention_serving_delta_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-5, "bf16": 5e-3}
+
+
+def rel(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    nb = np.linalg.norm(b)
+    return np.linalg.norm(a - b) / (nb if nb > 0 else 1.0)
+
+
+def host(t):
+    return None if t is None else t.detach().float().cpu().numpy()
+
+
+def to_dev(inp):
+    return {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+
+
+def make_inputs(lens, H, dk, dv, dtype, seed, s0_std=0.0, g_shift=0.0):
+    w = W.PrefillWorkload("case", None, len(lens), H, dk, dv, dtype, seed, len_range=(1, 1),
+                          s0_std=s0_std)
+    inp = W.prefill_inputs(w, lens=lens)
+    if g_shift:
+        inp["g"] = (inp["g"].float() + g_shift).to(inp["g"].dtype)
+    return inp
+
+
+def run_both(inp, dtype, scale=1.0, interval=0, boundaries=None):
+    """Returns (gpu (o, S, snaps), oracle (o, S, snaps))."""
+    lens = inp["lens"]
+    cu = inp["cu_seqlens"]
+    bpos = cub = None
+    if boundaries is not None:
+        bl, cb = [], [0]
+        for s, pts in enumerate(boundaries):
+            bl += list(pts)
+            cb.append(len(bl))
+        bpos = torch.tensor(bl, dtype=torch.int64)
+        cub = torch.tensor(cb, dtype=torch.int64)
+    d = to_dev(inp)
+    p = kda.Prefill(d["q"], d["k"], d["v"], d["g"], d["b"], d["cu_seqlens"], scale=scale,
+                    initial_state=d["S0"], snapshot_interval=interval,
+                    boundary_pos=None if bpos is None else bpos.cuda(),
+                    cu_boundaries=None if cub is None else cub.cuda(),
+                    host_cu_seqlens=cu, host_boundary_pos=bpos, host_cu_boundaries=cub)
+    p.run()
+    torch.cuda.synchronize()
+    assert p.device_status() == 0
+    import oracle
+    sp = cs = None
+    if interval > 0 or bpos is not None:
+        sp, cs = oracle.snapshot_positions(lens, interval, None if bpos is None else bpos.numpy(),
+                                           None if cub is None else cub.numpy())
+    ref = oracle.prefill(host(inp["q"]), host(inp["k"]), host(inp["v"]), host(inp["g"]),
+                         host(inp["b"]), cu.numpy(), scale=scale, S0=host(inp["S0"]),
+                         snap_pos=sp, cu_snap=cs)
+    gpu = (host(p.o), host(p.final_state), host(p.snapshot_view))
+    return gpu, ref
+
+
+def assert_close(gpu, ref, tol, what=""):
+    o, S, sn = gpu
+    ro, rS, rsn = ref
+    e_o, e_S = rel(o, ro), rel(S, rS)
+    assert e_o <= tol, f"{what} o rel err {e_o:.3e} > {tol}"
+    assert e_S <= tol, f"{what} final state rel err {e_S:.3e} > {tol}"
+    if rsn is not None and len(rsn):
+        e_sn = rel(sn, rsn)
+        assert e_sn <= tol, f"{what} snapshots rel err {e_sn:.3e} > {tol}"
+
+
+# ------------------------------------------------------------------ decode (K4)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(16, 16), (32, 64), (64, 32), (128, 128), (128, 16)])
+def test_decode_small(dtype, dk, dv, oracle_mod):
+    dw = W.DecodeWorkload("small", 5, 3, dk, dv, 4, 77 + dk + dv)
+    inp = W.decode_inputs(dw, dtype=dtype)
+    state = inp["state"].cuda().contiguous()
+    ref_state = host(inp["state"]).astype(np.float64)
+    slots = torch.tensor([3, 0, -1, 4, 1], dtype=torch.int32)
+    for step in range(dw.steps):
+        args = [inp[x][step].cuda().contiguous() for x in "qkvgb"]
+        o = torch.zeros(5, 3, dv, dtype=args[0].dtype, device="cuda")
+        kda.kda_decode_step(*args, state, o, state_slots=slots.cuda(), scale=0.7)
+        ro = oracle_mod.decode(*[host(inp[x][step]) for x in "qkvgb"], ref_state,
+                               slots=slots.numpy(), scale=0.7)
+        torch.cuda.synchronize()
+        assert rel(host(o), ro) <= TOL[dtype]
+        assert np.all(host(o)[2] == 0)                      # skipped row untouched
+    assert rel(host(state), ref_state) <= 1e-5              # fp32 state math
+    np.testing.assert_array_equal(host(state)[2], host(inp["state"])[2])  # slot 2 unused
+
+
+def test_decode_full_size(oracle_mod):
+    """256 sequences x 32 heads x 128x128 fp32 states, three consecutive steps."""
+    dw = W.DECODE_WORKLOADS["decode_256"]
+    inp = W.decode_inputs(dw, steps=3)
+    state = inp["state"].cuda()
+    ref_state = host(inp["state"]).astype(np.float64)
+    for step in range(3):
+        args = [inp[x][step].cuda() for x in "qkvgb"]
+        o = kda.decode_step(*args, state)
+        ro = oracle_mod.decode(*[host(inp[x][step]) for x in "qkvgb"], ref_state)
+        torch.cuda.synchronize()
+        assert rel(host(o), ro) <= TOL["bf16"]
+    assert rel(host(state), ref_state) <= 1e-5
+
+
+# ------------------------------------------------------------------ prep (K1)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_prep(dtype, oracle_mod):
+    lens = [5, 64, 130, 1, 0, 77]
+    inp = make_inputs(lens, 3, 64, 16, dtype, 11)
+    d = to_dev(inp)
+    qh, kh, G, beta = kda.prep(d["q"], d["k"], d["g"], d["b"], d["cu_seqlens"])
+    torch.cuda.synchronize()
+    rq, rk, rla, rb = oracle_mod.prep(host(inp["q"]), host(inp["k"]), host(inp["g"]),
+                                      host(inp["b"]))
+    # G restarts at every 64-token chunk of every sequence (plain definition)
+    rG = np.zeros_like(rla)
+    cu = inp["cu_seqlens"].numpy()
+    for s in range(len(lens)):
+        for c0 in range(cu[s], cu[s + 1], 64):
+            c1 = min(c0 + 64, cu[s + 1])
+            rG[c0:c1] = np.cumsum(rla[c0:c1], axis=0)
+    assert rel(host(qh), rq) < 1e-6 and rel(host(kh), rk) < 1e-6
+    assert rel(host(beta), rb) < 1e-6
+    assert np.max(np.abs(host(G) - rG)) < 1e-5 * max(1.0, np.max(np.abs(rG)))
+
+
+# ------------------------------------------------------------------ prefill (K0-K3)
+def test_prefill_tiny_f32():
+    w = W.WORKLOADS["tiny_f32"]
+    inp = W.prefill_inputs(w)
+    gpu, ref = run_both(inp, "f32")
+    assert_close(gpu, ref, TOL["f32"], "tiny_f32")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 32), (16, 128)])
+def test_prefill_ragged_varlen(dtype, dk, dv):
+    """Ragged tails and lengths around the chunk size, initial states,
+    snapshots every 64 tokens plus interior boundaries, scale != 1."""
+    lens = [1, 63, 64, 65, 200, 0, 129]
+    inp = make_inputs(lens, 2, dk, dv, dtype, 21, s0_std=0.02)
+    bnd = [[1], [10, 63], [], [64, 65], [3, 100, 150, 200], [], [128]]
+    gpu, ref = run_both(inp, dtype, scale=0.5, interval=64, boundaries=bnd)
+    assert_close(gpu, ref, TOL[dtype], f"{dtype} {dk}x{dv}")
+
+
+def test_prefill_strong_decay():
+    """g ~ N(0, 1): about 0.7 of log-decay per token, ~45 over a chunk."""
+    inp = make_inputs([300, 64], 2, 128, 128, "bf16", 31, g_shift=3.0)
+    gpu, ref = run_both(inp, "bf16")
+    assert_close(gpu, ref, TOL["bf16"], "strong decay")
+
+
+def test_prefill_8k_full():
+    """Single-sequence prefill, H=32, T=8192, dk=dv=128, bf16 in, fp32 state."""
+    inp = W.prefill_inputs(W.WORKLOADS["prefill_8k"])
+    gpu, ref = run_both(inp, "bf16")
+    assert_close(gpu, ref, TOL["bf16"], "prefill_8k")
+
+
+@pytest.mark.slow
+def test_prefill_varlen_full():
+    """8 packed sequences of U[1024, 32768] tokens, seeded initial states,
+    snapshots every 4096 tokens and at the boundaries (one interior + end)."""
+    w = W.WORKLOADS["varlen_8"]
+    inp = W.prefill_inputs(w)
+    bp, cb = inp["boundary_pos"], inp["cu_boundaries"]
+    bnd = [bp[cb[s]:cb[s + 1]].tolist() for s in range(len(inp["lens"]))]
+    gpu, ref = run_both(inp, "bf16", interval=4096, boundaries=bnd)
+    assert_close(gpu, ref, TOL["bf16"], "varlen_8")
+
+
+def test_prefill_empty_sequences_keep_initial_state():
+    inp = make_inputs([0, 5, 0], 2, 32, 32, "f32", 41, s0_std=0.5)
+    gpu, ref = run_both(inp, "f32")
+    np.testing.assert_array_equal(gpu[1][0], host(inp["S0"])[0])
+    np.testing.assert_array_equal(gpu[1][2], host(inp["S0"])[2])
+    assert_close(gpu, ref, TOL["f32"])
+
+
+def test_resume_from_snapshot_gpu():
+    """Prefill to a snapshot, resume from it: equals one uninterrupted call."""
+    lens = [300]
+    inp = make_inputs(lens, 4, 128, 128, "bf16", 51)
+    d = to_dev(inp)
+    full = kda.Prefill(d["q"], d["k"], d["v"], d["g"], d["b"], d["cu_seqlens"],
+                       boundary_pos=torch.tensor([100], device="cuda"),
+                       cu_boundaries=torch.tensor([0, 1], device="cuda"),
+                       host_cu_seqlens=inp["cu_seqlens"],
+                       host_boundary_pos=torch.tensor([100]),
+                       host_cu_boundaries=torch.tensor([0, 1])).run()
+    snap = full.snapshot_view.clone()
+    rest = {x: d[x][100:].contiguous() for x in "qkvgb"}
+    part = kda.Prefill(rest["q"], rest["k"], rest["v"], rest["g"], rest["b"],
+                       torch.tensor([0, 200], device="cuda"), initial_state=snap).run()
+    torch.cuda.synchronize()
+    assert rel(host(part.o), host(full.o)[100:]) < 2e-3
+    assert rel(host(part.final_state), host(full.final_state)) < 2e-3
+
+
+def test_prefill_then_decode_equals_longer_prefill():
+    lens = [150]
+    inp = make_inputs(lens, 2, 128, 128, "f32", 61)
+    d = to_dev(inp)
+    n_dec = 5
+    head = {x: d[x][: 150 - n_dec].contiguous() for x in "qkvgb"}
+    p = kda.Prefill(head["q"], head["k"], head["v"], head["g"], head["b"],
+                    torch.tensor([0, 150 - n_dec], device="cuda")).run()
+    state = p.final_state.clone()
+    outs = []
+    for t in range(150 - n_dec, 150):
+        args = [d[x][t:t + 1].contiguous() for x in "qkvgb"]
+        outs.append(kda.decode_step(*args, state))
+    full = kda.Prefill(d["q"], d["k"], d["v"], d["g"], d["b"], d["cu_seqlens"]).run()
+    torch.cuda.synchronize()
+    assert rel(host(torch.cat(outs)), host(full.o)[150 - n_dec:]) < 1e-5
+    assert rel(host(state), host(full.final_state)) < 1e-5
+
+
+def test_malformed_device_data_is_flagged():
+    """Decreasing cu_seqlens: the sequence is skipped and the status word says so."""
+    inp = make_inputs([10, 10], 1, 16, 16, "f32", 71)
+    d = to_dev(inp)
+    bad_cu = torch.tensor([0, 15, 12], dtype=torch.int64, device="cuda")
+    p = kda.Prefill(d["q"], d["k"], d["v"], d["g"], d["b"], bad_cu).run()
+    assert p.device_status() & 1

@@ -120,6 +120,10 @@ def bench_prefill(torch, kda, W, steps, warmup, dev):
                     host_cu_seqlens=inp["cu_seqlens"].cpu())
     nph = kda.PREFILL_PHASES
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)]
+    for e in ev:  # torch creates the cudaEvent_t on first record
+        e.record()
+    torch.cuda.synchronize()
+    assert all(e.cuda_event for e in ev)
     ev_handles = (kda.c_vp * (nph + 1))(*[e.cuda_event for e in ev])
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > L2 (129 MB)

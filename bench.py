@@ -243,6 +243,10 @@ def gpu_arm(a):
     with ClockSampler(local) as clk:
         pre = bench_prefill(torch, kda, W, a.steps, a.warmup, dev)
         barrier()
+        if a.prefill_only:
+            print(json.dumps({"prefill_ms_per_step": sum(pre["step_ms"]) / len(pre["step_ms"]),
+                              "phase_ms": [sum(x) / len(x) for x in pre["phase_ms"]]}))
+            return
         dec = bench_decode(torch, kda, W, a.decode_steps, max(3, a.warmup), dev)
         barrier()
     step_ms = sum(pre["step_ms"]) / len(pre["step_ms"])
@@ -359,6 +363,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time the prefill workload alone (for profiler captures)")
     a = ap.parse_args()
     if a.warmup < 3:
         a.warmup = 3

@@ -11,8 +11,15 @@ namespace {
 bool head_size_ok(int32_t d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 bool dtype_ok(kda_dtype_t t) { return t == KDA_F32 || t == KDA_BF16; }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// The tensor-core kernels move q, k, g, v, o and the states with 16-byte
+// vector accesses; other layouts take the fp32 CUDA-core path.
 bool use_tensor_cores(const kda_prefill_args* a) {
-  return kHaveTensorCorePath && a->in_dtype == KDA_BF16 && a->dk == 128 && a->dv == 128;
+  return kHaveTensorCorePath && a->in_dtype == KDA_BF16 && a->dk == 128 && a->dv == 128 &&
+         aligned16(a->q) && aligned16(a->k) && aligned16(a->v) && aligned16(a->g) &&
+         aligned16(a->o) && aligned16(a->initial_state) && aligned16(a->final_state) &&
+         aligned16(a->snapshots);
 }
 
 kda_status_t validate_prefill(const kda_prefill_args* a) {

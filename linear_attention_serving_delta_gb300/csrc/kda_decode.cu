@@ -14,6 +14,7 @@
 // for dv = 128), reduces S'^T k^ and S'^T q^ over the key channels in
 // registers and through shared memory, and writes the state back once.
 #include "kda_internal.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 namespace {
@@ -32,8 +33,13 @@ __global__ void __launch_bounds__(DecodeShape<TIn, DK, DV>::NT)
 decode_step(kda_decode_args a) {
   using Sh = DecodeShape<TIn, DK, DV>;
   constexpr int QPR = Sh::QPR, NT = Sh::NT, NRG = Sh::NRG, RPT = Sh::RPT;
-  __shared__ float qn[DK], kn[DK], al[DK], vv[DV];
-  __shared__ float red_p[NRG][DV], red_o[NRG][DV];
+  // arrays read through float4 are 16-byte aligned explicitly
+  __shared__ __align__(16) float qn[DK];
+  __shared__ __align__(16) float kn[DK];
+  __shared__ __align__(16) float al[DK];
+  __shared__ __align__(16) float vv[DV];
+  __shared__ __align__(16) float red_p[NRG][DV];
+  __shared__ __align__(16) float red_o[NRG][DV];
   __shared__ float sc[2];  // beta, q^.k^
 
   const int row = blockIdx.x, h = blockIdx.y, H = a.num_heads;
@@ -145,8 +151,204 @@ decode_step(kda_decode_args a) {
   }
 }
 
+// ------------------------------------------------------------ dk = dv = 128
+// Persistent variant: one CTA per SM walks (row, head) items; a ring of
+// kStages shared-memory slots is filled by 1-D bulk copies (TMA engine) of
+// each item's 64 KB state plus its q, k, g, v rows, kStages items ahead, so
+// HBM reads of the next states overlap the arithmetic and the write-back of
+// the current one.  The state is written back with 16-byte stores.
+constexpr int kStages = 3;
+constexpr int kRingThreads = 256;
+constexpr uint32_t kStateBytes = 128 * 128 * 4;
+
+template <typename TIn>
+struct Ring {
+  static constexpr uint32_t ROW = 128 * sizeof(TIn);  // one q / k / g / v row
+  static constexpr uint32_t STAGE = kStateBytes + 4 * ROW;
+  static constexpr uint32_t BYTES = kStages * STAGE;
+};
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+
+template <typename TIn>
+__device__ __forceinline__ void ring_issue(const kda_decode_args& a, uint8_t* stage, uint64_t* bar,
+                                           int32_t* valid_flag, int64_t item) {
+  const int H = a.num_heads;
+  const int row = (int)(item / H), h = (int)(item % H);
+  const int slot = a.state_slots ? a.state_slots[row] : row;
+  const bool valid = slot >= 0 && slot < a.num_slots;
+  *valid_flag = valid ? 1 : 0;
+  if (!valid) {
+    mbar_arrive(bar);
+    return;
+  }
+  constexpr uint32_t ROW = Ring<TIn>::ROW;
+  tc::mbar_arrive_expect_tx(bar, kStateBytes + 4 * ROW);
+  const int64_t e = ((int64_t)row * H + h) * 128;
+  tc::bulk_g2s(stage, a.state + ((size_t)slot * H + h) * 128 * 128, kStateBytes, bar);
+  tc::bulk_g2s(stage + kStateBytes, static_cast<const TIn*>(a.q) + e, ROW, bar);
+  tc::bulk_g2s(stage + kStateBytes + ROW, static_cast<const TIn*>(a.k) + e, ROW, bar);
+  tc::bulk_g2s(stage + kStateBytes + 2 * ROW, static_cast<const TIn*>(a.g) + e, ROW, bar);
+  tc::bulk_g2s(stage + kStateBytes + 3 * ROW, static_cast<const TIn*>(a.v) + e, ROW, bar);
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(kRingThreads, 1)
+decode_ring(kda_decode_args a, int64_t n_items) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  __shared__ __align__(8) uint64_t full[kStages];
+  __shared__ int32_t valid_flag[kStages];
+  __shared__ __align__(16) float qn[2][128];
+  __shared__ __align__(16) float kn[2][128];
+  __shared__ __align__(16) float al[2][128];
+  __shared__ __align__(16) float vv[2][128];
+  __shared__ float sc[2][2];
+  __shared__ __align__(16) float red_p[8][128];
+  __shared__ __align__(16) float red_o[8][128];
+  constexpr uint32_t ROW = Ring<TIn>::ROW;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = a.num_heads;
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+  const int64_t n_local = first < n_items ? (n_items - first + stride - 1) / stride : 0;
+
+  if (tid == 0) {
+    for (int st = 0; st < kStages; ++st) tc::mbar_init(&full[st], 1);
+    tc::mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int64_t k = 0; k < kStages && k < n_local; ++k)
+      ring_issue<TIn>(a, sm + k * Ring<TIn>::STAGE, &full[k], &valid_flag[k], first + k * stride);
+
+  // the update logit of the next item, prefetched one item ahead by lane 0 of warp 0
+  const TIn* gb = static_cast<const TIn*>(a.b);
+  float b_next = (tid == 0 && n_local > 0) ? ld_in(gb, first) : 0.f;
+
+  for (int64_t k = 0; k < n_local; ++k) {
+    const int st = (int)(k % kStages);
+    uint8_t* stage = sm + st * Ring<TIn>::STAGE;
+    const int64_t item = first + k * stride;
+    const int buf = (int)(k & 1);
+    bool ok = tc::mbar_wait(&full[st], (uint32_t)((k / kStages) & 1), tc::kWaitLimitNs);
+    const bool valid = valid_flag[st] != 0;
+    float b_cur = b_next;
+    if (tid == 0 && k + 1 < n_local) b_next = ld_in(gb, item + stride);
+    if (ok && valid && warp == 0) {
+      // token preparation: q^, k^, alpha, beta, q^.k^
+      const TIn* rq = reinterpret_cast<const TIn*>(stage + kStateBytes);
+      const TIn* rk = reinterpret_cast<const TIn*>(stage + kStateBytes + ROW);
+      const TIn* rg = reinterpret_cast<const TIn*>(stage + kStateBytes + 2 * ROW);
+      const TIn* rv = reinterpret_cast<const TIn*>(stage + kStateBytes + 3 * ROW);
+      float xq[4], xk[4], sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int c = lane + 32 * t;
+        xq[t] = ld_in(rq, c);
+        xk[t] = ld_in(rk, c);
+        sq += xq[t] * xq[t];
+        sk += xk[t] * xk[t];
+        al[buf][c] = expf(log_alpha_of(ld_in(rg, c)));
+        vv[buf][c] = ld_in(rv, c);
+      }
+      const float iq = inv_norm_of(warp_sum(sq)), ik = inv_norm_of(warp_sum(sk));
+      float qk = 0.f;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int c = lane + 32 * t;
+        qn[buf][c] = xq[t] * iq;
+        kn[buf][c] = xk[t] * ik;
+        qk += (xq[t] * iq) * (xk[t] * ik);
+      }
+      qk = warp_sum(qk);
+      if (lane == 0) {
+        sc[buf][0] = beta_of(b_cur);
+        sc[buf][1] = qk;
+      }
+    }
+    if (!__syncthreads_and(ok)) break;
+    if (!valid) {
+      __syncthreads();  // every thread has read valid_flag[st] before the slot is refilled
+      if (tid == 0 && k + kStages < n_local)
+        ring_issue<TIn>(a, stage, &full[st], &valid_flag[st], item + kStages * stride);
+      continue;
+    }
+    // retention and the two reductions over key channels; rows warp + 8i
+    const float* S = reinterpret_cast<const float*>(stage);
+    float4 s[16];
+    float4 pp = make_float4(0.f, 0.f, 0.f, 0.f), po = pp;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int r = warp + 8 * i;
+      s[i] = reinterpret_cast<const float4*>(S + r * 128)[lane];
+      const float a_r = al[buf][r], k_r = kn[buf][r], q_r = qn[buf][r];
+      s[i].x *= a_r; s[i].y *= a_r; s[i].z *= a_r; s[i].w *= a_r;
+      pp.x += k_r * s[i].x; pp.y += k_r * s[i].y; pp.z += k_r * s[i].z; pp.w += k_r * s[i].w;
+      po.x += q_r * s[i].x; po.y += q_r * s[i].y; po.z += q_r * s[i].z; po.w += q_r * s[i].w;
+    }
+    *reinterpret_cast<float4*>(&red_p[warp][4 * lane]) = pp;
+    *reinterpret_cast<float4*>(&red_o[warp][4 * lane]) = po;
+    __syncthreads();
+    // the slot has been read: refill it kStages items ahead
+    if (tid == 0 && k + kStages < n_local)
+      ring_issue<TIn>(a, stage, &full[st], &valid_flag[st], item + kStages * stride);
+    float4 p = make_float4(0.f, 0.f, 0.f, 0.f), oq = p;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const float4 x = *reinterpret_cast<const float4*>(&red_p[w][4 * lane]);
+      const float4 y = *reinterpret_cast<const float4*>(&red_o[w][4 * lane]);
+      p.x += x.x; p.y += x.y; p.z += x.z; p.w += x.w;
+      oq.x += y.x; oq.y += y.y; oq.z += y.z; oq.w += y.w;
+    }
+    const float beta = sc[buf][0];
+    const float4 vq = *reinterpret_cast<const float4*>(&vv[buf][4 * lane]);
+    const float4 u = make_float4(beta * (vq.x - p.x), beta * (vq.y - p.y), beta * (vq.z - p.z),
+                                 beta * (vq.w - p.w));
+    const int row = (int)(item / H), h = (int)(item % H);
+    const int slot = a.state_slots ? a.state_slots[row] : row;
+    float* Sg = a.state + ((size_t)slot * H + h) * 128 * 128;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int r = warp + 8 * i;
+      const float k_r = kn[buf][r];
+      float4 x = s[i];
+      x.x += k_r * u.x; x.y += k_r * u.y; x.z += k_r * u.z; x.w += k_r * u.w;
+      reinterpret_cast<float4*>(Sg + r * 128)[lane] = x;
+    }
+    if (warp == 0) {
+      const float qk = sc[buf][1], scl = a.scale;
+      TIn* o = static_cast<TIn*>(a.o);
+      const int64_t ob = ((int64_t)row * H + h) * 128 + 4 * lane;
+      st_out(o, ob + 0, scl * (oq.x + qk * u.x));
+      st_out(o, ob + 1, scl * (oq.y + qk * u.y));
+      st_out(o, ob + 2, scl * (oq.z + qk * u.z));
+      st_out(o, ob + 3, scl * (oq.w + qk * u.w));
+    }
+  }
+}
+
+template <typename TIn>
+cudaError_t launch_ring(const kda_decode_args& a, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_ring<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Ring<TIn>::BYTES);
+  if (e != cudaSuccess) return e;
+  const int64_t n_items = (int64_t)a.batch * a.num_heads;
+  const int64_t grid = n_items < sms ? n_items : sms;
+  decode_ring<TIn><<<(unsigned)grid, kRingThreads, Ring<TIn>::BYTES, stream>>>(a, n_items);
+  return cudaGetLastError();
+}
+
 template <typename TIn, int DK, int DV>
 cudaError_t launch_t(const kda_decode_args& a, cudaStream_t stream) {
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  // the bulk copies of the ring need 16-byte aligned sources
+  if (DK == 128 && DV == 128 && al16(a.q) && al16(a.k) && al16(a.g) && al16(a.v) && al16(a.state))
+    return launch_ring<TIn>(a, stream);
   dim3 grid((unsigned)a.batch, (unsigned)a.num_heads);
   decode_step<TIn, DK, DV><<<grid, DecodeShape<TIn, DK, DV>::NT, 0, stream>>>(a);
   return cudaGetLastError();

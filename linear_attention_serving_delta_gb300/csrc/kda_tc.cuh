@@ -37,10 +37,20 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   return d;
 }
 
+// byte offset of element (mn, k) of an "MN-major" operand tile: core
+// matrices of 8 K-rows x 16 bytes along MN; K-groups of 8 adjacent (stride
+// 128 B, the descriptor's leading-dimension offset), MN-groups of 8 at stride
+// `sbo` (the descriptor's stride offset).
+__host__ __device__ constexpr uint32_t mnmajor_off(uint32_t mn, uint32_t k, uint32_t sbo) {
+  return (mn >> 3) * sbo + (k >> 3) * 128u + (k & 7u) * 16u + (mn & 7u) * 2u;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator,
-// both operands K-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+// shape M x N; operands K-major unless a_mn / b_mn select MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, uint32_t a_mn = 0,
+                                                  uint32_t b_mn = 0) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) |
+         ((M >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.

@@ -1,0 +1,78 @@
+// kda_tc_common.cuh -- record layout and helpers shared by the tensor-core
+// intra-chunk (K2) and inter-chunk (K3) prefill kernels (bf16, dk = dv = 128,
+// chunk 64).
+//
+// Chunked form of the recurrence (delta rule with a diagonal gate, "From KV
+// Cache to Depth Attention", Technical Details; FlashKDA's unrolling in
+// chunks, "Kimi K3: The Manos, The Mythos, The Legendos", bullet list).  For
+// a chunk of L <= 64 tokens with start state S0, G_i = sum_{m<=i} log alpha_m
+// per key channel and Gamma = exp(G):
+//
+//   Kp = K^ o Gamma,  Kn = K^ o Gamma^{-1},  Qp = Q^ o Gamma,  Kr = K^ o Gamma_L/Gamma
+//   [A_kk ; A_qk] = [Kp ; Qp] Kn^T            (K2, tensor cores)
+//   A_kk <- diag(beta) strict-lower(A_kk),   A_qk <- lower(A_qk)
+//   Tb = (I + A_kk)^{-1} diag(beta)           (K2, CUDA cores)
+//   [W | U~] = Tb [Kp | V]                    (K2, tensor cores)
+//   per chunk, in order (K3):  U = U~ - W S0
+//                              O = scale (Qp S0 + A_qk U)
+//                              S_end = Diag(Gamma_L) S0 + Kr^T U
+//
+// The factored exponentials exp(G_i) exp(-G_j) stay finite while a chunk's
+// total log-decay per channel is above about -80; the fp32 CUDA-core path
+// (kda_simt.cu) has no such limit.
+#pragma once
+
+#include "kda_internal.cuh"
+#include "kda_tc.cuh"
+
+namespace kda {
+namespace tcp {
+
+constexpr uint32_t kD = 128;  // dk = dv on this path
+
+// Record written by K2 for every (chunk, head) and read by K3, bytes.  The
+// tiles are in the tcgen05 no-swizzle K-major operand layout (kda_tc.cuh), so
+// K3 moves them into shared memory with single bulk copies.
+//   AW  [128][128] bf16, R=128: rows 0-63 W, rows 64-127 Qp (K = key channel)
+//   AK  [128][64]  bf16, MN-major (M = key channel, K = token): Kr^T
+//   AQ  [64][64]   bf16, R=64:  A_qk (row i, K = j)
+//   UT  fp32, element (i, e) at ((e/4)*64 + i)*4 + e%4   (U~)
+//   GL  [128] fp32: Gamma_L
+struct Rec {
+  static constexpr uint32_t AW = 0;
+  static constexpr uint32_t AK = AW + 128 * 128 * 2;
+  static constexpr uint32_t AQ = AK + 128 * 64 * 2;
+  static constexpr uint32_t UT = AQ + 64 * 64 * 2;
+  static constexpr uint32_t GL = UT + 64 * 128 * 4;
+  static constexpr uint32_t BYTES = GL + 128 * 4;
+  static constexpr uint32_t kAkSbo = 8 * 128;  // AK: 8 K-groups (64 tokens) per MN-group
+};
+static_assert(Rec::BYTES % 256 == 0, "records stay 256-byte aligned");
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t bf16_bits(float x) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// element j (0..7) of 8 bf16 packed in a uint4
+__device__ __forceinline__ float bf16_at(const uint4& v, int j) {
+  const uint32_t w = j < 2 ? v.x : j < 4 ? v.y : j < 6 ? v.z : v.w;
+  return (j & 1) ? bf16_hi(w) : bf16_lo(w);
+}
+
+__device__ __forceinline__ void flag(int32_t* status, int32_t f) { atomicOr(status, f); }
+
+// log alpha = -softplus(g) with the fast exp/log intrinsics (relative error a
+// few 1e-7; the operands it feeds are rounded to bf16)
+__device__ __forceinline__ float log_alpha_fast(float g) {
+  return g > 20.f ? -g : -__logf(1.f + __expf(g));
+}
+
+cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream);
+
+}  // namespace tcp
+}  // namespace kda

@@ -115,7 +115,6 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
   auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
 
   cudaError_t e = mark(0);
-  if (e == cudaSuccess) e = cudaMemsetAsync(w + L.status, 0, 256, stream);
   if (e == cudaSuccess) e = launch_plan(pp, stream);
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return KDA_ERR_CUDA;

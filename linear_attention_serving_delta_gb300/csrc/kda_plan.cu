@@ -55,11 +55,9 @@ __device__ int64_t block_exclusive_scan(int64_t x, int64_t* sh, int64_t& total) 
   return incl - x;
 }
 
-__global__ void __launch_bounds__(kPlanThreads)
-plan_sequences(PlanParams p) {
-  __shared__ int64_t sh[kPlanThreads];
+// Per-sequence validation, counts and prefix sums (whole block).
+__device__ void plan_sequences(const PlanParams& p, int64_t* sh, int32_t& flags) {
   const int tid = threadIdx.x;
-  int32_t flags = 0;
   int64_t seg_carry = 0, chunk_carry = 0;
   for (int32_t base = 0; base < p.num_seqs; base += kPlanThreads) {
     const int32_t s = base + tid;
@@ -113,29 +111,18 @@ plan_sequences(PlanParams p) {
     seg_carry += seg_total;
     chunk_carry += ch_total;
   }
-  // reduce flags
-  __shared__ int32_t shf;
-  if (tid == 0) shf = 0;
-  __syncthreads();
-  if (flags) atomicOr(&shf, flags);
-  __syncthreads();
   if (tid == 0) {
-    int32_t f = shf;
     int64_t total = chunk_carry;
-    if (total > p.max_chunks) { f |= kFlagChunkOverflow; total = 0; }
+    if (total > p.max_chunks) { flags |= kFlagChunkOverflow; total = 0; }
     p.seq_seg_begin[p.num_seqs] = seg_carry;
     p.seq_chunk_begin[p.num_seqs] = chunk_carry;
     p.meta->total_chunks = total;
-    if (f) atomicOr(p.status, f);
   }
 }
 
-__global__ void plan_fill(PlanParams p, int64_t max_segs) {
-  const int64_t gidx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (gidx >= max_segs) return;
-  if (p.meta->total_chunks == 0) return;
-  const int64_t total_segs = p.seq_seg_begin[p.num_seqs];
-  if (gidx >= total_segs) return;
+// Writes the chunk entries of aligned 64-token segment gidx; bad |= 1 on a
+// snapshot slot outside the caller's snapshot buffer.
+__device__ void fill_segment(const PlanParams& p, int64_t gidx, int32_t& bad) {
   // sequence owning this aligned segment: largest s with seg_begin[s] <= gidx
   int32_t lo = 0, hi = p.num_seqs - 1;
   while (lo < hi) {
@@ -155,7 +142,6 @@ __global__ void plan_fill(PlanParams p, int64_t max_segs) {
   const int64_t snap_lo = p.cu_snapshots ? p.cu_snapshots[s] : 0;
   const int64_t snap_hi = p.cu_snapshots ? p.cu_snapshots[s + 1] : 0;
   int64_t start = seg0;
-  int32_t bad = 0;
   while (start < seg1) {
     int64_t end = seg1;
     if (has_b && j < b1 && p.boundary_pos[j] < seg1) end = p.boundary_pos[j];
@@ -186,23 +172,42 @@ __global__ void plan_fill(PlanParams p, int64_t max_segs) {
     if (has_b && j < b1 && p.boundary_pos[j] == end) ++j;
     start = end;
   }
-  if (bad) atomicOr(p.status, kFlagBadBoundaries);
+}
+
+// One CTA: clears the status word, plans the sequences, writes every chunk
+// entry, and marks the unused tail of the table (len = 0) so that the
+// per-chunk kernels can read their entry without consulting the totals.
+__global__ void __launch_bounds__(kPlanThreads)
+plan_kernel(PlanParams p) {
+  __shared__ int64_t sh[kPlanThreads];
+  __shared__ int32_t shf;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    *p.status = 0;
+    shf = 0;
+  }
+  __syncthreads();
+  int32_t flags = 0;
+  plan_sequences(p, sh, flags);
+  __syncthreads();  // totals written by thread 0 are visible to the block
+  const int64_t total = p.meta->total_chunks;
+  const int64_t total_segs = total > 0 ? p.seq_seg_begin[p.num_seqs] : 0;
+  int32_t bad = 0;
+  for (int64_t gidx = tid; gidx < total_segs; gidx += kPlanThreads) fill_segment(p, gidx, bad);
+  if (bad) flags |= kFlagBadBoundaries;
+  Chunk empty{};
+  empty.snap_slot = -1;
+  for (int64_t ci = total + tid; ci < p.max_chunks; ci += kPlanThreads) p.chunks[ci] = empty;
+  if (flags) atomicOr(&shf, flags);
+  __syncthreads();
+  if (tid == 0 && shf) atomicOr(p.status, shf);
 }
 
 }  // namespace
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
-  plan_sequences<<<1, kPlanThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int64_t max_segs = (p.total_tokens + kChunk - 1) / kChunk + p.num_seqs;
-  if (max_segs > 0) {
-    const int threads = 256;
-    const int64_t blocks = (max_segs + threads - 1) / threads;
-    plan_fill<<<(unsigned)blocks, threads, 0, stream>>>(p, max_segs);
-    e = cudaGetLastError();
-  }
-  return e;
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace kda

@@ -34,9 +34,9 @@ __global__ void __launch_bounds__(kThreads)
 simt_intra(ChunkParams p) {
   extern __shared__ float sm[];
   const int64_t c = blockIdx.x;
-  if (c >= p.meta->total_chunks) return;
+  const Chunk ch = p.chunks[c];  // entries past the table's end have len 0
+  if (ch.len == 0) return;
   const int h = blockIdx.y, H = p.H, dk = p.dk, dv = p.dv;
-  const Chunk ch = p.chunks[c];
   const int len = ch.len;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 

@@ -39,19 +39,21 @@ struct K3Smem {
   static constexpr uint32_t UHI = SOP + kNs * 128 * 2;    // U operand, MN-major (n, i)
   static constexpr uint32_t ULO = UHI + kNs * 64 * 2;
   static constexpr uint32_t BYTES = ULO + kNs * 64 * 2;
-  static constexpr uint32_t TX = 128 * 128 * 2 + 128 * 64 * 2 + 64 * 64 * 2 + 64 * kNs * 4 + 128 * 4;
+  static constexpr uint32_t TILES = UT;  // AW | AK | AQ, contiguous in the record too
+  static constexpr uint32_t TX = TILES + 64 * kNs * 4 + 128 * 4;
 };
+static_assert(K3Smem::AK - K3Smem::AW == Rec::AK - Rec::AW &&
+                  K3Smem::AQ - K3Smem::AW == Rec::AQ - Rec::AW &&
+                  K3Smem::UT - K3Smem::AW == Rec::UT - Rec::AW,
+              "the operand tiles keep the record's relative layout");
 
+// Three bulk copies per chunk: the operand tiles (64 KB), this CTA's slice of
+// U~ and Gamma_L.
 __device__ __forceinline__ void k3_issue_loads(const ChunkParams& p, uint8_t* slot, uint64_t* bar,
                                                int64_t cidx, int h, int n0) {
   const uint8_t* rec = reinterpret_cast<const uint8_t*>(p.inter) + ((size_t)cidx * p.H + h) * Rec::BYTES;
   mbar_arrive_expect_tx(bar, K3Smem::TX);
-  bulk_g2s(slot + K3Smem::AW, rec + Rec::AW, 128 * 128 * 2, bar);
-  bulk_g2s(slot + K3Smem::AK, rec + Rec::AK, 128 * 64 * 2, bar);
-  // A_qk rows into rows 64-127 of a R=128 K-major tile: the second 1 KB of each 2 KB K-block
-#pragma unroll
-  for (int kb = 0; kb < 8; ++kb)
-    bulk_g2s(slot + K3Smem::AQ + kb * 2048 + 1024, rec + Rec::AQ + kb * 1024, 1024, bar);
+  bulk_g2s(slot + K3Smem::AW, rec + Rec::AW, K3Smem::TILES, bar);
   bulk_g2s(slot + K3Smem::UT, rec + Rec::UT + (n0 / 4) * 64 * 16, 64 * kNs * 4, bar);
   bulk_g2s(slot + K3Smem::GL, rec + Rec::GL, 128 * 4, bar);
 }
@@ -94,7 +96,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_inter(ChunkParams p) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ __align__(8) uint64_t bar_full[2];
-  __shared__ __align__(8) uint64_t bar_mma;
+  __shared__ __align__(8) uint64_t bar_mma;   // MMA 1 (one issuing thread)
+  __shared__ __align__(8) uint64_t bar_mma2;  // MMA 2 (state chain)
+  __shared__ __align__(8) uint64_t bar_mma3;  // MMA 3 (output path)
   __shared__ uint32_t tmem_base;
 
   const int s = blockIdx.x, h = blockIdx.y, n0 = blockIdx.z * kNs;
@@ -107,14 +111,13 @@ tc_inter(ChunkParams p) {
   uint8_t* UHI = sm + K3Smem::UHI;
   uint8_t* ULO = sm + K3Smem::ULO;
 
-  // zero both ring slots once: rows 0-63 of the AQ tiles are never loaded
-  for (uint32_t off = tid * 16; off < 2 * K3Smem::SLOT; off += kThreads * 16)
-    *reinterpret_cast<uint4*>(sm + off) = make_uint4(0, 0, 0, 0);
   if (warp == 0) tmem_alloc(&tmem_base, 128);
   if (tid == 0) {
     mbar_init(&bar_full[0], 1);
     mbar_init(&bar_full[1], 1);
     mbar_init(&bar_mma, 1);
+    mbar_init(&bar_mma2, 1);
+    mbar_init(&bar_mma3, 1);
     mbar_init_fence();
   }
   fence_async_smem();
@@ -151,8 +154,8 @@ tc_inter(ChunkParams p) {
 
   const uint32_t id = idesc_bf16(128, kNs, 0, 1);     // B operands MN-major
   const uint32_t id_ak = idesc_bf16(128, kNs, 1, 1);  // Kr^T is MN-major too
-  uint32_t mma_phase = 0;
-  bool ok = true;
+  uint32_t mma_phase = 0, mma2_phase = 0, mma3_phase = 0;
+  bool ok = true, ok3 = true;
   Chunk prev{};
   Chunk next = nchunks > 0 ? p.chunks[c_begin] : Chunk{};
   for (int64_t it = 0; it < nchunks && ok; ++it) {
@@ -163,7 +166,7 @@ tc_inter(ChunkParams p) {
     // S operand (previous iteration) and this slot are ready
     fence_async_smem();
     fence_before_sync();
-    ok = __syncthreads_and(mbar_wait(&bar_full[slot_i], (uint32_t)((it >> 1) & 1), kWaitLimitNs));
+    ok = __syncthreads_and(ok3 && mbar_wait(&bar_full[slot_i], (uint32_t)((it >> 1) & 1), kWaitLimitNs));
     fence_after_sync();
     if (!ok) break;
     if (tid == 0) {
@@ -220,29 +223,33 @@ tc_inter(ChunkParams p) {
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
+    // MMA 2, the state chain: S += Kr^T U; then MMA 3, the output path:
+    // D1[b][64..127] += A_qk U (U as hi + lo).  Separate commits, so the
+    // state write-back below waits for MMA 2 only and overlaps MMA 3.
     if (tid == 0) {
-      // S += Kr^T U   and   D1[b][64..127] += A_qk U   (U as hi + lo)
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         const uint32_t ub = smem_u32(part ? ULO : UHI);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t bdesc = sdesc(ub + k * 256, 128, kUopSbo);
-          mma_bf16(DS, sdesc(smem_u32(slot + K3Smem::AK) + k * 256, 128, Rec::kAkSbo), bdesc,
-                   id_ak, 1);
-          mma_bf16(D1[b], sdesc(smem_u32(slot + K3Smem::AQ) + k * 2 * 128 * 16, 128 * 16, 128),
-                   bdesc, id, 1);
-        }
+        for (int k = 0; k < 4; ++k)
+          mma_bf16(DS, sdesc(smem_u32(slot + K3Smem::AK) + k * 256, 128, Rec::kAkSbo),
+                   sdesc(ub + k * 256, 128, kUopSbo), id_ak, 1);
       }
-      mma_commit(&bar_mma);
+      mma_commit(&bar_mma2);
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        const uint32_t ub = smem_u32(part ? ULO : UHI);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_bf16(D1[b], sdesc(smem_u32(slot + K3Smem::AQ) + k * 2 * 128 * 16, 128 * 16, 128),
+                   sdesc(ub + k * 256, 128, kUopSbo), id, 1);
+      }
+      mma_commit(&bar_mma3);
     }
-    ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, kWaitLimitNs));
-    mma_phase ^= 1;
+    ok = __syncthreads_and(mbar_wait(&bar_mma2, mma2_phase, kWaitLimitNs));
+    mma2_phase ^= 1;
     fence_after_sync();
     if (!ok) break;
-    // this slot is free: prefetch chunk it + 2 into it
-    if (tid == 0 && it + 2 < nchunks)
-      k3_issue_loads(p, slot, &bar_full[slot_i], c_begin + it + 2, h, n0);
     // new state: bf16 operand copy, snapshot if this chunk ends at one
     {
       float v[kNs];
@@ -255,8 +262,20 @@ tc_inter(ChunkParams p) {
           *reinterpret_cast<float4*>(dst + n) = make_float4(v[n], v[n + 1], v[n + 2], v[n + 3]);
       }
     }
+    // warps 2-3 read the outputs of this chunk next step: after their state
+    // rows are written back they wait for MMA 3, after which the slot is free
+    // and a thread of warp 2 refills it with chunk it + 2
+    if (warp >= 2) {
+      ok3 = ok3 && mbar_wait(&bar_mma3, mma3_phase, kWaitLimitNs);
+      fence_after_sync();
+      if (tid == 64 && ok3 && it + 2 < nchunks)
+        k3_issue_loads(p, slot, &bar_full[slot_i], c_begin + it + 2, h, n0);
+    }
+    mma3_phase ^= 1;
     prev = ch;
   }
+  ok = __syncthreads_and(ok && ok3);
+  fence_after_sync();
   if (ok && nchunks > 0 && warp >= 2)
     store_output(p, prev, D1[(nchunks - 1) & 1], lane_off, tid - 64, h, n0);
   if (!ok && tid == 0) flag(p.status, kFlagTimeout);

@@ -132,17 +132,60 @@ __device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ 
   __syncthreads();
 }
 
+// Raw rows of one work item (chunk, head) for this thread: 4 tokens (tb + 16 r)
+// x 8 channels of q, k, g, v, and the update logit of token `tid` (tid < 64).
+struct RawRows {
+  uint4 g[4], q[4], k[4], v[4];
+  float b;
+};
+
+// 16-byte read-only global load kept at its place in the program (volatile),
+// so a prefetch is issued where it is written and not sunk to its first use
+__device__ __forceinline__ uint4 ld_nc16(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
+}
+
+__device__ __forceinline__ void load_rows(const ChunkParams& p, const Chunk& ch, int h, int tb, int c0,
+                                          int tid, RawRows& R) {
+  const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(p.q);
+  const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
+  const __nv_bfloat16* gv = static_cast<const __nv_bfloat16*>(p.v);
+  const __nv_bfloat16* gg = static_cast<const __nv_bfloat16*>(p.g);
+  const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(p.b);
+  const int H = p.H, len = ch.len;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = tb + 16 * r;
+    const int64_t e = ((ch.tok0 + i) * H + h) * (int64_t)kD + c0;
+    const bool live = i < len;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    R.g[r] = live ? ld_nc16(gg + e) : z;
+    R.q[r] = live ? ld_nc16(gq + e) : z;
+    R.k[r] = live ? ld_nc16(gk + e) : z;
+    R.v[r] = live ? ld_nc16(gv + e) : z;
+  }
+  R.b = (tid < 64 && tid < len) ? __bfloat162float(gb[(ch.tok0 + tid) * H + h]) : 0.f;
+}
+
+// Persistent: two CTAs per SM walk the (chunk, head) items with stride
+// gridDim.x.  The raw rows of the next item are loaded into the registers
+// freed once the current item's operands are built, so its DRAM reads
+// overlap this item's MMAs, inverse and record stores.  TMEM and the
+// mbarrier are set up once per CTA.
 __global__ void __launch_bounds__(kThreads, 2)
-tc_intra(ChunkParams p) {
+tc_intra(ChunkParams p, int64_t n_items) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ __align__(8) uint64_t bar_mma;
   __shared__ uint32_t tmem_base;
 
-  const int64_t cidx = blockIdx.x;
-  if (cidx >= p.meta->total_chunks) return;
-  const int h = blockIdx.y, H = p.H;
-  const Chunk ch = p.chunks[cidx];
-  const int len = ch.len;
+  const int64_t stride = gridDim.x;
+  int64_t item = blockIdx.x;
+  if (item >= n_items) return;
+  const int H = p.H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // this thread: tokens tb + 16 r (r = 0..3), channels 8 cb .. 8 cb + 7.  Rows
   // strided by 16 make the eight lanes of each 16-byte store phase hit eight
@@ -150,6 +193,7 @@ tc_intra(ChunkParams p) {
   const int tb = lane & 15;
   const int cb = 2 * warp + (lane >> 4);
   const int c0 = 8 * cb;
+  const int quarter = warp & 3, half = warp >> 2;
 
   uint8_t* A1 = sm + Smem::A1;
   uint8_t* B1 = sm + Smem::B1;
@@ -162,27 +206,6 @@ tc_intra(ChunkParams p) {
   float* inv_k = inv_q + 64;
   float* beta = inv_k + 64;
   float* part = beta + 64;  // [2][8][64]
-  uint8_t* rec = reinterpret_cast<uint8_t*>(p.inter) + ((size_t)cidx * H + h) * Rec::BYTES;
-
-  // ---- all raw loads up front
-  const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(p.q);
-  const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
-  const __nv_bfloat16* gv = static_cast<const __nv_bfloat16*>(p.v);
-  const __nv_bfloat16* gg = static_cast<const __nv_bfloat16*>(p.g);
-  const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(p.b);
-  uint4 gr[4], qr[4], kr[4], vr[4];
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int i = tb + 16 * r;
-    const int64_t e = ((ch.tok0 + i) * H + h) * (int64_t)kD + c0;
-    const bool live = i < len;
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    gr[r] = live ? __ldg(reinterpret_cast<const uint4*>(gg + e)) : z;
-    qr[r] = live ? __ldg(reinterpret_cast<const uint4*>(gq + e)) : z;
-    kr[r] = live ? __ldg(reinterpret_cast<const uint4*>(gk + e)) : z;
-    vr[r] = live ? __ldg(reinterpret_cast<const uint4*>(gv + e)) : z;
-  }
-  const float bval = (tid < 64 && tid < len) ? __bfloat162float(gb[(ch.tok0 + tid) * H + h]) : 0.f;
 
   if (warp == 0) tmem_alloc(&tmem_base, 256);
   if (tid == 0) {
@@ -190,153 +213,182 @@ tc_intra(ChunkParams p) {
     mbar_init_fence();
   }
 
-  // ---- V into B2 MN-major rows 128..255: the raw 16 bytes are one core-matrix row
-#pragma unroll
-  for (int r = 0; r < 4; ++r) st_s16(B2, mnmajor_off(128 + c0, tb + 16 * r, kB2Sbo), vr[r]);
+  // the pipeline: chunk entry and raw rows of the current item, chunk entry of the next
+  Chunk ch = p.chunks[item / H];  // entries past the table's end have len 0
+  RawRows R;
+  load_rows(p, ch, (int)(item % H), tb, c0, tid, R);
+  Chunk ch_next = item + stride < n_items ? p.chunks[(item + stride) / H] : Chunk{};
 
-  // ---- running sums of log alpha: a 16-lane scan per block of 16 tokens,
-  // blocks chained in registers; GL ends as the chunk total
-  float G[4][8], GL[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) GL[j] = 0.f;
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const bool live = tb + 16 * r < len;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float x = live ? log_alpha_fast(bf16_at(gr[r], j)) : 0.f;
-#pragma unroll
-      for (int off = 1; off < 16; off <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, off, 16);
-        if (tb >= off) x += y;
-      }
-      G[r][j] = GL[j] + x;
-      GL[j] += __shfl_sync(0xffffffffu, x, 15, 16);
-    }
-  }
-
-  // ---- L2 norms per token: 8 channels here, 2 per warp, 8 warps
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    float sq = 0.f, sk = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float xq = bf16_at(qr[r], j), xk = bf16_at(kr[r], j);
-      sq += xq * xq;
-      sk += xk * xk;
-    }
-    sq += __shfl_xor_sync(0xffffffffu, sq, 16);
-    sk += __shfl_xor_sync(0xffffffffu, sk, 16);
-    if (lane < 16) {
-      part[warp * 64 + tb + 16 * r] = sq;
-      part[512 + warp * 64 + tb + 16 * r] = sk;
-    }
-  }
-  if (tid < 64) beta[tid] = tid < len ? beta_of(bval) : 0.f;
-  __syncthreads();
-  if (tid < 64) {
-    float sq = 0.f, sk = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      sq += part[w * 64 + tid];
-      sk += part[512 + w * 64 + tid];
-    }
-    inv_q[tid] = inv_norm_of(sq);
-    inv_k[tid] = inv_norm_of(sk);
-  }
-  __syncthreads();
-
-  // ---- operands Kp, Qp (A1), Kn (B1), Kp (B2 MN-major rows 0-127), Kr (record AK, MN-major)
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int i = tb + 16 * r;
-    const float ik = inv_k[i], iq = inv_q[i];
-    float kp[8], qp[8], kn[8], kx[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float kh = bf16_at(kr[r], j) * ik;
-      const float qh = bf16_at(qr[r], j) * iq;
-      const float eg = __expf(G[r][j]);
-      kp[j] = kh * eg;
-      qp[j] = qh * eg;
-      kn[j] = kh * __expf(-G[r][j]);
-      kx[j] = kh * __expf(GL[j] - G[r][j]);
-    }
-    const uint4 kpv = make_uint4(pack_bf16(kp[0], kp[1]), pack_bf16(kp[2], kp[3]),
-                                 pack_bf16(kp[4], kp[5]), pack_bf16(kp[6], kp[7]));
-    st_s16(A1, kmajor_off(i, c0, 128), kpv);
-    st_s16(B2, mnmajor_off(c0, i, kB2Sbo), kpv);
-    st_s16(A1, kmajor_off(64 + i, c0, 128),
-           make_uint4(pack_bf16(qp[0], qp[1]), pack_bf16(qp[2], qp[3]), pack_bf16(qp[4], qp[5]),
-                      pack_bf16(qp[6], qp[7])));
-    st_s16(B1, kmajor_off(i, c0, 64),
-           make_uint4(pack_bf16(kn[0], kn[1]), pack_bf16(kn[2], kn[3]), pack_bf16(kn[4], kn[5]),
-                      pack_bf16(kn[6], kn[7])));
-    *reinterpret_cast<uint4*>(rec + Rec::AK + mnmajor_off(c0, i, Rec::kAkSbo)) =
-        make_uint4(pack_bf16(kx[0], kx[1]), pack_bf16(kx[2], kx[3]), pack_bf16(kx[4], kx[5]),
-                   pack_bf16(kx[6], kx[7]));
-  }
-  if (tb == 0) {  // every lane of the 16-lane group holds the chunk totals
-    float* gl = reinterpret_cast<float*>(rec + Rec::GL) + c0;
-    *reinterpret_cast<float4*>(gl) = make_float4(expf(GL[0]), expf(GL[1]), expf(GL[2]), expf(GL[3]));
-    *reinterpret_cast<float4*>(gl + 4) = make_float4(expf(GL[4]), expf(GL[5]), expf(GL[6]), expf(GL[7]));
-  }
-
-  fence_async_smem();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base;
+  bool ok = true;
 
-  // ---- MMA 1: [A_kk ; A_qk] = [Kp ; Qp] Kn^T   (M=128, N=64, K=128)
-  if (tid == 0) {
-    const uint32_t id = idesc_bf16(128, 64);
+  for (; item < n_items; item += stride) {
+    const int h = (int)(item % H);
+    const int64_t cidx = item / H;
+    const int len = ch.len;
+    if (len == 0) {  // past the end of the chunk table (uniform across the CTA)
+      if (item + stride < n_items) load_rows(p, ch_next, (int)((item + stride) % H), tb, c0, tid, R);
+      ch = ch_next;
+      ch_next = item + 2 * stride < n_items ? p.chunks[(item + 2 * stride) / H] : Chunk{};
+      continue;
+    }
+    uint8_t* rec = reinterpret_cast<uint8_t*>(p.inter) + ((size_t)cidx * H + h) * Rec::BYTES;
+
+    // ---- V into B2 MN-major rows 128..255: the raw 16 bytes are one core-matrix row
 #pragma unroll
-    for (int s = 0; s < 8; ++s)
-      mma_bf16(tmem, sdesc(smem_u32(A1) + s * 2 * 128 * 16, 128 * 16, 128),
-               sdesc(smem_u32(B1) + s * 2 * 64 * 16, 64 * 16, 128), id, s > 0);
-    mma_commit(&bar_mma);
-  }
-  bool ok = __syncthreads_and(mbar_wait(&bar_mma, 0, kWaitLimitNs));
-  fence_after_sync();
-  const int quarter = warp & 3, half = warp >> 2;
-  if (ok) {
-    float d[32];
-    const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + 32 * half;
-    tmem_ld16(ta, d);
-    tmem_ld16(ta + 16, d + 16);
-    tmem_ld_wait();
-    const int row = 32 * quarter + lane;
-    if (quarter < 2) {
-      const int i = row;
-      const float bi = beta[i];
+    for (int r = 0; r < 4; ++r) st_s16(B2, mnmajor_off(128 + c0, tb + 16 * r, kB2Sbo), R.v[r]);
+
+    // ---- running sums of log alpha: a 16-lane scan per block of 16 tokens,
+    // blocks chained in registers; GL ends as the chunk total
+    float G[4][8], GL[8];
 #pragma unroll
-      for (int t = 0; t < 32; t += 4) {
-        const int j = 32 * half + t;
-        *reinterpret_cast<float4*>(AKK + i * kAs + j) =
-            make_float4(j < i ? bi * d[t] : 0.f, j + 1 < i ? bi * d[t + 1] : 0.f,
-                        j + 2 < i ? bi * d[t + 2] : 0.f, j + 3 < i ? bi * d[t + 3] : 0.f);
-      }
-    } else {
-      const int i = row - 64;
-      const bool live = i < len;
+    for (int j = 0; j < 8; ++j) GL[j] = 0.f;
 #pragma unroll
-      for (int t8 = 0; t8 < 4; ++t8) {
-        const int jb = 4 * half + t8;
-        float a[8];
+    for (int r = 0; r < 4; ++r) {
+      const bool live = tb + 16 * r < len;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) a[t] = (live && 8 * jb + t <= i) ? d[8 * t8 + t] : 0.f;
-        *reinterpret_cast<uint4*>(rec + Rec::AQ + kmajor_off(i, 8 * jb, 64)) =
-            make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]),
-                       pack_bf16(a[6], a[7]));
+      for (int j = 0; j < 8; ++j) {
+        float x = live ? log_alpha_fast(bf16_at(R.g[r], j)) : 0.f;
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, x, off, 16);
+          if (tb >= off) x += y;
+        }
+        G[r][j] = GL[j] + x;
+        GL[j] += __shfl_sync(0xffffffffu, x, 15, 16);
       }
     }
-  }
-  fence_before_sync();
-  __syncthreads();
 
-  // ---- T = (I + A_kk)^{-1}; Tb = T diag(beta) -> A2 (bf16, R=64)
-  if (ok) {
+    // ---- L2 norms per token: 8 channels here, 2 per warp, 8 warps
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float xq = bf16_at(R.q[r], j), xk = bf16_at(R.k[r], j);
+        sq += xq * xq;
+        sk += xk * xk;
+      }
+      sq += __shfl_xor_sync(0xffffffffu, sq, 16);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 16);
+      if (lane < 16) {
+        part[warp * 64 + tb + 16 * r] = sq;
+        part[512 + warp * 64 + tb + 16 * r] = sk;
+      }
+    }
+    if (tid < 64) beta[tid] = tid < len ? beta_of(R.b) : 0.f;
+    // the previous item's record copy must have finished reading A1
+    if (tid == 0) bulk_wait_read_all();
+    __syncthreads();
+    if (tid < 64) {
+      float sq = 0.f, sk = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        sq += part[w * 64 + tid];
+        sk += part[512 + w * 64 + tid];
+      }
+      inv_q[tid] = inv_norm_of(sq);
+      inv_k[tid] = inv_norm_of(sk);
+    }
+    __syncthreads();
+
+    // ---- operands Kp, Qp (A1), Kn (B1), Kp (B2 MN-major rows 0-127), Kr (record AK, MN-major)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = tb + 16 * r;
+      const float ik = inv_k[i], iq = inv_q[i];
+      float kp[8], qp[8], kn[8], kx[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float kh = bf16_at(R.k[r], j) * ik;
+        const float qh = bf16_at(R.q[r], j) * iq;
+        const float eg = __expf(G[r][j]);
+        kp[j] = kh * eg;
+        qp[j] = qh * eg;
+        kn[j] = kh * __expf(-G[r][j]);
+        kx[j] = kh * __expf(GL[j] - G[r][j]);
+      }
+      const uint4 kpv = make_uint4(pack_bf16(kp[0], kp[1]), pack_bf16(kp[2], kp[3]),
+                                   pack_bf16(kp[4], kp[5]), pack_bf16(kp[6], kp[7]));
+      st_s16(A1, kmajor_off(i, c0, 128), kpv);
+      st_s16(B2, mnmajor_off(c0, i, kB2Sbo), kpv);
+      st_s16(A1, kmajor_off(64 + i, c0, 128),
+             make_uint4(pack_bf16(qp[0], qp[1]), pack_bf16(qp[2], qp[3]), pack_bf16(qp[4], qp[5]),
+                        pack_bf16(qp[6], qp[7])));
+      st_s16(B1, kmajor_off(i, c0, 64),
+             make_uint4(pack_bf16(kn[0], kn[1]), pack_bf16(kn[2], kn[3]), pack_bf16(kn[4], kn[5]),
+                        pack_bf16(kn[6], kn[7])));
+      *reinterpret_cast<uint4*>(rec + Rec::AK + mnmajor_off(c0, i, Rec::kAkSbo)) =
+          make_uint4(pack_bf16(kx[0], kx[1]), pack_bf16(kx[2], kx[3]), pack_bf16(kx[4], kx[5]),
+                     pack_bf16(kx[6], kx[7]));
+    }
+    if (tb == 0) {  // every lane of the 16-lane group holds the chunk totals
+      float* gl = reinterpret_cast<float*>(rec + Rec::GL) + c0;
+      *reinterpret_cast<float4*>(gl) = make_float4(expf(GL[0]), expf(GL[1]), expf(GL[2]), expf(GL[3]));
+      *reinterpret_cast<float4*>(gl + 4) = make_float4(expf(GL[4]), expf(GL[5]), expf(GL[6]), expf(GL[7]));
+    }
+
+    // ---- the raw registers are free: start loading the next item
+    if (item + stride < n_items) load_rows(p, ch_next, (int)((item + stride) % H), tb, c0, tid, R);
+    ch = ch_next;
+    ch_next = item + 2 * stride < n_items ? p.chunks[(item + 2 * stride) / H] : Chunk{};
+
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    // ---- MMA 1: [A_kk ; A_qk] = [Kp ; Qp] Kn^T   (M=128, N=64, K=128)
+    if (tid == 0) {
+      const uint32_t id = idesc_bf16(128, 64);
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        mma_bf16(tmem, sdesc(smem_u32(A1) + s * 2 * 128 * 16, 128 * 16, 128),
+                 sdesc(smem_u32(B1) + s * 2 * 64 * 16, 64 * 16, 128), id, s > 0);
+      mma_commit(&bar_mma);
+    }
+    ok = __syncthreads_and(mbar_wait(&bar_mma, 0, kWaitLimitNs));
+    fence_after_sync();
+    if (!ok) break;
+    {
+      float d[32];
+      const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + 32 * half;
+      tmem_ld16(ta, d);
+      tmem_ld16(ta + 16, d + 16);
+      tmem_ld_wait();
+      const int row = 32 * quarter + lane;
+      if (quarter < 2) {
+        const int i = row;
+        const float bi = beta[i];
+#pragma unroll
+        for (int t = 0; t < 32; t += 4) {
+          const int j = 32 * half + t;
+          *reinterpret_cast<float4*>(AKK + i * kAs + j) =
+              make_float4(j < i ? bi * d[t] : 0.f, j + 1 < i ? bi * d[t + 1] : 0.f,
+                          j + 2 < i ? bi * d[t + 2] : 0.f, j + 3 < i ? bi * d[t + 3] : 0.f);
+        }
+      } else {
+        const int i = row - 64;
+        const bool live = i < len;
+#pragma unroll
+        for (int t8 = 0; t8 < 4; ++t8) {
+          const int jb = 4 * half + t8;
+          float a[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) a[t] = (live && 8 * jb + t <= i) ? d[8 * t8 + t] : 0.f;
+          *reinterpret_cast<uint4*>(rec + Rec::AQ + kmajor_off(64 + i, 8 * jb, 128)) =
+              make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]),
+                         pack_bf16(a[6], a[7]));
+        }
+      }
+    }
+    fence_before_sync();
+    __syncthreads();
+
+    // ---- T = (I + A_kk)^{-1}; Tb = T diag(beta) -> A2 (bf16, R=64)
     tri_inverse_64(AKK, TT, XS);
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -350,65 +402,69 @@ tc_intra(ChunkParams p) {
              make_uint4(pack_bf16(t0.x * b0.x, t0.y * b0.y), pack_bf16(t0.z * b0.z, t0.w * b0.w),
                         pack_bf16(t1.x * b1.x, t1.y * b1.y), pack_bf16(t1.z * b1.z, t1.w * b1.w)));
     }
-  }
-  fence_async_smem();
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
 
-  // ---- MMA 2: [W | U~] = Tb [Kp | V]   (M=64, N=256, K=64)
-  if (ok && tid == 0) {
-    const uint32_t id = idesc_bf16(64, 256, 0, 1);  // B2 is MN-major
+    // ---- MMA 2: [W | U~] = Tb [Kp | V]   (M=64, N=256, K=64)
+    if (tid == 0) {
+      const uint32_t id = idesc_bf16(64, 256, 0, 1);  // B2 is MN-major
 #pragma unroll
-    for (int s = 0; s < 4; ++s)
-      mma_bf16(tmem, sdesc(smem_u32(A2) + s * 2 * 64 * 16, 64 * 16, 128),
-               sdesc(smem_u32(B2) + s * 256, 128, kB2Sbo), id, s > 0);
-    mma_commit(&bar_mma);
-  }
-  ok = __syncthreads_and(ok && mbar_wait(&bar_mma, 1, kWaitLimitNs));
-  fence_after_sync();
-  if (ok) {
-    // M=64 accumulator: row r sits in TMEM lane (r/16)*32 + r%16; warps 0-3
-    // take W (columns 0-127), warps 4-7 take U~ (columns 128-255)
-    const int i = 16 * quarter + (lane & 15);
-    const bool row_lane = lane < 16;
-    const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + 128 * half;
+      for (int s = 0; s < 4; ++s)
+        mma_bf16(tmem, sdesc(smem_u32(A2) + s * 2 * 64 * 16, 64 * 16, 128),
+                 sdesc(smem_u32(B2) + s * 256, 128, kB2Sbo), id, s > 0);
+      mma_commit(&bar_mma);
+    }
+    ok = __syncthreads_and(mbar_wait(&bar_mma, 1, kWaitLimitNs));
+    fence_after_sync();
+    if (!ok) break;
+    {
+      // M=64 accumulator: row r sits in TMEM lane (r/16)*32 + r%16; warps 0-3
+      // take W (columns 0-127), warps 4-7 take U~ (columns 128-255)
+      const int i = 16 * quarter + (lane & 15);
+      const bool row_lane = lane < 16;
+      const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + 128 * half;
 #pragma unroll
-    for (int c = 0; c < 128; c += 64) {
-      float d[64];
+      for (int c = 0; c < 128; c += 32) {
+        float d[32];
+        tmem_ld16(ta + c, d);
+        tmem_ld16(ta + c + 16, d + 16);
+        tmem_ld_wait();
+        if (row_lane) {
+          if (half == 0) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) tmem_ld16(ta + c + 16 * u, d + 16 * u);
-      tmem_ld_wait();
-      if (row_lane) {
-        if (half == 0) {
+            for (int u = 0; u < 4; ++u)
+              st_s16(A1, kmajor_off(i, c + 8 * u, 128),
+                     make_uint4(pack_bf16(d[8 * u], d[8 * u + 1]), pack_bf16(d[8 * u + 2], d[8 * u + 3]),
+                                pack_bf16(d[8 * u + 4], d[8 * u + 5]),
+                                pack_bf16(d[8 * u + 6], d[8 * u + 7])));
+          } else {
+            float* ut = reinterpret_cast<float*>(rec + Rec::UT);
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            st_s16(A1, kmajor_off(i, c + 8 * u, 128),
-                   make_uint4(pack_bf16(d[8 * u], d[8 * u + 1]), pack_bf16(d[8 * u + 2], d[8 * u + 3]),
-                              pack_bf16(d[8 * u + 4], d[8 * u + 5]),
-                              pack_bf16(d[8 * u + 6], d[8 * u + 7])));
-        } else {
-          float* ut = reinterpret_cast<float*>(rec + Rec::UT);
-#pragma unroll
-          for (int q4 = 0; q4 < 16; ++q4)
-            *reinterpret_cast<float4*>(ut + (((c >> 2) + q4) * 64 + i) * 4) =
-                make_float4(d[4 * q4], d[4 * q4 + 1], d[4 * q4 + 2], d[4 * q4 + 3]);
+            for (int q4 = 0; q4 < 8; ++q4)
+              *reinterpret_cast<float4*>(ut + (((c >> 2) + q4) * 64 + i) * 4) =
+                  make_float4(d[4 * q4], d[4 * q4 + 1], d[4 * q4 + 2], d[4 * q4 + 3]);
+          }
         }
       }
     }
-  }
-  fence_async_smem();
-  fence_before_sync();
-  __syncthreads();
-  if (tid == 0) {
-    if (ok) {
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    // [W ; Qp] to the record in one bulk copy; its completion is awaited
+    // before A1 is rewritten by the next item
+    if (tid == 0) {
       bulk_s2g(rec + Rec::AW, A1, 128 * 128 * 2);
       bulk_commit();
-      bulk_wait_read_all();  // shared memory may be released once the copy has read it
-    } else {
-      flag(p.status, kFlagTimeout);
     }
   }
+  if (tid == 0) {
+    if (!ok) flag(p.status, kFlagTimeout);
+    bulk_wait_all();
+  }
+  fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
@@ -419,8 +475,13 @@ cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(tc_intra, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)Smem::BYTES);
   if (e != cudaSuccess || p.max_chunks == 0) return e;
-  dim3 grid((unsigned)p.max_chunks, (unsigned)p.H);
-  tc_intra<<<grid, kThreads, Smem::BYTES, stream>>>(p);
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t n_items = p.max_chunks * (int64_t)p.H;
+  const int64_t grid = n_items < 2 * (int64_t)sms ? n_items : 2 * (int64_t)sms;
+  tc_intra<<<(unsigned)grid, kThreads, Smem::BYTES, stream>>>(p, n_items);
   return cudaGetLastError();
 }
 

@@ -123,6 +123,25 @@ size_t kda_prefill_workspace_size(const kda_prefill_args* args);
 kda_status_t kda_prefill(const kda_prefill_args* args, void* ws, size_t ws_bytes,
                          void* stream);
 
+/* kda_prefill for callers that cannot allocate device memory at the point of
+ * the call (all of HBM reserved up front for state pools, a host framework
+ * that owns every allocation, or a path where an allocation would
+ * synchronise the device).  This entry has no counterpart on the pages; it
+ * is a deployment convenience.  It runs the same kernels as kda_prefill on a
+ * workspace held in a fixed 64 MiB (67108864-byte) __device__ array inside
+ * this library, which every GPU that loads the library keeps until the
+ * process exits; the call itself allocates nothing.
+ *   - Arguments whose kda_prefill_workspace_size exceeds 64 MiB are rejected
+ *     with KDA_ERR_WORKSPACE before any launch (for example about 650
+ *     (chunk, head) pairs on the bf16 dk = dv = 128 path).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the array: calls whose kernels overlap on the GPU race
+ *     on it, so serialise them (one stream, or events).  Nothing in it needs
+ *     to start at zero; its device status word is not readable afterwards
+ *     through kda_prefill_device_status. */
+kda_status_t kda_prefill_noalloc(const kda_prefill_args* args, void* stream);
+
 /* Copies the workspace status word of the last kda_prefill that used `ws`
  * to *out (host), synchronising `stream`.  0 = clean; otherwise a bitwise OR
  * of 1 (malformed cu_seqlens), 2 (malformed boundary positions), 4 (chunk

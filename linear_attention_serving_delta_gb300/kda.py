@@ -30,9 +30,10 @@ PREFILL_PHASES = 3  # chunk planning, intra-chunk, inter-chunk
 _STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED",
                  3: "KDA_ERR_WORKSPACE", 4: "KDA_ERR_CUDA", 5: "KDA_ERR_TIMEOUT",
                  6: "KDA_ERR_DEVICE_DATA"}
-EXPORTED = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_device_status",
-            "kda_snapshot_plan", "kda_decode_step", "kda_prep", "kda_status_string",
-            "kda_version")
+EXPORTED = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_noalloc",
+            "kda_prefill_device_status", "kda_snapshot_plan", "kda_decode_step", "kda_prep",
+            "kda_status_string", "kda_version")
+NOALLOC_SCRATCH_BYTES = 64 << 20  # fixed workspace behind kda_prefill_noalloc
 
 
 class KdaError(RuntimeError):
@@ -86,6 +87,8 @@ def lib() -> ctypes.CDLL:
             L.kda_prefill_workspace_size.restype = ctypes.c_size_t
             L.kda_prefill.argtypes = [ctypes.POINTER(PrefillArgs), c_vp, ctypes.c_size_t, c_vp]
             L.kda_prefill.restype = ctypes.c_int
+            L.kda_prefill_noalloc.argtypes = [ctypes.POINTER(PrefillArgs), c_vp]
+            L.kda_prefill_noalloc.restype = ctypes.c_int
             L.kda_prefill_device_status.argtypes = [c_vp, ctypes.POINTER(c_i32), c_vp]
             L.kda_prefill_device_status.restype = ctypes.c_int
             L.kda_snapshot_plan.argtypes = [c_vp, c_i32, c_i64, c_vp, c_vp, c_vp]
@@ -183,6 +186,12 @@ def kda_prefill(args: PrefillArgs, workspace: torch.Tensor, stream=None) -> None
     ws = _ptr(workspace, torch.uint8, "workspace")
     _check(lib().kda_prefill(ctypes.byref(args), ws, workspace.numel(), _stream(stream)),
            "kda_prefill")
+
+
+def kda_prefill_noalloc(args: PrefillArgs, stream=None) -> None:
+    """kda_prefill on the library's fixed workspace (for callers that cannot
+    allocate device memory at the call); see include/kda.h for its limits."""
+    _check(lib().kda_prefill_noalloc(ctypes.byref(args), _stream(stream)), "kda_prefill_noalloc")
 
 
 def kda_prefill_device_status(workspace: torch.Tensor, stream=None) -> int:

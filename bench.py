@@ -37,6 +37,42 @@ INTER_FLOP_PER_CHUNK_HEAD = 2 * 64 * 128 * 128 * 2 + 2 * 64 * 64 * 128 + 2 * 128
 DECODE_STATE_BYTES_PER_HEAD = 2 * 128 * 128 * 4                # read + write fp32 state
 
 
+# sources each kernel is built from: a profile summary counts only while
+# these files hash to the value recorded in it
+KERNEL_SOURCES = {
+    "tc_intra": ["kda_tc_intra.cu", "kda_tc_common.cuh", "kda_tc.cuh", "kda_internal.cuh",
+                 "kda_common.cuh"],
+    "tc_inter": ["kda_tc_inter.cu", "kda_tc_common.cuh", "kda_tc.cuh", "kda_internal.cuh",
+                 "kda_common.cuh"],
+    "decode_ring": ["kda_decode.cu", "kda_tc.cuh", "kda_internal.cuh", "kda_common.cuh"],
+}
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (read + write) from the committed ncu summary
+    profiles/<kernel>_<workload>.md, or None if the kernel changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
+        return None
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "linear_attention_serving_delta_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    rec = {}
+    with open(path) as fh:
+        for line in fh:
+            if line.startswith("- ") and ":" in line:
+                key, val = line[2:].split(":", 1)
+                rec[key.strip()] = val.split()[0] if val.split() else ""
+    if rec.get("source_sha256") != h.hexdigest()[:16]:
+        return None
+    try:
+        return int(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -145,7 +181,7 @@ def bench_prefill(torch, kda, W, steps, warmup, dev):
     assert p.device_status() == 0
     n_chunks = (T + 63) // 64
     return dict(T=T, H=w.H, step_ms=step_ms, phase_ms=phase_ms, n_chunks=n_chunks,
-                launches_per_step=4, workload=w)
+                launches_per_step=3, workload=w)
 
 
 def bench_decode(torch, kda, W, steps, warmup, dev):
@@ -276,13 +312,18 @@ def gpu_arm(a):
     if names[dom] == "intra_chunk":
         roof = {"kernel": "intra_chunk", "bound": "tensor", "achieved": intra_tflops,
                 "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": intra_tflops / pk["bf16_tflops"], "traffic": None}
+                "frac": intra_tflops / pk["bf16_tflops"],
+                "traffic": ncu_traffic("tc_intra", PREFILL_WL),
+                "algorithmic_flop_per_chunk_head": INTRA_FLOP_PER_CHUNK_HEAD}
     else:
         # the serial inter-chunk kernel: its algorithmic FLOPs against the tensor peak
         roof = {"kernel": names[dom], "bound": "tensor", "achieved": inter_tflops,
                 "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": inter_tflops / pk["bf16_tflops"], "traffic": None}
+                "frac": inter_tflops / pk["bf16_tflops"],
+                "traffic": ncu_traffic("tc_inter", PREFILL_WL),
+                "algorithmic_flop_per_chunk_head": INTER_FLOP_PER_CHUNK_HEAD}
     roof["peak_source"] = pk["source"]
+    roof["input_bytes_per_launch"] = (PREFILL_BYTES_PER_TOKEN_HEAD - 256) * T * H
     dec_gbs = DECODE_STATE_BYTES_PER_HEAD * dec["heads"] / (dec_ms * 1e-3) / 1e9
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -302,7 +343,9 @@ def gpu_arm(a):
                    "tokens_per_s": world * dec["batch"] / (dec_ms * 1e-3),
                    "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": pk["hbm_gbs"],
                                 "unit": "GB/s", "frac": dec_gbs / pk["hbm_gbs"],
-                                "traffic": None, "peak_source": pk["source"]},
+                                "traffic": ncu_traffic("decode_ring", DECODE_WL),
+                                "algorithmic_bytes_per_launch": DECODE_STATE_BYTES_PER_HEAD * dec["heads"],
+                                "peak_source": pk["source"]},
                    "steps": dec["steps"]},
         "kernels": kernels,
         "e2e": {"value": e2e["value"], "unit": e2e["unit"],

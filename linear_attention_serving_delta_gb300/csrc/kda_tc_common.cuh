@@ -69,11 +69,10 @@ __device__ __forceinline__ float bf16_at(const uint4& v, int j) {
 
 __device__ __forceinline__ void flag(int32_t* status, int32_t f) { atomicOr(status, f); }
 
-// log alpha = -softplus(g) with the fast exp/log intrinsics (relative error a
-// few 1e-7; the operands it feeds are rounded to bf16)
-__device__ __forceinline__ float log_alpha_fast(float g) {
-  return g > 20.f ? -g : -__logf(1.f + __expf(g));
-}
+// alpha = exp(-softplus(g)) = 1 / (1 + e^g) with the fast exp and division
+// intrinsics (relative error a few 1e-7; the operands it feeds are rounded to
+// bf16).  e^g overflowing to +inf gives alpha = 0.
+__device__ __forceinline__ float alpha_fast(float g) { return __fdividef(1.f, 1.f + __expf(g)); }
 
 cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream);
 

@@ -1,12 +1,13 @@
 // kda_tc_intra.cu -- K2, the intra-chunk kernel of the tensor-core prefill.
 //
-// One CTA per (chunk, head), 256 threads, two CTAs per SM.  Each thread owns
-// 4 tokens (strided by 16) x 8 channels: it issues all of its q, k, g, v loads
-// up front (16-byte loads, one DRAM round trip), scans the log-decays (16-lane
-// shuffle scans chained over the 4 token blocks), normalises q and k, and
-// writes the operands with conflict-free 16-byte shared stores straight into
-// the tcgen05 layouts (K-major where a row of 8 channels is one core-matrix
-// row, MN-major where 8 channels of one token are).  Then:
+// Persistent, two CTAs of 256 threads per SM.  For each (chunk, head) item
+// every thread owns 4 consecutive tokens x 8 channels: its q, k, g, v rows
+// (16-byte loads, prefetched during the previous item), the cumulative decay
+// Gamma as a product scan (in registers, then across the 16 token blocks with
+// shuffles), normalised q and k, and the operands written with 16-byte
+// shared stores straight into the tcgen05 layouts (K-major where a row of 8
+// channels is one core-matrix row, MN-major where 8 channels of one token
+// are).  Then:
 //   MMA 1 (M=128, N=64, K=128):  [A_kk ; A_qk] = [Kp ; Qp] Kn^T  -> TMEM
 //   CUDA cores: T = (I + A_kk)^{-1}, two-level blocked inverse
 //   MMA 2 (M=64, N=256, K=64):   [W | U~] = T diag(beta) [Kp | V] -> TMEM
@@ -132,7 +133,7 @@ __device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ 
   __syncthreads();
 }
 
-// Raw rows of one work item (chunk, head) for this thread: 4 tokens (tb + 16 r)
+// Raw rows of one work item (chunk, head) for this thread: 4 tokens (4 tb + r)
 // x 8 channels of q, k, g, v, and the update logit of token `tid` (tid < 64).
 struct RawRows {
   uint4 g[4], q[4], k[4], v[4];
@@ -149,26 +150,34 @@ __device__ __forceinline__ uint4 ld_nc16(const void* ptr) {
   return v;
 }
 
-__device__ __forceinline__ void load_rows(const ChunkParams& p, const Chunk& ch, int h, int tb, int c0,
-                                          int tid, RawRows& R) {
-  const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(p.q);
-  const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.k);
-  const __nv_bfloat16* gv = static_cast<const __nv_bfloat16*>(p.v);
-  const __nv_bfloat16* gg = static_cast<const __nv_bfloat16*>(p.g);
-  const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(p.b);
+// One of the four tensors' rows (0 g, 1 q, 2 k, 3 v) of an item.  The
+// prefetch of the next item is spread over the current item's phases, so
+// that the load-queue back-pressure of each group drains behind compute.
+__device__ __forceinline__ void load_part(const ChunkParams& p, const Chunk& ch, int h, int tb, int c0,
+                                          int which, uint4* dst) {
+  const void* base = which == 0 ? p.g : which == 1 ? p.q : which == 2 ? p.k : p.v;
+  const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(base);
   const int H = p.H, len = ch.len;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
-    const int i = tb + 16 * r;
+    const int i = 4 * tb + r;
     const int64_t e = ((ch.tok0 + i) * H + h) * (int64_t)kD + c0;
-    const bool live = i < len;
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    R.g[r] = live ? ld_nc16(gg + e) : z;
-    R.q[r] = live ? ld_nc16(gq + e) : z;
-    R.k[r] = live ? ld_nc16(gk + e) : z;
-    R.v[r] = live ? ld_nc16(gv + e) : z;
+    dst[r] = i < len ? ld_nc16(src + e) : make_uint4(0, 0, 0, 0);
   }
-  R.b = (tid < 64 && tid < len) ? __bfloat162float(gb[(ch.tok0 + tid) * H + h]) : 0.f;
+}
+
+__device__ __forceinline__ float load_b(const ChunkParams& p, const Chunk& ch, int h, int tid) {
+  const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(p.b);
+  return (tid < 64 && tid < ch.len) ? __bfloat162float(gb[(ch.tok0 + tid) * p.H + h]) : 0.f;
+}
+
+__device__ __forceinline__ void load_rows(const ChunkParams& p, const Chunk& ch, int h, int tb, int c0,
+                                          int tid, RawRows& R) {
+  load_part(p, ch, h, tb, c0, 0, R.g);
+  load_part(p, ch, h, tb, c0, 1, R.q);
+  load_part(p, ch, h, tb, c0, 2, R.k);
+  load_part(p, ch, h, tb, c0, 3, R.v);
+  R.b = load_b(p, ch, h, tid);
 }
 
 // Persistent: two CTAs per SM walk the (chunk, head) items with stride
@@ -187,11 +196,11 @@ tc_intra(ChunkParams p, int64_t n_items) {
   if (item >= n_items) return;
   const int H = p.H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // this thread: tokens tb + 16 r (r = 0..3), channels 8 cb .. 8 cb + 7.  Rows
-  // strided by 16 make the eight lanes of each 16-byte store phase hit eight
-  // distinct rows (i % 8), so the operand stores are free of bank conflicts.
-  const int tb = lane & 15;
-  const int cb = 2 * warp + (lane >> 4);
+  // this thread: tokens 4 tb .. 4 tb + 3, channels 8 cb .. 8 cb + 7.  Four
+  // consecutive tokens per thread keep the decay scan in registers (one
+  // shuffle per element); the operand stores see at most 4-way bank conflicts.
+  const int tb = lane >> 1;
+  const int cb = 2 * warp + (lane & 1);
   const int c0 = 8 * cb;
   const int quarter = warp & 3, half = warp >> 2;
 
@@ -239,27 +248,32 @@ tc_intra(ChunkParams p, int64_t n_items) {
 
     // ---- V into B2 MN-major rows 128..255: the raw 16 bytes are one core-matrix row
 #pragma unroll
-    for (int r = 0; r < 4; ++r) st_s16(B2, mnmajor_off(128 + c0, tb + 16 * r, kB2Sbo), R.v[r]);
+    for (int r = 0; r < 4; ++r) st_s16(B2, mnmajor_off(128 + c0, 4 * tb + r, kB2Sbo), R.v[r]);
 
-    // ---- running sums of log alpha: a 16-lane scan per block of 16 tokens,
-    // blocks chained in registers; GL ends as the chunk total
-    float G[4][8], GL[8];
+    // ---- cumulative decay Gamma_i = prod_{m<=i} alpha_m, alpha = 1 / (1 + e^g)
+    // (= exp(-softplus(g))): a product over this thread's 4 tokens, then an
+    // exclusive product scan across the 16 token blocks (lanes 2 apart)
+    float Gm[4][8], GLm[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) GL[j] = 0.f;
+    for (int j = 0; j < 8; ++j) {
+      float run = 1.f;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const bool live = tb + 16 * r < len;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float x = live ? log_alpha_fast(bf16_at(R.g[r], j)) : 0.f;
-#pragma unroll
-        for (int off = 1; off < 16; off <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, x, off, 16);
-          if (tb >= off) x += y;
-        }
-        G[r][j] = GL[j] + x;
-        GL[j] += __shfl_sync(0xffffffffu, x, 15, 16);
+      for (int r = 0; r < 4; ++r) {
+        const float a = 4 * tb + r < len ? alpha_fast(bf16_at(R.g[r], j)) : 1.f;
+        run *= a;
+        Gm[r][j] = run;
       }
+      float inc = run;
+#pragma unroll
+      for (int off = 2; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc *= y;
+      }
+      float ex = __shfl_up_sync(0xffffffffu, inc, 2);
+      if (lane < 2) ex = 1.f;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) Gm[r][j] *= ex;
+      GLm[j] = __shfl_sync(0xffffffffu, inc, 30 + (lane & 1));
     }
 
     // ---- L2 norms per token: 8 channels here, 2 per warp, 8 warps
@@ -272,11 +286,11 @@ tc_intra(ChunkParams p, int64_t n_items) {
         sq += xq * xq;
         sk += xk * xk;
       }
-      sq += __shfl_xor_sync(0xffffffffu, sq, 16);
-      sk += __shfl_xor_sync(0xffffffffu, sk, 16);
-      if (lane < 16) {
-        part[warp * 64 + tb + 16 * r] = sq;
-        part[512 + warp * 64 + tb + 16 * r] = sk;
+      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+      if ((lane & 1) == 0) {
+        part[warp * 64 + 4 * tb + r] = sq;
+        part[512 + warp * 64 + 4 * tb + r] = sk;
       }
     }
     if (tid < 64) beta[tid] = tid < len ? beta_of(R.b) : 0.f;
@@ -298,18 +312,18 @@ tc_intra(ChunkParams p, int64_t n_items) {
     // ---- operands Kp, Qp (A1), Kn (B1), Kp (B2 MN-major rows 0-127), Kr (record AK, MN-major)
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const int i = tb + 16 * r;
+      const int i = 4 * tb + r;
       const float ik = inv_k[i], iq = inv_q[i];
       float kp[8], qp[8], kn[8], kx[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float kh = bf16_at(R.k[r], j) * ik;
         const float qh = bf16_at(R.q[r], j) * iq;
-        const float eg = __expf(G[r][j]);
-        kp[j] = kh * eg;
-        qp[j] = qh * eg;
-        kn[j] = kh * __expf(-G[r][j]);
-        kx[j] = kh * __expf(GL[j] - G[r][j]);
+        const float gam = Gm[r][j];
+        kp[j] = kh * gam;
+        qp[j] = qh * gam;
+        kn[j] = __fdividef(kh, gam);
+        kx[j] = kn[j] * GLm[j];
       }
       const uint4 kpv = make_uint4(pack_bf16(kp[0], kp[1]), pack_bf16(kp[2], kp[3]),
                                    pack_bf16(kp[4], kp[5]), pack_bf16(kp[6], kp[7]));
@@ -325,14 +339,18 @@ tc_intra(ChunkParams p, int64_t n_items) {
           make_uint4(pack_bf16(kx[0], kx[1]), pack_bf16(kx[2], kx[3]), pack_bf16(kx[4], kx[5]),
                      pack_bf16(kx[6], kx[7]));
     }
-    if (tb == 0) {  // every lane of the 16-lane group holds the chunk totals
+    if (tb == 0) {  // every lane holds its channels' chunk totals
       float* gl = reinterpret_cast<float*>(rec + Rec::GL) + c0;
-      *reinterpret_cast<float4*>(gl) = make_float4(expf(GL[0]), expf(GL[1]), expf(GL[2]), expf(GL[3]));
-      *reinterpret_cast<float4*>(gl + 4) = make_float4(expf(GL[4]), expf(GL[5]), expf(GL[6]), expf(GL[7]));
+      *reinterpret_cast<float4*>(gl) = make_float4(GLm[0], GLm[1], GLm[2], GLm[3]);
+      *reinterpret_cast<float4*>(gl + 4) = make_float4(GLm[4], GLm[5], GLm[6], GLm[7]);
     }
 
-    // ---- the raw registers are free: start loading the next item
-    if (item + stride < n_items) load_rows(p, ch_next, (int)((item + stride) % H), tb, c0, tid, R);
+    // ---- the raw registers are free: the next item's rows are loaded in four
+    // groups spread over this item's phases (g now, q, k, v below)
+    const bool has_next = item + stride < n_items;
+    const Chunk chn = ch_next;
+    const int hn = (int)((item + stride) % H);
+    if (has_next) load_part(p, chn, hn, tb, c0, 0, R.g);
     ch = ch_next;
     ch_next = item + 2 * stride < n_items ? p.chunks[(item + 2 * stride) / H] : Chunk{};
 
@@ -350,6 +368,7 @@ tc_intra(ChunkParams p, int64_t n_items) {
                  sdesc(smem_u32(B1) + s * 2 * 64 * 16, 64 * 16, 128), id, s > 0);
       mma_commit(&bar_mma);
     }
+    if (has_next) load_part(p, chn, hn, tb, c0, 1, R.q);
     ok = __syncthreads_and(mbar_wait(&bar_mma, 0, kWaitLimitNs));
     fence_after_sync();
     if (!ok) break;
@@ -385,6 +404,7 @@ tc_intra(ChunkParams p, int64_t n_items) {
         }
       }
     }
+    if (has_next) load_part(p, chn, hn, tb, c0, 2, R.k);
     fence_before_sync();
     __syncthreads();
 
@@ -401,6 +421,10 @@ tc_intra(ChunkParams p, int64_t n_items) {
       st_s16(A2, kmajor_off(i, 8 * jb, 64),
              make_uint4(pack_bf16(t0.x * b0.x, t0.y * b0.y), pack_bf16(t0.z * b0.z, t0.w * b0.w),
                         pack_bf16(t1.x * b1.x, t1.y * b1.y), pack_bf16(t1.z * b1.z, t1.w * b1.w)));
+    }
+    if (has_next) {
+      load_part(p, chn, hn, tb, c0, 3, R.v);
+      R.b = load_b(p, chn, hn, tid);
     }
     fence_async_smem();
     fence_before_sync();

@@ -35,17 +35,18 @@ constexpr uint32_t kD = 128;  // dk = dv on this path
 // K3 moves them into shared memory with single bulk copies.
 //   AW  [128][128] bf16, R=128: rows 0-63 W, rows 64-127 Qp (K = key channel)
 //   AK  [128][64]  bf16, MN-major (M = key channel, K = token): Kr^T
-//   AQ  rows 64-127 of a [128][64] bf16 K-major tile, R=128: A_qk (row 64+i,
-//       K = j); rows 0-63 are never written (their product lands in
-//       accumulator rows that are dead by then), so AW | AK | AQ is one
-//       contiguous 64 KB block that K3 moves with a single bulk copy
+//   AQ  [64][64]   bf16, K-major, R=64: A_qk (row i, K = j).  K3 multiplies it
+//       as rows 64-127 of an M=128 tile whose descriptor starts 1 KB early, so
+//       the product lands in the accumulator lanes of the Qp S0 rows; rows
+//       0-63 of that tile are whatever precedes it in shared memory and feed
+//       accumulator lanes that are dead by then
 //   UT  fp32, element (i, e) at ((e/4)*64 + i)*4 + e%4   (U~)
 //   GL  [128] fp32: Gamma_L
 struct Rec {
   static constexpr uint32_t AW = 0;
   static constexpr uint32_t AK = AW + 128 * 128 * 2;
   static constexpr uint32_t AQ = AK + 128 * 64 * 2;
-  static constexpr uint32_t UT = AQ + 128 * 64 * 2;
+  static constexpr uint32_t UT = AQ + 64 * 64 * 2;
   static constexpr uint32_t GL = UT + 64 * 128 * 4;
   static constexpr uint32_t BYTES = GL + 128 * 4;
   static constexpr uint32_t kAkSbo = 8 * 128;  // AK: 8 K-groups (64 tokens) per MN-group

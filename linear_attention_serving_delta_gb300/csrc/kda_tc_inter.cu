@@ -4,16 +4,24 @@
 // One CTA per (sequence, head, 32-column slice of S), walking the sequence's
 // chunks in order.  The state slice lives in TMEM as an fp32 accumulator
 // (lane = key channel); a bf16 copy of it in shared memory is the MMA
-// operand.  Per chunk:
-//   MMA 1 (M=128, N=32, K=128): [W S0 ; Qp S0]                 -> TMEM D1[b]
-//   meanwhile: S <- Diag(Gamma_L) S with tcgen05.ld / st, and the output
-//              rows of the previous chunk are read from D1[1-b]
-//   threads: U = U~ - W S0 as a bf16 hi + lo pair
-//   MMA 2/3 (M=128, N=32, K=64): S += Kr^T U,  D1[b][64..127] += A_qk U
-//   threads: new bf16 state operand; snapshot
-// The state and U operands are stored MN-major, so each thread writes its
-// row as 16-byte chunks.  Records are prefetched two chunks ahead with bulk
-// copies (TMA engine).  The math is stated in kda_tc_common.cuh.
+// operand.  Step j of the walk:
+//   thread 0:  MMA 1 (M=128, N=32, K=128): [W S0 ; Qp S0] of chunk j -> D1[j % 3]
+//   all:       S <- Diag(Gamma_L) S (tcgen05.ld / st) while MMA 1 runs;
+//              warps 2-3 store the output rows of chunk j-2 and issue the
+//              copies of chunks j+1 (A_qk) and j+2 (chain operands)
+//   warps 0-1: U = U~ - W S0 as a bf16 hi + lo pair, while thread 64 issues
+//              MMA 3 of chunk j-1 (M=128, N=32, K=64):
+//              D1[(j-1) % 3][64..127] += A_qk U
+//   thread 0:  MMA 2 (M=128, N=32, K=64): S += Kr^T U
+//   all:       new bf16 state operand; snapshot
+// Only MMA 1, U, MMA 2 and the state write-back are on the chunk-to-chunk
+// dependency chain.  Everything else -- the output product and its store, the
+// copies -- runs in the shadow of the chain on warps that would otherwise
+// wait, with the tensor pipe taking MMA 3 while U is formed.  Three output
+// accumulators, three slots of chain operands, three A_qk tiles and two U
+// operands are in flight for that.  The state and U operands are stored
+// MN-major, so each thread writes its row as 16-byte chunks.  The math is
+// stated in kda_tc_common.cuh.
 #include "kda_tc_common.cuh"
 
 namespace kda {
@@ -26,36 +34,52 @@ constexpr int kThreads = 128;
 constexpr int kNs = 32;                 // state columns per CTA
 constexpr uint32_t kSopSbo = 16 * 128;  // S operand: 16 K-groups (key channels) per MN-group
 constexpr uint32_t kUopSbo = 8 * 128;   // U operand: 8 K-groups (tokens) per MN-group
+constexpr int kMmaThread = 0, kOutThread = 64, kLoadThread = 96;
 
 struct K3Smem {
-  // one ring slot: AW (32 KB) | AK (16 KB) | AQ128 (16 KB, rows 64-127 used) | UT slice | GL
+  // ring of chain operands: AW (32 KB) | AK (16 KB) | UT slice | GL
   static constexpr uint32_t AW = 0;
   static constexpr uint32_t AK = AW + 128 * 128 * 2;
-  static constexpr uint32_t AQ = AK + 128 * 64 * 2;
-  static constexpr uint32_t UT = AQ + 128 * 64 * 2;
+  static constexpr uint32_t UT = AK + 128 * 64 * 2;
   static constexpr uint32_t GL = UT + 64 * kNs * 4;
   static constexpr uint32_t SLOT = GL + 128 * 4;
-  static constexpr uint32_t SOP = 2 * SLOT;              // S operand, MN-major (n, c)
-  static constexpr uint32_t UHI = SOP + kNs * 128 * 2;    // U operand, MN-major (n, i)
-  static constexpr uint32_t ULO = UHI + kNs * 64 * 2;
-  static constexpr uint32_t BYTES = ULO + kNs * 64 * 2;
-  static constexpr uint32_t TILES = UT;  // AW | AK | AQ, contiguous in the record too
+  static constexpr int kSlots = 3;
+  static constexpr uint32_t SOP = kSlots * SLOT;  // S operand, MN-major (n, c)
+  // ring of A_qk tiles; each is read as rows 64-127 of an M=128 tile that
+  // starts 1 KB before it, inside the S operand or the tile before
+  static constexpr int kAqSlots = 3;
+  static constexpr uint32_t AQ_BYTES = 64 * 64 * 2;
+  static constexpr uint32_t AQ0 = SOP + kNs * 128 * 2;
+  // two U operands, each hi | lo, MN-major (n, i)
+  static constexpr uint32_t U_HALF = kNs * 64 * 2;
+  static constexpr uint32_t U0 = AQ0 + kAqSlots * AQ_BYTES;
+  static constexpr uint32_t BYTES = U0 + 2 * 2 * U_HALF;
+  static constexpr uint32_t TILES = UT;  // AW | AK, contiguous in the record too
   static constexpr uint32_t TX = TILES + 64 * kNs * 4 + 128 * 4;
 };
-static_assert(K3Smem::AK - K3Smem::AW == Rec::AK - Rec::AW &&
-                  K3Smem::AQ - K3Smem::AW == Rec::AQ - Rec::AW &&
-                  K3Smem::UT - K3Smem::AW == Rec::UT - Rec::AW,
-              "the operand tiles keep the record's relative layout");
+static_assert(K3Smem::AK - K3Smem::AW == Rec::AK - Rec::AW, "AW | AK keep the record's layout");
+static_assert(K3Smem::SLOT % 16 == 0 && K3Smem::AQ0 % 16 == 0 && K3Smem::U0 % 16 == 0,
+              "bulk-copy destinations and operand tiles are 16-byte aligned");
+static_assert(K3Smem::AQ0 >= 1024, "the A_qk tile descriptor starts 1 KB early inside shared memory");
+static_assert(K3Smem::BYTES <= 226 * 1024, "fits one CTA per SM");
 
-// Three bulk copies per chunk: the operand tiles (64 KB), this CTA's slice of
-// U~ and Gamma_L.
-__device__ __forceinline__ void k3_issue_loads(const ChunkParams& p, uint8_t* slot, uint64_t* bar,
-                                               int64_t cidx, int h, int n0) {
+// The chain operands of chunk cidx: three bulk copies (AW | AK, this CTA's
+// slice of U~, Gamma_L) on one barrier.
+__device__ __forceinline__ void k3_load_chain(const ChunkParams& p, uint8_t* slot, uint64_t* bar,
+                                              int64_t cidx, int h, int n0) {
   const uint8_t* rec = reinterpret_cast<const uint8_t*>(p.inter) + ((size_t)cidx * p.H + h) * Rec::BYTES;
   mbar_arrive_expect_tx(bar, K3Smem::TX);
   bulk_g2s(slot + K3Smem::AW, rec + Rec::AW, K3Smem::TILES, bar);
   bulk_g2s(slot + K3Smem::UT, rec + Rec::UT + (n0 / 4) * 64 * 16, 64 * kNs * 4, bar);
   bulk_g2s(slot + K3Smem::GL, rec + Rec::GL, 128 * 4, bar);
+}
+
+// The A_qk tile of chunk cidx.
+__device__ __forceinline__ void k3_load_aq(const ChunkParams& p, uint8_t* dst, uint64_t* bar,
+                                           int64_t cidx, int h) {
+  const uint8_t* rec = reinterpret_cast<const uint8_t*>(p.inter) + ((size_t)cidx * p.H + h) * Rec::BYTES;
+  mbar_arrive_expect_tx(bar, K3Smem::AQ_BYTES);
+  bulk_g2s(dst, rec + Rec::AQ, K3Smem::AQ_BYTES, bar);
 }
 
 // 32 consecutive fp32 values of one TMEM lane (two 16-column loads)
@@ -95,10 +119,12 @@ __device__ __forceinline__ void store_output(const ChunkParams& p, const Chunk& 
 __global__ void __launch_bounds__(kThreads, 1)
 tc_inter(ChunkParams p) {
   extern __shared__ __align__(1024) uint8_t sm[];
-  __shared__ __align__(8) uint64_t bar_full[2];
-  __shared__ __align__(8) uint64_t bar_mma;   // MMA 1 (one issuing thread)
-  __shared__ __align__(8) uint64_t bar_mma2;  // MMA 2 (state chain)
-  __shared__ __align__(8) uint64_t bar_mma3;  // MMA 3 (output path)
+  __shared__ __align__(8) uint64_t bar_full[K3Smem::kSlots];
+  __shared__ __align__(8) uint64_t bar_aq[K3Smem::kAqSlots];
+  __shared__ __align__(8) uint64_t bar_mma1;   // MMA 1
+  __shared__ __align__(8) uint64_t bar_mma2;   // MMA 2 (state chain)
+  __shared__ __align__(8) uint64_t bar_mma3;   // MMA 3 (output path)
+  __shared__ __align__(8) uint64_t bar_drain;  // every MMA, on the error path
   __shared__ uint32_t tmem_base;
 
   const int s = blockIdx.x, h = blockIdx.y, n0 = blockIdx.z * kNs;
@@ -108,16 +134,15 @@ tc_inter(ChunkParams p) {
   const int64_t nchunks = c_end - c_begin;
 
   uint8_t* SOP = sm + K3Smem::SOP;
-  uint8_t* UHI = sm + K3Smem::UHI;
-  uint8_t* ULO = sm + K3Smem::ULO;
 
   if (warp == 0) tmem_alloc(&tmem_base, 128);
   if (tid == 0) {
-    mbar_init(&bar_full[0], 1);
-    mbar_init(&bar_full[1], 1);
-    mbar_init(&bar_mma, 1);
+    for (int i = 0; i < K3Smem::kSlots; ++i) mbar_init(&bar_full[i], 1);
+    for (int i = 0; i < K3Smem::kAqSlots; ++i) mbar_init(&bar_aq[i], 1);
+    mbar_init(&bar_mma1, 1);
     mbar_init(&bar_mma2, 1);
     mbar_init(&bar_mma3, 1);
+    mbar_init(&bar_drain, 2);  // the two MMA-issuing threads
     mbar_init_fence();
   }
   fence_async_smem();
@@ -125,14 +150,26 @@ tc_inter(ChunkParams p) {
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const uint32_t D1[2] = {tmem, tmem + kNs};  // [W;Qp] S0, then + A_qk U in lanes 64-127
-  const uint32_t DS = tmem + 2 * kNs;         // the state slice, lane = key channel
+  const uint32_t DS = tmem + 3 * kNs;  // the state slice, lane = key channel
   const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+  // output accumulator of chunk j: [W;Qp] S0, then + A_qk U in lanes 64-127
+  auto d1_of = [&](int64_t j) { return tmem + (uint32_t)(j % 3) * kNs; };
+  auto slot_of = [&](int64_t j) { return sm + (uint32_t)(j % K3Smem::kSlots) * K3Smem::SLOT; };
+  auto aq_of = [&](int64_t j) {
+    return sm + K3Smem::AQ0 + (uint32_t)(j % K3Smem::kAqSlots) * K3Smem::AQ_BYTES;
+  };
+  auto u_of = [&](int64_t j) { return sm + K3Smem::U0 + (uint32_t)(j & 1) * 2 * K3Smem::U_HALF; };
 
-  if (tid == 0) {
-    for (int64_t it = 0; it < 2 && it < nchunks; ++it)
-      k3_issue_loads(p, sm + it * K3Smem::SLOT, &bar_full[it], c_begin + it, h, n0);
-  }
+  // Thread 96 issues the chain-operand copies and thread 64 the A_qk copies;
+  // each counts what it issued and what was waited for, so the error path
+  // can let copies in flight land.
+  int64_t chain_issued = 0, chain_waited = 0, aq_issued = 0, aq_waited = 0;
+  if (tid == kLoadThread)
+    for (; chain_issued < K3Smem::kSlots && chain_issued < nchunks; ++chain_issued)
+      k3_load_chain(p, slot_of(chain_issued), &bar_full[chain_issued], c_begin + chain_issued, h, n0);
+  if (tid == kOutThread)
+    for (; aq_issued < K3Smem::kAqSlots && aq_issued < nchunks; ++aq_issued)
+      k3_load_aq(p, aq_of(aq_issued), &bar_aq[aq_issued], c_begin + aq_issued, h);
 
   // initial state slice: TMEM (fp32) and the bf16 operand copy
   const int c = tid;  // key channel == TMEM lane
@@ -154,27 +191,50 @@ tc_inter(ChunkParams p) {
 
   const uint32_t id = idesc_bf16(128, kNs, 0, 1);     // B operands MN-major
   const uint32_t id_ak = idesc_bf16(128, kNs, 1, 1);  // Kr^T is MN-major too
-  uint32_t mma_phase = 0, mma2_phase = 0, mma3_phase = 0;
-  bool ok = true, ok3 = true;
-  Chunk prev{};
+  // MMA 3 of chunk j, thread 64: wait for its A_qk tile, then
+  // D1[j % 3] += A_qk U (U as hi + lo).  False if the tile never came.
+  auto mma3 = [&](int64_t j) -> bool {
+    if (!mbar_wait(&bar_aq[j % K3Smem::kAqSlots], (uint32_t)((j / K3Smem::kAqSlots) & 1), kWaitLimitNs))
+      return false;
+    aq_waited = j + 1;
+    const uint32_t a = smem_u32(aq_of(j)) - 1024, ub = smem_u32(u_of(j));
+#pragma unroll
+    for (int part = 0; part < 2; ++part)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_bf16(d1_of(j), sdesc(a + k * 2 * 1024, 1024, 128),
+                 sdesc(ub + part * K3Smem::U_HALF + k * 256, 128, kUopSbo), id, 1);
+    mma_commit(&bar_mma3);
+    return true;
+  };
+
+  // MMA 3 of chunk j is the j-th phase of bar_mma3.  Warps 2-3 wait for it
+  // before MMA 3 of chunk j+1 is issued (a step later, or behind a barrier at
+  // the end), so a parity wait never sees two phases complete.
+  uint32_t ph1 = 0, ph2 = 0;
+  bool ok = true;
+  bool oko = true;  // warps 2-3: MMA 3 issued and finished in time
+  Chunk prev1{}, prev2{};
   Chunk next = nchunks > 0 ? p.chunks[c_begin] : Chunk{};
-  for (int64_t it = 0; it < nchunks && ok; ++it) {
-    const int slot_i = (int)(it & 1), b = (int)(it & 1);
-    uint8_t* slot = sm + slot_i * K3Smem::SLOT;
+  for (int64_t it = 0; it < nchunks; ++it) {
+    uint8_t* slot = slot_of(it);
+    uint8_t* uop = u_of(it);
     const Chunk ch = next;  // chunk entries are read one step ahead
     if (it + 1 < nchunks) next = p.chunks[c_begin + it + 1];
-    // S operand (previous iteration) and this slot are ready
+    // S operand (previous step) and this slot are ready
     fence_async_smem();
     fence_before_sync();
-    ok = __syncthreads_and(ok3 && mbar_wait(&bar_full[slot_i], (uint32_t)((it >> 1) & 1), kWaitLimitNs));
+    ok = __syncthreads_and(oko && mbar_wait(&bar_full[it % K3Smem::kSlots],
+                                            (uint32_t)((it / K3Smem::kSlots) & 1), kWaitLimitNs));
     fence_after_sync();
     if (!ok) break;
-    if (tid == 0) {
+    chain_waited = it + 1;
+    if (tid == kMmaThread) {
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        mma_bf16(D1[b], sdesc(smem_u32(slot + K3Smem::AW) + k * 2 * 128 * 16, 128 * 16, 128),
+        mma_bf16(d1_of(it), sdesc(smem_u32(slot + K3Smem::AW) + k * 2 * 128 * 16, 128 * 16, 128),
                  sdesc(smem_u32(SOP) + k * 256, 128, kSopSbo), id, k > 0);
-      mma_commit(&bar_mma);
+      mma_commit(&bar_mma1);
     }
     // while MMA 1 runs: retention of the carried state, S <- Diag(Gamma_L) S ...
     {
@@ -187,18 +247,34 @@ tc_inter(ChunkParams p) {
       tmem_st16(DS + lane_off + 16, v + 16);
       tmem_st_wait();
     }
-    // ... and the outputs of the previous chunk
-    if (it > 0 && warp >= 2) store_output(p, prev, D1[b ^ 1], lane_off, tid - 64, h, n0);
+    if (warp >= 2) {
+      // ... the outputs of chunk it-2, whose MMA 3 was issued last step ...
+      if (it >= 2) {
+        oko = oko && mbar_wait(&bar_mma3, (uint32_t)((it - 2) & 1), kWaitLimitNs);
+        fence_after_sync();
+        if (oko) store_output(p, prev2, d1_of(it - 2), lane_off, tid - 64, h, n0);
+        // ... its A_qk tile takes chunk it+1 ...
+        if (tid == kOutThread && oko && it + 1 < nchunks && aq_issued == it + 1) {
+          k3_load_aq(p, aq_of(it + 1), &bar_aq[(it + 1) % K3Smem::kAqSlots], c_begin + it + 1, h);
+          aq_issued = it + 2;
+        }
+      }
+      // ... and the slot of chunk it-1 (MMA 2 done) takes chunk it+2
+      if (tid == kLoadThread && it >= 1 && it + 2 < nchunks) {
+        k3_load_chain(p, slot_of(it + 2), &bar_full[(it + 2) % K3Smem::kSlots], c_begin + it + 2, h, n0);
+        chain_issued = it + 3;
+      }
+    }
     fence_before_sync();
-    ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, kWaitLimitNs));
-    mma_phase ^= 1;
+    ok = __syncthreads_and(mbar_wait(&bar_mma1, ph1, kWaitLimitNs));
+    ph1 ^= 1;
     fence_after_sync();
     if (!ok) break;
     if (warp < 2) {
       // U = U~ - W S0 for token i = lane row, split into bf16 hi + lo
       const int i = tid;
       float d[kNs];
-      tmem_ld32(D1[b] + lane_off, d);
+      tmem_ld32(d1_of(it) + lane_off, d);
       const float* ut = reinterpret_cast<const float*>(slot + K3Smem::UT);
 #pragma unroll
       for (int m = 0; m < kNs / 8; ++m) {
@@ -213,41 +289,31 @@ tc_inter(ChunkParams p) {
           hi[t] = pack_bf16(u[2 * t], u[2 * t + 1]);
           lo[t] = pack_bf16(u[2 * t] - bf16_lo(hi[t]), u[2 * t + 1] - bf16_hi(hi[t]));
         }
-        *reinterpret_cast<uint4*>(UHI + mnmajor_off(8 * m, i, kUopSbo)) =
+        *reinterpret_cast<uint4*>(uop + mnmajor_off(8 * m, i, kUopSbo)) =
             make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(ULO + mnmajor_off(8 * m, i, kUopSbo)) =
+        *reinterpret_cast<uint4*>(uop + K3Smem::U_HALF + mnmajor_off(8 * m, i, kUopSbo)) =
             make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
+    } else if (tid == kOutThread && it >= 1 && oko) {
+      oko = mma3(it - 1);  // the output product of the previous chunk, in U's shadow
     }
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    // MMA 2, the state chain: S += Kr^T U; then MMA 3, the output path:
-    // D1[b][64..127] += A_qk U (U as hi + lo).  Separate commits, so the
-    // state write-back below waits for MMA 2 only and overlaps MMA 3.
-    if (tid == 0) {
+    // MMA 2, the state chain: S += Kr^T U (U as hi + lo)
+    if (tid == kMmaThread) {
+      const uint32_t ub = smem_u32(uop);
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const uint32_t ub = smem_u32(part ? ULO : UHI);
+      for (int part = 0; part < 2; ++part)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_bf16(DS, sdesc(smem_u32(slot + K3Smem::AK) + k * 256, 128, Rec::kAkSbo),
-                   sdesc(ub + k * 256, 128, kUopSbo), id_ak, 1);
-      }
+                   sdesc(ub + part * K3Smem::U_HALF + k * 256, 128, kUopSbo), id_ak, 1);
       mma_commit(&bar_mma2);
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const uint32_t ub = smem_u32(part ? ULO : UHI);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(D1[b], sdesc(smem_u32(slot + K3Smem::AQ) + k * 2 * 128 * 16, 128 * 16, 128),
-                   sdesc(ub + k * 256, 128, kUopSbo), id, 1);
-      }
-      mma_commit(&bar_mma3);
     }
-    ok = __syncthreads_and(mbar_wait(&bar_mma2, mma2_phase, kWaitLimitNs));
-    mma2_phase ^= 1;
+    ok = __syncthreads_and(mbar_wait(&bar_mma2, ph2, kWaitLimitNs));
+    ph2 ^= 1;
     fence_after_sync();
     if (!ok) break;
     // new state: bf16 operand copy, snapshot if this chunk ends at one
@@ -262,24 +328,30 @@ tc_inter(ChunkParams p) {
           *reinterpret_cast<float4*>(dst + n) = make_float4(v[n], v[n + 1], v[n + 2], v[n + 3]);
       }
     }
-    // warps 2-3 read the outputs of this chunk next step: after their state
-    // rows are written back they wait for MMA 3, after which the slot is free
-    // and a thread of warp 2 refills it with chunk it + 2
-    if (warp >= 2) {
-      ok3 = ok3 && mbar_wait(&bar_mma3, mma3_phase, kWaitLimitNs);
-      fence_after_sync();
-      if (tid == 64 && ok3 && it + 2 < nchunks)
-        k3_issue_loads(p, slot, &bar_full[slot_i], c_begin + it + 2, h, n0);
-    }
-    mma3_phase ^= 1;
-    prev = ch;
+    prev2 = prev1;
+    prev1 = ch;
   }
-  ok = __syncthreads_and(ok && ok3);
+  // the output products still open: chunk n-2 (issued) and chunk n-1 (not yet)
+  if (ok && warp >= 2 && nchunks >= 2) {
+    oko = oko && mbar_wait(&bar_mma3, (uint32_t)((nchunks - 2) & 1), kWaitLimitNs);
+    fence_after_sync();
+    if (oko) store_output(p, prev2, d1_of(nchunks - 2), lane_off, tid - 64, h, n0);
+  }
+  fence_before_sync();
+  ok = __syncthreads_and(ok && oko);
   fence_after_sync();
-  if (ok && nchunks > 0 && warp >= 2)
-    store_output(p, prev, D1[(nchunks - 1) & 1], lane_off, tid - 64, h, n0);
-  if (!ok && tid == 0) flag(p.status, kFlagTimeout);
-  if (p.final_state && ok) {
+  if (ok && nchunks >= 1) {
+    if (tid == kOutThread) oko = mma3(nchunks - 1);
+    if (warp >= 2) {
+      oko = oko && mbar_wait(&bar_mma3, (uint32_t)((nchunks - 1) & 1), kWaitLimitNs);
+      fence_after_sync();
+      if (oko) store_output(p, prev1, d1_of(nchunks - 1), lane_off, tid - 64, h, n0);
+    }
+  }
+  fence_before_sync();
+  ok = __syncthreads_and(ok && oko);
+  fence_after_sync();
+  if (ok && p.final_state) {
     float v[kNs];
     tmem_ld32(DS + lane_off, v);
     float* dst = p.final_state + sbase + (size_t)c * kD + n0;
@@ -287,8 +359,22 @@ tc_inter(ChunkParams p) {
     for (int n = 0; n < kNs; n += 4)
       *reinterpret_cast<float4*>(dst + n) = make_float4(v[n], v[n + 1], v[n + 2], v[n + 3]);
   }
+  if (!ok) {
+    // let the copies and MMAs still in flight finish (each wait bounded)
+    // before the shared memory and TMEM are given back
+    if (tid == 0) flag(p.status, kFlagTimeout);
+    if (tid == kLoadThread)
+      for (int64_t j = chain_waited; j < chain_issued; ++j)
+        mbar_wait(&bar_full[j % K3Smem::kSlots], (uint32_t)((j / K3Smem::kSlots) & 1), kWaitLimitNs);
+    if (tid == kOutThread)
+      for (int64_t j = aq_waited; j < aq_issued; ++j)
+        mbar_wait(&bar_aq[j % K3Smem::kAqSlots], (uint32_t)((j / K3Smem::kAqSlots) & 1), kWaitLimitNs);
+    if (tid == kMmaThread || tid == kOutThread) mma_commit(&bar_drain);
+    if (tid == kMmaThread) mbar_wait(&bar_drain, 0, kWaitLimitNs);
+  }
   fence_before_sync();
   __syncthreads();
+  fence_after_sync();
   if (warp == 0) tmem_dealloc(tmem, 128);
 }
 

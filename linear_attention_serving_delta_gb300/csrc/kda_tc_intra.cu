@@ -398,7 +398,7 @@ tc_intra(ChunkParams p, int64_t n_items) {
           float a[8];
 #pragma unroll
           for (int t = 0; t < 8; ++t) a[t] = (live && 8 * jb + t <= i) ? d[8 * t8 + t] : 0.f;
-          *reinterpret_cast<uint4*>(rec + Rec::AQ + kmajor_off(64 + i, 8 * jb, 128)) =
+          *reinterpret_cast<uint4*>(rec + Rec::AQ + kmajor_off(i, 8 * jb, 64)) =
               make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]),
                          pack_bf16(a[6], a[7]));
         }

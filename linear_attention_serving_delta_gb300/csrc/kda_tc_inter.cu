@@ -4,15 +4,22 @@
 // One CTA per (sequence, head, 32-column slice of S), walking the sequence's
 // chunks in order.  The state slice lives in TMEM as an fp32 accumulator
 // (lane = key channel); a bf16 copy of it in shared memory is the MMA
-// operand.  Step j of the walk:
-//   thread 0:  MMA 1 (M=128, N=32, K=128): [W S0 ; Qp S0] of chunk j -> D1[j % 3]
-//   all:       S <- Diag(Gamma_L) S (tcgen05.ld / st) while MMA 1 runs;
+// operand.  Every MMA runs at N=64: the bf16 operand of a 32-column fp32
+// block is its hi half next to its lo half (x = hi + lo to about 2^-16), so
+// one instruction multiplies both.  A tcgen05.mma costs about the same for
+// any N <= 64, so this doubles the precision of the state and U operands for
+// free and halves the instruction count of MMA 2 and MMA 3.  The state is
+// kept as two fp32 accumulators S = Sa + Sb (Sa takes the hi products, Sb
+// the lo products).  Step j of the walk:
+//   thread 0:  MMA 1 (M=128, N=64, K=128): [W ; Qp] [S0hi | S0lo] of chunk j
+//              -> D1[j % 3]
+//   all:       Sa <- Diag(Gamma_L) (Sa + Sb), Sb <- 0 while MMA 1 runs;
 //              warps 2-3 store the output rows of chunk j-2 and issue the
 //              copies of chunks j+1 (A_qk) and j+2 (chain operands)
 //   warps 0-1: U = U~ - W S0 as a bf16 hi + lo pair, while thread 64 issues
-//              MMA 3 of chunk j-1 (M=128, N=32, K=64):
-//              D1[(j-1) % 3][64..127] += A_qk U
-//   thread 0:  MMA 2 (M=128, N=32, K=64): S += Kr^T U
+//              MMA 3 of chunk j-1 (M=128, N=64, K=64):
+//              D1[(j-1) % 3][64..127] += A_qk [Uhi | Ulo]
+//   thread 0:  MMA 2 (M=128, N=64, K=64): [Sa | Sb] += Kr^T [Uhi | Ulo]
 //   all:       new bf16 state operand; snapshot
 // Only MMA 1, U, MMA 2 and the state write-back are on the chunk-to-chunk
 // dependency chain.  Everything else -- the output product and its store, the
@@ -20,7 +27,8 @@
 // wait, with the tensor pipe taking MMA 3 while U is formed.  Three output
 // accumulators, three slots of chain operands, three A_qk tiles and two U
 // operands are in flight for that.  The state and U operands are stored
-// MN-major, so each thread writes its row as 16-byte chunks.  The math is
+// MN-major, so each thread writes its row as 16-byte chunks.  TMEM holds
+// 3 x 64 columns of output accumulators and 64 of state.  The math is
 // stated in kda_tc_common.cuh.
 #include "kda_tc_common.cuh"
 
@@ -32,8 +40,10 @@ using namespace tc;
 
 constexpr int kThreads = 128;
 constexpr int kNs = 32;                 // state columns per CTA
+constexpr int kNop = 2 * kNs;           // MMA N: hi and lo halves side by side
 constexpr uint32_t kSopSbo = 16 * 128;  // S operand: 16 K-groups (key channels) per MN-group
 constexpr uint32_t kUopSbo = 8 * 128;   // U operand: 8 K-groups (tokens) per MN-group
+constexpr uint32_t kTmemCols = 4 * kNop;
 constexpr int kMmaThread = 0, kOutThread = 64, kLoadThread = 96;
 
 struct K3Smem {
@@ -44,16 +54,16 @@ struct K3Smem {
   static constexpr uint32_t GL = UT + 64 * kNs * 4;
   static constexpr uint32_t SLOT = GL + 128 * 4;
   static constexpr int kSlots = 3;
-  static constexpr uint32_t SOP = kSlots * SLOT;  // S operand, MN-major (n, c)
+  static constexpr uint32_t SOP = kSlots * SLOT;  // S operand [hi | lo], MN-major (n, c)
   // ring of A_qk tiles; each is read as rows 64-127 of an M=128 tile that
   // starts 1 KB before it, inside the S operand or the tile before
   static constexpr int kAqSlots = 3;
   static constexpr uint32_t AQ_BYTES = 64 * 64 * 2;
-  static constexpr uint32_t AQ0 = SOP + kNs * 128 * 2;
-  // two U operands, each hi | lo, MN-major (n, i)
-  static constexpr uint32_t U_HALF = kNs * 64 * 2;
+  static constexpr uint32_t AQ0 = SOP + kNop * 128 * 2;
+  // two U operands [hi | lo], MN-major (n, i)
+  static constexpr uint32_t U_BYTES = kNop * 64 * 2;
   static constexpr uint32_t U0 = AQ0 + kAqSlots * AQ_BYTES;
-  static constexpr uint32_t BYTES = U0 + 2 * 2 * U_HALF;
+  static constexpr uint32_t BYTES = U0 + 2 * U_BYTES;
   static constexpr uint32_t TILES = UT;  // AW | AK, contiguous in the record too
   static constexpr uint32_t TX = TILES + 64 * kNs * 4 + 128 * 4;
 };
@@ -82,27 +92,47 @@ __device__ __forceinline__ void k3_load_aq(const ChunkParams& p, uint8_t* dst, u
   bulk_g2s(dst, rec + Rec::AQ, K3Smem::AQ_BYTES, bar);
 }
 
-// 32 consecutive fp32 values of one TMEM lane (two 16-column loads)
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+// 64 consecutive fp32 values of one TMEM lane, summed in pairs: v[n] =
+// column n + column 32 + n (the two halves of a hi | lo accumulator)
+__device__ __forceinline__ void tmem_ld_sum(uint32_t taddr, float* v) {
+  float b[kNs];
   tmem_ld16(taddr, v);
   tmem_ld16(taddr + 16, v + 16);
+  tmem_ld16(taddr + 32, b);
+  tmem_ld16(taddr + 48, b + 16);
   tmem_ld_wait();
+#pragma unroll
+  for (int n = 0; n < kNs; ++n) v[n] += b[n];
 }
 
-// the S operand row of key channel c: 4 chunks of 8 bf16 (MN-major)
+// bf16 hi and lo parts of 8 fp32 values, packed
+__device__ __forceinline__ void split8(const float* u, uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    h[t] = pack_bf16(u[2 * t], u[2 * t + 1]);
+    l[t] = pack_bf16(u[2 * t] - bf16_lo(h[t]), u[2 * t + 1] - bf16_hi(h[t]));
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// the S operand row of key channel c: [hi | lo], 8 chunks of 8 bf16 (MN-major)
 __device__ __forceinline__ void store_state_operand(uint8_t* sop, int c, const float* v) {
 #pragma unroll
-  for (int m = 0; m < kNs / 8; ++m)
-    *reinterpret_cast<uint4*>(sop + mnmajor_off(8 * m, c, kSopSbo)) =
-        make_uint4(pack_bf16(v[8 * m], v[8 * m + 1]), pack_bf16(v[8 * m + 2], v[8 * m + 3]),
-                   pack_bf16(v[8 * m + 4], v[8 * m + 5]), pack_bf16(v[8 * m + 6], v[8 * m + 7]));
+  for (int m = 0; m < kNs / 8; ++m) {
+    uint4 hi, lo;
+    split8(v + 8 * m, hi, lo);
+    *reinterpret_cast<uint4*>(sop + mnmajor_off(8 * m, c, kSopSbo)) = hi;
+    *reinterpret_cast<uint4*>(sop + mnmajor_off(kNs + 8 * m, c, kSopSbo)) = lo;
+  }
 }
 
 // o rows of one chunk from lanes 64-127 of an output accumulator (warps 2, 3)
 __device__ __forceinline__ void store_output(const ChunkParams& p, const Chunk& ch, uint32_t d1,
                                              uint32_t lane_off, int i, int h, int n0) {
   float d[kNs];
-  tmem_ld32(d1 + lane_off, d);
+  tmem_ld_sum(d1 + lane_off, d);
   if (i < ch.len) {
     const float scale = p.scale;
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o);
@@ -135,7 +165,7 @@ tc_inter(ChunkParams p) {
 
   uint8_t* SOP = sm + K3Smem::SOP;
 
-  if (warp == 0) tmem_alloc(&tmem_base, 128);
+  if (warp == 0) tmem_alloc(&tmem_base, kTmemCols);
   if (tid == 0) {
     for (int i = 0; i < K3Smem::kSlots; ++i) mbar_init(&bar_full[i], 1);
     for (int i = 0; i < K3Smem::kAqSlots; ++i) mbar_init(&bar_aq[i], 1);
@@ -150,15 +180,15 @@ tc_inter(ChunkParams p) {
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const uint32_t DS = tmem + 3 * kNs;  // the state slice, lane = key channel
+  const uint32_t DS = tmem + 3 * kNop;  // the state slice [Sa | Sb], lane = key channel
   const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
   // output accumulator of chunk j: [W;Qp] S0, then + A_qk U in lanes 64-127
-  auto d1_of = [&](int64_t j) { return tmem + (uint32_t)(j % 3) * kNs; };
+  auto d1_of = [&](int64_t j) { return tmem + (uint32_t)(j % 3) * kNop; };
   auto slot_of = [&](int64_t j) { return sm + (uint32_t)(j % K3Smem::kSlots) * K3Smem::SLOT; };
   auto aq_of = [&](int64_t j) {
     return sm + K3Smem::AQ0 + (uint32_t)(j % K3Smem::kAqSlots) * K3Smem::AQ_BYTES;
   };
-  auto u_of = [&](int64_t j) { return sm + K3Smem::U0 + (uint32_t)(j & 1) * 2 * K3Smem::U_HALF; };
+  auto u_of = [&](int64_t j) { return sm + K3Smem::U0 + (uint32_t)(j & 1) * K3Smem::U_BYTES; };
 
   // Thread 96 issues the chain-operand copies and thread 64 the A_qk copies;
   // each counts what it issued and what was waited for, so the error path
@@ -183,27 +213,29 @@ tc_inter(ChunkParams p) {
                      : make_float4(0.f, 0.f, 0.f, 0.f);
       v[n] = x.x; v[n + 1] = x.y; v[n + 2] = x.z; v[n + 3] = x.w;
     }
+    float z[16];
+#pragma unroll
+    for (int n = 0; n < 16; ++n) z[n] = 0.f;
     tmem_st16(DS + lane_off, v);
     tmem_st16(DS + lane_off + 16, v + 16);
+    tmem_st16(DS + lane_off + 32, z);
+    tmem_st16(DS + lane_off + 48, z);
     tmem_st_wait();
     store_state_operand(SOP, c, v);
   }
 
-  const uint32_t id = idesc_bf16(128, kNs, 0, 1);     // B operands MN-major
-  const uint32_t id_ak = idesc_bf16(128, kNs, 1, 1);  // Kr^T is MN-major too
+  const uint32_t id = idesc_bf16(128, kNop, 0, 1);     // B operands MN-major
+  const uint32_t id_ak = idesc_bf16(128, kNop, 1, 1);  // Kr^T is MN-major too
   // MMA 3 of chunk j, thread 64: wait for its A_qk tile, then
-  // D1[j % 3] += A_qk U (U as hi + lo).  False if the tile never came.
+  // D1[j % 3] += A_qk [Uhi | Ulo].  False if the tile never came.
   auto mma3 = [&](int64_t j) -> bool {
     if (!mbar_wait(&bar_aq[j % K3Smem::kAqSlots], (uint32_t)((j / K3Smem::kAqSlots) & 1), kWaitLimitNs))
       return false;
     aq_waited = j + 1;
     const uint32_t a = smem_u32(aq_of(j)) - 1024, ub = smem_u32(u_of(j));
 #pragma unroll
-    for (int part = 0; part < 2; ++part)
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_bf16(d1_of(j), sdesc(a + k * 2 * 1024, 1024, 128),
-                 sdesc(ub + part * K3Smem::U_HALF + k * 256, 128, kUopSbo), id, 1);
+    for (int k = 0; k < 4; ++k)
+      mma_bf16(d1_of(j), sdesc(a + k * 2 * 1024, 1024, 128), sdesc(ub + k * 256, 128, kUopSbo), id, 1);
     mma_commit(&bar_mma3);
     return true;
   };
@@ -236,15 +268,20 @@ tc_inter(ChunkParams p) {
                  sdesc(smem_u32(SOP) + k * 256, 128, kSopSbo), id, k > 0);
       mma_commit(&bar_mma1);
     }
-    // while MMA 1 runs: retention of the carried state, S <- Diag(Gamma_L) S ...
+    // while MMA 1 runs: retention of the carried state,
+    // Sa <- Diag(Gamma_L) (Sa + Sb), Sb <- 0 ...
     {
       const float gl = reinterpret_cast<const float*>(slot + K3Smem::GL)[c];
-      float v[kNs];
-      tmem_ld32(DS + lane_off, v);
+      float v[kNs], z[16];
+      tmem_ld_sum(DS + lane_off, v);
 #pragma unroll
       for (int n = 0; n < kNs; ++n) v[n] *= gl;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) z[n] = 0.f;
       tmem_st16(DS + lane_off, v);
       tmem_st16(DS + lane_off + 16, v + 16);
+      tmem_st16(DS + lane_off + 32, z);
+      tmem_st16(DS + lane_off + 48, z);
       tmem_st_wait();
     }
     if (warp >= 2) {
@@ -274,7 +311,7 @@ tc_inter(ChunkParams p) {
       // U = U~ - W S0 for token i = lane row, split into bf16 hi + lo
       const int i = tid;
       float d[kNs];
-      tmem_ld32(d1_of(it) + lane_off, d);
+      tmem_ld_sum(d1_of(it) + lane_off, d);
       const float* ut = reinterpret_cast<const float*>(slot + K3Smem::UT);
 #pragma unroll
       for (int m = 0; m < kNs / 8; ++m) {
@@ -283,16 +320,10 @@ tc_inter(ChunkParams p) {
         const float u[8] = {ua.x - d[8 * m], ua.y - d[8 * m + 1], ua.z - d[8 * m + 2],
                             ua.w - d[8 * m + 3], ub.x - d[8 * m + 4], ub.y - d[8 * m + 5],
                             ub.z - d[8 * m + 6], ub.w - d[8 * m + 7]};
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          hi[t] = pack_bf16(u[2 * t], u[2 * t + 1]);
-          lo[t] = pack_bf16(u[2 * t] - bf16_lo(hi[t]), u[2 * t + 1] - bf16_hi(hi[t]));
-        }
-        *reinterpret_cast<uint4*>(uop + mnmajor_off(8 * m, i, kUopSbo)) =
-            make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(uop + K3Smem::U_HALF + mnmajor_off(8 * m, i, kUopSbo)) =
-            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        uint4 hi, lo;
+        split8(u, hi, lo);
+        *reinterpret_cast<uint4*>(uop + mnmajor_off(8 * m, i, kUopSbo)) = hi;
+        *reinterpret_cast<uint4*>(uop + mnmajor_off(kNs + 8 * m, i, kUopSbo)) = lo;
       }
     } else if (tid == kOutThread && it >= 1 && oko) {
       oko = mma3(it - 1);  // the output product of the previous chunk, in U's shadow
@@ -301,15 +332,13 @@ tc_inter(ChunkParams p) {
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    // MMA 2, the state chain: S += Kr^T U (U as hi + lo)
+    // MMA 2, the state chain: [Sa | Sb] += Kr^T [Uhi | Ulo]
     if (tid == kMmaThread) {
       const uint32_t ub = smem_u32(uop);
 #pragma unroll
-      for (int part = 0; part < 2; ++part)
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(DS, sdesc(smem_u32(slot + K3Smem::AK) + k * 256, 128, Rec::kAkSbo),
-                   sdesc(ub + part * K3Smem::U_HALF + k * 256, 128, kUopSbo), id_ak, 1);
+      for (int k = 0; k < 4; ++k)
+        mma_bf16(DS, sdesc(smem_u32(slot + K3Smem::AK) + k * 256, 128, Rec::kAkSbo),
+                 sdesc(ub + k * 256, 128, kUopSbo), id_ak, 1);
       mma_commit(&bar_mma2);
     }
     ok = __syncthreads_and(mbar_wait(&bar_mma2, ph2, kWaitLimitNs));
@@ -319,7 +348,7 @@ tc_inter(ChunkParams p) {
     // new state: bf16 operand copy, snapshot if this chunk ends at one
     {
       float v[kNs];
-      tmem_ld32(DS + lane_off, v);
+      tmem_ld_sum(DS + lane_off, v);
       store_state_operand(SOP, c, v);
       if (ch.snap_slot >= 0 && p.snapshots) {
         float* dst = p.snapshots + ((size_t)ch.snap_slot * H + h) * kD * kD + (size_t)c * kD + n0;
@@ -353,7 +382,7 @@ tc_inter(ChunkParams p) {
   fence_after_sync();
   if (ok && p.final_state) {
     float v[kNs];
-    tmem_ld32(DS + lane_off, v);
+    tmem_ld_sum(DS + lane_off, v);
     float* dst = p.final_state + sbase + (size_t)c * kD + n0;
 #pragma unroll
     for (int n = 0; n < kNs; n += 4)
@@ -375,7 +404,7 @@ tc_inter(ChunkParams p) {
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 0) tmem_dealloc(tmem, 128);
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace

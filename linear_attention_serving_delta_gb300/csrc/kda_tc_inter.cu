@@ -1,35 +1,32 @@
 // kda_tc_inter.cu -- K3, the inter-chunk kernel of the tensor-core prefill,
 // and the launcher of the whole tensor-core prefill (K2 then K3).
 //
-// One CTA per (sequence, head, 32-column slice of S), walking the sequence's
-// chunks in order.  The state slice lives in TMEM as an fp32 accumulator
-// (lane = key channel); a bf16 copy of it in shared memory is the MMA
-// operand.  Every MMA runs at N=64: the bf16 operand of a 32-column fp32
-// block is its hi half next to its lo half (x = hi + lo to about 2^-16), so
-// one instruction multiplies both.  A tcgen05.mma costs about the same for
-// any N <= 64, so this doubles the precision of the state and U operands for
-// free and halves the instruction count of MMA 2 and MMA 3.  The state is
-// kept as two fp32 accumulators S = Sa + Sb (Sa takes the hi products, Sb
-// the lo products).  Step j of the walk:
-//   thread 0:  MMA 1 (M=128, N=64, K=128): [W ; Qp] [S0hi | S0lo] of chunk j
-//              -> D1[j % 3]
-//   all:       Sa <- Diag(Gamma_L) (Sa + Sb), Sb <- 0 while MMA 1 runs;
-//              warps 2-3 store the output rows of chunk j-2 and issue the
-//              copies of chunks j+1 (A_qk) and j+2 (chain operands)
-//   warps 0-1: U = U~ - W S0 as a bf16 hi + lo pair, while thread 64 issues
-//              MMA 3 of chunk j-1 (M=128, N=64, K=64):
-//              D1[(j-1) % 3][64..127] += A_qk [Uhi | Ulo]
-//   thread 0:  MMA 2 (M=128, N=64, K=64): [Sa | Sb] += Kr^T [Uhi | Ulo]
-//   all:       new bf16 state operand; snapshot
-// Only MMA 1, U, MMA 2 and the state write-back are on the chunk-to-chunk
-// dependency chain.  Everything else -- the output product and its store, the
-// copies -- runs in the shadow of the chain on warps that would otherwise
-// wait, with the tensor pipe taking MMA 3 while U is formed.  Three output
-// accumulators, three slots of chain operands, three A_qk tiles and two U
-// operands are in flight for that.  The state and U operands are stored
-// MN-major, so each thread writes its row as 16-byte chunks.  TMEM holds
-// 3 x 64 columns of output accumulators and 64 of state.  The math is
-// stated in kda_tc_common.cuh.
+// One CTA of 256 threads per (sequence, head, 32-column slice of S), walking
+// the sequence's chunks in order.  The state slice lives in TMEM as fp32
+// accumulators (lane = key channel); a bf16 copy of it in shared memory is
+// the MMA operand.  Every MMA runs at N=64: the bf16 operand of a 32-column
+// fp32 block is its hi half next to its lo half (x = hi + lo to about
+// 2^-16), so one instruction multiplies both.  A tcgen05.mma costs about the
+// same for any N <= 64, so this doubles the precision of the state and U
+// operands for free.  The state is kept as two accumulators S = Sa + Sb (Sa
+// takes the hi products, Sb the lo products).
+//
+// Two warps share each TMEM lane quarter (warps w and w+4), each taking 16 of
+// the 32 columns.  Step j of the walk, with S = S_j (the state entering
+// chunk j), the operand holding S_j and TMEM holding Gamma_L(j) S_j:
+//   thread 0:      MMA 1 (M=128, N=64, K=128): [W ; Qp] [S_hi | S_lo] -> D1[j % 3]
+//   warps 2,3,6,7: the output rows of chunk j-2 (its MMA 3 is done), copies;
+//                  thread 64 then issues MMA 3 of chunk j-1 (M=128, N=64,
+//                  K=64): D1[(j-1) % 3][64..127] += A_qk [U_hi | U_lo]
+//   warps 0,1,4,5: U = U~ - W S_j as bf16 hi | lo, then thread 0 issues
+//                  MMA 2 (M=128, N=64, K=64): [Sa | Sb] += Kr^T [U_hi | U_lo]
+//   all:           S_{j+1} = Sa + Sb: the bf16 operand, a snapshot if chunk j
+//                  ends at one, and Sa <- Gamma_L(j+1) S_{j+1}, Sb <- 0
+// The chunk-to-chunk chain is MMA 1 -> U -> MMA 2 -> state write-back; the
+// output product, its store and the copies run beside it.  Records are
+// prefetched two chunks ahead with bulk copies (TMA engine).  TMEM holds
+// 3 x 64 columns of output accumulators and 64 of state.  The math is stated
+// in kda_tc_common.cuh.
 #include "kda_tc_common.cuh"
 
 namespace kda {
@@ -38,13 +35,15 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr int kNs = 32;                 // state columns per CTA
+constexpr int kNh = kNs / 2;            // columns per thread
 constexpr int kNop = 2 * kNs;           // MMA N: hi and lo halves side by side
 constexpr uint32_t kSopSbo = 16 * 128;  // S operand: 16 K-groups (key channels) per MN-group
 constexpr uint32_t kUopSbo = 8 * 128;   // U operand: 8 K-groups (tokens) per MN-group
 constexpr uint32_t kTmemCols = 4 * kNop;
 constexpr int kMmaThread = 0, kOutThread = 64, kLoadThread = 96;
+constexpr int kUBarrier = 1;            // named barrier of the U warps (0, 1, 4, 5)
 
 struct K3Smem {
   // ring of chain operands: AW (32 KB) | AK (16 KB) | UT slice | GL
@@ -92,17 +91,15 @@ __device__ __forceinline__ void k3_load_aq(const ChunkParams& p, uint8_t* dst, u
   bulk_g2s(dst, rec + Rec::AQ, K3Smem::AQ_BYTES, bar);
 }
 
-// 64 consecutive fp32 values of one TMEM lane, summed in pairs: v[n] =
-// column n + column 32 + n (the two halves of a hi | lo accumulator)
-__device__ __forceinline__ void tmem_ld_sum(uint32_t taddr, float* v) {
-  float b[kNs];
-  tmem_ld16(taddr, v);
-  tmem_ld16(taddr + 16, v + 16);
-  tmem_ld16(taddr + 32, b);
-  tmem_ld16(taddr + 48, b + 16);
+// This thread's 16 columns of a hi | lo accumulator pair, summed: v[n] =
+// column (h16 + n) + column (32 + h16 + n) of one TMEM lane.
+__device__ __forceinline__ void tmem_ld_sum(uint32_t taddr, int h16, float* v) {
+  float b[kNh];
+  tmem_ld16(taddr + h16, v);
+  tmem_ld16(taddr + kNs + h16, b);
   tmem_ld_wait();
 #pragma unroll
-  for (int n = 0; n < kNs; ++n) v[n] += b[n];
+  for (int n = 0; n < kNh; ++n) v[n] += b[n];
 }
 
 // bf16 hi and lo parts of 8 fp32 values, packed
@@ -117,28 +114,18 @@ __device__ __forceinline__ void split8(const float* u, uint4& hi, uint4& lo) {
   lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// the S operand row of key channel c: [hi | lo], 8 chunks of 8 bf16 (MN-major)
-__device__ __forceinline__ void store_state_operand(uint8_t* sop, int c, const float* v) {
-#pragma unroll
-  for (int m = 0; m < kNs / 8; ++m) {
-    uint4 hi, lo;
-    split8(v + 8 * m, hi, lo);
-    *reinterpret_cast<uint4*>(sop + mnmajor_off(8 * m, c, kSopSbo)) = hi;
-    *reinterpret_cast<uint4*>(sop + mnmajor_off(kNs + 8 * m, c, kSopSbo)) = lo;
-  }
-}
-
-// o rows of one chunk from lanes 64-127 of an output accumulator (warps 2, 3)
+// o rows of one chunk from lanes 64-127 of an output accumulator: row i, this
+// thread's 16 columns
 __device__ __forceinline__ void store_output(const ChunkParams& p, const Chunk& ch, uint32_t d1,
-                                             uint32_t lane_off, int i, int h, int n0) {
-  float d[kNs];
-  tmem_ld_sum(d1 + lane_off, d);
+                                             int h16, int i, int h, int n0) {
+  float d[kNh];
+  tmem_ld_sum(d1, h16, d);
   if (i < ch.len) {
     const float scale = p.scale;
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o);
-    uint4* dst = reinterpret_cast<uint4*>(o + ((ch.tok0 + i) * p.H + h) * (int64_t)kD + n0);
+    uint4* dst = reinterpret_cast<uint4*>(o + ((ch.tok0 + i) * p.H + h) * (int64_t)kD + n0 + h16);
 #pragma unroll
-    for (int q8 = 0; q8 < kNs / 8; ++q8)
+    for (int q8 = 0; q8 < kNh / 8; ++q8)
       dst[q8] = make_uint4(pack_bf16(scale * d[8 * q8], scale * d[8 * q8 + 1]),
                            pack_bf16(scale * d[8 * q8 + 2], scale * d[8 * q8 + 3]),
                            pack_bf16(scale * d[8 * q8 + 4], scale * d[8 * q8 + 5]),
@@ -146,15 +133,37 @@ __device__ __forceinline__ void store_output(const ChunkParams& p, const Chunk& 
   }
 }
 
+// The state write-back of one TMEM lane (key channel c), this thread's 16
+// columns: the bf16 operand [hi | lo] of v, and Sa <- gl v, Sb <- 0.
+__device__ __forceinline__ void write_state(uint8_t* sop, uint32_t ds, int c, int h16, const float* v,
+                                            float gl) {
+#pragma unroll
+  for (int m = 0; m < kNh / 8; ++m) {
+    uint4 hi, lo;
+    split8(v + 8 * m, hi, lo);
+    *reinterpret_cast<uint4*>(sop + mnmajor_off(h16 + 8 * m, c, kSopSbo)) = hi;
+    *reinterpret_cast<uint4*>(sop + mnmajor_off(kNs + h16 + 8 * m, c, kSopSbo)) = lo;
+  }
+  float s[kNh], z[kNh];
+#pragma unroll
+  for (int n = 0; n < kNh; ++n) {
+    s[n] = gl * v[n];
+    z[n] = 0.f;
+  }
+  tmem_st16(ds + h16, s);
+  tmem_st16(ds + kNs + h16, z);
+  tmem_st_wait();
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 tc_inter(ChunkParams p) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ __align__(8) uint64_t bar_full[K3Smem::kSlots];
   __shared__ __align__(8) uint64_t bar_aq[K3Smem::kAqSlots];
-  __shared__ __align__(8) uint64_t bar_mma1;   // MMA 1
-  __shared__ __align__(8) uint64_t bar_mma2;   // MMA 2 (state chain)
-  __shared__ __align__(8) uint64_t bar_mma3;   // MMA 3 (output path)
-  __shared__ __align__(8) uint64_t bar_drain;  // every MMA, on the error path
+  __shared__ __align__(8) uint64_t bar_mma1;     // MMA 1
+  __shared__ __align__(8) uint64_t bar_mma2;     // MMA 2 (state chain)
+  __shared__ __align__(8) uint64_t bar_mma3[2];  // MMA 3 of even / odd chunks (output path)
+  __shared__ __align__(8) uint64_t bar_drain;    // every MMA, on the error path
   __shared__ uint32_t tmem_base;
 
   const int s = blockIdx.x, h = blockIdx.y, n0 = blockIdx.z * kNs;
@@ -163,6 +172,11 @@ tc_inter(ChunkParams p) {
   if (c_end > c_begin && p.meta->total_chunks == 0) return;  // chunk table overflowed
   const int64_t nchunks = c_end - c_begin;
 
+  // TMEM lane quarter of this warp, its 16 columns, its key channel / token row
+  const int quarter = warp & 3;
+  const int h16 = (warp >> 2) * kNh;
+  const int c = tid & 127;
+  const bool u_warp = quarter < 2;  // warps 0, 1, 4, 5: lanes 0-63 (W rows, U)
   uint8_t* SOP = sm + K3Smem::SOP;
 
   if (warp == 0) tmem_alloc(&tmem_base, kTmemCols);
@@ -171,7 +185,8 @@ tc_inter(ChunkParams p) {
     for (int i = 0; i < K3Smem::kAqSlots; ++i) mbar_init(&bar_aq[i], 1);
     mbar_init(&bar_mma1, 1);
     mbar_init(&bar_mma2, 1);
-    mbar_init(&bar_mma3, 1);
+    mbar_init(&bar_mma3[0], 1);
+    mbar_init(&bar_mma3[1], 1);
     mbar_init(&bar_drain, 2);  // the two MMA-issuing threads
     mbar_init_fence();
   }
@@ -180,15 +195,19 @@ tc_inter(ChunkParams p) {
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const uint32_t DS = tmem + 3 * kNop;  // the state slice [Sa | Sb], lane = key channel
-  const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-  // output accumulator of chunk j: [W;Qp] S0, then + A_qk U in lanes 64-127
+  const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+  const uint32_t DS = tmem + 3 * kNop + lane_off;  // [Sa | Sb], lane = key channel
+  // output accumulator of chunk j (this warp's lanes): [W;Qp] S_j, then
+  // + A_qk U in lanes 64-127
   auto d1_of = [&](int64_t j) { return tmem + (uint32_t)(j % 3) * kNop; };
   auto slot_of = [&](int64_t j) { return sm + (uint32_t)(j % K3Smem::kSlots) * K3Smem::SLOT; };
   auto aq_of = [&](int64_t j) {
     return sm + K3Smem::AQ0 + (uint32_t)(j % K3Smem::kAqSlots) * K3Smem::AQ_BYTES;
   };
   auto u_of = [&](int64_t j) { return sm + K3Smem::U0 + (uint32_t)(j & 1) * K3Smem::U_BYTES; };
+  auto wait_chain = [&](int64_t j) {
+    return mbar_wait(&bar_full[j % K3Smem::kSlots], (uint32_t)((j / K3Smem::kSlots) & 1), kWaitLimitNs);
+  };
 
   // Thread 96 issues the chain-operand copies and thread 64 the A_qk copies;
   // each counts what it issued and what was waited for, so the error path
@@ -201,33 +220,32 @@ tc_inter(ChunkParams p) {
     for (; aq_issued < K3Smem::kAqSlots && aq_issued < nchunks; ++aq_issued)
       k3_load_aq(p, aq_of(aq_issued), &bar_aq[aq_issued], c_begin + aq_issued, h);
 
-  // initial state slice: TMEM (fp32) and the bf16 operand copy
-  const int c = tid;  // key channel == TMEM lane
+  bool ok = true;
+  bool okl = true;  // this thread's own waits succeeded
+  // initial state: the operand holds S_0, TMEM Gamma_L(0) S_0
   const size_t sbase = ((size_t)s * H + h) * kD * kD;
   {
-    float v[kNs];
+    float v[kNh];
 #pragma unroll
-    for (int n = 0; n < kNs; n += 4) {
+    for (int n = 0; n < kNh; n += 4) {
       float4 x = p.initial_state
-                     ? *reinterpret_cast<const float4*>(p.initial_state + sbase + (size_t)c * kD + n0 + n)
+                     ? *reinterpret_cast<const float4*>(p.initial_state + sbase + (size_t)c * kD + n0 + h16 + n)
                      : make_float4(0.f, 0.f, 0.f, 0.f);
       v[n] = x.x; v[n + 1] = x.y; v[n + 2] = x.z; v[n + 3] = x.w;
     }
-    float z[16];
-#pragma unroll
-    for (int n = 0; n < 16; ++n) z[n] = 0.f;
-    tmem_st16(DS + lane_off, v);
-    tmem_st16(DS + lane_off + 16, v + 16);
-    tmem_st16(DS + lane_off + 32, z);
-    tmem_st16(DS + lane_off + 48, z);
-    tmem_st_wait();
-    store_state_operand(SOP, c, v);
+    float gl = 1.f;
+    if (nchunks > 0) {
+      okl = wait_chain(0);
+      chain_waited = 1;
+      gl = reinterpret_cast<const float*>(slot_of(0) + K3Smem::GL)[c];
+    }
+    write_state(SOP, DS, c, h16, v, gl);
   }
 
   const uint32_t id = idesc_bf16(128, kNop, 0, 1);     // B operands MN-major
   const uint32_t id_ak = idesc_bf16(128, kNop, 1, 1);  // Kr^T is MN-major too
   // MMA 3 of chunk j, thread 64: wait for its A_qk tile, then
-  // D1[j % 3] += A_qk [Uhi | Ulo].  False if the tile never came.
+  // D1[j % 3] += A_qk [U_hi | U_lo].  False if the tile never came.
   auto mma3 = [&](int64_t j) -> bool {
     if (!mbar_wait(&bar_aq[j % K3Smem::kAqSlots], (uint32_t)((j / K3Smem::kAqSlots) & 1), kWaitLimitNs))
       return false;
@@ -236,16 +254,17 @@ tc_inter(ChunkParams p) {
 #pragma unroll
     for (int k = 0; k < 4; ++k)
       mma_bf16(d1_of(j), sdesc(a + k * 2 * 1024, 1024, 128), sdesc(ub + k * 256, 128, kUopSbo), id, 1);
-    mma_commit(&bar_mma3);
+    mma_commit(&bar_mma3[j & 1]);
     return true;
   };
+  // MMA 3 of chunk j completes phase j / 2 of bar_mma3[j & 1].  Its waiters
+  // are done before the next commit to that barrier (two steps later, behind
+  // a CTA barrier), so a parity wait never sees two phases complete.
+  auto wait_mma3 = [&](int64_t j) {
+    return mbar_wait(&bar_mma3[j & 1], (uint32_t)((j >> 1) & 1), kWaitLimitNs);
+  };
 
-  // MMA 3 of chunk j is the j-th phase of bar_mma3.  Warps 2-3 wait for it
-  // before MMA 3 of chunk j+1 is issued (a step later, or behind a barrier at
-  // the end), so a parity wait never sees two phases complete.
   uint32_t ph1 = 0, ph2 = 0;
-  bool ok = true;
-  bool oko = true;  // warps 2-3: MMA 3 issued and finished in time
   Chunk prev1{}, prev2{};
   Chunk next = nchunks > 0 ? p.chunks[c_begin] : Chunk{};
   for (int64_t it = 0; it < nchunks; ++it) {
@@ -253,14 +272,13 @@ tc_inter(ChunkParams p) {
     uint8_t* uop = u_of(it);
     const Chunk ch = next;  // chunk entries are read one step ahead
     if (it + 1 < nchunks) next = p.chunks[c_begin + it + 1];
-    // S operand (previous step) and this slot are ready
+    // the state operand and TMEM state of this step are written; this
+    // slot's copies have landed (waited during the previous write-back)
     fence_async_smem();
     fence_before_sync();
-    ok = __syncthreads_and(oko && mbar_wait(&bar_full[it % K3Smem::kSlots],
-                                            (uint32_t)((it / K3Smem::kSlots) & 1), kWaitLimitNs));
+    ok = __syncthreads_and(okl);
     fence_after_sync();
     if (!ok) break;
-    chain_waited = it + 1;
     if (tid == kMmaThread) {
 #pragma unroll
       for (int k = 0; k < 8; ++k)
@@ -268,124 +286,115 @@ tc_inter(ChunkParams p) {
                  sdesc(smem_u32(SOP) + k * 256, 128, kSopSbo), id, k > 0);
       mma_commit(&bar_mma1);
     }
-    // while MMA 1 runs: retention of the carried state,
-    // Sa <- Diag(Gamma_L) (Sa + Sb), Sb <- 0 ...
-    {
-      const float gl = reinterpret_cast<const float*>(slot + K3Smem::GL)[c];
-      float v[kNs], z[16];
-      tmem_ld_sum(DS + lane_off, v);
-#pragma unroll
-      for (int n = 0; n < kNs; ++n) v[n] *= gl;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) z[n] = 0.f;
-      tmem_st16(DS + lane_off, v);
-      tmem_st16(DS + lane_off + 16, v + 16);
-      tmem_st16(DS + lane_off + 32, z);
-      tmem_st16(DS + lane_off + 48, z);
-      tmem_st_wait();
-    }
-    if (warp >= 2) {
-      // ... the outputs of chunk it-2, whose MMA 3 was issued last step ...
+    if (!u_warp) {
+      // the outputs of chunk it-2, whose MMA 3 was issued last step ...
       if (it >= 2) {
-        oko = oko && mbar_wait(&bar_mma3, (uint32_t)((it - 2) & 1), kWaitLimitNs);
+        okl = okl && wait_mma3(it - 2);
         fence_after_sync();
-        if (oko) store_output(p, prev2, d1_of(it - 2), lane_off, tid - 64, h, n0);
+        if (okl) store_output(p, prev2, d1_of(it - 2) + lane_off, h16, c - 64, h, n0);
         // ... its A_qk tile takes chunk it+1 ...
-        if (tid == kOutThread && oko && it + 1 < nchunks && aq_issued == it + 1) {
+        if (tid == kOutThread && okl && it + 1 < nchunks && aq_issued == it + 1) {
           k3_load_aq(p, aq_of(it + 1), &bar_aq[(it + 1) % K3Smem::kAqSlots], c_begin + it + 1, h);
           aq_issued = it + 2;
         }
       }
-      // ... and the slot of chunk it-1 (MMA 2 done) takes chunk it+2
+      // ... the slot of chunk it-1 (MMA 2 done) takes chunk it+2 ...
       if (tid == kLoadThread && it >= 1 && it + 2 < nchunks) {
         k3_load_chain(p, slot_of(it + 2), &bar_full[(it + 2) % K3Smem::kSlots], c_begin + it + 2, h, n0);
         chain_issued = it + 3;
       }
-    }
-    fence_before_sync();
-    ok = __syncthreads_and(mbar_wait(&bar_mma1, ph1, kWaitLimitNs));
-    ph1 ^= 1;
-    fence_after_sync();
-    if (!ok) break;
-    if (warp < 2) {
-      // U = U~ - W S0 for token i = lane row, split into bf16 hi + lo
-      const int i = tid;
-      float d[kNs];
-      tmem_ld_sum(d1_of(it) + lane_off, d);
+      // ... and the output product of chunk it-1 runs once MMA 1 is done
+      if (tid == kOutThread && it >= 1 && okl) {
+        okl = mbar_wait(&bar_mma1, ph1, kWaitLimitNs);
+        if (okl) okl = mma3(it - 1);
+      }
+    } else {
+      // U = U~ - W S_j for token i = lane row, this thread's 16 columns.  The
+      // U buffer of this step was last read by MMA 3 of chunk it-2, issued by
+      // another thread: its completion is awaited too.
+      okl = okl && mbar_wait(&bar_mma1, ph1, kWaitLimitNs);
+      if (it >= 2) okl = okl && wait_mma3(it - 2);
+      fence_after_sync();
+      const int i = c;
+      float d[kNh];
+      tmem_ld_sum(d1_of(it) + lane_off, h16, d);
       const float* ut = reinterpret_cast<const float*>(slot + K3Smem::UT);
 #pragma unroll
-      for (int m = 0; m < kNs / 8; ++m) {
-        const float4 ua = *reinterpret_cast<const float4*>(ut + ((2 * m) * 64 + i) * 4);
-        const float4 ub = *reinterpret_cast<const float4*>(ut + ((2 * m + 1) * 64 + i) * 4);
+      for (int m = 0; m < kNh / 8; ++m) {
+        const int e = h16 + 8 * m;  // first of 8 columns
+        const float4 ua = *reinterpret_cast<const float4*>(ut + ((e / 4) * 64 + i) * 4);
+        const float4 ub = *reinterpret_cast<const float4*>(ut + ((e / 4 + 1) * 64 + i) * 4);
         const float u[8] = {ua.x - d[8 * m], ua.y - d[8 * m + 1], ua.z - d[8 * m + 2],
                             ua.w - d[8 * m + 3], ub.x - d[8 * m + 4], ub.y - d[8 * m + 5],
                             ub.z - d[8 * m + 6], ub.w - d[8 * m + 7]};
         uint4 hi, lo;
         split8(u, hi, lo);
-        *reinterpret_cast<uint4*>(uop + mnmajor_off(8 * m, i, kUopSbo)) = hi;
-        *reinterpret_cast<uint4*>(uop + mnmajor_off(kNs + 8 * m, i, kUopSbo)) = lo;
+        *reinterpret_cast<uint4*>(uop + mnmajor_off(e, i, kUopSbo)) = hi;
+        *reinterpret_cast<uint4*>(uop + mnmajor_off(kNs + e, i, kUopSbo)) = lo;
       }
-    } else if (tid == kOutThread && it >= 1 && oko) {
-      oko = mma3(it - 1);  // the output product of the previous chunk, in U's shadow
-    }
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    // MMA 2, the state chain: [Sa | Sb] += Kr^T [Uhi | Ulo]
-    if (tid == kMmaThread) {
-      const uint32_t ub = smem_u32(uop);
+      fence_async_smem();
+      asm volatile("bar.sync %0, 128;" ::"n"(kUBarrier) : "memory");
+      // MMA 2, the state chain: [Sa | Sb] += Kr^T [U_hi | U_lo]
+      if (tid == kMmaThread) {
+        const uint32_t ub = smem_u32(uop);
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_bf16(DS, sdesc(smem_u32(slot + K3Smem::AK) + k * 256, 128, Rec::kAkSbo),
-                 sdesc(ub + k * 256, 128, kUopSbo), id_ak, 1);
-      mma_commit(&bar_mma2);
+        for (int k = 0; k < 4; ++k)
+          mma_bf16(DS - lane_off, sdesc(smem_u32(slot + K3Smem::AK) + k * 256, 128, Rec::kAkSbo),
+                   sdesc(ub + k * 256, 128, kUopSbo), id_ak, 1);
+        mma_commit(&bar_mma2);
+      }
     }
-    ok = __syncthreads_and(mbar_wait(&bar_mma2, ph2, kWaitLimitNs));
+    ph1 ^= 1;
+    // the state write-back: S_{j+1} = Sa + Sb
+    okl = okl && mbar_wait(&bar_mma2, ph2, kWaitLimitNs);
     ph2 ^= 1;
     fence_after_sync();
-    if (!ok) break;
-    // new state: bf16 operand copy, snapshot if this chunk ends at one
     {
-      float v[kNs];
-      tmem_ld_sum(DS + lane_off, v);
-      store_state_operand(SOP, c, v);
+      float v[kNh];
+      tmem_ld_sum(DS, h16, v);
       if (ch.snap_slot >= 0 && p.snapshots) {
-        float* dst = p.snapshots + ((size_t)ch.snap_slot * H + h) * kD * kD + (size_t)c * kD + n0;
+        float* dst = p.snapshots + ((size_t)ch.snap_slot * H + h) * kD * kD + (size_t)c * kD + n0 + h16;
 #pragma unroll
-        for (int n = 0; n < kNs; n += 4)
+        for (int n = 0; n < kNh; n += 4)
           *reinterpret_cast<float4*>(dst + n) = make_float4(v[n], v[n + 1], v[n + 2], v[n + 3]);
       }
+      float gl = 1.f;  // the last chunk leaves S_n itself in TMEM
+      if (it + 1 < nchunks) {
+        okl = okl && wait_chain(it + 1);
+        chain_waited = it + 2;
+        gl = reinterpret_cast<const float*>(slot_of(it + 1) + K3Smem::GL)[c];
+      }
+      write_state(SOP, DS, c, h16, v, gl);
     }
     prev2 = prev1;
     prev1 = ch;
   }
   // the output products still open: chunk n-2 (issued) and chunk n-1 (not yet)
-  if (ok && warp >= 2 && nchunks >= 2) {
-    oko = oko && mbar_wait(&bar_mma3, (uint32_t)((nchunks - 2) & 1), kWaitLimitNs);
-    fence_after_sync();
-    if (oko) store_output(p, prev2, d1_of(nchunks - 2), lane_off, tid - 64, h, n0);
-  }
   fence_before_sync();
-  ok = __syncthreads_and(ok && oko);
+  ok = __syncthreads_and(ok && okl);
   fence_after_sync();
   if (ok && nchunks >= 1) {
-    if (tid == kOutThread) oko = mma3(nchunks - 1);
-    if (warp >= 2) {
-      oko = oko && mbar_wait(&bar_mma3, (uint32_t)((nchunks - 1) & 1), kWaitLimitNs);
+    if (tid == kOutThread) okl = mma3(nchunks - 1);
+    if (!u_warp) {
+      if (nchunks >= 2) {
+        okl = okl && wait_mma3(nchunks - 2);
+        fence_after_sync();
+        if (okl) store_output(p, prev2, d1_of(nchunks - 2) + lane_off, h16, c - 64, h, n0);
+      }
+      okl = okl && wait_mma3(nchunks - 1);
       fence_after_sync();
-      if (oko) store_output(p, prev1, d1_of(nchunks - 1), lane_off, tid - 64, h, n0);
+      if (okl) store_output(p, prev1, d1_of(nchunks - 1) + lane_off, h16, c - 64, h, n0);
     }
   }
   fence_before_sync();
-  ok = __syncthreads_and(ok && oko);
+  ok = __syncthreads_and(ok && okl);
   fence_after_sync();
   if (ok && p.final_state) {
-    float v[kNs];
-    tmem_ld_sum(DS + lane_off, v);
-    float* dst = p.final_state + sbase + (size_t)c * kD + n0;
+    float v[kNh];
+    tmem_ld_sum(DS, h16, v);
+    float* dst = p.final_state + sbase + (size_t)c * kD + n0 + h16;
 #pragma unroll
-    for (int n = 0; n < kNs; n += 4)
+    for (int n = 0; n < kNh; n += 4)
       *reinterpret_cast<float4*>(dst + n) = make_float4(v[n], v[n + 1], v[n + 2], v[n + 3]);
   }
   if (!ok) {
@@ -393,8 +402,7 @@ tc_inter(ChunkParams p) {
     // before the shared memory and TMEM are given back
     if (tid == 0) flag(p.status, kFlagTimeout);
     if (tid == kLoadThread)
-      for (int64_t j = chain_waited; j < chain_issued; ++j)
-        mbar_wait(&bar_full[j % K3Smem::kSlots], (uint32_t)((j / K3Smem::kSlots) & 1), kWaitLimitNs);
+      for (int64_t j = chain_waited; j < chain_issued; ++j) wait_chain(j);
     if (tid == kOutThread)
       for (int64_t j = aq_waited; j < aq_issued; ++j)
         mbar_wait(&bar_aq[j % K3Smem::kAqSlots], (uint32_t)((j / K3Smem::kAqSlots) & 1), kWaitLimitNs);

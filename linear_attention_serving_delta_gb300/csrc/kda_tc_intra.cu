@@ -1,18 +1,25 @@
 // kda_tc_intra.cu -- K2, the intra-chunk kernel of the tensor-core prefill.
 //
 // Persistent, two CTAs of 256 threads per SM.  For each (chunk, head) item
-// every thread owns 4 consecutive tokens x 8 channels: its q, k, g, v rows
-// (16-byte loads, prefetched during the previous item), the cumulative decay
-// Gamma as a product scan (in registers, then across the 16 token blocks with
-// shuffles), normalised q and k, and the operands written with 16-byte
-// shared stores straight into the tcgen05 layouts (K-major where a row of 8
-// channels is one core-matrix row, MN-major where 8 channels of one token
-// are).  Then:
+// every thread owns 4 consecutive tokens x 8 channels: warp w takes channel
+// half w % 2 and token quarter w / 2, lane l channel group l % 8 and token
+// block l / 8.  A warp's 16-byte loads of one token row index then cover four
+// whole 128-byte lines (coalesced); the rows are prefetched into L2 during
+// the previous item.  The cumulative decay Gamma is a product scan (in
+// registers over a thread's 4 tokens, across the warp's 4 token blocks with
+// shuffles, across the 4 token quarters through shared memory), the norms
+// reduce over 8 lanes and a pair of warps.  The operands are written with
+// 16-byte shared stores straight into the tcgen05 no-swizzle layouts, whose
+// stride between 8-channel groups is padded by 16 bytes so that the 8 channel
+// groups and 4 tokens of one warp store fall in distinct banks.  Then:
 //   MMA 1 (M=128, N=64, K=128):  [A_kk ; A_qk] = [Kp ; Qp] Kn^T  -> TMEM
 //   CUDA cores: T = (I + A_kk)^{-1}, two-level blocked inverse
 //   MMA 2 (M=64, N=256, K=64):   [W | U~] = T diag(beta) [Kp | V] -> TMEM
-// and the record of kda_tc_common.cuh is written (AW with one bulk copy).
-// The math is stated in kda_tc_common.cuh.
+// and the record of kda_tc_common.cuh is written with bulk copies (TMA
+// engine) out of shared memory: AW and AK one per 8-channel group (dropping
+// the padding), A_qk and U~ each in one, staged in tiles that are free at
+// that point.  The load/store unit then carries only the raw-row loads.  The
+// math is stated in kda_tc_common.cuh.
 #include "kda_tc_common.cuh"
 
 namespace kda {
@@ -24,29 +31,51 @@ using namespace tc;
 constexpr int kThreads = 256;
 constexpr int kAs = 68;  // row stride (floats) of A_kk in shared memory
 constexpr int kTs = 64;  // row stride (floats) of T
-constexpr uint32_t kB2Sbo = 8 * 128;  // B2 MN-major: 8 K-groups (64 tokens) per MN-group
+// Padded no-swizzle operand layouts (strides of the descriptors, bytes)
+constexpr uint32_t kA1Lbo = 128 * 16 + 16;  // A1 K-major, R=128: stride between 8-channel groups
+constexpr uint32_t kB1Lbo = 64 * 16 + 16;   // B1 K-major, R=64
+constexpr uint32_t kB2Sbo = 8 * 128 + 16;   // B2 MN-major (n, token): stride between 8-n groups
+constexpr uint32_t kAkStage = 8 * 128 + 16; // Kr^T staged for its record copy: stride between 8-channel groups
+// threads that issue the record's bulk copies (each waits for its own)
+constexpr int kAwCopy0 = 0;    // AW: threads 0-15, one 8-channel group each
+constexpr int kUtCopy = 16;    // U~
+constexpr int kAkCopy0 = 32;   // AK: threads 32-47, one 8-channel group each
+constexpr int kAqCopy = 64;    // A_qk
 
 struct Smem {
-  static constexpr uint32_t A1 = 0;                    // [Kp;Qp] -> [W;Qp], R=128, K=128
-  static constexpr uint32_t B1 = A1 + 128 * 128 * 2;   // Kn, R=64, K=128; then T fp32 [64][64]
-  static constexpr uint32_t B2 = B1 + 64 * 128 * 2;    // [Kp | V] as MN-major (n, token), N=256
-  static constexpr uint32_t A2 = B2 + 256 * 64 * 2;    // inverse scratch; then Tb, R=64, K=64
+  static constexpr uint32_t A1 = 0;                    // [Kp;Qp] -> [W;Qp], K=128 (16 groups)
+  static constexpr uint32_t B1 = A1 + 16 * kA1Lbo;     // Kn, K=128; then T fp32 [64][64]
+  static constexpr uint32_t B2 = B1 + 16 * kB1Lbo;     // [Kp | V] MN-major, N=256 (32 groups), K=64
+  static constexpr uint32_t A2 = B2 + 32 * kB2Sbo;     // inverse scratch; then Tb, R=64, K=64
   static constexpr uint32_t AKK = A2 + 64 * 64 * 2;    // fp32 [64][kAs]
-  static constexpr uint32_t MISC = AKK + 64 * kAs * 4; // inv_q, inv_k, beta [64]; part [2][8][64]
-  static constexpr uint32_t BYTES = MISC + (3 * 64 + 2 * 8 * 64) * 4;
+  // inv_q, inv_k, beta [64]; norm partials [q/k][channel half][64];
+  // decay totals of each token quarter [4][128]
+  static constexpr uint32_t MISC = AKK + 64 * kAs * 4;
+  static constexpr uint32_t BYTES = MISC + (3 * 64 + 2 * 2 * 64 + 4 * 128) * 4;
 };
+static_assert(Smem::B1 % 16 == 0 && Smem::B2 % 16 == 0 && Smem::A2 % 16 == 0 && Smem::AKK % 16 == 0,
+              "operand tiles and float4 arrays are 16-byte aligned");
+static_assert(16 * kB1Lbo >= 64 * kTs * 4, "T fits in the Kn tile");
+static_assert(16 * kAkStage <= 64 * kAs * 4, "the Kr^T staging fits in the A_kk tile");
+static_assert(32 * kB2Sbo >= 64 * 128 * 4, "the U~ staging fits in the B2 tile");
 
 __device__ __forceinline__ void st_s16(uint8_t* base, uint32_t off, uint4 v) {
   *reinterpret_cast<uint4*>(base + off) = v;
+}
+// byte offset of element (r, k) of a K-major operand whose 8-channel groups
+// are `lbo` bytes apart
+__device__ __forceinline__ uint32_t kmaj(uint32_t r, uint32_t k, uint32_t lbo) {
+  return (k >> 3) * lbo + (r >> 3) * 128u + (r & 7u) * 16u + (k & 7u) * 2u;
 }
 
 // T = (I + A)^{-1} for strictly lower-triangular A (64x64, stride kAs).
 // Level 0: the four 16x16 diagonal tiles by forward substitution (a thread
 // per column).  Level 1: the two 16x16 tiles below them inside each 32x32
 // half, T10 = -T11 A10 T00.  Level 2: the lower-left 32x32 tile,
-// T = -T_hi A T_lo.  X: scratch of 32x32 floats.  256 threads.
+// T = -T_hi A T_lo.  X: scratch of 32x32 floats.  256 threads; the thread
+// given x_busy first waits until its bulk copy out of X has read it.
 __device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ T,
-                               float* __restrict__ X) {
+                               float* __restrict__ X, bool x_busy) {
   const int tid = threadIdx.x;
   if (tid < 64) {
     const int d = tid >> 4, jj = tid & 15, j = 16 * d + jj;
@@ -78,8 +107,10 @@ __device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ 
       T[(16 * bi + (e >> 4)) * kTs + 16 * bj + (e & 15)] = 0.f;
     }
   }
+  if (x_busy) bulk_wait_read_all();
   __syncthreads();
   // level 1: P = 0, 1 -> tile rows 32P+16.., cols 32P..
+  // (X held the staged A_qk of the record: its copy has read it)
   {
     const int P = tid >> 7, rr = (tid >> 3) & 15, cc = (tid & 7) * 2;
     const int r0 = 32 * P + 16, c0 = 32 * P;
@@ -133,7 +164,7 @@ __device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ 
   __syncthreads();
 }
 
-// Raw rows of one work item (chunk, head) for this thread: 4 tokens (4 tb + r)
+// Raw rows of one work item (chunk, head) for this thread: 4 tokens (i0 + r)
 // x 8 channels of q, k, g, v, and the update logit of token `tid` (tid < 64).
 struct RawRows {
   uint4 g[4], q[4], k[4], v[4];
@@ -150,17 +181,16 @@ __device__ __forceinline__ uint4 ld_nc16(const void* ptr) {
   return v;
 }
 
-// One of the four tensors' rows (0 g, 1 q, 2 k, 3 v) of an item.  The
-// prefetch of the next item is spread over the current item's phases, so
-// that the load-queue back-pressure of each group drains behind compute.
-__device__ __forceinline__ void load_part(const ChunkParams& p, const Chunk& ch, int h, int tb, int c0,
+// This thread's rows of one of the four tensors (0 g, 1 q, 2 k, 3 v) of an
+// item; rows past the chunk's length read as zero.
+__device__ __forceinline__ void load_part(const ChunkParams& p, const Chunk& ch, int h, int i0, int c0,
                                           int which, uint4* dst) {
   const void* base = which == 0 ? p.g : which == 1 ? p.q : which == 2 ? p.k : p.v;
   const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(base);
   const int H = p.H, len = ch.len;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
-    const int i = 4 * tb + r;
+    const int i = i0 + r;
     const int64_t e = ((ch.tok0 + i) * H + h) * (int64_t)kD + c0;
     dst[r] = i < len ? ld_nc16(src + e) : make_uint4(0, 0, 0, 0);
   }
@@ -171,20 +201,30 @@ __device__ __forceinline__ float load_b(const ChunkParams& p, const Chunk& ch, i
   return (tid < 64 && tid < ch.len) ? __bfloat162float(gb[(ch.tok0 + tid) * p.H + h]) : 0.f;
 }
 
-__device__ __forceinline__ void load_rows(const ChunkParams& p, const Chunk& ch, int h, int tb, int c0,
+__device__ __forceinline__ void load_rows(const ChunkParams& p, const Chunk& ch, int h, int i0, int c0,
                                           int tid, RawRows& R) {
-  load_part(p, ch, h, tb, c0, 0, R.g);
-  load_part(p, ch, h, tb, c0, 1, R.q);
-  load_part(p, ch, h, tb, c0, 2, R.k);
-  load_part(p, ch, h, tb, c0, 3, R.v);
+  load_part(p, ch, h, i0, c0, 0, R.g);
+  load_part(p, ch, h, i0, c0, 1, R.q);
+  load_part(p, ch, h, i0, c0, 2, R.k);
+  load_part(p, ch, h, i0, c0, 3, R.v);
   R.b = load_b(p, ch, h, tid);
 }
 
+// An item's rows into L2: one 256-byte row per thread (tensor tid / 64,
+// token tid % 64) as a bulk prefetch, which occupies neither registers nor
+// load slots of the issuing warp.
+__device__ __forceinline__ void prefetch_rows_l2(const ChunkParams& p, const Chunk& ch, int h, int tid) {
+  const int which = tid >> 6, i = tid & 63;
+  if (i < ch.len) {
+    const void* base = which == 0 ? p.g : which == 1 ? p.q : which == 2 ? p.k : p.v;
+    bulk_prefetch_l2(static_cast<const __nv_bfloat16*>(base) + ((ch.tok0 + i) * p.H + h) * (int64_t)kD, kD * 2);
+  }
+}
+
 // Persistent: two CTAs per SM walk the (chunk, head) items with stride
-// gridDim.x.  The raw rows of the next item are loaded into the registers
-// freed once the current item's operands are built, so its DRAM reads
-// overlap this item's MMAs, inverse and record stores.  TMEM and the
-// mbarrier are set up once per CTA.
+// gridDim.x.  The rows of the next item are prefetched into L2 while this
+// item is computed, so its register loads hit L2.  TMEM and the mbarrier are
+// set up once per CTA.
 __global__ void __launch_bounds__(kThreads, 2)
 tc_intra(ChunkParams p, int64_t n_items) {
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -196,12 +236,12 @@ tc_intra(ChunkParams p, int64_t n_items) {
   if (item >= n_items) return;
   const int H = p.H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // this thread: tokens 4 tb .. 4 tb + 3, channels 8 cb .. 8 cb + 7.  Four
-  // consecutive tokens per thread keep the decay scan in registers (one
-  // shuffle per element); the operand stores see at most 4-way bank conflicts.
-  const int tb = lane >> 1;
-  const int cb = 2 * warp + (lane & 1);
-  const int c0 = 8 * cb;
+  // this thread: tokens i0 .. i0 + 3, channels c0 .. c0 + 7
+  const int cg = lane & 7, tb = lane >> 3;  // channel group in the half, token block in the quarter
+  const int hc = warp & 1, qt = warp >> 1;  // channel half, token quarter
+  const int c0 = 64 * hc + 8 * cg;
+  const int i0 = 16 * qt + 4 * tb;
+  // TMEM lane quarter and column half, for the accumulator read-outs
   const int quarter = warp & 3, half = warp >> 2;
 
   uint8_t* A1 = sm + Smem::A1;
@@ -214,7 +254,8 @@ tc_intra(ChunkParams p, int64_t n_items) {
   float* inv_q = reinterpret_cast<float*>(sm + Smem::MISC);
   float* inv_k = inv_q + 64;
   float* beta = inv_k + 64;
-  float* part = beta + 64;  // [2][8][64]
+  float* nrm = beta + 64;        // [q/k][channel half][64]
+  float* qtot = nrm + 2 * 2 * 64;  // [token quarter][128]
 
   if (warp == 0) tmem_alloc(&tmem_base, 256);
   if (tid == 0) {
@@ -222,11 +263,12 @@ tc_intra(ChunkParams p, int64_t n_items) {
     mbar_init_fence();
   }
 
-  // the pipeline: chunk entry and raw rows of the current item, chunk entry of the next
+  // the pipeline: chunk entries of the current and the next item; the rows
+  // of the first item are brought into L2 here, each later item's during the
+  // item before it
   Chunk ch = p.chunks[item / H];  // entries past the table's end have len 0
-  RawRows R;
-  load_rows(p, ch, (int)(item % H), tb, c0, tid, R);
   Chunk ch_next = item + stride < n_items ? p.chunks[(item + stride) / H] : Chunk{};
+  prefetch_rows_l2(p, ch, (int)(item % H), tid);
 
   fence_before_sync();
   __syncthreads();
@@ -239,44 +281,51 @@ tc_intra(ChunkParams p, int64_t n_items) {
     const int64_t cidx = item / H;
     const int len = ch.len;
     if (len == 0) {  // past the end of the chunk table (uniform across the CTA)
-      if (item + stride < n_items) load_rows(p, ch_next, (int)((item + stride) % H), tb, c0, tid, R);
+      if (item + stride < n_items) prefetch_rows_l2(p, ch_next, (int)((item + stride) % H), tid);
       ch = ch_next;
       ch_next = item + 2 * stride < n_items ? p.chunks[(item + 2 * stride) / H] : Chunk{};
       continue;
     }
     uint8_t* rec = reinterpret_cast<uint8_t*>(p.inter) + ((size_t)cidx * H + h) * Rec::BYTES;
-
-    // ---- V into B2 MN-major rows 128..255: the raw 16 bytes are one core-matrix row
-#pragma unroll
-    for (int r = 0; r < 4; ++r) st_s16(B2, mnmajor_off(128 + c0, 4 * tb + r, kB2Sbo), R.v[r]);
+    // this item's rows (L2 hits: prefetched during the previous item), and
+    // the next item's rows into L2
+    RawRows R;
+    load_rows(p, ch, h, i0, c0, tid, R);
+    if (item + stride < n_items) prefetch_rows_l2(p, ch_next, (int)((item + stride) % H), tid);
 
     // ---- cumulative decay Gamma_i = prod_{m<=i} alpha_m, alpha = 1 / (1 + e^g)
-    // (= exp(-softplus(g))): a product over this thread's 4 tokens, then an
-    // exclusive product scan across the 16 token blocks (lanes 2 apart)
-    float Gm[4][8], GLm[8];
+    // (= exp(-softplus(g))): a product over this thread's 4 tokens, a scan
+    // across the warp's 4 token blocks (lanes 8 apart), then across the token
+    // quarters through shared memory (below)
+    float Gm[4][8], qtot_own[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       float run = 1.f;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const float a = 4 * tb + r < len ? alpha_fast(bf16_at(R.g[r], j)) : 1.f;
+        const float a = i0 + r < len ? alpha_fast(bf16_at(R.g[r], j)) : 1.f;
         run *= a;
         Gm[r][j] = run;
       }
       float inc = run;
-#pragma unroll
-      for (int off = 2; off < 32; off <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, inc, off);
-        if (lane >= off) inc *= y;
-      }
-      float ex = __shfl_up_sync(0xffffffffu, inc, 2);
-      if (lane < 2) ex = 1.f;
+      float y = __shfl_up_sync(0xffffffffu, inc, 8);
+      if (tb >= 1) inc *= y;
+      y = __shfl_up_sync(0xffffffffu, inc, 16);
+      if (tb >= 2) inc *= y;
+      float ex = __shfl_up_sync(0xffffffffu, inc, 8);
+      if (tb == 0) ex = 1.f;
 #pragma unroll
       for (int r = 0; r < 4; ++r) Gm[r][j] *= ex;
-      GLm[j] = __shfl_sync(0xffffffffu, inc, 30 + (lane & 1));
+      qtot_own[j] = __shfl_sync(0xffffffffu, inc, 24 + cg);  // this quarter's product
+    }
+    if (tb == 0) {
+      *reinterpret_cast<float4*>(qtot + qt * 128 + c0) =
+          make_float4(qtot_own[0], qtot_own[1], qtot_own[2], qtot_own[3]);
+      *reinterpret_cast<float4*>(qtot + qt * 128 + c0 + 4) =
+          make_float4(qtot_own[4], qtot_own[5], qtot_own[6], qtot_own[7]);
     }
 
-    // ---- L2 norms per token: 8 channels here, 2 per warp, 8 warps
+    // ---- L2 norms per token: 8 channels here, 8 lanes, then the two channel halves
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       float sq = 0.f, sk = 0.f;
@@ -286,33 +335,60 @@ tc_intra(ChunkParams p, int64_t n_items) {
         sq += xq * xq;
         sk += xk * xk;
       }
-      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-      if ((lane & 1) == 0) {
-        part[warp * 64 + 4 * tb + r] = sq;
-        part[512 + warp * 64 + 4 * tb + r] = sk;
+#pragma unroll
+      for (int m = 1; m < 8; m <<= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, m);
+        sk += __shfl_xor_sync(0xffffffffu, sk, m);
+      }
+      if (cg == 0) {
+        nrm[hc * 64 + i0 + r] = sq;
+        nrm[128 + hc * 64 + i0 + r] = sk;
       }
     }
     if (tid < 64) beta[tid] = tid < len ? beta_of(R.b) : 0.f;
-    // the previous item's record copy must have finished reading A1
-    if (tid == 0) bulk_wait_read_all();
+    // the previous item's record copies must have finished reading A1 and B2
+    if (tid <= kUtCopy) bulk_wait_read_all();
     __syncthreads();
     if (tid < 64) {
-      float sq = 0.f, sk = 0.f;
+      inv_q[tid] = inv_norm_of(nrm[tid] + nrm[64 + tid]);
+      inv_k[tid] = inv_norm_of(nrm[128 + tid] + nrm[192 + tid]);
+    }
+    // the decay entering this token quarter, and the chunk total Gamma_L
+    float GLm[8];
+    {
+      float pre[8], tot[8];
 #pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        sq += part[w * 64 + tid];
-        sk += part[512 + w * 64 + tid];
+      for (int j = 0; j < 8; ++j) pre[j] = tot[j] = 1.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 a = *reinterpret_cast<const float4*>(qtot + q * 128 + c0);
+        const float4 b = *reinterpret_cast<const float4*>(qtot + q * 128 + c0 + 4);
+        const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (q < qt) pre[j] *= x[j];
+          tot[j] *= x[j];
+        }
       }
-      inv_q[tid] = inv_norm_of(sq);
-      inv_k[tid] = inv_norm_of(sk);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        GLm[j] = tot[j];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) Gm[r][j] *= pre[j];
+      }
     }
     __syncthreads();
 
-    // ---- operands Kp, Qp (A1), Kn (B1), Kp (B2 MN-major rows 0-127), Kr (record AK, MN-major)
+    // ---- V into B2 MN-major rows 128..255: the raw 16 bytes are one core-matrix row
+#pragma unroll
+    for (int r = 0; r < 4; ++r) st_s16(B2, mnmajor_off(128 + c0, i0 + r, kB2Sbo), R.v[r]);
+
+    // ---- operands Kp, Qp (A1), Kn (B1), Kp (B2 MN-major rows 0-127), Kr
+    // (staged MN-major in the A_kk tile for the record's AK)
+    uint8_t* AKS = sm + Smem::AKK;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const int i = 4 * tb + r;
+      const int i = i0 + r;
       const float ik = inv_k[i], iq = inv_q[i];
       float kp[8], qp[8], kn[8], kx[8];
 #pragma unroll
@@ -327,30 +403,24 @@ tc_intra(ChunkParams p, int64_t n_items) {
       }
       const uint4 kpv = make_uint4(pack_bf16(kp[0], kp[1]), pack_bf16(kp[2], kp[3]),
                                    pack_bf16(kp[4], kp[5]), pack_bf16(kp[6], kp[7]));
-      st_s16(A1, kmajor_off(i, c0, 128), kpv);
+      st_s16(A1, kmaj(i, c0, kA1Lbo), kpv);
       st_s16(B2, mnmajor_off(c0, i, kB2Sbo), kpv);
-      st_s16(A1, kmajor_off(64 + i, c0, 128),
+      st_s16(A1, kmaj(64 + i, c0, kA1Lbo),
              make_uint4(pack_bf16(qp[0], qp[1]), pack_bf16(qp[2], qp[3]), pack_bf16(qp[4], qp[5]),
                         pack_bf16(qp[6], qp[7])));
-      st_s16(B1, kmajor_off(i, c0, 64),
+      st_s16(B1, kmaj(i, c0, kB1Lbo),
              make_uint4(pack_bf16(kn[0], kn[1]), pack_bf16(kn[2], kn[3]), pack_bf16(kn[4], kn[5]),
                         pack_bf16(kn[6], kn[7])));
-      *reinterpret_cast<uint4*>(rec + Rec::AK + mnmajor_off(c0, i, Rec::kAkSbo)) =
-          make_uint4(pack_bf16(kx[0], kx[1]), pack_bf16(kx[2], kx[3]), pack_bf16(kx[4], kx[5]),
-                     pack_bf16(kx[6], kx[7]));
+      st_s16(AKS, mnmajor_off(c0, i, kAkStage),
+             make_uint4(pack_bf16(kx[0], kx[1]), pack_bf16(kx[2], kx[3]), pack_bf16(kx[4], kx[5]),
+                        pack_bf16(kx[6], kx[7])));
     }
-    if (tb == 0) {  // every lane holds its channels' chunk totals
+    if (qt == 0 && tb == 0) {  // warps 0-1, lanes 0-7: the chunk totals of all 128 channels
       float* gl = reinterpret_cast<float*>(rec + Rec::GL) + c0;
       *reinterpret_cast<float4*>(gl) = make_float4(GLm[0], GLm[1], GLm[2], GLm[3]);
       *reinterpret_cast<float4*>(gl + 4) = make_float4(GLm[4], GLm[5], GLm[6], GLm[7]);
     }
 
-    // ---- the raw registers are free: the next item's rows are loaded in four
-    // groups spread over this item's phases (g now, q, k, v below)
-    const bool has_next = item + stride < n_items;
-    const Chunk chn = ch_next;
-    const int hn = (int)((item + stride) % H);
-    if (has_next) load_part(p, chn, hn, tb, c0, 0, R.g);
     ch = ch_next;
     ch_next = item + 2 * stride < n_items ? p.chunks[(item + 2 * stride) / H] : Chunk{};
 
@@ -359,16 +429,24 @@ tc_intra(ChunkParams p, int64_t n_items) {
     __syncthreads();
     fence_after_sync();
 
+    // Kr^T to the record's AK, one bulk copy per 8-channel group (dropping
+    // the staging's padding)
+    if (tid >= kAkCopy0 && tid < kAkCopy0 + 16) {
+      const int g = tid - kAkCopy0;
+      bulk_s2g(rec + Rec::AK + g * Rec::kAkSbo, AKS + g * kAkStage, Rec::kAkSbo);
+      bulk_commit();
+    }
     // ---- MMA 1: [A_kk ; A_qk] = [Kp ; Qp] Kn^T   (M=128, N=64, K=128)
     if (tid == 0) {
       const uint32_t id = idesc_bf16(128, 64);
 #pragma unroll
       for (int s = 0; s < 8; ++s)
-        mma_bf16(tmem, sdesc(smem_u32(A1) + s * 2 * 128 * 16, 128 * 16, 128),
-                 sdesc(smem_u32(B1) + s * 2 * 64 * 16, 64 * 16, 128), id, s > 0);
+        mma_bf16(tmem, sdesc(smem_u32(A1) + s * 2 * kA1Lbo, kA1Lbo, 128),
+                 sdesc(smem_u32(B1) + s * 2 * kB1Lbo, kB1Lbo, 128), id, s > 0);
       mma_commit(&bar_mma);
     }
-    if (has_next) load_part(p, chn, hn, tb, c0, 1, R.q);
+    // the A_kk tile is rewritten below: the AK copies must have read it
+    if (tid >= kAkCopy0 && tid < kAkCopy0 + 16) bulk_wait_read_all();
     ok = __syncthreads_and(mbar_wait(&bar_mma, 0, kWaitLimitNs));
     fence_after_sync();
     if (!ok) break;
@@ -398,18 +476,23 @@ tc_intra(ChunkParams p, int64_t n_items) {
           float a[8];
 #pragma unroll
           for (int t = 0; t < 8; ++t) a[t] = (live && 8 * jb + t <= i) ? d[8 * t8 + t] : 0.f;
-          *reinterpret_cast<uint4*>(rec + Rec::AQ + kmajor_off(i, 8 * jb, 64)) =
+          *reinterpret_cast<uint4*>(A2 + kmajor_off(i, 8 * jb, 64)) =
               make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]),
                          pack_bf16(a[6], a[7]));
         }
       }
     }
-    if (has_next) load_part(p, chn, hn, tb, c0, 2, R.k);
+    fence_async_smem();
     fence_before_sync();
     __syncthreads();
+    // A_qk, staged in A2, to the record
+    if (tid == kAqCopy) {
+      bulk_s2g(rec + Rec::AQ, A2, 64 * 64 * 2);
+      bulk_commit();
+    }
 
     // ---- T = (I + A_kk)^{-1}; Tb = T diag(beta) -> A2 (bf16, R=64)
-    tri_inverse_64(AKK, TT, XS);
+    tri_inverse_64(AKK, TT, XS, tid == kAqCopy);
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int idx = tid + kThreads * t;
@@ -421,10 +504,6 @@ tc_intra(ChunkParams p, int64_t n_items) {
       st_s16(A2, kmajor_off(i, 8 * jb, 64),
              make_uint4(pack_bf16(t0.x * b0.x, t0.y * b0.y), pack_bf16(t0.z * b0.z, t0.w * b0.w),
                         pack_bf16(t1.x * b1.x, t1.y * b1.y), pack_bf16(t1.z * b1.z, t1.w * b1.w)));
-    }
-    if (has_next) {
-      load_part(p, chn, hn, tb, c0, 3, R.v);
-      R.b = load_b(p, chn, hn, tid);
     }
     fence_async_smem();
     fence_before_sync();
@@ -459,12 +538,12 @@ tc_intra(ChunkParams p, int64_t n_items) {
           if (half == 0) {
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-              st_s16(A1, kmajor_off(i, c + 8 * u, 128),
+              st_s16(A1, kmaj(i, c + 8 * u, kA1Lbo),
                      make_uint4(pack_bf16(d[8 * u], d[8 * u + 1]), pack_bf16(d[8 * u + 2], d[8 * u + 3]),
                                 pack_bf16(d[8 * u + 4], d[8 * u + 5]),
                                 pack_bf16(d[8 * u + 6], d[8 * u + 7])));
           } else {
-            float* ut = reinterpret_cast<float*>(rec + Rec::UT);
+            float* ut = reinterpret_cast<float*>(B2);  // staged in the record's layout
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4)
               *reinterpret_cast<float4*>(ut + (((c >> 2) + q4) * 64 + i) * 4) =
@@ -477,17 +556,19 @@ tc_intra(ChunkParams p, int64_t n_items) {
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    // [W ; Qp] to the record in one bulk copy; its completion is awaited
-    // before A1 is rewritten by the next item
-    if (tid == 0) {
-      bulk_s2g(rec + Rec::AW, A1, 128 * 128 * 2);
+    // [W ; Qp] to the record's unpadded layout, one bulk copy per 8-channel
+    // group, each from its own thread, and U~ (staged in B2) in one; their
+    // reads are awaited before A1 and B2 are rewritten by the next item
+    if (tid < kAwCopy0 + 16) {
+      bulk_s2g(rec + Rec::AW + tid * 128 * 16, A1 + tid * kA1Lbo, 128 * 16);
+      bulk_commit();
+    } else if (tid == kUtCopy) {
+      bulk_s2g(rec + Rec::UT, B2, 64 * 128 * 4);
       bulk_commit();
     }
   }
-  if (tid == 0) {
-    if (!ok) flag(p.status, kFlagTimeout);
-    bulk_wait_all();
-  }
+  if (tid == 0 && !ok) flag(p.status, kFlagTimeout);
+  bulk_wait_all();  // every thread's own copies
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);

@@ -15,8 +15,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 // The tensor-core kernels move q, k, g, v, o and the states with 16-byte
 // vector accesses; other layouts take the fp32 CUDA-core path.
+// The tensor-core path: bf16, dk = dv = 128, 16-byte aligned buffers, and
+// token indices that fit the int32 coordinates of its tensor-map copies.
 bool use_tensor_cores(const kda_prefill_args* a) {
   return kHaveTensorCorePath && a->in_dtype == KDA_BF16 && a->dk == 128 && a->dv == 128 &&
+         a->total_tokens < ((int64_t)1 << 31) &&
          aligned16(a->q) && aligned16(a->k) && aligned16(a->v) && aligned16(a->g) &&
          aligned16(a->o) && aligned16(a->initial_state) && aligned16(a->final_state) &&
          aligned16(a->snapshots);
@@ -125,6 +128,7 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
   cp.dk = a->dk;
   cp.dv = a->dv;
   cp.max_chunks = L.max_chunks;
+  cp.total_tokens = a->total_tokens;
   cp.q = a->q;
   cp.k = a->k;
   cp.v = a->v;

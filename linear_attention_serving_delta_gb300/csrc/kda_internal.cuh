@@ -33,6 +33,7 @@ struct PlanParams {
 struct ChunkParams {
   int32_t num_seqs, H, dk, dv;
   int64_t max_chunks;
+  int64_t total_tokens;
   const void* q;
   const void* k;
   const void* v;

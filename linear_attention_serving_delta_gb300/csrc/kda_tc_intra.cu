@@ -22,6 +22,8 @@
 // math is stated in kda_tc_common.cuh.
 #include "kda_tc_common.cuh"
 
+#include <cuda.h>  // CUtensorMap and the enums of its encoder (fetched at run time)
+
 namespace kda {
 namespace tcp {
 namespace {
@@ -164,36 +166,57 @@ __device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ 
   __syncthreads();
 }
 
-// Raw rows of one work item (chunk, head) for this thread: 4 tokens (i0 + r)
-// x 8 channels of q, k, g, v, and the update logit of token `tid` (tid < 64).
-struct RawRows {
-  uint4 g[4], q[4], k[4], v[4];
-  float b;
+// The raw rows of an item are staged row-major ([64 tokens][128 channels]
+// bf16, 256 bytes a row) by one tensor-map copy per tensor (TMA engine: box
+// of 128 channels x 1 head x 64 tokens), inside operand tiles that are free
+// at that point: g in B1 and k in the A_kk tile (group A, once T diag(beta)
+// is formed), q and v in A1 (group B, once the record copies have read it).
+// Every thread reads its raw chunks into registers before the first barrier
+// of the item and writes operands over the staging only after the second.
+// Rows past the chunk's length hold other tokens (or zeros past the tensor's
+// end) and are masked where they are read.
+constexpr uint32_t kGStage = Smem::B1, kKStage = Smem::AKK, kQStage = Smem::A1,
+                   kVStage = Smem::A1 + 64 * 256;
+static_assert(16 * kB1Lbo >= 64 * 256 && 64 * kAs * 4 >= 64 * 256 && 16 * kA1Lbo >= 2 * 64 * 256,
+              "the staging fits the tiles it borrows");
+static_assert(kGStage % 128 == 0 && kKStage % 128 == 0 && kQStage % 128 == 0 && kVStage % 128 == 0,
+              "tensor-map copies land on 128-byte boundaries");
+constexpr uint32_t kRowsBytes = 64 * 256;  // one tensor's rows of an item
+
+// Tensor maps of q, k, v, g viewed as [T][H][128] bf16, box {128, 1, 64}
+struct RowMaps {
+  CUtensorMap g, q, k, v;
 };
 
-// 16-byte read-only global load kept at its place in the program (volatile),
-// so a prefetch is issued where it is written and not sunk to its first use
-__device__ __forceinline__ uint4 ld_nc16(const void* ptr) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr));
-  return v;
+// rows of one tensor, tokens tok0..tok0+63 of head h, into shared memory
+__device__ __forceinline__ void tma_rows(uint8_t* dst, const CUtensorMap* m, int h, int tok0,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(0), "r"(h), "r"(tok0), "r"(smem_u32(bar))
+      : "memory");
+}
+// the same rows into L2 only
+__device__ __forceinline__ void tma_rows_l2(const CUtensorMap* m, int h, int tok0) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(m), "r"(0), "r"(h),
+               "r"(tok0)
+               : "memory");
 }
 
-// This thread's rows of one of the four tensors (0 g, 1 q, 2 k, 3 v) of an
-// item; rows past the chunk's length read as zero.
-__device__ __forceinline__ void load_part(const ChunkParams& p, const Chunk& ch, int h, int i0, int c0,
-                                          int which, uint4* dst) {
-  const void* base = which == 0 ? p.g : which == 1 ? p.q : which == 2 ? p.k : p.v;
-  const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(base);
-  const int H = p.H, len = ch.len;
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int i = i0 + r;
-    const int64_t e = ((ch.tok0 + i) * H + h) * (int64_t)kD + c0;
-    dst[r] = i < len ? ld_nc16(src + e) : make_uint4(0, 0, 0, 0);
-  }
+// One staging group: the rows of two tensors of item (ch, h), both counted
+// on `bar`.  Issued by one thread.
+__device__ __forceinline__ void stage_group(uint8_t* sm, uint64_t* bar, const Chunk& ch, int h,
+                                            const CUtensorMap* t0, uint32_t s0, const CUtensorMap* t1,
+                                            uint32_t s1) {
+  mbar_arrive_expect_tx(bar, 2 * kRowsBytes);
+  tma_rows(sm + s0, t0, h, (int)ch.tok0, bar);
+  tma_rows(sm + s1, t1, h, (int)ch.tok0, bar);
+}
+
+// 16 bytes of a raw row in a staging: token i, channels c0..c0+7
+__device__ __forceinline__ uint4 raw16(const uint8_t* sm, uint32_t stage, int i, int c0) {
+  return *reinterpret_cast<const uint4*>(sm + stage + i * 256 + c0 * 2);
 }
 
 __device__ __forceinline__ float load_b(const ChunkParams& p, const Chunk& ch, int h, int tid) {
@@ -201,34 +224,15 @@ __device__ __forceinline__ float load_b(const ChunkParams& p, const Chunk& ch, i
   return (tid < 64 && tid < ch.len) ? __bfloat162float(gb[(ch.tok0 + tid) * p.H + h]) : 0.f;
 }
 
-__device__ __forceinline__ void load_rows(const ChunkParams& p, const Chunk& ch, int h, int i0, int c0,
-                                          int tid, RawRows& R) {
-  load_part(p, ch, h, i0, c0, 0, R.g);
-  load_part(p, ch, h, i0, c0, 1, R.q);
-  load_part(p, ch, h, i0, c0, 2, R.k);
-  load_part(p, ch, h, i0, c0, 3, R.v);
-  R.b = load_b(p, ch, h, tid);
-}
-
-// An item's rows into L2: one 256-byte row per thread (tensor tid / 64,
-// token tid % 64) as a bulk prefetch, which occupies neither registers nor
-// load slots of the issuing warp.
-__device__ __forceinline__ void prefetch_rows_l2(const ChunkParams& p, const Chunk& ch, int h, int tid) {
-  const int which = tid >> 6, i = tid & 63;
-  if (i < ch.len) {
-    const void* base = which == 0 ? p.g : which == 1 ? p.q : which == 2 ? p.k : p.v;
-    bulk_prefetch_l2(static_cast<const __nv_bfloat16*>(base) + ((ch.tok0 + i) * p.H + h) * (int64_t)kD, kD * 2);
-  }
-}
-
 // Persistent: two CTAs per SM walk the (chunk, head) items with stride
-// gridDim.x.  The rows of the next item are prefetched into L2 while this
-// item is computed, so its register loads hit L2.  TMEM and the mbarrier are
-// set up once per CTA.
+// gridDim.x.  The next item's rows are prefetched into L2 at the top of an
+// item and staged by bulk copies as soon as their tiles are free.  TMEM and
+// the mbarriers are set up once per CTA.
 __global__ void __launch_bounds__(kThreads, 2)
-tc_intra(ChunkParams p, int64_t n_items) {
+tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ __align__(8) uint64_t bar_mma;
+  __shared__ __align__(8) uint64_t bar_ga, bar_gb;  // staging groups A (g, k) and B (q, v)
   __shared__ uint32_t tmem_base;
 
   const int64_t stride = gridDim.x;
@@ -260,15 +264,27 @@ tc_intra(ChunkParams p, int64_t n_items) {
   if (warp == 0) tmem_alloc(&tmem_base, 256);
   if (tid == 0) {
     mbar_init(&bar_mma, 1);
+    mbar_init(&bar_ga, 1);
+    mbar_init(&bar_gb, 1);
     mbar_init_fence();
   }
+  __syncthreads();
 
-  // the pipeline: chunk entries of the current and the next item; the rows
-  // of the first item are brought into L2 here, each later item's during the
-  // item before it
+  // the pipeline: chunk entries of the current and the next item; the first
+  // item's rows are staged here (groups A and B), each later item's during
+  // the item before it
   Chunk ch = p.chunks[item / H];  // entries past the table's end have len 0
   Chunk ch_next = item + stride < n_items ? p.chunks[(item + stride) / H] : Chunk{};
-  prefetch_rows_l2(p, ch, (int)(item % H), tid);
+  {
+    const int h0 = (int)(item % H);
+    if (tid == 0) {
+      stage_group(sm, &bar_ga, ch, h0, &maps.g, kGStage, &maps.k, kKStage);
+      stage_group(sm, &bar_gb, ch, h0, &maps.q, kQStage, &maps.v, kVStage);
+    }
+  }
+  bool a_fly = true, b_fly = true;  // staging groups in flight, not yet awaited
+  uint32_t sph = 0;                 // the phase they complete
+  float bnext = load_b(p, ch, (int)(item % H), tid);
 
   fence_before_sync();
   __syncthreads();
@@ -280,30 +296,36 @@ tc_intra(ChunkParams p, int64_t n_items) {
     const int h = (int)(item % H);
     const int64_t cidx = item / H;
     const int len = ch.len;
-    if (len == 0) {  // past the end of the chunk table (uniform across the CTA)
-      if (item + stride < n_items) prefetch_rows_l2(p, ch_next, (int)((item + stride) % H), tid);
-      ch = ch_next;
-      ch_next = item + 2 * stride < n_items ? p.chunks[(item + 2 * stride) / H] : Chunk{};
-      continue;
-    }
+    // past the end of the chunk table (uniform across the CTA); every later
+    // item of this CTA is past it too
+    if (len == 0) break;
     uint8_t* rec = reinterpret_cast<uint8_t*>(p.inter) + ((size_t)cidx * H + h) * Rec::BYTES;
-    // this item's rows (L2 hits: prefetched during the previous item), and
-    // the next item's rows into L2
-    RawRows R;
-    load_rows(p, ch, h, i0, c0, tid, R);
-    if (item + stride < n_items) prefetch_rows_l2(p, ch_next, (int)((item + stride) % H), tid);
+    const bool has_next = item + stride < n_items;
+    const Chunk chn = ch_next;
+    const int hn = (int)((item + stride) % H);
+    const float bcur = bnext;
+    // the next item's rows into L2 now, so that their staging copies hit L2
+    if (has_next && tid < 4)
+      tma_rows_l2(tid == 0 ? &maps.g : tid == 1 ? &maps.k : tid == 2 ? &maps.q : &maps.v, hn,
+                  (int)chn.tok0);
+    // this item's g and k (group A) have landed; q and v (group B) may still fly
+    ok = mbar_wait(&bar_ga, sph, kWaitLimitNs);
+    a_fly = false;
 
     // ---- cumulative decay Gamma_i = prod_{m<=i} alpha_m, alpha = 1 / (1 + e^g)
     // (= exp(-softplus(g))): a product over this thread's 4 tokens, a scan
     // across the warp's 4 token blocks (lanes 8 apart), then across the token
     // quarters through shared memory (below)
     float Gm[4][8], qtot_own[8];
+    uint4 graw[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) graw[r] = raw16(sm, kGStage, i0 + r, c0);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       float run = 1.f;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const float a = i0 + r < len ? alpha_fast(bf16_at(R.g[r], j)) : 1.f;
+        const float a = i0 + r < len ? alpha_fast(bf16_at(graw[r], j)) : 1.f;
         run *= a;
         Gm[r][j] = run;
       }
@@ -325,13 +347,27 @@ tc_intra(ChunkParams p, int64_t n_items) {
           make_float4(qtot_own[4], qtot_own[5], qtot_own[6], qtot_own[7]);
     }
 
-    // ---- L2 norms per token: 8 channels here, 8 lanes, then the two channel halves
+    // ---- L2 norms per token: 8 channels here, 8 lanes, then the two channel
+    // halves.  The raw q, k, v chunks go to registers now: the operands are
+    // written over their stagings after the next two barriers.
+    ok = mbar_wait(&bar_gb, sph, kWaitLimitNs) && ok;
+    b_fly = false;
+    sph ^= 1;
+    uint4 qraw[4], kraw[4], vraw[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const bool live = i0 + r < len;
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      qraw[r] = live ? raw16(sm, kQStage, i0 + r, c0) : z;
+      kraw[r] = live ? raw16(sm, kKStage, i0 + r, c0) : z;
+      vraw[r] = live ? raw16(sm, kVStage, i0 + r, c0) : z;
+    }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       float sq = 0.f, sk = 0.f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float xq = bf16_at(R.q[r], j), xk = bf16_at(R.k[r], j);
+        const float xq = bf16_at(qraw[r], j), xk = bf16_at(kraw[r], j);
         sq += xq * xq;
         sk += xk * xk;
       }
@@ -345,10 +381,11 @@ tc_intra(ChunkParams p, int64_t n_items) {
         nrm[128 + hc * 64 + i0 + r] = sk;
       }
     }
-    if (tid < 64) beta[tid] = tid < len ? beta_of(R.b) : 0.f;
-    // the previous item's record copies must have finished reading A1 and B2
-    if (tid <= kUtCopy) bulk_wait_read_all();
-    __syncthreads();
+    if (tid < 64) beta[tid] = tid < len ? beta_of(bcur) : 0.f;
+    // the previous item's U~ copy must have read B2 before V is written there
+    if (tid == kUtCopy) bulk_wait_read_all();
+    ok = __syncthreads_and(ok);
+    if (!ok) break;
     if (tid < 64) {
       inv_q[tid] = inv_norm_of(nrm[tid] + nrm[64 + tid]);
       inv_k[tid] = inv_norm_of(nrm[128 + tid] + nrm[192 + tid]);
@@ -381,7 +418,7 @@ tc_intra(ChunkParams p, int64_t n_items) {
 
     // ---- V into B2 MN-major rows 128..255: the raw 16 bytes are one core-matrix row
 #pragma unroll
-    for (int r = 0; r < 4; ++r) st_s16(B2, mnmajor_off(128 + c0, i0 + r, kB2Sbo), R.v[r]);
+    for (int r = 0; r < 4; ++r) st_s16(B2, mnmajor_off(128 + c0, i0 + r, kB2Sbo), vraw[r]);
 
     // ---- operands Kp, Qp (A1), Kn (B1), Kp (B2 MN-major rows 0-127), Kr
     // (staged MN-major in the A_kk tile for the record's AK)
@@ -390,11 +427,12 @@ tc_intra(ChunkParams p, int64_t n_items) {
     for (int r = 0; r < 4; ++r) {
       const int i = i0 + r;
       const float ik = inv_k[i], iq = inv_q[i];
+      const uint4 qr = qraw[r], kr = kraw[r];
       float kp[8], qp[8], kn[8], kx[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float kh = bf16_at(R.k[r], j) * ik;
-        const float qh = bf16_at(R.q[r], j) * iq;
+        const float kh = bf16_at(kr, j) * ik;
+        const float qh = bf16_at(qr, j) * iq;
         const float gam = Gm[r][j];
         kp[j] = kh * gam;
         qp[j] = qh * gam;
@@ -420,9 +458,6 @@ tc_intra(ChunkParams p, int64_t n_items) {
       *reinterpret_cast<float4*>(gl) = make_float4(GLm[0], GLm[1], GLm[2], GLm[3]);
       *reinterpret_cast<float4*>(gl + 4) = make_float4(GLm[4], GLm[5], GLm[6], GLm[7]);
     }
-
-    ch = ch_next;
-    ch_next = item + 2 * stride < n_items ? p.chunks[(item + 2 * stride) / H] : Chunk{};
 
     fence_async_smem();
     fence_before_sync();
@@ -510,6 +545,13 @@ tc_intra(ChunkParams p, int64_t n_items) {
     __syncthreads();
     fence_after_sync();
 
+    // T is consumed (B1) and the A_kk tile free: the next item's g and k
+    // (group A) are staged now
+    if (has_next) {
+      if (tid == 0) stage_group(sm, &bar_ga, chn, hn, &maps.g, kGStage, &maps.k, kKStage);
+      bnext = load_b(p, chn, hn, tid);
+      a_fly = true;
+    }
     // ---- MMA 2: [W | U~] = Tb [Kp | V]   (M=64, N=256, K=64)
     if (tid == 0) {
       const uint32_t id = idesc_bf16(64, 256, 0, 1);  // B2 is MN-major
@@ -566,7 +608,19 @@ tc_intra(ChunkParams p, int64_t n_items) {
       bulk_s2g(rec + Rec::UT, B2, 64 * 128 * 4);
       bulk_commit();
     }
+    // once they have read A1, the next item's q and v (group B)
+    if (tid < kAwCopy0 + 16) bulk_wait_read_all();
+    __syncthreads();
+    if (has_next) {
+      if (tid == 0) stage_group(sm, &bar_gb, chn, hn, &maps.q, kQStage, &maps.v, kVStage);
+      b_fly = true;
+    }
+    ch = ch_next;
+    ch_next = item + 2 * stride < n_items ? p.chunks[(item + 2 * stride) / H] : Chunk{};
   }
+  // no staging copy is left in flight when the CTA exits (waits bounded)
+  if (a_fly) mbar_wait(&bar_ga, sph, kWaitLimitNs);
+  if (b_fly) mbar_wait(&bar_gb, sph, kWaitLimitNs);
   if (tid == 0 && !ok) flag(p.status, kFlagTimeout);
   bulk_wait_all();  // every thread's own copies
   fence_before_sync();
@@ -574,19 +628,54 @@ tc_intra(ChunkParams p, int64_t n_items) {
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+// cuTensorMapEncodeTiled, fetched from the driver once
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// [T][H][128] bf16 rows, box {128 channels, 1 head, 64 tokens}, zero fill past T
+bool encode_rows(CUtensorMap* m, const void* base, int H, int64_t T) {
+  const EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {kD, (cuuint64_t)H, (cuuint64_t)T};
+  const cuuint64_t strides[2] = {kD * 2, (cuuint64_t)H * kD * 2};
+  const cuuint32_t box[3] = {kD, 1, 64};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(tc_intra, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)Smem::BYTES);
-  if (e != cudaSuccess || p.max_chunks == 0) return e;
+  if (e != cudaSuccess || p.max_chunks == 0 || p.total_tokens == 0) return e;
+  RowMaps maps;
+  if (!encode_rows(&maps.g, p.g, p.H, p.total_tokens) || !encode_rows(&maps.q, p.q, p.H, p.total_tokens) ||
+      !encode_rows(&maps.k, p.k, p.H, p.total_tokens) || !encode_rows(&maps.v, p.v, p.H, p.total_tokens))
+    return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int64_t n_items = p.max_chunks * (int64_t)p.H;
   const int64_t grid = n_items < 2 * (int64_t)sms ? n_items : 2 * (int64_t)sms;
-  tc_intra<<<(unsigned)grid, kThreads, Smem::BYTES, stream>>>(p, n_items);
+  tc_intra<<<(unsigned)grid, kThreads, Smem::BYTES, stream>>>(p, n_items, maps);
   return cudaGetLastError();
 }
 

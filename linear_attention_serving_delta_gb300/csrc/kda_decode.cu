@@ -156,7 +156,9 @@ decode_step(kda_decode_args a) {
 // kStages shared-memory slots is filled by 1-D bulk copies (TMA engine) of
 // each item's 64 KB state plus its q, k, g, v rows, kStages items ahead, so
 // HBM reads of the next states overlap the arithmetic and the write-back of
-// the current one.  The state is written back with 16-byte stores.
+// the current one.  The updated state is written into its slot and leaves
+// through one 64 KB bulk copy (TMA engine); the slot is refilled once that
+// copy has read it.
 constexpr int kStages = 3;
 constexpr int kRingThreads = 256;
 constexpr uint32_t kStateBytes = 128 * 128 * 4;
@@ -267,13 +269,17 @@ decode_ring(kda_decode_args a, int64_t n_items) {
         sc[buf][1] = qk;
       }
     }
-    if (!__syncthreads_and(ok)) break;
-    if (!valid) {
-      __syncthreads();  // every thread has read valid_flag[st] before the slot is refilled
-      if (tid == 0 && k + kStages < n_local)
-        ring_issue<TIn>(a, stage, &full[st], &valid_flag[st], item + kStages * stride);
-      continue;
+    // the previous item's state copy has read its slot: refill that slot
+    if (tid == 0 && k >= 1) {
+      tc::bulk_wait_read_all();
+      if (k - 1 + kStages < n_local) {
+        const int pst = (int)((k - 1) % kStages);
+        ring_issue<TIn>(a, sm + pst * Ring<TIn>::STAGE, &full[pst], &valid_flag[pst],
+                        item - stride + kStages * stride);
+      }
     }
+    if (!__syncthreads_and(ok)) break;
+    if (!valid) continue;  // its slot is refilled at the top of the next item
     // retention and the two reductions over key channels; rows warp + 8i
     const float* S = reinterpret_cast<const float*>(stage);
     float4 s[16];
@@ -290,9 +296,6 @@ decode_ring(kda_decode_args a, int64_t n_items) {
     *reinterpret_cast<float4*>(&red_p[warp][4 * lane]) = pp;
     *reinterpret_cast<float4*>(&red_o[warp][4 * lane]) = po;
     __syncthreads();
-    // the slot has been read: refill it kStages items ahead
-    if (tid == 0 && k + kStages < n_local)
-      ring_issue<TIn>(a, stage, &full[st], &valid_flag[st], item + kStages * stride);
     float4 p = make_float4(0.f, 0.f, 0.f, 0.f), oq = p;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
@@ -308,13 +311,20 @@ decode_ring(kda_decode_args a, int64_t n_items) {
     const int row = (int)(item / H), h = (int)(item % H);
     const int slot = a.state_slots ? a.state_slots[row] : row;
     float* Sg = a.state + ((size_t)slot * H + h) * 128 * 128;
+    float* Ss = reinterpret_cast<float*>(stage);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int r = warp + 8 * i;
       const float k_r = kn[buf][r];
       float4 x = s[i];
       x.x += k_r * u.x; x.y += k_r * u.y; x.z += k_r * u.z; x.w += k_r * u.w;
-      reinterpret_cast<float4*>(Sg + r * 128)[lane] = x;
+      reinterpret_cast<float4*>(Ss + r * 128)[lane] = x;
+    }
+    tc::fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc::bulk_s2g(Sg, Ss, kStateBytes);
+      tc::bulk_commit();
     }
     if (warp == 0) {
       const float qk = sc[buf][1], scl = a.scale;
@@ -326,6 +336,7 @@ decode_ring(kda_decode_args a, int64_t n_items) {
       st_out(o, ob + 3, scl * (oq.w + qk * u.w));
     }
   }
+  if (tid == 0) tc::bulk_wait_all();
 }
 
 template <typename TIn>

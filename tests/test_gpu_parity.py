@@ -189,6 +189,33 @@ def test_prefill_varlen_full():
     assert_close(gpu, ref, TOL["bf16"], "varlen_8")
 
 
+@pytest.mark.slow
+def test_prefill_1m_sampled(oracle_mod):
+    """The million-token prefill (B=1, H=32, T=2^20, dk=dv=128, bf16, snapshots
+    every 65536 tokens) at full size on the device; o, the 16 snapshots and
+    the final state of four of the 32 heads are checked against the oracle
+    (the oracle's cost is what bounds the sample)."""
+    w = W.WORKLOADS["prefill_1m"]
+    inp = W.prefill_inputs(w, device="cuda", gen_device="cuda")
+    cu = inp["cu_seqlens"].cpu()
+    p = kda.Prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["b"], inp["cu_seqlens"],
+                    snapshot_interval=w.snapshot_interval, host_cu_seqlens=cu)
+    p.run()
+    torch.cuda.synchronize()
+    assert p.device_status() == 0
+    heads = slice(8, 12)
+    sample = {x: host(inp[x][:, heads]) for x in "qkvgb"}
+    T = int(cu[-1])
+    sp, cs = oracle_mod.snapshot_positions([T], w.snapshot_interval)
+    assert len(sp) == 16
+    ref = oracle_mod.prefill(sample["q"], sample["k"], sample["v"], sample["g"], sample["b"],
+                             cu.numpy(), snap_pos=sp, cu_snap=cs)
+    gpu = (host(p.o[:, heads]), host(p.final_state[:, heads]), host(p.snapshot_view[:, heads]))
+    del inp, p
+    torch.cuda.empty_cache()
+    assert_close(gpu, ref, TOL["bf16"], "prefill_1m heads 8-11")
+
+
 def test_prefill_empty_sequences_keep_initial_state():
     inp = make_inputs([0, 5, 0], 2, 32, 32, "f32", 41, s0_std=0.5)
     gpu, ref = run_both(inp, "f32")

@@ -15,11 +15,11 @@
 //   MMA 1 (M=128, N=64, K=128):  [A_kk ; A_qk] = [Kp ; Qp] Kn^T  -> TMEM
 //   CUDA cores: T = (I + A_kk)^{-1}, two-level blocked inverse
 //   MMA 2 (M=64, N=256, K=64):   [W | U~] = T diag(beta) [Kp | V] -> TMEM
-// and the record of kda_tc_common.cuh is written with bulk copies (TMA
-// engine) out of shared memory: AW and AK one per 8-channel group (dropping
-// the padding), A_qk and U~ each in one, staged in tiles that are free at
-// that point.  The load/store unit then carries only the raw-row loads.  The
-// math is stated in kda_tc_common.cuh.
+// and the record of kda_tc_common.cuh is written: AW and AK with bulk copies
+// (TMA engine) out of shared memory, one per 8-channel group (dropping the
+// padding), A_qk with one, each staged in a tile that is free at that point;
+// U~ and Gamma_L with 16-byte stores from registers.  The math is stated in
+// kda_tc_common.cuh.
 #include "kda_tc_common.cuh"
 
 #include <cuda.h>  // CUtensorMap and the enums of its encoder (fetched at run time)
@@ -40,7 +40,6 @@ constexpr uint32_t kB2Sbo = 8 * 128 + 16;   // B2 MN-major (n, token): stride be
 constexpr uint32_t kAkStage = 8 * 128 + 16; // Kr^T staged for its record copy: stride between 8-channel groups
 // threads that issue the record's bulk copies (each waits for its own)
 constexpr int kAwCopy0 = 0;    // AW: threads 0-15, one 8-channel group each
-constexpr int kUtCopy = 16;    // U~
 constexpr int kAkCopy0 = 32;   // AK: threads 32-47, one 8-channel group each
 constexpr int kAqCopy = 64;    // A_qk
 
@@ -170,14 +169,14 @@ __device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ 
 // bf16, 256 bytes a row) by one tensor-map copy per tensor (TMA engine: box
 // of 128 channels x 1 head x 64 tokens), inside operand tiles that are free
 // at that point: g in B1 and k in the A_kk tile (group A, once T diag(beta)
-// is formed), q and v in A1 (group B, once the record copies have read it).
-// Every thread reads its raw chunks into registers before the first barrier
-// of the item and writes operands over the staging only after the second.
-// Rows past the chunk's length hold other tokens (or zeros past the tensor's
-// end) and are masked where they are read.
-constexpr uint32_t kGStage = Smem::B1, kKStage = Smem::AKK, kQStage = Smem::A1,
-                   kVStage = Smem::A1 + 64 * 256;
-static_assert(16 * kB1Lbo >= 64 * 256 && 64 * kAs * 4 >= 64 * 256 && 16 * kA1Lbo >= 2 * 64 * 256,
+// is formed), q and v in B2 (group B, once MMA 2 has read it).  Every thread
+// reads its raw chunks into registers before the first barrier of the item
+// and writes operands over the staging only after the second.  Rows past the
+// chunk's length hold other tokens (or zeros past the tensor's end) and are
+// masked where they are read.
+constexpr uint32_t kGStage = Smem::B1, kKStage = Smem::AKK, kQStage = Smem::B2,
+                   kVStage = Smem::B2 + 64 * 256;
+static_assert(16 * kB1Lbo >= 64 * 256 && 64 * kAs * 4 >= 64 * 256 && 32 * kB2Sbo >= 2 * 64 * 256,
               "the staging fits the tiles it borrows");
 static_assert(kGStage % 128 == 0 && kKStage % 128 == 0 && kQStage % 128 == 0 && kVStage % 128 == 0,
               "tensor-map copies land on 128-byte boundaries");
@@ -382,8 +381,8 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
       }
     }
     if (tid < 64) beta[tid] = tid < len ? beta_of(bcur) : 0.f;
-    // the previous item's U~ copy must have read B2 before V is written there
-    if (tid == kUtCopy) bulk_wait_read_all();
+    // the previous item's record copies must have read A1 before it is rewritten
+    if (tid < kAwCopy0 + 16) bulk_wait_read_all();
     ok = __syncthreads_and(ok);
     if (!ok) break;
     if (tid < 64) {
@@ -564,6 +563,11 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     ok = __syncthreads_and(mbar_wait(&bar_mma, 1, kWaitLimitNs));
     fence_after_sync();
     if (!ok) break;
+    // MMA 2 has read B2: the next item's q and v (group B) are staged there now
+    if (has_next) {
+      if (tid == 0) stage_group(sm, &bar_gb, chn, hn, &maps.q, kQStage, &maps.v, kVStage);
+      b_fly = true;
+    }
     {
       // M=64 accumulator: row r sits in TMEM lane (r/16)*32 + r%16; warps 0-3
       // take W (columns 0-127), warps 4-7 take U~ (columns 128-255)
@@ -585,7 +589,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
                                 pack_bf16(d[8 * u + 4], d[8 * u + 5]),
                                 pack_bf16(d[8 * u + 6], d[8 * u + 7])));
           } else {
-            float* ut = reinterpret_cast<float*>(B2);  // staged in the record's layout
+            float* ut = reinterpret_cast<float*>(rec + Rec::UT);
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4)
               *reinterpret_cast<float4*>(ut + (((c >> 2) + q4) * 64 + i) * 4) =
@@ -599,21 +603,11 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     __syncthreads();
     fence_after_sync();
     // [W ; Qp] to the record's unpadded layout, one bulk copy per 8-channel
-    // group, each from its own thread, and U~ (staged in B2) in one; their
-    // reads are awaited before A1 and B2 are rewritten by the next item
+    // group, each from its own thread; their reads are awaited before A1 is
+    // rewritten by the next item
     if (tid < kAwCopy0 + 16) {
       bulk_s2g(rec + Rec::AW + tid * 128 * 16, A1 + tid * kA1Lbo, 128 * 16);
       bulk_commit();
-    } else if (tid == kUtCopy) {
-      bulk_s2g(rec + Rec::UT, B2, 64 * 128 * 4);
-      bulk_commit();
-    }
-    // once they have read A1, the next item's q and v (group B)
-    if (tid < kAwCopy0 + 16) bulk_wait_read_all();
-    __syncthreads();
-    if (has_next) {
-      if (tid == 0) stage_group(sm, &bar_gb, chn, hn, &maps.q, kQStage, &maps.v, kVStage);
-      b_fly = true;
     }
     ch = ch_next;
     ch_next = item + 2 * stride < n_items ? p.chunks[(item + 2 * stride) / H] : Chunk{};

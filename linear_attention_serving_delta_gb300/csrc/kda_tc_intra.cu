@@ -37,6 +37,7 @@ constexpr int kTs = 64;  // row stride (floats) of T
 constexpr uint32_t kA1Lbo = 128 * 16 + 16;  // A1 K-major, R=128: stride between 8-channel groups
 constexpr uint32_t kB1Lbo = 64 * 16 + 16;   // B1 K-major, R=64
 constexpr uint32_t kB2Sbo = 8 * 128 + 16;   // B2 MN-major (n, token): stride between 8-n groups
+constexpr uint32_t kA2Lbo = 64 * 16 + 16;   // A2 (T diag(beta)) K-major, R=64
 constexpr uint32_t kAkStage = 8 * 128 + 16; // Kr^T staged for its record copy: stride between 8-channel groups
 // threads that issue the record's bulk copies (each waits for its own)
 constexpr int kAwCopy0 = 0;    // AW: threads 0-15, one 8-channel group each
@@ -48,7 +49,7 @@ struct Smem {
   static constexpr uint32_t B1 = A1 + 16 * kA1Lbo;     // Kn, K=128; then T fp32 [64][64]
   static constexpr uint32_t B2 = B1 + 16 * kB1Lbo;     // [Kp | V] MN-major, N=256 (32 groups), K=64
   static constexpr uint32_t A2 = B2 + 32 * kB2Sbo;     // inverse scratch; then Tb, R=64, K=64
-  static constexpr uint32_t AKK = A2 + 64 * 64 * 2;    // fp32 [64][kAs]
+  static constexpr uint32_t AKK = A2 + 8 * kA2Lbo;     // fp32 [64][kAs]
   // inv_q, inv_k, beta [64]; norm partials [q/k][channel half][64];
   // decay totals of each token quarter [4][128]
   static constexpr uint32_t MISC = AKK + 64 * kAs * 4;
@@ -56,6 +57,7 @@ struct Smem {
 };
 static_assert(Smem::B1 % 16 == 0 && Smem::B2 % 16 == 0 && Smem::A2 % 16 == 0 && Smem::AKK % 16 == 0,
               "operand tiles and float4 arrays are 16-byte aligned");
+static_assert(8 * kA2Lbo >= 64 * 64 * 2, "A2 holds the unpadded A_qk staging too");
 static_assert(16 * kB1Lbo >= 64 * kTs * 4, "T fits in the Kn tile");
 static_assert(16 * kAkStage <= 64 * kAs * 4, "the Kr^T staging fits in the A_kk tile");
 static_assert(32 * kB2Sbo >= 64 * 128 * 4, "the U~ staging fits in the B2 tile");
@@ -530,12 +532,12 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int idx = tid + kThreads * t;
-      const int i = idx & 63, jb = idx >> 6;
+      const int i = idx >> 3, jb = idx & 7;  // lanes along a row of T: few bank conflicts
       const float4 t0 = *reinterpret_cast<const float4*>(TT + i * kTs + 8 * jb);
       const float4 t1 = *reinterpret_cast<const float4*>(TT + i * kTs + 8 * jb + 4);
       const float4 b0 = *reinterpret_cast<const float4*>(beta + 8 * jb);
       const float4 b1 = *reinterpret_cast<const float4*>(beta + 8 * jb + 4);
-      st_s16(A2, kmajor_off(i, 8 * jb, 64),
+      st_s16(A2, kmaj(i, 8 * jb, kA2Lbo),
              make_uint4(pack_bf16(t0.x * b0.x, t0.y * b0.y), pack_bf16(t0.z * b0.z, t0.w * b0.w),
                         pack_bf16(t1.x * b1.x, t1.y * b1.y), pack_bf16(t1.z * b1.z, t1.w * b1.w)));
     }
@@ -556,7 +558,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
       const uint32_t id = idesc_bf16(64, 256, 0, 1);  // B2 is MN-major
 #pragma unroll
       for (int s = 0; s < 4; ++s)
-        mma_bf16(tmem, sdesc(smem_u32(A2) + s * 2 * 64 * 16, 64 * 16, 128),
+        mma_bf16(tmem, sdesc(smem_u32(A2) + s * 2 * kA2Lbo, kA2Lbo, 128),
                  sdesc(smem_u32(B2) + s * 256, 128, kB2Sbo), id, s > 0);
       mma_commit(&bar_mma);
     }

@@ -152,15 +152,24 @@ decode_step(kda_decode_args a) {
 }
 
 // ------------------------------------------------------------ dk = dv = 128
-// Persistent variant: one CTA per SM walks (row, head) items; a ring of
+// Persistent variant: one CTA per SM walks (row, head) items.  A ring of
 // kStages shared-memory slots is filled by 1-D bulk copies (TMA engine) of
-// each item's 64 KB state plus its q, k, g, v rows, kStages items ahead, so
-// HBM reads of the next states overlap the arithmetic and the write-back of
-// the current one.  The updated state is written into its slot and leaves
-// through one 64 KB bulk copy (TMA engine); the slot is refilled once that
-// copy has read it.
+// each item's 64 KB state plus its q, k, g, v rows, kStages items ahead.
+// Warps 0-7 compute; warp 8 is the producer: once the compute warps have
+// written an item's updated state into its slot, it sends the state back to
+// HBM with one 64 KB bulk copy, waits for that copy to read the slot and
+// refills it with the item kStages further on.  No compute warp waits on a
+// copy.
+//
+// The compute warps need no token-preparation phase: with raw q, k,
+// p = S'^T k^ = ik (S'^T k) and S'^T q^ = iq (S'^T q) (ik, iq the inverse
+// norms), so each warp reads q, k and g of its own 16 key channels straight
+// from the slot, and the norms' partial sums travel with the reduction
+// partials through the one barrier of the item.
 constexpr int kStages = 3;
-constexpr int kRingThreads = 256;
+constexpr int kRingThreads = 256;            // compute warps 0-7
+constexpr int kRingAllThreads = kRingThreads + 32;  // + the producer warp
+constexpr int kComputeBarrier = 1;           // named barrier of warps 0-7
 constexpr uint32_t kStateBytes = 128 * 128 * 4;
 
 template <typename TIn>
@@ -172,6 +181,20 @@ struct Ring {
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+
+// barrier.red.and over the `n` threads of named barrier `id`
+__device__ __forceinline__ bool bar_and(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q, p;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
 }
 
 template <typename TIn>
@@ -197,18 +220,15 @@ __device__ __forceinline__ void ring_issue(const kda_decode_args& a, uint8_t* st
 }
 
 template <typename TIn>
-__global__ void __launch_bounds__(kRingThreads, 1)
+__global__ void __launch_bounds__(kRingAllThreads, 1)
 decode_ring(kda_decode_args a, int64_t n_items) {
   extern __shared__ __align__(128) uint8_t sm[];
-  __shared__ __align__(8) uint64_t full[kStages];
+  __shared__ __align__(8) uint64_t full[kStages];  // slot loaded
+  __shared__ __align__(8) uint64_t done[kStages];  // slot's state updated by warps 0-7
   __shared__ int32_t valid_flag[kStages];
-  __shared__ __align__(16) float qn[2][128];
-  __shared__ __align__(16) float kn[2][128];
-  __shared__ __align__(16) float al[2][128];
-  __shared__ __align__(16) float vv[2][128];
-  __shared__ float sc[2][2];
-  __shared__ __align__(16) float red_p[8][128];
-  __shared__ __align__(16) float red_o[8][128];
+  __shared__ __align__(16) float red_p[2][8][128];
+  __shared__ __align__(16) float red_o[2][8][128];
+  __shared__ __align__(16) float part[2][8][4];    // per warp: sum q^2, sum k^2, sum q k
   constexpr uint32_t ROW = Ring<TIn>::ROW;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.num_heads;
@@ -216,18 +236,42 @@ decode_ring(kda_decode_args a, int64_t n_items) {
   const int64_t n_local = first < n_items ? (n_items - first + stride - 1) / stride : 0;
 
   if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) tc::mbar_init(&full[st], 1);
+    for (int st = 0; st < kStages; ++st) {
+      tc::mbar_init(&full[st], 1);
+      tc::mbar_init(&done[st], kRingThreads);
+    }
     tc::mbar_init_fence();
   }
   __syncthreads();
-  if (tid == 0)
-    for (int64_t k = 0; k < kStages && k < n_local; ++k)
-      ring_issue<TIn>(a, sm + k * Ring<TIn>::STAGE, &full[k], &valid_flag[k], first + k * stride);
 
-  // the update logit of the next item, prefetched one item ahead by lane 0 of warp 0
+  if (warp == 8) {
+    // ---- producer
+    if (lane == 0) {
+      for (int64_t k = 0; k < kStages && k < n_local; ++k)
+        ring_issue<TIn>(a, sm + k * Ring<TIn>::STAGE, &full[k], &valid_flag[k], first + k * stride);
+      for (int64_t k = 0; k < n_local; ++k) {
+        const int st = (int)(k % kStages);
+        uint8_t* stage = sm + st * Ring<TIn>::STAGE;
+        if (!tc::mbar_wait(&done[st], (uint32_t)((k / kStages) & 1), tc::kWaitLimitNs)) break;
+        const int64_t item = first + k * stride;
+        if (valid_flag[st]) {
+          const int row = (int)(item / H), h = (int)(item % H);
+          const int slot = a.state_slots ? a.state_slots[row] : row;
+          tc::bulk_s2g(a.state + ((size_t)slot * H + h) * 128 * 128, stage, kStateBytes);
+          tc::bulk_commit();
+          tc::bulk_wait_read_all();
+        }
+        if (k + kStages < n_local)
+          ring_issue<TIn>(a, stage, &full[st], &valid_flag[st], item + kStages * stride);
+      }
+      tc::bulk_wait_all();
+    }
+    return;
+  }
+
+  // ---- compute warps 0-7; warp w owns key channels (rows) w + 8 i, i < 16
   const TIn* gb = static_cast<const TIn*>(a.b);
-  float b_next = (tid == 0 && n_local > 0) ? ld_in(gb, first) : 0.f;
-
+  float b_next = n_local > 0 ? ld_in(gb, first) : 0.f;
   for (int64_t k = 0; k < n_local; ++k) {
     const int st = (int)(k % kStages);
     uint8_t* stage = sm + st * Ring<TIn>::STAGE;
@@ -235,52 +279,30 @@ decode_ring(kda_decode_args a, int64_t n_items) {
     const int buf = (int)(k & 1);
     bool ok = tc::mbar_wait(&full[st], (uint32_t)((k / kStages) & 1), tc::kWaitLimitNs);
     const bool valid = valid_flag[st] != 0;
-    float b_cur = b_next;
-    if (tid == 0 && k + 1 < n_local) b_next = ld_in(gb, item + stride);
-    if (ok && valid && warp == 0) {
-      // token preparation: q^, k^, alpha, beta, q^.k^
-      const TIn* rq = reinterpret_cast<const TIn*>(stage + kStateBytes);
-      const TIn* rk = reinterpret_cast<const TIn*>(stage + kStateBytes + ROW);
-      const TIn* rg = reinterpret_cast<const TIn*>(stage + kStateBytes + 2 * ROW);
-      const TIn* rv = reinterpret_cast<const TIn*>(stage + kStateBytes + 3 * ROW);
-      float xq[4], xk[4], sq = 0.f, sk = 0.f;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int c = lane + 32 * t;
-        xq[t] = ld_in(rq, c);
-        xk[t] = ld_in(rk, c);
-        sq += xq[t] * xq[t];
-        sk += xk[t] * xk[t];
-        al[buf][c] = expf(log_alpha_of(ld_in(rg, c)));
-        vv[buf][c] = ld_in(rv, c);
-      }
-      const float iq = inv_norm_of(warp_sum(sq)), ik = inv_norm_of(warp_sum(sk));
-      float qk = 0.f;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int c = lane + 32 * t;
-        qn[buf][c] = xq[t] * iq;
-        kn[buf][c] = xk[t] * ik;
-        qk += (xq[t] * iq) * (xk[t] * ik);
-      }
-      qk = warp_sum(qk);
-      if (lane == 0) {
-        sc[buf][0] = beta_of(b_cur);
-        sc[buf][1] = qk;
-      }
+    const float b_cur = b_next;
+    if (k + 1 < n_local) b_next = ld_in(gb, item + stride);
+    if (!valid) {  // uniform: nothing to compute, the slot is handed back
+      mbar_arrive(&done[st]);
+      if (!bar_and(kComputeBarrier, kRingThreads, ok)) break;
+      continue;
     }
-    // the previous item's state copy has read its slot: refill that slot
-    if (tid == 0 && k >= 1) {
-      tc::bulk_wait_read_all();
-      if (k - 1 + kStages < n_local) {
-        const int pst = (int)((k - 1) % kStages);
-        ring_issue<TIn>(a, sm + pst * Ring<TIn>::STAGE, &full[pst], &valid_flag[pst],
-                        item - stride + kStages * stride);
-      }
+    const TIn* rq = reinterpret_cast<const TIn*>(stage + kStateBytes);
+    const TIn* rk = reinterpret_cast<const TIn*>(stage + kStateBytes + ROW);
+    const TIn* rg = reinterpret_cast<const TIn*>(stage + kStateBytes + 2 * ROW);
+    const TIn* rv = reinterpret_cast<const TIn*>(stage + kStateBytes + 3 * ROW);
+    // this warp's 16 rows: lane i < 16 holds raw q, k and alpha of row warp + 8 i
+    float xq = 0.f, xk = 0.f, xa = 0.f;
+    if (lane < 16) {
+      const int r = warp + 8 * lane;
+      xq = ld_in(rq, r);
+      xk = ld_in(rk, r);
+      xa = expf(log_alpha_of(ld_in(rg, r)));
     }
-    if (!__syncthreads_and(ok)) break;
-    if (!valid) continue;  // its slot is refilled at the top of the next item
-    // retention and the two reductions over key channels; rows warp + 8i
+    {
+      const float sq = warp_sum(xq * xq), sk = warp_sum(xk * xk), sqk = warp_sum(xq * xk);
+      if (lane == 0) *reinterpret_cast<float4*>(&part[buf][warp][0]) = make_float4(sq, sk, sqk, 0.f);
+    }
+    // retention and the two reductions over this warp's rows (raw q, k)
     const float* S = reinterpret_cast<const float*>(stage);
     float4 s[16];
     float4 pp = make_float4(0.f, 0.f, 0.f, 0.f), po = pp;
@@ -288,55 +310,57 @@ decode_ring(kda_decode_args a, int64_t n_items) {
     for (int i = 0; i < 16; ++i) {
       const int r = warp + 8 * i;
       s[i] = reinterpret_cast<const float4*>(S + r * 128)[lane];
-      const float a_r = al[buf][r], k_r = kn[buf][r], q_r = qn[buf][r];
+      const float a_r = __shfl_sync(0xffffffffu, xa, i), k_r = __shfl_sync(0xffffffffu, xk, i),
+                  q_r = __shfl_sync(0xffffffffu, xq, i);
       s[i].x *= a_r; s[i].y *= a_r; s[i].z *= a_r; s[i].w *= a_r;
       pp.x += k_r * s[i].x; pp.y += k_r * s[i].y; pp.z += k_r * s[i].z; pp.w += k_r * s[i].w;
       po.x += q_r * s[i].x; po.y += q_r * s[i].y; po.z += q_r * s[i].z; po.w += q_r * s[i].w;
     }
-    *reinterpret_cast<float4*>(&red_p[warp][4 * lane]) = pp;
-    *reinterpret_cast<float4*>(&red_o[warp][4 * lane]) = po;
-    __syncthreads();
+    *reinterpret_cast<float4*>(&red_p[buf][warp][4 * lane]) = pp;
+    *reinterpret_cast<float4*>(&red_o[buf][warp][4 * lane]) = po;
+    if (!bar_and(kComputeBarrier, kRingThreads, ok)) break;
+    float sq = 0.f, sk = 0.f, sqk = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const float4 x = *reinterpret_cast<const float4*>(&part[buf][w][0]);
+      sq += x.x; sk += x.y; sqk += x.z;
+    }
+    const float iq = inv_norm_of(sq), ik = inv_norm_of(sk), qk = sqk * iq * ik;
     float4 p = make_float4(0.f, 0.f, 0.f, 0.f), oq = p;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-      const float4 x = *reinterpret_cast<const float4*>(&red_p[w][4 * lane]);
-      const float4 y = *reinterpret_cast<const float4*>(&red_o[w][4 * lane]);
+      const float4 x = *reinterpret_cast<const float4*>(&red_p[buf][w][4 * lane]);
+      const float4 y = *reinterpret_cast<const float4*>(&red_o[buf][w][4 * lane]);
       p.x += x.x; p.y += x.y; p.z += x.z; p.w += x.w;
       oq.x += y.x; oq.y += y.y; oq.z += y.z; oq.w += y.w;
     }
-    const float beta = sc[buf][0];
-    const float4 vq = *reinterpret_cast<const float4*>(&vv[buf][4 * lane]);
-    const float4 u = make_float4(beta * (vq.x - p.x), beta * (vq.y - p.y), beta * (vq.z - p.z),
-                                 beta * (vq.w - p.w));
-    const int row = (int)(item / H), h = (int)(item % H);
-    const int slot = a.state_slots ? a.state_slots[row] : row;
-    float* Sg = a.state + ((size_t)slot * H + h) * 128 * 128;
+    const float beta = beta_of(b_cur);
+    const float4 u = make_float4(beta * (ld_in(rv, 4 * lane) - ik * p.x), beta * (ld_in(rv, 4 * lane + 1) - ik * p.y),
+                                 beta * (ld_in(rv, 4 * lane + 2) - ik * p.z), beta * (ld_in(rv, 4 * lane + 3) - ik * p.w));
+    // the updated state into the slot (each thread its own rows), then the
+    // producer sends it back
     float* Ss = reinterpret_cast<float*>(stage);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int r = warp + 8 * i;
-      const float k_r = kn[buf][r];
+      const float k_r = ik * __shfl_sync(0xffffffffu, xk, i);
       float4 x = s[i];
       x.x += k_r * u.x; x.y += k_r * u.y; x.z += k_r * u.z; x.w += k_r * u.w;
       reinterpret_cast<float4*>(Ss + r * 128)[lane] = x;
     }
     tc::fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      tc::bulk_s2g(Sg, Ss, kStateBytes);
-      tc::bulk_commit();
-    }
+    mbar_arrive(&done[st]);
     if (warp == 0) {
-      const float qk = sc[buf][1], scl = a.scale;
+      const float scl = a.scale;
+      const int row = (int)(item / H), h = (int)(item % H);
       TIn* o = static_cast<TIn*>(a.o);
       const int64_t ob = ((int64_t)row * H + h) * 128 + 4 * lane;
-      st_out(o, ob + 0, scl * (oq.x + qk * u.x));
-      st_out(o, ob + 1, scl * (oq.y + qk * u.y));
-      st_out(o, ob + 2, scl * (oq.z + qk * u.z));
-      st_out(o, ob + 3, scl * (oq.w + qk * u.w));
+      st_out(o, ob + 0, scl * (iq * oq.x + qk * u.x));
+      st_out(o, ob + 1, scl * (iq * oq.y + qk * u.y));
+      st_out(o, ob + 2, scl * (iq * oq.z + qk * u.z));
+      st_out(o, ob + 3, scl * (iq * oq.w + qk * u.w));
     }
   }
-  if (tid == 0) tc::bulk_wait_all();
 }
 
 template <typename TIn>
@@ -350,7 +374,7 @@ cudaError_t launch_ring(const kda_decode_args& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int64_t n_items = (int64_t)a.batch * a.num_heads;
   const int64_t grid = n_items < sms ? n_items : sms;
-  decode_ring<TIn><<<(unsigned)grid, kRingThreads, Ring<TIn>::BYTES, stream>>>(a, n_items);
+  decode_ring<TIn><<<(unsigned)grid, kRingAllThreads, Ring<TIn>::BYTES, stream>>>(a, n_items);
   return cudaGetLastError();
 }
 

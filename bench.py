@@ -34,6 +34,12 @@ DECODE_WL = "decode_256"
 PREFILL_BYTES_PER_TOKEN_HEAD = 4 * 128 * 2 + 2 + 128 * 2      # q,k,v,g + b in, o out (bf16)
 INTRA_FLOP_PER_CHUNK_HEAD = 4 * 2 * 64 * 64 * 128              # A_kk, A_qk, W, U~ (dense)
 INTER_FLOP_PER_CHUNK_HEAD = 2 * 64 * 128 * 128 * 2 + 2 * 64 * 64 * 128 + 2 * 128 * 64 * 128
+# bytes per chunk-head of the two prefill kernels: the intra-chunk kernel reads
+# 64 tokens of q, k, v, g, b and writes its 90,624-byte record; the inter-chunk
+# kernel reads the record and writes 64 rows of o
+RECORD_BYTES = 90624
+INTRA_BYTES_PER_CHUNK_HEAD = 64 * (4 * 128 * 2 + 2) + RECORD_BYTES
+INTER_BYTES_PER_CHUNK_HEAD = RECORD_BYTES + 64 * 128 * 2
 DECODE_STATE_BYTES_PER_HEAD = 2 * 128 * 128 * 4                # read + write fp32 state
 
 
@@ -309,18 +315,28 @@ def gpu_arm(a):
     kernels["inter_chunk"]["achieved_tflops"] = inter_tflops
     kernels["inter_chunk"]["us_per_chunk_step"] = ph[2] * 1e3 / pre["n_chunks"]
     dom = max(range(3), key=lambda i: ph[i])
+    # Both prefill kernels sit below the ridge of the roofline (K2: 4.19 MFLOP
+    # per 156 KB, ~27 FLOP/B; K3: ~68 FLOP/B; ridge ~283 FLOP/B), so HBM is
+    # their roofline; the tensor-peak fraction is reported beside it.
     if names[dom] == "intra_chunk":
-        roof = {"kernel": "intra_chunk", "bound": "tensor", "achieved": intra_tflops,
-                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": intra_tflops / pk["bf16_tflops"],
+        gbs = INTRA_BYTES_PER_CHUNK_HEAD * chunk_heads / (ph[1] * 1e-3) / 1e9
+        roof = {"kernel": "intra_chunk", "bound": "hbm", "achieved": gbs,
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
                 "traffic": ncu_traffic("tc_intra", PREFILL_WL),
+                "algorithmic_bytes_per_chunk_head": INTRA_BYTES_PER_CHUNK_HEAD,
+                "chunk_heads_per_launch": chunk_heads,
+                "tensor_achieved_tflops": intra_tflops,
+                "tensor_frac": intra_tflops / pk["bf16_tflops"],
                 "algorithmic_flop_per_chunk_head": INTRA_FLOP_PER_CHUNK_HEAD}
     else:
-        # the serial inter-chunk kernel: its algorithmic FLOPs against the tensor peak
-        roof = {"kernel": names[dom], "bound": "tensor", "achieved": inter_tflops,
-                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": inter_tflops / pk["bf16_tflops"],
+        gbs = INTER_BYTES_PER_CHUNK_HEAD * chunk_heads / (ph[2] * 1e-3) / 1e9
+        roof = {"kernel": names[dom], "bound": "hbm", "achieved": gbs,
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
                 "traffic": ncu_traffic("tc_inter", PREFILL_WL),
+                "algorithmic_bytes_per_chunk_head": INTER_BYTES_PER_CHUNK_HEAD,
+                "chunk_heads_per_launch": chunk_heads,
+                "tensor_achieved_tflops": inter_tflops,
+                "tensor_frac": inter_tflops / pk["bf16_tflops"],
                 "algorithmic_flop_per_chunk_head": INTER_FLOP_PER_CHUNK_HEAD}
     roof["peak_source"] = pk["source"]
     roof["input_bytes_per_launch"] = (PREFILL_BYTES_PER_TOKEN_HEAD - 256) * T * H

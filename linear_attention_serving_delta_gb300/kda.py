@@ -263,12 +263,12 @@ class Prefill:
     def __init__(self, q, k, v, g, b, cu_seqlens, *, scale=1.0, initial_state=None,
                  snapshot_interval=0, boundary_pos=None, cu_boundaries=None,
                  want_final=True, host_cu_seqlens=None, host_boundary_pos=None,
-                 host_cu_boundaries=None):
+                 host_cu_boundaries=None, o=None):
         dev = q.device
         T, H, dk = q.shape
         dv = v.shape[-1]
         N = cu_seqlens.numel() - 1
-        self.o = torch.empty(T, H, dv, dtype=q.dtype, device=dev)
+        self.o = torch.empty(T, H, dv, dtype=q.dtype, device=dev) if o is None else o
         self.final_state = (torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
                             if want_final else None)
         self.cu_snapshots = self.snapshots = None
@@ -313,23 +313,92 @@ def prefill(q, k, v, g, b, cu_seqlens, **kw):
     return p.o, p.final_state, p.snapshot_view
 
 
-def prefill_host(q, k, v, g, b, cu_seqlens, *, device="cuda", stream=None, **kw):
+_side_streams = {}
+
+
+def _streams(device):
+    """Two side streams per device (host->device copies, device->host copies)."""
+    key = torch.device(device).index or 0
+    if key not in _side_streams:
+        _side_streams[key] = (torch.cuda.Stream(device=device), torch.cuda.Stream(device=device))
+    return _side_streams[key]
+
+
+def prefill_host(q, k, v, g, b, cu_seqlens, *, device="cuda", stream=None, segments=None, **kw):
     """End-to-end prefill from host tensors: copies the inputs (pinned host
     memory is copied asynchronously) to the device, runs kda_prefill, and
-    copies o and the final state back.  Returns host (o, final_state)."""
+    copies o and the final state back.  Returns host (o, final_state).
+
+    A single sequence without snapshots or boundaries is cut into
+    ``segments`` chunk-aligned pieces (by default one per 2048 tokens, at
+    most 4): the host->device copy of a piece overlaps the prefill of the
+    one before, each piece starts from the fp32 final state of the one
+    before (the same arithmetic as one call, since the cuts fall on chunk
+    boundaries), and each piece's o is copied back as soon as it is ready."""
     s = torch.cuda.current_stream() if stream is None else stream
-    with torch.cuda.stream(s):
-        dq, dk_, dv_, dg, db = (t.to(device, non_blocking=True) for t in (q, k, v, g, b))
-        dcu = cu_seqlens.to(device, non_blocking=True)
-        init = kw.pop("initial_state", None)
-        dinit = None if init is None else init.to(device, non_blocking=True)
-        p = Prefill(dq, dk_, dv_, dg, db, dcu, initial_state=dinit,
-                    host_cu_seqlens=cu_seqlens, **kw).run(s)
-        o = torch.empty(p.o.shape, dtype=p.o.dtype, pin_memory=True)
-        o.copy_(p.o, non_blocking=True)
-        fs = torch.empty(p.final_state.shape, dtype=torch.float32, pin_memory=True)
-        fs.copy_(p.final_state, non_blocking=True)
-    s.synchronize()
+    T = q.shape[0]
+    plain = (cu_seqlens.numel() == 2 and kw.get("snapshot_interval", 0) == 0
+             and kw.get("boundary_pos") is None)
+    nseg = segments if segments is not None else max(1, min(4, T // 2048))
+    if not plain or nseg <= 1 or T < 2 * nseg * 64:
+        with torch.cuda.stream(s):
+            dq, dk_, dv_, dg, db = (t.to(device, non_blocking=True) for t in (q, k, v, g, b))
+            dcu = cu_seqlens.to(device, non_blocking=True)
+            init = kw.pop("initial_state", None)
+            dinit = None if init is None else init.to(device, non_blocking=True)
+            p = Prefill(dq, dk_, dv_, dg, db, dcu, initial_state=dinit,
+                        host_cu_seqlens=cu_seqlens, **kw).run(s)
+            o = torch.empty(p.o.shape, dtype=p.o.dtype, pin_memory=True)
+            o.copy_(p.o, non_blocking=True)
+            fs = torch.empty(p.final_state.shape, dtype=torch.float32, pin_memory=True)
+            fs.copy_(p.final_state, non_blocking=True)
+        s.synchronize()
+        return o, fs
+    # pipelined single-sequence path
+    cs, ds = _streams(device)
+    step = -(-T // (nseg * 64)) * 64
+    cuts = list(range(0, T, step)) + [T]
+    H, dvv = v.shape[1], v.shape[2]
+    init = kw.pop("initial_state", None)
+    dev_in = [torch.empty(t.shape, dtype=t.dtype, device=device) for t in (q, k, v, g, b)]
+    o_dev = torch.empty(T, H, dvv, dtype=q.dtype, device=device)
+    o = torch.empty(T, H, dvv, dtype=q.dtype, pin_memory=True)
+    cs.wait_stream(s)
+    state = None
+    with torch.cuda.stream(cs):
+        if init is not None:
+            state = init.to(device, non_blocking=True)
+    arrived = []
+    for p0, p1 in zip(cuts[:-1], cuts[1:]):
+        with torch.cuda.stream(cs):
+            for d, h in zip(dev_in, (q, k, v, g, b)):
+                d[p0:p1].copy_(h[p0:p1], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(cs)
+        arrived.append(ev)
+    ds.wait_stream(s)
+    last = None
+    for (p0, p1), ev in zip(zip(cuts[:-1], cuts[1:]), arrived):
+        with torch.cuda.stream(s):
+            s.wait_event(ev)
+            L = p1 - p0
+            dcu = torch.zeros(2, dtype=torch.int64, device=device)
+            dcu[1] = L
+            hcu = torch.tensor([0, L], dtype=torch.int64)
+            piece = Prefill(*(d[p0:p1] for d in dev_in), dcu, initial_state=state,
+                            host_cu_seqlens=hcu, o=o_dev[p0:p1], **kw).run(s)
+            state = piece.final_state
+            done = torch.cuda.Event()
+            done.record(s)
+        with torch.cuda.stream(ds):
+            ds.wait_event(done)
+            o[p0:p1].copy_(o_dev[p0:p1], non_blocking=True)
+        last = piece
+    with torch.cuda.stream(ds):
+        fs = torch.empty(last.final_state.shape, dtype=torch.float32, pin_memory=True)
+        fs.copy_(last.final_state, non_blocking=True)
+    ds.synchronize()
+    s.wait_stream(ds)
     return o, fs
 
 

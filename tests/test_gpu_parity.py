@@ -216,6 +216,28 @@ def test_prefill_1m_sampled(oracle_mod):
     assert_close(gpu, ref, TOL["bf16"], "prefill_1m heads 8-11")
 
 
+def test_prefill_host_segments_match_one_call():
+    """The host-buffer prefill cut into chunk-aligned segments (copies of one
+    segment overlapping the prefill of the one before, the fp32 state carried
+    between them) gives bit-identical o and final state to a single call."""
+    inp = make_inputs([3000], 4, 128, 128, "bf16", 51, s0_std=0.02)
+    host_in = {x: inp[x].pin_memory() for x in "qkvgb"}
+    args = [host_in[x] for x in "qkvgb"] + [inp["cu_seqlens"]]
+    o1, s1 = kda.prefill_host(*args, initial_state=inp["S0"], segments=1)
+    o4, s4 = kda.prefill_host(*args, initial_state=inp["S0"], segments=4)
+    assert torch.equal(o1, o4)
+    assert torch.equal(s1, s4)
+    ro, rS, _ = oracle_prefill_of(inp)
+    assert rel(o4.float().numpy(), ro) <= TOL["bf16"]
+    assert rel(s4.numpy(), rS) <= TOL["bf16"]
+
+
+def oracle_prefill_of(inp):
+    import oracle
+    return oracle.prefill(host(inp["q"]), host(inp["k"]), host(inp["v"]), host(inp["g"]),
+                          host(inp["b"]), inp["cu_seqlens"].numpy(), S0=host(inp["S0"]))
+
+
 def test_prefill_empty_sequences_keep_initial_state():
     inp = make_inputs([0, 5, 0], 2, 32, 32, "f32", 41, s0_std=0.5)
     gpu, ref = run_both(inp, "f32")

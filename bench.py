@@ -258,6 +258,23 @@ def cpu_baseline(seconds_budget=20.0):
             "sample": f"prefill_8k, all {T} tokens of {heads}/{w.H} heads, fp64, {dt:.2f} s"}
 
 
+def max_over_ranks(dist, world, values, device):
+    """Each rank's per-step times reduced to their maximum over the ranks (the
+    slowest replica sets the whole job's step time)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_tokens_per_s(world, tokens_per_replica, step_ms):
+    """Throughput of N independent replicas (weak scaling): the tokens all
+    ranks processed per step over the slowest rank's step time."""
+    return world * tokens_per_replica / (step_ms * 1e-3)
+
+
 def gpu_arm(a):
     import torch
     import torch.distributed as dist
@@ -293,17 +310,14 @@ def gpu_arm(a):
         barrier()
     step_ms = sum(pre["step_ms"]) / len(pre["step_ms"])
     dec_ms = dec["ms_per_step"]
-    if world > 1:
-        t = torch.tensor([step_ms, dec_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, dec_ms = t.tolist()
+    step_ms, dec_ms = max_over_ranks(dist, world, [step_ms, dec_ms], dev)
     e2e = bench_e2e(torch, kda, W, max(1, min(a.steps, 5)), 1, dev) if rank == 0 else None
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
     T, H = pre["T"], pre["H"]
-    value = world * T / (step_ms * 1e-3)
+    value = whole_job_tokens_per_s(world, T, step_ms)
     ph = [sum(x) / len(x) for x in pre["phase_ms"]]
     names = ["plan", "intra_chunk", "inter_chunk"]
     kernels = {n: {"ms": m, "share": m / max(sum(ph), 1e-12)} for n, m in zip(names, ph)}

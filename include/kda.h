@@ -142,6 +142,70 @@ kda_status_t kda_prefill(const kda_prefill_args* args, void* ws, size_t ws_bytes
  *     through kda_prefill_device_status. */
 kda_status_t kda_prefill_noalloc(const kda_prefill_args* args, void* stream);
 
+/*
+ * kda_prefill from HOST buffers, end to end: the inputs are copied to the
+ * device, the prefill runs, and o and the final state are copied back, with
+ * the copies of one piece of the batch overlapping the prefill of another.
+ * The operation and its results are those of kda_prefill (the same kernels,
+ * bit for bit); only where the tensors live differs.  This entry has no
+ * counterpart on the pages; it is the call a serving host makes when a
+ * prompt's q, k, v, g, b sit in host memory.
+ *
+ * Pipelining.  The batch is cut into about `segments` equal pieces (0 = one
+ * per 48 chunks of the batch, at most 4; 1 = no cut).  A single sequence is
+ * cut at chunk boundaries, and the end of it into a few halving pieces (1/8,
+ * 1/4, 1/2 of a piece) so that the prefill and copy-out of the last piece,
+ * which nothing overlaps, are short.  Piece p starts from the fp32 final
+ * state of piece p-1: the same arithmetic as one call, because the chunked
+ * recurrence restarts its chunk algebra at every chunk boundary anyway.  A
+ * batch of several sequences is cut only between sequences.  Piece p+1 is copied in on
+ * copy_in_stream while piece p is computed on `stream`; piece p's o is copied
+ * out on copy_out_stream as soon as it is ready.
+ *
+ * Memory.  All host buffers are caller-owned, row-major and contiguous with
+ * the shapes of kda_prefill_args; pinned (page-locked) host memory is needed
+ * for the copies to overlap (pageable memory works but copies synchronously).
+ * ws is a caller-owned device buffer of kda_prefill_host_workspace_size()
+ * bytes, 256-byte aligned, holding the device copies of every tensor and the
+ * prefill workspace; kda_prefill_device_status(ws) afterwards reports the
+ * OR of the status words of all pieces.
+ *
+ * Ordering.  The copy streams first wait for work already queued on
+ * `stream`; when `stream` reaches the point after this call, o and
+ * final_state in host memory are complete.  The call creates and releases
+ * its own CUDA events; it allocates no memory.  Snapshots and boundary
+ * positions are not offered here (they live in device memory; use
+ * kda_prefill).  cu_seqlens is validated on the host (cu[0] = 0,
+ * non-decreasing, cu[N] = total_tokens): KDA_ERR_INVALID_ARG otherwise.
+ */
+typedef struct {
+  int32_t num_seqs;            /* N >= 1                                          */
+  int32_t num_heads;           /* H >= 1                                          */
+  int32_t dk, dv;              /* each in {16, 32, 64, 128}                       */
+  int64_t total_tokens;        /* T = cu_seqlens[N]                               */
+  const int64_t* cu_seqlens;   /* HOST [N+1]                                      */
+  kda_dtype_t in_dtype;        /* dtype of q, k, v, g, b and of o                 */
+  const void* q;               /* HOST [T, H, dk]                                 */
+  const void* k;               /* HOST [T, H, dk]                                 */
+  const void* v;               /* HOST [T, H, dv]                                 */
+  const void* g;               /* HOST [T, H, dk]                                 */
+  const void* b;               /* HOST [T, H]                                     */
+  float scale;
+  const float* initial_state;  /* HOST [N, H, dk, dv] or NULL (zeros)             */
+  void* o;                     /* HOST [T, H, dv], in_dtype                       */
+  float* final_state;          /* HOST [N, H, dk, dv] or NULL                     */
+  int32_t segments;            /* pieces of the pipeline, 0 = default, <= 64     */
+  void* copy_in_stream;        /* cudaStream_t for host->device copies (not `stream`) */
+  void* copy_out_stream;       /* cudaStream_t for device->host copies (not `stream`) */
+} kda_prefill_host_args;
+
+/* Device workspace bytes kda_prefill_host needs (host-side fields only);
+ * 0 if the arguments are invalid. */
+size_t kda_prefill_host_workspace_size(const kda_prefill_host_args* args);
+
+kda_status_t kda_prefill_host(const kda_prefill_host_args* args, void* ws, size_t ws_bytes,
+                              void* stream);
+
 /* Copies the workspace status word of the last kda_prefill that used `ws`
  * to *out (host), synchronising `stream`.  0 = clean; otherwise a bitwise OR
  * of 1 (malformed cu_seqlens), 2 (malformed boundary positions), 4 (chunk

@@ -7,9 +7,9 @@ built, or no CUDA device is present, the calls raise.
 
 The names follow the C ABI: ``kda_prefill``, ``kda_prefill_workspace_size``,
 ``kda_prefill_device_status``, ``kda_snapshot_plan``, ``kda_decode_step``,
-``kda_prep``, ``kda_status_string``.  ``prefill`` and ``prefill_host`` are
-conveniences that allocate outputs and workspace with torch and call
-``kda_prefill``.
+``kda_prep``, ``kda_status_string``, ``kda_prefill_host`` (host buffers).
+``prefill`` and ``prefill_host`` are conveniences that allocate outputs and
+workspace with torch and call ``kda_prefill`` / ``kda_prefill_host``.
 """
 from __future__ import annotations
 
@@ -31,6 +31,7 @@ _STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED"
                  3: "KDA_ERR_WORKSPACE", 4: "KDA_ERR_CUDA", 5: "KDA_ERR_TIMEOUT",
                  6: "KDA_ERR_DEVICE_DATA"}
 EXPORTED = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_noalloc",
+            "kda_prefill_host_workspace_size", "kda_prefill_host",
             "kda_prefill_device_status", "kda_snapshot_plan", "kda_decode_step", "kda_prep",
             "kda_status_string", "kda_version")
 NOALLOC_SCRATCH_BYTES = 64 << 20  # fixed workspace behind kda_prefill_noalloc
@@ -54,6 +55,14 @@ class PrefillArgs(ctypes.Structure):
                 ("snapshot_interval", c_i64), ("boundary_pos", c_vp), ("cu_boundaries", c_vp),
                 ("num_boundaries", c_i64), ("cu_snapshots", c_vp), ("snapshots", c_vp),
                 ("num_snapshots", c_i64), ("phase_events", c_vp)]
+
+
+class PrefillHostArgs(ctypes.Structure):
+    _fields_ = [("num_seqs", c_i32), ("num_heads", c_i32), ("dk", c_i32), ("dv", c_i32),
+                ("total_tokens", c_i64), ("cu_seqlens", c_vp), ("in_dtype", ctypes.c_int),
+                ("q", c_vp), ("k", c_vp), ("v", c_vp), ("g", c_vp), ("b", c_vp),
+                ("scale", c_f32), ("initial_state", c_vp), ("o", c_vp), ("final_state", c_vp),
+                ("segments", c_i32), ("copy_in_stream", c_vp), ("copy_out_stream", c_vp)]
 
 
 class DecodeArgs(ctypes.Structure):
@@ -87,6 +96,11 @@ def lib() -> ctypes.CDLL:
             L.kda_prefill_workspace_size.restype = ctypes.c_size_t
             L.kda_prefill.argtypes = [ctypes.POINTER(PrefillArgs), c_vp, ctypes.c_size_t, c_vp]
             L.kda_prefill.restype = ctypes.c_int
+            L.kda_prefill_host_workspace_size.argtypes = [ctypes.POINTER(PrefillHostArgs)]
+            L.kda_prefill_host_workspace_size.restype = ctypes.c_size_t
+            L.kda_prefill_host.argtypes = [ctypes.POINTER(PrefillHostArgs), c_vp, ctypes.c_size_t,
+                                           c_vp]
+            L.kda_prefill_host.restype = ctypes.c_int
             L.kda_prefill_noalloc.argtypes = [ctypes.POINTER(PrefillArgs), c_vp]
             L.kda_prefill_noalloc.restype = ctypes.c_int
             L.kda_prefill_device_status.argtypes = [c_vp, ctypes.POINTER(c_i32), c_vp]
@@ -186,6 +200,57 @@ def kda_prefill(args: PrefillArgs, workspace: torch.Tensor, stream=None) -> None
     ws = _ptr(workspace, torch.uint8, "workspace")
     _check(lib().kda_prefill(ctypes.byref(args), ws, workspace.numel(), _stream(stream)),
            "kda_prefill")
+
+
+def _host_ptr(t: torch.Tensor | None, dtype=None, name: str = "") -> int | None:
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def make_prefill_host_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=None,
+                           final_state=None, segments=0, copy_in_stream=None,
+                           copy_out_stream=None) -> PrefillHostArgs:
+    """kda_prefill_host_args over HOST tensors (pinned for overlapped copies)."""
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    for name, t, shp in (("k", k, (T, H, dk)), ("g", g, (T, H, dk)), ("v", v, (T, H, dv)),
+                         ("b", b, (T, H)), ("o", o, (T, H, dv))):
+        if tuple(t.shape) != shp:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shp}")
+    a = PrefillHostArgs()
+    a.num_seqs = cu_seqlens.numel() - 1
+    a.num_heads, a.dk, a.dv, a.total_tokens = H, dk, dv, T
+    a.cu_seqlens = _host_ptr(cu_seqlens, torch.int64, "cu_seqlens")
+    a.in_dtype = _dtype_code(dt)
+    a.q, a.k, a.v = _host_ptr(q, dt, "q"), _host_ptr(k, dt, "k"), _host_ptr(v, dt, "v")
+    a.g, a.b, a.o = _host_ptr(g, dt, "g"), _host_ptr(b, dt, "b"), _host_ptr(o, dt, "o")
+    a.scale = float(scale)
+    a.initial_state = _host_ptr(initial_state, torch.float32, "initial_state")
+    a.final_state = _host_ptr(final_state, torch.float32, "final_state")
+    a.segments = int(segments)
+    a.copy_in_stream = None if copy_in_stream is None else _stream(copy_in_stream)
+    a.copy_out_stream = None if copy_out_stream is None else _stream(copy_out_stream)
+    return a
+
+
+def kda_prefill_host_workspace_size(args: PrefillHostArgs) -> int:
+    return int(lib().kda_prefill_host_workspace_size(ctypes.byref(args)))
+
+
+def kda_prefill_host(args: PrefillHostArgs, workspace: torch.Tensor, stream=None) -> None:
+    """Enqueues the host-buffer prefill described by ``args``; the host
+    outputs are complete once ``stream`` has passed this point."""
+    ws = _ptr(workspace, torch.uint8, "workspace")
+    _check(lib().kda_prefill_host(ctypes.byref(args), ws, workspace.numel(), _stream(stream)),
+           "kda_prefill_host")
 
 
 def kda_prefill_noalloc(args: PrefillArgs, stream=None) -> None:
@@ -324,82 +389,70 @@ def _streams(device):
     return _side_streams[key]
 
 
-def prefill_host(q, k, v, g, b, cu_seqlens, *, device="cuda", stream=None, segments=None, **kw):
-    """End-to-end prefill from host tensors: copies the inputs (pinned host
-    memory is copied asynchronously) to the device, runs kda_prefill, and
-    copies o and the final state back.  Returns host (o, final_state).
+def prefill_host(q, k, v, g, b, cu_seqlens, *, device="cuda", stream=None, segments=None,
+                 scale=1.0, initial_state=None, want_final=True, **kw):
+    """End-to-end prefill from host tensors through ``kda_prefill_host``:
+    inputs copied in, prefill, o and the final state copied back, pipelined
+    over ``segments`` pieces of the batch (None = the library's choice).
+    Returns host (o, final_state), complete when this returns.
 
-    A single sequence without snapshots or boundaries is cut into
-    ``segments`` chunk-aligned pieces (by default one per 2048 tokens, at
-    most 4): the host->device copy of a piece overlaps the prefill of the
-    one before, each piece starts from the fp32 final state of the one
-    before (the same arithmetic as one call, since the cuts fall on chunk
-    boundaries), and each piece's o is copied back as soon as it is ready."""
-    s = torch.cuda.current_stream() if stream is None else stream
-    T = q.shape[0]
-    plain = (cu_seqlens.numel() == 2 and kw.get("snapshot_interval", 0) == 0
-             and kw.get("boundary_pos") is None)
-    nseg = segments if segments is not None else max(1, min(4, T // 2048))
-    if not plain or nseg <= 1 or T < 2 * nseg * 64:
+    Snapshots and boundary positions need device buffers: with those
+    arguments the inputs are copied to the device and ``kda_prefill`` runs
+    as one call."""
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    if kw.get("snapshot_interval", 0) or kw.get("boundary_pos") is not None:
         with torch.cuda.stream(s):
             dq, dk_, dv_, dg, db = (t.to(device, non_blocking=True) for t in (q, k, v, g, b))
             dcu = cu_seqlens.to(device, non_blocking=True)
-            init = kw.pop("initial_state", None)
-            dinit = None if init is None else init.to(device, non_blocking=True)
-            p = Prefill(dq, dk_, dv_, dg, db, dcu, initial_state=dinit,
-                        host_cu_seqlens=cu_seqlens, **kw).run(s)
+            dinit = None if initial_state is None else initial_state.to(device, non_blocking=True)
+            p = Prefill(dq, dk_, dv_, dg, db, dcu, scale=scale, initial_state=dinit,
+                        want_final=want_final, host_cu_seqlens=cu_seqlens, **kw).run(s)
             o = torch.empty(p.o.shape, dtype=p.o.dtype, pin_memory=True)
             o.copy_(p.o, non_blocking=True)
-            fs = torch.empty(p.final_state.shape, dtype=torch.float32, pin_memory=True)
-            fs.copy_(p.final_state, non_blocking=True)
+            fs = None
+            if p.final_state is not None:
+                fs = torch.empty(p.final_state.shape, dtype=torch.float32, pin_memory=True)
+                fs.copy_(p.final_state, non_blocking=True)
         s.synchronize()
         return o, fs
-    # pipelined single-sequence path
-    cs, ds = _streams(device)
-    step = -(-T // (nseg * 64)) * 64
-    cuts = list(range(0, T, step)) + [T]
-    H, dvv = v.shape[1], v.shape[2]
-    init = kw.pop("initial_state", None)
-    dev_in = [torch.empty(t.shape, dtype=t.dtype, device=device) for t in (q, k, v, g, b)]
-    o_dev = torch.empty(T, H, dvv, dtype=q.dtype, device=device)
-    o = torch.empty(T, H, dvv, dtype=q.dtype, pin_memory=True)
-    cs.wait_stream(s)
-    state = None
-    with torch.cuda.stream(cs):
-        if init is not None:
-            state = init.to(device, non_blocking=True)
-    arrived = []
-    for p0, p1 in zip(cuts[:-1], cuts[1:]):
-        with torch.cuda.stream(cs):
-            for d, h in zip(dev_in, (q, k, v, g, b)):
-                d[p0:p1].copy_(h[p0:p1], non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(cs)
-        arrived.append(ev)
-    ds.wait_stream(s)
-    last = None
-    for (p0, p1), ev in zip(zip(cuts[:-1], cuts[1:]), arrived):
-        with torch.cuda.stream(s):
-            s.wait_event(ev)
-            L = p1 - p0
-            dcu = torch.zeros(2, dtype=torch.int64, device=device)
-            dcu[1] = L
-            hcu = torch.tensor([0, L], dtype=torch.int64)
-            piece = Prefill(*(d[p0:p1] for d in dev_in), dcu, initial_state=state,
-                            host_cu_seqlens=hcu, o=o_dev[p0:p1], **kw).run(s)
-            state = piece.final_state
-            done = torch.cuda.Event()
-            done.record(s)
-        with torch.cuda.stream(ds):
-            ds.wait_event(done)
-            o[p0:p1].copy_(o_dev[p0:p1], non_blocking=True)
-        last = piece
-    with torch.cuda.stream(ds):
-        fs = torch.empty(last.final_state.shape, dtype=torch.float32, pin_memory=True)
-        fs.copy_(last.final_state, non_blocking=True)
-    ds.synchronize()
-    s.wait_stream(ds)
-    return o, fs
+    if kw:
+        raise TypeError(f"unexpected arguments {sorted(kw)}")
+    p = PrefillHost(q, k, v, g, b, cu_seqlens, device=device, segments=segments, scale=scale,
+                    initial_state=initial_state, want_final=want_final)
+    p.run(s)
+    s.synchronize()
+    return p.o, p.final_state
+
+
+class PrefillHost:
+    """A planned host-buffer prefill (``kda_prefill_host``): the pinned host
+    outputs, the device workspace and the argument block are made once;
+    ``run()`` enqueues the copies in, the kernels and the copies out.  The
+    inputs are the host tensors given here (refill them in place between
+    runs); o and final_state are complete once ``stream`` passes the run."""
+
+    def __init__(self, q, k, v, g, b, cu_seqlens, *, device="cuda", segments=None, scale=1.0,
+                 initial_state=None, want_final=True):
+        T, H, dk = q.shape
+        dv = v.shape[-1]
+        N = cu_seqlens.numel() - 1
+        self.o = torch.empty(T, H, dv, dtype=q.dtype, pin_memory=True)
+        self.final_state = (torch.empty(N, H, dk, dv, dtype=torch.float32, pin_memory=True)
+                            if want_final else None)
+        self.copy_in, self.copy_out = _streams(device)
+        self.args = make_prefill_host_args(
+            q, k, v, g, b, cu_seqlens, self.o, scale=scale, initial_state=initial_state,
+            final_state=self.final_state, segments=segments or 0, copy_in_stream=self.copy_in,
+            copy_out_stream=self.copy_out)
+        nbytes = kda_prefill_host_workspace_size(self.args)
+        if nbytes == 0:
+            raise ValueError("kda_prefill_host_workspace_size rejected the arguments")
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self._keep = (q, k, v, g, b, cu_seqlens, initial_state)
+
+    def run(self, stream=None):
+        kda_prefill_host(self.args, self.workspace, stream)
+        return self
 
 
 def decode_step(q, k, v, g, b, state, state_slots=None, scale=1.0, o=None, stream=None):

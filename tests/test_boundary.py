@@ -59,6 +59,11 @@ int main(void) {
   printf("kda_prefill_args %zu\n", sizeof(kda_prefill_args));
   printf("kda_decode_args %zu\n", sizeof(kda_decode_args));
   printf("kda_prep_args %zu\n", sizeof(kda_prep_args));
+  printf("kda_prefill_host_args %zu\n", sizeof(kda_prefill_host_args));
+  F(kda_prefill_host_args, cu_seqlens) F(kda_prefill_host_args, in_dtype)
+  F(kda_prefill_host_args, scale) F(kda_prefill_host_args, final_state)
+  F(kda_prefill_host_args, segments) F(kda_prefill_host_args, copy_in_stream)
+  F(kda_prefill_host_args, copy_out_stream)
   F(kda_prefill_args, cu_seqlens) F(kda_prefill_args, in_dtype) F(kda_prefill_args, q)
   F(kda_prefill_args, scale) F(kda_prefill_args, initial_state)
   F(kda_prefill_args, snapshot_interval) F(kda_prefill_args, num_boundaries)
@@ -77,7 +82,7 @@ int main(void) {
     lines = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
     got = dict(l.rsplit(" ", 1) for l in lines if l)
     structs = {"kda_prefill_args": kda.PrefillArgs, "kda_decode_args": kda.DecodeArgs,
-               "kda_prep_args": kda.PrepArgs}
+               "kda_prep_args": kda.PrepArgs, "kda_prefill_host_args": kda.PrefillHostArgs}
     for key, val in got.items():
         if "." in key:
             s, m = key.split(".")
@@ -169,3 +174,56 @@ def test_snapshot_plan_matches_oracle_definition(kda, oracle_mod):
         kda.kda_snapshot_plan([0, 10], 0, [5, 5], [0, 2])      # not strictly increasing
     with pytest.raises(ValueError):
         kda.kda_snapshot_plan([0, 10], 0, [11], [0, 1])        # beyond the sequence
+
+
+def _host_args(kda, cu, **over):
+    a = kda.PrefillHostArgs()
+    a.num_seqs, a.num_heads, a.dk, a.dv = len(cu) - 1, 2, 128, 128
+    a.total_tokens = int(cu[-1])
+    a.cu_seqlens = cu.ctypes.data
+    a.in_dtype = kda.KDA_BF16
+    a.q = a.k = a.v = a.g = a.b = a.o = 0x2000
+    a.scale = 1.0
+    a.copy_in_stream, a.copy_out_stream = 0x10, 0x20
+    for k_, v_ in over.items():
+        setattr(a, k_, v_)
+    return a
+
+
+def test_host_entry_workspace_and_validation(kda):
+    """kda_prefill_host: its workspace holds the device copies of every
+    tensor, and host-side validation (cu_seqlens read on the host, streams,
+    segment count) rejects bad arguments before any CUDA call."""
+    L = kda.lib()
+    T, H = 8192, 2
+    cu = np.array([0, T], dtype=np.int64)
+    good = _host_args(kda, cu)
+    ws = L.kda_prefill_host_workspace_size(ctypes.byref(good))
+    tensors = T * H * 128 * 2 * 5 + T * H * 2 + 3 * H * 128 * 128 * 4
+    assert ws % 256 == 0 and ws > tensors
+    # more pieces of one sequence: the per-piece prefill workspace shrinks
+    one = L.kda_prefill_host_workspace_size(ctypes.byref(_host_args(kda, cu, segments=1)))
+    eight = L.kda_prefill_host_workspace_size(ctypes.byref(_host_args(kda, cu, segments=8)))
+    assert one > eight > tensors
+    multi = np.array([0, 100, 100, 3000, T], dtype=np.int64)
+    assert L.kda_prefill_host_workspace_size(ctypes.byref(_host_args(kda, multi, segments=3))) > 0
+    bad_cus = [np.array([1, T], dtype=np.int64), np.array([0, 10, 5, T], dtype=np.int64),
+               np.array([0, T - 1], dtype=np.int64)]
+    for bad_cu in bad_cus:
+        a = _host_args(kda, bad_cu)
+        a.total_tokens = T
+        assert L.kda_prefill_host_workspace_size(ctypes.byref(a)) == 0
+        assert L.kda_prefill_host(ctypes.byref(a), 0x4000, 1 << 40, None) == 1
+    for bad, code in [(dict(dk=24), 2), (dict(segments=-1), 1), (dict(segments=65), 1),
+                      (dict(q=None), 1), (dict(in_dtype=5), 1), (dict(cu_seqlens=None), 1)]:
+        a = _host_args(kda, cu, **bad)
+        assert L.kda_prefill_host_workspace_size(ctypes.byref(a)) == 0, bad
+        assert L.kda_prefill_host(ctypes.byref(a), 0x4000, 1 << 40, None) == code, bad
+    # the copy streams are required and distinct from each other and `stream`
+    for streams in [(None, 0x20), (0x10, None), (0x10, 0x10), (0x30, 0x20)]:
+        a = _host_args(kda, cu)
+        a.copy_in_stream, a.copy_out_stream = streams
+        assert L.kda_prefill_host(ctypes.byref(a), 0x4000, 1 << 40, 0x30) == 1, streams
+    # workspace too small or misaligned
+    assert L.kda_prefill_host(ctypes.byref(good), 0x4000, ws - 256, None) == 3
+    assert L.kda_prefill_host(ctypes.byref(good), 0x4010, ws, None) == 3

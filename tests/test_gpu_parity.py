@@ -232,6 +232,52 @@ def test_prefill_host_segments_match_one_call():
     assert rel(s4.numpy(), rS) <= TOL["bf16"]
 
 
+def device_prefill_of(inp, scale=1.0):
+    d = to_dev(inp)
+    p = kda.Prefill(d["q"], d["k"], d["v"], d["g"], d["b"], d["cu_seqlens"], scale=scale,
+                    initial_state=d["S0"], host_cu_seqlens=inp["cu_seqlens"]).run()
+    torch.cuda.synchronize()
+    return p.o.cpu(), p.final_state.cpu()
+
+
+@pytest.mark.parametrize("dtype,dk,dv,segments", [("bf16", 128, 128, 3), ("bf16", 128, 128, 0),
+                                                  ("f32", 64, 32, 2)])
+def test_prefill_host_batch_matches_device_call(dtype, dk, dv, segments):
+    """kda_prefill_host over a batch of sequences (pieces of whole sequences,
+    an empty sequence among them) gives the same bits as kda_prefill on
+    device copies, and the oracle's values."""
+    lens = [700, 0, 1500, 64, 2100, 33]
+    inp = make_inputs(lens, 3, dk, dv, dtype, 57, s0_std=0.05)
+    host_in = {x: inp[x].pin_memory() for x in "qkvgb"}
+    o, S = kda.prefill_host(*(host_in[x] for x in "qkvgb"), inp["cu_seqlens"], scale=0.7,
+                            initial_state=inp["S0"], segments=segments)
+    od, Sd = device_prefill_of(inp, scale=0.7)
+    assert torch.equal(o, od)
+    assert torch.equal(S, Sd)
+    np.testing.assert_array_equal(S[1].numpy(), host(inp["S0"])[1])
+    import oracle
+    ro, rS, _ = oracle.prefill(host(inp["q"]), host(inp["k"]), host(inp["v"]), host(inp["g"]),
+                               host(inp["b"]), inp["cu_seqlens"].numpy(), S0=host(inp["S0"]),
+                               scale=0.7)
+    assert rel(o.float().numpy(), ro) <= TOL[dtype]
+    assert rel(S.numpy(), rS) <= TOL[dtype]
+
+
+def test_prefill_host_pageable_and_empty():
+    """Pageable (not pinned) host buffers give the same result as pinned ones;
+    an empty prompt returns its initial state."""
+    inp = make_inputs([1000], 2, 128, 128, "bf16", 58, s0_std=0.05)
+    args = [inp[x] for x in "qkvgb"] + [inp["cu_seqlens"]]
+    o_pg, S_pg = kda.prefill_host(*args, initial_state=inp["S0"], segments=5)
+    pinned = [inp[x].pin_memory() for x in "qkvgb"] + [inp["cu_seqlens"]]
+    o_pn, S_pn = kda.prefill_host(*pinned, initial_state=inp["S0"], segments=5)
+    assert torch.equal(o_pg, o_pn) and torch.equal(S_pg, S_pn)
+    e = make_inputs([0], 2, 128, 128, "bf16", 59, s0_std=0.3)
+    o0, S0 = kda.prefill_host(*(e[x] for x in "qkvgb"), e["cu_seqlens"], initial_state=e["S0"])
+    assert o0.shape[0] == 0
+    assert torch.equal(S0, e["S0"])
+
+
 def oracle_prefill_of(inp):
     import oracle
     return oracle.prefill(host(inp["q"]), host(inp["k"]), host(inp["v"]), host(inp["g"]),

@@ -190,6 +190,36 @@ def bench_prefill(torch, kda, W, steps, warmup, dev):
                 launches_per_step=3, workload=w)
 
 
+def bench_scan(torch, kda, W, dev, T=131072, H=2, reps=5):
+    """The segment scan against the plain chunk chain on a workload it is
+    for: one sequence of T tokens with few heads (bf16, 128 x 128), so that
+    the plain chain keeps 4 H of the SMs busy.  Whole prefill per call,
+    CUDA events, inputs (268 MB) larger than L2."""
+    w = W.PrefillWorkload("scan_probe", (T,), 1, H, 128, 128, "bf16", 77)
+    inp = W.prefill_inputs(w, device=dev, gen_device=dev)
+    args = [inp[x] for x in "qkvgb"] + [inp["cu_seqlens"]]
+    hcu = inp["cu_seqlens"].cpu()
+    out = {"workload": f"one sequence, T={T}, H={H}, dk=dv=128, bf16"}
+    for name, P in (("plain", 1), ("scan", 0)):
+        p = kda.Prefill(*args, host_cu_seqlens=hcu, scan_segments=P)
+        for _ in range(2):
+            p.run()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            p.run()
+        e1.record()
+        e1.synchronize()
+        assert p.device_status() == 0
+        out[f"{name}_ms"] = e0.elapsed_time(e1) / reps
+        if P == 0:
+            out["segments"] = int(min(152 // (8 * H), ((T + 63) // 64) // 16, 64))
+    out["speedup"] = out["plain_ms"] / out["scan_ms"]
+    out["tokens_per_s"] = T / (out["scan_ms"] * 1e-3)
+    return out
+
+
 def bench_decode(torch, kda, W, steps, warmup, dev):
     dw = W.DECODE_WORKLOADS[DECODE_WL]
     n = steps + warmup
@@ -317,6 +347,7 @@ def gpu_arm(a):
     dec_ms = dec["ms_per_step"]
     step_ms, dec_ms = max_over_ranks(dist, world, [step_ms, dec_ms], dev)
     e2e = bench_e2e(torch, kda, W, max(1, min(a.steps, 5)), 1, dev) if rank == 0 else None
+    scan = bench_scan(torch, kda, W, dev) if rank == 0 else None
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -387,6 +418,7 @@ def gpu_arm(a):
                 "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
                 "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
                 "ms_per_step": e2e["ms_per_step"]},
+        "segment_scan": scan,
         "gpu_launches": pre["launches_per_step"] * a.steps + dec["steps"],
         "clocks": clk.summary(),
     }

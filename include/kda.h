@@ -106,7 +106,27 @@ typedef struct {
                                   records on `stream` before the first phase and after
                                   each phase (chunk planning, intra-chunk,
                                   inter-chunk), for per-kernel timing             */
+  int32_t scan_segments;       /* segment scan: 0 = automatic, 1 = off, P >= 2 = P
+                                  segments (see below); at most 64                */
 } kda_prefill_args;
+
+/*
+ * Segment scan.  The inter-chunk recurrence of one sequence is a chain over
+ * its chunks, and each (sequence, head) runs it on a few SMs only.  When the
+ * call has few heads and one long sequence, the chain is cut into P
+ * chunk-aligned segments.  Every segment runs in parallel twice from a
+ * known start: from the zero state, giving its state offset B_s, and from
+ * the identity with v = 0, giving its transition map A_s (dk x dk), so that
+ * S_end(s) = A_s S_start(s) + B_s, the recurrence being affine in S.  A
+ * short serial combine forms the true start states, and a second parallel
+ * pass over the segments writes o and the final state.  The chunk algebra
+ * itself runs once.  This is a reading of the recurrence's linearity, not a
+ * step the pages give.  It applies on the tensor-core path, to one sequence
+ * without snapshots or boundary positions; otherwise scan_segments is
+ * ignored.  Automatic (0) uses it when 8 * num_heads * P CTAs fit the GPU
+ * with P >= 3 segments of >= 16 chunks each.  The results match the unsplit
+ * chain to rounding (fp32 state combine), not bit for bit.
+ */
 
 /* Number of timed phases of kda_prefill (see phase_events). */
 #define KDA_PREFILL_PHASES 3
@@ -146,8 +166,9 @@ kda_status_t kda_prefill_noalloc(const kda_prefill_args* args, void* stream);
  * kda_prefill from HOST buffers, end to end: the inputs are copied to the
  * device, the prefill runs, and o and the final state are copied back, with
  * the copies of one piece of the batch overlapping the prefill of another.
- * The operation and its results are those of kda_prefill (the same kernels,
- * bit for bit); only where the tensors live differs.  This entry has no
+ * The operation and its results are those of kda_prefill without the
+ * segment scan (the same kernels, bit for bit); only where the tensors live
+ * differs.  This entry has no
  * counterpart on the pages; it is the call a serving host makes when a
  * prompt's q, k, v, g, b sit in host memory.
  *

@@ -25,6 +25,27 @@ bool use_tensor_cores(const kda_prefill_args* a) {
          aligned16(a->snapshots);
 }
 
+constexpr int32_t kMaxScanSegments = 64;
+constexpr int32_t kScanSms = 152;  // SMs of the part the automatic choice is sized for
+
+// Segments of the segment scan for these arguments (host-side fields only):
+// 1 = no scan.  See kda.h.
+int32_t scan_segments_of(const kda_prefill_args* a) {
+  if (!use_tensor_cores(a) || a->num_seqs != 1 || a->snapshot_interval != 0 || a->boundary_pos ||
+      a->snapshots || a->scan_segments == 1)
+    return 1;
+  const int64_t nch = (a->total_tokens + kChunk - 1) / kChunk;
+  int64_t P;
+  if (a->scan_segments >= 2) {
+    P = a->scan_segments;
+  } else {
+    P = kScanSms / (8 * (int64_t)a->num_heads);
+    if (nch / 16 < P) P = nch / 16;
+    if (P < 3) return 1;
+  }
+  return (int32_t)(P > kMaxScanSegments ? kMaxScanSegments : P);
+}
+
 kda_status_t validate_prefill(const kda_prefill_args* a) {
   if (!a) return KDA_ERR_INVALID_ARG;
   if (a->num_seqs < 1 || a->num_heads < 1 || a->total_tokens < 0) return KDA_ERR_INVALID_ARG;
@@ -39,6 +60,7 @@ kda_status_t validate_prefill(const kda_prefill_args* a) {
     return KDA_ERR_INVALID_ARG;
   if ((a->snapshots == nullptr) != (a->cu_snapshots == nullptr)) return KDA_ERR_INVALID_ARG;
   if (a->num_snapshots < 0 || (a->snapshots && a->num_snapshots == 0)) return KDA_ERR_INVALID_ARG;
+  if (a->scan_segments < 0 || a->scan_segments > kMaxScanSegments) return KDA_ERR_INVALID_ARG;
   // sizes whose products must stay inside the index types used by the kernels
   if (a->total_tokens > ((int64_t)1 << 40)) return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
@@ -46,7 +68,9 @@ kda_status_t validate_prefill(const kda_prefill_args* a) {
 
 WsLayout prefill_layout(const kda_prefill_args* a) {
   WsLayout L;
-  const int64_t N = a->num_seqs, nb = a->num_boundaries;
+  // with the segment scan the planner sees P sequences (the segments)
+  const int32_t P = scan_segments_of(a);
+  const int64_t N = P > 1 ? P : a->num_seqs, nb = a->num_boundaries;
   L.max_chunks = (a->total_tokens + kChunk - 1) / kChunk + N + nb;
   L.rec_bytes = use_tensor_cores(a) ? tc_record_bytes()
                                     : SimtRec::floats(a->dk, a->dv) * sizeof(float);
@@ -66,6 +90,15 @@ WsLayout prefill_layout(const kda_prefill_args* a) {
   L.seq_aux = take(sizeof(int64_t) * 3 * N);  // seq_len [N] + seq_bnd [2N]
   L.chunks = take(sizeof(Chunk) * (size_t)L.max_chunks);
   L.inter = take(L.rec_bytes * (size_t)L.max_chunks * (size_t)a->num_heads);
+  L.scan_P = P;
+  if (P > 1) {
+    const size_t mats = (size_t)P * a->num_heads * a->dk * a->dv * sizeof(float);
+    L.scan_cu = take(sizeof(int64_t) * (P + 1));
+    L.scan_A = take(mats);
+    L.scan_B = take(mats);
+    L.scan_inits = take(mats);
+    L.scan_finals = take(mats);
+  }
   L.total = off;
   return L;
 }
@@ -93,10 +126,11 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   char* w = static_cast<char*>(ws);
 
+  const int32_t P = L.scan_P;
   PlanParams pp{};
-  pp.num_seqs = a->num_seqs;
+  pp.num_seqs = P > 1 ? P : a->num_seqs;
   pp.total_tokens = a->total_tokens;
-  pp.cu_seqlens = a->cu_seqlens;
+  pp.cu_seqlens = P > 1 ? reinterpret_cast<const int64_t*>(w + L.scan_cu) : a->cu_seqlens;
   pp.snapshot_interval = a->snapshot_interval;
   pp.boundary_pos = a->boundary_pos;
   pp.cu_boundaries = a->cu_boundaries;
@@ -118,12 +152,15 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
   auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
 
   cudaError_t e = mark(0);
+  if (e == cudaSuccess && P > 1)
+    e = launch_scan_plan(a->cu_seqlens, a->total_tokens, P, reinterpret_cast<int64_t*>(w + L.scan_cu),
+                         stream);
   if (e == cudaSuccess) e = launch_plan(pp, stream);
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return KDA_ERR_CUDA;
 
   ChunkParams cp{};
-  cp.num_seqs = a->num_seqs;
+  cp.num_seqs = pp.num_seqs;
   cp.H = a->num_heads;
   cp.dk = a->dk;
   cp.dv = a->dv;
@@ -145,8 +182,19 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
   cp.chunks = pp.chunks;
   cp.inter = reinterpret_cast<float*>(w + L.inter);
   cp.rec_floats = L.rec_bytes / sizeof(float);
-  e = use_tensor_cores(a) ? launch_tc_prefill(cp, stream, ev ? ev[2] : nullptr)
-                          : launch_simt_prefill(cp, a->in_dtype, stream, ev ? ev[2] : nullptr);
+  if (P > 1) {
+    ScanBuffers sb;
+    sb.A = reinterpret_cast<float*>(w + L.scan_A);
+    sb.B = reinterpret_cast<float*>(w + L.scan_B);
+    sb.inits = reinterpret_cast<float*>(w + L.scan_inits);
+    sb.finals = reinterpret_cast<float*>(w + L.scan_finals);
+    sb.s0 = a->initial_state;
+    sb.final_state = a->final_state;
+    e = launch_tc_prefill_scan(cp, sb, stream, ev ? ev[2] : nullptr);
+  } else {
+    e = use_tensor_cores(a) ? launch_tc_prefill(cp, stream, ev ? ev[2] : nullptr)
+                            : launch_simt_prefill(cp, a->in_dtype, stream, ev ? ev[2] : nullptr);
+  }
   if (e == cudaSuccess) e = mark(3);
   return from_cuda(e);
 }

@@ -116,6 +116,9 @@ struct WsLayout {
          bnd_nonaligned = 0, bnd_nonmult = 0, seq_aux = 0, chunks = 0, inter = 0, total = 0;
   int64_t max_chunks = 0;
   size_t rec_bytes = 0;  // bytes of one (chunk, head) intermediate record
+  // segment scan: segment count (1 = off) and its buffers
+  int32_t scan_P = 1;
+  size_t scan_cu = 0, scan_A = 0, scan_B = 0, scan_inits = 0, scan_finals = 0;
 };
 
 }  // namespace kda

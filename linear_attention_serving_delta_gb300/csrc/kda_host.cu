@@ -127,6 +127,7 @@ kda_prefill_args piece_args(const kda_prefill_host_args* a, const HostLayout& L,
   s.b = w + L.b + p.tok0 * H * es;
   s.scale = a->scale;
   s.o = w + L.o + p.tok0 * H * a->dv * es;
+  s.scan_segments = 1;  // the pieces already cut the chain; keep kda_prefill's plain path
   float* init = a->initial_state ? reinterpret_cast<float*>(w + L.init) : nullptr;
   float* fin = reinterpret_cast<float*>(w + L.fin);
   float* carry = reinterpret_cast<float*>(w + L.carry);

@@ -51,7 +51,13 @@ struct ChunkParams {
   const Chunk* chunks;
   float* inter;     // [max_chunks][H] records
   size_t rec_floats;
+  // segment scan (tensor-core path): mode kScanPass1 runs grid z = 0..3 from
+  // a zero state (final -> final_state) and z = 4..7 as the transition maps
+  // (identity state, U~ taken as zero, final -> trans); no o or snapshots
+  int32_t k3_mode;
+  float* trans;     // [num_seqs][H][dk][dk] in kScanPass1
 };
+constexpr int32_t kScanPass1 = 1;
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 
@@ -65,6 +71,25 @@ cudaError_t launch_simt_prefill(const ChunkParams& p, kda_dtype_t dt, cudaStream
 extern const bool kHaveTensorCorePath;
 size_t tc_record_bytes();
 cudaError_t launch_tc_prefill(const ChunkParams& p, cudaStream_t stream, cudaEvent_t mid);
+// The segment scan over P chunk-aligned segments of one sequence (planned as
+// P sequences in `p`): K2 once, K3 pass 1 (state offsets B and transition
+// maps A of every segment, in parallel), the combine (inits[s+1] = A_s
+// inits[s] + B_s), K3 pass 2 from the true segment states.  Buffers are
+// [P][H][128][128] fp32; `s0` may be null (zeros); `final_state` (may be
+// null) receives the last segment's final state.
+struct ScanBuffers {
+  float* A;
+  float* B;
+  float* inits;
+  float* finals;
+  const float* s0;
+  float* final_state;
+};
+cudaError_t launch_tc_prefill_scan(const ChunkParams& p, const ScanBuffers& sb, cudaStream_t stream,
+                                   cudaEvent_t mid);
+// seg_cu[0..P] from cu_seqlens[0..1] of one sequence: chunk-aligned cuts
+cudaError_t launch_scan_plan(const int64_t* cu_seqlens, int64_t total_tokens, int32_t P,
+                             int64_t* seg_cu, cudaStream_t stream);
 
 cudaError_t launch_decode(const kda_decode_args& a, cudaStream_t stream);
 cudaError_t launch_prep(const kda_prep_args& a, cudaStream_t stream);

@@ -115,12 +115,12 @@ __device__ __forceinline__ void split8(const float* u, uint4& hi, uint4& lo) {
 }
 
 // o rows of one chunk from lanes 64-127 of an output accumulator: row i, this
-// thread's 16 columns
+// thread's 16 columns (none in the first pass of the segment scan)
 __device__ __forceinline__ void store_output(const ChunkParams& p, const Chunk& ch, uint32_t d1,
                                              int h16, int i, int h, int n0) {
   float d[kNh];
   tmem_ld_sum(d1, h16, d);
-  if (i < ch.len) {
+  if (i < ch.len && p.k3_mode != kScanPass1) {
     const float scale = p.scale;
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o);
     uint4* dst = reinterpret_cast<uint4*>(o + ((ch.tok0 + i) * p.H + h) * (int64_t)kD + n0 + h16);
@@ -166,7 +166,11 @@ tc_inter(ChunkParams p) {
   __shared__ __align__(8) uint64_t bar_drain;    // every MMA, on the error path
   __shared__ uint32_t tmem_base;
 
-  const int s = blockIdx.x, h = blockIdx.y, n0 = blockIdx.z * kNs;
+  const int s = blockIdx.x, h = blockIdx.y, n0 = (blockIdx.z & 3) * kNs;
+  // first pass of the segment scan: CTAs z >= 4 carry the transition map
+  // (identity state, U~ = 0), the others the state offset (zero state)
+  const bool pass1 = p.k3_mode == kScanPass1;
+  const bool trans = pass1 && blockIdx.z >= 4;
   const int H = p.H, tid = threadIdx.x, warp = tid >> 5;
   const int64_t c_begin = p.seq_chunk_begin[s], c_end = p.seq_chunk_begin[s + 1];
   if (c_end > c_begin && p.meta->total_chunks == 0) return;  // chunk table overflowed
@@ -228,11 +232,14 @@ tc_inter(ChunkParams p) {
     float v[kNh];
 #pragma unroll
     for (int n = 0; n < kNh; n += 4) {
-      float4 x = p.initial_state
+      float4 x = p.initial_state && !pass1
                      ? *reinterpret_cast<const float4*>(p.initial_state + sbase + (size_t)c * kD + n0 + h16 + n)
                      : make_float4(0.f, 0.f, 0.f, 0.f);
       v[n] = x.x; v[n + 1] = x.y; v[n + 2] = x.z; v[n + 3] = x.w;
     }
+    if (trans)
+#pragma unroll
+      for (int n = 0; n < kNh; ++n) v[n] = c == n0 + h16 + n ? 1.f : 0.f;
     float gl = 1.f;
     if (nchunks > 0) {
       okl = wait_chain(0);
@@ -319,11 +326,12 @@ tc_inter(ChunkParams p) {
       float d[kNh];
       tmem_ld_sum(d1_of(it) + lane_off, h16, d);
       const float* ut = reinterpret_cast<const float*>(slot + K3Smem::UT);
+      const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int m = 0; m < kNh / 8; ++m) {
         const int e = h16 + 8 * m;  // first of 8 columns
-        const float4 ua = *reinterpret_cast<const float4*>(ut + ((e / 4) * 64 + i) * 4);
-        const float4 ub = *reinterpret_cast<const float4*>(ut + ((e / 4 + 1) * 64 + i) * 4);
+        const float4 ua = trans ? zero4 : *reinterpret_cast<const float4*>(ut + ((e / 4) * 64 + i) * 4);
+        const float4 ub = trans ? zero4 : *reinterpret_cast<const float4*>(ut + ((e / 4 + 1) * 64 + i) * 4);
         const float u[8] = {ua.x - d[8 * m], ua.y - d[8 * m + 1], ua.z - d[8 * m + 2],
                             ua.w - d[8 * m + 3], ub.x - d[8 * m + 4], ub.y - d[8 * m + 5],
                             ub.z - d[8 * m + 6], ub.w - d[8 * m + 7]};
@@ -352,7 +360,7 @@ tc_inter(ChunkParams p) {
     {
       float v[kNh];
       tmem_ld_sum(DS, h16, v);
-      if (ch.snap_slot >= 0 && p.snapshots) {
+      if (ch.snap_slot >= 0 && p.snapshots && !pass1) {
         float* dst = p.snapshots + ((size_t)ch.snap_slot * H + h) * kD * kD + (size_t)c * kD + n0 + h16;
 #pragma unroll
         for (int n = 0; n < kNh; n += 4)
@@ -389,10 +397,11 @@ tc_inter(ChunkParams p) {
   fence_before_sync();
   ok = __syncthreads_and(ok && okl);
   fence_after_sync();
-  if (ok && p.final_state) {
+  float* const fin = trans ? p.trans : p.final_state;
+  if (ok && fin) {
     float v[kNh];
     tmem_ld_sum(DS, h16, v);
-    float* dst = p.final_state + sbase + (size_t)c * kD + n0 + h16;
+    float* dst = fin + sbase + (size_t)c * kD + n0 + h16;
 #pragma unroll
     for (int n = 0; n < kNh; n += 4)
       *reinterpret_cast<float4*>(dst + n) = make_float4(v[n], v[n + 1], v[n + 2], v[n + 3]);
@@ -436,6 +445,121 @@ cudaError_t launch_tc_prefill(const ChunkParams& p, cudaStream_t stream, cudaEve
   dim3 grid2((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)(kD / kNs));
   tc_inter<<<grid2, kThreads, K3Smem::BYTES, stream>>>(p);
   return cudaGetLastError();
+}
+
+namespace {
+
+using namespace tcp;
+
+// inits[0] = S0 (or zeros); inits[s+1] = A_s inits[s] + B_s.  One CTA per
+// (head, 32-column slice); thread t owns row t / 2 and 16 columns.  The
+// slice of the running state sits in shared memory; A_s rows are read
+// straight from global memory (L2), 4 floats at a time.
+__global__ void __launch_bounds__(256) scan_combine(ScanBuffers sb, int P, int H) {
+  __shared__ __align__(16) float S[kD * kNs];
+  const int h = blockIdx.x, n0 = blockIdx.y * kNs;
+  const int r = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * 16;
+  const size_t mat = (size_t)kD * kD;
+  float acc[16];
+  {
+    const float* s0 = sb.s0 ? sb.s0 + (size_t)h * mat + (size_t)r * kD + n0 + c0 : nullptr;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) acc[n] = s0 ? s0[n] : 0.f;
+  }
+  for (int s = 0;; ++s) {
+    float* out = sb.inits + ((size_t)s * H + h) * mat + (size_t)r * kD + n0 + c0;
+#pragma unroll
+    for (int n = 0; n < 16; n += 4) {
+      *reinterpret_cast<float4*>(out + n) = make_float4(acc[n], acc[n + 1], acc[n + 2], acc[n + 3]);
+      *reinterpret_cast<float4*>(S + r * kNs + c0 + n) = make_float4(acc[n], acc[n + 1], acc[n + 2], acc[n + 3]);
+    }
+    if (s + 1 >= P) break;
+    __syncthreads();
+    const float* a = sb.A + ((size_t)s * H + h) * mat + (size_t)r * kD;
+    const float* b = sb.B + ((size_t)s * H + h) * mat + (size_t)r * kD + n0 + c0;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) acc[n] = b[n];
+    for (int k = 0; k < kD; k += 4) {
+      const float4 a4 = __ldg(reinterpret_cast<const float4*>(a + k));
+      const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const float* srow = S + (k + kk) * kNs + c0;
+#pragma unroll
+        for (int n = 0; n < 16; n += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(srow + n);
+          acc[n] += av[kk] * x.x;
+          acc[n + 1] += av[kk] * x.y;
+          acc[n + 2] += av[kk] * x.z;
+          acc[n + 3] += av[kk] * x.w;
+        }
+      }
+    }
+    __syncthreads();  // every row of S read before it is overwritten
+  }
+}
+
+// Chunk-aligned cuts of one sequence [cu[0], cu[1]) into P segments.  A
+// malformed cu (cu[0] != 0, or cu[1] outside [0, total_tokens]) yields
+// segments the planning kernel flags (start 1) and skips (all empty).
+__global__ void scan_plan(const int64_t* cu, int64_t total_tokens, int32_t P, int64_t* seg_cu) {
+  if (threadIdx.x != 0) return;
+  const int64_t c0 = cu[0], len = cu[1] - cu[0];
+  if (c0 != 0 || len < 0 || cu[1] > total_tokens) {
+    for (int32_t s = 0; s <= P; ++s) seg_cu[s] = 1;
+    return;
+  }
+  const int64_t nch = (len + kChunk - 1) / kChunk;
+  const int64_t step = ((nch + P - 1) / P) * kChunk;
+  for (int32_t s = 0; s <= P; ++s) seg_cu[s] = s * step < len ? s * step : len;
+}
+
+}  // namespace
+
+cudaError_t launch_scan_plan(const int64_t* cu_seqlens, int64_t total_tokens, int32_t P,
+                             int64_t* seg_cu, cudaStream_t stream) {
+  scan_plan<<<1, 32, 0, stream>>>(cu_seqlens, total_tokens, P, seg_cu);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_prefill_scan(const ChunkParams& p, const ScanBuffers& sb, cudaStream_t stream,
+                                   cudaEvent_t mid) {
+  using namespace tcp;
+  cudaError_t e = launch_intra(p, stream);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc_inter, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)K3Smem::BYTES);
+  if (e != cudaSuccess) return e;
+  if (mid) {
+    e = cudaEventRecord(mid, stream);
+    if (e != cudaSuccess) return e;
+  }
+  // pass 1: the state offset B_s and the transition map A_s of every segment
+  ChunkParams p1 = p;
+  p1.k3_mode = kScanPass1;
+  p1.initial_state = nullptr;
+  p1.final_state = sb.B;
+  p1.trans = sb.A;
+  p1.snapshots = nullptr;
+  tc_inter<<<dim3((unsigned)p.num_seqs, (unsigned)p.H, 2 * (unsigned)(kD / kNs)), kThreads, K3Smem::BYTES,
+             stream>>>(p1);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  scan_combine<<<dim3((unsigned)p.H, (unsigned)(kD / kNs)), 256, 0, stream>>>(sb, p.num_seqs, p.H);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // pass 2: every segment from its true initial state
+  ChunkParams p2 = p;
+  p2.k3_mode = 0;
+  p2.initial_state = sb.inits;
+  p2.final_state = sb.finals;
+  p2.trans = nullptr;
+  tc_inter<<<dim3((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)(kD / kNs)), kThreads, K3Smem::BYTES,
+             stream>>>(p2);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !sb.final_state) return e;
+  return cudaMemcpyAsync(sb.final_state, sb.finals + (size_t)(p.num_seqs - 1) * p.H * kD * kD,
+                         (size_t)p.H * kD * kD * sizeof(float), cudaMemcpyDeviceToDevice, stream);
 }
 
 }  // namespace kda

@@ -54,7 +54,7 @@ class PrefillArgs(ctypes.Structure):
                 ("scale", c_f32), ("initial_state", c_vp), ("o", c_vp), ("final_state", c_vp),
                 ("snapshot_interval", c_i64), ("boundary_pos", c_vp), ("cu_boundaries", c_vp),
                 ("num_boundaries", c_i64), ("cu_snapshots", c_vp), ("snapshots", c_vp),
-                ("num_snapshots", c_i64), ("phase_events", c_vp)]
+                ("num_snapshots", c_i64), ("phase_events", c_vp), ("scan_segments", c_i32)]
 
 
 class PrefillHostArgs(ctypes.Structure):
@@ -162,7 +162,8 @@ def _check(status: int, what: str):
 
 def make_prefill_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=None,
                       final_state=None, snapshot_interval=0, boundary_pos=None,
-                      cu_boundaries=None, cu_snapshots=None, snapshots=None) -> PrefillArgs:
+                      cu_boundaries=None, cu_snapshots=None, snapshots=None,
+                      scan_segments=0) -> PrefillArgs:
     T, H, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
@@ -187,6 +188,7 @@ def make_prefill_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=
     a.cu_snapshots = _ptr(cu_snapshots, torch.int64, "cu_snapshots")
     a.snapshots = _ptr(snapshots, torch.float32, "snapshots")
     a.num_snapshots = 0 if snapshots is None else snapshots.shape[0]
+    a.scan_segments = int(scan_segments)
     return a
 
 
@@ -328,7 +330,7 @@ class Prefill:
     def __init__(self, q, k, v, g, b, cu_seqlens, *, scale=1.0, initial_state=None,
                  snapshot_interval=0, boundary_pos=None, cu_boundaries=None,
                  want_final=True, host_cu_seqlens=None, host_boundary_pos=None,
-                 host_cu_boundaries=None, o=None):
+                 host_cu_boundaries=None, o=None, scan_segments=0):
         dev = q.device
         T, H, dk = q.shape
         dv = v.shape[-1]
@@ -353,7 +355,8 @@ class Prefill:
             q, k, v, g, b, cu_seqlens, self.o, scale=scale, initial_state=initial_state,
             final_state=self.final_state, snapshot_interval=snapshot_interval,
             boundary_pos=boundary_pos, cu_boundaries=cu_boundaries,
-            cu_snapshots=self.cu_snapshots, snapshots=self.snapshots)
+            cu_snapshots=self.cu_snapshots, snapshots=self.snapshots,
+            scan_segments=scan_segments)
         nbytes = kda_prefill_workspace_size(self.args)
         if nbytes == 0:
             raise ValueError("kda_prefill_workspace_size rejected the arguments")

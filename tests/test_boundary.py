@@ -68,7 +68,7 @@ int main(void) {
   F(kda_prefill_args, scale) F(kda_prefill_args, initial_state)
   F(kda_prefill_args, snapshot_interval) F(kda_prefill_args, num_boundaries)
   F(kda_prefill_args, snapshots) F(kda_prefill_args, num_snapshots)
-  F(kda_prefill_args, phase_events)
+  F(kda_prefill_args, phase_events) F(kda_prefill_args, scan_segments)
   F(kda_decode_args, scale) F(kda_decode_args, q) F(kda_decode_args, state_slots)
   F(kda_decode_args, o)
   F(kda_prep_args, total_tokens) F(kda_prep_args, in_dtype) F(kda_prep_args, beta)
@@ -124,6 +124,21 @@ def test_workspace_size_and_validation(kda):
     # the workspace grows with tokens, sequences and boundaries
     big = _args(kda, total_tokens=8192)
     assert L.kda_prefill_workspace_size(ctypes.byref(big)) > ws
+    # segment scan: out-of-range counts are rejected; on the tensor-core path
+    # (bf16, 128 x 128) with few heads and one long sequence it adds its
+    # per-segment state buffers (4 x P x H x 64 KB)
+    for bad in (-1, 65):
+        a = _args(kda, scan_segments=bad)
+        assert L.kda_prefill_workspace_size(ctypes.byref(a)) == 0
+        assert L.kda_prefill(ctypes.byref(a), 0x4000, 1 << 30, None) == 1
+    tc = dict(in_dtype=kda.KDA_BF16, dk=128, dv=128, num_heads=2, total_tokens=65536)
+    off = L.kda_prefill_workspace_size(ctypes.byref(_args(kda, scan_segments=1, **tc)))
+    auto = L.kda_prefill_workspace_size(ctypes.byref(_args(kda, **tc)))
+    four = L.kda_prefill_workspace_size(ctypes.byref(_args(kda, scan_segments=4, **tc)))
+    mat = 2 * 128 * 128 * 4
+    assert four - off >= 4 * 4 * mat and auto - off >= 4 * 9 * mat  # auto: 152 // 16 = 9
+    # never with several sequences, snapshots, or on the fp32 path
+    assert L.kda_prefill_workspace_size(ctypes.byref(_args(kda, scan_segments=4))) == ws
     assert L.kda_prefill(None, 0x4000, ws, None) == 1
     assert kda.kda_status_string(3).startswith("workspace")
 

@@ -278,6 +278,48 @@ def test_prefill_host_pageable_and_empty():
     assert torch.equal(S0, e["S0"])
 
 
+@pytest.mark.parametrize("H,T,P", [(2, 20000, 0), (3, 5000, 5), (1, 300, 8), (2, 4113, 3)])
+def test_prefill_segment_scan(H, T, P):
+    """The segment scan (the chain cut into P chunk-aligned segments; their
+    state offsets and transition maps in parallel, a serial combine, a second
+    pass from the true segment states) gives the oracle's o and final state.
+    P = 0 is the automatic choice (9 segments for 2 heads and 313 chunks);
+    P = 8 over 5 chunks leaves three segments empty."""
+    inp = make_inputs([T], H, 128, 128, "bf16", 61 + H, s0_std=0.05)
+    d = to_dev(inp)
+    kw = dict(scale=0.9, initial_state=d["S0"], host_cu_seqlens=inp["cu_seqlens"])
+    args = [d[x] for x in "qkvgb"] + [d["cu_seqlens"]]
+    p = kda.Prefill(*args, scan_segments=P, **kw)
+    plain = kda.Prefill(*args, scan_segments=1, **kw)
+    assert p.workspace.numel() > plain.workspace.numel()  # the scan's buffers: it is on
+    p.run()
+    plain.run()
+    torch.cuda.synchronize()
+    assert p.device_status() == 0
+    import oracle
+    ro, rS, _ = oracle.prefill(host(inp["q"]), host(inp["k"]), host(inp["v"]), host(inp["g"]),
+                               host(inp["b"]), inp["cu_seqlens"].numpy(), S0=host(inp["S0"]),
+                               scale=0.9)
+    assert rel(host(p.o), ro) <= TOL["bf16"]
+    assert rel(host(p.final_state), rS) <= TOL["bf16"]
+    # and the unsplit chain agrees to rounding of the fp32 state
+    assert rel(host(p.final_state), host(plain.final_state)) < 1e-4
+    assert rel(host(p.o), host(plain.o)) < 2e-3
+
+
+def test_prefill_segment_scan_bad_seqlens():
+    """A malformed cu_seqlens on the segment-scan path raises status flag 1
+    and leaves the sequence's state as it was, like the plain path."""
+    inp = make_inputs([4096], 2, 128, 128, "bf16", 66, s0_std=0.05)
+    d = to_dev(inp)
+    bad = torch.tensor([0, 4096 + 5], dtype=torch.int64, device="cuda")
+    p = kda.Prefill(*(d[x] for x in "qkvgb"), bad, initial_state=d["S0"], scan_segments=4,
+                    host_cu_seqlens=inp["cu_seqlens"]).run()
+    torch.cuda.synchronize()
+    assert p.device_status() & 1
+    np.testing.assert_array_equal(host(p.final_state), host(inp["S0"]))
+
+
 def oracle_prefill_of(inp):
     import oracle
     return oracle.prefill(host(inp["q"]), host(inp["k"]), host(inp["v"]), host(inp["g"]),

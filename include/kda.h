@@ -24,8 +24,9 @@
  * Conventions shared by every call.
  *   - Every tensor is caller-owned device memory, row-major and contiguous,
  *     token-major: q, k, g [T, H, dk]; v, o [T, H, dv]; b [T, H]; states
- *     [.., H, dk, dv] fp32.  The library allocates nothing and keeps no
- *     mutable global state; calls from several host threads are safe.
+ *     [.., H, dk, dv] fp32.  The library allocates no device memory and keeps
+ *     no mutable global state (the prefix cache's host index lives in the
+ *     object the caller creates); calls from several host threads are safe.
  *   - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
  *     default stream).  Arguments are validated on the host before any
  *     launch; on an error nothing is launched and the status says why.
@@ -108,6 +109,14 @@ typedef struct {
                                   inter-chunk), for per-kernel timing             */
   int32_t scan_segments;       /* segment scan: 0 = automatic, 1 = off, P >= 2 = P
                                   segments (see below); at most 64                */
+  const int32_t* snapshot_slot_map; /* device [snapshot_map_len] or NULL: snapshot j of
+                                  the call (j counted through cu_snapshots) goes to row
+                                  snapshot_slot_map[j] of `snapshots` instead of row
+                                  j; a negative entry skips it; a row at or past
+                                  num_snapshots, or j at or past snapshot_map_len,
+                                  raises status flag 2 (for a prefix cache choosing
+                                  pool rows, see kda_prefix_cache_reserve)        */
+  int64_t snapshot_map_len;    /* entries of snapshot_slot_map (0 if NULL)       */
 } kda_prefill_args;
 
 /*
@@ -240,6 +249,51 @@ kda_status_t kda_prefill_device_status(const void* ws, int32_t* out, void* strea
 int64_t kda_snapshot_plan(const int64_t* h_cu_seqlens, int32_t n, int64_t interval,
                           const int64_t* h_boundary_pos, const int64_t* h_cu_boundaries,
                           int64_t* h_cu_snapshots_out);
+
+/*
+ * Snapshot retention (a prefix cache over a pool of saved states).
+ *
+ * A serving host keeps states of earlier prompts in a pool of device rows
+ * ([rows, H, dk, dv] fp32, caller-owned) so that a later prompt sharing a
+ * prefix resumes from the saved state instead of recomputing it ("Kimi K3:
+ * The Manos, The Mythos, The Legendos", Context: the engine keeps selected
+ * checkpoints, prompt boundaries among them; more of them cost memory and
+ * save recomputation, so the retention policy matters).  These calls are
+ * the policy: they track which row holds the state after which prefix of
+ * token ids, and they never touch device memory.  They are the only calls of
+ * the library that allocate (host memory for their index).
+ *
+ *   - An entry is keyed by its length p and two independent 64-bit hashes
+ *     of the first p token ids (a false match needs both to collide).
+ *   - kda_prefix_cache_lookup returns the longest cached prefix of
+ *     tokens[0..n) (0 if none) and its row in *row (-1 if none), and marks
+ *     it recently used.  Resume with initial_state = that row, over the
+ *     tokens from p on.
+ *   - kda_prefix_cache_reserve assigns rows for the states a prefill of
+ *     tokens[0..n) will save at positions pos[0..m) (strictly increasing,
+ *     1..n); is_boundary[i] != 0 marks prompt-boundary checkpoints (may be
+ *     NULL: none).  rows_out[i] is the row to write, or -1 when the state
+ *     is already cached (it is marked used) or no row could be freed.
+ *     Pass rows_out as kda_prefill's snapshot_slot_map.  When the pool is
+ *     full, interval checkpoints are evicted before boundary ones, least
+ *     recently used first; boundary positions are placed first, then the
+ *     others from the latest back, and a reservation never evicts a row it
+ *     placed itself nor keep_row (the row the prefill resumes from, so that
+ *     its initial state and its snapshots do not overlap; -1 = none).
+ *     Returns the number of rows assigned, -1 on invalid arguments.  An entry is valid once the prefill that writes its row has
+ *     run (order lookups' use of a row after it, e.g. on one stream).
+ *   - Calls on one cache are serialised by an internal lock.
+ */
+typedef struct kda_prefix_cache kda_prefix_cache;
+
+kda_prefix_cache* kda_prefix_cache_create(int64_t num_rows); /* NULL if num_rows < 1 */
+void kda_prefix_cache_destroy(kda_prefix_cache* cache);
+int64_t kda_prefix_cache_entries(kda_prefix_cache* cache);   /* -1 if cache is NULL */
+int64_t kda_prefix_cache_lookup(kda_prefix_cache* cache, const int32_t* tokens, int64_t n,
+                                int32_t* row);
+int64_t kda_prefix_cache_reserve(kda_prefix_cache* cache, const int32_t* tokens, int64_t n,
+                                 const int64_t* pos, const uint8_t* is_boundary, int64_t m,
+                                 int32_t keep_row, int32_t* rows_out);
 
 /*
  * One decode step for a batch of independent rows ("constant decode": a

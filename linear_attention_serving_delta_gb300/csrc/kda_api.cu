@@ -61,6 +61,8 @@ kda_status_t validate_prefill(const kda_prefill_args* a) {
   if ((a->snapshots == nullptr) != (a->cu_snapshots == nullptr)) return KDA_ERR_INVALID_ARG;
   if (a->num_snapshots < 0 || (a->snapshots && a->num_snapshots == 0)) return KDA_ERR_INVALID_ARG;
   if (a->scan_segments < 0 || a->scan_segments > kMaxScanSegments) return KDA_ERR_INVALID_ARG;
+  if (a->snapshot_slot_map && (!a->snapshots || a->snapshot_map_len < 0)) return KDA_ERR_INVALID_ARG;
+  if (!a->snapshot_slot_map && a->snapshot_map_len != 0) return KDA_ERR_INVALID_ARG;
   // sizes whose products must stay inside the index types used by the kernels
   if (a->total_tokens > ((int64_t)1 << 40)) return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
@@ -137,6 +139,8 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
   pp.num_boundaries = a->num_boundaries;
   pp.cu_snapshots = a->cu_snapshots;
   pp.num_snapshots = a->snapshots ? a->num_snapshots : 0;
+  pp.slot_map = a->snapshot_slot_map;
+  pp.map_len = a->snapshot_slot_map ? a->snapshot_map_len : 0;
   pp.max_chunks = L.max_chunks;
   pp.status = reinterpret_cast<int32_t*>(w + L.status);
   pp.meta = reinterpret_cast<PlanMeta*>(w + L.meta);

@@ -16,6 +16,8 @@ struct PlanParams {
   int64_t num_boundaries;
   const int64_t* cu_snapshots;
   int64_t num_snapshots;
+  const int32_t* slot_map;  // [map_len] or null: snapshot index -> row of the snapshot buffer
+  int64_t map_len;
   int64_t max_chunks;
   // workspace outputs
   int32_t* status;

@@ -154,8 +154,20 @@ __device__ void fill_segment(const PlanParams& p, int64_t gidx, int32_t& bad) {
       if (is_mult || is_bnd) {
         int64_t rank = (p.snapshot_interval > 0 ? end / p.snapshot_interval : 0) +
                        (has_b ? p.bnd_nonmult[jb + s] : 0) - 1;
-        int64_t sl = snap_lo + rank;
-        if (sl >= snap_lo && sl < snap_hi && sl < p.num_snapshots) slot = (int32_t)sl; else bad = 1;
+        const int64_t sl = snap_lo + rank;
+        if (sl < snap_lo || sl >= snap_hi) {
+          bad = 1;
+        } else if (p.slot_map) {
+          // snapshot sl goes to the row the map gives (negative: not written)
+          const int32_t row = sl < p.map_len ? p.slot_map[sl] : INT32_MAX;
+          if (row < 0) slot = -1;
+          else if (row < p.num_snapshots) slot = row;
+          else bad = 1;
+        } else if (sl < p.num_snapshots) {
+          slot = (int32_t)sl;
+        } else {
+          bad = 1;
+        }
       }
     }
     if (ci < p.max_chunks) {

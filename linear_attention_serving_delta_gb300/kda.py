@@ -32,6 +32,8 @@ _STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED"
                  6: "KDA_ERR_DEVICE_DATA"}
 EXPORTED = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_noalloc",
             "kda_prefill_host_workspace_size", "kda_prefill_host",
+            "kda_prefix_cache_create", "kda_prefix_cache_destroy", "kda_prefix_cache_entries",
+            "kda_prefix_cache_lookup", "kda_prefix_cache_reserve",
             "kda_prefill_device_status", "kda_snapshot_plan", "kda_decode_step", "kda_prep",
             "kda_status_string", "kda_version")
 NOALLOC_SCRATCH_BYTES = 64 << 20  # fixed workspace behind kda_prefill_noalloc
@@ -54,7 +56,8 @@ class PrefillArgs(ctypes.Structure):
                 ("scale", c_f32), ("initial_state", c_vp), ("o", c_vp), ("final_state", c_vp),
                 ("snapshot_interval", c_i64), ("boundary_pos", c_vp), ("cu_boundaries", c_vp),
                 ("num_boundaries", c_i64), ("cu_snapshots", c_vp), ("snapshots", c_vp),
-                ("num_snapshots", c_i64), ("phase_events", c_vp), ("scan_segments", c_i32)]
+                ("num_snapshots", c_i64), ("phase_events", c_vp), ("scan_segments", c_i32),
+                ("snapshot_slot_map", c_vp), ("snapshot_map_len", c_i64)]
 
 
 class PrefillHostArgs(ctypes.Structure):
@@ -101,6 +104,17 @@ def lib() -> ctypes.CDLL:
             L.kda_prefill_host.argtypes = [ctypes.POINTER(PrefillHostArgs), c_vp, ctypes.c_size_t,
                                            c_vp]
             L.kda_prefill_host.restype = ctypes.c_int
+            L.kda_prefix_cache_create.argtypes = [c_i64]
+            L.kda_prefix_cache_create.restype = c_vp
+            L.kda_prefix_cache_destroy.argtypes = [c_vp]
+            L.kda_prefix_cache_destroy.restype = None
+            L.kda_prefix_cache_entries.argtypes = [c_vp]
+            L.kda_prefix_cache_entries.restype = c_i64
+            L.kda_prefix_cache_lookup.argtypes = [c_vp, c_vp, c_i64, ctypes.POINTER(c_i32)]
+            L.kda_prefix_cache_lookup.restype = c_i64
+            L.kda_prefix_cache_reserve.argtypes = [c_vp, c_vp, c_i64, c_vp, c_vp, c_i64, c_i32,
+                                                   c_vp]
+            L.kda_prefix_cache_reserve.restype = c_i64
             L.kda_prefill_noalloc.argtypes = [ctypes.POINTER(PrefillArgs), c_vp]
             L.kda_prefill_noalloc.restype = ctypes.c_int
             L.kda_prefill_device_status.argtypes = [c_vp, ctypes.POINTER(c_i32), c_vp]
@@ -163,7 +177,7 @@ def _check(status: int, what: str):
 def make_prefill_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=None,
                       final_state=None, snapshot_interval=0, boundary_pos=None,
                       cu_boundaries=None, cu_snapshots=None, snapshots=None,
-                      scan_segments=0) -> PrefillArgs:
+                      scan_segments=0, snapshot_slot_map=None) -> PrefillArgs:
     T, H, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
@@ -189,6 +203,8 @@ def make_prefill_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=
     a.snapshots = _ptr(snapshots, torch.float32, "snapshots")
     a.num_snapshots = 0 if snapshots is None else snapshots.shape[0]
     a.scan_segments = int(scan_segments)
+    a.snapshot_slot_map = _ptr(snapshot_slot_map, torch.int32, "snapshot_slot_map")
+    a.snapshot_map_len = 0 if snapshot_slot_map is None else snapshot_slot_map.numel()
     return a
 
 
@@ -330,7 +346,8 @@ class Prefill:
     def __init__(self, q, k, v, g, b, cu_seqlens, *, scale=1.0, initial_state=None,
                  snapshot_interval=0, boundary_pos=None, cu_boundaries=None,
                  want_final=True, host_cu_seqlens=None, host_boundary_pos=None,
-                 host_cu_boundaries=None, o=None, scan_segments=0):
+                 host_cu_boundaries=None, o=None, scan_segments=0, snapshot_pool=None,
+                 snapshot_slot_map=None):
         dev = q.device
         T, H, dk = q.shape
         dv = v.shape[-1]
@@ -349,19 +366,25 @@ class Prefill:
             cs, n_snap = kda_snapshot_plan(hcu, snapshot_interval, hbp, hcb)
             self.n_snap = n_snap
             self.cu_snapshots = torch.from_numpy(cs).to(dev)
-            self.snapshots = torch.empty(max(n_snap, 1), H, dk, dv, dtype=torch.float32,
-                                         device=dev)
+            if snapshot_pool is not None:
+                # snapshots go to the pool rows the slot map names
+                self.snapshots = snapshot_pool
+            else:
+                self.snapshots = torch.empty(max(n_snap, 1), H, dk, dv, dtype=torch.float32,
+                                             device=dev)
         self.args = make_prefill_args(
             q, k, v, g, b, cu_seqlens, self.o, scale=scale, initial_state=initial_state,
             final_state=self.final_state, snapshot_interval=snapshot_interval,
             boundary_pos=boundary_pos, cu_boundaries=cu_boundaries,
             cu_snapshots=self.cu_snapshots, snapshots=self.snapshots,
-            scan_segments=scan_segments)
+            scan_segments=scan_segments,
+            snapshot_slot_map=snapshot_slot_map if self.snapshots is not None else None)
         nbytes = kda_prefill_workspace_size(self.args)
         if nbytes == 0:
             raise ValueError("kda_prefill_workspace_size rejected the arguments")
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-        self._keep = (q, k, v, g, b, cu_seqlens, initial_state, boundary_pos, cu_boundaries)
+        self._keep = (q, k, v, g, b, cu_seqlens, initial_state, boundary_pos, cu_boundaries,
+                      snapshot_slot_map)
 
     def run(self, stream=None):
         kda_prefill(self.args, self.workspace, stream)
@@ -456,6 +479,92 @@ class PrefillHost:
     def run(self, stream=None):
         kda_prefill_host(self.args, self.workspace, stream)
         return self
+
+
+class PrefixCache:
+    """The snapshot retention policy of kda.h (``kda_prefix_cache_*``): which
+    row of a device state pool holds the state after which prefix of token
+    ids.  Host-side only; the pool itself is a tensor the caller owns."""
+
+    def __init__(self, num_rows: int):
+        self._h = lib().kda_prefix_cache_create(int(num_rows))
+        if not self._h:
+            raise ValueError("kda_prefix_cache_create failed")
+        self.num_rows = int(num_rows)
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h and _lib is not None:
+            _lib.kda_prefix_cache_destroy(h)
+
+    @staticmethod
+    def _tokens(tokens):
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        return t, (t.ctypes.data if t.size else None)
+
+    def entries(self) -> int:
+        return int(lib().kda_prefix_cache_entries(self._h))
+
+    def lookup(self, tokens):
+        """(p, row): the longest cached prefix of ``tokens`` and its pool row
+        (0, -1 if none)."""
+        t, tp = self._tokens(tokens)
+        row = c_i32(-1)
+        p = lib().kda_prefix_cache_lookup(self._h, tp, t.size, ctypes.byref(row))
+        if p < 0:
+            raise ValueError("kda_prefix_cache_lookup rejected the arguments")
+        return int(p), int(row.value)
+
+    def reserve(self, tokens, positions, boundary=None, keep_row=-1):
+        """Rows for the states at ``positions`` (increasing, 1..len(tokens));
+        ``boundary``: per position, True for prompt-boundary checkpoints;
+        ``keep_row``: a row not to evict (the one being resumed from).
+        Returns an int32 array (-1: already cached or no row)."""
+        t, tp = self._tokens(tokens)
+        pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+        bnd = None if boundary is None else np.ascontiguousarray(np.asarray(boundary, dtype=np.uint8))
+        if bnd is not None and bnd.size != pos.size:
+            raise ValueError("boundary needs one flag per position")
+        rows = np.full(pos.size, -1, dtype=np.int32)
+        n = lib().kda_prefix_cache_reserve(self._h, tp, t.size, pos.ctypes.data if pos.size else None,
+                                           None if bnd is None else bnd.ctypes.data, pos.size,
+                                           int(keep_row), rows.ctypes.data if pos.size else None)
+        if n < 0:
+            raise ValueError("kda_prefix_cache_reserve rejected the arguments")
+        return rows
+
+
+def prefill_cached(cache: PrefixCache, pool, tokens, q, k, v, g, b, *, interval=4096,
+                   scale=1.0, stream=None):
+    """One prompt through the prefix cache (single sequence, device tensors
+    [T, H, .] for all of its tokens): resume from the longest cached prefix
+    p, prefill tokens p..T with ``kda_prefill`` from the pool row's state,
+    and save the states at the multiples of ``interval`` past p and at the
+    prompt end into the rows the cache assigns (``snapshot_slot_map``).
+    Returns (p, o for tokens p..T, final state [1, H, dk, dv])."""
+    T = q.shape[0]
+    if len(tokens) != T:
+        raise ValueError("one token id per row of q")
+    if T == 0:
+        raise ValueError("an empty prompt has nothing to prefill")
+    p, row = cache.lookup(tokens)
+    if p == T:
+        # the whole prompt is cached: nothing to run, the state is the row's
+        return p, q.new_empty((0,) + tuple(v.shape[1:])), pool[row:row + 1].clone()
+    absolute = [x for x in range(interval * (p // interval + 1), T, interval)] if interval > 0 else []
+    absolute.append(T)
+    rows = cache.reserve(tokens, absolute, [False] * (len(absolute) - 1) + [True], keep_row=row)
+    dev = q.device
+    rel = torch.tensor([x - p for x in absolute], dtype=torch.int64)
+    cu_b = torch.tensor([0, len(absolute)], dtype=torch.int64)
+    hcu = torch.tensor([0, T - p], dtype=torch.int64)
+    pr = Prefill(q[p:], k[p:], v[p:], g[p:], b[p:], hcu.to(dev),
+                 scale=scale, initial_state=pool[row:row + 1] if p > 0 else None,
+                 boundary_pos=rel.to(dev), cu_boundaries=cu_b.to(dev),
+                 host_cu_seqlens=hcu, host_boundary_pos=rel, host_cu_boundaries=cu_b,
+                 snapshot_pool=pool, snapshot_slot_map=torch.from_numpy(rows).to(dev))
+    pr.run(stream)
+    return p, pr.o, pr.final_state
 
 
 def decode_step(q, k, v, g, b, state, state_slots=None, scale=1.0, o=None, stream=None):

@@ -39,10 +39,15 @@ constexpr uint32_t kB1Lbo = 64 * 16 + 16;   // B1 K-major, R=64
 constexpr uint32_t kB2Sbo = 8 * 128 + 16;   // B2 MN-major (n, token): stride between 8-n groups
 constexpr uint32_t kA2Lbo = 64 * 16 + 16;   // A2 (T diag(beta)) K-major, R=64
 constexpr uint32_t kAkStage = 8 * 128 + 16; // Kr^T staged for its record copy: stride between 8-channel groups
-// threads that issue the record's bulk copies (each waits for its own)
-constexpr int kAwCopy0 = 0;    // AW: threads 0-15, one 8-channel group each
-constexpr int kAkCopy0 = 32;   // AK: threads 32-47, one 8-channel group each
+// threads that issue the record's bulk copies (each waits for its own).  The
+// AW and AK copies go one per 8-channel group g, from lane g % 2 of warp
+// g / 2: a bulk-copy issue holds its warp until the copy engine takes it, so
+// spreading the 16 of a tile over the warps keeps any one warp from waiting
+// for all of them.
 constexpr int kAqCopy = 64;    // A_qk
+__device__ __forceinline__ int copy_group(int tid) {
+  return (tid & 31) < 2 ? 2 * (tid >> 5) + (tid & 31) : -1;
+}
 
 struct Smem {
   static constexpr uint32_t A1 = 0;                    // [Kp;Qp] -> [W;Qp], K=128 (16 groups)
@@ -205,14 +210,24 @@ __device__ __forceinline__ void tma_rows_l2(const CUtensorMap* m, int h, int tok
                : "memory");
 }
 
+// What an item needs of its chunk-table entry: first token and length (the
+// token index fits the int32 coordinates of the tensor maps on this path).
+// Two registers instead of the entry's eight.
+struct ItemChunk {
+  int tok0, len;
+};
+__device__ __forceinline__ ItemChunk item_chunk(const Chunk* chunks, int64_t idx) {
+  return ItemChunk{(int)chunks[idx].tok0, chunks[idx].len};
+}
+
 // One staging group: the rows of two tensors of item (ch, h), both counted
 // on `bar`.  Issued by one thread.
-__device__ __forceinline__ void stage_group(uint8_t* sm, uint64_t* bar, const Chunk& ch, int h,
+__device__ __forceinline__ void stage_group(uint8_t* sm, uint64_t* bar, const ItemChunk& ch, int h,
                                             const CUtensorMap* t0, uint32_t s0, const CUtensorMap* t1,
                                             uint32_t s1) {
   mbar_arrive_expect_tx(bar, 2 * kRowsBytes);
-  tma_rows(sm + s0, t0, h, (int)ch.tok0, bar);
-  tma_rows(sm + s1, t1, h, (int)ch.tok0, bar);
+  tma_rows(sm + s0, t0, h, ch.tok0, bar);
+  tma_rows(sm + s1, t1, h, ch.tok0, bar);
 }
 
 // 16 bytes of a raw row in a staging: token i, channels c0..c0+7
@@ -220,9 +235,9 @@ __device__ __forceinline__ uint4 raw16(const uint8_t* sm, uint32_t stage, int i,
   return *reinterpret_cast<const uint4*>(sm + stage + i * 256 + c0 * 2);
 }
 
-__device__ __forceinline__ float load_b(const ChunkParams& p, const Chunk& ch, int h, int tid) {
+__device__ __forceinline__ float load_b(const ChunkParams& p, const ItemChunk& ch, int h, int tid) {
   const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(p.b);
-  return (tid < 64 && tid < ch.len) ? __bfloat162float(gb[(ch.tok0 + tid) * p.H + h]) : 0.f;
+  return (tid < 64 && tid < ch.len) ? __bfloat162float(gb[((int64_t)ch.tok0 + tid) * p.H + h]) : 0.f;
 }
 
 // Persistent: two CTAs per SM walk the (chunk, head) items with stride
@@ -274,8 +289,8 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
   // the pipeline: chunk entries of the current and the next item; the first
   // item's rows are staged here (groups A and B), each later item's during
   // the item before it
-  Chunk ch = p.chunks[item / H];  // entries past the table's end have len 0
-  Chunk ch_next = item + stride < n_items ? p.chunks[(item + stride) / H] : Chunk{};
+  ItemChunk ch = item_chunk(p.chunks, item / H);  // entries past the table's end have len 0
+  ItemChunk ch_next = item + stride < n_items ? item_chunk(p.chunks, (item + stride) / H) : ItemChunk{0, 0};
   {
     const int h0 = (int)(item % H);
     if (tid == 0) {
@@ -302,13 +317,13 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     if (len == 0) break;
     uint8_t* rec = reinterpret_cast<uint8_t*>(p.inter) + ((size_t)cidx * H + h) * Rec::BYTES;
     const bool has_next = item + stride < n_items;
-    const Chunk chn = ch_next;
+    const ItemChunk chn = ch_next;
     const int hn = (int)((item + stride) % H);
     const float bcur = bnext;
     // the next item's rows into L2 now, so that their staging copies hit L2
     if (has_next && tid < 4)
       tma_rows_l2(tid == 0 ? &maps.g : tid == 1 ? &maps.k : tid == 2 ? &maps.q : &maps.v, hn,
-                  (int)chn.tok0);
+                  chn.tok0);
     // this item's g and k (group A) have landed; q and v (group B) may still fly
     ok = mbar_wait(&bar_ga, sph, kWaitLimitNs);
     a_fly = false;
@@ -384,13 +399,17 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     }
     if (tid < 64) beta[tid] = tid < len ? beta_of(bcur) : 0.f;
     // the previous item's record copies must have read A1 before it is rewritten
-    if (tid < kAwCopy0 + 16) bulk_wait_read_all();
+    if (copy_group(tid) >= 0) bulk_wait_read_all();
     ok = __syncthreads_and(ok);
     if (!ok) break;
     if (tid < 64) {
       inv_q[tid] = inv_norm_of(nrm[tid] + nrm[64 + tid]);
       inv_k[tid] = inv_norm_of(nrm[128 + tid] + nrm[192 + tid]);
     }
+    // ---- V into B2 MN-major rows 128..255 (every raw row has been read:
+    // the staging is free): the raw 16 bytes are one core-matrix row
+#pragma unroll
+    for (int r = 0; r < 4; ++r) st_s16(B2, mnmajor_off(128 + c0, i0 + r, kB2Sbo), vraw[r]);
     // the decay entering this token quarter, and the chunk total Gamma_L
     float GLm[8];
     {
@@ -416,10 +435,6 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
       }
     }
     __syncthreads();
-
-    // ---- V into B2 MN-major rows 128..255: the raw 16 bytes are one core-matrix row
-#pragma unroll
-    for (int r = 0; r < 4; ++r) st_s16(B2, mnmajor_off(128 + c0, i0 + r, kB2Sbo), vraw[r]);
 
     // ---- operands Kp, Qp (A1), Kn (B1), Kp (B2 MN-major rows 0-127), Kr
     // (staged MN-major in the A_kk tile for the record's AK)
@@ -467,8 +482,8 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
 
     // Kr^T to the record's AK, one bulk copy per 8-channel group (dropping
     // the staging's padding)
-    if (tid >= kAkCopy0 && tid < kAkCopy0 + 16) {
-      const int g = tid - kAkCopy0;
+    if (copy_group(tid) >= 0) {
+      const int g = copy_group(tid);
       bulk_s2g(rec + Rec::AK + g * Rec::kAkSbo, AKS + g * kAkStage, Rec::kAkSbo);
       bulk_commit();
     }
@@ -482,7 +497,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
       mma_commit(&bar_mma);
     }
     // the A_kk tile is rewritten below: the AK copies must have read it
-    if (tid >= kAkCopy0 && tid < kAkCopy0 + 16) bulk_wait_read_all();
+    if (copy_group(tid) >= 0) bulk_wait_read_all();
     ok = __syncthreads_and(mbar_wait(&bar_mma, 0, kWaitLimitNs));
     fence_after_sync();
     if (!ok) break;
@@ -607,12 +622,13 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     // [W ; Qp] to the record's unpadded layout, one bulk copy per 8-channel
     // group, each from its own thread; their reads are awaited before A1 is
     // rewritten by the next item
-    if (tid < kAwCopy0 + 16) {
-      bulk_s2g(rec + Rec::AW + tid * 128 * 16, A1 + tid * kA1Lbo, 128 * 16);
+    if (copy_group(tid) >= 0) {
+      const int g = copy_group(tid);
+      bulk_s2g(rec + Rec::AW + g * 128 * 16, A1 + g * kA1Lbo, 128 * 16);
       bulk_commit();
     }
     ch = ch_next;
-    ch_next = item + 2 * stride < n_items ? p.chunks[(item + 2 * stride) / H] : Chunk{};
+    ch_next = item + 2 * stride < n_items ? item_chunk(p.chunks, (item + 2 * stride) / H) : ItemChunk{0, 0};
   }
   // no staging copy is left in flight when the CTA exits (waits bounded)
   if (a_fly) mbar_wait(&bar_ga, sph, kWaitLimitNs);

@@ -190,6 +190,35 @@ def bench_prefill(torch, kda, W, steps, warmup, dev):
                 launches_per_step=3, workload=w)
 
 
+def bench_prep(torch, kda, W, dev, reps=10):
+    """The preparation step alone (kda_prep: q^, k^, beta, chunk-restarted G)
+    on the prefill_8k inputs, against HBM: it reads q, k, g (bf16) and b and
+    writes q^, k^, G (fp32) and beta.  L2 flushed before every call."""
+    w = W.WORKLOADS[PREFILL_WL]
+    inp = W.prefill_inputs(w, device=dev, gen_device=dev)
+    T, H, dk = inp["q"].shape
+    f = dict(dtype=torch.float32, device=dev)
+    qh, kh, G = (torch.empty(T, H, dk, **f) for _ in range(3))
+    beta = torch.empty(T, H, **f)
+    args = (inp["q"], inp["k"], inp["g"], inp["b"], inp["cu_seqlens"], qh, kh, G, beta)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        kda.kda_prep(*args)
+    ms = []
+    for _ in range(reps):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        kda.kda_prep(*args)
+        e1.record()
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    t = sum(ms) / len(ms)
+    nbytes = T * H * (3 * dk * 2 + 2) + T * H * (3 * dk * 4 + 4)
+    return {"workload": "prefill_8k inputs (T=8192, H=32, dk=128, bf16 in, fp32 out)",
+            "us": t * 1e3, "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (t * 1e-3) / 1e9}
+
+
 def bench_scan(torch, kda, W, dev, T=131072, H=2, reps=5):
     """The segment scan against the plain chunk chain on a workload it is
     for: one sequence of T tokens with few heads (bf16, 128 x 128), so that
@@ -348,6 +377,7 @@ def gpu_arm(a):
     step_ms, dec_ms = max_over_ranks(dist, world, [step_ms, dec_ms], dev)
     e2e = bench_e2e(torch, kda, W, max(1, min(a.steps, 5)), 1, dev) if rank == 0 else None
     scan = bench_scan(torch, kda, W, dev) if rank == 0 else None
+    prep = bench_prep(torch, kda, W, dev) if rank == 0 else None
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -419,6 +449,8 @@ def gpu_arm(a):
                 "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
                 "ms_per_step": e2e["ms_per_step"]},
         "segment_scan": scan,
+        "prep": dict(prep, peak=pk["hbm_gbs"], frac=prep["achieved_gbs"] / pk["hbm_gbs"],
+                     unit="GB/s", bound="hbm"),
         "gpu_launches": pre["launches_per_step"] * a.steps + dec["steps"],
         "clocks": clk.summary(),
     }

@@ -122,10 +122,12 @@ def test_decode_full_size(oracle_mod):
 
 
 # ------------------------------------------------------------------ prep (K1)
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_prep(dtype, oracle_mod):
-    lens = [5, 64, 130, 1, 0, 77]
-    inp = make_inputs(lens, 3, 64, 16, dtype, 11)
+@pytest.mark.parametrize("dtype,dk", [("f32", 64), ("bf16", 64), ("bf16", 128)])
+def test_prep(dtype, dk, oracle_mod):
+    """bf16 with dk = 128 takes the vectorised kernel: its 64-token tiles
+    start mid-chunk and mid-sequence here (lengths 5, 64, 130, ...)."""
+    lens = [5, 64, 130, 1, 0, 77, 300]
+    inp = make_inputs(lens, 3, dk, 16, dtype, 11)
     d = to_dev(inp)
     qh, kh, G, beta = kda.prep(d["q"], d["k"], d["g"], d["b"], d["cu_seqlens"])
     torch.cuda.synchronize()

@@ -51,6 +51,7 @@ KERNEL_SOURCES = {
     "tc_inter": ["kda_tc_inter.cu", "kda_tc_common.cuh", "kda_tc.cuh", "kda_internal.cuh",
                  "kda_common.cuh"],
     "decode_ring": ["kda_decode.cu", "kda_tc.cuh", "kda_internal.cuh", "kda_common.cuh"],
+    "prep_vec": ["kda_prep.cu", "kda_internal.cuh", "kda_common.cuh"],
 }
 
 
@@ -450,7 +451,7 @@ def gpu_arm(a):
                 "ms_per_step": e2e["ms_per_step"]},
         "segment_scan": scan,
         "prep": dict(prep, peak=pk["hbm_gbs"], frac=prep["achieved_gbs"] / pk["hbm_gbs"],
-                     unit="GB/s", bound="hbm"),
+                     unit="GB/s", bound="hbm", traffic=ncu_traffic("prep_vec", PREFILL_WL)),
         "gpu_launches": pre["launches_per_step"] * a.steps + dec["steps"],
         "clocks": clk.summary(),
     }

@@ -261,6 +261,31 @@ def test_chunk_form_equivalence(oracle_mod, C):
     np.testing.assert_allclose(S_c, S[0], rtol=0, atol=1e-12)
 
 
+def test_state_map_is_affine(oracle_mod):
+    """The recurrence is affine in the state: over any run of tokens,
+    S_end = A S_start + B with A the run from the identity with v = 0 and B
+    the run from zero -- the property the segment scan relies on.  Checked on
+    a random start state and on a split into two runs composed by hand."""
+    rng = rnd(65)
+    T, H, d = 90, 2, 8
+    q, k, v, g, b = random_inputs(rng, T, H, d, d)
+    eye = np.broadcast_to(np.eye(d), (1, H, d, d)).copy()
+    zero_v = np.zeros_like(v)
+    _, A, _ = oracle_mod.prefill(q, k, zero_v, g, b, [0, T], S0=eye)
+    _, B, _ = oracle_mod.prefill(q, k, v, g, b, [0, T])
+    S0 = rng.standard_normal((1, H, d, d))
+    _, S, _ = oracle_mod.prefill(q, k, v, g, b, [0, T], S0=S0)
+    np.testing.assert_allclose(S[0], np.einsum("hij,hjk->hik", A[0], S0[0]) + B[0], rtol=0, atol=1e-12)
+    # two runs: S_end = A2 (A1 S0 + B1) + B2
+    p = 41
+    _, A1, _ = oracle_mod.prefill(q[:p], k[:p], zero_v[:p], g[:p], b[:p], [0, p], S0=eye)
+    _, B1, _ = oracle_mod.prefill(q[:p], k[:p], v[:p], g[:p], b[:p], [0, p])
+    _, A2, _ = oracle_mod.prefill(q[p:], k[p:], zero_v[p:], g[p:], b[p:], [0, T - p], S0=eye)
+    _, B2, _ = oracle_mod.prefill(q[p:], k[p:], v[p:], g[p:], b[p:], [0, T - p])
+    mid = np.einsum("hij,hjk->hik", A1[0], S0[0]) + B1[0]
+    np.testing.assert_allclose(np.einsum("hij,hjk->hik", A2[0], mid) + B2[0], S[0], rtol=0, atol=1e-12)
+
+
 # ---------------------------------------------------------------- serving semantics
 def test_resume_from_snapshot(oracle_mod):
     """Prefill of [0,p) then of [p,len) from the state at p equals one pass

@@ -220,6 +220,33 @@ def bench_prep(torch, kda, W, dev, reps=10):
             "us": t * 1e3, "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (t * 1e-3) / 1e9}
 
 
+def bench_1m(torch, kda, W, dev, steps=3):
+    """The million-token configuration (one sequence of 2^20 tokens, H=32,
+    d=128, bf16, fp32 snapshots every 65,536 tokens): whole prefill per call
+    with CUDA events; inputs 34 GB, far larger than L2."""
+    w = W.WORKLOADS["prefill_1m"]
+    inp = W.prefill_inputs(w, device=dev, gen_device=dev)
+    cu = inp["cu_seqlens"]
+    p = kda.Prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["b"], cu,
+                    snapshot_interval=w.snapshot_interval, host_cu_seqlens=cu.cpu())
+    p.run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        p.run()
+    e1.record()
+    e1.synchronize()
+    assert p.device_status() == 0
+    ms = e0.elapsed_time(e1) / steps
+    T = sum(inp["lens"])
+    out = {"workload": w.description, "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3),
+           "snapshots": p.n_snap, "steps": steps}
+    del p, inp
+    torch.cuda.empty_cache()
+    return out
+
+
 def bench_scan(torch, kda, W, dev, T=131072, H=2, reps=5):
     """The segment scan against the plain chunk chain on a workload it is
     for: one sequence of T tokens with few heads (bf16, 128 x 128), so that
@@ -379,6 +406,7 @@ def gpu_arm(a):
     e2e = bench_e2e(torch, kda, W, max(1, min(a.steps, 5)), 1, dev) if rank == 0 else None
     scan = bench_scan(torch, kda, W, dev) if rank == 0 else None
     prep = bench_prep(torch, kda, W, dev) if rank == 0 else None
+    m1 = bench_1m(torch, kda, W, dev) if rank == 0 and a.with_1m else None
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -450,6 +478,7 @@ def gpu_arm(a):
                 "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
                 "ms_per_step": e2e["ms_per_step"]},
         "segment_scan": scan,
+        **({"prefill_1m": m1} if m1 else {}),
         "prep": dict(prep, peak=pk["hbm_gbs"], frac=prep["achieved_gbs"] / pk["hbm_gbs"],
                      unit="GB/s", bound="hbm", traffic=ncu_traffic("prep_vec", PREFILL_WL)),
         "gpu_launches": pre["launches_per_step"] * a.steps + dec["steps"],
@@ -506,6 +535,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--with-1m", action="store_true",
+                    help="also time the million-token configuration (~100 GB of device memory)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time the prefill workload alone (for profiler captures)")
     a = ap.parse_args()

@@ -220,6 +220,36 @@ def bench_prep(torch, kda, W, dev, reps=10):
             "us": t * 1e3, "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (t * 1e-3) / 1e9}
 
 
+def bench_varlen(torch, kda, W, dev, steps=10):
+    """The varlen configuration: 8 packed sequences of U[1024, 32768] tokens,
+    H=32, d=128, bf16, seeded fp32 initial states, fp32 snapshots every 4096
+    tokens and at the boundaries (one interior position and the end of each
+    sequence).  Whole prefill per call, CUDA events, L2 flushed before each."""
+    w = W.WORKLOADS["varlen_8"]
+    inp = W.prefill_inputs(w, device=dev, gen_device=dev)
+    cu, bp, cb = inp["cu_seqlens"], inp["boundary_pos"], inp["cu_boundaries"]
+    p = kda.Prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["b"], cu, initial_state=inp["S0"],
+                    snapshot_interval=w.snapshot_interval, boundary_pos=bp, cu_boundaries=cb,
+                    host_cu_seqlens=cu.cpu(), host_boundary_pos=bp.cpu(), host_cu_boundaries=cb.cpu())
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        p.run()
+    ms = []
+    for _ in range(steps):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        p.run()
+        e1.record()
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    assert p.device_status() == 0
+    t = sum(ms) / len(ms)
+    T = sum(inp["lens"])
+    return {"workload": w.description, "tokens": T, "ms_per_step": t, "tokens_per_s": T / (t * 1e-3),
+            "snapshots": p.n_snap, "steps": steps}
+
+
 def bench_1m(torch, kda, W, dev, steps=3):
     """The million-token configuration (one sequence of 2^20 tokens, H=32,
     d=128, bf16, fp32 snapshots every 65,536 tokens): whole prefill per call
@@ -407,6 +437,7 @@ def gpu_arm(a):
     scan = bench_scan(torch, kda, W, dev) if rank == 0 else None
     prep = bench_prep(torch, kda, W, dev) if rank == 0 else None
     m1 = bench_1m(torch, kda, W, dev) if rank == 0 and a.with_1m else None
+    vl = bench_varlen(torch, kda, W, dev) if rank == 0 else None
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -477,6 +508,7 @@ def gpu_arm(a):
                 "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
                 "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
                 "ms_per_step": e2e["ms_per_step"]},
+        "prefill_varlen": vl,
         "segment_scan": scan,
         **({"prefill_1m": m1} if m1 else {}),
         "prep": dict(prep, peak=pk["hbm_gbs"], frac=prep["achieved_gbs"] / pk["hbm_gbs"],

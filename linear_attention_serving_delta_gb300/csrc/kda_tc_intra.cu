@@ -124,21 +124,30 @@ __device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ 
     const int r0 = 32 * P + 16, c0 = 32 * P;
     float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float a = A[(r0 + rr) * kAs + c0 + m];
-      const float2 t = *reinterpret_cast<const float2*>(T + (c0 + m) * kTs + c0 + cc);
-      x0 += a * t.x;
-      x1 += a * t.y;
+    for (int m4 = 0; m4 < 16; m4 += 4) {  // four entries of the A row per 16-byte load
+      const float4 a = *reinterpret_cast<const float4*>(A + (r0 + rr) * kAs + c0 + m4);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 t = *reinterpret_cast<const float2*>(T + (c0 + m4 + u) * kTs + c0 + cc);
+        x0 += av[u] * t.x;
+        x1 += av[u] * t.y;
+      }
     }
     X[P * 256 + rr * 16 + cc] = x0;
     X[P * 256 + rr * 16 + cc + 1] = x1;
     __syncthreads();
     float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float t = T[(r0 + rr) * kTs + r0 + m];
-      y0 += t * X[P * 256 + m * 16 + cc];
-      y1 += t * X[P * 256 + m * 16 + cc + 1];
+    for (int m4 = 0; m4 < 16; m4 += 4) {
+      const float4 t = *reinterpret_cast<const float4*>(T + (r0 + rr) * kTs + r0 + m4);
+      const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 x = *reinterpret_cast<const float2*>(X + P * 256 + (m4 + u) * 16 + cc);
+        y0 += tv[u] * x.x;
+        y1 += tv[u] * x.y;
+      }
     }
     T[(r0 + rr) * kTs + c0 + cc] = -y0;
     T[(r0 + rr) * kTs + c0 + cc + 1] = -y1;
@@ -148,23 +157,33 @@ __device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ 
   {
     const int rr = (tid >> 4) * 2, cc = (tid & 15) * 2;
     float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
-#pragma unroll 8
-    for (int m = 0; m < 32; ++m) {
-      const float a0 = A[(32 + rr) * kAs + m], a1 = A[(33 + rr) * kAs + m];
-      const float2 t = *reinterpret_cast<const float2*>(T + m * kTs + cc);
-      x00 += a0 * t.x; x01 += a0 * t.y;
-      x10 += a1 * t.x; x11 += a1 * t.y;
+#pragma unroll 2
+    for (int m4 = 0; m4 < 32; m4 += 4) {  // four entries of each A row per 16-byte load
+      const float4 a0 = *reinterpret_cast<const float4*>(A + (32 + rr) * kAs + m4);
+      const float4 a1 = *reinterpret_cast<const float4*>(A + (33 + rr) * kAs + m4);
+      const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 t = *reinterpret_cast<const float2*>(T + (m4 + u) * kTs + cc);
+        x00 += av0[u] * t.x; x01 += av0[u] * t.y;
+        x10 += av1[u] * t.x; x11 += av1[u] * t.y;
+      }
     }
     X[rr * 32 + cc] = x00; X[rr * 32 + cc + 1] = x01;
     X[(rr + 1) * 32 + cc] = x10; X[(rr + 1) * 32 + cc + 1] = x11;
     __syncthreads();
     float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
-#pragma unroll 8
-    for (int m = 0; m < 32; ++m) {
-      const float t0 = T[(32 + rr) * kTs + 32 + m], t1 = T[(33 + rr) * kTs + 32 + m];
-      const float2 x = *reinterpret_cast<const float2*>(X + m * 32 + cc);
-      y00 += t0 * x.x; y01 += t0 * x.y;
-      y10 += t1 * x.x; y11 += t1 * x.y;
+#pragma unroll 2
+    for (int m4 = 0; m4 < 32; m4 += 4) {
+      const float4 t0 = *reinterpret_cast<const float4*>(T + (32 + rr) * kTs + 32 + m4);
+      const float4 t1 = *reinterpret_cast<const float4*>(T + (33 + rr) * kTs + 32 + m4);
+      const float tv0[4] = {t0.x, t0.y, t0.z, t0.w}, tv1[4] = {t1.x, t1.y, t1.z, t1.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 x = *reinterpret_cast<const float2*>(X + (m4 + u) * 32 + cc);
+        y00 += tv0[u] * x.x; y01 += tv0[u] * x.y;
+        y10 += tv1[u] * x.x; y11 += tv1[u] * x.y;
+      }
     }
     T[(32 + rr) * kTs + cc] = -y00; T[(32 + rr) * kTs + cc + 1] = -y01;
     T[(33 + rr) * kTs + cc] = -y10; T[(33 + rr) * kTs + cc + 1] = -y11;

@@ -117,6 +117,11 @@ typedef struct {
                                   raises status flag 2 (for a prefix cache choosing
                                   pool rows, see kda_prefix_cache_reserve)        */
   int64_t snapshot_map_len;    /* entries of snapshot_slot_map (0 if NULL)       */
+  int64_t wait_limit_ns;       /* 0 = 1 s: how long a kernel's bounded wait on a
+                                  copy or an MMA lasts before the kernel gives up,
+                                  raises status flag 8 and winds down (its copies
+                                  and MMAs in flight are still awaited, with the
+                                  1 s limit).  A short limit exercises that path. */
 } kda_prefill_args;
 
 /*

@@ -63,6 +63,7 @@ kda_status_t validate_prefill(const kda_prefill_args* a) {
   if (a->scan_segments < 0 || a->scan_segments > kMaxScanSegments) return KDA_ERR_INVALID_ARG;
   if (a->snapshot_slot_map && (!a->snapshots || a->snapshot_map_len < 0)) return KDA_ERR_INVALID_ARG;
   if (!a->snapshot_slot_map && a->snapshot_map_len != 0) return KDA_ERR_INVALID_ARG;
+  if (a->wait_limit_ns < 0) return KDA_ERR_INVALID_ARG;
   // sizes whose products must stay inside the index types used by the kernels
   if (a->total_tokens > ((int64_t)1 << 40)) return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
@@ -186,6 +187,7 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
   cp.chunks = pp.chunks;
   cp.inter = reinterpret_cast<float*>(w + L.inter);
   cp.rec_floats = L.rec_bytes / sizeof(float);
+  cp.wait_ns = a->wait_limit_ns > 0 ? (uint64_t)a->wait_limit_ns : 1000000000ull;
   if (P > 1) {
     ScanBuffers sb;
     sb.A = reinterpret_cast<float*>(w + L.scan_A);

@@ -58,6 +58,7 @@ struct ChunkParams {
   // (identity state, U~ taken as zero, final -> trans); no o or snapshots
   int32_t k3_mode;
   float* trans;     // [num_seqs][H][dk][dk] in kScanPass1
+  uint64_t wait_ns; // limit of the bounded waits on copies and MMAs (not of the drains)
 };
 constexpr int32_t kScanPass1 = 1;
 

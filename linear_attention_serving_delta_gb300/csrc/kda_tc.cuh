@@ -166,7 +166,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
         : "memory");
     if (done) return true;
     if (it == 0) t0 = globaltimer_ns();
-    else if ((it & 63) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    else if ((it == 1 || (it & 63) == 0) && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -209,8 +209,8 @@ tc_inter(ChunkParams p) {
     return sm + K3Smem::AQ0 + (uint32_t)(j % K3Smem::kAqSlots) * K3Smem::AQ_BYTES;
   };
   auto u_of = [&](int64_t j) { return sm + K3Smem::U0 + (uint32_t)(j & 1) * K3Smem::U_BYTES; };
-  auto wait_chain = [&](int64_t j) {
-    return mbar_wait(&bar_full[j % K3Smem::kSlots], (uint32_t)((j / K3Smem::kSlots) & 1), kWaitLimitNs);
+  auto wait_chain = [&](int64_t j, uint64_t limit) {
+    return mbar_wait(&bar_full[j % K3Smem::kSlots], (uint32_t)((j / K3Smem::kSlots) & 1), limit);
   };
 
   // Thread 96 issues the chain-operand copies and thread 64 the A_qk copies;
@@ -242,8 +242,8 @@ tc_inter(ChunkParams p) {
       for (int n = 0; n < kNh; ++n) v[n] = c == n0 + h16 + n ? 1.f : 0.f;
     float gl = 1.f;
     if (nchunks > 0) {
-      okl = wait_chain(0);
-      chain_waited = 1;
+      okl = wait_chain(0, p.wait_ns);
+      if (okl) chain_waited = 1;  // a copy still in flight is left to the drain
       gl = reinterpret_cast<const float*>(slot_of(0) + K3Smem::GL)[c];
     }
     write_state(SOP, DS, c, h16, v, gl);
@@ -254,7 +254,7 @@ tc_inter(ChunkParams p) {
   // MMA 3 of chunk j, thread 64: wait for its A_qk tile, then
   // D1[j % 3] += A_qk [U_hi | U_lo].  False if the tile never came.
   auto mma3 = [&](int64_t j) -> bool {
-    if (!mbar_wait(&bar_aq[j % K3Smem::kAqSlots], (uint32_t)((j / K3Smem::kAqSlots) & 1), kWaitLimitNs))
+    if (!mbar_wait(&bar_aq[j % K3Smem::kAqSlots], (uint32_t)((j / K3Smem::kAqSlots) & 1), p.wait_ns))
       return false;
     aq_waited = j + 1;
     const uint32_t a = smem_u32(aq_of(j)) - 1024, ub = smem_u32(u_of(j));
@@ -268,7 +268,7 @@ tc_inter(ChunkParams p) {
   // are done before the next commit to that barrier (two steps later, behind
   // a CTA barrier), so a parity wait never sees two phases complete.
   auto wait_mma3 = [&](int64_t j) {
-    return mbar_wait(&bar_mma3[j & 1], (uint32_t)((j >> 1) & 1), kWaitLimitNs);
+    return mbar_wait(&bar_mma3[j & 1], (uint32_t)((j >> 1) & 1), p.wait_ns);
   };
 
   uint32_t ph1 = 0, ph2 = 0;
@@ -306,20 +306,20 @@ tc_inter(ChunkParams p) {
         }
       }
       // ... the slot of chunk it-1 (MMA 2 done) takes chunk it+2 ...
-      if (tid == kLoadThread && it >= 1 && it + 2 < nchunks) {
+      if (tid == kLoadThread && okl && it >= 1 && it + 2 < nchunks) {
         k3_load_chain(p, slot_of(it + 2), &bar_full[(it + 2) % K3Smem::kSlots], c_begin + it + 2, h, n0);
         chain_issued = it + 3;
       }
       // ... and the output product of chunk it-1 runs once MMA 1 is done
       if (tid == kOutThread && it >= 1 && okl) {
-        okl = mbar_wait(&bar_mma1, ph1, kWaitLimitNs);
+        okl = mbar_wait(&bar_mma1, ph1, p.wait_ns);
         if (okl) okl = mma3(it - 1);
       }
     } else {
       // U = U~ - W S_j for token i = lane row, this thread's 16 columns.  The
       // U buffer of this step was last read by MMA 3 of chunk it-2, issued by
       // another thread: its completion is awaited too.
-      okl = okl && mbar_wait(&bar_mma1, ph1, kWaitLimitNs);
+      okl = okl && mbar_wait(&bar_mma1, ph1, p.wait_ns);
       if (it >= 2) okl = okl && wait_mma3(it - 2);
       fence_after_sync();
       const int i = c;
@@ -354,7 +354,7 @@ tc_inter(ChunkParams p) {
     }
     ph1 ^= 1;
     // the state write-back: S_{j+1} = Sa + Sb
-    okl = okl && mbar_wait(&bar_mma2, ph2, kWaitLimitNs);
+    okl = okl && mbar_wait(&bar_mma2, ph2, p.wait_ns);
     ph2 ^= 1;
     fence_after_sync();
     {
@@ -368,8 +368,8 @@ tc_inter(ChunkParams p) {
       }
       float gl = 1.f;  // the last chunk leaves S_n itself in TMEM
       if (it + 1 < nchunks) {
-        okl = okl && wait_chain(it + 1);
-        chain_waited = it + 2;
+        okl = okl && wait_chain(it + 1, p.wait_ns);
+        if (okl) chain_waited = it + 2;
         gl = reinterpret_cast<const float*>(slot_of(it + 1) + K3Smem::GL)[c];
       }
       write_state(SOP, DS, c, h16, v, gl);
@@ -411,7 +411,7 @@ tc_inter(ChunkParams p) {
     // before the shared memory and TMEM are given back
     if (tid == 0) flag(p.status, kFlagTimeout);
     if (tid == kLoadThread)
-      for (int64_t j = chain_waited; j < chain_issued; ++j) wait_chain(j);
+      for (int64_t j = chain_waited; j < chain_issued; ++j) wait_chain(j, kWaitLimitNs);
     if (tid == kOutThread)
       for (int64_t j = aq_waited; j < aq_issued; ++j)
         mbar_wait(&bar_aq[j % K3Smem::kAqSlots], (uint32_t)((j / K3Smem::kAqSlots) & 1), kWaitLimitNs);

@@ -268,6 +268,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ __align__(8) uint64_t bar_mma;
   __shared__ __align__(8) uint64_t bar_ga, bar_gb;  // staging groups A (g, k) and B (q, v)
+  __shared__ __align__(8) uint64_t bar_drain;       // every MMA, on the error path
   __shared__ uint32_t tmem_base;
 
   const int64_t stride = gridDim.x;
@@ -301,6 +302,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     mbar_init(&bar_mma, 1);
     mbar_init(&bar_ga, 1);
     mbar_init(&bar_gb, 1);
+    mbar_init(&bar_drain, 1);
     mbar_init_fence();
   }
   __syncthreads();
@@ -344,8 +346,11 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
       tma_rows_l2(tid == 0 ? &maps.g : tid == 1 ? &maps.k : tid == 2 ? &maps.q : &maps.v, hn,
                   chn.tok0);
     // this item's g and k (group A) have landed; q and v (group B) may still fly
-    ok = mbar_wait(&bar_ga, sph, kWaitLimitNs);
-    a_fly = false;
+    // (a group still in flight after a wait that gave up stays marked, with
+    // its phase, for the drain at the end)
+    const bool got_a = mbar_wait(&bar_ga, sph, p.wait_ns);
+    a_fly = !got_a;
+    ok = got_a;
 
     // ---- cumulative decay Gamma_i = prod_{m<=i} alpha_m, alpha = 1 / (1 + e^g)
     // (= exp(-softplus(g))): a product over this thread's 4 tokens, a scan
@@ -385,9 +390,10 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     // ---- L2 norms per token: 8 channels here, 8 lanes, then the two channel
     // halves.  The raw q, k, v chunks go to registers now: the operands are
     // written over their stagings after the next two barriers.
-    ok = mbar_wait(&bar_gb, sph, kWaitLimitNs) && ok;
-    b_fly = false;
-    sph ^= 1;
+    const bool got_b = mbar_wait(&bar_gb, sph, p.wait_ns);
+    b_fly = !got_b;
+    ok = got_b && ok;
+    if (got_a && got_b) sph ^= 1;
     uint4 qraw[4], kraw[4], vraw[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -517,7 +523,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     }
     // the A_kk tile is rewritten below: the AK copies must have read it
     if (copy_group(tid) >= 0) bulk_wait_read_all();
-    ok = __syncthreads_and(mbar_wait(&bar_mma, 0, kWaitLimitNs));
+    ok = __syncthreads_and(mbar_wait(&bar_mma, 0, p.wait_ns));
     fence_after_sync();
     if (!ok) break;
     {
@@ -596,7 +602,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
                  sdesc(smem_u32(B2) + s * 256, 128, kB2Sbo), id, s > 0);
       mma_commit(&bar_mma);
     }
-    ok = __syncthreads_and(mbar_wait(&bar_mma, 1, kWaitLimitNs));
+    ok = __syncthreads_and(mbar_wait(&bar_mma, 1, p.wait_ns));
     fence_after_sync();
     if (!ok) break;
     // MMA 2 has read B2: the next item's q and v (group B) are staged there now
@@ -649,10 +655,15 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     ch = ch_next;
     ch_next = item + 2 * stride < n_items ? item_chunk(p.chunks, (item + 2 * stride) / H) : ItemChunk{0, 0};
   }
-  // no staging copy is left in flight when the CTA exits (waits bounded)
+  // no staging copy and no MMA is left in flight when the CTA exits (these
+  // waits keep the long limit whatever the caller chose for the others)
   if (a_fly) mbar_wait(&bar_ga, sph, kWaitLimitNs);
   if (b_fly) mbar_wait(&bar_gb, sph, kWaitLimitNs);
-  if (tid == 0 && !ok) flag(p.status, kFlagTimeout);
+  if (tid == 0 && !ok) {
+    flag(p.status, kFlagTimeout);
+    mma_commit(&bar_drain);
+    mbar_wait(&bar_drain, 0, kWaitLimitNs);
+  }
   bulk_wait_all();  // every thread's own copies
   fence_before_sync();
   __syncthreads();

@@ -57,7 +57,8 @@ class PrefillArgs(ctypes.Structure):
                 ("snapshot_interval", c_i64), ("boundary_pos", c_vp), ("cu_boundaries", c_vp),
                 ("num_boundaries", c_i64), ("cu_snapshots", c_vp), ("snapshots", c_vp),
                 ("num_snapshots", c_i64), ("phase_events", c_vp), ("scan_segments", c_i32),
-                ("snapshot_slot_map", c_vp), ("snapshot_map_len", c_i64)]
+                ("snapshot_slot_map", c_vp), ("snapshot_map_len", c_i64),
+                ("wait_limit_ns", c_i64)]
 
 
 class PrefillHostArgs(ctypes.Structure):
@@ -177,7 +178,7 @@ def _check(status: int, what: str):
 def make_prefill_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=None,
                       final_state=None, snapshot_interval=0, boundary_pos=None,
                       cu_boundaries=None, cu_snapshots=None, snapshots=None,
-                      scan_segments=0, snapshot_slot_map=None) -> PrefillArgs:
+                      scan_segments=0, snapshot_slot_map=None, wait_limit_ns=0) -> PrefillArgs:
     T, H, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
@@ -205,6 +206,7 @@ def make_prefill_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=
     a.scan_segments = int(scan_segments)
     a.snapshot_slot_map = _ptr(snapshot_slot_map, torch.int32, "snapshot_slot_map")
     a.snapshot_map_len = 0 if snapshot_slot_map is None else snapshot_slot_map.numel()
+    a.wait_limit_ns = int(wait_limit_ns)
     return a
 
 
@@ -347,7 +349,7 @@ class Prefill:
                  snapshot_interval=0, boundary_pos=None, cu_boundaries=None,
                  want_final=True, host_cu_seqlens=None, host_boundary_pos=None,
                  host_cu_boundaries=None, o=None, scan_segments=0, snapshot_pool=None,
-                 snapshot_slot_map=None):
+                 snapshot_slot_map=None, wait_limit_ns=0):
         dev = q.device
         T, H, dk = q.shape
         dv = v.shape[-1]
@@ -378,7 +380,8 @@ class Prefill:
             boundary_pos=boundary_pos, cu_boundaries=cu_boundaries,
             cu_snapshots=self.cu_snapshots, snapshots=self.snapshots,
             scan_segments=scan_segments,
-            snapshot_slot_map=snapshot_slot_map if self.snapshots is not None else None)
+            snapshot_slot_map=snapshot_slot_map if self.snapshots is not None else None,
+            wait_limit_ns=wait_limit_ns)
         nbytes = kda_prefill_workspace_size(self.args)
         if nbytes == 0:
             raise ValueError("kda_prefill_workspace_size rejected the arguments")

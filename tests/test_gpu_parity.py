@@ -388,3 +388,25 @@ def test_malformed_device_data_is_flagged():
     bad_cu = torch.tensor([0, 15, 12], dtype=torch.int64, device="cuda")
     p = kda.Prefill(d["q"], d["k"], d["v"], d["g"], d["b"], bad_cu).run()
     assert p.device_status() & 1
+
+
+def test_bounded_waits_give_up_cleanly():
+    """A wait limit of 1 ns makes the tensor-core kernels' bounded waits on
+    their copies and MMAs give up: the call still returns, the workspace
+    status carries flag 8, and the context stays usable -- the next call with
+    the default limit gives the oracle's results.  No wait is left to hang
+    and nothing faults (the copies and MMAs in flight are drained with the
+    long limit before shared memory and TMEM are given back)."""
+    inp = make_inputs([4096, 1000], 4, 128, 128, "bf16", 91, s0_std=0.02)
+    d = to_dev(inp)
+    args = [d[x] for x in "qkvgb"] + [d["cu_seqlens"]]
+    hurried = kda.Prefill(*args, initial_state=d["S0"], host_cu_seqlens=inp["cu_seqlens"],
+                          wait_limit_ns=1).run()
+    torch.cuda.synchronize()
+    assert hurried.device_status() & 8
+    calm = kda.Prefill(*args, initial_state=d["S0"], host_cu_seqlens=inp["cu_seqlens"]).run()
+    torch.cuda.synchronize()
+    assert calm.device_status() == 0
+    ro, rS, _ = oracle_prefill_of(inp)
+    assert rel(host(calm.o), ro) <= TOL["bf16"]
+    assert rel(host(calm.final_state), rS) <= TOL["bf16"]

@@ -322,6 +322,12 @@ typedef struct {
   float* state;                /* device pool [num_slots, H, dk, dv], in place    */
   const int32_t* state_slots;  /* device [B] or NULL; two rows must not share a slot */
   void* o;                     /* device [B, H, dv]                               */
+  int64_t wait_limit_ns;       /* 0 = 1 s: the limit of the bounded waits of the
+                                  128 x 128 kernel on its copies (see
+                                  kda_prefill_args.wait_limit_ns)                 */
+  int32_t* status;             /* device int32 or NULL: bit 8 is OR-ed in when a
+                                  bounded wait gives up (the rows after it are
+                                  then not updated)                               */
 } kda_decode_args;
 
 kda_status_t kda_decode_step(const kda_decode_args* args, void* stream);

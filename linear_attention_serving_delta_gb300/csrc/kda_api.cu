@@ -246,6 +246,7 @@ kda_status_t kda_decode_step(const kda_decode_args* a, void* stream) {
   if (!a->q || !a->k || !a->v || !a->g || !a->b || !a->state || !a->o) return KDA_ERR_INVALID_ARG;
   if (!a->state_slots && a->num_slots < a->batch) return KDA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(a->state) & 15) != 0) return KDA_ERR_INVALID_ARG;
+  if (a->wait_limit_ns < 0) return KDA_ERR_INVALID_ARG;
   return from_cuda(launch_decode(*a, static_cast<cudaStream_t>(stream)));
 }
 

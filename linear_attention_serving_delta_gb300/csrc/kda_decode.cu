@@ -244,15 +244,25 @@ decode_ring(kda_decode_args a, int64_t n_items) {
   }
   __syncthreads();
 
+  const uint64_t lim = a.wait_limit_ns > 0 ? (uint64_t)a.wait_limit_ns : tc::kWaitLimitNs;
   if (warp == 8) {
     // ---- producer
     if (lane == 0) {
-      for (int64_t k = 0; k < kStages && k < n_local; ++k)
-        ring_issue<TIn>(a, sm + k * Ring<TIn>::STAGE, &full[k], &valid_flag[k], first + k * stride);
+      int64_t issued = 0;  // items whose slot copies were issued
+      for (; issued < kStages && issued < n_local; ++issued)
+        ring_issue<TIn>(a, sm + issued * Ring<TIn>::STAGE, &full[issued], &valid_flag[issued],
+                        first + issued * stride);
       for (int64_t k = 0; k < n_local; ++k) {
         const int st = (int)(k % kStages);
         uint8_t* stage = sm + st * Ring<TIn>::STAGE;
-        if (!tc::mbar_wait(&done[st], (uint32_t)((k / kStages) & 1), tc::kWaitLimitNs)) break;
+        if (!tc::mbar_wait(&done[st], (uint32_t)((k / kStages) & 1), lim)) {
+          // the compute warps gave up: let the slot copies still in flight
+          // land (long limit) before the shared memory is given back
+          if (a.status) atomicOr(a.status, kFlagTimeout);
+          for (int64_t j = k; j < issued; ++j)
+            tc::mbar_wait(&full[j % kStages], (uint32_t)((j / kStages) & 1), tc::kWaitLimitNs);
+          break;
+        }
         const int64_t item = first + k * stride;
         if (valid_flag[st]) {
           const int row = (int)(item / H), h = (int)(item % H);
@@ -261,8 +271,10 @@ decode_ring(kda_decode_args a, int64_t n_items) {
           tc::bulk_commit();
           tc::bulk_wait_read_all();
         }
-        if (k + kStages < n_local)
+        if (k + kStages < n_local) {
           ring_issue<TIn>(a, stage, &full[st], &valid_flag[st], item + kStages * stride);
+          issued = k + kStages + 1;
+        }
       }
       tc::bulk_wait_all();
     }
@@ -277,13 +289,16 @@ decode_ring(kda_decode_args a, int64_t n_items) {
     uint8_t* stage = sm + st * Ring<TIn>::STAGE;
     const int64_t item = first + k * stride;
     const int buf = (int)(k & 1);
-    bool ok = tc::mbar_wait(&full[st], (uint32_t)((k / kStages) & 1), tc::kWaitLimitNs);
+    bool ok = tc::mbar_wait(&full[st], (uint32_t)((k / kStages) & 1), lim);
     const bool valid = valid_flag[st] != 0;
     const float b_cur = b_next;
     if (k + 1 < n_local) b_next = ld_in(gb, item + stride);
     if (!valid) {  // uniform: nothing to compute, the slot is handed back
       mbar_arrive(&done[st]);
-      if (!bar_and(kComputeBarrier, kRingThreads, ok)) break;
+      if (!bar_and(kComputeBarrier, kRingThreads, ok)) {
+        if (tid == 0 && a.status) atomicOr(a.status, kFlagTimeout);
+        break;
+      }
       continue;
     }
     const TIn* rq = reinterpret_cast<const TIn*>(stage + kStateBytes);
@@ -318,7 +333,10 @@ decode_ring(kda_decode_args a, int64_t n_items) {
     }
     *reinterpret_cast<float4*>(&red_p[buf][warp][4 * lane]) = pp;
     *reinterpret_cast<float4*>(&red_o[buf][warp][4 * lane]) = po;
-    if (!bar_and(kComputeBarrier, kRingThreads, ok)) break;
+    if (!bar_and(kComputeBarrier, kRingThreads, ok)) {
+      if (tid == 0 && a.status) atomicOr(a.status, kFlagTimeout);
+      break;
+    }
     float sq = 0.f, sk = 0.f, sqk = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {

@@ -151,22 +151,35 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 // Waits for phase `parity` of `bar` to complete, for at most `limit_ns`
 // nanoseconds of wall time.  Returns false on expiry (the caller records the
-// timeout and winds down instead of hanging).
+// timeout and winds down instead of hanging).  A limit under 100 us (a test
+// of the give-up path) polls without suspending and reads the clock on every
+// poll, so that it expires whenever the phase is not already complete; the
+// normal limits use the suspending try_wait and read the clock now and then.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
+  const bool short_limit = limit_ns < 100000;
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(done)
-        : "r"(a), "r"(parity)
-        : "memory");
+    if (short_limit)
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}\n"
+          : "=r"(done)
+          : "r"(a), "r"(parity)
+          : "memory");
+    else
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}\n"
+          : "=r"(done)
+          : "r"(a), "r"(parity)
+          : "memory");
     if (done) return true;
     if (it == 0) t0 = globaltimer_ns();
-    else if ((it == 1 || (it & 63) == 0) && globaltimer_ns() - t0 > limit_ns) return false;
+    else if ((short_limit || (it & 63) == 0) && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

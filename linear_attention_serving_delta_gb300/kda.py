@@ -73,7 +73,8 @@ class DecodeArgs(ctypes.Structure):
     _fields_ = [("batch", c_i32), ("num_heads", c_i32), ("dk", c_i32), ("dv", c_i32),
                 ("num_slots", c_i32), ("in_dtype", ctypes.c_int), ("scale", c_f32),
                 ("q", c_vp), ("k", c_vp), ("v", c_vp), ("g", c_vp), ("b", c_vp),
-                ("state", c_vp), ("state_slots", c_vp), ("o", c_vp)]
+                ("state", c_vp), ("state_slots", c_vp), ("o", c_vp), ("wait_limit_ns", c_i64),
+                ("status", c_vp)]
 
 
 class PrepArgs(ctypes.Structure):
@@ -306,7 +307,8 @@ def kda_snapshot_plan(cu_seqlens, interval: int, boundary_pos=None, cu_boundarie
     return out, int(n_snap)
 
 
-def kda_decode_step(q, k, v, g, b, state, o, state_slots=None, scale=1.0, stream=None) -> None:
+def kda_decode_step(q, k, v, g, b, state, o, state_slots=None, scale=1.0, stream=None,
+                    wait_limit_ns=0, status=None) -> None:
     B, H, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
@@ -321,6 +323,8 @@ def kda_decode_step(q, k, v, g, b, state, o, state_slots=None, scale=1.0, stream
     a.g, a.b, a.o = _ptr(g, dt, "g"), _ptr(b, dt, "b"), _ptr(o, dt, "o")
     a.state = _ptr(state, torch.float32, "state")
     a.state_slots = _ptr(state_slots, torch.int32, "state_slots")
+    a.wait_limit_ns = int(wait_limit_ns)
+    a.status = _ptr(status, torch.int32, "status")
     _check(lib().kda_decode_step(ctypes.byref(a), _stream(stream)), "kda_decode_step")
 
 

@@ -71,7 +71,7 @@ int main(void) {
   F(kda_prefill_args, phase_events) F(kda_prefill_args, scan_segments)
   F(kda_prefill_args, snapshot_slot_map) F(kda_prefill_args, wait_limit_ns)
   F(kda_decode_args, scale) F(kda_decode_args, q) F(kda_decode_args, state_slots)
-  F(kda_decode_args, o)
+  F(kda_decode_args, o) F(kda_decode_args, wait_limit_ns) F(kda_decode_args, status)
   F(kda_prep_args, total_tokens) F(kda_prep_args, in_dtype) F(kda_prep_args, beta)
   return 0;
 }
@@ -160,6 +160,10 @@ def test_decode_and_prep_validation(kda):
     d.state = 0x3000
     d.num_slots = 2                                                # pool smaller than batch
     assert L.kda_decode_step(ctypes.byref(d), None) == 1
+    d.num_slots = 4
+    d.wait_limit_ns = -1                                           # negative wait limit
+    assert L.kda_decode_step(ctypes.byref(d), None) == 1
+    d.wait_limit_ns = 0
     d.dk = 96
     assert L.kda_decode_step(ctypes.byref(d), None) == 2
     p = kda.PrepArgs()

@@ -410,3 +410,28 @@ def test_bounded_waits_give_up_cleanly():
     ro, rS, _ = oracle_prefill_of(inp)
     assert rel(host(calm.o), ro) <= TOL["bf16"]
     assert rel(host(calm.final_state), rS) <= TOL["bf16"]
+
+
+def test_decode_bounded_waits_give_up_cleanly(oracle_mod):
+    """The 128 x 128 decode kernel with a 1 ns wait limit: its waits on the
+    slot copies give up, the status word gets flag 8, nothing hangs or
+    faults, and a later step on the same context with the default limit
+    matches the oracle."""
+    dw = W.DecodeWorkload("waits", 64, 8, 128, 128, 1, 93)
+    inp = W.decode_inputs(dw)
+    args = [inp[x][0].cuda().contiguous() for x in "qkvgb"]
+    o = torch.zeros(64, 8, 128, dtype=args[0].dtype, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hurried = inp["state"].cuda().contiguous()
+    kda.kda_decode_step(*args, hurried, o, wait_limit_ns=1, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 8
+    status.zero_()
+    state = inp["state"].cuda().contiguous()
+    kda.kda_decode_step(*args, state, o, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_state = host(inp["state"]).astype(np.float64)
+    ro = oracle_mod.decode(*[host(inp[x][0]) for x in "qkvgb"], ref_state)
+    assert rel(host(o), ro) <= TOL["bf16"]
+    assert rel(host(state), ref_state) <= 1e-5

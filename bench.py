@@ -287,8 +287,10 @@ def bench_scan(torch, kda, W, dev, T=131072, H=2, reps=5):
     args = [inp[x] for x in "qkvgb"] + [inp["cu_seqlens"]]
     hcu = inp["cu_seqlens"].cpu()
     out = {"workload": f"one sequence, T={T}, H={H}, dk=dv=128, bf16"}
+    ws = {}
     for name, P in (("plain", 1), ("scan", 0)):
         p = kda.Prefill(*args, host_cu_seqlens=hcu, scan_segments=P)
+        ws[name] = p.workspace.numel()
         for _ in range(2):
             p.run()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -300,8 +302,9 @@ def bench_scan(torch, kda, W, dev, T=131072, H=2, reps=5):
         e1.synchronize()
         assert p.device_status() == 0
         out[f"{name}_ms"] = e0.elapsed_time(e1) / reps
-        if P == 0:
-            out["segments"] = int(min(152 // (8 * H), ((T + 63) // 64) // 16, 64))
+    # the automatic choice as include/kda.h states it (segment scan section)
+    out["segments"] = int(min(152 // (8 * H), ((T + 63) // 64) // 16, 64))
+    assert ws["scan"] > ws["plain"], "the automatic choice took the segment scan"
     out["speedup"] = out["plain_ms"] / out["scan_ms"]
     out["tokens_per_s"] = T / (out["scan_ms"] * 1e-3)
     return out

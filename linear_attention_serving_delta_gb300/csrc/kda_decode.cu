@@ -219,7 +219,8 @@ __device__ __forceinline__ void ring_issue(const kda_decode_args& a, uint8_t* st
   tc::bulk_g2s(stage + kStateBytes + 3 * ROW, static_cast<const TIn*>(a.v) + e, ROW, bar);
 }
 
-template <typename TIn>
+// kPoll: the instantiation for wait limits under kPollLimitNs (the give-up test)
+template <typename TIn, bool kPoll>
 __global__ void __launch_bounds__(kRingAllThreads, 1)
 decode_ring(kda_decode_args a, int64_t n_items) {
   extern __shared__ __align__(128) uint8_t sm[];
@@ -255,7 +256,7 @@ decode_ring(kda_decode_args a, int64_t n_items) {
       for (int64_t k = 0; k < n_local; ++k) {
         const int st = (int)(k % kStages);
         uint8_t* stage = sm + st * Ring<TIn>::STAGE;
-        if (!tc::mbar_wait(&done[st], (uint32_t)((k / kStages) & 1), lim)) {
+        if (!tc::mbar_wait_t<kPoll>(&done[st], (uint32_t)((k / kStages) & 1), lim)) {
           // the compute warps gave up: let the slot copies still in flight
           // land (long limit) before the shared memory is given back
           if (a.status) atomicOr(a.status, kFlagTimeout);
@@ -289,7 +290,7 @@ decode_ring(kda_decode_args a, int64_t n_items) {
     uint8_t* stage = sm + st * Ring<TIn>::STAGE;
     const int64_t item = first + k * stride;
     const int buf = (int)(k & 1);
-    bool ok = tc::mbar_wait(&full[st], (uint32_t)((k / kStages) & 1), lim);
+    bool ok = tc::mbar_wait_t<kPoll>(&full[st], (uint32_t)((k / kStages) & 1), lim);
     const bool valid = valid_flag[st] != 0;
     const float b_cur = b_next;
     if (k + 1 < n_local) b_next = ld_in(gb, item + stride);
@@ -386,13 +387,17 @@ cudaError_t launch_ring(const kda_decode_args& a, cudaStream_t stream) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const bool poll = a.wait_limit_ns > 0 && (uint64_t)a.wait_limit_ns < tc::kPollLimitNs;
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_ring<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Ring<TIn>::BYTES);
+    e = cudaFuncSetAttribute(poll ? decode_ring<TIn, true> : decode_ring<TIn, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Ring<TIn>::BYTES);
   if (e != cudaSuccess) return e;
   const int64_t n_items = (int64_t)a.batch * a.num_heads;
   const int64_t grid = n_items < sms ? n_items : sms;
-  decode_ring<TIn><<<(unsigned)grid, kRingAllThreads, Ring<TIn>::BYTES, stream>>>(a, n_items);
+  if (poll)
+    decode_ring<TIn, true><<<(unsigned)grid, kRingAllThreads, Ring<TIn>::BYTES, stream>>>(a, n_items);
+  else
+    decode_ring<TIn, false><<<(unsigned)grid, kRingAllThreads, Ring<TIn>::BYTES, stream>>>(a, n_items);
   return cudaGetLastError();
 }
 

@@ -151,36 +151,51 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 // Waits for phase `parity` of `bar` to complete, for at most `limit_ns`
 // nanoseconds of wall time.  Returns false on expiry (the caller records the
-// timeout and winds down instead of hanging).  A limit under 100 us (a test
-// of the give-up path) polls without suspending and reads the clock on every
-// poll, so that it expires whenever the phase is not already complete; the
-// normal limits use the suspending try_wait and read the clock now and then.
+// timeout and winds down instead of hanging).  The wait suspends in
+// mbarrier.try_wait and reads the clock every 64 polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
-  const bool short_limit = limit_ns < 100000;
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     uint32_t done;
-    if (short_limit)
-      asm volatile(
-          "{\n\t.reg .pred p;\n\t"
-          "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-          "selp.u32 %0, 1, 0, p;\n\t}\n"
-          : "=r"(done)
-          : "r"(a), "r"(parity)
-          : "memory");
-    else
-      asm volatile(
-          "{\n\t.reg .pred p;\n\t"
-          "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-          "selp.u32 %0, 1, 0, p;\n\t}\n"
-          : "=r"(done)
-          : "r"(a), "r"(parity)
-          : "memory");
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
     if (done) return true;
     if (it == 0) t0 = globaltimer_ns();
-    else if ((short_limit || (it & 63) == 0) && globaltimer_ns() - t0 > limit_ns) return false;
+    else if ((it & 63) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// The same wait polled with the non-blocking test, reading the clock on
+// every poll, so that a short limit expires whenever the phase is not already
+// complete.  The kernels take it for limits under kPollLimitNs (a test of
+// their give-up path) through a separate instantiation, which keeps the
+// normal wait loop as it is.
+__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+constexpr uint64_t kPollLimitNs = 100000;
+template <bool kPoll>
+__device__ __forceinline__ bool mbar_wait_t(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  return kPoll ? mbar_poll(bar, parity, limit_ns) : mbar_wait(bar, parity, limit_ns);
 }
 
 // 1-D bulk copy global -> shared (TMA engine), completion counted in bytes

@@ -155,6 +155,8 @@ __device__ __forceinline__ void write_state(uint8_t* sop, uint32_t ds, int c, in
   tmem_st_wait();
 }
 
+// kPoll: the instantiation for wait limits under kPollLimitNs (the give-up test)
+template <bool kPoll>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_inter(ChunkParams p) {
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -209,8 +211,11 @@ tc_inter(ChunkParams p) {
     return sm + K3Smem::AQ0 + (uint32_t)(j % K3Smem::kAqSlots) * K3Smem::AQ_BYTES;
   };
   auto u_of = [&](int64_t j) { return sm + K3Smem::U0 + (uint32_t)(j & 1) * K3Smem::U_BYTES; };
-  auto wait_chain = [&](int64_t j, uint64_t limit) {
-    return mbar_wait(&bar_full[j % K3Smem::kSlots], (uint32_t)((j / K3Smem::kSlots) & 1), limit);
+  // (the drain of the error path waits with the long limit)
+  auto wait_chain = [&](int64_t j, bool drain) {
+    uint64_t* bar = &bar_full[j % K3Smem::kSlots];
+    const uint32_t par = (uint32_t)((j / K3Smem::kSlots) & 1);
+    return drain ? mbar_wait(bar, par, kWaitLimitNs) : mbar_wait_t<kPoll>(bar, par, p.wait_ns);
   };
 
   // Thread 96 issues the chain-operand copies and thread 64 the A_qk copies;
@@ -242,7 +247,7 @@ tc_inter(ChunkParams p) {
       for (int n = 0; n < kNh; ++n) v[n] = c == n0 + h16 + n ? 1.f : 0.f;
     float gl = 1.f;
     if (nchunks > 0) {
-      okl = wait_chain(0, p.wait_ns);
+      okl = wait_chain(0, false);
       if (okl) chain_waited = 1;  // a copy still in flight is left to the drain
       gl = reinterpret_cast<const float*>(slot_of(0) + K3Smem::GL)[c];
     }
@@ -254,7 +259,7 @@ tc_inter(ChunkParams p) {
   // MMA 3 of chunk j, thread 64: wait for its A_qk tile, then
   // D1[j % 3] += A_qk [U_hi | U_lo].  False if the tile never came.
   auto mma3 = [&](int64_t j) -> bool {
-    if (!mbar_wait(&bar_aq[j % K3Smem::kAqSlots], (uint32_t)((j / K3Smem::kAqSlots) & 1), p.wait_ns))
+    if (!mbar_wait_t<kPoll>(&bar_aq[j % K3Smem::kAqSlots], (uint32_t)((j / K3Smem::kAqSlots) & 1), p.wait_ns))
       return false;
     aq_waited = j + 1;
     const uint32_t a = smem_u32(aq_of(j)) - 1024, ub = smem_u32(u_of(j));
@@ -268,7 +273,7 @@ tc_inter(ChunkParams p) {
   // are done before the next commit to that barrier (two steps later, behind
   // a CTA barrier), so a parity wait never sees two phases complete.
   auto wait_mma3 = [&](int64_t j) {
-    return mbar_wait(&bar_mma3[j & 1], (uint32_t)((j >> 1) & 1), p.wait_ns);
+    return mbar_wait_t<kPoll>(&bar_mma3[j & 1], (uint32_t)((j >> 1) & 1), p.wait_ns);
   };
 
   uint32_t ph1 = 0, ph2 = 0;
@@ -312,14 +317,14 @@ tc_inter(ChunkParams p) {
       }
       // ... and the output product of chunk it-1 runs once MMA 1 is done
       if (tid == kOutThread && it >= 1 && okl) {
-        okl = mbar_wait(&bar_mma1, ph1, p.wait_ns);
+        okl = mbar_wait_t<kPoll>(&bar_mma1, ph1, p.wait_ns);
         if (okl) okl = mma3(it - 1);
       }
     } else {
       // U = U~ - W S_j for token i = lane row, this thread's 16 columns.  The
       // U buffer of this step was last read by MMA 3 of chunk it-2, issued by
       // another thread: its completion is awaited too.
-      okl = okl && mbar_wait(&bar_mma1, ph1, p.wait_ns);
+      okl = okl && mbar_wait_t<kPoll>(&bar_mma1, ph1, p.wait_ns);
       if (it >= 2) okl = okl && wait_mma3(it - 2);
       fence_after_sync();
       const int i = c;
@@ -354,7 +359,7 @@ tc_inter(ChunkParams p) {
     }
     ph1 ^= 1;
     // the state write-back: S_{j+1} = Sa + Sb
-    okl = okl && mbar_wait(&bar_mma2, ph2, p.wait_ns);
+    okl = okl && mbar_wait_t<kPoll>(&bar_mma2, ph2, p.wait_ns);
     ph2 ^= 1;
     fence_after_sync();
     {
@@ -368,7 +373,7 @@ tc_inter(ChunkParams p) {
       }
       float gl = 1.f;  // the last chunk leaves S_n itself in TMEM
       if (it + 1 < nchunks) {
-        okl = okl && wait_chain(it + 1, p.wait_ns);
+        okl = okl && wait_chain(it + 1, false);
         if (okl) chain_waited = it + 2;
         gl = reinterpret_cast<const float*>(slot_of(it + 1) + K3Smem::GL)[c];
       }
@@ -411,7 +416,7 @@ tc_inter(ChunkParams p) {
     // before the shared memory and TMEM are given back
     if (tid == 0) flag(p.status, kFlagTimeout);
     if (tid == kLoadThread)
-      for (int64_t j = chain_waited; j < chain_issued; ++j) wait_chain(j, kWaitLimitNs);
+      for (int64_t j = chain_waited; j < chain_issued; ++j) wait_chain(j, true);
     if (tid == kOutThread)
       for (int64_t j = aq_waited; j < aq_issued; ++j)
         mbar_wait(&bar_aq[j % K3Smem::kAqSlots], (uint32_t)((j / K3Smem::kAqSlots) & 1), kWaitLimitNs);
@@ -422,6 +427,19 @@ tc_inter(ChunkParams p) {
   __syncthreads();
   fence_after_sync();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// tc_inter with the wait mode its limit asks for
+cudaError_t run_inter(const ChunkParams& p, dim3 grid, cudaStream_t stream) {
+  const bool poll = p.wait_ns < kPollLimitNs;
+  cudaError_t e = cudaFuncSetAttribute(poll ? tc_inter<true> : tc_inter<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K3Smem::BYTES);
+  if (e != cudaSuccess) return e;
+  if (poll)
+    tc_inter<true><<<grid, kThreads, K3Smem::BYTES, stream>>>(p);
+  else
+    tc_inter<false><<<grid, kThreads, K3Smem::BYTES, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -435,16 +453,11 @@ cudaError_t launch_tc_prefill(const ChunkParams& p, cudaStream_t stream, cudaEve
   using namespace tcp;
   cudaError_t e = launch_intra(p, stream);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc_inter, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)K3Smem::BYTES);
-  if (e != cudaSuccess) return e;
   if (mid) {
     e = cudaEventRecord(mid, stream);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid2((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)(kD / kNs));
-  tc_inter<<<grid2, kThreads, K3Smem::BYTES, stream>>>(p);
-  return cudaGetLastError();
+  return run_inter(p, dim3((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)(kD / kNs)), stream);
 }
 
 namespace {
@@ -527,9 +540,6 @@ cudaError_t launch_tc_prefill_scan(const ChunkParams& p, const ScanBuffers& sb, 
   using namespace tcp;
   cudaError_t e = launch_intra(p, stream);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc_inter, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)K3Smem::BYTES);
-  if (e != cudaSuccess) return e;
   if (mid) {
     e = cudaEventRecord(mid, stream);
     if (e != cudaSuccess) return e;
@@ -541,9 +551,7 @@ cudaError_t launch_tc_prefill_scan(const ChunkParams& p, const ScanBuffers& sb, 
   p1.final_state = sb.B;
   p1.trans = sb.A;
   p1.snapshots = nullptr;
-  tc_inter<<<dim3((unsigned)p.num_seqs, (unsigned)p.H, 2 * (unsigned)(kD / kNs)), kThreads, K3Smem::BYTES,
-             stream>>>(p1);
-  e = cudaGetLastError();
+  e = run_inter(p1, dim3((unsigned)p.num_seqs, (unsigned)p.H, 2 * (unsigned)(kD / kNs)), stream);
   if (e != cudaSuccess) return e;
   scan_combine<<<dim3((unsigned)p.H, (unsigned)(kD / kNs)), 256, 0, stream>>>(sb, p.num_seqs, p.H);
   e = cudaGetLastError();
@@ -554,9 +562,7 @@ cudaError_t launch_tc_prefill_scan(const ChunkParams& p, const ScanBuffers& sb, 
   p2.initial_state = sb.inits;
   p2.final_state = sb.finals;
   p2.trans = nullptr;
-  tc_inter<<<dim3((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)(kD / kNs)), kThreads, K3Smem::BYTES,
-             stream>>>(p2);
-  e = cudaGetLastError();
+  e = run_inter(p2, dim3((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)(kD / kNs)), stream);
   if (e != cudaSuccess || !sb.final_state) return e;
   return cudaMemcpyAsync(sb.final_state, sb.finals + (size_t)(p.num_seqs - 1) * p.H * kD * kD,
                          (size_t)p.H * kD * kD * sizeof(float), cudaMemcpyDeviceToDevice, stream);

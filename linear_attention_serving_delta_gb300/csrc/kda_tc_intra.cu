@@ -263,6 +263,8 @@ __device__ __forceinline__ float load_b(const ChunkParams& p, const ItemChunk& c
 // gridDim.x.  The next item's rows are prefetched into L2 at the top of an
 // item and staged by bulk copies as soon as their tiles are free.  TMEM and
 // the mbarriers are set up once per CTA.
+// kPoll: the instantiation for wait limits under kPollLimitNs (the give-up test)
+template <bool kPoll>
 __global__ void __launch_bounds__(kThreads, 2)
 tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -346,11 +348,8 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
       tma_rows_l2(tid == 0 ? &maps.g : tid == 1 ? &maps.k : tid == 2 ? &maps.q : &maps.v, hn,
                   chn.tok0);
     // this item's g and k (group A) have landed; q and v (group B) may still fly
-    // (a group still in flight after a wait that gave up stays marked, with
-    // its phase, for the drain at the end)
-    const bool got_a = mbar_wait(&bar_ga, sph, p.wait_ns);
-    a_fly = !got_a;
-    ok = got_a;
+    ok = mbar_wait_t<kPoll>(&bar_ga, sph, p.wait_ns);
+    a_fly = false;
 
     // ---- cumulative decay Gamma_i = prod_{m<=i} alpha_m, alpha = 1 / (1 + e^g)
     // (= exp(-softplus(g))): a product over this thread's 4 tokens, a scan
@@ -390,10 +389,9 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     // ---- L2 norms per token: 8 channels here, 8 lanes, then the two channel
     // halves.  The raw q, k, v chunks go to registers now: the operands are
     // written over their stagings after the next two barriers.
-    const bool got_b = mbar_wait(&bar_gb, sph, p.wait_ns);
-    b_fly = !got_b;
-    ok = got_b && ok;
-    if (got_a && got_b) sph ^= 1;
+    ok = mbar_wait_t<kPoll>(&bar_gb, sph, p.wait_ns) && ok;
+    b_fly = false;
+    sph ^= 1;
     uint4 qraw[4], kraw[4], vraw[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -426,7 +424,13 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     // the previous item's record copies must have read A1 before it is rewritten
     if (copy_group(tid) >= 0) bulk_wait_read_all();
     ok = __syncthreads_and(ok);
-    if (!ok) break;
+    if (!ok) {
+      // a wait above gave up: this item's staging groups may still be in
+      // flight; mark both, with their phase, for the drain at the end
+      a_fly = b_fly = true;
+      sph ^= 1;
+      break;
+    }
     if (tid < 64) {
       inv_q[tid] = inv_norm_of(nrm[tid] + nrm[64 + tid]);
       inv_k[tid] = inv_norm_of(nrm[128 + tid] + nrm[192 + tid]);
@@ -523,7 +527,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     }
     // the A_kk tile is rewritten below: the AK copies must have read it
     if (copy_group(tid) >= 0) bulk_wait_read_all();
-    ok = __syncthreads_and(mbar_wait(&bar_mma, 0, p.wait_ns));
+    ok = __syncthreads_and(mbar_wait_t<kPoll>(&bar_mma, 0, p.wait_ns));
     fence_after_sync();
     if (!ok) break;
     {
@@ -602,7 +606,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
                  sdesc(smem_u32(B2) + s * 256, 128, kB2Sbo), id, s > 0);
       mma_commit(&bar_mma);
     }
-    ok = __syncthreads_and(mbar_wait(&bar_mma, 1, p.wait_ns));
+    ok = __syncthreads_and(mbar_wait_t<kPoll>(&bar_mma, 1, p.wait_ns));
     fence_after_sync();
     if (!ok) break;
     // MMA 2 has read B2: the next item's q and v (group B) are staged there now
@@ -704,8 +708,9 @@ bool encode_rows(CUtensorMap* m, const void* base, int H, int64_t T) {
 }  // namespace
 
 cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(tc_intra, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)Smem::BYTES);
+  const bool poll = p.wait_ns < kPollLimitNs;
+  cudaError_t e = cudaFuncSetAttribute(poll ? tc_intra<true> : tc_intra<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem::BYTES);
   if (e != cudaSuccess || p.max_chunks == 0 || p.total_tokens == 0) return e;
   RowMaps maps;
   if (!encode_rows(&maps.g, p.g, p.H, p.total_tokens) || !encode_rows(&maps.q, p.q, p.H, p.total_tokens) ||
@@ -717,7 +722,10 @@ cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int64_t n_items = p.max_chunks * (int64_t)p.H;
   const int64_t grid = n_items < 2 * (int64_t)sms ? n_items : 2 * (int64_t)sms;
-  tc_intra<<<(unsigned)grid, kThreads, Smem::BYTES, stream>>>(p, n_items, maps);
+  if (poll)
+    tc_intra<true><<<(unsigned)grid, kThreads, Smem::BYTES, stream>>>(p, n_items, maps);
+  else
+    tc_intra<false><<<(unsigned)grid, kThreads, Smem::BYTES, stream>>>(p, n_items, maps);
   return cudaGetLastError();
 }
 

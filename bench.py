@@ -220,6 +220,35 @@ def bench_prep(torch, kda, W, dev, reps=10):
             "us": t * 1e3, "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (t * 1e-3) / 1e9}
 
 
+def bench_gate_per_head(torch, kda, W, dev, steps=10):
+    """prefill_8k with one decay per token and head (g [T, H], the gated
+    delta rule) instead of one per key channel: the same prefill without
+    the g rows (1282 - 254 = 1028 algorithmic bytes per token-head).  L2
+    flushed before every call."""
+    w = W.WORKLOADS[PREFILL_WL]
+    inp = W.prefill_inputs(w, device=dev, gen_device=dev)
+    gh = inp["g"][:, :, 0].contiguous()
+    p = kda.Prefill(inp["q"], inp["k"], inp["v"], gh, inp["b"], inp["cu_seqlens"],
+                    host_cu_seqlens=inp["cu_seqlens"].cpu())
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        p.run()
+    ms = []
+    for _ in range(steps):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        p.run()
+        e1.record()
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    assert p.device_status() == 0
+    t = sum(ms) / len(ms)
+    T = sum(inp["lens"])
+    return {"workload": w.description + ", g [T, H] (one decay per token and head)",
+            "ms_per_step": t, "tokens_per_s": T / (t * 1e-3), "steps": steps}
+
+
 def bench_varlen(torch, kda, W, dev, steps=10):
     """The varlen configuration: 8 packed sequences of U[1024, 32768] tokens,
     H=32, d=128, bf16, seeded fp32 initial states, fp32 snapshots every 4096
@@ -441,6 +470,7 @@ def gpu_arm(a):
     prep = bench_prep(torch, kda, W, dev) if rank == 0 else None
     m1 = bench_1m(torch, kda, W, dev) if rank == 0 and a.with_1m else None
     vl = bench_varlen(torch, kda, W, dev) if rank == 0 else None
+    gph = bench_gate_per_head(torch, kda, W, dev) if rank == 0 else None
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -512,6 +542,7 @@ def gpu_arm(a):
                 "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
                 "ms_per_step": e2e["ms_per_step"]},
         "prefill_varlen": vl,
+        "prefill_gate_per_head": gph,
         "segment_scan": scan,
         **({"prefill_1m": m1} if m1 else {}),
         "prep": dict(prep, peak=pk["hbm_gbs"], frac=prep["achieved_gbs"] / pk["hbm_gbs"],

@@ -23,7 +23,8 @@
  *
  * Conventions shared by every call.
  *   - Every tensor is caller-owned device memory, row-major and contiguous,
- *     token-major: q, k, g [T, H, dk]; v, o [T, H, dv]; b [T, H]; states
+ *     token-major: q, k, g [T, H, dk] (g [T, H] with gate_per_head);
+ *     v, o [T, H, dv]; b [T, H]; states
  *     [.., H, dk, dv] fp32.  The library allocates no device memory and keeps
  *     no mutable global state (the prefix cache's host index lives in the
  *     object the caller creates); calls from several host threads are safe.
@@ -122,6 +123,13 @@ typedef struct {
                                   raises status flag 8 and winds down (its copies
                                   and MMAs in flight are still awaited, with the
                                   1 s limit).  A short limit exercises that path. */
+  int32_t gate_per_head;       /* 0: g is [T, H, dk], a decay per key channel (KDA);
+                                  1: g is [T, H], one decay per token and head (the
+                                  gated delta rule: "Kimi K3: The Manos, The
+                                  Mythos, The Legendos" bullet on KDA as online
+                                  learning -- a forget gate, which KDA makes
+                                  diagonal); the result is that of a per-channel g
+                                  holding the same value in every channel       */
 } kda_prefill_args;
 
 /*
@@ -232,6 +240,7 @@ typedef struct {
   int32_t segments;            /* pieces of the pipeline, 0 = default, <= 64     */
   void* copy_in_stream;        /* cudaStream_t for host->device copies (not `stream`) */
   void* copy_out_stream;       /* cudaStream_t for device->host copies (not `stream`) */
+  int32_t gate_per_head;       /* as in kda_prefill_args: g is [T, H] when set    */
 } kda_prefill_host_args;
 
 /* Device workspace bytes kda_prefill_host needs (host-side fields only);
@@ -328,6 +337,7 @@ typedef struct {
   int32_t* status;             /* device int32 or NULL: bit 8 is OR-ed in when a
                                   bounded wait gives up (the rows after it are
                                   then not updated)                               */
+  int32_t gate_per_head;       /* as in kda_prefill_args: g is [B, H] when set    */
 } kda_decode_args;
 
 kda_status_t kda_decode_step(const kda_decode_args* args, void* stream);
@@ -354,6 +364,8 @@ typedef struct {
   float* khat;                 /* device [T, H, dk]                               */
   float* G;                    /* device [T, H, dk]                               */
   float* beta;                 /* device [T, H]                                   */
+  int32_t gate_per_head;       /* as in kda_prefill_args: g is [T, H] when set (G
+                                  is still written [T, H, dk], equal across dk)  */
 } kda_prep_args;
 
 kda_status_t kda_prep(const kda_prep_args* args, void* stream);

@@ -64,6 +64,7 @@ kda_status_t validate_prefill(const kda_prefill_args* a) {
   if (a->snapshot_slot_map && (!a->snapshots || a->snapshot_map_len < 0)) return KDA_ERR_INVALID_ARG;
   if (!a->snapshot_slot_map && a->snapshot_map_len != 0) return KDA_ERR_INVALID_ARG;
   if (a->wait_limit_ns < 0) return KDA_ERR_INVALID_ARG;
+  if (a->gate_per_head != 0 && a->gate_per_head != 1) return KDA_ERR_INVALID_ARG;
   // sizes whose products must stay inside the index types used by the kernels
   if (a->total_tokens > ((int64_t)1 << 40)) return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
@@ -188,6 +189,7 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
   cp.inter = reinterpret_cast<float*>(w + L.inter);
   cp.rec_floats = L.rec_bytes / sizeof(float);
   cp.wait_ns = a->wait_limit_ns > 0 ? (uint64_t)a->wait_limit_ns : 1000000000ull;
+  cp.gate_per_head = a->gate_per_head;
   if (P > 1) {
     ScanBuffers sb;
     sb.A = reinterpret_cast<float*>(w + L.scan_A);
@@ -247,6 +249,7 @@ kda_status_t kda_decode_step(const kda_decode_args* a, void* stream) {
   if (!a->state_slots && a->num_slots < a->batch) return KDA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(a->state) & 15) != 0) return KDA_ERR_INVALID_ARG;
   if (a->wait_limit_ns < 0) return KDA_ERR_INVALID_ARG;
+  if (a->gate_per_head != 0 && a->gate_per_head != 1) return KDA_ERR_INVALID_ARG;
   return from_cuda(launch_decode(*a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -259,6 +262,7 @@ kda_status_t kda_prep(const kda_prep_args* a, void* stream) {
   if (a->total_tokens > 0 &&
       (!a->q || !a->k || !a->g || !a->b || !a->qhat || !a->khat || !a->G || !a->beta))
     return KDA_ERR_INVALID_ARG;
+  if (a->gate_per_head != 0 && a->gate_per_head != 1) return KDA_ERR_INVALID_ARG;
   return from_cuda(launch_prep(*a, static_cast<cudaStream_t>(stream)));
 }
 

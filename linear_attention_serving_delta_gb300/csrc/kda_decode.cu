@@ -68,7 +68,7 @@ decode_step(kda_decode_args a) {
       const float xq = ld_in(q, base_k + c), xk = ld_in(k, base_k + c);
       qn[c] = xq;
       kn[c] = xk;
-      al[c] = expf(log_alpha_of(ld_in(g, base_k + c)));
+      al[c] = expf(log_alpha_of(ld_in(g, a.gate_per_head ? (int64_t)row * H + h : base_k + c)));
       sq += xq * xq;
       sk += xk * xk;
     }
@@ -210,12 +210,14 @@ __device__ __forceinline__ void ring_issue(const kda_decode_args& a, uint8_t* st
     return;
   }
   constexpr uint32_t ROW = Ring<TIn>::ROW;
-  tc::mbar_arrive_expect_tx(bar, kStateBytes + 4 * ROW);
+  // (with a gate per head there is no g row: the compute warps read its one value)
+  tc::mbar_arrive_expect_tx(bar, kStateBytes + (a.gate_per_head ? 3 : 4) * ROW);
   const int64_t e = ((int64_t)row * H + h) * 128;
   tc::bulk_g2s(stage, a.state + ((size_t)slot * H + h) * 128 * 128, kStateBytes, bar);
   tc::bulk_g2s(stage + kStateBytes, static_cast<const TIn*>(a.q) + e, ROW, bar);
   tc::bulk_g2s(stage + kStateBytes + ROW, static_cast<const TIn*>(a.k) + e, ROW, bar);
-  tc::bulk_g2s(stage + kStateBytes + 2 * ROW, static_cast<const TIn*>(a.g) + e, ROW, bar);
+  if (!a.gate_per_head)
+    tc::bulk_g2s(stage + kStateBytes + 2 * ROW, static_cast<const TIn*>(a.g) + e, ROW, bar);
   tc::bulk_g2s(stage + kStateBytes + 3 * ROW, static_cast<const TIn*>(a.v) + e, ROW, bar);
 }
 
@@ -312,7 +314,7 @@ decode_ring(kda_decode_args a, int64_t n_items) {
       const int r = warp + 8 * lane;
       xq = ld_in(rq, r);
       xk = ld_in(rk, r);
-      xa = expf(log_alpha_of(ld_in(rg, r)));
+      xa = expf(log_alpha_of(a.gate_per_head ? ld_in(static_cast<const TIn*>(a.g), item) : ld_in(rg, r)));
     }
     {
       const float sq = warp_sum(xq * xq), sk = warp_sum(xk * xk), sqk = warp_sum(xq * xk);
@@ -405,7 +407,8 @@ template <typename TIn, int DK, int DV>
 cudaError_t launch_t(const kda_decode_args& a, cudaStream_t stream) {
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   // the bulk copies of the ring need 16-byte aligned sources
-  if (DK == 128 && DV == 128 && al16(a.q) && al16(a.k) && al16(a.g) && al16(a.v) && al16(a.state))
+  if (DK == 128 && DV == 128 && al16(a.q) && al16(a.k) && (a.gate_per_head || al16(a.g)) && al16(a.v) &&
+      al16(a.state))
     return launch_ring<TIn>(a, stream);
   dim3 grid((unsigned)a.batch, (unsigned)a.num_heads);
   decode_step<TIn, DK, DV><<<grid, DecodeShape<TIn, DK, DV>::NT, 0, stream>>>(a);

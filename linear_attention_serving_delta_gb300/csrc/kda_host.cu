@@ -35,6 +35,7 @@ kda_status_t validate_host(const kda_prefill_host_args* a) {
   if (a->total_tokens > 0 && (!a->q || !a->k || !a->v || !a->g || !a->b || !a->o))
     return KDA_ERR_INVALID_ARG;
   if (a->segments < 0 || a->segments > kMaxSegments) return KDA_ERR_INVALID_ARG;
+  if (a->gate_per_head != 0 && a->gate_per_head != 1) return KDA_ERR_INVALID_ARG;
   if (a->total_tokens > ((int64_t)1 << 40)) return KDA_ERR_UNSUPPORTED;
   const int64_t* cu = a->cu_seqlens;
   if (cu[0] != 0 || cu[a->num_seqs] != a->total_tokens) return KDA_ERR_INVALID_ARG;
@@ -123,7 +124,8 @@ kda_prefill_args piece_args(const kda_prefill_host_args* a, const HostLayout& L,
   s.q = w + L.q + p.tok0 * H * a->dk * es;
   s.k = w + L.k + p.tok0 * H * a->dk * es;
   s.v = w + L.v + p.tok0 * H * a->dv * es;
-  s.g = w + L.g + p.tok0 * H * a->dk * es;
+  s.g = w + L.g + p.tok0 * H * (a->gate_per_head ? 1 : a->dk) * es;
+  s.gate_per_head = a->gate_per_head;
   s.b = w + L.b + p.tok0 * H * es;
   s.scale = a->scale;
   s.o = w + L.o + p.tok0 * H * a->dv * es;
@@ -158,7 +160,7 @@ HostLayout host_layout(const kda_prefill_host_args* a, const std::vector<Piece>&
   L.q = take((size_t)T * H * a->dk * es);
   L.k = take((size_t)T * H * a->dk * es);
   L.v = take((size_t)T * H * a->dv * es);
-  L.g = take((size_t)T * H * a->dk * es);
+  L.g = take((size_t)T * H * (a->gate_per_head ? 1 : a->dk) * es);
   L.b = take((size_t)T * H * es);
   L.o = take((size_t)T * H * a->dv * es);
   L.init = take(a->initial_state ? N * state : 0);
@@ -271,9 +273,10 @@ extern "C" kda_status_t kda_prefill_host(const kda_prefill_host_args* a, void* w
   for (size_t i = 0; i < np && e == cudaSuccess; ++i) {
     const int64_t t0 = pieces[i].tok0, n = pieces[i].tok1 - pieces[i].tok0;
     const size_t rk = (size_t)H * a->dk * es, rv = (size_t)H * a->dv * es;
+    const size_t rg = a->gate_per_head ? (size_t)H * es : rk;
     h2d(L.q + t0 * rk, hq + t0 * rk, n * rk);
     h2d(L.k + t0 * rk, hk + t0 * rk, n * rk);
-    h2d(L.g + t0 * rk, hg + t0 * rk, n * rk);
+    h2d(L.g + t0 * rg, hg + t0 * rg, n * rg);
     h2d(L.v + t0 * rv, hv + t0 * rv, n * rv);
     ok(cudaEventRecord(ev_in[i], in));
   }

@@ -59,6 +59,7 @@ struct ChunkParams {
   int32_t k3_mode;
   float* trans;     // [num_seqs][H][dk][dk] in kScanPass1
   uint64_t wait_ns; // limit of the bounded waits on copies and MMAs (not of the drains)
+  int32_t gate_per_head;  // g is [T, H] (one decay per token and head), else [T, H, dk]
 };
 constexpr int32_t kScanPass1 = 1;
 

@@ -62,7 +62,8 @@ prep_kernel(kda_prep_args a) {
     if (cs < lo) cs = lo;  // only reachable with malformed cu_seqlens
     if (cs > t0) cs = t0;
     float run = 0.f;
-    for (int64_t t = cs; t < t0; ++t) run += log_alpha_of(ld_in(g, (t * H + h) * dk + c));
+    const bool ph = a.gate_per_head != 0;  // g [T, H]: one logit per token and head
+    for (int64_t t = cs; t < t0; ++t) run += log_alpha_of(ld_in(g, ph ? t * H + h : (t * H + h) * dk + c));
     for (int64_t t = t0; t < t1; ++t) {
       while (s + 1 < a.num_seqs && a.cu_seqlens[s + 1] <= t) {
         ++s;
@@ -70,7 +71,7 @@ prep_kernel(kda_prep_args a) {
       }
       if ((t - seq0) % kChunk == 0) run = 0.f;
       const int64_t e = (t * H + h) * dk + c;
-      run += log_alpha_of(ld_in(g, e));
+      run += log_alpha_of(ld_in(g, ph ? t * H + h : e));
       a.G[e] = run;
       a.qhat[e] = ld_in(q, e) * inv_q[t - t0];
       a.khat[e] = ld_in(k, e) * inv_k[t - t0];
@@ -242,7 +243,8 @@ bool aligned16p(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) ==
 cudaError_t launch_prep(const kda_prep_args& a, cudaStream_t stream) {
   if (a.total_tokens == 0) return cudaSuccess;
   dim3 grid((unsigned)((a.total_tokens + kChunk - 1) / kChunk), (unsigned)a.num_heads);
-  if (a.in_dtype == KDA_BF16 && a.dk == 128 && aligned16p(a.q) && aligned16p(a.k) && aligned16p(a.g) &&
+  if (a.in_dtype == KDA_BF16 && a.dk == 128 && !a.gate_per_head && aligned16p(a.q) && aligned16p(a.k) &&
+      aligned16p(a.g) &&
       aligned16p(a.qhat) && aligned16p(a.khat) && aligned16p(a.G))
     prep_vec<<<grid, kVecThreads, 0, stream>>>(a);
   else if (a.in_dtype == KDA_BF16)

@@ -61,7 +61,7 @@ simt_intra(ChunkParams p) {
       const int64_t e = ((ch.tok0 + i) * H + h) * dk + col;
       xq = ld_in(q, e);
       xk = ld_in(k, e);
-      la = log_alpha_of(ld_in(g, e));
+      la = log_alpha_of(ld_in(g, p.gate_per_head ? (ch.tok0 + i) * H + h : e));
     }
     qh[idx] = xq;
     kh[idx] = xk;

@@ -58,7 +58,8 @@ struct Smem {
   // inv_q, inv_k, beta [64]; norm partials [q/k][channel half][64];
   // decay totals of each token quarter [4][128]
   static constexpr uint32_t MISC = AKK + 64 * kAs * 4;
-  static constexpr uint32_t BYTES = MISC + (3 * 64 + 2 * 2 * 64 + 4 * 128) * 4;
+  // + the per-token decay logits of the item (gate per head), [64]
+  static constexpr uint32_t BYTES = MISC + (3 * 64 + 2 * 2 * 64 + 4 * 128 + 64) * 4;
 };
 static_assert(Smem::B1 % 16 == 0 && Smem::B2 % 16 == 0 && Smem::A2 % 16 == 0 && Smem::AKK % 16 == 0,
               "operand tiles and float4 arrays are 16-byte aligned");
@@ -249,6 +250,14 @@ __device__ __forceinline__ void stage_group(uint8_t* sm, uint64_t* bar, const It
   tma_rows(sm + s1, t1, h, ch.tok0, bar);
 }
 
+// The rows of one tensor of item (ch, h) on `bar` (group A with a gate per
+// head: k alone).  Issued by one thread.
+__device__ __forceinline__ void stage_one(uint8_t* sm, uint64_t* bar, const ItemChunk& ch, int h,
+                                          const CUtensorMap* t0, uint32_t s0) {
+  mbar_arrive_expect_tx(bar, kRowsBytes);
+  tma_rows(sm + s0, t0, h, ch.tok0, bar);
+}
+
 // 16 bytes of a raw row in a staging: token i, channels c0..c0+7
 __device__ __forceinline__ uint4 raw16(const uint8_t* sm, uint32_t stage, int i, int c0) {
   return *reinterpret_cast<const uint4*>(sm + stage + i * 256 + c0 * 2);
@@ -258,13 +267,21 @@ __device__ __forceinline__ float load_b(const ChunkParams& p, const ItemChunk& c
   const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(p.b);
   return (tid < 64 && tid < ch.len) ? __bfloat162float(gb[((int64_t)ch.tok0 + tid) * p.H + h]) : 0.f;
 }
+// the decay logit of token tid of item (ch, h) with a gate per head (g [T, H]);
+// rows past the chunk get 0 (they are masked where they are used)
+__device__ __forceinline__ float load_gh(const ChunkParams& p, const ItemChunk& ch, int h, int tid) {
+  const __nv_bfloat16* gg = static_cast<const __nv_bfloat16*>(p.g);
+  return (tid < 64 && tid < ch.len) ? __bfloat162float(gg[((int64_t)ch.tok0 + tid) * p.H + h]) : 0.f;
+}
 
 // Persistent: two CTAs per SM walk the (chunk, head) items with stride
 // gridDim.x.  The next item's rows are prefetched into L2 at the top of an
 // item and staged by bulk copies as soon as their tiles are free.  TMEM and
 // the mbarriers are set up once per CTA.
-// kPoll: the instantiation for wait limits under kPollLimitNs (the give-up test)
-template <bool kPoll>
+// kPoll: the instantiation for wait limits under kPollLimitNs (the give-up
+// test).  kHeadGate: g is [T, H], one decay per token and head (the gated
+// delta rule): no g rows are staged, the scan runs over tokens only.
+template <bool kPoll, bool kHeadGate>
 __global__ void __launch_bounds__(kThreads, 2)
 tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -298,6 +315,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
   float* beta = inv_k + 64;
   float* nrm = beta + 64;        // [q/k][channel half][64]
   float* qtot = nrm + 2 * 2 * 64;  // [token quarter][128]
+  float* gtok = qtot + 4 * 128;    // [64] decay logits of this item's tokens (gate per head)
 
   if (warp == 0) tmem_alloc(&tmem_base, 256);
   if (tid == 0) {
@@ -317,13 +335,16 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
   {
     const int h0 = (int)(item % H);
     if (tid == 0) {
-      stage_group(sm, &bar_ga, ch, h0, &maps.g, kGStage, &maps.k, kKStage);
+      if (kHeadGate) stage_one(sm, &bar_ga, ch, h0, &maps.k, kKStage);
+      else stage_group(sm, &bar_ga, ch, h0, &maps.g, kGStage, &maps.k, kKStage);
       stage_group(sm, &bar_gb, ch, h0, &maps.q, kQStage, &maps.v, kVStage);
     }
+    if (kHeadGate && tid < 64) gtok[tid] = load_gh(p, ch, h0, tid);
   }
   bool a_fly = true, b_fly = true;  // staging groups in flight, not yet awaited
   uint32_t sph = 0;                 // the phase they complete
   float bnext = load_b(p, ch, (int)(item % H), tid);
+  float gnext = 0.f;                // the next item's decay logit of token tid (gate per head)
 
   fence_before_sync();
   __syncthreads();
@@ -344,7 +365,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     const int hn = (int)((item + stride) % H);
     const float bcur = bnext;
     // the next item's rows into L2 now, so that their staging copies hit L2
-    if (has_next && tid < 4)
+    if (has_next && tid < 4 && !(kHeadGate && tid == 0))
       tma_rows_l2(tid == 0 ? &maps.g : tid == 1 ? &maps.k : tid == 2 ? &maps.q : &maps.v, hn,
                   chn.tok0);
     // this item's g and k (group A) have landed; q and v (group B) may still fly
@@ -356,16 +377,12 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     // across the warp's 4 token blocks (lanes 8 apart), then across the token
     // quarters through shared memory (below)
     float Gm[4][8], qtot_own[8];
-    uint4 graw[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) graw[r] = raw16(sm, kGStage, i0 + r, c0);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    // the scan of one channel: a[r] = alpha of token i0 + r -> Gm[r][j], qtot_own[j]
+    auto scan_channel = [&](const float* a, int j) {
       float run = 1.f;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const float a = i0 + r < len ? alpha_fast(bf16_at(graw[r], j)) : 1.f;
-        run *= a;
+        run *= a[r];
         Gm[r][j] = run;
       }
       float inc = run;
@@ -378,6 +395,30 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
 #pragma unroll
       for (int r = 0; r < 4; ++r) Gm[r][j] *= ex;
       qtot_own[j] = __shfl_sync(0xffffffffu, inc, 24 + cg);  // this quarter's product
+    };
+    if constexpr (kHeadGate) {
+      // one decay per token: the scan of one channel, shared by all eight
+      float a[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) a[r] = i0 + r < len ? alpha_fast(gtok[i0 + r]) : 1.f;
+      scan_channel(a, 0);
+#pragma unroll
+      for (int j = 1; j < 8; ++j) {
+        qtot_own[j] = qtot_own[0];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) Gm[r][j] = Gm[r][0];
+      }
+    } else {
+      uint4 graw[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) graw[r] = raw16(sm, kGStage, i0 + r, c0);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float a[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) a[r] = i0 + r < len ? alpha_fast(bf16_at(graw[r], j)) : 1.f;
+        scan_channel(a, j);
+      }
     }
     if (tb == 0) {
       *reinterpret_cast<float4*>(qtot + qt * 128 + c0) =
@@ -593,8 +634,12 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     // T is consumed (B1) and the A_kk tile free: the next item's g and k
     // (group A) are staged now
     if (has_next) {
-      if (tid == 0) stage_group(sm, &bar_ga, chn, hn, &maps.g, kGStage, &maps.k, kKStage);
+      if (tid == 0) {
+        if (kHeadGate) stage_one(sm, &bar_ga, chn, hn, &maps.k, kKStage);
+        else stage_group(sm, &bar_ga, chn, hn, &maps.g, kGStage, &maps.k, kKStage);
+      }
       bnext = load_b(p, chn, hn, tid);
+      if (kHeadGate) gnext = load_gh(p, chn, hn, tid);
       a_fly = true;
     }
     // ---- MMA 2: [W | U~] = Tb [Kp | V]   (M=64, N=256, K=64)
@@ -644,6 +689,8 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
         }
       }
     }
+    // the next item's decay logits (gate per head): this item's scan is done
+    if (kHeadGate && has_next && tid < 64) gtok[tid] = gnext;
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -708,13 +755,16 @@ bool encode_rows(CUtensorMap* m, const void* base, int H, int64_t T) {
 }  // namespace
 
 cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream) {
-  const bool poll = p.wait_ns < kPollLimitNs;
-  cudaError_t e = cudaFuncSetAttribute(poll ? tc_intra<true> : tc_intra<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem::BYTES);
+  const bool poll = p.wait_ns < kPollLimitNs, head = p.gate_per_head != 0;
+  auto kernel = poll ? (head ? tc_intra<true, true> : tc_intra<true, false>)
+                     : (head ? tc_intra<false, true> : tc_intra<false, false>);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem::BYTES);
   if (e != cudaSuccess || p.max_chunks == 0 || p.total_tokens == 0) return e;
   RowMaps maps;
-  if (!encode_rows(&maps.g, p.g, p.H, p.total_tokens) || !encode_rows(&maps.q, p.q, p.H, p.total_tokens) ||
-      !encode_rows(&maps.k, p.k, p.H, p.total_tokens) || !encode_rows(&maps.v, p.v, p.H, p.total_tokens))
+  // with a gate per head there are no g rows to stage (the g map is not used)
+  if (!encode_rows(&maps.g, head ? p.k : p.g, p.H, p.total_tokens) ||
+      !encode_rows(&maps.q, p.q, p.H, p.total_tokens) || !encode_rows(&maps.k, p.k, p.H, p.total_tokens) ||
+      !encode_rows(&maps.v, p.v, p.H, p.total_tokens))
     return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);
@@ -722,10 +772,7 @@ cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int64_t n_items = p.max_chunks * (int64_t)p.H;
   const int64_t grid = n_items < 2 * (int64_t)sms ? n_items : 2 * (int64_t)sms;
-  if (poll)
-    tc_intra<true><<<(unsigned)grid, kThreads, Smem::BYTES, stream>>>(p, n_items, maps);
-  else
-    tc_intra<false><<<(unsigned)grid, kThreads, Smem::BYTES, stream>>>(p, n_items, maps);
+  kernel<<<(unsigned)grid, kThreads, Smem::BYTES, stream>>>(p, n_items, maps);
   return cudaGetLastError();
 }
 

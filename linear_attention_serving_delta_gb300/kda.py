@@ -58,7 +58,7 @@ class PrefillArgs(ctypes.Structure):
                 ("num_boundaries", c_i64), ("cu_snapshots", c_vp), ("snapshots", c_vp),
                 ("num_snapshots", c_i64), ("phase_events", c_vp), ("scan_segments", c_i32),
                 ("snapshot_slot_map", c_vp), ("snapshot_map_len", c_i64),
-                ("wait_limit_ns", c_i64)]
+                ("wait_limit_ns", c_i64), ("gate_per_head", c_i32)]
 
 
 class PrefillHostArgs(ctypes.Structure):
@@ -66,7 +66,8 @@ class PrefillHostArgs(ctypes.Structure):
                 ("total_tokens", c_i64), ("cu_seqlens", c_vp), ("in_dtype", ctypes.c_int),
                 ("q", c_vp), ("k", c_vp), ("v", c_vp), ("g", c_vp), ("b", c_vp),
                 ("scale", c_f32), ("initial_state", c_vp), ("o", c_vp), ("final_state", c_vp),
-                ("segments", c_i32), ("copy_in_stream", c_vp), ("copy_out_stream", c_vp)]
+                ("segments", c_i32), ("copy_in_stream", c_vp), ("copy_out_stream", c_vp),
+                ("gate_per_head", c_i32)]
 
 
 class DecodeArgs(ctypes.Structure):
@@ -74,14 +75,14 @@ class DecodeArgs(ctypes.Structure):
                 ("num_slots", c_i32), ("in_dtype", ctypes.c_int), ("scale", c_f32),
                 ("q", c_vp), ("k", c_vp), ("v", c_vp), ("g", c_vp), ("b", c_vp),
                 ("state", c_vp), ("state_slots", c_vp), ("o", c_vp), ("wait_limit_ns", c_i64),
-                ("status", c_vp)]
+                ("status", c_vp), ("gate_per_head", c_i32)]
 
 
 class PrepArgs(ctypes.Structure):
     _fields_ = [("num_seqs", c_i32), ("num_heads", c_i32), ("dk", c_i32),
                 ("total_tokens", c_i64), ("cu_seqlens", c_vp), ("in_dtype", ctypes.c_int),
                 ("q", c_vp), ("k", c_vp), ("g", c_vp), ("b", c_vp), ("qhat", c_vp),
-                ("khat", c_vp), ("G", c_vp), ("beta", c_vp)]
+                ("khat", c_vp), ("G", c_vp), ("beta", c_vp), ("gate_per_head", c_i32)]
 
 
 _lock = threading.Lock()
@@ -183,7 +184,8 @@ def make_prefill_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=
     T, H, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
-    for name, t, shp in (("k", k, (T, H, dk)), ("g", g, (T, H, dk)), ("v", v, (T, H, dv)),
+    gshape = (T, H) if g.dim() == 2 else (T, H, dk)  # [T, H]: one decay per token and head
+    for name, t, shp in (("k", k, (T, H, dk)), ("g", g, gshape), ("v", v, (T, H, dv)),
                          ("b", b, (T, H)), ("o", o, (T, H, dv))):
         if tuple(t.shape) != shp:
             raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shp}")
@@ -208,6 +210,7 @@ def make_prefill_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=
     a.snapshot_slot_map = _ptr(snapshot_slot_map, torch.int32, "snapshot_slot_map")
     a.snapshot_map_len = 0 if snapshot_slot_map is None else snapshot_slot_map.numel()
     a.wait_limit_ns = int(wait_limit_ns)
+    a.gate_per_head = 1 if g.dim() == 2 else 0
     return a
 
 
@@ -242,7 +245,8 @@ def make_prefill_host_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_s
     T, H, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
-    for name, t, shp in (("k", k, (T, H, dk)), ("g", g, (T, H, dk)), ("v", v, (T, H, dv)),
+    gshape = (T, H) if g.dim() == 2 else (T, H, dk)  # [T, H]: one decay per token and head
+    for name, t, shp in (("k", k, (T, H, dk)), ("g", g, gshape), ("v", v, (T, H, dv)),
                          ("b", b, (T, H)), ("o", o, (T, H, dv))):
         if tuple(t.shape) != shp:
             raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shp}")
@@ -259,6 +263,7 @@ def make_prefill_host_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_s
     a.segments = int(segments)
     a.copy_in_stream = None if copy_in_stream is None else _stream(copy_in_stream)
     a.copy_out_stream = None if copy_out_stream is None else _stream(copy_out_stream)
+    a.gate_per_head = 1 if g.dim() == 2 else 0
     return a
 
 
@@ -325,6 +330,7 @@ def kda_decode_step(q, k, v, g, b, state, o, state_slots=None, scale=1.0, stream
     a.state_slots = _ptr(state_slots, torch.int32, "state_slots")
     a.wait_limit_ns = int(wait_limit_ns)
     a.status = _ptr(status, torch.int32, "status")
+    a.gate_per_head = 1 if g.dim() == 2 else 0  # g [B, H]: one decay per row and head
     _check(lib().kda_decode_step(ctypes.byref(a), _stream(stream)), "kda_decode_step")
 
 
@@ -338,6 +344,7 @@ def kda_prep(q, k, g, b, cu_seqlens, qhat, khat, G, beta, stream=None) -> None:
     a.q, a.k, a.g, a.b = _ptr(q, dt, "q"), _ptr(k, dt, "k"), _ptr(g, dt, "g"), _ptr(b, dt, "b")
     a.qhat, a.khat = _ptr(qhat, torch.float32, "qhat"), _ptr(khat, torch.float32, "khat")
     a.G, a.beta = _ptr(G, torch.float32, "G"), _ptr(beta, torch.float32, "beta")
+    a.gate_per_head = 1 if g.dim() == 2 else 0  # g [T, H]: one decay per token and head
     _check(lib().kda_prep(ctypes.byref(a), _stream(stream)), "kda_prep")
 
 

@@ -70,6 +70,8 @@ int main(void) {
   F(kda_prefill_args, snapshots) F(kda_prefill_args, num_snapshots)
   F(kda_prefill_args, phase_events) F(kda_prefill_args, scan_segments)
   F(kda_prefill_args, snapshot_slot_map) F(kda_prefill_args, wait_limit_ns)
+  F(kda_prefill_args, gate_per_head) F(kda_decode_args, gate_per_head)
+  F(kda_prep_args, gate_per_head) F(kda_prefill_host_args, gate_per_head)
   F(kda_decode_args, scale) F(kda_decode_args, q) F(kda_decode_args, state_slots)
   F(kda_decode_args, o) F(kda_decode_args, wait_limit_ns) F(kda_decode_args, status)
   F(kda_prep_args, total_tokens) F(kda_prep_args, in_dtype) F(kda_prep_args, beta)
@@ -128,6 +130,8 @@ def test_workspace_size_and_validation(kda):
     # segment scan: out-of-range counts are rejected; on the tensor-core path
     # (bf16, 128 x 128) with few heads and one long sequence it adds its
     # per-segment state buffers (4 x P x H x 64 KB)
+    a = _args(kda, gate_per_head=2)
+    assert L.kda_prefill_workspace_size(ctypes.byref(a)) == 0
     a = _args(kda, wait_limit_ns=-1)
     assert L.kda_prefill_workspace_size(ctypes.byref(a)) == 0
     assert L.kda_prefill(ctypes.byref(a), 0x4000, 1 << 30, None) == 1

@@ -435,3 +435,85 @@ def test_decode_bounded_waits_give_up_cleanly(oracle_mod):
     ro = oracle_mod.decode(*[host(inp[x][0]) for x in "qkvgb"], ref_state)
     assert rel(host(o), ro) <= TOL["bf16"]
     assert rel(host(state), ref_state) <= 1e-5
+
+
+# ------------------------------------------------------------------ gate per head
+def head_gate(inp):
+    """g [T, H] (one decay logit per token and head) and the same values
+    broadcast to [T, H, dk] for the oracle and the per-channel kernels."""
+    gh = inp["g"][:, :, 0].contiguous()
+    return gh, gh[:, :, None].expand(inp["g"].shape).contiguous()
+
+
+@pytest.mark.parametrize("dtype,dk,dv", [("bf16", 128, 128), ("f32", 64, 32)])
+def test_prefill_gate_per_head(dtype, dk, dv):
+    """g given per (token, head) -- the gated delta rule -- equals the oracle
+    with that value in every channel, and the per-channel kernels on the
+    broadcast g bit for bit (initial states, snapshots, ragged lengths)."""
+    lens = [1, 63, 64, 65, 200, 0, 1300]
+    inp = make_inputs(lens, 3, dk, dv, dtype, 95, s0_std=0.02)
+    gh, gb = head_gate(inp)
+    d = to_dev(inp)
+    kw = dict(initial_state=d["S0"], snapshot_interval=64, scale=0.8,
+              host_cu_seqlens=inp["cu_seqlens"])
+    args = [d["q"], d["k"], d["v"]]
+    ph = kda.Prefill(*args, gh.cuda(), d["b"], d["cu_seqlens"], **kw).run()
+    pc = kda.Prefill(*args, gb.cuda(), d["b"], d["cu_seqlens"], **kw).run()
+    torch.cuda.synchronize()
+    assert ph.device_status() == 0
+    assert torch.equal(ph.o, pc.o) and torch.equal(ph.final_state, pc.final_state)
+    assert torch.equal(ph.snapshot_view, pc.snapshot_view)
+    import oracle
+    sp, cs = oracle.snapshot_positions(lens, 64)
+    ro, rS, rsn = oracle.prefill(host(inp["q"]), host(inp["k"]), host(inp["v"]), host(gb),
+                                 host(inp["b"]), inp["cu_seqlens"].numpy(), S0=host(inp["S0"]),
+                                 scale=0.8, snap_pos=sp, cu_snap=cs)
+    assert rel(host(ph.o), ro) <= TOL[dtype]
+    assert rel(host(ph.final_state), rS) <= TOL[dtype]
+    assert rel(host(ph.snapshot_view), rsn) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 32)])
+def test_decode_and_prep_gate_per_head(dk, dv, oracle_mod):
+    """Decode (the 128 x 128 ring kernel and the generic one) and the prep
+    step with g [rows, H] against the oracle on the broadcast g."""
+    dw = W.DecodeWorkload("gate", 40, 4, dk, dv, 1, 96 + dk)
+    inp = W.decode_inputs(dw)
+    gh = inp["g"][0][:, :, 0].contiguous()
+    gb = gh[:, :, None].expand(inp["g"][0].shape).contiguous()
+    args = [inp[x][0].cuda().contiguous() for x in "qkv"]
+    state = inp["state"].cuda().contiguous()
+    o = torch.zeros(40, 4, dv, dtype=args[0].dtype, device="cuda")
+    kda.kda_decode_step(args[0], args[1], args[2], gh.cuda(), inp["b"][0].cuda().contiguous(), state, o)
+    torch.cuda.synchronize()
+    ref_state = host(inp["state"]).astype(np.float64)
+    ro = oracle_mod.decode(host(inp["q"][0]), host(inp["k"][0]), host(inp["v"][0]), host(gb),
+                           host(inp["b"][0]), ref_state)
+    assert rel(host(o), ro) <= TOL["bf16"]
+    assert rel(host(state), ref_state) <= 1e-5
+    # prep: G equal across channels, q^, k^, beta unchanged
+    pin = make_inputs([70, 130], 3, dk, 16, "bf16", 97)
+    ghp, gbp = head_gate(pin)
+    d = to_dev(pin)
+    qh, kh, G, beta = kda.prep(d["q"], d["k"], ghp.cuda(), d["b"], d["cu_seqlens"])
+    qh2, kh2, G2, beta2 = kda.prep(d["q"], d["k"], gbp.cuda(), d["b"], d["cu_seqlens"])
+    torch.cuda.synchronize()
+    # (for dk = 128 the per-channel g takes the vectorised kernel: another
+    # summation order, hence a tolerance instead of equality)
+    for x, y in ((qh, qh2), (kh, kh2), (beta, beta2), (G, G2)):
+        assert rel(host(x), host(y)) < 1e-6
+
+
+def test_prefill_host_gate_per_head():
+    """The host-buffer entry with g [T, H] equals the device call."""
+    inp = make_inputs([2000], 2, 128, 128, "bf16", 98, s0_std=0.02)
+    gh, _ = head_gate(inp)
+    host_in = {x: inp[x].pin_memory() for x in "qkvb"}
+    o, S = kda.prefill_host(host_in["q"], host_in["k"], host_in["v"], gh.pin_memory(), host_in["b"],
+                            inp["cu_seqlens"], initial_state=inp["S0"], segments=3)
+    d = to_dev(inp)
+    p = kda.Prefill(d["q"], d["k"], d["v"], gh.cuda(), d["b"], d["cu_seqlens"], initial_state=d["S0"],
+                    host_cu_seqlens=inp["cu_seqlens"], scan_segments=1).run()
+    torch.cuda.synchronize()
+    assert rel(o.float().numpy(), host(p.o)) < 2e-3
+    assert rel(S.numpy(), host(p.final_state)) < 1e-4

@@ -249,6 +249,41 @@ def bench_gate_per_head(torch, kda, W, dev, steps=10):
             "ms_per_step": t, "tokens_per_s": T / (t * 1e-3), "steps": steps}
 
 
+def bench_layer_steps(torch, kda, W, dev, steps=10):
+    """prefill_8k with the layer steps around the recurrence: the short
+    convolution (4 taps, SiLU) on q, k, v inside the intra-chunk kernel, with
+    windows in and out, and the per-channel output gate inside the
+    inter-chunk kernel's store.  Algorithmic bytes per token-head: 1282 of
+    the prefill + 256 of gate logits (the taps and windows are a few KB per
+    call).  L2 flushed before every call."""
+    w = W.WORKLOADS[PREFILL_WL]
+    inp = W.prefill_inputs(w, device=dev, gen_device=dev)
+    T = sum(inp["lens"])
+    li = W.layer_inputs(w.seed + 7, 1, T, w.H, w.dk, w.dv, 4, w.dtype, device=dev)
+    p = kda.Prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["b"], inp["cu_seqlens"],
+                    host_cu_seqlens=inp["cu_seqlens"].cpu(), conv_weights=li["taps"],
+                    conv_silu=True, conv_window=li["windows"], conv_window_out=True,
+                    out_gate=li["gate"])
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        p.run()
+    ms = []
+    for _ in range(steps):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        p.run()
+        e1.record()
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    assert p.device_status() == 0
+    t = sum(ms) / len(ms)
+    return {"workload": w.description + ", short convolution (4 taps, SiLU) on q, k, v and a "
+                                        "per-channel output gate",
+            "ms_per_step": t, "tokens_per_s": T / (t * 1e-3), "steps": steps,
+            "algorithmic_bytes": T * w.H * (1282 + 256)}
+
+
 def bench_varlen(torch, kda, W, dev, steps=10):
     """The varlen configuration: 8 packed sequences of U[1024, 32768] tokens,
     H=32, d=128, bf16, seeded fp32 initial states, fp32 snapshots every 4096
@@ -471,6 +506,7 @@ def gpu_arm(a):
     m1 = bench_1m(torch, kda, W, dev) if rank == 0 and a.with_1m else None
     vl = bench_varlen(torch, kda, W, dev) if rank == 0 else None
     gph = bench_gate_per_head(torch, kda, W, dev) if rank == 0 else None
+    lay = bench_layer_steps(torch, kda, W, dev) if rank == 0 else None
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -543,6 +579,7 @@ def gpu_arm(a):
                 "ms_per_step": e2e["ms_per_step"]},
         "prefill_varlen": vl,
         "prefill_gate_per_head": gph,
+        "prefill_layer_steps": lay,
         "segment_scan": scan,
         **({"prefill_1m": m1} if m1 else {}),
         "prep": dict(prep, peak=pk["hbm_gbs"], frac=prep["achieved_gbs"] / pk["hbm_gbs"],

@@ -65,6 +65,54 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
 #define KDA_CHUNK 64
 
 /*
+ * The layer steps on either side of the recurrence (optional).
+ *
+ * "Kimi K3: The Manos, The Mythos, The Legendos" (bullet on the stability
+ * details) names a short convolution on q, k and v and a per-head output
+ * forget gate around the recurrence.  The pages give neither formula; the
+ * readings implemented here:
+ *
+ *   Short convolution, per channel c of each of q, k, v (x one of them):
+ *     y_t[c] = sum_{j < conv_width} w[j][h][c] * x_{t-j}[c]
+ *   a causal depthwise convolution along the tokens of one sequence; tap j
+ *   multiplies the input j tokens back.  Inputs before the first token of a
+ *   sequence come from its window (the conv_width - 1 inputs that preceded
+ *   it), zeros when no window is given.  With conv_silu, y <- y * sigmoid(y).
+ *   The result is rounded to in_dtype (the precision a separate layer would
+ *   store it in) and is what the recurrence then takes as q, k, v (so the
+ *   L2 normalisation of q and k follows the convolution).
+ *
+ *   Output gate: o_t <- o_t * sigmoid(r_t), with r [T, H, dv] (a gate per
+ *   value channel) or [T, H] (out_gate_per_head: one gate per token and
+ *   head), applied after scale and before the rounding of o.
+ *
+ * Windows.  A window holds the raw (unconvolved) inputs of the last
+ * conv_width - 1 tokens, oldest first: [rows, conv_width - 1, H, d] in
+ * in_dtype, row = sequence (prefill) or state slot (decode).  conv_in gives
+ * the windows before the call, conv_out receives those after it (a sequence
+ * shorter than the window keeps the older entries of its input window).  In
+ * the prefill, conv_out may be the same buffer as conv_in (updated in place)
+ * but must not partly overlap it; in the decode both are indexed by the
+ * row's state slot and may be the same buffer.  Snapshots hold only S: a
+ * prefill that resumes at a snapshot position p passes the raw inputs of
+ * tokens p - conv_width + 1 .. p - 1 as its window.
+ */
+#define KDA_CONV_MAX 4
+
+typedef struct {
+  int32_t conv_width;          /* 0 = no convolution, else 1..KDA_CONV_MAX taps  */
+  int32_t conv_silu;           /* nonzero: SiLU after the convolution            */
+  const float* conv_w[3];      /* taps of q, k, v: device [conv_width, H, d] fp32
+                                  (d = dk, dk, dv); all three when conv_width > 0 */
+  const void* conv_in[3];      /* windows of q, k, v before the call, or NULL
+                                  (zeros); each may be NULL on its own           */
+  void* conv_out[3];           /* windows of q, k, v after the call, or NULL     */
+  const void* out_gate;        /* device gate logits, in_dtype: [T, H, dv], or
+                                  [T, H] with out_gate_per_head; NULL = no gate   */
+  int32_t out_gate_per_head;
+} kda_layer_args;
+
+/*
  * Prefill over packed variable-length sequences.
  *
  * Sequence s holds packed tokens [cu_seqlens[s], cu_seqlens[s+1]).  Each
@@ -130,6 +178,9 @@ typedef struct {
                                   learning -- a forget gate, which KDA makes
                                   diagonal); the result is that of a per-channel g
                                   holding the same value in every channel       */
+  const kda_layer_args* layer; /* host pointer, or NULL: the short convolution and
+                                  output gate (above); read during the call only.
+                                  Windows are [N, conv_width - 1, H, d]          */
 } kda_prefill_args;
 
 /*
@@ -338,6 +389,10 @@ typedef struct {
                                   bounded wait gives up (the rows after it are
                                   then not updated)                               */
   int32_t gate_per_head;       /* as in kda_prefill_args: g is [B, H] when set    */
+  const kda_layer_args* layer; /* host pointer, or NULL: the short convolution and
+                                  output gate; windows [num_slots, conv_width - 1,
+                                  H, d] indexed by the row's slot, updated in
+                                  place when conv_out == conv_in                  */
 } kda_decode_args;
 
 kda_status_t kda_decode_step(const kda_decode_args* args, void* stream);

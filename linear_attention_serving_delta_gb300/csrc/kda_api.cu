@@ -13,6 +13,15 @@ bool dtype_ok(kda_dtype_t t) { return t == KDA_F32 || t == KDA_BF16; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// The layer steps' buffers read with 16-byte vector accesses on the
+// tensor-core path (taps, windows, a per-channel output gate).
+bool layer_aligned16(const kda_layer_args* l) {
+  if (!l) return true;
+  for (int t = 0; t < 3; ++t)
+    if (l->conv_width > 0 && (!aligned16(l->conv_w[t]) || !aligned16(l->conv_in[t]))) return false;
+  return l->out_gate_per_head || aligned16(l->out_gate);
+}
+
 // The tensor-core kernels move q, k, g, v, o and the states with 16-byte
 // vector accesses; other layouts take the fp32 CUDA-core path.
 // The tensor-core path: bf16, dk = dv = 128, 16-byte aligned buffers, and
@@ -22,8 +31,35 @@ bool use_tensor_cores(const kda_prefill_args* a) {
          a->total_tokens < ((int64_t)1 << 31) &&
          aligned16(a->q) && aligned16(a->k) && aligned16(a->v) && aligned16(a->g) &&
          aligned16(a->o) && aligned16(a->initial_state) && aligned16(a->final_state) &&
-         aligned16(a->snapshots);
+         aligned16(a->snapshots) && layer_aligned16(a->layer);
 }
+
+// Byte ranges [p, p + n) that overlap without being the same range.
+bool partly_overlap(const void* p, const void* q, size_t n) {
+  if (!p || !q || p == q) return false;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+  return a < b + n && b < a + n;
+}
+
+// The layer steps' arguments (kda.h): `rows` = sequences (prefill) or state
+// slots (decode); `elem` = bytes per element of in_dtype.
+kda_status_t validate_layer(const kda_layer_args* l, int64_t rows, int32_t H, int32_t dk, int32_t dv,
+                            size_t elem) {
+  if (!l) return KDA_OK;
+  if (l->conv_width < 0 || l->conv_width > KDA_CONV_MAX) return KDA_ERR_INVALID_ARG;
+  if (l->out_gate_per_head != 0 && l->out_gate_per_head != 1) return KDA_ERR_INVALID_ARG;
+  if (l->conv_width > 0) {
+    const int32_t d[3] = {dk, dk, dv};
+    for (int t = 0; t < 3; ++t) {
+      if (!l->conv_w[t]) return KDA_ERR_INVALID_ARG;
+      const size_t bytes = (size_t)rows * (l->conv_width - 1) * H * d[t] * elem;
+      if (partly_overlap(l->conv_in[t], l->conv_out[t], bytes)) return KDA_ERR_INVALID_ARG;
+    }
+  }
+  return KDA_OK;
+}
+
+size_t elem_bytes(kda_dtype_t t) { return t == KDA_BF16 ? 2 : 4; }
 
 constexpr int32_t kMaxScanSegments = 64;
 constexpr int32_t kScanSms = 152;  // SMs of the part the automatic choice is sized for
@@ -65,6 +101,8 @@ kda_status_t validate_prefill(const kda_prefill_args* a) {
   if (!a->snapshot_slot_map && a->snapshot_map_len != 0) return KDA_ERR_INVALID_ARG;
   if (a->wait_limit_ns < 0) return KDA_ERR_INVALID_ARG;
   if (a->gate_per_head != 0 && a->gate_per_head != 1) return KDA_ERR_INVALID_ARG;
+  kda_status_t ls = validate_layer(a->layer, a->num_seqs, a->num_heads, a->dk, a->dv, elem_bytes(a->in_dtype));
+  if (ls != KDA_OK) return ls;
   // sizes whose products must stay inside the index types used by the kernels
   if (a->total_tokens > ((int64_t)1 << 40)) return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
@@ -190,6 +228,17 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
   cp.rec_floats = L.rec_bytes / sizeof(float);
   cp.wait_ns = a->wait_limit_ns > 0 ? (uint64_t)a->wait_limit_ns : 1000000000ull;
   cp.gate_per_head = a->gate_per_head;
+  if (const kda_layer_args* l = a->layer) {
+    cp.conv_width = l->conv_width;
+    cp.conv_silu = l->conv_silu != 0;
+    for (int t = 0; t < 3; ++t) {
+      cp.conv_w[t] = l->conv_width > 0 ? l->conv_w[t] : nullptr;
+      cp.conv_in[t] = l->conv_width > 1 ? l->conv_in[t] : nullptr;
+    }
+    cp.conv_one_seq = P > 1;
+    cp.out_gate = l->out_gate;
+    cp.out_gate_per_head = l->out_gate_per_head;
+  }
   if (P > 1) {
     ScanBuffers sb;
     sb.A = reinterpret_cast<float*>(w + L.scan_A);
@@ -202,6 +251,11 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
   } else {
     e = use_tensor_cores(a) ? launch_tc_prefill(cp, stream, ev ? ev[2] : nullptr)
                             : launch_simt_prefill(cp, a->in_dtype, stream, ev ? ev[2] : nullptr);
+  }
+  if (e == cudaSuccess && a->layer && a->layer->conv_width > 1) {
+    const void* x[3] = {a->q, a->k, a->v};
+    e = launch_conv_windows(*a->layer, a->num_seqs, a->num_heads, a->dk, a->dv, a->cu_seqlens,
+                            a->total_tokens, a->in_dtype, x, stream);
   }
   if (e == cudaSuccess) e = mark(3);
   return from_cuda(e);
@@ -250,6 +304,8 @@ kda_status_t kda_decode_step(const kda_decode_args* a, void* stream) {
   if ((reinterpret_cast<uintptr_t>(a->state) & 15) != 0) return KDA_ERR_INVALID_ARG;
   if (a->wait_limit_ns < 0) return KDA_ERR_INVALID_ARG;
   if (a->gate_per_head != 0 && a->gate_per_head != 1) return KDA_ERR_INVALID_ARG;
+  kda_status_t ls = validate_layer(a->layer, a->num_slots, a->num_heads, a->dk, a->dv, elem_bytes(a->in_dtype));
+  if (ls != KDA_OK) return ls;
   return from_cuda(launch_decode(*a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -31,7 +31,7 @@ struct Chunk {
   int32_t len;       // 1..kChunk tokens
   int32_t snap_slot; // snapshot slot written after this chunk, or -1
   int32_t flags;     // kChunkFirst | kChunkLast
-  int64_t pad;
+  int64_t pos;       // its first token's index within its sequence
 };
 static_assert(sizeof(Chunk) == 32, "chunk table entry is 32 bytes");
 enum : int32_t { kChunkFirst = 1, kChunkLast = 2 };
@@ -68,6 +68,19 @@ __device__ __forceinline__ float log_alpha_of(float g) {
 }
 // beta = sigmoid(b)
 __device__ __forceinline__ float beta_of(float b) { return 1.f / (1.f + expf(-b)); }
+// y sigmoid(y), the activation after the short convolution
+__device__ __forceinline__ float silu_of(float y) { return y / (1.f + expf(-y)); }
+// the output gate's factor sigmoid(r)
+__device__ __forceinline__ float out_gate_of(float r) { return 1.f / (1.f + expf(-r)); }
+// x rounded to the input dtype (the precision the convolution's output is kept in)
+template <typename T>
+__device__ __forceinline__ float round_in(float x);
+template <>
+__device__ __forceinline__ float round_in<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float round_in<__nv_bfloat16>(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
 // 1 / max(sqrt(ss), 1e-6)
 __device__ __forceinline__ float inv_norm_of(float ss) {
   return 1.f / fmaxf(sqrtf(ss), 1e-6f);

@@ -19,6 +19,51 @@
 namespace kda {
 namespace {
 
+// ---------------------------------------------------------- layer steps
+// The short convolution of one input channel for one decode token ("Kimi K3:
+// The Manos, The Mythos, The Legendos", bullet on the stability details;
+// formula in include/kda.h): tap 0 on the token's own input x, tap j on the
+// input j tokens back, which is row W - 1 - j of the slot's window (zeros
+// without one); SiLU if asked; rounded to the input dtype.  `prev(m)` reads
+// window row m.
+template <typename TIn, typename Prev>
+__device__ __forceinline__ float conv_token(const kda_layer_args& l, int t, float x, int H, int h, int c, int d,
+                                            Prev prev) {
+  const int W = l.conv_width;
+  const float* w = l.conv_w[t];
+  float acc = w[(int64_t)h * d + c] * x;
+  for (int j = 1; j < W; ++j) acc += w[((int64_t)j * H + h) * d + c] * prev(W - 1 - j);
+  if (l.conv_silu) acc = silu_of(acc);
+  return round_in<TIn>(acc);
+}
+// Row m of the window of tensor t in global memory (slot's rows), 0 without one
+template <typename TIn>
+__device__ __forceinline__ float window_at(const kda_layer_args& l, int t, int slot, int m, int H, int h, int c,
+                                           int d) {
+  const TIn* win = static_cast<const TIn*>(l.conv_in[t]);
+  return win ? ld_in(win, (((int64_t)slot * (l.conv_width - 1) + m) * H + h) * d + c) : 0.f;
+}
+// The window after the token: rows shift down by one (row m <- row m + 1) and
+// the last row takes the raw input x.  Reads precede writes per element, so
+// conv_out may be conv_in.
+template <typename TIn, typename Prev>
+__device__ __forceinline__ void window_push(const kda_layer_args& l, int t, float x, int slot, int H, int h,
+                                            int c, int d, Prev prev) {
+  const int W = l.conv_width;
+  TIn* out = static_cast<TIn*>(l.conv_out[t]);
+  if (W <= 1 || !out) return;
+  const int64_t base = (int64_t)slot * (W - 1);
+  for (int m = 0; m + 1 < W - 1; ++m) st_out(out, ((base + m) * H + h) * d + c, prev(m + 1));
+  st_out(out, ((base + W - 2) * H + h) * d + c, x);
+}
+// the output gate's factor for o element `e` of row `row`, head h (1 without a gate)
+template <typename TIn>
+__device__ __forceinline__ float gate_at(const kda_layer_args& l, int64_t row, int H, int h, int64_t e) {
+  if (!l.out_gate) return 1.f;
+  const TIn* r = static_cast<const TIn*>(l.out_gate);
+  return out_gate_of(ld_in(r, l.out_gate_per_head ? row * H + h : e));
+}
+
 template <typename TIn, int DK, int DV>
 struct DecodeShape {
   static constexpr int QPR = DV / 4;                           // float4 quads per row
@@ -30,7 +75,7 @@ struct DecodeShape {
 
 template <typename TIn, int DK, int DV>
 __global__ void __launch_bounds__(DecodeShape<TIn, DK, DV>::NT)
-decode_step(kda_decode_args a) {
+decode_step(kda_decode_args a, const kda_layer_args l) {
   using Sh = DecodeShape<TIn, DK, DV>;
   constexpr int QPR = Sh::QPR, NT = Sh::NT, NRG = Sh::NRG, RPT = Sh::RPT;
   // arrays read through float4 are 16-byte aligned explicitly
@@ -65,14 +110,32 @@ decode_step(kda_decode_args a) {
     const int64_t base_v = ((int64_t)row * H + h) * DV;
     float sq = 0.f, sk = 0.f;
     for (int c = lane; c < DK; c += 32) {
-      const float xq = ld_in(q, base_k + c), xk = ld_in(k, base_k + c);
+      float xq = ld_in(q, base_k + c), xk = ld_in(k, base_k + c);
+      if (l.conv_width > 0) {
+        auto pq = [&](int m) { return window_at<TIn>(l, 0, slot, m, H, h, c, DK); };
+        auto pk = [&](int m) { return window_at<TIn>(l, 1, slot, m, H, h, c, DK); };
+        const float rq = xq, rk = xk;
+        xq = conv_token<TIn>(l, 0, rq, H, h, c, DK, pq);
+        xk = conv_token<TIn>(l, 1, rk, H, h, c, DK, pk);
+        window_push<TIn>(l, 0, rq, slot, H, h, c, DK, pq);
+        window_push<TIn>(l, 1, rk, slot, H, h, c, DK, pk);
+      }
       qn[c] = xq;
       kn[c] = xk;
       al[c] = expf(log_alpha_of(ld_in(g, a.gate_per_head ? (int64_t)row * H + h : base_k + c)));
       sq += xq * xq;
       sk += xk * xk;
     }
-    for (int c = lane; c < DV; c += 32) vv[c] = ld_in(v, base_v + c);
+    for (int c = lane; c < DV; c += 32) {
+      float xv = ld_in(v, base_v + c);
+      if (l.conv_width > 0) {
+        auto pv = [&](int m) { return window_at<TIn>(l, 2, slot, m, H, h, c, DV); };
+        const float rv = xv;
+        xv = conv_token<TIn>(l, 2, rv, H, h, c, DV, pv);
+        window_push<TIn>(l, 2, rv, slot, H, h, c, DV, pv);
+      }
+      vv[c] = xv;
+    }
     const float iq = inv_norm_of(warp_sum(sq)), ik = inv_norm_of(warp_sum(sk));
     float qk = 0.f;
     for (int c = lane; c < DK; c += 32) {
@@ -144,10 +207,10 @@ decode_step(kda_decode_args a) {
     const float qk = sc[1], scl = a.scale;
     TIn* o = static_cast<TIn*>(a.o);
     const int64_t ob = ((int64_t)row * H + h) * DV + 4 * cq;
-    st_out(o, ob + 0, scl * (oq.x + qk * u.x));
-    st_out(o, ob + 1, scl * (oq.y + qk * u.y));
-    st_out(o, ob + 2, scl * (oq.z + qk * u.z));
-    st_out(o, ob + 3, scl * (oq.w + qk * u.w));
+    st_out(o, ob + 0, scl * (oq.x + qk * u.x) * gate_at<TIn>(l, row, H, h, ob + 0));
+    st_out(o, ob + 1, scl * (oq.y + qk * u.y) * gate_at<TIn>(l, row, H, h, ob + 1));
+    st_out(o, ob + 2, scl * (oq.z + qk * u.z) * gate_at<TIn>(l, row, H, h, ob + 2));
+    st_out(o, ob + 3, scl * (oq.w + qk * u.w) * gate_at<TIn>(l, row, H, h, ob + 3));
   }
 }
 
@@ -172,10 +235,14 @@ constexpr int kRingAllThreads = kRingThreads + 32;  // + the producer warp
 constexpr int kComputeBarrier = 1;           // named barrier of warps 0-7
 constexpr uint32_t kStateBytes = 128 * 128 * 4;
 
-template <typename TIn>
+// A slot: the state, the q, k, g, v rows and, with the short convolution,
+// up to KDA_CONV_MAX - 1 window rows of each of q, k, v
+constexpr int kWinRows = KDA_CONV_MAX - 1;
+template <typename TIn, bool kConv>
 struct Ring {
   static constexpr uint32_t ROW = 128 * sizeof(TIn);  // one q / k / g / v row
-  static constexpr uint32_t STAGE = kStateBytes + 4 * ROW;
+  static constexpr uint32_t WIN = kStateBytes + 4 * ROW;  // window row m of tensor t at WIN + (3 m + t) ROW
+  static constexpr uint32_t STAGE = WIN + (kConv ? 3 * kWinRows * ROW : 0);
   static constexpr uint32_t BYTES = kStages * STAGE;
 };
 
@@ -197,9 +264,9 @@ __device__ __forceinline__ bool bar_and(int id, int n, bool v) {
   return r != 0;
 }
 
-template <typename TIn>
-__device__ __forceinline__ void ring_issue(const kda_decode_args& a, uint8_t* stage, uint64_t* bar,
-                                           int32_t* valid_flag, int64_t item) {
+template <typename TIn, bool kConv>
+__device__ __forceinline__ void ring_issue(const kda_decode_args& a, const kda_layer_args& l, uint8_t* stage,
+                                           uint64_t* bar, int32_t* valid_flag, int64_t item) {
   const int H = a.num_heads;
   const int row = (int)(item / H), h = (int)(item % H);
   const int slot = a.state_slots ? a.state_slots[row] : row;
@@ -209,9 +276,15 @@ __device__ __forceinline__ void ring_issue(const kda_decode_args& a, uint8_t* st
     mbar_arrive(bar);
     return;
   }
-  constexpr uint32_t ROW = Ring<TIn>::ROW;
+  using R = Ring<TIn, kConv>;
+  constexpr uint32_t ROW = R::ROW;
   // (with a gate per head there is no g row: the compute warps read its one value)
-  tc::mbar_arrive_expect_tx(bar, kStateBytes + (a.gate_per_head ? 3 : 4) * ROW);
+  uint32_t bytes = kStateBytes + (a.gate_per_head ? 3 : 4) * ROW;
+  const int nw = kConv ? l.conv_width - 1 : 0;  // window rows per tensor
+  if (kConv)
+    for (int t = 0; t < 3; ++t)
+      if (l.conv_in[t]) bytes += nw * ROW;
+  tc::mbar_arrive_expect_tx(bar, bytes);
   const int64_t e = ((int64_t)row * H + h) * 128;
   tc::bulk_g2s(stage, a.state + ((size_t)slot * H + h) * 128 * 128, kStateBytes, bar);
   tc::bulk_g2s(stage + kStateBytes, static_cast<const TIn*>(a.q) + e, ROW, bar);
@@ -219,12 +292,21 @@ __device__ __forceinline__ void ring_issue(const kda_decode_args& a, uint8_t* st
   if (!a.gate_per_head)
     tc::bulk_g2s(stage + kStateBytes + 2 * ROW, static_cast<const TIn*>(a.g) + e, ROW, bar);
   tc::bulk_g2s(stage + kStateBytes + 3 * ROW, static_cast<const TIn*>(a.v) + e, ROW, bar);
+  if (kConv)
+    for (int t = 0; t < 3; ++t)
+      if (l.conv_in[t])
+        for (int m = 0; m < nw; ++m)
+          tc::bulk_g2s(stage + R::WIN + (3 * m + t) * ROW,
+                       static_cast<const TIn*>(l.conv_in[t]) + (((int64_t)slot * nw + m) * H + h) * 128, ROW,
+                       bar);
 }
 
-// kPoll: the instantiation for wait limits under kPollLimitNs (the give-up test)
-template <typename TIn, bool kPoll>
+// kPoll: the instantiation for wait limits under kPollLimitNs (the give-up
+// test).  kConv: the short convolution (window rows in the slot).
+template <typename TIn, bool kPoll, bool kConv>
 __global__ void __launch_bounds__(kRingAllThreads, 1)
-decode_ring(kda_decode_args a, int64_t n_items) {
+decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
+  using R = Ring<TIn, kConv>;
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ __align__(8) uint64_t full[kStages];  // slot loaded
   __shared__ __align__(8) uint64_t done[kStages];  // slot's state updated by warps 0-7
@@ -232,7 +314,7 @@ decode_ring(kda_decode_args a, int64_t n_items) {
   __shared__ __align__(16) float red_p[2][8][128];
   __shared__ __align__(16) float red_o[2][8][128];
   __shared__ __align__(16) float part[2][8][4];    // per warp: sum q^2, sum k^2, sum q k
-  constexpr uint32_t ROW = Ring<TIn>::ROW;
+  constexpr uint32_t ROW = R::ROW;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.num_heads;
   const int64_t first = blockIdx.x, stride = gridDim.x;
@@ -253,11 +335,11 @@ decode_ring(kda_decode_args a, int64_t n_items) {
     if (lane == 0) {
       int64_t issued = 0;  // items whose slot copies were issued
       for (; issued < kStages && issued < n_local; ++issued)
-        ring_issue<TIn>(a, sm + issued * Ring<TIn>::STAGE, &full[issued], &valid_flag[issued],
-                        first + issued * stride);
+        ring_issue<TIn, kConv>(a, l, sm + issued * R::STAGE, &full[issued], &valid_flag[issued],
+                               first + issued * stride);
       for (int64_t k = 0; k < n_local; ++k) {
         const int st = (int)(k % kStages);
-        uint8_t* stage = sm + st * Ring<TIn>::STAGE;
+        uint8_t* stage = sm + st * R::STAGE;
         if (!tc::mbar_wait_t<kPoll>(&done[st], (uint32_t)((k / kStages) & 1), lim)) {
           // the compute warps gave up: let the slot copies still in flight
           // land (long limit) before the shared memory is given back
@@ -275,7 +357,7 @@ decode_ring(kda_decode_args a, int64_t n_items) {
           tc::bulk_wait_read_all();
         }
         if (k + kStages < n_local) {
-          ring_issue<TIn>(a, stage, &full[st], &valid_flag[st], item + kStages * stride);
+          ring_issue<TIn, kConv>(a, l, stage, &full[st], &valid_flag[st], item + kStages * stride);
           issued = k + kStages + 1;
         }
       }
@@ -289,7 +371,7 @@ decode_ring(kda_decode_args a, int64_t n_items) {
   float b_next = n_local > 0 ? ld_in(gb, first) : 0.f;
   for (int64_t k = 0; k < n_local; ++k) {
     const int st = (int)(k % kStages);
-    uint8_t* stage = sm + st * Ring<TIn>::STAGE;
+    uint8_t* stage = sm + st * R::STAGE;
     const int64_t item = first + k * stride;
     const int buf = (int)(k & 1);
     bool ok = tc::mbar_wait_t<kPoll>(&full[st], (uint32_t)((k / kStages) & 1), lim);
@@ -310,11 +392,29 @@ decode_ring(kda_decode_args a, int64_t n_items) {
     const TIn* rv = reinterpret_cast<const TIn*>(stage + kStateBytes + 3 * ROW);
     // this warp's 16 rows: lane i < 16 holds raw q, k and alpha of row warp + 8 i
     float xq = 0.f, xk = 0.f, xa = 0.f;
+    // with the convolution: window row m of tensor t in the slot (0 without one)
+    auto wrow = [&](int t, int m, int c) {
+      return l.conv_in[t] ? ld_in(reinterpret_cast<const TIn*>(stage + R::WIN + (3 * m + t) * ROW), c) : 0.f;
+    };
+    int slot = 0;
+    if (kConv) {
+      const int row = (int)(item / H);
+      slot = a.state_slots ? a.state_slots[row] : row;
+    }
+    const int hh = (int)(item % H);
     if (lane < 16) {
       const int r = warp + 8 * lane;
       xq = ld_in(rq, r);
       xk = ld_in(rk, r);
       xa = expf(log_alpha_of(a.gate_per_head ? ld_in(static_cast<const TIn*>(a.g), item) : ld_in(rg, r)));
+      if (kConv) {
+        auto pq = [&](int m) { return wrow(0, m, r); };
+        auto pk = [&](int m) { return wrow(1, m, r); };
+        window_push<TIn>(l, 0, xq, slot, H, hh, r, 128, pq);
+        window_push<TIn>(l, 1, xk, slot, H, hh, r, 128, pk);
+        xq = conv_token<TIn>(l, 0, xq, H, hh, r, 128, pq);
+        xk = conv_token<TIn>(l, 1, xk, H, hh, r, 128, pk);
+      }
     }
     {
       const float sq = warp_sum(xq * xq), sk = warp_sum(xk * xk), sqk = warp_sum(xq * xk);
@@ -356,8 +456,19 @@ decode_ring(kda_decode_args a, int64_t n_items) {
       oq.x += y.x; oq.y += y.y; oq.z += y.z; oq.w += y.w;
     }
     const float beta = beta_of(b_cur);
-    const float4 u = make_float4(beta * (ld_in(rv, 4 * lane) - ik * p.x), beta * (ld_in(rv, 4 * lane + 1) - ik * p.y),
-                                 beta * (ld_in(rv, 4 * lane + 2) - ik * p.z), beta * (ld_in(rv, 4 * lane + 3) - ik * p.w));
+    float vx[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      vx[t] = ld_in(rv, 4 * lane + t);
+      if (kConv) {
+        const int c = 4 * lane + t;
+        auto pv = [&](int m) { return wrow(2, m, c); };
+        if (warp == 0) window_push<TIn>(l, 2, vx[t], slot, H, hh, c, 128, pv);
+        vx[t] = conv_token<TIn>(l, 2, vx[t], H, hh, c, 128, pv);
+      }
+    }
+    const float4 u = make_float4(beta * (vx[0] - ik * p.x), beta * (vx[1] - ik * p.y),
+                                 beta * (vx[2] - ik * p.z), beta * (vx[3] - ik * p.w));
     // the updated state into the slot (each thread its own rows), then the
     // producer sends it back
     float* Ss = reinterpret_cast<float*>(stage);
@@ -376,63 +487,68 @@ decode_ring(kda_decode_args a, int64_t n_items) {
       const int row = (int)(item / H), h = (int)(item % H);
       TIn* o = static_cast<TIn*>(a.o);
       const int64_t ob = ((int64_t)row * H + h) * 128 + 4 * lane;
-      st_out(o, ob + 0, scl * (iq * oq.x + qk * u.x));
-      st_out(o, ob + 1, scl * (iq * oq.y + qk * u.y));
-      st_out(o, ob + 2, scl * (iq * oq.z + qk * u.z));
-      st_out(o, ob + 3, scl * (iq * oq.w + qk * u.w));
+      st_out(o, ob + 0, scl * (iq * oq.x + qk * u.x) * gate_at<TIn>(l, row, H, h, ob + 0));
+      st_out(o, ob + 1, scl * (iq * oq.y + qk * u.y) * gate_at<TIn>(l, row, H, h, ob + 1));
+      st_out(o, ob + 2, scl * (iq * oq.z + qk * u.z) * gate_at<TIn>(l, row, H, h, ob + 2));
+      st_out(o, ob + 3, scl * (iq * oq.w + qk * u.w) * gate_at<TIn>(l, row, H, h, ob + 3));
     }
   }
 }
 
-template <typename TIn>
-cudaError_t launch_ring(const kda_decode_args& a, cudaStream_t stream) {
+template <typename TIn, bool kConv>
+cudaError_t launch_ring(const kda_decode_args& a, const kda_layer_args& l, cudaStream_t stream) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool poll = a.wait_limit_ns > 0 && (uint64_t)a.wait_limit_ns < tc::kPollLimitNs;
+  auto kernel = poll ? decode_ring<TIn, true, kConv> : decode_ring<TIn, false, kConv>;
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(poll ? decode_ring<TIn, true> : decode_ring<TIn, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Ring<TIn>::BYTES);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Ring<TIn, kConv>::BYTES);
   if (e != cudaSuccess) return e;
   const int64_t n_items = (int64_t)a.batch * a.num_heads;
   const int64_t grid = n_items < sms ? n_items : sms;
-  if (poll)
-    decode_ring<TIn, true><<<(unsigned)grid, kRingAllThreads, Ring<TIn>::BYTES, stream>>>(a, n_items);
-  else
-    decode_ring<TIn, false><<<(unsigned)grid, kRingAllThreads, Ring<TIn>::BYTES, stream>>>(a, n_items);
+  kernel<<<(unsigned)grid, kRingAllThreads, Ring<TIn, kConv>::BYTES, stream>>>(a, n_items, l);
   return cudaGetLastError();
 }
 
 template <typename TIn, int DK, int DV>
-cudaError_t launch_t(const kda_decode_args& a, cudaStream_t stream) {
+cudaError_t launch_t(const kda_decode_args& a, const kda_layer_args& l, cudaStream_t stream) {
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-  // the bulk copies of the ring need 16-byte aligned sources
+  // the bulk copies of the ring need 16-byte aligned sources; with the
+  // convolution the ring takes bf16 only (fp32 window rows overflow its
+  // shared memory)
+  const bool conv = l.conv_width > 0;
   if (DK == 128 && DV == 128 && al16(a.q) && al16(a.k) && (a.gate_per_head || al16(a.g)) && al16(a.v) &&
-      al16(a.state))
-    return launch_ring<TIn>(a, stream);
+      al16(a.state) && (!conv || (sizeof(TIn) == 2 && al16(l.conv_in[0]) && al16(l.conv_in[1]) &&
+                                  al16(l.conv_in[2]))))
+  {
+    if constexpr (sizeof(TIn) == 2)
+      if (conv) return launch_ring<TIn, true>(a, l, stream);
+    return launch_ring<TIn, false>(a, l, stream);
+  }
   dim3 grid((unsigned)a.batch, (unsigned)a.num_heads);
-  decode_step<TIn, DK, DV><<<grid, DecodeShape<TIn, DK, DV>::NT, 0, stream>>>(a);
+  decode_step<TIn, DK, DV><<<grid, DecodeShape<TIn, DK, DV>::NT, 0, stream>>>(a, l);
   return cudaGetLastError();
 }
 
 template <typename TIn, int DK>
-cudaError_t launch_dv(const kda_decode_args& a, cudaStream_t stream) {
+cudaError_t launch_dv(const kda_decode_args& a, const kda_layer_args& l, cudaStream_t stream) {
   switch (a.dv) {
-    case 16: return launch_t<TIn, DK, 16>(a, stream);
-    case 32: return launch_t<TIn, DK, 32>(a, stream);
-    case 64: return launch_t<TIn, DK, 64>(a, stream);
-    case 128: return launch_t<TIn, DK, 128>(a, stream);
+    case 16: return launch_t<TIn, DK, 16>(a, l, stream);
+    case 32: return launch_t<TIn, DK, 32>(a, l, stream);
+    case 64: return launch_t<TIn, DK, 64>(a, l, stream);
+    case 128: return launch_t<TIn, DK, 128>(a, l, stream);
   }
   return cudaErrorInvalidValue;
 }
 
 template <typename TIn>
-cudaError_t launch_dk(const kda_decode_args& a, cudaStream_t stream) {
+cudaError_t launch_dk(const kda_decode_args& a, const kda_layer_args& l, cudaStream_t stream) {
   switch (a.dk) {
-    case 16: return launch_dv<TIn, 16>(a, stream);
-    case 32: return launch_dv<TIn, 32>(a, stream);
-    case 64: return launch_dv<TIn, 64>(a, stream);
-    case 128: return launch_dv<TIn, 128>(a, stream);
+    case 16: return launch_dv<TIn, 16>(a, l, stream);
+    case 32: return launch_dv<TIn, 32>(a, l, stream);
+    case 64: return launch_dv<TIn, 64>(a, l, stream);
+    case 128: return launch_dv<TIn, 128>(a, l, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -441,7 +557,11 @@ cudaError_t launch_dk(const kda_decode_args& a, cudaStream_t stream) {
 
 cudaError_t launch_decode(const kda_decode_args& a, cudaStream_t stream) {
   if (a.batch == 0) return cudaSuccess;
-  return a.in_dtype == KDA_BF16 ? launch_dk<__nv_bfloat16>(a, stream) : launch_dk<float>(a, stream);
+  kda_layer_args l{};  // by value: the kernels cannot read the caller's host struct
+  if (a.layer) l = *a.layer;
+  if (l.conv_width == 0)
+    for (int t = 0; t < 3; ++t) l.conv_in[t] = l.conv_out[t] = nullptr;
+  return a.in_dtype == KDA_BF16 ? launch_dk<__nv_bfloat16>(a, l, stream) : launch_dk<float>(a, l, stream);
 }
 
 }  // namespace kda

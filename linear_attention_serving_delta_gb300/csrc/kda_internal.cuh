@@ -60,8 +60,25 @@ struct ChunkParams {
   float* trans;     // [num_seqs][H][dk][dk] in kScanPass1
   uint64_t wait_ns; // limit of the bounded waits on copies and MMAs (not of the drains)
   int32_t gate_per_head;  // g is [T, H] (one decay per token and head), else [T, H, dk]
+  // the layer steps (kda_layer_args): short convolution of q, k, v (width 0 =
+  // off) and output gate (null = off)
+  int32_t conv_width, conv_silu;
+  const float* conv_w[3];   // taps of q, k, v: [conv_width][H][d]
+  const void* conv_in[3];   // windows [N][conv_width - 1][H][d], or null (zeros)
+  // the chunk table's sequences are segments of the one sequence of the call
+  // (segment scan): a chunk's position in it is its first token's index
+  int32_t conv_one_seq;
+  const void* out_gate;     // [T][H][dv], or [T][H] with out_gate_per_head
+  int32_t out_gate_per_head;
 };
 constexpr int32_t kScanPass1 = 1;
+
+// The window of each sequence after the call (kda_layer_args::conv_out):
+// the raw inputs of the last conv_width - 1 positions of window ++ sequence.
+// Runs after every kernel that reads conv_in (the two may be one buffer).
+cudaError_t launch_conv_windows(const kda_layer_args& l, int32_t num_seqs, int32_t H, int32_t dk,
+                                int32_t dv, const int64_t* cu_seqlens, int64_t total_tokens,
+                                kda_dtype_t dt, const void* const x[3], cudaStream_t stream);
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 

@@ -177,7 +177,7 @@ __device__ void fill_segment(const PlanParams& p, int64_t gidx, int32_t& bad) {
       c.len = (int32_t)(end - start);
       c.snap_slot = slot;
       c.flags = (start == 0 ? kChunkFirst : 0) | (end == len ? kChunkLast : 0);
-      c.pad = 0;
+      c.pos = start;
       p.chunks[ci] = c;
     }
     ++ci;

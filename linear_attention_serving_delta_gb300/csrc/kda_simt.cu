@@ -29,6 +29,33 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Tensor t (0 q, 1 k, 2 v; head size d) at token i of chunk ch, channel col,
+// after the short convolution when there is one:
+//   y = sum_{j < W} w[j][h][col] x_{i-j}   (x before the sequence start from
+//   its window, or 0), SiLU if asked, rounded to the input dtype.
+template <typename TIn>
+__device__ float conv_input(const ChunkParams& p, int t, const TIn* x, int d, const Chunk& ch, int i, int h,
+                            int col) {
+  const int H = p.H, W = p.conv_width;
+  const int64_t e = ((ch.tok0 + i) * H + h) * (int64_t)d + col;
+  if (W == 0) return ld_in(x, e);
+  const int64_t pos = (p.conv_one_seq ? ch.tok0 : ch.pos) + i;  // index in the sequence
+  const int seq = p.conv_one_seq ? 0 : ch.seq;
+  const TIn* win = static_cast<const TIn*>(p.conv_in[t]);
+  const float* w = p.conv_w[t];
+  float acc = 0.f;
+  for (int j = 0; j < W; ++j) {
+    float xv = 0.f;
+    if (pos - j >= 0)
+      xv = ld_in(x, e - (int64_t)j * H * d);
+    else if (win)  // window row W - 1 + (pos - j): the input (j - pos) tokens before the start
+      xv = ld_in(win, (((int64_t)seq * (W - 1) + (W - 1) + (pos - j)) * H + h) * d + col);
+    acc += w[((int64_t)j * H + h) * d + col] * xv;
+  }
+  if (p.conv_silu) acc = silu_of(acc);
+  return round_in<TIn>(acc);
+}
+
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads)
 simt_intra(ChunkParams p) {
@@ -59,8 +86,8 @@ simt_intra(ChunkParams p) {
     float xq = 0.f, xk = 0.f, la = 0.f;
     if (i < len) {
       const int64_t e = ((ch.tok0 + i) * H + h) * dk + col;
-      xq = ld_in(q, e);
-      xk = ld_in(k, e);
+      xq = conv_input(p, 0, q, dk, ch, i, h, col);
+      xk = conv_input(p, 1, k, dk, ch, i, h, col);
       la = log_alpha_of(ld_in(g, p.gate_per_head ? (ch.tok0 + i) * H + h : e));
     }
     qh[idx] = xq;
@@ -69,7 +96,7 @@ simt_intra(ChunkParams p) {
   }
   for (int idx = tid; idx < kChunk * dv; idx += kThreads) {
     const int i = idx / dv, col = idx - i * dv;
-    V[idx] = i < len ? ld_in(v, ((ch.tok0 + i) * H + h) * dv + col) : 0.f;
+    V[idx] = i < len ? conv_input(p, 2, v, dv, ch, i, h, col) : 0.f;
   }
   if (tid < kChunk) beta[tid] = tid < len ? beta_of(ld_in(b, (ch.tok0 + tid) * H + h)) : 0.f;
   __syncthreads();
@@ -177,6 +204,7 @@ simt_inter(ChunkParams p, int ns) {
   }
   __syncthreads();
   TIn* o = static_cast<TIn*>(p.o);
+  const TIn* og = static_cast<const TIn*>(p.out_gate);
   for (int64_t c = c_begin; c < c_end; ++c) {
     const Chunk ch = p.chunks[c];
     const float* rec = p.inter + ((size_t)c * H + h) * p.rec_floats;
@@ -203,7 +231,10 @@ simt_inter(ChunkParams p, int ns) {
       if (i < ch.len) {
         float acc = QS[idx];
         for (int j = 0; j <= i; ++j) acc += AQK[i * kChunk + j] * U[j * ns + n];
-        st_out(o, ((ch.tok0 + i) * H + h) * dv + n0 + n, p.scale * acc);
+        const int64_t oi = ((ch.tok0 + i) * H + h) * dv + n0 + n;
+        float val = p.scale * acc;
+        if (og) val *= out_gate_of(ld_in(og, p.out_gate_per_head ? (ch.tok0 + i) * H + h : oi));
+        st_out(o, oi, val);
       }
     }
     for (int idx = tid; idx < dk * ns; idx += kThreads) {

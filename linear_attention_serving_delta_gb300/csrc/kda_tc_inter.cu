@@ -115,7 +115,8 @@ __device__ __forceinline__ void split8(const float* u, uint4& hi, uint4& lo) {
 }
 
 // o rows of one chunk from lanes 64-127 of an output accumulator: row i, this
-// thread's 16 columns (none in the first pass of the segment scan)
+// thread's 16 columns (none in the first pass of the segment scan), times
+// the output gate's sigmoid(r) when there is one
 __device__ __forceinline__ void store_output(const ChunkParams& p, const Chunk& ch, uint32_t d1,
                                              int h16, int i, int h, int n0) {
   float d[kNh];
@@ -123,7 +124,24 @@ __device__ __forceinline__ void store_output(const ChunkParams& p, const Chunk& 
   if (i < ch.len && p.k3_mode != kScanPass1) {
     const float scale = p.scale;
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o);
-    uint4* dst = reinterpret_cast<uint4*>(o + ((ch.tok0 + i) * p.H + h) * (int64_t)kD + n0 + h16);
+    const int64_t row = (ch.tok0 + i) * p.H + h;
+    uint4* dst = reinterpret_cast<uint4*>(o + row * (int64_t)kD + n0 + h16);
+    if (p.out_gate) {
+      const __nv_bfloat16* r = static_cast<const __nv_bfloat16*>(p.out_gate);
+      if (p.out_gate_per_head) {
+        const float f = out_gate_of(__bfloat162float(r[row]));
+#pragma unroll
+        for (int n = 0; n < kNh; ++n) d[n] *= f;
+      } else {
+        const uint4* rg = reinterpret_cast<const uint4*>(r + row * (int64_t)kD + n0 + h16);
+#pragma unroll
+        for (int q8 = 0; q8 < kNh / 8; ++q8) {
+          const uint4 x = rg[q8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) d[8 * q8 + j] *= out_gate_of(bf16_at(x, j));
+        }
+      }
+    }
 #pragma unroll
     for (int q8 = 0; q8 < kNh / 8; ++q8)
       dst[q8] = make_uint4(pack_bf16(scale * d[8 * q8], scale * d[8 * q8 + 1]),

@@ -209,10 +209,28 @@ static_assert(kGStage % 128 == 0 && kKStage % 128 == 0 && kQStage % 128 == 0 && 
               "tensor-map copies land on 128-byte boundaries");
 constexpr uint32_t kRowsBytes = 64 * 256;  // one tensor's rows of an item
 
-// Tensor maps of q, k, v, g viewed as [T][H][128] bf16, box {128, 1, 64}
+// Tensor maps of q, k, v, g viewed as [T][H][128] bf16, box {128, 1, 64};
+// with the short convolution also q, k, v with box {128, 1, 3}: the halo
+// rows, the three tokens before an item's first (a negative start reads
+// zeros)
 struct RowMaps {
   CUtensorMap g, q, k, v;
+  CUtensorMap qh, kh, vh;
 };
+
+// The halo rows of the short convolution ("Kimi K3: The Manos, The Mythos,
+// The Legendos", bullet on the stability details), KDA_CONV_MAX - 1 rows of
+// 256 bytes per tensor, staged with their tensor's group in tiles that are
+// free from the staging to the raw reads: k's after its rows in the A_kk
+// tile (group A), q's and v's in A2 (group B, issued once MMA 2 has read A2;
+// A2 is next written after MMA 1 of the item).
+constexpr int kHaloRows = KDA_CONV_MAX - 1;
+constexpr uint32_t kHaloBytes = kHaloRows * 256;
+constexpr uint32_t kKHalo = kKStage + kRowsBytes, kQHalo = Smem::A2, kVHalo = Smem::A2 + kHaloBytes;
+static_assert(kKHalo + kHaloBytes <= Smem::AKK + 64 * kAs * 4 && 2 * kHaloBytes <= 8 * kA2Lbo,
+              "the halo rows fit the tiles they borrow");
+static_assert(kKHalo % 128 == 0 && kQHalo % 128 == 0 && kVHalo % 128 == 0,
+              "halo copies land on 128-byte boundaries");
 
 // rows of one tensor, tokens tok0..tok0+63 of head h, into shared memory
 __device__ __forceinline__ void tma_rows(uint8_t* dst, const CUtensorMap* m, int h, int tok0,
@@ -231,36 +249,118 @@ __device__ __forceinline__ void tma_rows_l2(const CUtensorMap* m, int h, int tok
 }
 
 // What an item needs of its chunk-table entry: first token and length (the
-// token index fits the int32 coordinates of the tensor maps on this path).
-// Two registers instead of the entry's eight.
+// token index fits the int32 coordinates of the tensor maps on this path);
+// with the short convolution also how many of the halo rows lie inside the
+// sequence (pre, at most kHaloRows) and the sequence (for its window).
+// A few registers instead of the entry's eight.
 struct ItemChunk {
-  int tok0, len;
+  int tok0, len, pre, seq;
 };
-__device__ __forceinline__ ItemChunk item_chunk(const Chunk* chunks, int64_t idx) {
-  return ItemChunk{(int)chunks[idx].tok0, chunks[idx].len};
+template <bool kConv>
+__device__ __forceinline__ ItemChunk item_chunk(const ChunkParams& p, int64_t idx) {
+  const Chunk* c = p.chunks + idx;
+  ItemChunk r{(int)c->tok0, c->len, 0, 0};
+  if (kConv) {
+    // segment scan: the table's sequences are segments of sequence 0, which
+    // starts at token 0
+    const int64_t pos = p.conv_one_seq ? c->tok0 : c->pos;
+    r.pre = pos < kHaloRows ? (int)pos : kHaloRows;
+    r.seq = p.conv_one_seq ? 0 : c->seq;
+  }
+  return r;
 }
 
-// One staging group: the rows of two tensors of item (ch, h), both counted
-// on `bar`.  Issued by one thread.
-__device__ __forceinline__ void stage_group(uint8_t* sm, uint64_t* bar, const ItemChunk& ch, int h,
-                                            const CUtensorMap* t0, uint32_t s0, const CUtensorMap* t1,
-                                            uint32_t s1) {
-  mbar_arrive_expect_tx(bar, 2 * kRowsBytes);
-  tma_rows(sm + s0, t0, h, ch.tok0, bar);
-  tma_rows(sm + s1, t1, h, ch.tok0, bar);
+// Staging group A of item (ch, h): the rows of g (not with a gate per head)
+// and k, and k's halo rows with the convolution, counted on `bar`.  Issued
+// by one thread.
+template <bool kHeadGate, bool kConv>
+__device__ __forceinline__ void stage_a(uint8_t* sm, uint64_t* bar, const ItemChunk& ch, int h,
+                                        const RowMaps& maps) {
+  mbar_arrive_expect_tx(bar, (kHeadGate ? 1 : 2) * kRowsBytes + (kConv ? kHaloBytes : 0));
+  if (!kHeadGate) tma_rows(sm + kGStage, &maps.g, h, ch.tok0, bar);
+  tma_rows(sm + kKStage, &maps.k, h, ch.tok0, bar);
+  if (kConv) tma_rows(sm + kKHalo, &maps.kh, h, ch.tok0 - kHaloRows, bar);
 }
 
-// The rows of one tensor of item (ch, h) on `bar` (group A with a gate per
-// head: k alone).  Issued by one thread.
-__device__ __forceinline__ void stage_one(uint8_t* sm, uint64_t* bar, const ItemChunk& ch, int h,
-                                          const CUtensorMap* t0, uint32_t s0) {
-  mbar_arrive_expect_tx(bar, kRowsBytes);
-  tma_rows(sm + s0, t0, h, ch.tok0, bar);
+// Staging group B of item (ch, h): the rows of q and v (and their halo rows).
+template <bool kConv>
+__device__ __forceinline__ void stage_b(uint8_t* sm, uint64_t* bar, const ItemChunk& ch, int h,
+                                        const RowMaps& maps) {
+  mbar_arrive_expect_tx(bar, 2 * kRowsBytes + (kConv ? 2 * kHaloBytes : 0));
+  tma_rows(sm + kQStage, &maps.q, h, ch.tok0, bar);
+  tma_rows(sm + kVStage, &maps.v, h, ch.tok0, bar);
+  if (kConv) {
+    tma_rows(sm + kQHalo, &maps.qh, h, ch.tok0 - kHaloRows, bar);
+    tma_rows(sm + kVHalo, &maps.vh, h, ch.tok0 - kHaloRows, bar);
+  }
 }
 
 // 16 bytes of a raw row in a staging: token i, channels c0..c0+7
 __device__ __forceinline__ uint4 raw16(const uint8_t* sm, uint32_t stage, int i, int c0) {
   return *reinterpret_cast<const uint4*>(sm + stage + i * 256 + c0 * 2);
+}
+
+// 16 bytes of input row -back (back = 1..kHaloRows tokens before the item's
+// first) of one tensor: the staged halo row while inside the sequence, else
+// the sequence's window row (W - 1) - (tokens before the sequence start), or
+// zeros without a window; zeros past the convolution's reach
+__device__ __forceinline__ uint4 halo16(const uint8_t* sm, uint32_t halo, const void* win,
+                                        const ChunkParams& p, const ItemChunk& ch, int h, int back, int c0) {
+  const int W = p.conv_width;
+  if (back > W - 1) return make_uint4(0, 0, 0, 0);
+  if (back <= ch.pre) return raw16(sm, halo, kHaloRows - back, c0);
+  if (!win) return make_uint4(0, 0, 0, 0);
+  const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(win);
+  const int64_t row = (int64_t)ch.seq * (W - 1) + (W - 1) - (back - ch.pre);
+  return *reinterpret_cast<const uint4*>(wb + (row * p.H + h) * kD + c0);
+}
+
+// Rows i0..i0+3 (channels c0..c0+7) of tensor t (0 q, 1 k, 2 v) after the
+// short convolution, as bf16: y_i = sum_{j < W} w[j][h][c] x_{i-j} (taps at
+// or past W count as 0), SiLU if asked, rounded to bf16 (the input dtype);
+// rows at or past len give zeros, as the raw rows do.  The inputs come from
+// the item's staging and, for the first token block, the halo.
+__device__ __forceinline__ void conv_rows(const uint8_t* sm, uint32_t stage, uint32_t halo, int t,
+                                          const ChunkParams& p, const ItemChunk& ch, int h, int i0, int c0,
+                                          uint4 out[4]) {
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  uint4 x[7];  // input rows i0 - 3 .. i0 + 3
+#pragma unroll
+  for (int m = 0; m < 7; ++m) {
+    const int i = i0 - kHaloRows + m;
+    x[m] = i >= 0 ? (i < ch.len ? raw16(sm, stage, i, c0) : z) : halo16(sm, halo, p.conv_in[t], p, ch, h, -i, c0);
+  }
+  const int W = p.conv_width;
+  const float* w = p.conv_w[t] + (size_t)h * kD + c0;
+  const size_t tap = (size_t)p.H * kD;
+  uint32_t o[4][4];
+#pragma unroll
+  for (int pp = 0; pp < 4; ++pp) {  // channel pair c0 + 2 pp, c0 + 2 pp + 1
+    float w0[4], w1[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 wv = j < W ? __ldg(reinterpret_cast<const float2*>(w + j * tap + 2 * pp))
+                              : make_float2(0.f, 0.f);
+      w0[j] = wv.x;
+      w1[j] = wv.y;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        a0 += w0[j] * bf16_at(x[r + kHaloRows - j], 2 * pp);
+        a1 += w1[j] * bf16_at(x[r + kHaloRows - j], 2 * pp + 1);
+      }
+      if (p.conv_silu) {
+        a0 = silu_of(a0);
+        a1 = silu_of(a1);
+      }
+      o[r][pp] = i0 + r < ch.len ? pack_bf16(a0, a1) : 0u;
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) out[r] = make_uint4(o[r][0], o[r][1], o[r][2], o[r][3]);
 }
 
 __device__ __forceinline__ float load_b(const ChunkParams& p, const ItemChunk& ch, int h, int tid) {
@@ -281,7 +381,8 @@ __device__ __forceinline__ float load_gh(const ChunkParams& p, const ItemChunk& 
 // kPoll: the instantiation for wait limits under kPollLimitNs (the give-up
 // test).  kHeadGate: g is [T, H], one decay per token and head (the gated
 // delta rule): no g rows are staged, the scan runs over tokens only.
-template <bool kPoll, bool kHeadGate>
+// kConv: q, k, v pass through the short convolution as they are read.
+template <bool kPoll, bool kHeadGate, bool kConv>
 __global__ void __launch_bounds__(kThreads, 2)
 tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -330,14 +431,14 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
   // the pipeline: chunk entries of the current and the next item; the first
   // item's rows are staged here (groups A and B), each later item's during
   // the item before it
-  ItemChunk ch = item_chunk(p.chunks, item / H);  // entries past the table's end have len 0
-  ItemChunk ch_next = item + stride < n_items ? item_chunk(p.chunks, (item + stride) / H) : ItemChunk{0, 0};
+  ItemChunk ch = item_chunk<kConv>(p, item / H);  // entries past the table's end have len 0
+  ItemChunk ch_next =
+      item + stride < n_items ? item_chunk<kConv>(p, (item + stride) / H) : ItemChunk{0, 0, 0, 0};
   {
     const int h0 = (int)(item % H);
     if (tid == 0) {
-      if (kHeadGate) stage_one(sm, &bar_ga, ch, h0, &maps.k, kKStage);
-      else stage_group(sm, &bar_ga, ch, h0, &maps.g, kGStage, &maps.k, kKStage);
-      stage_group(sm, &bar_gb, ch, h0, &maps.q, kQStage, &maps.v, kVStage);
+      stage_a<kHeadGate, kConv>(sm, &bar_ga, ch, h0, maps);
+      stage_b<kConv>(sm, &bar_gb, ch, h0, maps);
     }
     if (kHeadGate && tid < 64) gtok[tid] = load_gh(p, ch, h0, tid);
   }
@@ -434,13 +535,19 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     b_fly = false;
     sph ^= 1;
     uint4 qraw[4], kraw[4], vraw[4];
+    if constexpr (kConv) {
+      conv_rows(sm, kKStage, kKHalo, 1, p, ch, h, i0, c0, kraw);
+      conv_rows(sm, kQStage, kQHalo, 0, p, ch, h, i0, c0, qraw);
+      conv_rows(sm, kVStage, kVHalo, 2, p, ch, h, i0, c0, vraw);
+    } else {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const bool live = i0 + r < len;
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      qraw[r] = live ? raw16(sm, kQStage, i0 + r, c0) : z;
-      kraw[r] = live ? raw16(sm, kKStage, i0 + r, c0) : z;
-      vraw[r] = live ? raw16(sm, kVStage, i0 + r, c0) : z;
+      for (int r = 0; r < 4; ++r) {
+        const bool live = i0 + r < len;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        qraw[r] = live ? raw16(sm, kQStage, i0 + r, c0) : z;
+        kraw[r] = live ? raw16(sm, kKStage, i0 + r, c0) : z;
+        vraw[r] = live ? raw16(sm, kVStage, i0 + r, c0) : z;
+      }
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -634,10 +741,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     // T is consumed (B1) and the A_kk tile free: the next item's g and k
     // (group A) are staged now
     if (has_next) {
-      if (tid == 0) {
-        if (kHeadGate) stage_one(sm, &bar_ga, chn, hn, &maps.k, kKStage);
-        else stage_group(sm, &bar_ga, chn, hn, &maps.g, kGStage, &maps.k, kKStage);
-      }
+      if (tid == 0) stage_a<kHeadGate, kConv>(sm, &bar_ga, chn, hn, maps);
       bnext = load_b(p, chn, hn, tid);
       if (kHeadGate) gnext = load_gh(p, chn, hn, tid);
       a_fly = true;
@@ -656,7 +760,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     if (!ok) break;
     // MMA 2 has read B2: the next item's q and v (group B) are staged there now
     if (has_next) {
-      if (tid == 0) stage_group(sm, &bar_gb, chn, hn, &maps.q, kQStage, &maps.v, kVStage);
+      if (tid == 0) stage_b<kConv>(sm, &bar_gb, chn, hn, maps);
       b_fly = true;
     }
     {
@@ -704,7 +808,8 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
       bulk_commit();
     }
     ch = ch_next;
-    ch_next = item + 2 * stride < n_items ? item_chunk(p.chunks, (item + 2 * stride) / H) : ItemChunk{0, 0};
+    ch_next = item + 2 * stride < n_items ? item_chunk<kConv>(p, (item + 2 * stride) / H)
+                                          : ItemChunk{0, 0, 0, 0};
   }
   // no staging copy and no MMA is left in flight when the CTA exits (these
   // waits keep the long limit whatever the caller chose for the others)
@@ -739,13 +844,14 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// [T][H][128] bf16 rows, box {128 channels, 1 head, 64 tokens}, zero fill past T
-bool encode_rows(CUtensorMap* m, const void* base, int H, int64_t T) {
+// [T][H][128] bf16 rows, box {128 channels, 1 head, `rows` tokens}, zero fill
+// outside [0, T)
+bool encode_rows(CUtensorMap* m, const void* base, int H, int64_t T, uint32_t rows = 64) {
   const EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
   const cuuint64_t dims[3] = {kD, (cuuint64_t)H, (cuuint64_t)T};
   const cuuint64_t strides[2] = {kD * 2, (cuuint64_t)H * kD * 2};
-  const cuuint32_t box[3] = {kD, 1, 64};
+  const cuuint32_t box[3] = {kD, 1, rows};
   const cuuint32_t elem[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -755,9 +861,13 @@ bool encode_rows(CUtensorMap* m, const void* base, int H, int64_t T) {
 }  // namespace
 
 cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream) {
-  const bool poll = p.wait_ns < kPollLimitNs, head = p.gate_per_head != 0;
-  auto kernel = poll ? (head ? tc_intra<true, true> : tc_intra<true, false>)
-                     : (head ? tc_intra<false, true> : tc_intra<false, false>);
+  const bool head = p.gate_per_head != 0, conv = p.conv_width > 0;
+  // (the convolution has no polling instance: its waits keep the suspending
+  // form, which honours the limit too, only less promptly)
+  const bool poll = p.wait_ns < kPollLimitNs && !conv;
+  auto kernel = conv ? (head ? tc_intra<false, true, true> : tc_intra<false, false, true>)
+                : poll ? (head ? tc_intra<true, true, false> : tc_intra<true, false, false>)
+                       : (head ? tc_intra<false, true, false> : tc_intra<false, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem::BYTES);
   if (e != cudaSuccess || p.max_chunks == 0 || p.total_tokens == 0) return e;
   RowMaps maps;
@@ -765,6 +875,10 @@ cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream) {
   if (!encode_rows(&maps.g, head ? p.k : p.g, p.H, p.total_tokens) ||
       !encode_rows(&maps.q, p.q, p.H, p.total_tokens) || !encode_rows(&maps.k, p.k, p.H, p.total_tokens) ||
       !encode_rows(&maps.v, p.v, p.H, p.total_tokens))
+    return cudaErrorInvalidValue;
+  if (conv && (!encode_rows(&maps.qh, p.q, p.H, p.total_tokens, kHaloRows) ||
+               !encode_rows(&maps.kh, p.k, p.H, p.total_tokens, kHaloRows) ||
+               !encode_rows(&maps.vh, p.v, p.H, p.total_tokens, kHaloRows)))
     return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);

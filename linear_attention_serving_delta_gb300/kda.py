@@ -47,6 +47,14 @@ class KdaError(RuntimeError):
 
 
 c_i32, c_i64, c_f32, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+CONV_MAX = 4  # KDA_CONV_MAX: taps of the short convolution
+
+
+class LayerArgs(ctypes.Structure):
+    """kda_layer_args: the short convolution on q, k, v and the output gate."""
+    _fields_ = [("conv_width", c_i32), ("conv_silu", c_i32), ("conv_w", c_vp * 3),
+                ("conv_in", c_vp * 3), ("conv_out", c_vp * 3), ("out_gate", c_vp),
+                ("out_gate_per_head", c_i32)]
 
 
 class PrefillArgs(ctypes.Structure):
@@ -58,7 +66,8 @@ class PrefillArgs(ctypes.Structure):
                 ("num_boundaries", c_i64), ("cu_snapshots", c_vp), ("snapshots", c_vp),
                 ("num_snapshots", c_i64), ("phase_events", c_vp), ("scan_segments", c_i32),
                 ("snapshot_slot_map", c_vp), ("snapshot_map_len", c_i64),
-                ("wait_limit_ns", c_i64), ("gate_per_head", c_i32)]
+                ("wait_limit_ns", c_i64), ("gate_per_head", c_i32),
+                ("layer", ctypes.POINTER(LayerArgs))]
 
 
 class PrefillHostArgs(ctypes.Structure):
@@ -75,7 +84,7 @@ class DecodeArgs(ctypes.Structure):
                 ("num_slots", c_i32), ("in_dtype", ctypes.c_int), ("scale", c_f32),
                 ("q", c_vp), ("k", c_vp), ("v", c_vp), ("g", c_vp), ("b", c_vp),
                 ("state", c_vp), ("state_slots", c_vp), ("o", c_vp), ("wait_limit_ns", c_i64),
-                ("status", c_vp), ("gate_per_head", c_i32)]
+                ("status", c_vp), ("gate_per_head", c_i32), ("layer", ctypes.POINTER(LayerArgs))]
 
 
 class PrepArgs(ctypes.Structure):
@@ -177,10 +186,47 @@ def _check(status: int, what: str):
         raise KdaError(status, what)
 
 
+def make_layer_args(*, rows, H, dk, dv, dtype, conv_weights=None, conv_silu=False,
+                    conv_window=None, conv_window_out=None, out_gate=None,
+                    gate_rows=None) -> LayerArgs | None:
+    """kda_layer_args from tensors (None when neither step is asked for).
+
+    conv_weights: (wq, wk, wv) float32 [W, H, d]; conv_window / conv_window_out:
+    (q, k, v) windows [rows, W-1, H, d] in the input dtype (an entry may be
+    None); out_gate: [gate_rows, H, dv] or [gate_rows, H] (one gate per head)."""
+    if conv_weights is None and out_gate is None:
+        return None
+    la = LayerArgs()
+    if conv_weights is not None:
+        W = conv_weights[0].shape[0]
+        if not 1 <= W <= CONV_MAX:
+            raise ValueError(f"conv width {W} outside 1..{CONV_MAX}")
+        la.conv_width, la.conv_silu = W, 1 if conv_silu else 0
+        for t, (w, d) in enumerate(zip(conv_weights, (dk, dk, dv))):
+            if tuple(w.shape) != (W, H, d):
+                raise ValueError(f"conv weights {t} have shape {tuple(w.shape)}, expected {(W, H, d)}")
+            la.conv_w[t] = _ptr(w, torch.float32, "conv_weights")
+            for arr, src in ((la.conv_in, conv_window), (la.conv_out, conv_window_out)):
+                x = None if src is None else src[t]
+                if x is not None and tuple(x.shape) != (rows, W - 1, H, d):
+                    raise ValueError(f"conv window {t} has shape {tuple(x.shape)}, "
+                                     f"expected {(rows, W - 1, H, d)}")
+                arr[t] = _ptr(x, dtype, "conv window")
+    if out_gate is not None:
+        per_head = out_gate.dim() == 2
+        want = (gate_rows, H) if per_head else (gate_rows, H, dv)
+        if tuple(out_gate.shape) != want:
+            raise ValueError(f"out_gate has shape {tuple(out_gate.shape)}, expected {want}")
+        la.out_gate = _ptr(out_gate, dtype, "out_gate")
+        la.out_gate_per_head = 1 if per_head else 0
+    return la
+
+
 def make_prefill_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=None,
                       final_state=None, snapshot_interval=0, boundary_pos=None,
                       cu_boundaries=None, cu_snapshots=None, snapshots=None,
-                      scan_segments=0, snapshot_slot_map=None, wait_limit_ns=0) -> PrefillArgs:
+                      scan_segments=0, snapshot_slot_map=None, wait_limit_ns=0,
+                      layer: LayerArgs | None = None) -> PrefillArgs:
     T, H, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
@@ -211,6 +257,8 @@ def make_prefill_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=
     a.snapshot_map_len = 0 if snapshot_slot_map is None else snapshot_slot_map.numel()
     a.wait_limit_ns = int(wait_limit_ns)
     a.gate_per_head = 1 if g.dim() == 2 else 0
+    if layer is not None:
+        a.layer = ctypes.pointer(layer)  # the pointer object keeps `layer` alive
     return a
 
 
@@ -313,7 +361,12 @@ def kda_snapshot_plan(cu_seqlens, interval: int, boundary_pos=None, cu_boundarie
 
 
 def kda_decode_step(q, k, v, g, b, state, o, state_slots=None, scale=1.0, stream=None,
-                    wait_limit_ns=0, status=None) -> None:
+                    wait_limit_ns=0, status=None, conv_weights=None, conv_silu=False,
+                    conv_window=None, out_gate=None) -> None:
+    """One decode step.  With conv_weights (wq, wk, wv) [W, H, d] the short
+    convolution runs on q, k, v; conv_window (q, k, v) [slots, W-1, H, d] holds
+    each slot's window and is advanced in place.  out_gate [B, H, dv] or
+    [B, H] gates o."""
     B, H, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
@@ -331,6 +384,12 @@ def kda_decode_step(q, k, v, g, b, state, o, state_slots=None, scale=1.0, stream
     a.wait_limit_ns = int(wait_limit_ns)
     a.status = _ptr(status, torch.int32, "status")
     a.gate_per_head = 1 if g.dim() == 2 else 0  # g [B, H]: one decay per row and head
+    layer = make_layer_args(rows=a.num_slots, H=H, dk=dk, dv=dv, dtype=dt,
+                            conv_weights=conv_weights, conv_silu=conv_silu,
+                            conv_window=conv_window, conv_window_out=conv_window,
+                            out_gate=out_gate, gate_rows=B)
+    if layer is not None:
+        a.layer = ctypes.pointer(layer)
     _check(lib().kda_decode_step(ctypes.byref(a), _stream(stream)), "kda_decode_step")
 
 
@@ -360,7 +419,14 @@ class Prefill:
                  snapshot_interval=0, boundary_pos=None, cu_boundaries=None,
                  want_final=True, host_cu_seqlens=None, host_boundary_pos=None,
                  host_cu_boundaries=None, o=None, scan_segments=0, snapshot_pool=None,
-                 snapshot_slot_map=None, wait_limit_ns=0):
+                 snapshot_slot_map=None, wait_limit_ns=0, conv_weights=None, conv_silu=False,
+                 conv_window=None, conv_window_out=None, out_gate=None):
+        """The layer steps: conv_weights (wq, wk, wv) float32 [W, H, d] turn on
+        the short convolution, with each sequence's window before the call in
+        conv_window ((q, k, v) [N, W-1, H, d], None = zeros); conv_window_out
+        receives the windows after it (True allocates them as
+        ``self.conv_window_out``; it may be conv_window itself).  out_gate
+        [T, H, dv] or [T, H] gates o."""
         dev = q.device
         T, H, dk = q.shape
         dv = v.shape[-1]
@@ -385,6 +451,18 @@ class Prefill:
             else:
                 self.snapshots = torch.empty(max(n_snap, 1), H, dk, dv, dtype=torch.float32,
                                              device=dev)
+        self.conv_window_out = None
+        if conv_weights is not None and conv_window_out is not None:
+            W = conv_weights[0].shape[0]
+            if conv_window_out is True:
+                conv_window_out = tuple(torch.empty(N, W - 1, H, d, dtype=q.dtype, device=dev)
+                                        for d in (dk, dk, dv))
+            self.conv_window_out = conv_window_out
+        self.layer = make_layer_args(rows=N, H=H, dk=dk, dv=dv, dtype=q.dtype,
+                                     conv_weights=conv_weights, conv_silu=conv_silu,
+                                     conv_window=conv_window,
+                                     conv_window_out=self.conv_window_out, out_gate=out_gate,
+                                     gate_rows=T)
         self.args = make_prefill_args(
             q, k, v, g, b, cu_seqlens, self.o, scale=scale, initial_state=initial_state,
             final_state=self.final_state, snapshot_interval=snapshot_interval,
@@ -392,13 +470,13 @@ class Prefill:
             cu_snapshots=self.cu_snapshots, snapshots=self.snapshots,
             scan_segments=scan_segments,
             snapshot_slot_map=snapshot_slot_map if self.snapshots is not None else None,
-            wait_limit_ns=wait_limit_ns)
+            wait_limit_ns=wait_limit_ns, layer=self.layer)
         nbytes = kda_prefill_workspace_size(self.args)
         if nbytes == 0:
             raise ValueError("kda_prefill_workspace_size rejected the arguments")
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self._keep = (q, k, v, g, b, cu_seqlens, initial_state, boundary_pos, cu_boundaries,
-                      snapshot_slot_map)
+                      snapshot_slot_map, conv_weights, conv_window, out_gate)
 
     def run(self, stream=None):
         kda_prefill(self.args, self.workspace, stream)
@@ -581,10 +659,13 @@ def prefill_cached(cache: PrefixCache, pool, tokens, q, k, v, g, b, *, interval=
     return p, pr.o, pr.final_state
 
 
-def decode_step(q, k, v, g, b, state, state_slots=None, scale=1.0, o=None, stream=None):
+def decode_step(q, k, v, g, b, state, state_slots=None, scale=1.0, o=None, stream=None, **layer):
+    """Allocates o and runs kda_decode_step; ``layer`` takes conv_weights,
+    conv_silu, conv_window and out_gate (see kda_decode_step)."""
     if o is None:
         o = torch.empty(q.shape[0], q.shape[1], v.shape[-1], dtype=q.dtype, device=q.device)
-    kda_decode_step(q, k, v, g, b, state, o, state_slots=state_slots, scale=scale, stream=stream)
+    kda_decode_step(q, k, v, g, b, state, o, state_slots=state_slots, scale=scale, stream=stream,
+                    **layer)
     return o
 
 

@@ -175,3 +175,21 @@ def decode_inputs(w: DecodeWorkload, steps: int | None = None, device: str = "cp
     b = torch.randn(steps, w.batch, w.H, **kw).to(dt)
     out = dict(q=q, k=k, v=v, g=g, b=b, state=state)
     return {key: t.to(device) for key, t in out.items()}
+
+
+def layer_inputs(seed: int, rows: int, T: int, H: int, dk: int, dv: int, width: int,
+                 dtype: str = "bf16", device: str = "cpu", gate_per_head: bool = False) -> dict:
+    """Inputs of the layer steps around the recurrence, from their own
+    generator (seed): the short convolution's taps (float32 [W, H, d] for q,
+    k, v, ~ N(0, 1/W) so that a convolved input keeps about unit variance),
+    the windows before the call (the workload dtype, [rows, W-1, H, d],
+    ~ N(0, 1) like the inputs they stand for) and the output gate's logits
+    r ~ N(0, 1) ([T, H, dv], or [T, H] with one gate per head)."""
+    gg = _gen(seed, device)
+    kw = dict(generator=gg, device=device, dtype=torch.float32)
+    dt = torch_dtype(dtype)
+    dims = (dk, dk, dv)
+    taps = tuple(torch.randn(width, H, d, **kw) / width ** 0.5 for d in dims)
+    windows = tuple(torch.randn(rows, width - 1, H, d, **kw).to(dt) for d in dims)
+    gate = torch.randn(*((T, H) if gate_per_head else (T, H, dv)), **kw).to(dt)
+    return dict(taps=taps, windows=windows, gate=gate)

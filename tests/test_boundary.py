@@ -60,6 +60,10 @@ int main(void) {
   printf("kda_decode_args %zu\n", sizeof(kda_decode_args));
   printf("kda_prep_args %zu\n", sizeof(kda_prep_args));
   printf("kda_prefill_host_args %zu\n", sizeof(kda_prefill_host_args));
+  printf("kda_layer_args %zu\n", sizeof(kda_layer_args));
+  F(kda_layer_args, conv_silu) F(kda_layer_args, conv_w) F(kda_layer_args, conv_in)
+  F(kda_layer_args, conv_out) F(kda_layer_args, out_gate) F(kda_layer_args, out_gate_per_head)
+  F(kda_prefill_args, layer) F(kda_decode_args, layer)
   F(kda_prefill_host_args, cu_seqlens) F(kda_prefill_host_args, in_dtype)
   F(kda_prefill_host_args, scale) F(kda_prefill_host_args, final_state)
   F(kda_prefill_host_args, segments) F(kda_prefill_host_args, copy_in_stream)
@@ -85,7 +89,8 @@ int main(void) {
     lines = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
     got = dict(l.rsplit(" ", 1) for l in lines if l)
     structs = {"kda_prefill_args": kda.PrefillArgs, "kda_decode_args": kda.DecodeArgs,
-               "kda_prep_args": kda.PrepArgs, "kda_prefill_host_args": kda.PrefillHostArgs}
+               "kda_prep_args": kda.PrepArgs, "kda_prefill_host_args": kda.PrefillHostArgs,
+               "kda_layer_args": kda.LayerArgs}
     for key, val in got.items():
         if "." in key:
             s, m = key.split(".")
@@ -149,6 +154,58 @@ def test_workspace_size_and_validation(kda):
     assert L.kda_prefill_workspace_size(ctypes.byref(_args(kda, scan_segments=4))) == ws
     assert L.kda_prefill(None, 0x4000, ws, None) == 1
     assert kda.kda_status_string(3).startswith("workspace")
+
+
+def test_layer_args_validation(kda):
+    """The short convolution and output gate arguments are checked on the
+    host: width outside 0..KDA_CONV_MAX, missing taps, a flag outside {0, 1},
+    and input/output windows that partly overlap are rejected before any
+    launch (a window updated in place, out == in, is allowed)."""
+    L = kda.lib()
+    W = 4
+    rows_bytes = 1 * (W - 1) * 2 * 16 * 4  # N x (W-1) x H x d x fp32, per tensor
+
+    def layer(**over):
+        la = kda.LayerArgs()
+        la.conv_width = W
+        for t in range(3):
+            la.conv_w[t] = 0x5000 + 0x100 * t
+        for k_, v_ in over.items():
+            setattr(la, k_, v_)
+        return la
+
+    def prefill_status(la):
+        a = _args(kda)
+        a.layer = ctypes.pointer(la)
+        return L.kda_prefill_workspace_size(ctypes.byref(a)), a
+
+    ok_ws, _ = prefill_status(layer())
+    assert ok_ws == L.kda_prefill_workspace_size(ctypes.byref(_args(kda)))  # no extra workspace
+    for bad in (dict(conv_width=5), dict(conv_width=-1), dict(out_gate_per_head=2)):
+        ws, a = prefill_status(layer(**bad))
+        assert ws == 0, bad
+        assert L.kda_prefill(ctypes.byref(a), 0x4000, 1 << 30, None) == 1, bad
+    la = layer()
+    la.conv_w[1] = None                                            # a missing tap tensor
+    assert prefill_status(la)[0] == 0
+    la = layer()                                                   # windows partly overlapping
+    la.conv_in[0], la.conv_out[0] = 0x10000, 0x10000 + rows_bytes // 2
+    assert prefill_status(la)[0] == 0
+    la.conv_out[0] = 0x10000                                       # in place: allowed
+    assert prefill_status(la)[0] > 0
+    la.conv_out[0] = 0x10000 + rows_bytes                          # adjacent: allowed
+    assert prefill_status(la)[0] > 0
+    la = layer(conv_width=0)                                       # off: taps not needed
+    for t in range(3):
+        la.conv_w[t] = None
+    assert prefill_status(la)[0] > 0
+    # decode: the same checks against the slot pool
+    d = kda.DecodeArgs()
+    d.batch, d.num_heads, d.dk, d.dv, d.num_slots = 4, 1, 16, 16, 4
+    d.q = d.k = d.v = d.g = d.b = d.o = 0x2000
+    d.state = 0x3000
+    d.layer = ctypes.pointer(layer(conv_width=7))
+    assert L.kda_decode_step(ctypes.byref(d), None) == 1
 
 
 def test_decode_and_prep_validation(kda):

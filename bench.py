@@ -267,21 +267,31 @@ def bench_layer_steps(torch, kda, W, dev, steps=10):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     for _ in range(3):
         p.run()
-    ms = []
+    nph = kda.PREFILL_PHASES
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)]
+    for e in ev:  # torch creates the cudaEvent_t on first record
+        e.record()
+    torch.cuda.synchronize()
+    handles = (kda.c_vp * (nph + 1))(*[e.cuda_event for e in ev])
+    p.args.phase_events = kda.ctypes.cast(handles, kda.c_vp)
+    ms, phase = [], [[] for _ in range(nph)]
     for _ in range(steps):
         flush_l2(flush)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
         p.run()
-        e1.record()
-        e1.synchronize()
-        ms.append(e0.elapsed_time(e1))
+        ev[-1].synchronize()
+        ms.append(ev[0].elapsed_time(ev[-1]))
+        for i in range(nph):
+            phase[i].append(ev[i].elapsed_time(ev[i + 1]))
+    p.args.phase_events = None
+    torch.cuda.synchronize()
     assert p.device_status() == 0
     t = sum(ms) / len(ms)
     return {"workload": w.description + ", short convolution (4 taps, SiLU) on q, k, v and a "
                                         "per-channel output gate",
             "ms_per_step": t, "tokens_per_s": T / (t * 1e-3), "steps": steps,
-            "algorithmic_bytes": T * w.H * (1282 + 256)}
+            "algorithmic_bytes": T * w.H * (1282 + 256),
+            "kernels_ms": {name: sum(x) / len(x) for name, x in
+                           zip(("plan", "intra_chunk", "inter_chunk_and_windows"), phase)}}
 
 
 def bench_varlen(torch, kda, W, dev, steps=10):

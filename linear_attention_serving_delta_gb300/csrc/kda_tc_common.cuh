@@ -75,6 +75,21 @@ __device__ __forceinline__ void flag(int32_t* status, int32_t f) { atomicOr(stat
 // bf16).  e^g overflowing to +inf gives alpha = 0.
 __device__ __forceinline__ float alpha_fast(float g) { return __fdividef(1.f, 1.f + __expf(g)); }
 
+// y sigmoid(y) = y / (1 + e^-y), the activation after the short convolution,
+// with the same intrinsics (its output is rounded to bf16 right after); a
+// very negative y gives -0.
+__device__ __forceinline__ float silu_fast(float y) { return __fdividef(y, 1.f + __expf(-y)); }
+
+// sigmoid(r), the output gate's factor, from t = e / (1 + e), e = e^-|r|:
+// t for r < 0 and 1 - t for r >= 0 (no cancellation on either side; a
+// saturated logit gives exactly 1 since t < 2^-25 rounds away).  Fast
+// exponential and division: o is rounded to bf16 right after.
+__device__ __forceinline__ float gate_fast(float r) {
+  const float e = __expf(-fabsf(r));
+  const float t = __fdividef(e, 1.f + e);
+  return r >= 0.f ? 1.f - t : t;
+}
+
 cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream);
 
 }  // namespace tcp

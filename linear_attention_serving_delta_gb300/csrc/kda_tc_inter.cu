@@ -114,11 +114,53 @@ __device__ __forceinline__ void split8(const float* u, uint4& hi, uint4& lo) {
   lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// The output gate's logits of one o row (token i of chunk ch, head h, this
+// thread's 16 columns; with a gate per head its one logit in r[0].x).  They
+// are read two steps before the row is stored and turned into factors one
+// step before, in the window where these warps wait for U and MMA 2, so the
+// store itself only multiplies.
+struct GateRow {
+  uint4 r[kNh / 8];
+};
+struct GateF {
+  float f[kNh];
+};
+__device__ __forceinline__ GateF gate_factors(const ChunkParams& p, const GateRow& g) {
+  GateF x;
+  if (p.out_gate_per_head) {
+    const float f = gate_fast(bf16_lo(g.r[0].x));
+#pragma unroll
+    for (int n = 0; n < kNh; ++n) x.f[n] = f;
+  } else {
+#pragma unroll
+    for (int q8 = 0; q8 < kNh / 8; ++q8)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x.f[8 * q8 + j] = gate_fast(bf16_at(g.r[q8], j));
+  }
+  return x;
+}
+__device__ __forceinline__ GateRow load_gate_row(const ChunkParams& p, const Chunk& ch, int i, int h,
+                                                 int n0, int h16) {
+  GateRow g{};
+  if (p.out_gate && i < ch.len && p.k3_mode != kScanPass1) {
+    const __nv_bfloat16* r = static_cast<const __nv_bfloat16*>(p.out_gate);
+    const int64_t row = (ch.tok0 + i) * p.H + h;
+    if (p.out_gate_per_head) {
+      g.r[0].x = (uint32_t)__bfloat16_as_ushort(r[row]);
+    } else {
+      const uint4* rg = reinterpret_cast<const uint4*>(r + row * (int64_t)kD + n0 + h16);
+#pragma unroll
+      for (int q8 = 0; q8 < kNh / 8; ++q8) g.r[q8] = __ldg(rg + q8);
+    }
+  }
+  return g;
+}
+
 // o rows of one chunk from lanes 64-127 of an output accumulator: row i, this
 // thread's 16 columns (none in the first pass of the segment scan), times
-// the output gate's sigmoid(r) when there is one
+// the output gate's factors gf when there is a gate
 __device__ __forceinline__ void store_output(const ChunkParams& p, const Chunk& ch, uint32_t d1,
-                                             int h16, int i, int h, int n0) {
+                                             int h16, int i, int h, int n0, const GateF& gf) {
   float d[kNh];
   tmem_ld_sum(d1, h16, d);
   if (i < ch.len && p.k3_mode != kScanPass1) {
@@ -126,22 +168,9 @@ __device__ __forceinline__ void store_output(const ChunkParams& p, const Chunk& 
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o);
     const int64_t row = (ch.tok0 + i) * p.H + h;
     uint4* dst = reinterpret_cast<uint4*>(o + row * (int64_t)kD + n0 + h16);
-    if (p.out_gate) {
-      const __nv_bfloat16* r = static_cast<const __nv_bfloat16*>(p.out_gate);
-      if (p.out_gate_per_head) {
-        const float f = out_gate_of(__bfloat162float(r[row]));
+    if (p.out_gate)
 #pragma unroll
-        for (int n = 0; n < kNh; ++n) d[n] *= f;
-      } else {
-        const uint4* rg = reinterpret_cast<const uint4*>(r + row * (int64_t)kD + n0 + h16);
-#pragma unroll
-        for (int q8 = 0; q8 < kNh / 8; ++q8) {
-          const uint4 x = rg[q8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) d[8 * q8 + j] *= out_gate_of(bf16_at(x, j));
-        }
-      }
-    }
+      for (int n = 0; n < kNh; ++n) d[n] *= gf.f[n];
 #pragma unroll
     for (int q8 = 0; q8 < kNh / 8; ++q8)
       dst[q8] = make_uint4(pack_bf16(scale * d[8 * q8], scale * d[8 * q8 + 1]),
@@ -296,6 +325,8 @@ tc_inter(ChunkParams p) {
 
   uint32_t ph1 = 0, ph2 = 0;
   Chunk prev1{}, prev2{};
+  GateRow graw{};   // the output gate's logits of chunk it-1's row (read last step)
+  GateF gfac{};     // its factors for chunk it-2's row (formed last step)
   Chunk next = nchunks > 0 ? p.chunks[c_begin] : Chunk{};
   for (int64_t it = 0; it < nchunks; ++it) {
     uint8_t* slot = slot_of(it);
@@ -321,7 +352,7 @@ tc_inter(ChunkParams p) {
       if (it >= 2) {
         okl = okl && wait_mma3(it - 2);
         fence_after_sync();
-        if (okl) store_output(p, prev2, d1_of(it - 2) + lane_off, h16, c - 64, h, n0);
+        if (okl) store_output(p, prev2, d1_of(it - 2) + lane_off, h16, c - 64, h, n0, gfac);
         // ... its A_qk tile takes chunk it+1 ...
         if (tid == kOutThread && okl && it + 1 < nchunks && aq_issued == it + 1) {
           k3_load_aq(p, aq_of(it + 1), &bar_aq[(it + 1) % K3Smem::kAqSlots], c_begin + it + 1, h);
@@ -333,10 +364,15 @@ tc_inter(ChunkParams p) {
         k3_load_chain(p, slot_of(it + 2), &bar_full[(it + 2) % K3Smem::kSlots], c_begin + it + 2, h, n0);
         chain_issued = it + 3;
       }
-      // ... and the output product of chunk it-1 runs once MMA 1 is done
+      // ... and the output product of chunk it-1 runs once MMA 1 is done; the
+      // gate logits of its row are fetched now, for its store next step
       if (tid == kOutThread && it >= 1 && okl) {
         okl = mbar_wait_t<kPoll>(&bar_mma1, ph1, p.wait_ns);
         if (okl) okl = mma3(it - 1);
+      }
+      if (p.out_gate) {  // factors of chunk it-1's row; logits of chunk it's row
+        gfac = gate_factors(p, graw);
+        graw = load_gate_row(p, ch, c - 64, h, n0, h16);
       }
     } else {
       // U = U~ - W S_j for token i = lane row, this thread's 16 columns.  The
@@ -410,11 +446,12 @@ tc_inter(ChunkParams p) {
       if (nchunks >= 2) {
         okl = okl && wait_mma3(nchunks - 2);
         fence_after_sync();
-        if (okl) store_output(p, prev2, d1_of(nchunks - 2) + lane_off, h16, c - 64, h, n0);
+        if (okl) store_output(p, prev2, d1_of(nchunks - 2) + lane_off, h16, c - 64, h, n0, gfac);
       }
+      if (p.out_gate) gfac = gate_factors(p, graw);  // chunk n-1's row
       okl = okl && wait_mma3(nchunks - 1);
       fence_after_sync();
-      if (okl) store_output(p, prev1, d1_of(nchunks - 1) + lane_off, h16, c - 64, h, n0);
+      if (okl) store_output(p, prev1, d1_of(nchunks - 1) + lane_off, h16, c - 64, h, n0, gfac);
     }
   }
   fence_before_sync();

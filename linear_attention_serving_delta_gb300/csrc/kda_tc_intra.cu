@@ -231,6 +231,14 @@ static_assert(kKHalo + kHaloBytes <= Smem::AKK + 64 * kAs * 4 && 2 * kHaloBytes 
               "the halo rows fit the tiles they borrow");
 static_assert(kKHalo % 128 == 0 && kQHalo % 128 == 0 && kVHalo % 128 == 0,
               "halo copies land on 128-byte boundaries");
+// The convolution's taps of the item's head (fp32, 128 channels a tap),
+// staged with group B after the q and v halo rows: tap j of tensor t at
+// kWStage + (4 t + j) * 512.  L1 holds little beside the shared memory, so
+// reading them from global memory would wait on L2 every item.
+constexpr uint32_t kTapBytes = kD * 4;
+constexpr uint32_t kWStage = kVHalo + kHaloBytes;
+static_assert(kWStage + 3 * KDA_CONV_MAX * kTapBytes <= Smem::A2 + 8 * kA2Lbo && kWStage % 128 == 0,
+              "the taps fit in A2 after the halo rows");
 
 // rows of one tensor, tokens tok0..tok0+63 of head h, into shared memory
 __device__ __forceinline__ void tma_rows(uint8_t* dst, const CUtensorMap* m, int h, int tok0,
@@ -250,22 +258,25 @@ __device__ __forceinline__ void tma_rows_l2(const CUtensorMap* m, int h, int tok
 
 // What an item needs of its chunk-table entry: first token and length (the
 // token index fits the int32 coordinates of the tensor maps on this path);
-// with the short convolution also how many of the halo rows lie inside the
-// sequence (pre, at most kHaloRows) and the sequence (for its window).
-// A few registers instead of the entry's eight.
+// with the short convolution also, packed as 4 seq + pre, how many of the
+// halo rows lie inside the sequence (pre, at most kHaloRows) and the
+// sequence (for its window).  A few registers instead of the entry's eight.
 struct ItemChunk {
-  int tok0, len, pre, seq;
+  int tok0, len, aux;
+  __device__ __forceinline__ int pre() const { return aux & 3; }
+  __device__ __forceinline__ int seq() const { return aux >> 2; }
 };
+static_assert(kHaloRows <= 3, "pre fits two bits");
 template <bool kConv>
 __device__ __forceinline__ ItemChunk item_chunk(const ChunkParams& p, int64_t idx) {
   const Chunk* c = p.chunks + idx;
-  ItemChunk r{(int)c->tok0, c->len, 0, 0};
+  ItemChunk r{(int)c->tok0, c->len, 0};
   if (kConv) {
     // segment scan: the table's sequences are segments of sequence 0, which
     // starts at token 0
     const int64_t pos = p.conv_one_seq ? c->tok0 : c->pos;
-    r.pre = pos < kHaloRows ? (int)pos : kHaloRows;
-    r.seq = p.conv_one_seq ? 0 : c->seq;
+    const int seq = p.conv_one_seq ? 0 : c->seq;
+    r.aux = 4 * seq + (pos < kHaloRows ? (int)pos : kHaloRows);
   }
   return r;
 }
@@ -282,16 +293,22 @@ __device__ __forceinline__ void stage_a(uint8_t* sm, uint64_t* bar, const ItemCh
   if (kConv) tma_rows(sm + kKHalo, &maps.kh, h, ch.tok0 - kHaloRows, bar);
 }
 
-// Staging group B of item (ch, h): the rows of q and v (and their halo rows).
+// Staging group B of item (ch, h): the rows of q and v (and, with the
+// convolution, their halo rows and head h's taps).
 template <bool kConv>
 __device__ __forceinline__ void stage_b(uint8_t* sm, uint64_t* bar, const ItemChunk& ch, int h,
-                                        const RowMaps& maps) {
-  mbar_arrive_expect_tx(bar, 2 * kRowsBytes + (kConv ? 2 * kHaloBytes : 0));
+                                        const RowMaps& maps, const ChunkParams& p) {
+  const int W = kConv ? p.conv_width : 0;
+  mbar_arrive_expect_tx(bar, 2 * kRowsBytes + (kConv ? 2 * kHaloBytes + 3 * W * kTapBytes : 0));
   tma_rows(sm + kQStage, &maps.q, h, ch.tok0, bar);
   tma_rows(sm + kVStage, &maps.v, h, ch.tok0, bar);
   if (kConv) {
     tma_rows(sm + kQHalo, &maps.qh, h, ch.tok0 - kHaloRows, bar);
     tma_rows(sm + kVHalo, &maps.vh, h, ch.tok0 - kHaloRows, bar);
+    for (int t = 0; t < 3; ++t)
+      for (int j = 0; j < W; ++j)
+        bulk_g2s(sm + kWStage + (4 * t + j) * kTapBytes, p.conv_w[t] + ((size_t)j * p.H + h) * kD, kTapBytes,
+                 bar);
   }
 }
 
@@ -308,18 +325,19 @@ __device__ __forceinline__ uint4 halo16(const uint8_t* sm, uint32_t halo, const 
                                         const ChunkParams& p, const ItemChunk& ch, int h, int back, int c0) {
   const int W = p.conv_width;
   if (back > W - 1) return make_uint4(0, 0, 0, 0);
-  if (back <= ch.pre) return raw16(sm, halo, kHaloRows - back, c0);
+  if (back <= ch.pre()) return raw16(sm, halo, kHaloRows - back, c0);
   if (!win) return make_uint4(0, 0, 0, 0);
   const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(win);
-  const int64_t row = (int64_t)ch.seq * (W - 1) + (W - 1) - (back - ch.pre);
+  const int64_t row = (int64_t)ch.seq() * (W - 1) + (W - 1) - (back - ch.pre());
   return *reinterpret_cast<const uint4*>(wb + (row * p.H + h) * kD + c0);
 }
 
 // Rows i0..i0+3 (channels c0..c0+7) of tensor t (0 q, 1 k, 2 v) after the
 // short convolution, as bf16: y_i = sum_{j < W} w[j][h][c] x_{i-j} (taps at
-// or past W count as 0), SiLU if asked, rounded to bf16 (the input dtype);
+// or past W count as 0), SiLU if asked (silu_fast), rounded to bf16 (the input dtype);
 // rows at or past len give zeros, as the raw rows do.  The inputs come from
-// the item's staging and, for the first token block, the halo.
+// the item's staging and, for the first token block, the halo; the taps
+// from their staging.
 __device__ __forceinline__ void conv_rows(const uint8_t* sm, uint32_t stage, uint32_t halo, int t,
                                           const ChunkParams& p, const ItemChunk& ch, int h, int i0, int c0,
                                           uint4 out[4]) {
@@ -331,32 +349,29 @@ __device__ __forceinline__ void conv_rows(const uint8_t* sm, uint32_t stage, uin
     x[m] = i >= 0 ? (i < ch.len ? raw16(sm, stage, i, c0) : z) : halo16(sm, halo, p.conv_in[t], p, ch, h, -i, c0);
   }
   const int W = p.conv_width;
-  const float* w = p.conv_w[t] + (size_t)h * kD + c0;
-  const size_t tap = (size_t)p.H * kD;
+  const float* w = reinterpret_cast<const float*>(sm + kWStage + 4 * t * kTapBytes) + c0;  // staged taps
   uint32_t o[4][4];
 #pragma unroll
-  for (int pp = 0; pp < 4; ++pp) {  // channel pair c0 + 2 pp, c0 + 2 pp + 1
-    float w0[4], w1[4];
+  for (int pp = 0; pp < 4; ++pp) {  // channel pair c0 + 2 pp, c0 + 2 pp + 1, two lanes of f32x2
+    float2 wv[4], xv[7];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 wv = j < W ? __ldg(reinterpret_cast<const float2*>(w + j * tap + 2 * pp))
-                              : make_float2(0.f, 0.f);
-      w0[j] = wv.x;
-      w1[j] = wv.y;
+    for (int j = 0; j < 4; ++j)
+      wv[j] = j < W ? *reinterpret_cast<const float2*>(w + j * kD + 2 * pp) : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 7; ++m) {
+      const uint32_t wd = pp == 0 ? x[m].x : pp == 1 ? x[m].y : pp == 2 ? x[m].z : x[m].w;
+      xv[m] = make_float2(bf16_lo(wd), bf16_hi(wd));
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      float a0 = 0.f, a1 = 0.f;
+      float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        a0 += w0[j] * bf16_at(x[r + kHaloRows - j], 2 * pp);
-        a1 += w1[j] * bf16_at(x[r + kHaloRows - j], 2 * pp + 1);
-      }
+      for (int j = 0; j < 4; ++j) a = __ffma2_rn(wv[j], xv[r + kHaloRows - j], a);
       if (p.conv_silu) {
-        a0 = silu_of(a0);
-        a1 = silu_of(a1);
+        a.x = silu_fast(a.x);
+        a.y = silu_fast(a.y);
       }
-      o[r][pp] = i0 + r < ch.len ? pack_bf16(a0, a1) : 0u;
+      o[r][pp] = i0 + r < ch.len ? pack_bf16(a.x, a.y) : 0u;
     }
   }
 #pragma unroll
@@ -433,12 +448,12 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
   // the item before it
   ItemChunk ch = item_chunk<kConv>(p, item / H);  // entries past the table's end have len 0
   ItemChunk ch_next =
-      item + stride < n_items ? item_chunk<kConv>(p, (item + stride) / H) : ItemChunk{0, 0, 0, 0};
+      item + stride < n_items ? item_chunk<kConv>(p, (item + stride) / H) : ItemChunk{0, 0, 0};
   {
     const int h0 = (int)(item % H);
     if (tid == 0) {
       stage_a<kHeadGate, kConv>(sm, &bar_ga, ch, h0, maps);
-      stage_b<kConv>(sm, &bar_gb, ch, h0, maps);
+      stage_b<kConv>(sm, &bar_gb, ch, h0, maps, p);
     }
     if (kHeadGate && tid < 64) gtok[tid] = load_gh(p, ch, h0, tid);
   }
@@ -472,6 +487,27 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     // this item's g and k (group A) have landed; q and v (group B) may still fly
     ok = mbar_wait_t<kPoll>(&bar_ga, sph, p.wait_ns);
     a_fly = false;
+    if constexpr (kConv) {
+      // the convolution, before the decay scan: q and v (group B) were staged
+      // during the previous item.  Its results replace the staged rows (once
+      // every thread has read its inputs, some of them other threads' rows),
+      // and the raw reads below take them from there like unconvolved rows:
+      // no registers are held through the scan.
+      ok = mbar_wait_t<kPoll>(&bar_gb, sph, p.wait_ns) && ok;
+      b_fly = false;
+      // one tensor at a time (a barrier each): only its 16 registers of
+      // results are live
+#pragma unroll 1
+      for (int u = 0; u < 3; ++u) {  // k (tensor 1), q (0), v (2)
+        const uint32_t stage = u == 0 ? kKStage : u == 1 ? kQStage : kVStage;
+        const uint32_t halo = u == 0 ? kKHalo : u == 1 ? kQHalo : kVHalo;
+        uint4 y[4];
+        conv_rows(sm, stage, halo, u == 0 ? 1 : u == 1 ? 0 : 2, p, ch, h, i0, c0, y);
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < 4; ++r) st_s16(sm, stage + (i0 + r) * 256 + c0 * 2, y[r]);
+      }
+    }
 
     // ---- cumulative decay Gamma_i = prod_{m<=i} alpha_m, alpha = 1 / (1 + e^g)
     // (= exp(-softplus(g))): a product over this thread's 4 tokens, a scan
@@ -531,23 +567,20 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     // ---- L2 norms per token: 8 channels here, 8 lanes, then the two channel
     // halves.  The raw q, k, v chunks go to registers now: the operands are
     // written over their stagings after the next two barriers.
-    ok = mbar_wait_t<kPoll>(&bar_gb, sph, p.wait_ns) && ok;
-    b_fly = false;
+    if constexpr (!kConv) {
+      ok = mbar_wait_t<kPoll>(&bar_gb, sph, p.wait_ns) && ok;
+      b_fly = false;
+    }
     sph ^= 1;
+    // (each thread reads back exactly the rows and channels it convolved)
     uint4 qraw[4], kraw[4], vraw[4];
-    if constexpr (kConv) {
-      conv_rows(sm, kKStage, kKHalo, 1, p, ch, h, i0, c0, kraw);
-      conv_rows(sm, kQStage, kQHalo, 0, p, ch, h, i0, c0, qraw);
-      conv_rows(sm, kVStage, kVHalo, 2, p, ch, h, i0, c0, vraw);
-    } else {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const bool live = i0 + r < len;
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        qraw[r] = live ? raw16(sm, kQStage, i0 + r, c0) : z;
-        kraw[r] = live ? raw16(sm, kKStage, i0 + r, c0) : z;
-        vraw[r] = live ? raw16(sm, kVStage, i0 + r, c0) : z;
-      }
+    for (int r = 0; r < 4; ++r) {
+      const bool live = i0 + r < len;
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      qraw[r] = live ? raw16(sm, kQStage, i0 + r, c0) : z;
+      kraw[r] = live ? raw16(sm, kKStage, i0 + r, c0) : z;
+      vraw[r] = live ? raw16(sm, kVStage, i0 + r, c0) : z;
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -760,7 +793,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     if (!ok) break;
     // MMA 2 has read B2: the next item's q and v (group B) are staged there now
     if (has_next) {
-      if (tid == 0) stage_b<kConv>(sm, &bar_gb, chn, hn, maps);
+      if (tid == 0) stage_b<kConv>(sm, &bar_gb, chn, hn, maps, p);
       b_fly = true;
     }
     {
@@ -809,7 +842,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     }
     ch = ch_next;
     ch_next = item + 2 * stride < n_items ? item_chunk<kConv>(p, (item + 2 * stride) / H)
-                                          : ItemChunk{0, 0, 0, 0};
+                                          : ItemChunk{0, 0, 0};
   }
   // no staging copy and no MMA is left in flight when the CTA exits (these
   // waits keep the long limit whatever the caller chose for the others)

@@ -498,6 +498,9 @@ def gpu_arm(a):
         torch.cuda.synchronize()
 
     barrier()
+    if a.layer_only:
+        print(json.dumps(bench_layer_steps(torch, kda, W, dev, steps=a.steps)))
+        return
     with ClockSampler(local) as clk:
         pre = bench_prefill(torch, kda, W, a.steps, a.warmup, dev)
         barrier()
@@ -652,6 +655,8 @@ def main():
                     help="also time the million-token configuration (~100 GB of device memory)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time the prefill workload alone (for profiler captures)")
+    ap.add_argument("--layer-only", action="store_true",
+                    help="time the prefill with the layer steps alone (for profiler captures)")
     a = ap.parse_args()
     if a.warmup < 3:
         a.warmup = 3

@@ -131,7 +131,7 @@ typedef struct {
 typedef struct {
   int32_t num_seqs;            /* N >= 1                                          */
   int32_t num_heads;           /* H >= 1                                          */
-  int32_t dk, dv;              /* each in {16, 32, 64, 128}                       */
+  int32_t dk, dv;              /* each in {16, 32, 64, 128, 256}                  */
   int64_t total_tokens;        /* T = cu_seqlens[N]; host-known upper bound, >= 0 */
   const int64_t* cu_seqlens;   /* device [N+1], cu[0] = 0, non-decreasing         */
   kda_dtype_t in_dtype;        /* dtype of q, k, v, g, b and of o                 */
@@ -212,7 +212,8 @@ size_t kda_prefill_workspace_size(const kda_prefill_args* args);
  * kda_prefill_workspace_size(args) bytes, 256-byte aligned, owned by the
  * caller and not used by another call in flight.  The path is chosen by the
  * arguments: bf16 inputs with dk = dv = 128 run on the tcgen05 tensor-core
- * kernels; every other supported shape runs on fp32 CUDA-core kernels. */
+ * kernels; every other supported shape runs on fp32 CUDA-core kernels
+ * (heads of 256 channels on a variant that takes 128 channels at a time). */
 kda_status_t kda_prefill(const kda_prefill_args* args, void* ws, size_t ws_bytes,
                          void* stream);
 
@@ -275,7 +276,7 @@ kda_status_t kda_prefill_noalloc(const kda_prefill_args* args, void* stream);
 typedef struct {
   int32_t num_seqs;            /* N >= 1                                          */
   int32_t num_heads;           /* H >= 1                                          */
-  int32_t dk, dv;              /* each in {16, 32, 64, 128}                       */
+  int32_t dk, dv;              /* each in {16, 32, 64, 128, 256}                  */
   int64_t total_tokens;        /* T = cu_seqlens[N]                               */
   const int64_t* cu_seqlens;   /* HOST [N+1]                                      */
   kda_dtype_t in_dtype;        /* dtype of q, k, v, g, b and of o                 */
@@ -370,7 +371,7 @@ int64_t kda_prefix_cache_reserve(kda_prefix_cache* cache, const int32_t* tokens,
 typedef struct {
   int32_t batch;               /* B >= 0 rows                                     */
   int32_t num_heads;           /* H                                               */
-  int32_t dk, dv;              /* each in {16, 32, 64, 128}                       */
+  int32_t dk, dv;              /* each in {16, 32, 64, 128, 256}                  */
   int32_t num_slots;           /* rows of the state pool                          */
   kda_dtype_t in_dtype;        /* dtype of q, k, v, g, b and of o                 */
   float scale;
@@ -392,7 +393,9 @@ typedef struct {
   const kda_layer_args* layer; /* host pointer, or NULL: the short convolution and
                                   output gate; windows [num_slots, conv_width - 1,
                                   H, d] indexed by the row's slot, updated in
-                                  place when conv_out == conv_in                  */
+                                  place when conv_out == conv_in.  The
+                                  convolution needs dk * dv <= 128 * 128 here
+                                  (KDA_ERR_UNSUPPORTED otherwise)               */
 } kda_decode_args;
 
 kda_status_t kda_decode_step(const kda_decode_args* args, void* stream);

@@ -8,7 +8,7 @@
 namespace kda {
 namespace {
 
-bool head_size_ok(int32_t d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool head_size_ok(int32_t d) { return d == 16 || d == 32 || d == 64 || d == 128 || d == 256; }
 bool dtype_ok(kda_dtype_t t) { return t == KDA_F32 || t == KDA_BF16; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -306,6 +306,9 @@ kda_status_t kda_decode_step(const kda_decode_args* a, void* stream) {
   if (a->gate_per_head != 0 && a->gate_per_head != 1) return KDA_ERR_INVALID_ARG;
   kda_status_t ls = validate_layer(a->layer, a->num_slots, a->num_heads, a->dk, a->dv, elem_bytes(a->in_dtype));
   if (ls != KDA_OK) return ls;
+  // heads wider than 128 x 128 run as several CTAs per (row, head), which
+  // would race on a q/k window updated in place
+  if (a->layer && a->layer->conv_width > 0 && (int64_t)a->dk * a->dv > 128 * 128) return KDA_ERR_UNSUPPORTED;
   return from_cuda(launch_decode(*a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -73,21 +73,30 @@ struct DecodeShape {
   static_assert(DK % NRG == 0, "row groups tile the key channels");
 };
 
-template <typename TIn, int DK, int DV>
-__global__ void __launch_bounds__(DecodeShape<TIn, DK, DV>::NT)
+// One CTA per (row, head, slice of DVS value columns): the reductions run
+// over key channels for each value column, so the columns split freely.
+// Heads up to 128 x 128 take one slice (DVS = DV); wider ones slices of 64,
+// which keep a thread's share of the state in registers.
+template <int DK, int DV>
+struct DecodeSlice {
+  static constexpr int DVS = DK * DV > 128 * 128 ? 64 : DV;
+};
+
+template <typename TIn, int DK, int DV, int DVS>
+__global__ void __launch_bounds__(DecodeShape<TIn, DK, DVS>::NT)
 decode_step(kda_decode_args a, const kda_layer_args l) {
-  using Sh = DecodeShape<TIn, DK, DV>;
+  using Sh = DecodeShape<TIn, DK, DVS>;
   constexpr int QPR = Sh::QPR, NT = Sh::NT, NRG = Sh::NRG, RPT = Sh::RPT;
   // arrays read through float4 are 16-byte aligned explicitly
   __shared__ __align__(16) float qn[DK];
   __shared__ __align__(16) float kn[DK];
   __shared__ __align__(16) float al[DK];
-  __shared__ __align__(16) float vv[DV];
-  __shared__ __align__(16) float red_p[NRG][DV];
-  __shared__ __align__(16) float red_o[NRG][DV];
+  __shared__ __align__(16) float vv[DVS];
+  __shared__ __align__(16) float red_p[NRG][DVS];
+  __shared__ __align__(16) float red_o[NRG][DVS];
   __shared__ float sc[2];  // beta, q^.k^
 
-  const int row = blockIdx.x, h = blockIdx.y, H = a.num_heads;
+  const int row = blockIdx.x, h = blockIdx.y, H = a.num_heads, n0 = blockIdx.z * DVS;
   const int slot = a.state_slots ? a.state_slots[row] : row;
   if (slot < 0 || slot >= a.num_slots) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -98,7 +107,7 @@ decode_step(kda_decode_args a, const kda_layer_args l) {
   float4 s[RPT];
 #pragma unroll
   for (int i = 0; i < RPT; ++i)
-    s[i] = reinterpret_cast<const float4*>(S + (size_t)(rg + i * NRG) * DV)[cq];
+    s[i] = reinterpret_cast<const float4*>(S + (size_t)(rg + i * NRG) * DV + n0)[cq];
 
   // token preparation (one warp): q^, k^, alpha, beta, q^.k^
   if (warp == 0) {
@@ -126,7 +135,8 @@ decode_step(kda_decode_args a, const kda_layer_args l) {
       sq += xq * xq;
       sk += xk * xk;
     }
-    for (int c = lane; c < DV; c += 32) {
+    for (int cs = lane; cs < DVS; cs += 32) {
+      const int c = n0 + cs;
       float xv = ld_in(v, base_v + c);
       if (l.conv_width > 0) {
         auto pv = [&](int m) { return window_at<TIn>(l, 2, slot, m, H, h, c, DV); };
@@ -134,7 +144,7 @@ decode_step(kda_decode_args a, const kda_layer_args l) {
         xv = conv_token<TIn>(l, 2, rv, H, h, c, DV, pv);
         window_push<TIn>(l, 2, rv, slot, H, h, c, DV, pv);
       }
-      vv[c] = xv;
+      vv[cs] = xv;
     }
     const float iq = inv_norm_of(warp_sum(sq)), ik = inv_norm_of(warp_sum(sk));
     float qk = 0.f;
@@ -201,12 +211,12 @@ decode_step(kda_decode_args a, const kda_layer_args l) {
     const float k_r = kn[r];
     float4 x = s[i];
     x.x += k_r * u.x; x.y += k_r * u.y; x.z += k_r * u.z; x.w += k_r * u.w;
-    reinterpret_cast<float4*>(S + (size_t)r * DV)[cq] = x;
+    reinterpret_cast<float4*>(S + (size_t)r * DV + n0)[cq] = x;
   }
   if (rg == 0) {
     const float qk = sc[1], scl = a.scale;
     TIn* o = static_cast<TIn*>(a.o);
-    const int64_t ob = ((int64_t)row * H + h) * DV + 4 * cq;
+    const int64_t ob = ((int64_t)row * H + h) * DV + n0 + 4 * cq;
     st_out(o, ob + 0, scl * (oq.x + qk * u.x) * gate_at<TIn>(l, row, H, h, ob + 0));
     st_out(o, ob + 1, scl * (oq.y + qk * u.y) * gate_at<TIn>(l, row, H, h, ob + 1));
     st_out(o, ob + 2, scl * (oq.z + qk * u.z) * gate_at<TIn>(l, row, H, h, ob + 2));
@@ -526,8 +536,9 @@ cudaError_t launch_t(const kda_decode_args& a, const kda_layer_args& l, cudaStre
       if (conv) return launch_ring<TIn, true>(a, l, stream);
     return launch_ring<TIn, false>(a, l, stream);
   }
-  dim3 grid((unsigned)a.batch, (unsigned)a.num_heads);
-  decode_step<TIn, DK, DV><<<grid, DecodeShape<TIn, DK, DV>::NT, 0, stream>>>(a, l);
+  constexpr int DVS = DecodeSlice<DK, DV>::DVS;
+  dim3 grid((unsigned)a.batch, (unsigned)a.num_heads, (unsigned)(DV / DVS));
+  decode_step<TIn, DK, DV, DVS><<<grid, DecodeShape<TIn, DK, DVS>::NT, 0, stream>>>(a, l);
   return cudaGetLastError();
 }
 
@@ -538,6 +549,7 @@ cudaError_t launch_dv(const kda_decode_args& a, const kda_layer_args& l, cudaStr
     case 32: return launch_t<TIn, DK, 32>(a, l, stream);
     case 64: return launch_t<TIn, DK, 64>(a, l, stream);
     case 128: return launch_t<TIn, DK, 128>(a, l, stream);
+    case 256: return launch_t<TIn, DK, 256>(a, l, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -549,6 +561,7 @@ cudaError_t launch_dk(const kda_decode_args& a, const kda_layer_args& l, cudaStr
     case 32: return launch_dv<TIn, 32>(a, l, stream);
     case 64: return launch_dv<TIn, 64>(a, l, stream);
     case 128: return launch_dv<TIn, 128>(a, l, stream);
+    case 256: return launch_dv<TIn, 256>(a, l, stream);
   }
   return cudaErrorInvalidValue;
 }

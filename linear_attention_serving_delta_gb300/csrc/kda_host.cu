@@ -24,7 +24,7 @@ struct Piece {
   int64_t cu_off;      // entries into the device table of per-piece cu_seqlens
 };
 
-bool head_ok(int32_t d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool head_ok(int32_t d) { return d == 16 || d == 32 || d == 64 || d == 128 || d == 256; }
 
 kda_status_t validate_host(const kda_prefill_host_args* a) {
   if (!a) return KDA_ERR_INVALID_ARG;

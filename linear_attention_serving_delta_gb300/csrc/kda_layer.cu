@@ -14,7 +14,8 @@ namespace kda {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kMaxPer = 3;  // elements per thread: (KDA_CONV_MAX - 1) rows x 128 channels / 128
+constexpr int kMaxD = 256;   // widest head
+constexpr int kMaxPer = (KDA_CONV_MAX - 1) * kMaxD / kThreads;  // elements per thread
 
 // One CTA per (sequence, tensor, head).  Every read comes before the first
 // write, so `out` may be the same buffer as `in`.
@@ -32,7 +33,7 @@ conv_windows(const int64_t* __restrict__ cu, int64_t T, int32_t H, int32_t dk, i
   const int64_t start = cu[s], len = cu[s + 1] - start;
   // a malformed cu_seqlens (flagged by the planner) leaves the window as it is
   if (start < 0 || len < 0 || start + len > T) return;
-  const int n = R * d;  // <= 3 * 128
+  const int n = R * d;  // <= (KDA_CONV_MAX - 1) * kMaxD
   E val[kMaxPer];
 #pragma unroll
   for (int u = 0; u < kMaxPer; ++u) {
@@ -65,7 +66,7 @@ cudaError_t launch_conv_windows(const kda_layer_args& l, int32_t num_seqs, int32
                                 const void* const x[3], cudaStream_t stream) {
   const int32_t R = l.conv_width - 1;
   if (R <= 0 || !(l.conv_out[0] || l.conv_out[1] || l.conv_out[2])) return cudaSuccess;
-  static_assert((KDA_CONV_MAX - 1) * 128 <= kMaxPer * kThreads, "one pass covers a window");
+  static_assert((KDA_CONV_MAX - 1) * kMaxD <= kMaxPer * kThreads, "one pass covers a window");
   dim3 grid((unsigned)num_seqs, 3, (unsigned)H);
   if (dt == KDA_BF16)
     conv_windows<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(

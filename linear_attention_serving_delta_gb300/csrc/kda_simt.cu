@@ -185,6 +185,161 @@ simt_intra(ChunkParams p) {
   for (int col = tid; col < dk; col += kThreads) rec[SimtRec::gl(dk, dv) + col] = expf(GLrow[col]);
 }
 
+// Heads wider than 128 channels (dk or dv = 256): the same chunk algebra with
+// the channels taken in blocks of kCB, so that shared memory holds one block
+// of q^, k^ and G (or of V) at a time.  Pass 1 forms the inverse norms of the
+// rows; pass 2 sums A_kk and A_qk over the key blocks (each block's G is its
+// channels' running sum, channels being independent); then T; pass 3 forms
+// W, Q^ o Gamma, K^ o Gamma_L / Gamma and Gamma_L block by block, and U~ over
+// the value blocks.  q, k, g are read twice (the second time mostly from L2).
+constexpr int kCB = 128;
+
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads)
+simt_intra_blocked(ChunkParams p) {
+  extern __shared__ float sm[];
+  const int64_t c = blockIdx.x;
+  const Chunk ch = p.chunks[c];  // entries past the table's end have len 0
+  if (ch.len == 0) return;
+  const int h = blockIdx.y, H = p.H, dk = p.dk, dv = p.dv;
+  const int len = ch.len;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  float* X = sm;                     // [64][kCB]: q^ block, then V block
+  float* Kb = X + kChunk * kCB;      // [64][kCB]: k^ block
+  float* G = Kb + kChunk * kCB;      // [64][kCB]: running log-decay block
+  float* A = G + kChunk * kCB;       // [64][64] A_kk
+  float* AQ = A + kChunk * kChunk;   // [64][64] A_qk
+  float* Tm = AQ + kChunk * kChunk;  // [64][64] T, then T diag(beta)
+  float* beta = Tm + kChunk * kChunk;  // [64]
+  float* invq = beta + kChunk;       // [64]
+  float* invk = invq + kChunk;       // [64]
+
+  const TIn* q = static_cast<const TIn*>(p.q);
+  const TIn* k = static_cast<const TIn*>(p.k);
+  const TIn* v = static_cast<const TIn*>(p.v);
+  const TIn* g = static_cast<const TIn*>(p.g);
+  const TIn* b = static_cast<const TIn*>(p.b);
+
+  // pass 1: inverse norms of the (convolved) q and k rows, one warp per token
+  for (int i = warp; i < kChunk; i += kThreads / 32) {
+    float sq = 0.f, sk = 0.f;
+    if (i < len)
+      for (int col = lane; col < dk; col += 32) {
+        const float xq = conv_input(p, 0, q, dk, ch, i, h, col), xk = conv_input(p, 1, k, dk, ch, i, h, col);
+        sq += xq * xq;
+        sk += xk * xk;
+      }
+    sq = warp_sum(sq);
+    sk = warp_sum(sk);
+    if (lane == 0) {
+      invq[i] = inv_norm_of(sq);
+      invk[i] = inv_norm_of(sk);
+    }
+  }
+  if (tid < kChunk) beta[tid] = tid < len ? beta_of(ld_in(b, (ch.tok0 + tid) * H + h)) : 0.f;
+  for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) A[idx] = AQ[idx] = 0.f;
+  __syncthreads();
+
+  // one key block [c0, c0 + nb) of q^, k^ and the running log-decay G
+  auto load_key_block = [&](int c0, int nb) {
+    for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
+      const int i = idx / nb, col = idx - i * nb;
+      float xq = 0.f, xk = 0.f, la = 0.f;
+      if (i < len) {
+        xq = conv_input(p, 0, q, dk, ch, i, h, c0 + col) * invq[i];
+        xk = conv_input(p, 1, k, dk, ch, i, h, c0 + col) * invk[i];
+        const int64_t e = ((ch.tok0 + i) * H + h) * dk + c0 + col;
+        la = log_alpha_of(ld_in(g, p.gate_per_head ? (ch.tok0 + i) * H + h : e));
+      }
+      X[i * kCB + col] = xq;
+      Kb[i * kCB + col] = xk;
+      G[i * kCB + col] = la;
+    }
+    __syncthreads();
+    for (int col = tid; col < nb; col += kThreads) {  // rows past len carry G_{L-1}
+      float run = 0.f;
+      for (int i = 0; i < kChunk; ++i) {
+        run += G[i * kCB + col];
+        G[i * kCB + col] = run;
+      }
+    }
+    __syncthreads();
+  };
+
+  // pass 2: A_kk and A_qk, summed over the key blocks
+  for (int c0 = 0; c0 < dk; c0 += kCB) {
+    const int nb = dk - c0 < kCB ? dk - c0 : kCB;
+    load_key_block(c0, nb);
+    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
+      const int i = idx >> 6, j = idx & 63;
+      if (j <= i && i < len) {
+        float akk = 0.f, aqk = 0.f;
+        for (int col = 0; col < nb; ++col) {
+          const float d = expf(G[i * kCB + col] - G[j * kCB + col]);
+          const float kj = Kb[j * kCB + col] * d;
+          akk += Kb[i * kCB + col] * kj;
+          aqk += X[i * kCB + col] * kj;
+        }
+        if (j < i) A[idx] += beta[i] * akk;
+        AQ[idx] += aqk;
+      }
+    }
+    __syncthreads();
+  }
+  float* rec = p.inter + ((size_t)c * H + h) * p.rec_floats;
+  for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) rec[SimtRec::aqk(dk) + idx] = AQ[idx];
+
+  // T = (I + A_kk)^{-1} by forward substitution (a thread per column), then
+  // T diag(beta)
+  if (tid < kChunk) {
+    const int j = tid;
+    for (int i = 0; i < kChunk; ++i) {
+      float t = i == j ? 1.f : 0.f;
+      if (i > j)
+        for (int m = j; m < i; ++m) t -= A[i * kChunk + m] * Tm[m * kChunk + j];
+      Tm[i * kChunk + j] = t;
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) Tm[idx] *= beta[idx & 63];
+  __syncthreads();
+
+  // pass 3: W, Q^ o Gamma, K^ o Gamma_L / Gamma and Gamma_L per key block
+  for (int c0 = 0; c0 < dk; c0 += kCB) {
+    const int nb = dk - c0 < kCB ? dk - c0 : kCB;
+    load_key_block(c0, nb);
+    const float* GL = G + (kChunk - 1) * kCB;
+    for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
+      const int i = idx / nb, col = idx - i * nb;
+      float w = 0.f;
+      for (int m = 0; m <= i; ++m) w += Tm[i * kChunk + m] * Kb[m * kCB + col] * expf(G[m * kCB + col]);
+      const size_t o = (size_t)i * dk + c0 + col;
+      rec[SimtRec::w(dk) + o] = w;
+      rec[SimtRec::qg(dk) + o] = X[i * kCB + col] * expf(G[i * kCB + col]);
+      rec[SimtRec::kr(dk) + o] = Kb[i * kCB + col] * expf(GL[col] - G[i * kCB + col]);
+    }
+    for (int col = tid; col < nb; col += kThreads) rec[SimtRec::gl(dk, dv) + c0 + col] = expf(GL[col]);
+    __syncthreads();
+  }
+  // U~ = T diag(beta) V per value block
+  for (int v0 = 0; v0 < dv; v0 += kCB) {
+    const int nb = dv - v0 < kCB ? dv - v0 : kCB;
+    for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
+      const int i = idx / nb, col = idx - i * nb;
+      X[i * kCB + col] = i < len ? conv_input(p, 2, v, dv, ch, i, h, v0 + col) : 0.f;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
+      const int i = idx / nb, col = idx - i * nb;
+      float u = 0.f;
+      for (int m = 0; m <= i; ++m) u += Tm[i * kChunk + m] * X[m * kCB + col];
+      rec[SimtRec::ut(dk) + (size_t)i * dv + v0 + col] = u;
+    }
+    __syncthreads();
+  }
+}
+
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads)
 simt_inter(ChunkParams p, int ns) {
@@ -262,14 +417,18 @@ simt_inter(ChunkParams p, int ns) {
 
 template <typename TIn>
 cudaError_t launch_simt_t(const ChunkParams& p, cudaStream_t stream, cudaEvent_t mid) {
+  // heads up to 128 channels keep a whole chunk in shared memory; wider ones
+  // take the blocked kernel
+  const bool blocked = p.dk > kCB || p.dv > kCB;
   const size_t smem_intra =
-      sizeof(float) * (3 * (size_t)kChunk * p.dk + (size_t)kChunk * p.dv + 2 * kChunk * kChunk + kChunk);
-  cudaError_t e = cudaFuncSetAttribute(simt_intra<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem_intra);
+      blocked ? sizeof(float) * (3 * (size_t)kChunk * kCB + 3 * kChunk * kChunk + 3 * kChunk)
+              : sizeof(float) * (3 * (size_t)kChunk * p.dk + (size_t)kChunk * p.dv + 2 * kChunk * kChunk + kChunk);
+  auto intra = blocked ? simt_intra_blocked<TIn> : simt_intra<TIn>;
+  cudaError_t e = cudaFuncSetAttribute(intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_intra);
   if (e != cudaSuccess) return e;
   if (p.max_chunks > 0) {
     dim3 grid((unsigned)p.max_chunks, (unsigned)p.H);
-    simt_intra<TIn><<<grid, kThreads, smem_intra, stream>>>(p);
+    intra<<<grid, kThreads, smem_intra, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -279,6 +438,8 @@ cudaError_t launch_simt_t(const ChunkParams& p, cudaStream_t stream, cudaEvent_t
   }
   const int ns = p.dv < 32 ? p.dv : 32;
   const size_t smem_inter = sizeof(float) * ((size_t)p.dk * ns + 2 * (size_t)kChunk * ns);
+  e = cudaFuncSetAttribute(simt_inter<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_inter);
+  if (e != cudaSuccess) return e;
   dim3 grid2((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)(p.dv / ns));
   simt_inter<TIn><<<grid2, kThreads, smem_inter, stream>>>(p, ns);
   return cudaGetLastError();

@@ -117,7 +117,7 @@ def test_workspace_size_and_validation(kda):
     ws = L.kda_prefill_workspace_size(ctypes.byref(good))
     assert ws > 0 and ws % 256 == 0
     # invalid arguments: size query returns 0 and the call returns a status, no launch
-    for bad, code in [(dict(dk=24), 2), (dict(dv=256), 2), (dict(num_seqs=0), 1),
+    for bad, code in [(dict(dk=24), 2), (dict(dv=512), 2), (dict(num_seqs=0), 1),
                       (dict(cu_seqlens=None), 1), (dict(q=None), 1),
                       (dict(snapshot_interval=100), 1), (dict(snapshot_interval=-64), 1),
                       (dict(boundary_pos=0x3000), 1), (dict(snapshots=0x3000), 1),
@@ -129,6 +129,9 @@ def test_workspace_size_and_validation(kda):
     assert L.kda_prefill(ctypes.byref(good), None, ws, None) == 3
     assert L.kda_prefill(ctypes.byref(good), 0x4000, ws - 256, None) == 3
     assert L.kda_prefill(ctypes.byref(good), 0x4010, ws, None) == 3
+    # heads of 256 channels are taken (the CUDA-core path's blocked kernel)
+    wide = _args(kda, dk=256, dv=256)
+    assert L.kda_prefill_workspace_size(ctypes.byref(wide)) > ws
     # the workspace grows with tokens, sequences and boundaries
     big = _args(kda, total_tokens=8192)
     assert L.kda_prefill_workspace_size(ctypes.byref(big)) > ws
@@ -206,6 +209,11 @@ def test_layer_args_validation(kda):
     d.state = 0x3000
     d.layer = ctypes.pointer(layer(conv_width=7))
     assert L.kda_decode_step(ctypes.byref(d), None) == 1
+    # the convolution in decode needs dk * dv <= 128 * 128 (wider heads run as
+    # several CTAs per row and head, which would race on an in-place window)
+    d.dk = d.dv = 256
+    d.layer = ctypes.pointer(layer())
+    assert L.kda_decode_step(ctypes.byref(d), None) == 2
 
 
 def test_decode_and_prep_validation(kda):

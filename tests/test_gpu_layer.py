@@ -114,7 +114,8 @@ def check(p, ref, dtype, what, snaps=True):
         np.testing.assert_array_equal(host(p.conv_window_out[t]), rwin[t], err_msg=f"{what} window {t}")
 
 
-@pytest.mark.parametrize("dtype,dk,dv", [("bf16", 128, 128), ("f32", 64, 64), ("f32", 32, 16)])
+@pytest.mark.parametrize("dtype,dk,dv", [("bf16", 128, 128), ("f32", 64, 64), ("f32", 32, 16),
+                                         ("bf16", 256, 256)])
 def test_prefill_conv_gate_varlen(dtype, dk, dv):
     lens = [1, 2, 3, 61, 130, 200]
     inp, li = case(lens, 4, dk, dv, dtype, seed=300, width=4)

@@ -86,7 +86,8 @@ def assert_close(gpu, ref, tol, what=""):
 
 # ------------------------------------------------------------------ decode (K4)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("dk,dv", [(16, 16), (32, 64), (64, 32), (128, 128), (128, 16)])
+@pytest.mark.parametrize("dk,dv", [(16, 16), (32, 64), (64, 32), (128, 128), (128, 16),
+                                   (256, 256), (256, 16), (64, 256)])
 def test_decode_small(dtype, dk, dv, oracle_mod):
     dw = W.DecodeWorkload("small", 5, 3, dk, dv, 4, 77 + dk + dv)
     inp = W.decode_inputs(dw, dtype=dtype)
@@ -122,7 +123,8 @@ def test_decode_full_size(oracle_mod):
 
 
 # ------------------------------------------------------------------ prep (K1)
-@pytest.mark.parametrize("dtype,dk", [("f32", 64), ("bf16", 64), ("bf16", 128)])
+@pytest.mark.parametrize("dtype,dk", [("f32", 64), ("bf16", 64), ("bf16", 128), ("f32", 256),
+                                      ("bf16", 256)])
 def test_prep(dtype, dk, oracle_mod):
     """bf16 with dk = 128 takes the vectorised kernel: its 64-token tiles
     start mid-chunk and mid-sequence here (lengths 5, 64, 130, ...)."""
@@ -154,7 +156,7 @@ def test_prefill_tiny_f32():
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 32), (16, 128)])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 32), (16, 128), (256, 256), (256, 64), (32, 256)])
 def test_prefill_ragged_varlen(dtype, dk, dv):
     """Ragged tails and lengths around the chunk size, initial states,
     snapshots every 64 tokens plus interior boundaries, scale != 1."""

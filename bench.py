@@ -294,6 +294,49 @@ def bench_layer_steps(torch, kda, W, dev, steps=10):
                            zip(("plan", "intra_chunk", "inter_chunk_and_windows"), phase)}}
 
 
+def bench_wide_heads(torch, kda, W, dev, steps=5):
+    """Heads of 256 channels (dk = dv = 256, bf16, fp32 state), which run on
+    the CUDA-core path: a prefill of one 8192-token sequence with 16 heads
+    (the same token-head bytes per channel as prefill_8k's 32 heads of 128)
+    and a decode step of 64 rows x 16 heads (256 KB of state per head, read
+    and written once: 2.15 GB a step).  L2 flushed before every call."""
+    w = W.PrefillWorkload("wide_prefill", (8192,), 1, 16, 256, 256, "bf16", 1005)
+    inp = W.prefill_inputs(w, device=dev, gen_device=dev)
+    p = kda.Prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["b"], inp["cu_seqlens"],
+                    host_cu_seqlens=inp["cu_seqlens"].cpu())
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ms = []
+        for _ in range(steps):
+            flush_l2(flush)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return sum(ms) / len(ms)
+
+    t_pre = timed(p.run)
+    assert p.device_status() == 0
+    del p, inp
+    dw = W.DecodeWorkload("wide_decode", 64, 16, 256, 256, 1, 1006)
+    di = W.decode_inputs(dw, device=dev, gen_device=dev)
+    state = di["state"]
+    x = [di[k][0] for k in "qkvgb"]
+    o = torch.empty(64, 16, 256, dtype=x[0].dtype, device=dev)
+    t_dec = timed(lambda: kda.kda_decode_step(*x, state, o))
+    state_bytes = 2 * 64 * 16 * 256 * 256 * 4
+    return {"workload": "dk = dv = 256, bf16: prefill of one 8192-token sequence x 16 heads; "
+                        "decode of 64 rows x 16 heads",
+            "prefill_ms": t_pre, "prefill_tokens_per_s": 8192 / (t_pre * 1e-3),
+            "decode_us": t_dec * 1e3, "decode_state_gbs": state_bytes / (t_dec * 1e-3) / 1e9,
+            "steps": steps}
+
+
 def bench_varlen(torch, kda, W, dev, steps=10):
     """The varlen configuration: 8 packed sequences of U[1024, 32768] tokens,
     H=32, d=128, bf16, seeded fp32 initial states, fp32 snapshots every 4096
@@ -501,6 +544,9 @@ def gpu_arm(a):
     if a.layer_only:
         print(json.dumps(bench_layer_steps(torch, kda, W, dev, steps=a.steps)))
         return
+    if a.wide_only:
+        print(json.dumps(bench_wide_heads(torch, kda, W, dev, steps=a.steps)))
+        return
     with ClockSampler(local) as clk:
         pre = bench_prefill(torch, kda, W, a.steps, a.warmup, dev)
         barrier()
@@ -520,6 +566,7 @@ def gpu_arm(a):
     vl = bench_varlen(torch, kda, W, dev) if rank == 0 else None
     gph = bench_gate_per_head(torch, kda, W, dev) if rank == 0 else None
     lay = bench_layer_steps(torch, kda, W, dev) if rank == 0 else None
+    wide = bench_wide_heads(torch, kda, W, dev) if rank == 0 else None
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -593,6 +640,7 @@ def gpu_arm(a):
         "prefill_varlen": vl,
         "prefill_gate_per_head": gph,
         "prefill_layer_steps": lay,
+        "wide_heads": wide,
         "segment_scan": scan,
         **({"prefill_1m": m1} if m1 else {}),
         "prep": dict(prep, peak=pk["hbm_gbs"], frac=prep["achieved_gbs"] / pk["hbm_gbs"],
@@ -657,6 +705,8 @@ def main():
                     help="time the prefill workload alone (for profiler captures)")
     ap.add_argument("--layer-only", action="store_true",
                     help="time the prefill with the layer steps alone (for profiler captures)")
+    ap.add_argument("--wide-only", action="store_true",
+                    help="time the 256-channel heads alone")
     a = ap.parse_args()
     if a.warmup < 3:
         a.warmup = 3

@@ -295,15 +295,12 @@ def bench_layer_steps(torch, kda, W, dev, steps=10):
 
 
 def bench_wide_heads(torch, kda, W, dev, steps=5):
-    """Heads of 256 channels (dk = dv = 256, bf16, fp32 state), which run on
-    the CUDA-core path: a prefill of one 8192-token sequence with 16 heads
-    (the same token-head bytes per channel as prefill_8k's 32 heads of 128)
-    and a decode step of 64 rows x 16 heads (256 KB of state per head, read
-    and written once: 2.15 GB a step).  L2 flushed before every call."""
-    w = W.PrefillWorkload("wide_prefill", (8192,), 1, 16, 256, 256, "bf16", 1005)
-    inp = W.prefill_inputs(w, device=dev, gen_device=dev)
-    p = kda.Prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["b"], inp["cu_seqlens"],
-                    host_cu_seqlens=inp["cu_seqlens"].cpu())
+    """Head sizes other than 128 (bf16, fp32 state).  64 channels: a prefill
+    of one 8192-token sequence with 32 heads, on the tensor-core kernels
+    zero-padded to 128.  256 channels, on the CUDA-core path: a prefill of one
+    8192-token sequence with 16 heads and a decode step of 64 rows x 16 heads
+    (256 KB of state per head, read and written once: 2.15 GB a step).  L2
+    flushed before every call."""
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
     def timed(fn):
@@ -320,9 +317,17 @@ def bench_wide_heads(torch, kda, W, dev, steps=5):
             ms.append(e0.elapsed_time(e1))
         return sum(ms) / len(ms)
 
-    t_pre = timed(p.run)
-    assert p.device_status() == 0
-    del p, inp
+    def prefill_ms(H, d):
+        w = W.PrefillWorkload("head_sizes", (8192,), 1, H, d, d, "bf16", 1005)
+        inp = W.prefill_inputs(w, device=dev, gen_device=dev)
+        p = kda.Prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["b"], inp["cu_seqlens"],
+                        host_cu_seqlens=inp["cu_seqlens"].cpu())
+        t = timed(p.run)
+        assert p.device_status() == 0
+        return t
+
+    t64 = prefill_ms(32, 64)
+    t_pre = prefill_ms(16, 256)
     dw = W.DecodeWorkload("wide_decode", 64, 16, 256, 256, 1, 1006)
     di = W.decode_inputs(dw, device=dev, gen_device=dev)
     state = di["state"]
@@ -330,8 +335,10 @@ def bench_wide_heads(torch, kda, W, dev, steps=5):
     o = torch.empty(64, 16, 256, dtype=x[0].dtype, device=dev)
     t_dec = timed(lambda: kda.kda_decode_step(*x, state, o))
     state_bytes = 2 * 64 * 16 * 256 * 256 * 4
-    return {"workload": "dk = dv = 256, bf16: prefill of one 8192-token sequence x 16 heads; "
-                        "decode of 64 rows x 16 heads",
+    return {"workload": "bf16; dk = dv = 64: prefill of one 8192-token sequence x 32 heads "
+                        "(tensor cores, zero-padded); dk = dv = 256: prefill of one 8192-token "
+                        "sequence x 16 heads, decode of 64 rows x 16 heads (CUDA cores)",
+            "d64_prefill_ms": t64, "d64_prefill_tokens_per_s": 8192 / (t64 * 1e-3),
             "prefill_ms": t_pre, "prefill_tokens_per_s": 8192 / (t_pre * 1e-3),
             "decode_us": t_dec * 1e3, "decode_state_gbs": state_bytes / (t_dec * 1e-3) / 1e9,
             "steps": steps}

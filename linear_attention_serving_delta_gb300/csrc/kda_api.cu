@@ -24,11 +24,17 @@ bool layer_aligned16(const kda_layer_args* l) {
 
 // The tensor-core kernels move q, k, g, v, o and the states with 16-byte
 // vector accesses; other layouts take the fp32 CUDA-core path.
-// The tensor-core path: bf16, dk = dv = 128, 16-byte aligned buffers, and
-// token indices that fit the int32 coordinates of its tensor-map copies.
+// The tensor-core path: bf16, heads of up to 128 channels (a narrower head
+// runs zero-padded to 128: its tensor-map copies fill the missing channels
+// with zeros, which changes no product, and the outputs keep the caller's
+// layout; dv a multiple of the inter-chunk kernel's 32-column slice),
+// 16-byte aligned buffers, and token indices that fit the int32 coordinates
+// of its tensor-map copies.  The short convolution's staging is laid out for
+// 128 channels: with it, only 128 x 128 heads.
 bool use_tensor_cores(const kda_prefill_args* a) {
-  return kHaveTensorCorePath && a->in_dtype == KDA_BF16 && a->dk == 128 && a->dv == 128 &&
-         a->total_tokens < ((int64_t)1 << 31) &&
+  const bool conv = a->layer && a->layer->conv_width > 0;
+  return kHaveTensorCorePath && a->in_dtype == KDA_BF16 && a->dk <= 128 && a->dv >= 32 && a->dv <= 128 &&
+         (!conv || (a->dk == 128 && a->dv == 128)) && a->total_tokens < ((int64_t)1 << 31) &&
          aligned16(a->q) && aligned16(a->k) && aligned16(a->v) && aligned16(a->g) &&
          aligned16(a->o) && aligned16(a->initial_state) && aligned16(a->final_state) &&
          aligned16(a->snapshots) && layer_aligned16(a->layer);
@@ -67,7 +73,8 @@ constexpr int32_t kScanSms = 152;  // SMs of the part the automatic choice is si
 // Segments of the segment scan for these arguments (host-side fields only):
 // 1 = no scan.  See kda.h.
 int32_t scan_segments_of(const kda_prefill_args* a) {
-  if (!use_tensor_cores(a) || a->num_seqs != 1 || a->snapshot_interval != 0 || a->boundary_pos ||
+  if (!use_tensor_cores(a) || a->dk != 128 || a->dv != 128 || a->num_seqs != 1 ||
+      a->snapshot_interval != 0 || a->boundary_pos ||
       a->snapshots || a->scan_segments == 1)
     return 1;
   const int64_t nch = (a->total_tokens + kChunk - 1) / kChunk;

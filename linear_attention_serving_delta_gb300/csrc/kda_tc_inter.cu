@@ -148,7 +148,7 @@ __device__ __forceinline__ GateRow load_gate_row(const ChunkParams& p, const Chu
     if (p.out_gate_per_head) {
       g.r[0].x = (uint32_t)__bfloat16_as_ushort(r[row]);
     } else {
-      const uint4* rg = reinterpret_cast<const uint4*>(r + row * (int64_t)kD + n0 + h16);
+      const uint4* rg = reinterpret_cast<const uint4*>(r + row * (int64_t)p.dv + n0 + h16);
 #pragma unroll
       for (int q8 = 0; q8 < kNh / 8; ++q8) g.r[q8] = __ldg(rg + q8);
     }
@@ -167,7 +167,7 @@ __device__ __forceinline__ void store_output(const ChunkParams& p, const Chunk& 
     const float scale = p.scale;
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o);
     const int64_t row = (ch.tok0 + i) * p.H + h;
-    uint4* dst = reinterpret_cast<uint4*>(o + row * (int64_t)kD + n0 + h16);
+    uint4* dst = reinterpret_cast<uint4*>(o + row * (int64_t)p.dv + n0 + h16);
     if (p.out_gate)
 #pragma unroll
       for (int n = 0; n < kNh; ++n) d[n] *= gf.f[n];
@@ -278,14 +278,19 @@ tc_inter(ChunkParams p) {
 
   bool ok = true;
   bool okl = true;  // this thread's own waits succeeded
-  // initial state: the operand holds S_0, TMEM Gamma_L(0) S_0
-  const size_t sbase = ((size_t)s * H + h) * kD * kD;
+  // initial state: the operand holds S_0, TMEM Gamma_L(0) S_0.  States are
+  // [dk][dv] in global memory; a head narrower than 128 channels (dk or dv =
+  // 64) runs zero-padded: key rows c >= dk hold zeros and are never written,
+  // and the grid covers only the dv / kNs column slices that exist.
+  const int DK = p.dk, DV = p.dv;
+  const bool row_live = c < DK;
+  const size_t sbase = ((size_t)s * H + h) * DK * DV;
   {
     float v[kNh];
 #pragma unroll
     for (int n = 0; n < kNh; n += 4) {
-      float4 x = p.initial_state && !pass1
-                     ? *reinterpret_cast<const float4*>(p.initial_state + sbase + (size_t)c * kD + n0 + h16 + n)
+      float4 x = p.initial_state && !pass1 && row_live
+                     ? *reinterpret_cast<const float4*>(p.initial_state + sbase + (size_t)c * DV + n0 + h16 + n)
                      : make_float4(0.f, 0.f, 0.f, 0.f);
       v[n] = x.x; v[n + 1] = x.y; v[n + 2] = x.z; v[n + 3] = x.w;
     }
@@ -419,8 +424,8 @@ tc_inter(ChunkParams p) {
     {
       float v[kNh];
       tmem_ld_sum(DS, h16, v);
-      if (ch.snap_slot >= 0 && p.snapshots && !pass1) {
-        float* dst = p.snapshots + ((size_t)ch.snap_slot * H + h) * kD * kD + (size_t)c * kD + n0 + h16;
+      if (ch.snap_slot >= 0 && p.snapshots && !pass1 && row_live) {
+        float* dst = p.snapshots + ((size_t)ch.snap_slot * H + h) * DK * DV + (size_t)c * DV + n0 + h16;
 #pragma unroll
         for (int n = 0; n < kNh; n += 4)
           *reinterpret_cast<float4*>(dst + n) = make_float4(v[n], v[n + 1], v[n + 2], v[n + 3]);
@@ -460,11 +465,12 @@ tc_inter(ChunkParams p) {
   float* const fin = trans ? p.trans : p.final_state;
   if (ok && fin) {
     float v[kNh];
-    tmem_ld_sum(DS, h16, v);
-    float* dst = fin + sbase + (size_t)c * kD + n0 + h16;
+    tmem_ld_sum(DS, h16, v);  // warp-collective: outside the row test
+    float* dst = fin + sbase + (size_t)c * DV + n0 + h16;
+    if (row_live)
 #pragma unroll
-    for (int n = 0; n < kNh; n += 4)
-      *reinterpret_cast<float4*>(dst + n) = make_float4(v[n], v[n + 1], v[n + 2], v[n + 3]);
+      for (int n = 0; n < kNh; n += 4)
+        *reinterpret_cast<float4*>(dst + n) = make_float4(v[n], v[n + 1], v[n + 2], v[n + 3]);
   }
   if (!ok) {
     // let the copies and MMAs still in flight finish (each wait bounded)
@@ -512,7 +518,7 @@ cudaError_t launch_tc_prefill(const ChunkParams& p, cudaStream_t stream, cudaEve
     e = cudaEventRecord(mid, stream);
     if (e != cudaSuccess) return e;
   }
-  return run_inter(p, dim3((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)(kD / kNs)), stream);
+  return run_inter(p, dim3((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)(p.dv / kNs)), stream);
 }
 
 namespace {

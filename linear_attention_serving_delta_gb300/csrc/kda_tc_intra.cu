@@ -877,13 +877,15 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// [T][H][128] bf16 rows, box {128 channels, 1 head, `rows` tokens}, zero fill
-// outside [0, T)
-bool encode_rows(CUtensorMap* m, const void* base, int H, int64_t T, uint32_t rows = 64) {
+// [T][H][D] bf16 rows, box {128 channels, 1 head, `rows` tokens}, zero fill
+// outside [0, T) and, for a head of D = 64 channels, in channels 64-127: the
+// kernel then runs on the head zero-padded to 128 channels, which leaves
+// every product of q^, k^ and v unchanged
+bool encode_rows(CUtensorMap* m, const void* base, int H, int64_t T, int D, uint32_t rows = 64) {
   const EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
-  const cuuint64_t dims[3] = {kD, (cuuint64_t)H, (cuuint64_t)T};
-  const cuuint64_t strides[2] = {kD * 2, (cuuint64_t)H * kD * 2};
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
   const cuuint32_t box[3] = {kD, 1, rows};
   const cuuint32_t elem[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
@@ -905,13 +907,13 @@ cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream) {
   if (e != cudaSuccess || p.max_chunks == 0 || p.total_tokens == 0) return e;
   RowMaps maps;
   // with a gate per head there are no g rows to stage (the g map is not used)
-  if (!encode_rows(&maps.g, head ? p.k : p.g, p.H, p.total_tokens) ||
-      !encode_rows(&maps.q, p.q, p.H, p.total_tokens) || !encode_rows(&maps.k, p.k, p.H, p.total_tokens) ||
-      !encode_rows(&maps.v, p.v, p.H, p.total_tokens))
+  const int64_t T = p.total_tokens;
+  if (!encode_rows(&maps.g, head ? p.k : p.g, p.H, T, p.dk) || !encode_rows(&maps.q, p.q, p.H, T, p.dk) ||
+      !encode_rows(&maps.k, p.k, p.H, T, p.dk) || !encode_rows(&maps.v, p.v, p.H, T, p.dv))
     return cudaErrorInvalidValue;
-  if (conv && (!encode_rows(&maps.qh, p.q, p.H, p.total_tokens, kHaloRows) ||
-               !encode_rows(&maps.kh, p.k, p.H, p.total_tokens, kHaloRows) ||
-               !encode_rows(&maps.vh, p.v, p.H, p.total_tokens, kHaloRows)))
+  if (conv && (!encode_rows(&maps.qh, p.q, p.H, T, p.dk, kHaloRows) ||
+               !encode_rows(&maps.kh, p.k, p.H, T, p.dk, kHaloRows) ||
+               !encode_rows(&maps.vh, p.v, p.H, T, p.dv, kHaloRows)))
     return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);

@@ -129,6 +129,13 @@ def test_workspace_size_and_validation(kda):
     assert L.kda_prefill(ctypes.byref(good), None, ws, None) == 3
     assert L.kda_prefill(ctypes.byref(good), 0x4000, ws - 256, None) == 3
     assert L.kda_prefill(ctypes.byref(good), 0x4010, ws, None) == 3
+    # bf16 heads of 64 channels take the tensor-core path (zero-padded to 128:
+    # its 90,624-byte record per chunk-head), fp32 ones the CUDA-core path
+    # (82,176 bytes): 2 chunk-table entries (64 tokens + one per sequence) x 2 heads
+    tcp = _args(kda, in_dtype=kda.KDA_BF16, dk=64, dv=64)
+    cup = _args(kda, dk=64, dv=64)
+    assert (L.kda_prefill_workspace_size(ctypes.byref(tcp)) -
+            L.kda_prefill_workspace_size(ctypes.byref(cup))) == 2 * 2 * (90624 - 82176)
     # heads of 256 channels are taken (the CUDA-core path's blocked kernel)
     wide = _args(kda, dk=256, dv=256)
     assert L.kda_prefill_workspace_size(ctypes.byref(wide)) > ws

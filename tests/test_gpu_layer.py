@@ -141,6 +141,31 @@ def test_prefill_conv_variants_tc(width, silu, windows, gate_mode, head_gate):
     check(p, ref, "bf16", f"W={width} silu={silu} win={windows} gate={gate_mode} hg={head_gate}")
 
 
+def test_output_gate_on_padded_heads():
+    """bf16 heads of 64 channels run on the tensor-core kernels zero-padded
+    to 128; the output gate (per channel and per head) rides on their store
+    with the caller's 64-column layout."""
+    lens = [70, 3, 129]
+    for mode in ("channel", "head"):
+        inp, li = case(lens, 2, 64, 64, "bf16", seed=325, width=1, gate_mode=mode)
+        li["taps"] = None
+        d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+        p = kda.Prefill(d["q"], d["k"], d["v"], d["g"], d["b"], d["cu_seqlens"],
+                        initial_state=d["S0"], snapshot_interval=64,
+                        host_cu_seqlens=inp["cu_seqlens"], out_gate=li["gate"].cuda()).run()
+        torch.cuda.synchronize()
+        from oracle import layer
+        import oracle
+        sp, cs = oracle.snapshot_positions(lens, 64)
+        ro, rS, rsn, _ = layer.prefill_layer(
+            host(inp["q"]), host(inp["k"]), host(inp["v"]), host(inp["g"]), host(inp["b"]),
+            inp["cu_seqlens"].numpy(), out_gate=host(li["gate"]), S0=host(inp["S0"]),
+            snap_pos=sp, cu_snap=cs)
+        assert rel(host(p.o), ro) <= TOL["bf16"], mode
+        assert rel(host(p.final_state), rS) <= TOL["bf16"], mode
+        assert rel(host(p.snapshot_view), rsn) <= TOL["bf16"], mode
+
+
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 32)])
 def test_prefill_windows_in_place(dtype, d):
     lens = [2, 90, 1]

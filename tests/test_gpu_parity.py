@@ -156,7 +156,8 @@ def test_prefill_tiny_f32():
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 32), (16, 128), (256, 256), (256, 64), (32, 256)])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 32), (16, 128), (256, 256), (256, 64), (32, 256),
+                                   (64, 64), (128, 64), (64, 128)])
 def test_prefill_ragged_varlen(dtype, dk, dv):
     """Ragged tails and lengths around the chunk size, initial states,
     snapshots every 64 tokens plus interior boundaries, scale != 1."""
@@ -447,7 +448,7 @@ def head_gate(inp):
     return gh, gh[:, :, None].expand(inp["g"].shape).contiguous()
 
 
-@pytest.mark.parametrize("dtype,dk,dv", [("bf16", 128, 128), ("f32", 64, 32)])
+@pytest.mark.parametrize("dtype,dk,dv", [("bf16", 128, 128), ("f32", 64, 32), ("bf16", 64, 64)])
 def test_prefill_gate_per_head(dtype, dk, dv):
     """g given per (token, head) -- the gated delta rule -- equals the oracle
     with that value in every channel, and the per-channel kernels on the

@@ -211,9 +211,12 @@ size_t kda_prefill_workspace_size(const kda_prefill_args* args);
 /* Runs the prefill.  ws: device buffer of at least
  * kda_prefill_workspace_size(args) bytes, 256-byte aligned, owned by the
  * caller and not used by another call in flight.  The path is chosen by the
- * arguments: bf16 inputs with dk = dv = 128 run on the tcgen05 tensor-core
- * kernels; every other supported shape runs on fp32 CUDA-core kernels
- * (heads of 256 channels on a variant that takes 128 channels at a time). */
+ * arguments: bf16 inputs with dk <= 128 and dv in {32, 64, 128} run on the
+ * tcgen05 tensor-core kernels (a head narrower than 128 channels runs
+ * zero-padded to 128, at the cost of a 128-channel head; with the short
+ * convolution only dk = dv = 128); every other supported shape runs on fp32
+ * CUDA-core kernels (heads of 256 channels on a variant that takes 128
+ * channels at a time). */
 kda_status_t kda_prefill(const kda_prefill_args* args, void* ws, size_t ws_bytes,
                          void* stream);
 

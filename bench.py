@@ -328,6 +328,16 @@ def bench_wide_heads(torch, kda, W, dev, steps=5):
 
     t64 = prefill_ms(32, 64)
     t_pre = prefill_ms(16, 256)
+
+    def decode_us(B, H, d):
+        dw = W.DecodeWorkload("head_sizes_decode", B, H, d, d, 1, 1006)
+        di = W.decode_inputs(dw, device=dev, gen_device=dev)
+        x = [di[k][0] for k in "qkvgb"]
+        o = torch.empty(B, H, d, dtype=x[0].dtype, device=dev)
+        st = di["state"]
+        return timed(lambda: kda.kda_decode_step(*x, st, o)) * 1e3
+
+    t_d64 = decode_us(1024, 32, 64)
     dw = W.DecodeWorkload("wide_decode", 64, 16, 256, 256, 1, 1006)
     di = W.decode_inputs(dw, device=dev, gen_device=dev)
     state = di["state"]
@@ -339,6 +349,8 @@ def bench_wide_heads(torch, kda, W, dev, steps=5):
                         "(tensor cores, zero-padded); dk = dv = 256: prefill of one 8192-token "
                         "sequence x 16 heads, decode of 64 rows x 16 heads (CUDA cores)",
             "d64_prefill_ms": t64, "d64_prefill_tokens_per_s": 8192 / (t64 * 1e-3),
+            "d64_decode_workload": "1024 rows x 32 heads of 64 x 64 fp32 state (1.07 GB a step)",
+            "d64_decode_us": t_d64, "d64_decode_state_gbs": 2 * 1024 * 32 * 64 * 64 * 4 / (t_d64 * 1e-6) / 1e9,
             "prefill_ms": t_pre, "prefill_tokens_per_s": 8192 / (t_pre * 1e-3),
             "decode_us": t_dec * 1e3, "decode_state_gbs": state_bytes / (t_dec * 1e-3) / 1e9,
             "steps": steps}

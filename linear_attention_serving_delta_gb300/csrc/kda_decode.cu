@@ -224,10 +224,12 @@ decode_step(kda_decode_args a, const kda_layer_args l) {
   }
 }
 
-// ------------------------------------------------------------ dk = dv = 128
+// ------------------------------------------------- dk, dv in {64, 128}
 // Persistent variant: one CTA per SM walks (row, head) items.  A ring of
-// kStages shared-memory slots is filled by 1-D bulk copies (TMA engine) of
-// each item's 64 KB state plus its q, k, g, v rows, kStages items ahead.
+// shared-memory slots is filled by 1-D bulk copies (TMA engine) of each
+// item's state (64 KB for 128 x 128) plus its q, k, g, v rows, a few items
+// ahead (3 slots for 128 x 128, up to 8 for smaller states, so that about
+// 200 KB stay in flight per SM).
 // Warps 0-7 compute; warp 8 is the producer: once the compute warps have
 // written an item's updated state into its slot, it sends the state back to
 // HBM with one 64 KB bulk copy, waits for that copy to read the slot and
@@ -236,25 +238,53 @@ decode_step(kda_decode_args a, const kda_layer_args l) {
 //
 // The compute warps need no token-preparation phase: with raw q, k,
 // p = S'^T k^ = ik (S'^T k) and S'^T q^ = iq (S'^T q) (ik, iq the inverse
-// norms), so each warp reads q, k and g of its own 16 key channels straight
-// from the slot, and the norms' partial sums travel with the reduction
-// partials through the one barrier of the item.
-constexpr int kStages = 3;
+// norms), so each warp reads q, k and g of its own DK / 8 key channels
+// straight from the slot, and the norms' partial sums travel with the
+// reduction partials through the one barrier of the item.
 constexpr int kRingThreads = 256;            // compute warps 0-7
 constexpr int kRingAllThreads = kRingThreads + 32;  // + the producer warp
 constexpr int kComputeBarrier = 1;           // named barrier of warps 0-7
-constexpr uint32_t kStateBytes = 128 * 128 * 4;
 
 // A slot: the state, the q, k, g, v rows and, with the short convolution,
-// up to KDA_CONV_MAX - 1 window rows of each of q, k, v
+// up to KDA_CONV_MAX - 1 window rows of each of q, k, v.  Warp w owns key
+// rows w + 8 i (i < RPW), lane l value columns CPL l .. CPL l + CPL - 1.
 constexpr int kWinRows = KDA_CONV_MAX - 1;
-template <typename TIn, bool kConv>
+template <typename TIn, bool kConv, int DK, int DV>
 struct Ring {
-  static constexpr uint32_t ROW = 128 * sizeof(TIn);  // one q / k / g / v row
-  static constexpr uint32_t WIN = kStateBytes + 4 * ROW;  // window row m of tensor t at WIN + (3 m + t) ROW
-  static constexpr uint32_t STAGE = WIN + (kConv ? 3 * kWinRows * ROW : 0);
-  static constexpr uint32_t BYTES = kStages * STAGE;
+  static_assert((DK == 64 || DK == 128) && (DV == 64 || DV == 128), "ring head sizes");
+  static constexpr int RPW = DK / 8, CPL = DV / 32;
+  static constexpr uint32_t STATE = DK * DV * 4;
+  static constexpr uint32_t RK = DK * sizeof(TIn), RV = DV * sizeof(TIn);  // a q / k / g row, a v row
+  static constexpr uint32_t QO = STATE, KO = QO + RK, GO = KO + RK, VO = GO + RK;
+  static constexpr uint32_t RW = RK > RV ? RK : RV;
+  static constexpr uint32_t WIN = VO + RV;  // window row m of tensor t at WIN + (3 m + t) RW
+  static constexpr uint32_t STAGE = WIN + (kConv ? 3 * kWinRows * RW : 0);
+  // 64 x 64 states (16 KB) run two CTAs per SM: an item's fixed costs (two
+  // barriers, the reductions) then overlap with the other CTA's
+  static constexpr int CTAS = STATE <= 16384 ? 2 : 1;
+  static constexpr uint32_t BUDGET = CTAS == 2 ? 96000 : 200000;
+  static constexpr int STAGES = BUDGET / STAGE < 3 ? 3 : (BUDGET / STAGE > 8 ? 8 : BUDGET / STAGE);
+  static constexpr uint32_t BYTES = STAGES * STAGE;
 };
+
+// CPL consecutive floats (one 8- or 16-byte access)
+template <int CPL>
+__device__ __forceinline__ void ld_cols(const float* p, float* x) {
+  if constexpr (CPL == 4) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  } else {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    x[0] = v.x; x[1] = v.y;
+  }
+}
+template <int CPL>
+__device__ __forceinline__ void st_cols(float* p, const float* x) {
+  if constexpr (CPL == 4)
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+  else
+    *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
+}
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
@@ -274,7 +304,7 @@ __device__ __forceinline__ bool bar_and(int id, int n, bool v) {
   return r != 0;
 }
 
-template <typename TIn, bool kConv>
+template <typename TIn, bool kConv, int DK, int DV>
 __device__ __forceinline__ void ring_issue(const kda_decode_args& a, const kda_layer_args& l, uint8_t* stage,
                                            uint64_t* bar, int32_t* valid_flag, int64_t item) {
   const int H = a.num_heads;
@@ -286,45 +316,45 @@ __device__ __forceinline__ void ring_issue(const kda_decode_args& a, const kda_l
     mbar_arrive(bar);
     return;
   }
-  using R = Ring<TIn, kConv>;
-  constexpr uint32_t ROW = R::ROW;
+  using R = Ring<TIn, kConv, DK, DV>;
   // (with a gate per head there is no g row: the compute warps read its one value)
-  uint32_t bytes = kStateBytes + (a.gate_per_head ? 3 : 4) * ROW;
+  uint32_t bytes = R::STATE + (a.gate_per_head ? 2 : 3) * R::RK + R::RV;
   const int nw = kConv ? l.conv_width - 1 : 0;  // window rows per tensor
   if (kConv)
     for (int t = 0; t < 3; ++t)
-      if (l.conv_in[t]) bytes += nw * ROW;
+      if (l.conv_in[t]) bytes += nw * (t == 2 ? R::RV : R::RK);
   tc::mbar_arrive_expect_tx(bar, bytes);
-  const int64_t e = ((int64_t)row * H + h) * 128;
-  tc::bulk_g2s(stage, a.state + ((size_t)slot * H + h) * 128 * 128, kStateBytes, bar);
-  tc::bulk_g2s(stage + kStateBytes, static_cast<const TIn*>(a.q) + e, ROW, bar);
-  tc::bulk_g2s(stage + kStateBytes + ROW, static_cast<const TIn*>(a.k) + e, ROW, bar);
-  if (!a.gate_per_head)
-    tc::bulk_g2s(stage + kStateBytes + 2 * ROW, static_cast<const TIn*>(a.g) + e, ROW, bar);
-  tc::bulk_g2s(stage + kStateBytes + 3 * ROW, static_cast<const TIn*>(a.v) + e, ROW, bar);
+  const int64_t ek = ((int64_t)row * H + h) * DK, ev = ((int64_t)row * H + h) * DV;
+  tc::bulk_g2s(stage, a.state + ((size_t)slot * H + h) * DK * DV, R::STATE, bar);
+  tc::bulk_g2s(stage + R::QO, static_cast<const TIn*>(a.q) + ek, R::RK, bar);
+  tc::bulk_g2s(stage + R::KO, static_cast<const TIn*>(a.k) + ek, R::RK, bar);
+  if (!a.gate_per_head) tc::bulk_g2s(stage + R::GO, static_cast<const TIn*>(a.g) + ek, R::RK, bar);
+  tc::bulk_g2s(stage + R::VO, static_cast<const TIn*>(a.v) + ev, R::RV, bar);
   if (kConv)
     for (int t = 0; t < 3; ++t)
-      if (l.conv_in[t])
+      if (l.conv_in[t]) {
+        const int d = t == 2 ? DV : DK;
         for (int m = 0; m < nw; ++m)
-          tc::bulk_g2s(stage + R::WIN + (3 * m + t) * ROW,
-                       static_cast<const TIn*>(l.conv_in[t]) + (((int64_t)slot * nw + m) * H + h) * 128, ROW,
-                       bar);
+          tc::bulk_g2s(stage + R::WIN + (3 * m + t) * R::RW,
+                       static_cast<const TIn*>(l.conv_in[t]) + (((int64_t)slot * nw + m) * H + h) * d,
+                       d * (uint32_t)sizeof(TIn), bar);
+      }
 }
 
 // kPoll: the instantiation for wait limits under kPollLimitNs (the give-up
 // test).  kConv: the short convolution (window rows in the slot).
-template <typename TIn, bool kPoll, bool kConv>
-__global__ void __launch_bounds__(kRingAllThreads, 1)
+template <typename TIn, bool kPoll, bool kConv, int DK, int DV>
+__global__ void __launch_bounds__(kRingAllThreads, (DK * DV <= 64 * 64) ? 2 : 1)
 decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
-  using R = Ring<TIn, kConv>;
+  using R = Ring<TIn, kConv, DK, DV>;
+  constexpr int kStages = R::STAGES, RPW = R::RPW, CPL = R::CPL;
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ __align__(8) uint64_t full[kStages];  // slot loaded
   __shared__ __align__(8) uint64_t done[kStages];  // slot's state updated by warps 0-7
   __shared__ int32_t valid_flag[kStages];
-  __shared__ __align__(16) float red_p[2][8][128];
-  __shared__ __align__(16) float red_o[2][8][128];
+  __shared__ __align__(16) float red_p[2][8][DV];
+  __shared__ __align__(16) float red_o[2][8][DV];
   __shared__ __align__(16) float part[2][8][4];    // per warp: sum q^2, sum k^2, sum q k
-  constexpr uint32_t ROW = R::ROW;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.num_heads;
   const int64_t first = blockIdx.x, stride = gridDim.x;
@@ -345,8 +375,8 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
     if (lane == 0) {
       int64_t issued = 0;  // items whose slot copies were issued
       for (; issued < kStages && issued < n_local; ++issued)
-        ring_issue<TIn, kConv>(a, l, sm + issued * R::STAGE, &full[issued], &valid_flag[issued],
-                               first + issued * stride);
+        ring_issue<TIn, kConv, DK, DV>(a, l, sm + issued * R::STAGE, &full[issued], &valid_flag[issued],
+                                       first + issued * stride);
       for (int64_t k = 0; k < n_local; ++k) {
         const int st = (int)(k % kStages);
         uint8_t* stage = sm + st * R::STAGE;
@@ -362,12 +392,12 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
         if (valid_flag[st]) {
           const int row = (int)(item / H), h = (int)(item % H);
           const int slot = a.state_slots ? a.state_slots[row] : row;
-          tc::bulk_s2g(a.state + ((size_t)slot * H + h) * 128 * 128, stage, kStateBytes);
+          tc::bulk_s2g(a.state + ((size_t)slot * H + h) * DK * DV, stage, R::STATE);
           tc::bulk_commit();
           tc::bulk_wait_read_all();
         }
         if (k + kStages < n_local) {
-          ring_issue<TIn, kConv>(a, l, stage, &full[st], &valid_flag[st], item + kStages * stride);
+          ring_issue<TIn, kConv, DK, DV>(a, l, stage, &full[st], &valid_flag[st], item + kStages * stride);
           issued = k + kStages + 1;
         }
       }
@@ -376,7 +406,7 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
     return;
   }
 
-  // ---- compute warps 0-7; warp w owns key channels (rows) w + 8 i, i < 16
+  // ---- compute warps 0-7; warp w owns key channels (rows) w + 8 i, i < RPW
   const TIn* gb = static_cast<const TIn*>(a.b);
   float b_next = n_local > 0 ? ld_in(gb, first) : 0.f;
   for (int64_t k = 0; k < n_local; ++k) {
@@ -396,15 +426,15 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
       }
       continue;
     }
-    const TIn* rq = reinterpret_cast<const TIn*>(stage + kStateBytes);
-    const TIn* rk = reinterpret_cast<const TIn*>(stage + kStateBytes + ROW);
-    const TIn* rg = reinterpret_cast<const TIn*>(stage + kStateBytes + 2 * ROW);
-    const TIn* rv = reinterpret_cast<const TIn*>(stage + kStateBytes + 3 * ROW);
-    // this warp's 16 rows: lane i < 16 holds raw q, k and alpha of row warp + 8 i
+    const TIn* rq = reinterpret_cast<const TIn*>(stage + R::QO);
+    const TIn* rk = reinterpret_cast<const TIn*>(stage + R::KO);
+    const TIn* rg = reinterpret_cast<const TIn*>(stage + R::GO);
+    const TIn* rv = reinterpret_cast<const TIn*>(stage + R::VO);
+    // this warp's RPW rows: lane i < RPW holds raw q, k and alpha of row warp + 8 i
     float xq = 0.f, xk = 0.f, xa = 0.f;
     // with the convolution: window row m of tensor t in the slot (0 without one)
     auto wrow = [&](int t, int m, int c) {
-      return l.conv_in[t] ? ld_in(reinterpret_cast<const TIn*>(stage + R::WIN + (3 * m + t) * ROW), c) : 0.f;
+      return l.conv_in[t] ? ld_in(reinterpret_cast<const TIn*>(stage + R::WIN + (3 * m + t) * R::RW), c) : 0.f;
     };
     int slot = 0;
     if (kConv) {
@@ -412,7 +442,7 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
       slot = a.state_slots ? a.state_slots[row] : row;
     }
     const int hh = (int)(item % H);
-    if (lane < 16) {
+    if (lane < RPW) {
       const int r = warp + 8 * lane;
       xq = ld_in(rq, r);
       xk = ld_in(rk, r);
@@ -420,10 +450,10 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
       if (kConv) {
         auto pq = [&](int m) { return wrow(0, m, r); };
         auto pk = [&](int m) { return wrow(1, m, r); };
-        window_push<TIn>(l, 0, xq, slot, H, hh, r, 128, pq);
-        window_push<TIn>(l, 1, xk, slot, H, hh, r, 128, pk);
-        xq = conv_token<TIn>(l, 0, xq, H, hh, r, 128, pq);
-        xk = conv_token<TIn>(l, 1, xk, H, hh, r, 128, pk);
+        window_push<TIn>(l, 0, xq, slot, H, hh, r, DK, pq);
+        window_push<TIn>(l, 1, xk, slot, H, hh, r, DK, pk);
+        xq = conv_token<TIn>(l, 0, xq, H, hh, r, DK, pq);
+        xk = conv_token<TIn>(l, 1, xk, H, hh, r, DK, pk);
       }
     }
     {
@@ -432,20 +462,24 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
     }
     // retention and the two reductions over this warp's rows (raw q, k)
     const float* S = reinterpret_cast<const float*>(stage);
-    float4 s[16];
-    float4 pp = make_float4(0.f, 0.f, 0.f, 0.f), po = pp;
+    float s[RPW][CPL], pp[CPL], po[CPL];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int j = 0; j < CPL; ++j) pp[j] = po[j] = 0.f;
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
       const int r = warp + 8 * i;
-      s[i] = reinterpret_cast<const float4*>(S + r * 128)[lane];
+      ld_cols<CPL>(S + r * DV + CPL * lane, s[i]);
       const float a_r = __shfl_sync(0xffffffffu, xa, i), k_r = __shfl_sync(0xffffffffu, xk, i),
                   q_r = __shfl_sync(0xffffffffu, xq, i);
-      s[i].x *= a_r; s[i].y *= a_r; s[i].z *= a_r; s[i].w *= a_r;
-      pp.x += k_r * s[i].x; pp.y += k_r * s[i].y; pp.z += k_r * s[i].z; pp.w += k_r * s[i].w;
-      po.x += q_r * s[i].x; po.y += q_r * s[i].y; po.z += q_r * s[i].z; po.w += q_r * s[i].w;
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) {
+        s[i][j] *= a_r;
+        pp[j] += k_r * s[i][j];
+        po[j] += q_r * s[i][j];
+      }
     }
-    *reinterpret_cast<float4*>(&red_p[buf][warp][4 * lane]) = pp;
-    *reinterpret_cast<float4*>(&red_o[buf][warp][4 * lane]) = po;
+    st_cols<CPL>(&red_p[buf][warp][CPL * lane], pp);
+    st_cols<CPL>(&red_o[buf][warp][CPL * lane], po);
     if (!bar_and(kComputeBarrier, kRingThreads, ok)) {
       if (tid == 0 && a.status) atomicOr(a.status, kFlagTimeout);
       break;
@@ -457,38 +491,43 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
       sq += x.x; sk += x.y; sqk += x.z;
     }
     const float iq = inv_norm_of(sq), ik = inv_norm_of(sk), qk = sqk * iq * ik;
-    float4 p = make_float4(0.f, 0.f, 0.f, 0.f), oq = p;
+    float p[CPL], oq[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) p[j] = oq[j] = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-      const float4 x = *reinterpret_cast<const float4*>(&red_p[buf][w][4 * lane]);
-      const float4 y = *reinterpret_cast<const float4*>(&red_o[buf][w][4 * lane]);
-      p.x += x.x; p.y += x.y; p.z += x.z; p.w += x.w;
-      oq.x += y.x; oq.y += y.y; oq.z += y.z; oq.w += y.w;
-    }
-    const float beta = beta_of(b_cur);
-    float vx[4];
+      float x[CPL], y[CPL];
+      ld_cols<CPL>(&red_p[buf][w][CPL * lane], x);
+      ld_cols<CPL>(&red_o[buf][w][CPL * lane], y);
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      vx[t] = ld_in(rv, 4 * lane + t);
-      if (kConv) {
-        const int c = 4 * lane + t;
-        auto pv = [&](int m) { return wrow(2, m, c); };
-        if (warp == 0) window_push<TIn>(l, 2, vx[t], slot, H, hh, c, 128, pv);
-        vx[t] = conv_token<TIn>(l, 2, vx[t], H, hh, c, 128, pv);
+      for (int j = 0; j < CPL; ++j) {
+        p[j] += x[j];
+        oq[j] += y[j];
       }
     }
-    const float4 u = make_float4(beta * (vx[0] - ik * p.x), beta * (vx[1] - ik * p.y),
-                                 beta * (vx[2] - ik * p.z), beta * (vx[3] - ik * p.w));
+    const float beta = beta_of(b_cur);
+    float u[CPL];
+#pragma unroll
+    for (int t = 0; t < CPL; ++t) {
+      const int c = CPL * lane + t;
+      float vx = ld_in(rv, c);
+      if (kConv) {
+        auto pv = [&](int m) { return wrow(2, m, c); };
+        if (warp == 0) window_push<TIn>(l, 2, vx, slot, H, hh, c, DV, pv);
+        vx = conv_token<TIn>(l, 2, vx, H, hh, c, DV, pv);
+      }
+      u[t] = beta * (vx - ik * p[t]);
+    }
     // the updated state into the slot (each thread its own rows), then the
     // producer sends it back
     float* Ss = reinterpret_cast<float*>(stage);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < RPW; ++i) {
       const int r = warp + 8 * i;
       const float k_r = ik * __shfl_sync(0xffffffffu, xk, i);
-      float4 x = s[i];
-      x.x += k_r * u.x; x.y += k_r * u.y; x.z += k_r * u.z; x.w += k_r * u.w;
-      reinterpret_cast<float4*>(Ss + r * 128)[lane] = x;
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) s[i][j] += k_r * u[j];
+      st_cols<CPL>(Ss + r * DV + CPL * lane, s[i]);
     }
     tc::fence_async_smem();
     mbar_arrive(&done[st]);
@@ -496,28 +535,28 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
       const float scl = a.scale;
       const int row = (int)(item / H), h = (int)(item % H);
       TIn* o = static_cast<TIn*>(a.o);
-      const int64_t ob = ((int64_t)row * H + h) * 128 + 4 * lane;
-      st_out(o, ob + 0, scl * (iq * oq.x + qk * u.x) * gate_at<TIn>(l, row, H, h, ob + 0));
-      st_out(o, ob + 1, scl * (iq * oq.y + qk * u.y) * gate_at<TIn>(l, row, H, h, ob + 1));
-      st_out(o, ob + 2, scl * (iq * oq.z + qk * u.z) * gate_at<TIn>(l, row, H, h, ob + 2));
-      st_out(o, ob + 3, scl * (iq * oq.w + qk * u.w) * gate_at<TIn>(l, row, H, h, ob + 3));
+      const int64_t ob = ((int64_t)row * H + h) * DV + CPL * lane;
+#pragma unroll
+      for (int t = 0; t < CPL; ++t)
+        st_out(o, ob + t, scl * (iq * oq[t] + qk * u[t]) * gate_at<TIn>(l, row, H, h, ob + t));
     }
   }
 }
 
-template <typename TIn, bool kConv>
+template <typename TIn, bool kConv, int DK, int DV>
 cudaError_t launch_ring(const kda_decode_args& a, const kda_layer_args& l, cudaStream_t stream) {
+  using R = Ring<TIn, kConv, DK, DV>;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool poll = a.wait_limit_ns > 0 && (uint64_t)a.wait_limit_ns < tc::kPollLimitNs;
-  auto kernel = poll ? decode_ring<TIn, true, kConv> : decode_ring<TIn, false, kConv>;
+  auto kernel = poll ? decode_ring<TIn, true, kConv, DK, DV> : decode_ring<TIn, false, kConv, DK, DV>;
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Ring<TIn, kConv>::BYTES);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)R::BYTES);
   if (e != cudaSuccess) return e;
-  const int64_t n_items = (int64_t)a.batch * a.num_heads;
-  const int64_t grid = n_items < sms ? n_items : sms;
-  kernel<<<(unsigned)grid, kRingAllThreads, Ring<TIn, kConv>::BYTES, stream>>>(a, n_items, l);
+  const int64_t n_items = (int64_t)a.batch * a.num_heads, slots = (int64_t)sms * R::CTAS;
+  const int64_t grid = n_items < slots ? n_items : slots;
+  kernel<<<(unsigned)grid, kRingAllThreads, R::BYTES, stream>>>(a, n_items, l);
   return cudaGetLastError();
 }
 
@@ -528,13 +567,14 @@ cudaError_t launch_t(const kda_decode_args& a, const kda_layer_args& l, cudaStre
   // convolution the ring takes bf16 only (fp32 window rows overflow its
   // shared memory)
   const bool conv = l.conv_width > 0;
-  if (DK == 128 && DV == 128 && al16(a.q) && al16(a.k) && (a.gate_per_head || al16(a.g)) && al16(a.v) &&
-      al16(a.state) && (!conv || (sizeof(TIn) == 2 && al16(l.conv_in[0]) && al16(l.conv_in[1]) &&
-                                  al16(l.conv_in[2]))))
-  {
-    if constexpr (sizeof(TIn) == 2)
-      if (conv) return launch_ring<TIn, true>(a, l, stream);
-    return launch_ring<TIn, false>(a, l, stream);
+  constexpr bool kRingShape = (DK == 64 || DK == 128) && (DV == 64 || DV == 128);
+  if constexpr (kRingShape) {
+    if (al16(a.q) && al16(a.k) && (a.gate_per_head || al16(a.g)) && al16(a.v) && al16(a.state) &&
+        (!conv || (sizeof(TIn) == 2 && al16(l.conv_in[0]) && al16(l.conv_in[1]) && al16(l.conv_in[2])))) {
+      if constexpr (sizeof(TIn) == 2)
+        if (conv) return launch_ring<TIn, true, DK, DV>(a, l, stream);
+      return launch_ring<TIn, false, DK, DV>(a, l, stream);
+    }
   }
   constexpr int DVS = DecodeSlice<DK, DV>::DVS;
   dim3 grid((unsigned)a.batch, (unsigned)a.num_heads, (unsigned)(DV / DVS));

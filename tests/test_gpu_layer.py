@@ -214,7 +214,8 @@ def test_prefill_conv_segment_scan():
 
 
 @pytest.mark.parametrize("dtype,d,gate_mode", [("bf16", 128, "channel"), ("bf16", 128, "head"),
-                                               ("f32", 128, "channel"), ("f32", 32, "head")])
+                                               ("f32", 128, "channel"), ("f32", 32, "head"),
+                                               ("bf16", 64, "channel")])
 def test_decode_conv_gate(dtype, d, gate_mode):
     """Three decode steps over a slot pool (rows map to permuted slots, one
     row skipped) with the windows advanced in place; bf16 at d = 128 runs

@@ -87,7 +87,7 @@ def assert_close(gpu, ref, tol, what=""):
 # ------------------------------------------------------------------ decode (K4)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("dk,dv", [(16, 16), (32, 64), (64, 32), (128, 128), (128, 16),
-                                   (256, 256), (256, 16), (64, 256)])
+                                   (256, 256), (256, 16), (64, 256), (64, 64), (128, 64), (64, 128)])
 def test_decode_small(dtype, dk, dv, oracle_mod):
     dw = W.DecodeWorkload("small", 5, 3, dk, dv, 4, 77 + dk + dv)
     inp = W.decode_inputs(dw, dtype=dtype)

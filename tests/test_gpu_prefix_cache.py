@@ -23,8 +23,8 @@ def host(t):
     return t.detach().float().cpu().numpy()
 
 
-def inputs(T, H, seed):
-    w = W.PrefillWorkload("cache", None, 1, H, 128, 128, "bf16", seed, len_range=(1, 1))
+def inputs(T, H, seed, d=128):
+    w = W.PrefillWorkload("cache", None, 1, H, d, d, "bf16", seed, len_range=(1, 1))
     return W.prefill_inputs(w, lens=[T])
 
 
@@ -34,13 +34,16 @@ def oracle_run(inp):
                           host(inp["b"]), inp["cu_seqlens"].numpy())
 
 
-def test_slot_map_places_and_skips_snapshots():
-    inp = inputs(256, 2, 81)
+@pytest.mark.parametrize("dh", [128, 64])
+def test_slot_map_places_and_skips_snapshots(dh):
+    """(64-channel heads run on the tensor-core kernels zero-padded: their
+    snapshot rows keep the [64, 64] layout and leave other rows untouched.)"""
+    inp = inputs(256, 2, 81, dh)
     d = {x: inp[x].cuda() for x in "qkvgb"}
     cu = inp["cu_seqlens"]
     plain = kda.Prefill(*(d[x] for x in "qkvgb"), cu.cuda(), snapshot_interval=64,
                         host_cu_seqlens=cu).run()
-    pool = torch.full((8, 2, 128, 128), 7.0, device="cuda")
+    pool = torch.full((8, 2, dh, dh), 7.0, device="cuda")
     smap = torch.tensor([3, -1, 0, 7], dtype=torch.int32, device="cuda")
     mapped = kda.Prefill(*(d[x] for x in "qkvgb"), cu.cuda(), snapshot_interval=64,
                          host_cu_seqlens=cu, snapshot_pool=pool, snapshot_slot_map=smap).run()

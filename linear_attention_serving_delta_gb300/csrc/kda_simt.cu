@@ -67,10 +67,14 @@ simt_intra(ChunkParams p) {
   const int len = ch.len;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  float* qh = sm;                   // [64][dk]
-  float* kh = qh + kChunk * dk;     // [64][dk]
-  float* G = kh + kChunk * dk;      // [64][dk]
-  float* V = G + kChunk * dk;       // [64][dv]
+  // rows of q^, k^, G and e^G padded to dk + 1 floats: the A loop's lanes
+  // read 32 different rows of one column, which then fall in distinct banks
+  const int ld = dk + 1;
+  float* qh = sm;                   // [64][ld]
+  float* kh = qh + kChunk * ld;     // [64][ld]
+  float* G = kh + kChunk * ld;      // [64][ld]
+  float* EG = G + kChunk * ld;      // [64][ld] e^G
+  float* V = EG + kChunk * ld;      // [64][dv]
   float* A = V + kChunk * dv;       // [64][64]
   float* Tm = A + kChunk * kChunk;  // [64][64]
   float* beta = Tm + kChunk * kChunk;  // [64]
@@ -90,9 +94,9 @@ simt_intra(ChunkParams p) {
       xk = conv_input(p, 1, k, dk, ch, i, h, col);
       la = log_alpha_of(ld_in(g, p.gate_per_head ? (ch.tok0 + i) * H + h : e));
     }
-    qh[idx] = xq;
-    kh[idx] = xk;
-    G[idx] = la;
+    qh[i * ld + col] = xq;
+    kh[i * ld + col] = xk;
+    G[i * ld + col] = la;
   }
   for (int idx = tid; idx < kChunk * dv; idx += kThreads) {
     const int i = idx / dv, col = idx - i * dv;
@@ -105,22 +109,23 @@ simt_intra(ChunkParams p) {
   for (int i = warp; i < kChunk; i += kThreads / 32) {
     float sq = 0.f, sk = 0.f;
     for (int col = lane; col < dk; col += 32) {
-      sq += qh[i * dk + col] * qh[i * dk + col];
-      sk += kh[i * dk + col] * kh[i * dk + col];
+      sq += qh[i * ld + col] * qh[i * ld + col];
+      sk += kh[i * ld + col] * kh[i * ld + col];
     }
     sq = inv_norm_of(warp_sum(sq));
     sk = inv_norm_of(warp_sum(sk));
     for (int col = lane; col < dk; col += 32) {
-      qh[i * dk + col] *= sq;
-      kh[i * dk + col] *= sk;
+      qh[i * ld + col] *= sq;
+      kh[i * ld + col] *= sk;
     }
   }
   // running sum of log alpha down the chunk, one thread per key channel
   for (int col = tid; col < dk; col += kThreads) {
     float run = 0.f;
     for (int i = 0; i < kChunk; ++i) {
-      run += G[i * dk + col];
-      G[i * dk + col] = run;
+      run += G[i * ld + col];
+      G[i * ld + col] = run;
+      EG[i * ld + col] = expf(run);
     }
   }
   __syncthreads();
@@ -132,10 +137,10 @@ simt_intra(ChunkParams p) {
     float akk = 0.f, aqk = 0.f;
     if (j <= i && i < len) {
       for (int col = 0; col < dk; ++col) {
-        const float d = expf(G[i * dk + col] - G[j * dk + col]);
-        const float kj = kh[j * dk + col] * d;
-        akk += kh[i * dk + col] * kj;
-        aqk += qh[i * dk + col] * kj;
+        const float d = expf(G[i * ld + col] - G[j * ld + col]);
+        const float kj = kh[j * ld + col] * d;
+        akk += kh[i * ld + col] * kj;
+        aqk += qh[i * ld + col] * kj;
       }
       akk = j < i ? beta[i] * akk : 0.f;
     }
@@ -166,15 +171,15 @@ simt_intra(ChunkParams p) {
   for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) Tm[idx] *= beta[idx & 63];
   __syncthreads();
 
-  const float* GLrow = G + (kChunk - 1) * dk;  // padded rows carry G_{L-1} forward
+  const float* GLrow = G + (kChunk - 1) * ld;  // padded rows carry G_{L-1} forward
   for (int idx = tid; idx < kChunk * dk; idx += kThreads) {
     const int i = idx / dk, col = idx - i * dk;
     float w = 0.f;
     for (int m = 0; m <= i; ++m)
-      w += Tm[i * kChunk + m] * kh[m * dk + col] * expf(G[m * dk + col]);
+      w += Tm[i * kChunk + m] * kh[m * ld + col] * EG[m * ld + col];
     rec[SimtRec::w(dk) + idx] = w;
-    rec[SimtRec::qg(dk) + idx] = qh[idx] * expf(G[idx]);
-    rec[SimtRec::kr(dk) + idx] = kh[idx] * expf(GLrow[col] - G[idx]);
+    rec[SimtRec::qg(dk) + idx] = qh[i * ld + col] * EG[i * ld + col];
+    rec[SimtRec::kr(dk) + idx] = kh[i * ld + col] * expf(GLrow[col] - G[i * ld + col]);
   }
   for (int idx = tid; idx < kChunk * dv; idx += kThreads) {
     const int i = idx / dv, col = idx - i * dv;
@@ -205,10 +210,13 @@ simt_intra_blocked(ChunkParams p) {
   const int len = ch.len;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  float* X = sm;                     // [64][kCB]: q^ block, then V block
-  float* Kb = X + kChunk * kCB;      // [64][kCB]: k^ block
-  float* G = Kb + kChunk * kCB;      // [64][kCB]: running log-decay block
-  float* A = G + kChunk * kCB;       // [64][64] A_kk
+  // block rows padded to kCB + 1 floats (the A loop's lanes read 32 rows of
+  // one column)
+  constexpr int kLd = kCB + 1;
+  float* X = sm;                     // [64][kLd]: q^ block, then V block
+  float* Kb = X + kChunk * kLd;      // [64][kLd]: k^ block
+  float* G = Kb + kChunk * kLd;      // [64][kLd]: running log-decay block
+  float* A = G + kChunk * kLd;       // [64][64] A_kk
   float* AQ = A + kChunk * kChunk;   // [64][64] A_qk
   float* Tm = AQ + kChunk * kChunk;  // [64][64] T, then T diag(beta)
   float* beta = Tm + kChunk * kChunk;  // [64]
@@ -252,16 +260,16 @@ simt_intra_blocked(ChunkParams p) {
         const int64_t e = ((ch.tok0 + i) * H + h) * dk + c0 + col;
         la = log_alpha_of(ld_in(g, p.gate_per_head ? (ch.tok0 + i) * H + h : e));
       }
-      X[i * kCB + col] = xq;
-      Kb[i * kCB + col] = xk;
-      G[i * kCB + col] = la;
+      X[i * kLd + col] = xq;
+      Kb[i * kLd + col] = xk;
+      G[i * kLd + col] = la;
     }
     __syncthreads();
     for (int col = tid; col < nb; col += kThreads) {  // rows past len carry G_{L-1}
       float run = 0.f;
       for (int i = 0; i < kChunk; ++i) {
-        run += G[i * kCB + col];
-        G[i * kCB + col] = run;
+        run += G[i * kLd + col];
+        G[i * kLd + col] = run;
       }
     }
     __syncthreads();
@@ -276,10 +284,10 @@ simt_intra_blocked(ChunkParams p) {
       if (j <= i && i < len) {
         float akk = 0.f, aqk = 0.f;
         for (int col = 0; col < nb; ++col) {
-          const float d = expf(G[i * kCB + col] - G[j * kCB + col]);
-          const float kj = Kb[j * kCB + col] * d;
-          akk += Kb[i * kCB + col] * kj;
-          aqk += X[i * kCB + col] * kj;
+          const float d = expf(G[i * kLd + col] - G[j * kLd + col]);
+          const float kj = Kb[j * kLd + col] * d;
+          akk += Kb[i * kLd + col] * kj;
+          aqk += X[i * kLd + col] * kj;
         }
         if (j < i) A[idx] += beta[i] * akk;
         AQ[idx] += aqk;
@@ -309,15 +317,15 @@ simt_intra_blocked(ChunkParams p) {
   for (int c0 = 0; c0 < dk; c0 += kCB) {
     const int nb = dk - c0 < kCB ? dk - c0 : kCB;
     load_key_block(c0, nb);
-    const float* GL = G + (kChunk - 1) * kCB;
+    const float* GL = G + (kChunk - 1) * kLd;
     for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
       const int i = idx / nb, col = idx - i * nb;
       float w = 0.f;
-      for (int m = 0; m <= i; ++m) w += Tm[i * kChunk + m] * Kb[m * kCB + col] * expf(G[m * kCB + col]);
+      for (int m = 0; m <= i; ++m) w += Tm[i * kChunk + m] * Kb[m * kLd + col] * expf(G[m * kLd + col]);
       const size_t o = (size_t)i * dk + c0 + col;
       rec[SimtRec::w(dk) + o] = w;
-      rec[SimtRec::qg(dk) + o] = X[i * kCB + col] * expf(G[i * kCB + col]);
-      rec[SimtRec::kr(dk) + o] = Kb[i * kCB + col] * expf(GL[col] - G[i * kCB + col]);
+      rec[SimtRec::qg(dk) + o] = X[i * kLd + col] * expf(G[i * kLd + col]);
+      rec[SimtRec::kr(dk) + o] = Kb[i * kLd + col] * expf(GL[col] - G[i * kLd + col]);
     }
     for (int col = tid; col < nb; col += kThreads) rec[SimtRec::gl(dk, dv) + c0 + col] = expf(GL[col]);
     __syncthreads();
@@ -327,89 +335,171 @@ simt_intra_blocked(ChunkParams p) {
     const int nb = dv - v0 < kCB ? dv - v0 : kCB;
     for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
       const int i = idx / nb, col = idx - i * nb;
-      X[i * kCB + col] = i < len ? conv_input(p, 2, v, dv, ch, i, h, v0 + col) : 0.f;
+      X[i * kLd + col] = i < len ? conv_input(p, 2, v, dv, ch, i, h, v0 + col) : 0.f;
     }
     __syncthreads();
     for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
       const int i = idx / nb, col = idx - i * nb;
       float u = 0.f;
-      for (int m = 0; m <= i; ++m) u += Tm[i * kChunk + m] * X[m * kCB + col];
+      for (int m = 0; m <= i; ++m) u += Tm[i * kChunk + m] * X[m * kLd + col];
       rec[SimtRec::ut(dk) + (size_t)i * dv + v0 + col] = u;
     }
     __syncthreads();
   }
 }
 
-template <typename TIn>
+// K3 on CUDA cores: one CTA per (sequence, head, NS-column slice of S),
+// walking the sequence's chunks with its slice of S in shared memory.  Per
+// chunk the record's W, Q^ o Gamma and K^ o Gamma_L / Gamma are staged in
+// shared memory one after another (16-byte loads, rows padded by 4 floats)
+// and each thread works on a register tile: token rows i0 .. i0 + RPT - 1 of
+// a column pair for U = U~ - W S and O = scale ((Q^ o Gamma) S + A_qk U),
+// and key rows r0 .. r0 + SR - 1 of the same column pair for
+// S <- Diag(Gamma_L) S + KR^T U (written in place: each thread reads and
+// writes only its own elements of S there).
+template <typename TIn, int NS>
 __global__ void __launch_bounds__(kThreads)
-simt_inter(ChunkParams p, int ns) {
+simt_inter(ChunkParams p) {
   extern __shared__ float sm[];
-  const int s = blockIdx.x, h = blockIdx.y, n0 = blockIdx.z * ns;
+  constexpr int NCP = NS / 2;         // column pairs
+  constexpr int RG = kThreads / NCP;  // row groups
+  constexpr int RPT = kChunk / RG;    // token rows per thread
+  constexpr int kMaxSR = 16;          // key rows per thread (dk <= 256)
+  const int s = blockIdx.x, h = blockIdx.y, n0 = blockIdx.z * NS;
   const int H = p.H, dk = p.dk, dv = p.dv, tid = threadIdx.x;
   const int64_t c_begin = p.seq_chunk_begin[s], c_end = p.seq_chunk_begin[s + 1];
   if (c_end > c_begin && p.meta->total_chunks == 0) return;  // chunk table overflowed
 
-  float* S = sm;               // [dk][ns]
-  float* U = S + dk * ns;      // [64][ns]
-  float* QS = U + kChunk * ns; // [64][ns]
+  const int xs = dk + 4;                  // padded row stride of the staged rows
+  float* S = sm;                          // [dk][NS]
+  float* U = S + dk * NS;                 // [64][NS]
+  float* X = U + kChunk * NS;             // [64][dk + 4]: W, then Q^ o Gamma, then KR
+  float* AQ = X + kChunk * xs;            // [64][64]
+  float* GLs = AQ + kChunk * kChunk;      // [dk]
+  const int cp = tid % NCP, rg = tid / NCP;
+  const int c0 = 2 * cp, i0 = rg * RPT;
+  const int SR = (dk + RG - 1) / RG, r0 = rg * SR;
+
   const size_t sbase = ((size_t)s * H + h) * dk * dv;
-  for (int idx = tid; idx < dk * ns; idx += kThreads) {
-    const int r = idx / ns, n = idx - r * ns;
+  for (int idx = tid; idx < dk * NS; idx += kThreads) {
+    const int r = idx / NS, n = idx - r * NS;
     S[idx] = p.initial_state ? p.initial_state[sbase + (size_t)r * dv + n0 + n] : 0.f;
   }
-  __syncthreads();
+  auto stage_rows = [&](const float* src) {
+    const int q4 = dk / 4;
+    for (int idx = tid; idx < kChunk * q4; idx += kThreads) {
+      const int i = idx / q4, c4 = idx - i * q4;
+      *reinterpret_cast<float4*>(X + i * xs + 4 * c4) =
+          *reinterpret_cast<const float4*>(src + (size_t)i * dk + 4 * c4);
+    }
+  };
+  // acc[ii] += X[i0 + ii] . S[:, c0 .. c0 + 1]
+  auto rows_times_state = [&](float (*acc)[2]) {
+    for (int r = 0; r < dk; ++r) {
+      const float2 sv = *reinterpret_cast<const float2*>(S + r * NS + c0);
+#pragma unroll
+      for (int ii = 0; ii < RPT; ++ii) {
+        const float x = X[(i0 + ii) * xs + r];
+        acc[ii][0] += x * sv.x;
+        acc[ii][1] += x * sv.y;
+      }
+    }
+  };
   TIn* o = static_cast<TIn*>(p.o);
   const TIn* og = static_cast<const TIn*>(p.out_gate);
   for (int64_t c = c_begin; c < c_end; ++c) {
     const Chunk ch = p.chunks[c];
     const float* rec = p.inter + ((size_t)c * H + h) * p.rec_floats;
-    const float* W = rec + SimtRec::w(dk);
-    const float* QG = rec + SimtRec::qg(dk);
-    const float* KR = rec + SimtRec::kr(dk);
-    const float* AQK = rec + SimtRec::aqk(dk);
     const float* UT = rec + SimtRec::ut(dk);
-    const float* GL = rec + SimtRec::gl(dk, dv);
-    for (int idx = tid; idx < kChunk * ns; idx += kThreads) {
-      const int i = idx / ns, n = idx - i * ns;
-      float ws = 0.f, qs = 0.f;
-      for (int r = 0; r < dk; ++r) {
-        const float sv = S[r * ns + n];
-        ws += W[i * dk + r] * sv;
-        qs += QG[i * dk + r] * sv;
-      }
-      U[idx] = UT[i * dv + n0 + n] - ws;
-      QS[idx] = qs;
-    }
+    // W, A_qk and Gamma_L in; S is complete (previous chunk's update)
+    stage_rows(rec + SimtRec::w(dk));
+    for (int idx = tid; idx < kChunk * kChunk / 4; idx += kThreads)
+      reinterpret_cast<float4*>(AQ)[idx] = reinterpret_cast<const float4*>(rec + SimtRec::aqk(dk))[idx];
+    for (int r = tid; r < dk; r += kThreads) GLs[r] = rec[SimtRec::gl(dk, dv) + r];
     __syncthreads();
-    for (int idx = tid; idx < kChunk * ns; idx += kThreads) {
-      const int i = idx / ns, n = idx - i * ns;
-      if (i < ch.len) {
-        float acc = QS[idx];
-        for (int j = 0; j <= i; ++j) acc += AQK[i * kChunk + j] * U[j * ns + n];
-        const int64_t oi = ((ch.tok0 + i) * H + h) * dv + n0 + n;
-        float val = p.scale * acc;
-        if (og) val *= out_gate_of(ld_in(og, p.out_gate_per_head ? (ch.tok0 + i) * H + h : oi));
-        st_out(o, oi, val);
+    // U = U~ - W S
+    {
+      float a[RPT][2] = {};
+      rows_times_state(a);
+#pragma unroll
+      for (int ii = 0; ii < RPT; ++ii) {
+        const int i = i0 + ii;
+        const float2 ut = *reinterpret_cast<const float2*>(UT + (size_t)i * dv + n0 + c0);
+        U[i * NS + c0] = ut.x - a[ii][0];
+        U[i * NS + c0 + 1] = ut.y - a[ii][1];
       }
     }
-    for (int idx = tid; idx < dk * ns; idx += kThreads) {
-      const int r = idx / ns, n = idx - r * ns;
-      float acc = GL[r] * S[idx];
-      for (int i = 0; i < kChunk; ++i) acc += KR[i * dk + r] * U[i * ns + n];
-      S[idx] = acc;
+    __syncthreads();  // U complete, W read
+    stage_rows(rec + SimtRec::qg(dk));
+    __syncthreads();
+    // O = scale ((Q^ o Gamma) S + A_qk U), A_qk masked j <= i
+    {
+      float a[RPT][2] = {};
+      rows_times_state(a);
+#pragma unroll
+      for (int ii = 0; ii < RPT; ++ii) {
+        const int i = i0 + ii;
+        for (int j = 0; j <= i; ++j) {
+          const float aq = AQ[i * kChunk + j];
+          const float2 u = *reinterpret_cast<const float2*>(U + j * NS + c0);
+          a[ii][0] += aq * u.x;
+          a[ii][1] += aq * u.y;
+        }
+        if (i < ch.len) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int64_t oi = ((ch.tok0 + i) * H + h) * dv + n0 + c0 + t;
+            float val = p.scale * a[ii][t];
+            if (og) val *= out_gate_of(ld_in(og, p.out_gate_per_head ? (ch.tok0 + i) * H + h : oi));
+            st_out(o, oi, val);
+          }
+        }
+      }
+    }
+    __syncthreads();  // Q^ o Gamma and S read
+    stage_rows(rec + SimtRec::kr(dk));
+    __syncthreads();
+    // S <- Diag(Gamma_L) S + KR^T U on this thread's key rows
+    {
+      float b[kMaxSR][2];
+#pragma unroll
+      for (int rr = 0; rr < kMaxSR; ++rr) {
+        const int r = r0 + rr;
+        const bool live = rr < SR && r < dk;
+        b[rr][0] = live ? GLs[r] * S[r * NS + c0] : 0.f;
+        b[rr][1] = live ? GLs[r] * S[r * NS + c0 + 1] : 0.f;
+      }
+      for (int i = 0; i < kChunk; ++i) {
+        const float2 u = *reinterpret_cast<const float2*>(U + i * NS + c0);
+        const float* xr = X + i * xs + r0;
+#pragma unroll
+        for (int rr = 0; rr < kMaxSR; ++rr)
+          if (rr < SR && r0 + rr < dk) {
+            const float x = xr[rr];
+            b[rr][0] += x * u.x;
+            b[rr][1] += x * u.y;
+          }
+      }
+#pragma unroll
+      for (int rr = 0; rr < kMaxSR; ++rr)
+        if (rr < SR && r0 + rr < dk) {
+          S[(r0 + rr) * NS + c0] = b[rr][0];
+          S[(r0 + rr) * NS + c0 + 1] = b[rr][1];
+        }
     }
     __syncthreads();
     if (ch.snap_slot >= 0 && p.snapshots) {
       const size_t base = ((size_t)ch.snap_slot * H + h) * dk * dv;
-      for (int idx = tid; idx < dk * ns; idx += kThreads) {
-        const int r = idx / ns, n = idx - r * ns;
+      for (int idx = tid; idx < dk * NS; idx += kThreads) {
+        const int r = idx / NS, n = idx - r * NS;
         p.snapshots[base + (size_t)r * dv + n0 + n] = S[idx];
       }
     }
   }
+  __syncthreads();
   if (p.final_state) {
-    for (int idx = tid; idx < dk * ns; idx += kThreads) {
-      const int r = idx / ns, n = idx - r * ns;
+    for (int idx = tid; idx < dk * NS; idx += kThreads) {
+      const int r = idx / NS, n = idx - r * NS;
       p.final_state[sbase + (size_t)r * dv + n0 + n] = S[idx];
     }
   }
@@ -421,8 +511,8 @@ cudaError_t launch_simt_t(const ChunkParams& p, cudaStream_t stream, cudaEvent_t
   // take the blocked kernel
   const bool blocked = p.dk > kCB || p.dv > kCB;
   const size_t smem_intra =
-      blocked ? sizeof(float) * (3 * (size_t)kChunk * kCB + 3 * kChunk * kChunk + 3 * kChunk)
-              : sizeof(float) * (3 * (size_t)kChunk * p.dk + (size_t)kChunk * p.dv + 2 * kChunk * kChunk + kChunk);
+      blocked ? sizeof(float) * (3 * (size_t)kChunk * (kCB + 1) + 3 * kChunk * kChunk + 3 * kChunk)
+              : sizeof(float) * (4 * (size_t)kChunk * (p.dk + 1) + (size_t)kChunk * p.dv + 2 * kChunk * kChunk + kChunk);
   auto intra = blocked ? simt_intra_blocked<TIn> : simt_intra<TIn>;
   cudaError_t e = cudaFuncSetAttribute(intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_intra);
   if (e != cudaSuccess) return e;
@@ -436,12 +526,14 @@ cudaError_t launch_simt_t(const ChunkParams& p, cudaStream_t stream, cudaEvent_t
     e = cudaEventRecord(mid, stream);
     if (e != cudaSuccess) return e;
   }
-  const int ns = p.dv < 32 ? p.dv : 32;
-  const size_t smem_inter = sizeof(float) * ((size_t)p.dk * ns + 2 * (size_t)kChunk * ns);
-  e = cudaFuncSetAttribute(simt_inter<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_inter);
+  const int ns = p.dv < 32 ? p.dv : 32;  // 16 or 32 value columns per CTA
+  const size_t smem_inter = sizeof(float) * ((size_t)p.dk * ns + (size_t)kChunk * ns +
+                                             (size_t)kChunk * (p.dk + 4) + kChunk * kChunk + p.dk);
+  auto inter = ns == 32 ? simt_inter<TIn, 32> : simt_inter<TIn, 16>;
+  e = cudaFuncSetAttribute(inter, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_inter);
   if (e != cudaSuccess) return e;
   dim3 grid2((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)(p.dv / ns));
-  simt_inter<TIn><<<grid2, kThreads, smem_inter, stream>>>(p, ns);
+  inter<<<grid2, kThreads, smem_inter, stream>>>(p);
   return cudaGetLastError();
 }
 

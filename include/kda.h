@@ -427,6 +427,12 @@ typedef struct {
   float* beta;                 /* device [T, H]                                   */
   int32_t gate_per_head;       /* as in kda_prefill_args: g is [T, H] when set (G
                                   is still written [T, H, dk], equal across dk)  */
+  const kda_layer_args* layer; /* host pointer, or NULL: with conv_width > 0, q
+                                  and k pass through the short convolution
+                                  before the normalisation, as in kda_prefill
+                                  (conv_w[0..1], conv_in[0..1] used; windows
+                                  [N, conv_width - 1, H, dk]; nothing else of
+                                  the struct is read or written)               */
 } kda_prep_args;
 
 kda_status_t kda_prep(const kda_prep_args* args, void* stream);

@@ -329,6 +329,10 @@ kda_status_t kda_prep(const kda_prep_args* a, void* stream) {
       (!a->q || !a->k || !a->g || !a->b || !a->qhat || !a->khat || !a->G || !a->beta))
     return KDA_ERR_INVALID_ARG;
   if (a->gate_per_head != 0 && a->gate_per_head != 1) return KDA_ERR_INVALID_ARG;
+  if (const kda_layer_args* l = a->layer) {
+    if (l->conv_width < 0 || l->conv_width > KDA_CONV_MAX) return KDA_ERR_INVALID_ARG;
+    if (l->conv_width > 0 && (!l->conv_w[0] || !l->conv_w[1])) return KDA_ERR_INVALID_ARG;
+  }
   return from_cuda(launch_prep(*a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -19,9 +19,35 @@ namespace {
 
 constexpr int kPrepThreads = 128;
 
+// Input x (q or k: tensor t) of token tok (sequence s starting at packed
+// index seq0), head h, channel c, after the short convolution when there is
+// one (formula and windows in include/kda.h): inputs before the sequence
+// start from its window, or zeros.
+template <typename TIn>
+__device__ float prep_input(const kda_prep_args& a, const kda_layer_args& l, int t, const TIn* x, int64_t tok,
+                            int32_t s, int64_t seq0, int h, int c) {
+  const int H = a.num_heads, dk = a.dk, W = l.conv_width;
+  const int64_t e = (tok * H + h) * dk + c;
+  if (W == 0) return ld_in(x, e);
+  const TIn* win = static_cast<const TIn*>(l.conv_in[t]);
+  float acc = 0.f;
+  for (int j = 0; j < W; ++j) {
+    const int64_t src = tok - j;
+    float xv = 0.f;
+    if (src >= seq0)
+      xv = ld_in(x, e - (int64_t)j * H * dk);
+    else if (win && seq0 - src <= W - 1)  // window row W - 1 - (seq0 - src) (further back:
+                                          // only with malformed cu_seqlens)
+      xv = ld_in(win, (((int64_t)s * (W - 1) + (W - 1) - (seq0 - src)) * H + h) * dk + c);
+    acc += l.conv_w[t][((int64_t)j * H + h) * dk + c] * xv;
+  }
+  if (l.conv_silu) acc = silu_of(acc);
+  return round_in<TIn>(acc);
+}
+
 template <typename TIn>
 __global__ void __launch_bounds__(kPrepThreads)
-prep_kernel(kda_prep_args a) {
+prep_kernel(kda_prep_args a, const kda_layer_args l) {
   __shared__ float inv_q[kChunk], inv_k[kChunk];
   const int64_t t0 = (int64_t)blockIdx.x * kChunk;
   const int h = blockIdx.y, H = a.num_heads, dk = a.dk;
@@ -36,10 +62,11 @@ prep_kernel(kda_prep_args a) {
   for (int i = warp; i < kChunk; i += kPrepThreads / 32) {
     const int64_t t = t0 + i;
     if (t >= t1) break;
-    const int64_t base = (t * H + h) * dk;
+    const int32_t st = l.conv_width > 0 ? seq_of_token(a.cu_seqlens, a.num_seqs, t) : 0;
+    const int64_t s0 = l.conv_width > 0 ? a.cu_seqlens[st] : 0;
     float sq = 0.f, sk = 0.f;
     for (int c = lane; c < dk; c += 32) {
-      const float xq = ld_in(q, base + c), xk = ld_in(k, base + c);
+      const float xq = prep_input(a, l, 0, q, t, st, s0, h, c), xk = prep_input(a, l, 1, k, t, st, s0, h, c);
       sq += xq * xq;
       sk += xk * xk;
     }
@@ -73,8 +100,8 @@ prep_kernel(kda_prep_args a) {
       const int64_t e = (t * H + h) * dk + c;
       run += log_alpha_of(ld_in(g, ph ? t * H + h : e));
       a.G[e] = run;
-      a.qhat[e] = ld_in(q, e) * inv_q[t - t0];
-      a.khat[e] = ld_in(k, e) * inv_k[t - t0];
+      a.qhat[e] = prep_input(a, l, 0, q, t, s, seq0, h, c) * inv_q[t - t0];
+      a.khat[e] = prep_input(a, l, 1, k, t, s, seq0, h, c) * inv_k[t - t0];
     }
   }
 }
@@ -243,14 +270,22 @@ bool aligned16p(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) ==
 cudaError_t launch_prep(const kda_prep_args& a, cudaStream_t stream) {
   if (a.total_tokens == 0) return cudaSuccess;
   dim3 grid((unsigned)((a.total_tokens + kChunk - 1) / kChunk), (unsigned)a.num_heads);
-  if (a.in_dtype == KDA_BF16 && a.dk == 128 && !a.gate_per_head && aligned16p(a.q) && aligned16p(a.k) &&
-      aligned16p(a.g) &&
-      aligned16p(a.qhat) && aligned16p(a.khat) && aligned16p(a.G))
+  kda_layer_args l{};  // by value: the kernel cannot read the caller's host struct
+  if (a.layer && a.layer->conv_width > 0) {
+    l.conv_width = a.layer->conv_width;
+    l.conv_silu = a.layer->conv_silu != 0;
+    for (int t = 0; t < 2; ++t) {
+      l.conv_w[t] = a.layer->conv_w[t];
+      l.conv_in[t] = l.conv_width > 1 ? a.layer->conv_in[t] : nullptr;
+    }
+  }
+  if (l.conv_width == 0 && a.in_dtype == KDA_BF16 && a.dk == 128 && !a.gate_per_head && aligned16p(a.q) &&
+      aligned16p(a.k) && aligned16p(a.g) && aligned16p(a.qhat) && aligned16p(a.khat) && aligned16p(a.G))
     prep_vec<<<grid, kVecThreads, 0, stream>>>(a);
   else if (a.in_dtype == KDA_BF16)
-    prep_kernel<__nv_bfloat16><<<grid, kPrepThreads, 0, stream>>>(a);
+    prep_kernel<__nv_bfloat16><<<grid, kPrepThreads, 0, stream>>>(a, l);
   else
-    prep_kernel<float><<<grid, kPrepThreads, 0, stream>>>(a);
+    prep_kernel<float><<<grid, kPrepThreads, 0, stream>>>(a, l);
   return cudaGetLastError();
 }
 

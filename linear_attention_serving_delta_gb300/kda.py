@@ -91,7 +91,8 @@ class PrepArgs(ctypes.Structure):
     _fields_ = [("num_seqs", c_i32), ("num_heads", c_i32), ("dk", c_i32),
                 ("total_tokens", c_i64), ("cu_seqlens", c_vp), ("in_dtype", ctypes.c_int),
                 ("q", c_vp), ("k", c_vp), ("g", c_vp), ("b", c_vp), ("qhat", c_vp),
-                ("khat", c_vp), ("G", c_vp), ("beta", c_vp), ("gate_per_head", c_i32)]
+                ("khat", c_vp), ("G", c_vp), ("beta", c_vp), ("gate_per_head", c_i32),
+                ("layer", ctypes.POINTER(LayerArgs))]
 
 
 _lock = threading.Lock()
@@ -393,7 +394,11 @@ def kda_decode_step(q, k, v, g, b, state, o, state_slots=None, scale=1.0, stream
     _check(lib().kda_decode_step(ctypes.byref(a), _stream(stream)), "kda_decode_step")
 
 
-def kda_prep(q, k, g, b, cu_seqlens, qhat, khat, G, beta, stream=None) -> None:
+def kda_prep(q, k, g, b, cu_seqlens, qhat, khat, G, beta, stream=None, conv_weights=None,
+             conv_silu=False, conv_window=None) -> None:
+    """The preparation step.  With conv_weights (wq, wk, ...) [W, H, dk] q and k
+    pass through the short convolution first (conv_window: (q, k) windows
+    [N, W-1, H, dk] before each sequence, or None)."""
     T, H, dk = q.shape
     dt = q.dtype
     a = PrepArgs()
@@ -404,6 +409,22 @@ def kda_prep(q, k, g, b, cu_seqlens, qhat, khat, G, beta, stream=None) -> None:
     a.qhat, a.khat = _ptr(qhat, torch.float32, "qhat"), _ptr(khat, torch.float32, "khat")
     a.G, a.beta = _ptr(G, torch.float32, "G"), _ptr(beta, torch.float32, "beta")
     a.gate_per_head = 1 if g.dim() == 2 else 0  # g [T, H]: one decay per token and head
+    if conv_weights is not None:
+        la = LayerArgs()
+        W = conv_weights[0].shape[0]
+        if not 1 <= W <= CONV_MAX:
+            raise ValueError(f"conv width {W} outside 1..{CONV_MAX}")
+        la.conv_width, la.conv_silu = W, 1 if conv_silu else 0
+        N = cu_seqlens.numel() - 1
+        for t in range(2):
+            if tuple(conv_weights[t].shape) != (W, H, dk):
+                raise ValueError(f"conv weights {t} have shape {tuple(conv_weights[t].shape)}")
+            la.conv_w[t] = _ptr(conv_weights[t], torch.float32, "conv_weights")
+            x = None if conv_window is None else conv_window[t]
+            if x is not None and tuple(x.shape) != (N, W - 1, H, dk):
+                raise ValueError(f"conv window {t} has shape {tuple(x.shape)}")
+            la.conv_in[t] = _ptr(x, dt, "conv window")
+        a.layer = ctypes.pointer(la)
     _check(lib().kda_prep(ctypes.byref(a), _stream(stream)), "kda_prep")
 
 
@@ -669,10 +690,12 @@ def decode_step(q, k, v, g, b, state, state_slots=None, scale=1.0, o=None, strea
     return o
 
 
-def prep(q, k, g, b, cu_seqlens, stream=None):
+def prep(q, k, g, b, cu_seqlens, stream=None, **conv):
+    """Allocates and runs kda_prep; ``conv`` takes conv_weights, conv_silu and
+    conv_window (see kda_prep)."""
     T, H, dk = q.shape
     f = dict(dtype=torch.float32, device=q.device)
     qhat, khat, G = (torch.empty(T, H, dk, **f) for _ in range(3))
     beta = torch.empty(T, H, **f)
-    kda_prep(q, k, g, b, cu_seqlens, qhat, khat, G, beta, stream=stream)
+    kda_prep(q, k, g, b, cu_seqlens, qhat, khat, G, beta, stream=stream, **conv)
     return qhat, khat, G, beta

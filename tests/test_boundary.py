@@ -63,7 +63,7 @@ int main(void) {
   printf("kda_layer_args %zu\n", sizeof(kda_layer_args));
   F(kda_layer_args, conv_silu) F(kda_layer_args, conv_w) F(kda_layer_args, conv_in)
   F(kda_layer_args, conv_out) F(kda_layer_args, out_gate) F(kda_layer_args, out_gate_per_head)
-  F(kda_prefill_args, layer) F(kda_decode_args, layer)
+  F(kda_prefill_args, layer) F(kda_decode_args, layer) F(kda_prep_args, layer)
   F(kda_prefill_host_args, cu_seqlens) F(kda_prefill_host_args, in_dtype)
   F(kda_prefill_host_args, scale) F(kda_prefill_host_args, final_state)
   F(kda_prefill_host_args, segments) F(kda_prefill_host_args, copy_in_stream)

@@ -166,6 +166,39 @@ def test_output_gate_on_padded_heads():
         assert rel(host(p.snapshot_view), rsn) <= TOL["bf16"], mode
 
 
+@pytest.mark.parametrize("dtype,dk", [("bf16", 128), ("f32", 64)])
+def test_prep_with_convolution(dtype, dk):
+    """kda_prep with the short convolution: q^ and k^ are the normalised
+    convolved inputs (the prefill's first step), G and beta unchanged;
+    sequences shorter than the window and an empty one."""
+    import oracle
+    from oracle import layer
+    lens = [5, 2, 64, 0, 130, 1]
+    inp, li = case(lens, 3, dk, 16, dtype, seed=380, width=4)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    taps = tuple(t.cuda() for t in li["taps"])
+    win = tuple(t.cuda() for t in li["windows"])
+    qh, kh, G, beta = kda.prep(d["q"], d["k"], d["g"], d["b"], d["cu_seqlens"],
+                               conv_weights=taps, conv_silu=True, conv_window=win[:2])
+    torch.cuda.synchronize()
+    cu = inp["cu_seqlens"].numpy()
+    cq, _ = layer.short_conv(host(inp["q"]), host(li["taps"][0]), cu, host(li["windows"][0]), True,
+                             ODT[dtype])
+    ck, _ = layer.short_conv(host(inp["k"]), host(li["taps"][1]), cu, host(li["windows"][1]), True,
+                             ODT[dtype])
+    rq, rk, _, rb = oracle.prep(cq, ck, host(inp["g"]), host(inp["b"]))
+    # (a convolved value may round to the other neighbouring bf16 value where the
+    # fp32 and fp64 sums straddle a rounding boundary: a few elements in 1e5)
+    assert rel(host(qh), rq) < 1e-4 and rel(host(kh), rk) < 1e-4
+    assert rel(host(beta), rb) < 1e-6
+    qp, kp, Gp, _ = kda.prep(d["q"], d["k"], d["g"], d["b"], d["cu_seqlens"])
+    torch.cuda.synchronize()
+    # G does not depend on the convolution (without it bf16 at dk = 128 takes
+    # the vectorised kernel, whose scan sums in another order: equal to rounding)
+    assert rel(host(G), host(Gp)) < 1e-6
+    assert rel(host(qh), host(qp)) > 1e-2  # the convolution did change q^
+
+
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 32)])
 def test_prefill_windows_in_place(dtype, d):
     lens = [2, 90, 1]

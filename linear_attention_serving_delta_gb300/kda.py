@@ -197,27 +197,33 @@ def make_layer_args(*, rows, H, dk, dv, dtype, conv_weights=None, conv_silu=Fals
     None); out_gate: [gate_rows, H, dv] or [gate_rows, H] (one gate per head)."""
     if conv_weights is None and out_gate is None:
         return None
-    la = LayerArgs()
+    # every shape first, then the pointers
+    W = 0
     if conv_weights is not None:
         W = conv_weights[0].shape[0]
         if not 1 <= W <= CONV_MAX:
             raise ValueError(f"conv width {W} outside 1..{CONV_MAX}")
-        la.conv_width, la.conv_silu = W, 1 if conv_silu else 0
         for t, (w, d) in enumerate(zip(conv_weights, (dk, dk, dv))):
             if tuple(w.shape) != (W, H, d):
                 raise ValueError(f"conv weights {t} have shape {tuple(w.shape)}, expected {(W, H, d)}")
-            la.conv_w[t] = _ptr(w, torch.float32, "conv_weights")
-            for arr, src in ((la.conv_in, conv_window), (la.conv_out, conv_window_out)):
+            for src in (conv_window, conv_window_out):
                 x = None if src is None else src[t]
                 if x is not None and tuple(x.shape) != (rows, W - 1, H, d):
                     raise ValueError(f"conv window {t} has shape {tuple(x.shape)}, "
                                      f"expected {(rows, W - 1, H, d)}")
-                arr[t] = _ptr(x, dtype, "conv window")
+    per_head = out_gate is not None and out_gate.dim() == 2
     if out_gate is not None:
-        per_head = out_gate.dim() == 2
         want = (gate_rows, H) if per_head else (gate_rows, H, dv)
         if tuple(out_gate.shape) != want:
             raise ValueError(f"out_gate has shape {tuple(out_gate.shape)}, expected {want}")
+    la = LayerArgs()
+    if conv_weights is not None:
+        la.conv_width, la.conv_silu = W, 1 if conv_silu else 0
+        for t in range(3):
+            la.conv_w[t] = _ptr(conv_weights[t], torch.float32, "conv_weights")
+            for arr, src in ((la.conv_in, conv_window), (la.conv_out, conv_window_out)):
+                arr[t] = _ptr(None if src is None else src[t], dtype, "conv window")
+    if out_gate is not None:
         la.out_gate = _ptr(out_gate, dtype, "out_gate")
         la.out_gate_per_head = 1 if per_head else 0
     return la

@@ -326,3 +326,28 @@ def test_host_entry_workspace_and_validation(kda):
     # workspace too small or misaligned
     assert L.kda_prefill_host(ctypes.byref(good), 0x4000, ws - 256, None) == 3
     assert L.kda_prefill_host(ctypes.byref(good), 0x4010, ws, None) == 3
+
+
+def test_layer_args_shapes_checked_in_the_binding(kda):
+    """The binding checks the layer steps' shapes before it touches device
+    memory: taps [W, H, d] with 1 <= W <= 4, windows [rows, W-1, H, d], the
+    gate [T, H, dv] or [T, H] (one gate per head)."""
+    import torch
+    H, dk, dv, W = 2, 16, 8, 3
+    taps = (torch.zeros(W, H, dk), torch.zeros(W, H, dk), torch.zeros(W, H, dv))
+    kw = dict(rows=4, H=H, dk=dk, dv=dv, dtype=torch.float32)
+    assert kda.make_layer_args(**kw) is None                      # nothing asked for
+    with pytest.raises(ValueError, match="conv width"):
+        kda.make_layer_args(conv_weights=tuple(torch.zeros(5, H, d) for d in (dk, dk, dv)), **kw)
+    with pytest.raises(ValueError, match="conv weights 2"):
+        kda.make_layer_args(conv_weights=taps[:2] + (torch.zeros(W, H, dk),), **kw)
+    with pytest.raises(ValueError, match="conv window 1"):
+        kda.make_layer_args(conv_weights=taps, conv_window=(None, torch.zeros(4, W, H, dk), None),
+                            **kw)
+    with pytest.raises(ValueError, match="out_gate"):
+        kda.make_layer_args(out_gate=torch.zeros(10, H, dk), gate_rows=10, **kw)
+    with pytest.raises(ValueError, match="out_gate"):
+        kda.make_layer_args(out_gate=torch.zeros(10, H + 1), gate_rows=10, **kw)
+    # shapes right: the host tensors are then refused as not on the device
+    with pytest.raises(ValueError, match="CUDA"):
+        kda.make_layer_args(conv_weights=taps, **kw)

@@ -61,6 +61,9 @@ int main(void) {
   printf("kda_prep_args %zu\n", sizeof(kda_prep_args));
   printf("kda_prefill_host_args %zu\n", sizeof(kda_prefill_host_args));
   printf("kda_layer_args %zu\n", sizeof(kda_layer_args));
+  printf("const.KDA_CONV_MAX %d\n", KDA_CONV_MAX);
+  printf("const.KDA_CHUNK %d\n", KDA_CHUNK);
+  printf("const.KDA_PREFILL_PHASES %d\n", KDA_PREFILL_PHASES);
   F(kda_layer_args, conv_silu) F(kda_layer_args, conv_w) F(kda_layer_args, conv_in)
   F(kda_layer_args, conv_out) F(kda_layer_args, out_gate) F(kda_layer_args, out_gate_per_head)
   F(kda_prefill_args, layer) F(kda_decode_args, layer) F(kda_prep_args, layer)
@@ -91,8 +94,12 @@ int main(void) {
     structs = {"kda_prefill_args": kda.PrefillArgs, "kda_decode_args": kda.DecodeArgs,
                "kda_prep_args": kda.PrepArgs, "kda_prefill_host_args": kda.PrefillHostArgs,
                "kda_layer_args": kda.LayerArgs}
+    consts = {"KDA_CONV_MAX": kda.CONV_MAX, "KDA_CHUNK": kda.CHUNK,
+              "KDA_PREFILL_PHASES": kda.PREFILL_PHASES}
     for key, val in got.items():
-        if "." in key:
+        if key.startswith("const."):
+            assert consts[key[6:]] == int(val), key
+        elif "." in key:
             s, m = key.split(".")
             assert getattr(structs[s], m).offset == int(val), key
         else:

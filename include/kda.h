@@ -25,9 +25,11 @@
  *   - Every tensor is caller-owned device memory, row-major and contiguous,
  *     token-major: q, k, g [T, H, dk] (g [T, H] with gate_per_head);
  *     v, o [T, H, dv]; b [T, H]; states
- *     [.., H, dk, dv] fp32.  The library allocates no device memory and keeps
- *     no mutable global state (the prefix cache's host index lives in the
- *     object the caller creates); calls from several host threads are safe.
+ *     [.., H, dk, dv] fp32.  No call allocates device memory.  The library
+ *     keeps no mutable global state, with one exception: the fixed workspace
+ *     array behind kda_prefill_noalloc (see there).  The prefix cache's host
+ *     index lives in the object the caller creates.  Calls from several host
+ *     threads are safe (kda_prefill_noalloc calls share its array: see there).
  *   - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
  *     default stream).  Arguments are validated on the host before any
  *     launch; on an error nothing is launched and the status says why.
@@ -231,13 +233,24 @@ kda_status_t kda_prefill(const kda_prefill_args* args, void* ws, size_t ws_bytes
  *   - Arguments whose kda_prefill_workspace_size exceeds 64 MiB are rejected
  *     with KDA_ERR_WORKSPACE before any launch (for example about 650
  *     (chunk, head) pairs on the bf16 dk = dv = 128 path).
- *   - The first call on a device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *   - A call made outside stream capture looks up the array's device
+ *     address on the current device (cudaGetSymbolAddress) and remembers it
+ *     for that device; a call made while `stream` is capturing uses the
+ *     remembered address.  Make the first call on each device before any
+ *     stream capture (a capturing call with none remembered returns
+ *     KDA_ERR_CUDA).
  *   - All calls share the array: calls whose kernels overlap on the GPU race
  *     on it, so serialise them (one stream, or events).  Nothing in it needs
- *     to start at zero; its device status word is not readable afterwards
- *     through kda_prefill_device_status. */
+ *     to start at zero.  kda_prefill_noalloc_device_status reads its status
+ *     word (the device-side flags of the last call). */
 kda_status_t kda_prefill_noalloc(const kda_prefill_args* args, void* stream);
+
+/* The device status word of the last kda_prefill_noalloc on the current
+ * device (the same flags as kda_prefill_device_status), copied to *out
+ * (host), synchronising `stream`.  Allocates nothing.  No counterpart on the
+ * pages: it completes kda_prefill_noalloc, whose workspace the caller cannot
+ * name. */
+kda_status_t kda_prefill_noalloc_device_status(int32_t* out, void* stream);
 
 /*
  * kda_prefill from HOST buffers, end to end: the inputs are copied to the
@@ -308,7 +321,13 @@ kda_status_t kda_prefill_host(const kda_prefill_host_args* args, void* ws, size_
 /* Copies the workspace status word of the last kda_prefill that used `ws`
  * to *out (host), synchronising `stream`.  0 = clean; otherwise a bitwise OR
  * of 1 (malformed cu_seqlens), 2 (malformed boundary positions), 4 (chunk
- * table overflow), 8 (bounded wait expired). */
+ * table overflow), 8 (bounded wait expired), 16 (tensor-core path only: a
+ * chunk's total decay in some key channel fell below 2^-250, about e^-173,
+ * i.e. more than ~2.7 nats of log-decay per token on average over 64 tokens;
+ * its operands leave the bf16 range and the results of such chunks are not
+ * reliable -- fp32 inputs take the CUDA-core path, which has no such limit).
+ * Below that bound the tensor-core path is exact in range: each channel's
+ * decay factors are referred to half its chunk total. */
 kda_status_t kda_prefill_device_status(const void* ws, int32_t* out, void* stream);
 
 /* Host helper: snapshot slot offsets.  From host copies of cu_seqlens [n+1],
@@ -349,8 +368,16 @@ int64_t kda_snapshot_plan(const int64_t* h_cu_seqlens, int32_t n, int64_t interv
  *     others from the latest back, and a reservation never evicts a row it
  *     placed itself nor keep_row (the row the prefill resumes from, so that
  *     its initial state and its snapshots do not overlap; -1 = none).
- *     Returns the number of rows assigned, -1 on invalid arguments.  An entry is valid once the prefill that writes its row has
- *     run (order lookups' use of a row after it, e.g. on one stream).
+ *     Returns the number of rows assigned, -1 on invalid arguments.  An
+ *     entry is valid once the prefill that writes its row has run (order
+ *     lookups' use of a row after it, e.g. on one stream).
+ *   - A reserved entry is indexed at once.  If the prefill meant to write
+ *     its rows fails (an error status, or a nonzero device status word), the
+ *     caller must pass those rows to kda_prefix_cache_forget, which drops
+ *     their entries and returns the rows to the free list, so that no later
+ *     lookup resumes from a state that was never written.  Entries -1 (and
+ *     rows not holding an entry) are ignored; returns the number of rows
+ *     freed, -1 on invalid arguments (a row outside [-1, rows)).
  *   - Calls on one cache are serialised by an internal lock.
  */
 typedef struct kda_prefix_cache kda_prefix_cache;
@@ -363,6 +390,7 @@ int64_t kda_prefix_cache_lookup(kda_prefix_cache* cache, const int32_t* tokens, 
 int64_t kda_prefix_cache_reserve(kda_prefix_cache* cache, const int32_t* tokens, int64_t n,
                                  const int64_t* pos, const uint8_t* is_boundary, int64_t m,
                                  int32_t keep_row, int32_t* rows_out);
+int64_t kda_prefix_cache_forget(kda_prefix_cache* cache, const int32_t* rows, int64_t m);
 
 /*
  * One decode step for a batch of independent rows ("constant decode": a

@@ -213,4 +213,20 @@ int64_t kda_prefix_cache_reserve(kda_prefix_cache* c, const int32_t* tokens, int
   return placed;
 }
 
+int64_t kda_prefix_cache_forget(kda_prefix_cache* c, const int32_t* rows, int64_t m) {
+  if (!c || m < 0 || (m > 0 && !rows)) return -1;
+  for (int64_t i = 0; i < m; ++i)
+    if (rows[i] < -1 || rows[i] >= (int64_t)c->rows.size()) return -1;
+  std::lock_guard<std::mutex> lock(c->mu);
+  int64_t freed = 0;
+  for (int64_t i = 0; i < m; ++i) {
+    const int32_t r = rows[i];
+    if (r < 0 || !c->rows[r].live) continue;  // -1 entries of a reservation, or already free
+    c->drop(r);
+    c->free_rows.push_back(r);
+    ++freed;
+  }
+  return freed;
+}
+
 }  // extern "C"

@@ -31,6 +31,7 @@ _STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED"
                  3: "KDA_ERR_WORKSPACE", 4: "KDA_ERR_CUDA", 5: "KDA_ERR_TIMEOUT",
                  6: "KDA_ERR_DEVICE_DATA"}
 EXPORTED = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_noalloc",
+            "kda_prefill_noalloc_device_status", "kda_prefix_cache_forget",
             "kda_prefill_host_workspace_size", "kda_prefill_host",
             "kda_prefix_cache_create", "kda_prefix_cache_destroy", "kda_prefix_cache_entries",
             "kda_prefix_cache_lookup", "kda_prefix_cache_reserve",
@@ -130,6 +131,10 @@ def lib() -> ctypes.CDLL:
             L.kda_prefix_cache_reserve.restype = c_i64
             L.kda_prefill_noalloc.argtypes = [ctypes.POINTER(PrefillArgs), c_vp]
             L.kda_prefill_noalloc.restype = ctypes.c_int
+            L.kda_prefill_noalloc_device_status.argtypes = [ctypes.POINTER(c_i32), c_vp]
+            L.kda_prefill_noalloc_device_status.restype = ctypes.c_int
+            L.kda_prefix_cache_forget.argtypes = [c_vp, c_vp, c_i64]
+            L.kda_prefix_cache_forget.restype = c_i64
             L.kda_prefill_device_status.argtypes = [c_vp, ctypes.POINTER(c_i32), c_vp]
             L.kda_prefill_device_status.restype = ctypes.c_int
             L.kda_snapshot_plan.argtypes = [c_vp, c_i32, c_i64, c_vp, c_vp, c_vp]
@@ -229,21 +234,45 @@ def make_layer_args(*, rows, H, dk, dv, dtype, conv_weights=None, conv_silu=Fals
     return la
 
 
+def _check_shapes(q, k, v, g, b, cu_seqlens, o, initial_state, final_state):
+    """Shapes of the per-token tensors and of the states, from q's [T, H, dk]
+    and v's dv.  The C ABI receives bare pointers and cannot check them, so a
+    wrong shape would make the kernels (or the host copies) run past a buffer:
+    every shape is checked before any pointer is taken."""
+    if q.dim() != 3 or v.dim() != 3:
+        raise ValueError(f"q and v must be [T, H, d], got {tuple(q.shape)} and {tuple(v.shape)}")
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError(f"cu_seqlens must be [N + 1] with N >= 1, got {tuple(cu_seqlens.shape)}")
+    N = cu_seqlens.numel() - 1
+    gshape = (T, H) if g.dim() == 2 else (T, H, dk)  # [T, H]: one decay per token and head
+    checks = [("k", k, (T, H, dk)), ("g", g, gshape), ("v", v, (T, H, dv)), ("b", b, (T, H)),
+              ("o", o, (T, H, dv))]
+    checks += [(name, t, (N, H, dk, dv)) for name, t in (("initial_state", initial_state),
+                                                          ("final_state", final_state))
+               if t is not None]
+    for name, t, shp in checks:
+        if tuple(t.shape) != shp:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shp}")
+    return T, H, dk, dv, N
+
+
 def make_prefill_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=None,
                       final_state=None, snapshot_interval=0, boundary_pos=None,
                       cu_boundaries=None, cu_snapshots=None, snapshots=None,
                       scan_segments=0, snapshot_slot_map=None, wait_limit_ns=0,
                       layer: LayerArgs | None = None) -> PrefillArgs:
-    T, H, dk = q.shape
-    dv = v.shape[-1]
+    T, H, dk, dv, N = _check_shapes(q, k, v, g, b, cu_seqlens, o, initial_state, final_state)
     dt = q.dtype
-    gshape = (T, H) if g.dim() == 2 else (T, H, dk)  # [T, H]: one decay per token and head
-    for name, t, shp in (("k", k, (T, H, dk)), ("g", g, gshape), ("v", v, (T, H, dv)),
-                         ("b", b, (T, H)), ("o", o, (T, H, dv))):
-        if tuple(t.shape) != shp:
-            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shp}")
+    if snapshots is not None and (snapshots.dim() != 4 or tuple(snapshots.shape[1:]) != (H, dk, dv)):
+        raise ValueError(f"snapshots has shape {tuple(snapshots.shape)}, expected [rows, {H}, {dk}, {dv}]")
+    if cu_snapshots is not None and tuple(cu_snapshots.shape) != (N + 1,):
+        raise ValueError(f"cu_snapshots has shape {tuple(cu_snapshots.shape)}, expected ({N + 1},)")
+    if cu_boundaries is not None and tuple(cu_boundaries.shape) != (N + 1,):
+        raise ValueError(f"cu_boundaries has shape {tuple(cu_boundaries.shape)}, expected ({N + 1},)")
     a = PrefillArgs()
-    a.num_seqs = cu_seqlens.numel() - 1
+    a.num_seqs = N
     a.num_heads, a.dk, a.dv, a.total_tokens = H, dk, dv, T
     a.cu_seqlens = _ptr(cu_seqlens, torch.int64, "cu_seqlens")
     a.in_dtype = _dtype_code(dt)
@@ -297,16 +326,10 @@ def make_prefill_host_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_s
                            final_state=None, segments=0, copy_in_stream=None,
                            copy_out_stream=None) -> PrefillHostArgs:
     """kda_prefill_host_args over HOST tensors (pinned for overlapped copies)."""
-    T, H, dk = q.shape
-    dv = v.shape[-1]
+    T, H, dk, dv, N = _check_shapes(q, k, v, g, b, cu_seqlens, o, initial_state, final_state)
     dt = q.dtype
-    gshape = (T, H) if g.dim() == 2 else (T, H, dk)  # [T, H]: one decay per token and head
-    for name, t, shp in (("k", k, (T, H, dk)), ("g", g, gshape), ("v", v, (T, H, dv)),
-                         ("b", b, (T, H)), ("o", o, (T, H, dv))):
-        if tuple(t.shape) != shp:
-            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shp}")
     a = PrefillHostArgs()
-    a.num_seqs = cu_seqlens.numel() - 1
+    a.num_seqs = N
     a.num_heads, a.dk, a.dv, a.total_tokens = H, dk, dv, T
     a.cu_seqlens = _host_ptr(cu_seqlens, torch.int64, "cu_seqlens")
     a.in_dtype = _dtype_code(dt)
@@ -338,6 +361,14 @@ def kda_prefill_noalloc(args: PrefillArgs, stream=None) -> None:
     """kda_prefill on the library's fixed workspace (for callers that cannot
     allocate device memory at the call); see include/kda.h for its limits."""
     _check(lib().kda_prefill_noalloc(ctypes.byref(args), _stream(stream)), "kda_prefill_noalloc")
+
+
+def kda_prefill_noalloc_device_status(stream=None) -> int:
+    """The status word of the last kda_prefill_noalloc on the current device."""
+    out = c_i32(0)
+    _check(lib().kda_prefill_noalloc_device_status(ctypes.byref(out), _stream(stream)),
+           "kda_prefill_noalloc_device_status")
+    return int(out.value)
 
 
 def kda_prefill_device_status(workspace: torch.Tensor, stream=None) -> int:
@@ -374,14 +405,25 @@ def kda_decode_step(q, k, v, g, b, state, o, state_slots=None, scale=1.0, stream
     convolution runs on q, k, v; conv_window (q, k, v) [slots, W-1, H, d] holds
     each slot's window and is advanced in place.  out_gate [B, H, dv] or
     [B, H] gates o."""
+    if q.dim() != 3 or v.dim() != 3 or state.dim() != 4:
+        raise ValueError("q, v must be [B, H, d] and state [slots, H, dk, dv]")
     B, H, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
+    if tuple(state.shape[1:]) != (H, dk, dv):
+        raise ValueError(f"state has shape {tuple(state.shape)}, expected [slots, {H}, {dk}, {dv}]")
+    gshape = (B, H) if g.dim() == 2 else (B, H, dk)  # [B, H]: one decay per row and head
+    for name, t, shp in (("k", k, (B, H, dk)), ("g", g, gshape), ("v", v, (B, H, dv)),
+                         ("b", b, (B, H)), ("o", o, (B, H, dv))):
+        if tuple(t.shape) != shp:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shp}")
+    if state_slots is not None and tuple(state_slots.shape) != (B,):
+        raise ValueError(f"state_slots has shape {tuple(state_slots.shape)}, expected ({B},)")
+    if status is not None and status.numel() < 1:
+        raise ValueError("status needs one int32")
     a = DecodeArgs()
     a.batch, a.num_heads, a.dk, a.dv = B, H, dk, dv
     a.num_slots = state.shape[0]
-    if tuple(state.shape[1:]) != (H, dk, dv):
-        raise ValueError(f"state has shape {tuple(state.shape)}, expected [slots, {H}, {dk}, {dv}]")
     a.in_dtype = _dtype_code(dt)
     a.scale = float(scale)
     a.q, a.k, a.v = _ptr(q, dt, "q"), _ptr(k, dt, "k"), _ptr(v, dt, "v")
@@ -405,8 +447,16 @@ def kda_prep(q, k, g, b, cu_seqlens, qhat, khat, G, beta, stream=None, conv_weig
     """The preparation step.  With conv_weights (wq, wk, ...) [W, H, dk] q and k
     pass through the short convolution first (conv_window: (q, k) windows
     [N, W-1, H, dk] before each sequence, or None)."""
+    if q.dim() != 3 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("q must be [T, H, dk] and cu_seqlens [N + 1]")
     T, H, dk = q.shape
     dt = q.dtype
+    gshape = (T, H) if g.dim() == 2 else (T, H, dk)  # [T, H]: one decay per token and head
+    for name, t, shp in (("k", k, (T, H, dk)), ("g", g, gshape), ("b", b, (T, H)),
+                         ("qhat", qhat, (T, H, dk)), ("khat", khat, (T, H, dk)),
+                         ("G", G, (T, H, dk)), ("beta", beta, (T, H))):
+        if tuple(t.shape) != shp:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shp}")
     a = PrepArgs()
     a.num_seqs, a.num_heads, a.dk, a.total_tokens = cu_seqlens.numel() - 1, H, dk, T
     a.cu_seqlens = _ptr(cu_seqlens, torch.int64, "cu_seqlens")
@@ -652,6 +702,16 @@ class PrefixCache:
             raise ValueError("kda_prefix_cache_reserve rejected the arguments")
         return rows
 
+    def forget(self, rows) -> int:
+        """Drops the entries of ``rows`` (as returned by reserve; -1 entries
+        are ignored) and frees their rows: for a prefill that failed before
+        writing them.  Returns the number of rows freed."""
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+        n = lib().kda_prefix_cache_forget(self._h, r.ctypes.data if r.size else None, r.size)
+        if n < 0:
+            raise ValueError("kda_prefix_cache_forget rejected the arguments")
+        return int(n)
+
 
 def prefill_cached(cache: PrefixCache, pool, tokens, q, k, v, g, b, *, interval=4096,
                    scale=1.0, stream=None):
@@ -682,7 +742,11 @@ def prefill_cached(cache: PrefixCache, pool, tokens, q, k, v, g, b, *, interval=
                  boundary_pos=rel.to(dev), cu_boundaries=cu_b.to(dev),
                  host_cu_seqlens=hcu, host_boundary_pos=rel, host_cu_boundaries=cu_b,
                  snapshot_pool=pool, snapshot_slot_map=torch.from_numpy(rows).to(dev))
-    pr.run(stream)
+    try:
+        pr.run(stream)
+    except Exception:
+        cache.forget(rows)  # the rows were never written: no lookup may resume from them
+        raise
     return p, pr.o, pr.final_state
 
 

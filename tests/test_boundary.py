@@ -358,3 +358,66 @@ def test_layer_args_shapes_checked_in_the_binding(kda):
     # shapes right: the host tensors are then refused as not on the device
     with pytest.raises(ValueError, match="CUDA"):
         kda.make_layer_args(conv_weights=taps, **kw)
+
+
+def test_state_and_snapshot_shapes_checked_in_the_binding(kda):
+    """The C ABI takes bare pointers and cannot see how large a state buffer
+    is, so the binding checks every shape before it takes a pointer: initial
+    and final states [N, H, dk, dv], snapshots [rows, H, dk, dv], the
+    snapshot and boundary offsets [N + 1] -- for the device call and the
+    host-buffer call -- and the decode and prep tensors.  Host tensors with
+    the right shapes get as far as the device check."""
+    import torch
+    T, H, dk, dv, N = 10, 2, 16, 8, 3
+    x = dict(q=torch.zeros(T, H, dk), k=torch.zeros(T, H, dk), v=torch.zeros(T, H, dv),
+             g=torch.zeros(T, H, dk), b=torch.zeros(T, H),
+             cu_seqlens=torch.tensor([0, 3, 7, 10]), o=torch.zeros(T, H, dv))
+    good = torch.zeros(N, H, dk, dv)
+    args = [x[n] for n in ("q", "k", "v", "g", "b", "cu_seqlens", "o")]
+    for make in (kda.make_prefill_args, kda.make_prefill_host_args):
+        for kw in (dict(initial_state=torch.zeros(N - 1, H, dk, dv)),
+                   dict(final_state=torch.zeros(N, H, dv, dk)),
+                   dict(initial_state=torch.zeros(N, H, dk, dv + 1))):
+            name = next(iter(kw))
+            with pytest.raises(ValueError, match=name):
+                make(*args, **kw)
+        with pytest.raises(ValueError, match="o has shape"):
+            make(*args[:6], torch.zeros(T, H, dk + 1), initial_state=good)
+    with pytest.raises(ValueError, match="snapshots"):
+        kda.make_prefill_args(*args, snapshots=torch.zeros(4, H, dk, dv - 1))
+    with pytest.raises(ValueError, match="cu_snapshots"):
+        kda.make_prefill_args(*args, snapshots=torch.zeros(4, H, dk, dv),
+                              cu_snapshots=torch.zeros(N, dtype=torch.int64))
+    with pytest.raises(ValueError, match="cu_boundaries"):
+        kda.make_prefill_args(*args, boundary_pos=torch.zeros(2, dtype=torch.int64),
+                              cu_boundaries=torch.zeros(N + 2, dtype=torch.int64))
+    # right shapes: refused only because the tensors are not on the device
+    with pytest.raises(ValueError, match="CUDA"):
+        kda.make_prefill_args(*args, initial_state=good, final_state=good,
+                              snapshots=torch.zeros(4, H, dk, dv),
+                              cu_snapshots=torch.zeros(N + 1, dtype=torch.int64))
+    ha = kda.make_prefill_host_args(*args, initial_state=good, final_state=good)
+    assert ha.num_seqs == N and ha.total_tokens == T
+    # decode: every tensor against q's [B, H, dk] and v's dv
+    B = 4
+    d = dict(q=torch.zeros(B, H, dk), k=torch.zeros(B, H, dk), v=torch.zeros(B, H, dv),
+             g=torch.zeros(B, H, dk), b=torch.zeros(B, H))
+    st, o = torch.zeros(6, H, dk, dv), torch.zeros(B, H, dv)
+    dargs = [d[n] for n in "qkvgb"]
+    with pytest.raises(ValueError, match="state"):
+        kda.kda_decode_step(*dargs, torch.zeros(6, H, dv, dk), o)
+    with pytest.raises(ValueError, match="o has shape"):
+        kda.kda_decode_step(*dargs, st, torch.zeros(B + 1, H, dv))
+    with pytest.raises(ValueError, match="b has shape"):
+        kda.kda_decode_step(*dargs[:4], torch.zeros(B, H + 1), st, o)
+    with pytest.raises(ValueError, match="state_slots"):
+        kda.kda_decode_step(*dargs, st, o, state_slots=torch.zeros(B + 1, dtype=torch.int32))
+    with pytest.raises(ValueError, match="CUDA"):
+        kda.kda_decode_step(*dargs, st, o)
+    # prep: outputs [T, H, dk] and beta [T, H]
+    f = torch.zeros(T, H, dk)
+    with pytest.raises(ValueError, match="beta"):
+        kda.kda_prep(x["q"], x["k"], x["g"], x["b"], x["cu_seqlens"], f, f, f, torch.zeros(T, H + 1))
+    with pytest.raises(ValueError, match="G has shape"):
+        kda.kda_prep(x["q"], x["k"], x["g"], x["b"], x["cu_seqlens"], f, f, torch.zeros(T, H, dk - 1),
+                     torch.zeros(T, H))

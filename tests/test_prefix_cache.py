@@ -96,3 +96,28 @@ def test_invalid_arguments(kda):
         c.reserve(a, [10], keep_row=2)
     L = kda.lib()
     assert L.kda_prefix_cache_entries(None) == -1
+
+
+def test_forget_frees_rows_of_a_failed_prefill(kda):
+    """A reservation indexes its entries at once; if the prefill that was to
+    write them fails, forget() drops them so no lookup resumes from an
+    unwritten row, and the rows go back to the free list."""
+    c = kda.PrefixCache(4)
+    a = toks(256, 11)
+    ok = c.reserve(a[:128], [64, 128], [False, True])
+    assert c.lookup(a) == (128, ok[1])
+    failed = c.reserve(a, [192, 256], [False, True])
+    assert (failed >= 0).all() and c.entries() == 4
+    assert c.lookup(a) == (256, failed[1])
+    assert c.forget(np.concatenate([failed, [-1]])) == 2   # -1 entries are ignored
+    assert c.entries() == 2
+    assert c.lookup(a) == (128, ok[1])                       # back to the written prefix
+    assert c.forget(failed) == 0                             # nothing left to drop
+    # the freed rows are reused before any kept entry is evicted
+    again = c.reserve(toks(200, 12), [100, 200], [False, True])
+    assert sorted(again.tolist()) == sorted(failed.tolist())
+    assert c.lookup(a) == (128, ok[1])
+    with pytest.raises(ValueError):
+        c.forget([4])                                        # outside the pool
+    with pytest.raises(ValueError):
+        c.forget([-2])

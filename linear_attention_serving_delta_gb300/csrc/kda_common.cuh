@@ -21,6 +21,7 @@ enum : int32_t {
   kFlagBadBoundaries = 2,
   kFlagChunkOverflow = 4,
   kFlagTimeout = 8,
+  kFlagDecayRange = 16,  // tensor-core path: a chunk decayed past its operands' range
 };
 
 // One entry of the chunk table: a run of <= kChunk tokens of one sequence

@@ -2,9 +2,18 @@
 // translation units of libkda (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap and the enums of its encoder (fetched at run time)
+
 #include "kda_common.cuh"
 
 namespace kda {
+
+// cuTensorMapEncodeTiled, fetched from the driver once (null if unavailable)
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled();
 
 struct PlanParams {
   int32_t num_seqs;

@@ -17,9 +17,18 @@
 //                              O = scale (Qp S0 + A_qk U)
 //                              S_end = Diag(Gamma_L) S0 + Kr^T U
 //
-// The factored exponentials exp(G_i) exp(-G_j) stay finite while a chunk's
-// total log-decay per channel is above about -80; the fp32 CUDA-core path
-// (kda_simt.cu) has no such limit.
+// Exponent range.  A_kk and A_qk need exp(G_i - G_j) for j <= i, formed by
+// the tensor cores as the product of a row factor and a column factor.  K2
+// keeps G in log2 units.  While a channel's total decay over the chunk G_L
+// stays above 2^-120 the factors are referred to the chunk start: row
+// factors 2^G_i <= 1 and column factors 2^-G_j <= 2^120.  Past that the
+// channel takes a power-of-two reference s = round(G_L / 2) (half the
+// chunk's decay): row factors 2^(G_i - s), column factors 2^(s - G_j), both
+// inside 2^-126 .. 2^126 while G_L stays above 2^-250 (about e^-173).  Only
+// MMA 1 sees these factors; the record keeps Qp, Kp and Kr referred to the
+// chunk start (Gamma <= 1, so they can only underflow, which is harmless).
+// A chunk past that range raises status flag 16 (its results are not
+// reliable); the fp32 CUDA-core path (kda_simt.cu) has no such limit.
 #pragma once
 
 #include "kda_internal.cuh"
@@ -70,10 +79,29 @@ __device__ __forceinline__ float bf16_at(const uint4& v, int j) {
 
 __device__ __forceinline__ void flag(int32_t* status, int32_t f) { atomicOr(status, f); }
 
-// alpha = exp(-softplus(g)) = 1 / (1 + e^g) with the fast exp and division
-// intrinsics (relative error a few 1e-7; the operands it feeds are rounded to
-// bf16).  e^g overflowing to +inf gives alpha = 0.
-__device__ __forceinline__ float alpha_fast(float g) { return __fdividef(1.f, 1.f + __expf(g)); }
+// 2^x with the hardware approximation (ex2.approx: relative error about
+// 2^-22), results below 2^-126 flushed to zero (every use keeps x >= -126 or
+// needs no more than that)
+__device__ __forceinline__ float exp2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;  // 1 / ln 2
+// A chunk whose total decay in some channel is below 2^-kMaxChunkDecayLog2
+// is past the range of the tensor-core operands (status flag 16)
+constexpr float kMaxChunkDecayLog2 = 250.f;
+// Below a total decay of 2^-kScaleFromLog2 in a channel, its factors are
+// referred to half the chunk's decay instead of the chunk start
+constexpr float kScaleFromLog2 = 120.f;
+
+// log2 alpha = -softplus(g) / ln 2, softplus(g) = max(g, 0) + ln(1 + e^-|g|),
+// with the fast base-2 exponential and logarithm (absolute error a few 1e-7
+// per token; the operands it feeds are rounded to bf16).  g = -inf gives 0
+// (alpha = 1), a large g gives -g / ln 2 without overflow.
+__device__ __forceinline__ float log2_alpha_fast(float g) {
+  return -fmaf(fmaxf(g, 0.f), kLog2e, __log2f(1.f + exp2_fast(-fabsf(g) * kLog2e)));
+}
 
 // y sigmoid(y) = y / (1 + e^-y), the activation after the short convolution,
 // with the same intrinsics (its output is rounded to bf16 right after); a

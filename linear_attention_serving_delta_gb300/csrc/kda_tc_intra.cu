@@ -22,8 +22,6 @@
 // kda_tc_common.cuh.
 #include "kda_tc_common.cuh"
 
-#include <cuda.h>  // CUtensorMap and the enums of its encoder (fetched at run time)
-
 namespace kda {
 namespace tcp {
 namespace {
@@ -59,7 +57,9 @@ struct Smem {
   // decay totals of each token quarter [4][128]
   static constexpr uint32_t MISC = AKK + 64 * kAs * 4;
   // + the per-token decay logits of the item (gate per head), [64]
-  static constexpr uint32_t BYTES = MISC + (3 * 64 + 2 * 2 * 64 + 4 * 128 + 64) * 4;
+  // + 2^s of each channel's decay reference and 2^(G_L - s) (see the
+  // operands), [2][128]
+  static constexpr uint32_t BYTES = MISC + (3 * 64 + 2 * 2 * 64 + 4 * 128 + 64 + 2 * 128) * 4;
 };
 static_assert(Smem::B1 % 16 == 0 && Smem::B2 % 16 == 0 && Smem::A2 % 16 == 0 && Smem::AKK % 16 == 0,
               "operand tiles and float4 arrays are 16-byte aligned");
@@ -68,6 +68,17 @@ static_assert(16 * kB1Lbo >= 64 * kTs * 4, "T fits in the Kn tile");
 static_assert(16 * kAkStage <= 64 * kAs * 4, "the Kr^T staging fits in the A_kk tile");
 static_assert(32 * kB2Sbo >= 64 * 128 * 4, "the U~ staging fits in the B2 tile");
 
+// 8 floats from shared memory (16-byte aligned), read where the call stands
+// (volatile: the compiler does not merge the reads of several calls, so it
+// keeps no copy in registers between them).  The values are written before
+// a barrier that precedes every call.
+__device__ __forceinline__ void lds_f8(const float* p, float* x) {
+  const uint32_t a = smem_u32(p);
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]) : "r"(a));
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(x[4]), "=f"(x[5]), "=f"(x[6]), "=f"(x[7]) : "r"(a + 16));
+}
 __device__ __forceinline__ void st_s16(uint8_t* base, uint32_t off, uint4 v) {
   *reinterpret_cast<uint4*>(base + off) = v;
 }
@@ -432,6 +443,8 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
   float* nrm = beta + 64;        // [q/k][channel half][64]
   float* qtot = nrm + 2 * 2 * 64;  // [token quarter][128]
   float* gtok = qtot + 4 * 128;    // [64] decay logits of this item's tokens (gate per head)
+  float* sref = gtok + 64;         // [128] 2^s per channel (decay reference)
+  float* sglr = sref + 128;        // [128] 2^(G_L - s) per channel
 
   if (warp == 0) tmem_alloc(&tmem_base, 256);
   if (tid == 0) {
@@ -509,35 +522,36 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
       }
     }
 
-    // ---- cumulative decay Gamma_i = prod_{m<=i} alpha_m, alpha = 1 / (1 + e^g)
-    // (= exp(-softplus(g))): a product over this thread's 4 tokens, a scan
-    // across the warp's 4 token blocks (lanes 8 apart), then across the token
-    // quarters through shared memory (below)
+    // ---- cumulative decay G_i = sum_{m<=i} log2 alpha_m (alpha = exp(-softplus(g)),
+    // log2 units): a sum over this thread's 4 tokens, a scan across the
+    // warp's 4 token blocks (lanes 8 apart), then across the token quarters
+    // through shared memory (below).  In log space G does not underflow,
+    // whatever the decay.
     float Gm[4][8], qtot_own[8];
-    // the scan of one channel: a[r] = alpha of token i0 + r -> Gm[r][j], qtot_own[j]
+    // the scan of one channel: a[r] = log2 alpha of token i0 + r -> Gm[r][j], qtot_own[j]
     auto scan_channel = [&](const float* a, int j) {
-      float run = 1.f;
+      float run = 0.f;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        run *= a[r];
+        run += a[r];
         Gm[r][j] = run;
       }
       float inc = run;
       float y = __shfl_up_sync(0xffffffffu, inc, 8);
-      if (tb >= 1) inc *= y;
+      if (tb >= 1) inc += y;
       y = __shfl_up_sync(0xffffffffu, inc, 16);
-      if (tb >= 2) inc *= y;
+      if (tb >= 2) inc += y;
       float ex = __shfl_up_sync(0xffffffffu, inc, 8);
-      if (tb == 0) ex = 1.f;
+      if (tb == 0) ex = 0.f;
 #pragma unroll
-      for (int r = 0; r < 4; ++r) Gm[r][j] *= ex;
-      qtot_own[j] = __shfl_sync(0xffffffffu, inc, 24 + cg);  // this quarter's product
+      for (int r = 0; r < 4; ++r) Gm[r][j] += ex;
+      qtot_own[j] = __shfl_sync(0xffffffffu, inc, 24 + cg);  // this quarter's sum
     };
     if constexpr (kHeadGate) {
       // one decay per token: the scan of one channel, shared by all eight
       float a[4];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) a[r] = i0 + r < len ? alpha_fast(gtok[i0 + r]) : 1.f;
+      for (int r = 0; r < 4; ++r) a[r] = i0 + r < len ? log2_alpha_fast(gtok[i0 + r]) : 0.f;
       scan_channel(a, 0);
 #pragma unroll
       for (int j = 1; j < 8; ++j) {
@@ -553,7 +567,7 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
       for (int j = 0; j < 8; ++j) {
         float a[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) a[r] = i0 + r < len ? alpha_fast(bf16_at(graw[r], j)) : 1.f;
+        for (int r = 0; r < 4; ++r) a[r] = i0 + r < len ? log2_alpha_fast(bf16_at(graw[r], j)) : 0.f;
         scan_channel(a, j);
       }
     }
@@ -620,12 +634,17 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     // the staging is free): the raw 16 bytes are one core-matrix row
 #pragma unroll
     for (int r = 0; r < 4; ++r) st_s16(B2, mnmajor_off(128 + c0, i0 + r, kB2Sbo), vraw[r]);
-    // the decay entering this token quarter, and the chunk total Gamma_L
-    float GLm[8];
+    // the decay entering this token quarter, and the chunk total G_L; then
+    // per channel the reference s, 2^s and 2^(G_L - s); Gm becomes t = G - s.
+    // s = 0 while G_L >= -kScaleFromLog2 (the factors 2^G and 2^-G of a
+    // chunk-start reference are then normal); past that s = round(G_L / 2),
+    // clamped so that 2^s stays normal
+    float two_s[8], glr[8];
+    bool rescale = false;  // some channel of this item has s != 0
     {
       float pre[8], tot[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) pre[j] = tot[j] = 1.f;
+      for (int j = 0; j < 8; ++j) pre[j] = tot[j] = 0.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float4 a = *reinterpret_cast<const float4*>(qtot + q * 128 + c0);
@@ -633,56 +652,83 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
         const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          if (q < qt) pre[j] *= x[j];
-          tot[j] *= x[j];
+          if (q < qt) pre[j] += x[j];
+          tot[j] += x[j];
         }
       }
+      bool out_of_range = false;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        GLm[j] = tot[j];
+        out_of_range |= tot[j] < -kMaxChunkDecayLog2;
+        const float sj = tot[j] < -kScaleFromLog2 ? fmaxf(rintf(0.5f * tot[j]), -126.f) : 0.f;
+        rescale |= sj != 0.f;
+        two_s[j] = __int_as_float(((int)sj + 127) << 23);
+        glr[j] = exp2_fast(tot[j] - sj);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) Gm[r][j] *= pre[j];
+        for (int r = 0; r < 4; ++r) Gm[r][j] += pre[j] - sj;
+      }
+      // warps 0 and 1 hold every channel's total (uniform per warp)
+      if (qt == 0 && __any_sync(0xffffffffu, out_of_range) && lane == 0) flag(p.status, kFlagDecayRange);
+      if (qt == 0 && tb == 0) {  // warps 0-1, lanes 0-7: Gamma_L and 2^s of all 128 channels
+        *reinterpret_cast<float4*>(sref + c0) = make_float4(two_s[0], two_s[1], two_s[2], two_s[3]);
+        *reinterpret_cast<float4*>(sref + c0 + 4) = make_float4(two_s[4], two_s[5], two_s[6], two_s[7]);
+        *reinterpret_cast<float4*>(sglr + c0) = make_float4(glr[0], glr[1], glr[2], glr[3]);
+        *reinterpret_cast<float4*>(sglr + c0 + 4) = make_float4(glr[4], glr[5], glr[6], glr[7]);
+        float* gl = reinterpret_cast<float*>(rec + Rec::GL) + c0;
+        *reinterpret_cast<float4*>(gl) = make_float4(glr[0] * two_s[0], glr[1] * two_s[1],
+                                                     glr[2] * two_s[2], glr[3] * two_s[3]);
+        *reinterpret_cast<float4*>(gl + 4) = make_float4(glr[4] * two_s[4], glr[5] * two_s[5],
+                                                         glr[6] * two_s[6], glr[7] * two_s[7]);
       }
     }
-    __syncthreads();
+    rescale = __syncthreads_or(rescale);
 
-    // ---- operands Kp, Qp (A1), Kn (B1), Kp (B2 MN-major rows 0-127), Kr
-    // (staged MN-major in the A_kk tile for the record's AK)
+    // ---- operands.  With a = 2^t (t = G - s): MMA 1 takes Kp' = k^ a, Qp' =
+    // q^ a (A1) and Kn' = k^ / a (B1), whose products are those of Kp Kn^T
+    // and Qp Kn^T (the 2^s cancel) with every factor inside the normal range;
+    // MMA 2 takes Kp = k^ Gamma (B2 MN-major rows 0-127, Gamma = a 2^s) and
+    // the record Kr = k^ Gamma_L / Gamma = Kn' 2^(G_L - s) (staged MN-major
+    // in the A_kk tile for the record's AK).  The record's Qp = q^ Gamma is
+    // Qp' 2^s: where some s != 0, A1's rows 64-127 are scaled by 2^s once
+    // MMA 1 has read them (an exact power-of-two scaling)
     uint8_t* AKS = sm + Smem::AKK;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int i = i0 + r;
       const float ik = inv_k[i], iq = inv_q[i];
       const uint4 qr = qraw[r], kr = kraw[r];
-      float kp[8], qp[8], kn[8], kx[8];
+      // the channels' 2^s and 2^(G_L - s), re-read for every row (kept out of
+      // registers across the loop)
+      float ts[8], tg[8];
+      lds_f8(sref + c0, ts);
+      lds_f8(sglr + c0, tg);
+      float kp[8], ks[8], qs[8], kn[8], kx[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float kh = bf16_at(kr, j) * ik;
         const float qh = bf16_at(qr, j) * iq;
-        const float gam = Gm[r][j];
-        kp[j] = kh * gam;
-        qp[j] = qh * gam;
-        kn[j] = __fdividef(kh, gam);
-        kx[j] = kn[j] * GLm[j];
+        const float a = exp2_fast(Gm[r][j]);
+        ks[j] = kh * a;
+        qs[j] = qh * a;
+        kp[j] = ks[j] * ts[j];
+        kn[j] = kh * exp2_fast(-Gm[r][j]);
+        kx[j] = kn[j] * tg[j];
       }
-      const uint4 kpv = make_uint4(pack_bf16(kp[0], kp[1]), pack_bf16(kp[2], kp[3]),
-                                   pack_bf16(kp[4], kp[5]), pack_bf16(kp[6], kp[7]));
-      st_s16(A1, kmaj(i, c0, kA1Lbo), kpv);
-      st_s16(B2, mnmajor_off(c0, i, kB2Sbo), kpv);
+      st_s16(A1, kmaj(i, c0, kA1Lbo),
+             make_uint4(pack_bf16(ks[0], ks[1]), pack_bf16(ks[2], ks[3]), pack_bf16(ks[4], ks[5]),
+                        pack_bf16(ks[6], ks[7])));
+      st_s16(B2, mnmajor_off(c0, i, kB2Sbo),
+             make_uint4(pack_bf16(kp[0], kp[1]), pack_bf16(kp[2], kp[3]), pack_bf16(kp[4], kp[5]),
+                        pack_bf16(kp[6], kp[7])));
       st_s16(A1, kmaj(64 + i, c0, kA1Lbo),
-             make_uint4(pack_bf16(qp[0], qp[1]), pack_bf16(qp[2], qp[3]), pack_bf16(qp[4], qp[5]),
-                        pack_bf16(qp[6], qp[7])));
+             make_uint4(pack_bf16(qs[0], qs[1]), pack_bf16(qs[2], qs[3]), pack_bf16(qs[4], qs[5]),
+                        pack_bf16(qs[6], qs[7])));
       st_s16(B1, kmaj(i, c0, kB1Lbo),
              make_uint4(pack_bf16(kn[0], kn[1]), pack_bf16(kn[2], kn[3]), pack_bf16(kn[4], kn[5]),
                         pack_bf16(kn[6], kn[7])));
       st_s16(AKS, mnmajor_off(c0, i, kAkStage),
              make_uint4(pack_bf16(kx[0], kx[1]), pack_bf16(kx[2], kx[3]), pack_bf16(kx[4], kx[5]),
                         pack_bf16(kx[6], kx[7])));
-    }
-    if (qt == 0 && tb == 0) {  // warps 0-1, lanes 0-7: the chunk totals of all 128 channels
-      float* gl = reinterpret_cast<float*>(rec + Rec::GL) + c0;
-      *reinterpret_cast<float4*>(gl) = make_float4(GLm[0], GLm[1], GLm[2], GLm[3]);
-      *reinterpret_cast<float4*>(gl + 4) = make_float4(GLm[4], GLm[5], GLm[6], GLm[7]);
     }
 
     fence_async_smem();
@@ -711,6 +757,21 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     ok = __syncthreads_and(mbar_wait_t<kPoll>(&bar_mma, 0, p.wait_ns));
     fence_after_sync();
     if (!ok) break;
+    if (rescale) {
+      // Qp = Qp' 2^s for the record (rows 64-127 of A1, this thread's 4 rows
+      // and 8 channels); the bulk copy that reads them comes after a barrier
+      const float4 s0 = *reinterpret_cast<const float4*>(sref + c0);
+      const float4 s1 = *reinterpret_cast<const float4*>(sref + c0 + 4);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        uint4* u = reinterpret_cast<uint4*>(A1 + kmaj(64 + i0 + r, c0, kA1Lbo));
+        const uint4 x = *u;
+        *u = make_uint4(pack_bf16(bf16_lo(x.x) * s0.x, bf16_hi(x.x) * s0.y),
+                        pack_bf16(bf16_lo(x.y) * s0.z, bf16_hi(x.y) * s0.w),
+                        pack_bf16(bf16_lo(x.z) * s1.x, bf16_hi(x.z) * s1.y),
+                        pack_bf16(bf16_lo(x.w) * s1.z, bf16_hi(x.w) * s1.w));
+      }
+    }
     {
       float d[32];
       const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + 32 * half;
@@ -859,24 +920,6 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
-// cuTensorMapEncodeTiled, fetched from the driver once
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
-                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                   CUtensorMapFloatOOBfill);
-EncodeTiledFn encode_tiled() {
-  static const EncodeTiledFn fn = [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return static_cast<EncodeTiledFn>(nullptr);
-    return reinterpret_cast<EncodeTiledFn>(f);
-  }();
-  return fn;
-}
-
 // [T][H][D] bf16 rows, box {128 channels, 1 head, `rows` tokens}, zero fill
 // outside [0, T) and, for a head of D = 64 channels, in channels 64-127: the
 // kernel then runs on the head zero-padded to 128 channels, which leaves
@@ -894,6 +937,23 @@ bool encode_rows(CUtensorMap* m, const void* base, int H, int64_t T, int D, uint
 }
 
 }  // namespace
+
+}  // namespace tcp
+
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+namespace tcp {
 
 cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream) {
   const bool head = p.gate_per_head != 0, conv = p.conv_width > 0;

@@ -224,12 +224,18 @@ decode_step(kda_decode_args a, const kda_layer_args l) {
   }
 }
 
-// ------------------------------------------------- dk, dv in {64, 128}
-// Persistent variant: one CTA per SM walks (row, head) items.  A ring of
-// shared-memory slots is filled by 1-D bulk copies (TMA engine) of each
-// item's state (64 KB for 128 x 128) plus its q, k, g, v rows, a few items
-// ahead (3 slots for 128 x 128, up to 8 for smaller states, so that about
-// 200 KB stay in flight per SM).
+// ------------------------------------------------- dk, dv in {64, 128, 256}
+// Persistent variant: one CTA per SM walks (row, head, column slice) items.
+// A ring of shared-memory slots is filled by copies (TMA engine) of each
+// item's state plus its q, k, g, v rows, a few items ahead (3 slots of 64 KB
+// states, up to 8 for smaller states, so that about 200 KB stay in flight
+// per SM).  A head of at most 64 KB of state (up to 128 x 128, or 256 x 64,
+// 64 x 256) is one item, its state one contiguous 1-D bulk copy; a larger
+// head (dk or dv = 256) is cut into slices of DVS value columns that hold
+// 64 KB each (256 x 64, 128 x 128), moved in and out by 2-D tensor-map
+// copies of the strided slice: the reductions over key channels are per
+// value column, so the slices of a head are independent (each reads the
+// head's whole q, k and g rows and its own columns of v).
 // Warps 0-7 compute; warp 8 is the producer: once the compute warps have
 // written an item's updated state into its slot, it sends the state back to
 // HBM with one 64 KB bulk copy, waits for that copy to read the slot and
@@ -249,16 +255,28 @@ constexpr int kComputeBarrier = 1;           // named barrier of warps 0-7
 // up to KDA_CONV_MAX - 1 window rows of each of q, k, v.  Warp w owns key
 // rows w + 8 i (i < RPW), lane l value columns CPL l .. CPL l + CPL - 1.
 constexpr int kWinRows = KDA_CONV_MAX - 1;
+// Value columns per item of a dk x dv head: at most 128 (a lane's 2 or 4
+// columns of a row are one 8- or 16-byte access) and at most 64 KB of state
+template <int DK, int DV>
+struct RingSlice {
+  static constexpr int CAP = 128 * 128 / DK < 128 ? 128 * 128 / DK : 128;
+  static constexpr int DVS = DV < CAP ? DV : CAP;
+  static constexpr int NS = DV / DVS;  // slices per head
+};
 template <typename TIn, bool kConv, int DK, int DV>
 struct Ring {
-  static_assert((DK == 64 || DK == 128) && (DV == 64 || DV == 128), "ring head sizes");
-  static constexpr int RPW = DK / 8, CPL = DV / 32;
-  static constexpr uint32_t STATE = DK * DV * 4;
-  static constexpr uint32_t RK = DK * sizeof(TIn), RV = DV * sizeof(TIn);  // a q / k / g row, a v row
+  static constexpr int DVS = RingSlice<DK, DV>::DVS, NS = RingSlice<DK, DV>::NS;
+  static_assert((DK == 64 || DK == 128 || DK == 256) && (DVS == 64 || DVS == 128) && DK * DVS <= 128 * 128,
+                "ring head sizes");
+  static constexpr int RPW = DK / 8, CPL = DVS / 32;
+  static constexpr uint32_t STATE = DK * DVS * 4;
+  static constexpr uint32_t RK = DK * sizeof(TIn), RV = DVS * sizeof(TIn);  // a q / k / g row, a v slice
   static constexpr uint32_t QO = STATE, KO = QO + RK, GO = KO + RK, VO = GO + RK;
   static constexpr uint32_t RW = RK > RV ? RK : RV;
   static constexpr uint32_t WIN = VO + RV;  // window row m of tensor t at WIN + (3 m + t) RW
-  static constexpr uint32_t STAGE = WIN + (kConv ? 3 * kWinRows * RW : 0);
+  // (128-byte multiple: the tensor-map copy of the next slot's state lands on
+  // a 128-byte boundary)
+  static constexpr uint32_t STAGE = (WIN + (kConv ? 3 * kWinRows * RW : 0) + 127) / 128 * 128;
   // 64 x 64 states (16 KB) run two CTAs per SM: an item's fixed costs (two
   // barriers, the reductions) then overlap with the other CTA's
   static constexpr int CTAS = STATE <= 16384 ? 2 : 1;
@@ -304,11 +322,39 @@ __device__ __forceinline__ bool bar_and(int id, int n, bool v) {
   return r != 0;
 }
 
+// The state of a slice item as a box of the pool viewed as [slots H DK][DV]
+// fp32 rows: DVS columns x DK rows at (column z DVS, row (slot H + h) DK)
+__device__ __forceinline__ void tma_state_load(uint8_t* dst, const CUtensorMap* m, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(tc::smem_u32(dst)),
+      "l"(m), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_state_store(const CUtensorMap* m, int x, int y, const uint8_t* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(m), "r"(x),
+               "r"(y), "r"(tc::smem_u32(src))
+               : "memory");
+}
+
+// An item: (row, head, slice z) with the slices of one head adjacent
+struct RingItem {
+  int row, h, z;
+};
+template <int NS>
+__device__ __forceinline__ RingItem ring_item(int64_t item, int H) {
+  const int64_t rh = item / NS;
+  return RingItem{(int)(rh / H), (int)(rh % H), (int)(item % NS)};
+}
+
 template <typename TIn, bool kConv, int DK, int DV>
 __device__ __forceinline__ void ring_issue(const kda_decode_args& a, const kda_layer_args& l, uint8_t* stage,
-                                           uint64_t* bar, int32_t* valid_flag, int64_t item) {
+                                           uint64_t* bar, int32_t* valid_flag, int64_t item,
+                                           const CUtensorMap* smap) {
+  using R = Ring<TIn, kConv, DK, DV>;
   const int H = a.num_heads;
-  const int row = (int)(item / H), h = (int)(item % H);
+  const RingItem it = ring_item<R::NS>(item, H);
+  const int row = it.row, h = it.h;
   const int slot = a.state_slots ? a.state_slots[row] : row;
   const bool valid = slot >= 0 && slot < a.num_slots;
   *valid_flag = valid ? 1 : 0;
@@ -316,7 +362,6 @@ __device__ __forceinline__ void ring_issue(const kda_decode_args& a, const kda_l
     mbar_arrive(bar);
     return;
   }
-  using R = Ring<TIn, kConv, DK, DV>;
   // (with a gate per head there is no g row: the compute warps read its one value)
   uint32_t bytes = R::STATE + (a.gate_per_head ? 2 : 3) * R::RK + R::RV;
   const int nw = kConv ? l.conv_width - 1 : 0;  // window rows per tensor
@@ -324,8 +369,11 @@ __device__ __forceinline__ void ring_issue(const kda_decode_args& a, const kda_l
     for (int t = 0; t < 3; ++t)
       if (l.conv_in[t]) bytes += nw * (t == 2 ? R::RV : R::RK);
   tc::mbar_arrive_expect_tx(bar, bytes);
-  const int64_t ek = ((int64_t)row * H + h) * DK, ev = ((int64_t)row * H + h) * DV;
-  tc::bulk_g2s(stage, a.state + ((size_t)slot * H + h) * DK * DV, R::STATE, bar);
+  const int64_t ek = ((int64_t)row * H + h) * DK, ev = ((int64_t)row * H + h) * DV + it.z * R::DVS;
+  if (R::NS > 1)
+    tma_state_load(stage, smap, it.z * R::DVS, (slot * H + h) * DK, bar);
+  else
+    tc::bulk_g2s(stage, a.state + ((size_t)slot * H + h) * DK * DV, R::STATE, bar);
   tc::bulk_g2s(stage + R::QO, static_cast<const TIn*>(a.q) + ek, R::RK, bar);
   tc::bulk_g2s(stage + R::KO, static_cast<const TIn*>(a.k) + ek, R::RK, bar);
   if (!a.gate_per_head) tc::bulk_g2s(stage + R::GO, static_cast<const TIn*>(a.g) + ek, R::RK, bar);
@@ -343,17 +391,19 @@ __device__ __forceinline__ void ring_issue(const kda_decode_args& a, const kda_l
 
 // kPoll: the instantiation for wait limits under kPollLimitNs (the give-up
 // test).  kConv: the short convolution (window rows in the slot).
+// smap: the pool as [slots H DK][DV] fp32 rows with a box of DVS columns x
+// DK rows (used when a head is cut into slices)
 template <typename TIn, bool kPoll, bool kConv, int DK, int DV>
 __global__ void __launch_bounds__(kRingAllThreads, (DK * DV <= 64 * 64) ? 2 : 1)
-decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
+decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l, const __grid_constant__ CUtensorMap smap) {
   using R = Ring<TIn, kConv, DK, DV>;
-  constexpr int kStages = R::STAGES, RPW = R::RPW, CPL = R::CPL;
+  constexpr int kStages = R::STAGES, RPW = R::RPW, CPL = R::CPL, DVS = R::DVS, NS = R::NS;
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ __align__(8) uint64_t full[kStages];  // slot loaded
   __shared__ __align__(8) uint64_t done[kStages];  // slot's state updated by warps 0-7
   __shared__ int32_t valid_flag[kStages];
-  __shared__ __align__(16) float red_p[2][8][DV];
-  __shared__ __align__(16) float red_o[2][8][DV];
+  __shared__ __align__(16) float red_p[2][8][DVS];
+  __shared__ __align__(16) float red_o[2][8][DVS];
   __shared__ __align__(16) float part[2][8][4];    // per warp: sum q^2, sum k^2, sum q k
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.num_heads;
@@ -376,7 +426,7 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
       int64_t issued = 0;  // items whose slot copies were issued
       for (; issued < kStages && issued < n_local; ++issued)
         ring_issue<TIn, kConv, DK, DV>(a, l, sm + issued * R::STAGE, &full[issued], &valid_flag[issued],
-                                       first + issued * stride);
+                                       first + issued * stride, &smap);
       for (int64_t k = 0; k < n_local; ++k) {
         const int st = (int)(k % kStages);
         uint8_t* stage = sm + st * R::STAGE;
@@ -390,14 +440,17 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
         }
         const int64_t item = first + k * stride;
         if (valid_flag[st]) {
-          const int row = (int)(item / H), h = (int)(item % H);
-          const int slot = a.state_slots ? a.state_slots[row] : row;
-          tc::bulk_s2g(a.state + ((size_t)slot * H + h) * DK * DV, stage, R::STATE);
+          const RingItem it = ring_item<NS>(item, H);
+          const int slot = a.state_slots ? a.state_slots[it.row] : it.row;
+          if (NS > 1)
+            tma_state_store(&smap, it.z * DVS, (slot * H + it.h) * DK, stage);
+          else
+            tc::bulk_s2g(a.state + ((size_t)slot * H + it.h) * DK * DV, stage, R::STATE);
           tc::bulk_commit();
           tc::bulk_wait_read_all();
         }
         if (k + kStages < n_local) {
-          ring_issue<TIn, kConv, DK, DV>(a, l, stage, &full[st], &valid_flag[st], item + kStages * stride);
+          ring_issue<TIn, kConv, DK, DV>(a, l, stage, &full[st], &valid_flag[st], item + kStages * stride, &smap);
           issued = k + kStages + 1;
         }
       }
@@ -408,7 +461,7 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
 
   // ---- compute warps 0-7; warp w owns key channels (rows) w + 8 i, i < RPW
   const TIn* gb = static_cast<const TIn*>(a.b);
-  float b_next = n_local > 0 ? ld_in(gb, first) : 0.f;
+  float b_next = n_local > 0 ? ld_in(gb, first / NS) : 0.f;  // b [B, H]: one per (row, head)
   for (int64_t k = 0; k < n_local; ++k) {
     const int st = (int)(k % kStages);
     uint8_t* stage = sm + st * R::STAGE;
@@ -417,7 +470,7 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
     bool ok = tc::mbar_wait_t<kPoll>(&full[st], (uint32_t)((k / kStages) & 1), lim);
     const bool valid = valid_flag[st] != 0;
     const float b_cur = b_next;
-    if (k + 1 < n_local) b_next = ld_in(gb, item + stride);
+    if (k + 1 < n_local) b_next = ld_in(gb, (item + stride) / NS);
     if (!valid) {  // uniform: nothing to compute, the slot is handed back
       mbar_arrive(&done[st]);
       if (!bar_and(kComputeBarrier, kRingThreads, ok)) {
@@ -436,17 +489,15 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
     auto wrow = [&](int t, int m, int c) {
       return l.conv_in[t] ? ld_in(reinterpret_cast<const TIn*>(stage + R::WIN + (3 * m + t) * R::RW), c) : 0.f;
     };
+    const RingItem it = ring_item<NS>(item, H);
     int slot = 0;
-    if (kConv) {
-      const int row = (int)(item / H);
-      slot = a.state_slots ? a.state_slots[row] : row;
-    }
-    const int hh = (int)(item % H);
+    if (kConv) slot = a.state_slots ? a.state_slots[it.row] : it.row;
+    const int hh = it.h;
     if (lane < RPW) {
       const int r = warp + 8 * lane;
       xq = ld_in(rq, r);
       xk = ld_in(rk, r);
-      xa = expf(log_alpha_of(a.gate_per_head ? ld_in(static_cast<const TIn*>(a.g), item) : ld_in(rg, r)));
+      xa = expf(log_alpha_of(a.gate_per_head ? ld_in(static_cast<const TIn*>(a.g), item / NS) : ld_in(rg, r)));
       if (kConv) {
         auto pq = [&](int m) { return wrow(0, m, r); };
         auto pk = [&](int m) { return wrow(1, m, r); };
@@ -468,7 +519,7 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
 #pragma unroll
     for (int i = 0; i < RPW; ++i) {
       const int r = warp + 8 * i;
-      ld_cols<CPL>(S + r * DV + CPL * lane, s[i]);
+      ld_cols<CPL>(S + r * DVS + CPL * lane, s[i]);
       const float a_r = __shfl_sync(0xffffffffu, xa, i), k_r = __shfl_sync(0xffffffffu, xk, i),
                   q_r = __shfl_sync(0xffffffffu, xq, i);
 #pragma unroll
@@ -527,20 +578,35 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l) {
       const float k_r = ik * __shfl_sync(0xffffffffu, xk, i);
 #pragma unroll
       for (int j = 0; j < CPL; ++j) s[i][j] += k_r * u[j];
-      st_cols<CPL>(Ss + r * DV + CPL * lane, s[i]);
+      st_cols<CPL>(Ss + r * DVS + CPL * lane, s[i]);
     }
     tc::fence_async_smem();
     mbar_arrive(&done[st]);
     if (warp == 0) {
       const float scl = a.scale;
-      const int row = (int)(item / H), h = (int)(item % H);
+      const int row = it.row, h = it.h;
       TIn* o = static_cast<TIn*>(a.o);
-      const int64_t ob = ((int64_t)row * H + h) * DV + CPL * lane;
+      const int64_t ob = ((int64_t)row * H + h) * DV + it.z * DVS + CPL * lane;
 #pragma unroll
       for (int t = 0; t < CPL; ++t)
         st_out(o, ob + t, scl * (iq * oq[t] + qk * u[t]) * gate_at<TIn>(l, row, H, h, ob + t));
     }
   }
+}
+
+// The state pool [slots, H, DK, DV] fp32 as rows of DV columns, box DVS x DK
+// (a slice of one head), for the ring's slice copies
+template <int DK, int DV>
+bool encode_state_map(CUtensorMap* m, const kda_decode_args& a) {
+  const EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)DV, (cuuint64_t)a.num_slots * a.num_heads * DK};
+  const cuuint64_t strides[1] = {(cuuint64_t)DV * 4};
+  const cuuint32_t box[2] = {(cuuint32_t)RingSlice<DK, DV>::DVS, (cuuint32_t)DK};
+  const cuuint32_t elem[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.state, dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <typename TIn, bool kConv, int DK, int DV>
@@ -554,9 +620,11 @@ cudaError_t launch_ring(const kda_decode_args& a, const kda_layer_args& l, cudaS
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)R::BYTES);
   if (e != cudaSuccess) return e;
-  const int64_t n_items = (int64_t)a.batch * a.num_heads, slots = (int64_t)sms * R::CTAS;
+  CUtensorMap smap{};
+  if (R::NS > 1 && !encode_state_map<DK, DV>(&smap, a)) return cudaErrorInvalidValue;
+  const int64_t n_items = (int64_t)a.batch * a.num_heads * R::NS, slots = (int64_t)sms * R::CTAS;
   const int64_t grid = n_items < slots ? n_items : slots;
-  kernel<<<(unsigned)grid, kRingAllThreads, R::BYTES, stream>>>(a, n_items, l);
+  kernel<<<(unsigned)grid, kRingAllThreads, R::BYTES, stream>>>(a, n_items, l, smap);
   return cudaGetLastError();
 }
 
@@ -567,11 +635,17 @@ cudaError_t launch_t(const kda_decode_args& a, const kda_layer_args& l, cudaStre
   // convolution the ring takes bf16 only (fp32 window rows overflow its
   // shared memory)
   const bool conv = l.conv_width > 0;
-  constexpr bool kRingShape = (DK == 64 || DK == 128) && (DV == 64 || DV == 128);
+  constexpr bool kRingShape = (DK == 64 || DK == 128 || DK == 256) && (DV == 64 || DV == 128 || DV == 256);
   if constexpr (kRingShape) {
-    if (al16(a.q) && al16(a.k) && (a.gate_per_head || al16(a.g)) && al16(a.v) && al16(a.state) &&
-        (!conv || (sizeof(TIn) == 2 && al16(l.conv_in[0]) && al16(l.conv_in[1]) && al16(l.conv_in[2])))) {
-      if constexpr (sizeof(TIn) == 2)
+    // heads cut into slices: the tensor-map rows (slot H + h) DK must fit its
+    // int32 coordinates, and the slices would share a q/k window (the
+    // convolution is refused for these heads anyway)
+    constexpr int NS = RingSlice<DK, DV>::NS;
+    const bool rows_fit = NS == 1 || (int64_t)a.num_slots * a.num_heads * DK < ((int64_t)1 << 31);
+    if (rows_fit && al16(a.q) && al16(a.k) && (a.gate_per_head || al16(a.g)) && al16(a.v) && al16(a.state) &&
+        (!conv || (NS == 1 && DK <= 128 && sizeof(TIn) == 2 && al16(l.conv_in[0]) && al16(l.conv_in[1]) &&
+                   al16(l.conv_in[2])))) {
+      if constexpr (sizeof(TIn) == 2 && NS == 1 && DK <= 128)
         if (conv) return launch_ring<TIn, true, DK, DV>(a, l, stream);
       return launch_ring<TIn, false, DK, DV>(a, l, stream);
     }

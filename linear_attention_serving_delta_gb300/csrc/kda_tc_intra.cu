@@ -65,6 +65,7 @@ static_assert(Smem::B1 % 16 == 0 && Smem::B2 % 16 == 0 && Smem::A2 % 16 == 0 && 
               "operand tiles and float4 arrays are 16-byte aligned");
 static_assert(8 * kA2Lbo >= 64 * 64 * 2, "A2 holds the unpadded A_qk staging too");
 static_assert(16 * kB1Lbo >= 64 * kTs * 4, "T fits in the Kn tile");
+static_assert(32 * 40 * 4 <= 8 * kA2Lbo, "the inverse's product scratch fits in A2");
 static_assert(16 * kAkStage <= 64 * kAs * 4, "the Kr^T staging fits in the A_kk tile");
 static_assert(32 * kB2Sbo >= 64 * 128 * 4, "the U~ staging fits in the B2 tile");
 
@@ -88,15 +89,59 @@ __device__ __forceinline__ uint32_t kmaj(uint32_t r, uint32_t k, uint32_t lbo) {
   return (k >> 3) * lbo + (r >> 3) * 128u + (r & 7u) * 16u + (k & 7u) * 2u;
 }
 
+// T (64 x 64 fp32, row stride kTs) keeps its columns XOR-swizzled by row:
+// element (r, c) at r kTs + (c ^ 8 (r % 4)).  Aligned groups of 8 columns
+// stay contiguous (16-byte row reads are unchanged), and the 4 rows x 8
+// columns that a warp-level MMA operand fragment reads fall in 32 distinct
+// banks.
+__device__ __forceinline__ int tsw(int r, int c) { return r * kTs + (c ^ ((r & 3) << 3)); }
+
+// Warp-level tensor-core MMA, m16n8k8, tf32 operands, fp32 accumulator
+// (d += a b): a = rows g, g+8 x columns t, t+4 of a 16 x 8 tile, b = rows t,
+// t+4 x column g of an 8 x 8 tile, d = rows g, g+8 x columns 2t, 2t+1, with
+// g = lane / 4 and t = lane % 4.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+constexpr int kXs = 40;  // row stride (floats) of the product scratch: 8 mod 32 banks
+
+// One 16 x 8 tile of P = L R (K = 8 ks_n steps), L and R given as element
+// readers: L(row, k) over rows m0 .. m0+15, R(k, col) over columns n0 .. n0+7.
+template <int KS, typename LF, typename RF>
+__device__ __forceinline__ void tile_product(float* d, int m0, int n0, int k0, LF L, RF R) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  d[0] = d[1] = d[2] = d[3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    const int k = k0 + 8 * ks + t;
+    const uint32_t a[4] = {to_tf32(L(m0 + g, k)), to_tf32(L(m0 + g + 8, k)), to_tf32(L(m0 + g, k + 4)),
+                           to_tf32(L(m0 + g + 8, k + 4))};
+    const uint32_t b[2] = {to_tf32(R(k, n0 + g)), to_tf32(R(k + 4, n0 + g))};
+    mma_tf32(d, a, b);
+  }
+}
+
 // T = (I + A)^{-1} for strictly lower-triangular A (64x64, stride kAs).
 // Level 0: the four 16x16 diagonal tiles by forward substitution (a thread
-// per column).  Level 1: the two 16x16 tiles below them inside each 32x32
-// half, T10 = -T11 A10 T00.  Level 2: the lower-left 32x32 tile,
-// T = -T_hi A T_lo.  X: scratch of 32x32 floats.  256 threads; the thread
-// given x_busy first waits until its bulk copy out of X has read it.
+// per column, CUDA cores).  Level 1: the two 16x16 tiles below them inside
+// each 32x32 half, T10 = -T11 A10 T00.  Level 2: the lower-left 32x32 tile,
+// T = -T_hi A T_lo.  The products of levels 1 and 2 run on the warp-level
+// tensor cores in tf32 with fp32 accumulation (T is rounded to bf16 once
+// scaled by beta, far coarser than tf32).  X: scratch of 32 x kXs floats.
+// 256 threads; the thread given x_busy first waits until its bulk copy out
+// of X has read it.
 __device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ T,
                                float* __restrict__ X, bool x_busy) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   if (tid < 64) {
     const int d = tid >> 4, jj = tid & 15, j = 16 * d + jj;
     float col[16];
@@ -117,88 +162,62 @@ __device__ void tri_inverse_64(const float* __restrict__ A, float* __restrict__ 
       col[ii] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     }
 #pragma unroll
-    for (int ii = 0; ii < 16; ++ii) T[(16 * d + ii) * kTs + j] = col[ii];
+    for (int ii = 0; ii < 16; ++ii) T[tsw(16 * d + ii, j)] = col[ii];
   } else {
     // tiles strictly above the diagonal are zero
     for (int idx = tid - 64; idx < 6 * 256; idx += kThreads - 64) {
-      const int t = idx >> 8, e = idx & 255;
-      const int bi = t < 3 ? 0 : (t < 5 ? 1 : 2);
-      const int bj = t < 3 ? t + 1 : (t < 5 ? t - 1 : 3);
-      T[(16 * bi + (e >> 4)) * kTs + 16 * bj + (e & 15)] = 0.f;
+      const int tt = idx >> 8, e = idx & 255;
+      const int bi = tt < 3 ? 0 : (tt < 5 ? 1 : 2);
+      const int bj = tt < 3 ? tt + 1 : (tt < 5 ? tt - 1 : 3);
+      T[tsw(16 * bi + (e >> 4), 16 * bj + (e & 15))] = 0.f;
     }
   }
   if (x_busy) bulk_wait_read_all();
   __syncthreads();
-  // level 1: P = 0, 1 -> tile rows 32P+16.., cols 32P..
-  // (X held the staged A_qk of the record: its copy has read it)
-  {
-    const int P = tid >> 7, rr = (tid >> 3) & 15, cc = (tid & 7) * 2;
-    const int r0 = 32 * P + 16, c0 = 32 * P;
-    float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-    for (int m4 = 0; m4 < 16; m4 += 4) {  // four entries of the A row per 16-byte load
-      const float4 a = *reinterpret_cast<const float4*>(A + (r0 + rr) * kAs + c0 + m4);
-      const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float2 t = *reinterpret_cast<const float2*>(T + (c0 + m4 + u) * kTs + c0 + cc);
-        x0 += av[u] * t.x;
-        x1 += av[u] * t.y;
-      }
-    }
-    X[P * 256 + rr * 16 + cc] = x0;
-    X[P * 256 + rr * 16 + cc + 1] = x1;
-    __syncthreads();
-    float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-    for (int m4 = 0; m4 < 16; m4 += 4) {
-      const float4 t = *reinterpret_cast<const float4*>(T + (r0 + rr) * kTs + r0 + m4);
-      const float tv[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float2 x = *reinterpret_cast<const float2*>(X + P * 256 + (m4 + u) * 16 + cc);
-        y0 += tv[u] * x.x;
-        y1 += tv[u] * x.y;
-      }
-    }
-    T[(r0 + rr) * kTs + c0 + cc] = -y0;
-    T[(r0 + rr) * kTs + c0 + cc + 1] = -y1;
+  // level 1, warps 0-3: P = warp / 2 -> tile rows r0 = 32P+16.., cols c0 = 32P..,
+  // 8-column half warp % 2.  (X held the staged A_qk of the record: its copy
+  // has read it.)
+  auto Ael = [&](int r, int c) { return A[r * kAs + c]; };
+  auto Tel = [&](int r, int c) { return T[tsw(r, c)]; };
+  const int P = warp >> 1, nh = warp & 1, r0 = 32 * P + 16, c0 = 32 * P;
+  float* X1 = X + P * 16 * kXs;
+  float d[4];
+  if (warp < 4) {
+    tile_product<2>(d, r0, c0 + 8 * nh, c0, Ael, Tel);  // A10 T00
+    const int c = 8 * nh + 2 * t;
+    X1[g * kXs + c] = d[0];
+    X1[g * kXs + c + 1] = d[1];
+    X1[(g + 8) * kXs + c] = d[2];
+    X1[(g + 8) * kXs + c + 1] = d[3];
   }
   __syncthreads();
-  // level 2: rows 32..63, cols 0..31, 2x2 outputs per thread
+  if (warp < 4) {
+    auto Xel = [&](int r, int c) { return X1[(r - r0) * kXs + c - c0]; };
+    tile_product<2>(d, r0, c0 + 8 * nh, r0, Tel, Xel);  // T11 (A10 T00)
+    const int c = c0 + 8 * nh + 2 * t;
+    T[tsw(r0 + g, c)] = -d[0];
+    T[tsw(r0 + g, c + 1)] = -d[1];
+    T[tsw(r0 + g + 8, c)] = -d[2];
+    T[tsw(r0 + g + 8, c + 1)] = -d[3];
+  }
+  __syncthreads();
+  // level 2, all warps: rows 32..63, cols 0..31; warp w takes rows 32 + 16 (w / 4)..,
+  // columns 8 (w % 4)..
   {
-    const int rr = (tid >> 4) * 2, cc = (tid & 15) * 2;
-    float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
-#pragma unroll 2
-    for (int m4 = 0; m4 < 32; m4 += 4) {  // four entries of each A row per 16-byte load
-      const float4 a0 = *reinterpret_cast<const float4*>(A + (32 + rr) * kAs + m4);
-      const float4 a1 = *reinterpret_cast<const float4*>(A + (33 + rr) * kAs + m4);
-      const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float2 t = *reinterpret_cast<const float2*>(T + (m4 + u) * kTs + cc);
-        x00 += av0[u] * t.x; x01 += av0[u] * t.y;
-        x10 += av1[u] * t.x; x11 += av1[u] * t.y;
-      }
-    }
-    X[rr * 32 + cc] = x00; X[rr * 32 + cc + 1] = x01;
-    X[(rr + 1) * 32 + cc] = x10; X[(rr + 1) * 32 + cc + 1] = x11;
+    const int m0 = 32 + 16 * (warp >> 2), n0 = 8 * (warp & 3);
+    tile_product<4>(d, m0, n0, 0, Ael, Tel);  // A[32:64, 0:32] T[0:32, 0:32]
+    const int r = m0 - 32 + g, c = n0 + 2 * t;
+    X[r * kXs + c] = d[0];
+    X[r * kXs + c + 1] = d[1];
+    X[(r + 8) * kXs + c] = d[2];
+    X[(r + 8) * kXs + c + 1] = d[3];
     __syncthreads();
-    float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
-#pragma unroll 2
-    for (int m4 = 0; m4 < 32; m4 += 4) {
-      const float4 t0 = *reinterpret_cast<const float4*>(T + (32 + rr) * kTs + 32 + m4);
-      const float4 t1 = *reinterpret_cast<const float4*>(T + (33 + rr) * kTs + 32 + m4);
-      const float tv0[4] = {t0.x, t0.y, t0.z, t0.w}, tv1[4] = {t1.x, t1.y, t1.z, t1.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float2 x = *reinterpret_cast<const float2*>(X + (m4 + u) * 32 + cc);
-        y00 += tv0[u] * x.x; y01 += tv0[u] * x.y;
-        y10 += tv1[u] * x.x; y11 += tv1[u] * x.y;
-      }
-    }
-    T[(32 + rr) * kTs + cc] = -y00; T[(32 + rr) * kTs + cc + 1] = -y01;
-    T[(33 + rr) * kTs + cc] = -y10; T[(33 + rr) * kTs + cc + 1] = -y11;
+    auto Xel = [&](int rr, int cc) { return X[(rr - 32) * kXs + cc]; };
+    tile_product<4>(d, m0, n0, 32, Tel, Xel);  // T[32:64, 32:64] X
+    T[tsw(m0 + g, c)] = -d[0];
+    T[tsw(m0 + g, c + 1)] = -d[1];
+    T[tsw(m0 + g + 8, c)] = -d[2];
+    T[tsw(m0 + g + 8, c + 1)] = -d[3];
   }
   __syncthreads();
 }
@@ -819,8 +838,8 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
     for (int t = 0; t < 2; ++t) {
       const int idx = tid + kThreads * t;
       const int i = idx >> 3, jb = idx & 7;  // lanes along a row of T: few bank conflicts
-      const float4 t0 = *reinterpret_cast<const float4*>(TT + i * kTs + 8 * jb);
-      const float4 t1 = *reinterpret_cast<const float4*>(TT + i * kTs + 8 * jb + 4);
+      const float4 t0 = *reinterpret_cast<const float4*>(TT + tsw(i, 8 * jb));
+      const float4 t1 = *reinterpret_cast<const float4*>(TT + tsw(i, 8 * jb) + 4);
       const float4 b0 = *reinterpret_cast<const float4*>(beta + 8 * jb);
       const float4 b1 = *reinterpret_cast<const float4*>(beta + 8 * jb + 4);
       st_s16(A2, kmaj(i, 8 * jb, kA2Lbo),

@@ -59,6 +59,7 @@ KERNEL_SOURCES = {
                  "kda_common.cuh"],
     "decode_ring": ["kda_decode.cu", "kda_tc.cuh", "kda_internal.cuh", "kda_common.cuh"],
     "prep_vec": ["kda_prep.cu", "kda_internal.cuh", "kda_common.cuh"],
+    "plan_kernel": ["kda_plan.cu", "kda_internal.cuh", "kda_common.cuh"],
 }
 
 
@@ -573,6 +574,14 @@ def gpu_arm(a):
     if a.wide_only:
         print(json.dumps(bench_wide_heads(torch, kda, W, dev, steps=a.steps)))
         return
+    if a.decode_only:
+        dec = bench_decode(torch, kda, W, a.decode_steps, a.warmup, dev)
+        gbs = DECODE_STATE_BYTES_PER_HEAD * dec["heads"] / (dec["ms_per_step"] * 1e-3) / 1e9
+        print(json.dumps({"decode_us_per_step": dec["ms_per_step"] * 1e3, "state_gbs": gbs}))
+        return
+    if a.prep_only:
+        print(json.dumps(bench_prep(torch, kda, W, dev, reps=a.steps)))
+        return
     with ClockSampler(local) as clk:
         pre = bench_prefill(torch, kda, W, a.steps, a.warmup, dev)
         barrier()
@@ -750,6 +759,10 @@ def main():
                     help="time the prefill with the layer steps alone (for profiler captures)")
     ap.add_argument("--wide-only", action="store_true",
                     help="time the 256-channel heads alone")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time the decode workload alone (for profiler captures)")
+    ap.add_argument("--prep-only", action="store_true",
+                    help="time the preparation step alone (for profiler captures)")
     a = ap.parse_args()
     if a.warmup < 3:
         a.warmup = 3

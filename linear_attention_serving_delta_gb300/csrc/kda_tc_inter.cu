@@ -35,68 +35,79 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 256;
-constexpr int kNs = 32;                 // state columns per CTA
-constexpr int kNh = kNs / 2;            // columns per thread
-constexpr int kNop = 2 * kNs;           // MMA N: hi and lo halves side by side
+constexpr int kNh = 16;                 // state columns per thread
 constexpr uint32_t kSopSbo = 16 * 128;  // S operand: 16 K-groups (key channels) per MN-group
 constexpr uint32_t kUopSbo = 8 * 128;   // U operand: 8 K-groups (tokens) per MN-group
-constexpr uint32_t kTmemCols = 4 * kNop;
 constexpr int kMmaThread = 0, kOutThread = 64, kLoadThread = 96;
-constexpr int kUBarrier = 1;            // named barrier of the U warps (0, 1, 4, 5)
+constexpr int kUBarrier = 1;            // named barrier of the U warps
+constexpr uint32_t kAqBytes = 64 * 64 * 2;
 
-struct K3Smem {
+// A CTA carries NS = 32 or 64 state columns of one (sequence, head): 8 NS
+// threads, two warps per TMEM lane quarter and column group of 16.  Every
+// MMA runs at N = 2 NS (hi | lo); a tcgen05.mma costs about the same for
+// any N <= 64 and little more at N = 128, so 64 columns per CTA take nearly
+// the time of 32 per chain step on half the SMs.
+template <int NS>
+struct K3Cfg {
+  static constexpr int kNop = 2 * NS;           // MMA N: hi and lo halves side by side
+  static constexpr int kThreads = 8 * NS;       // 256 or 512
+  static constexpr int kSlices = 128 / NS;      // column slices of a 128-column state
+  static constexpr int kUThreads = 4 * NS;      // threads of the U warps (TMEM lanes 0-63)
+  static constexpr uint32_t kTmemCols = 4 * kNop;
   // ring of chain operands: AW (32 KB) | AK (16 KB) | UT slice | GL
   static constexpr uint32_t AW = 0;
   static constexpr uint32_t AK = AW + 128 * 128 * 2;
   static constexpr uint32_t UT = AK + 128 * 64 * 2;
-  static constexpr uint32_t GL = UT + 64 * kNs * 4;
+  static constexpr uint32_t GL = UT + 64 * NS * 4;
   static constexpr uint32_t SLOT = GL + 128 * 4;
-  static constexpr int kSlots = 3;
+  static constexpr int kSlots = NS == 32 ? 3 : 2;
   static constexpr uint32_t SOP = kSlots * SLOT;  // S operand [hi | lo], MN-major (n, c)
   // ring of A_qk tiles; each is read as rows 64-127 of an M=128 tile that
   // starts 1 KB before it, inside the S operand or the tile before
   static constexpr int kAqSlots = 3;
-  static constexpr uint32_t AQ_BYTES = 64 * 64 * 2;
   static constexpr uint32_t AQ0 = SOP + kNop * 128 * 2;
   // two U operands [hi | lo], MN-major (n, i)
   static constexpr uint32_t U_BYTES = kNop * 64 * 2;
-  static constexpr uint32_t U0 = AQ0 + kAqSlots * AQ_BYTES;
+  static constexpr uint32_t U0 = AQ0 + kAqSlots * kAqBytes;
   static constexpr uint32_t BYTES = U0 + 2 * U_BYTES;
   static constexpr uint32_t TILES = UT;  // AW | AK, contiguous in the record too
-  static constexpr uint32_t TX = TILES + 64 * kNs * 4 + 128 * 4;
+  static constexpr uint32_t TX = TILES + 64 * NS * 4 + 128 * 4;
+  static_assert(AK - AW == Rec::AK - Rec::AW, "AW | AK keep the record's layout");
+  static_assert(SLOT % 16 == 0 && AQ0 % 16 == 0 && U0 % 16 == 0,
+                "bulk-copy destinations and operand tiles are 16-byte aligned");
+  static_assert(AQ0 >= 1024, "the A_qk tile descriptor starts 1 KB early inside shared memory");
+  static_assert(BYTES <= 226 * 1024, "fits one CTA per SM");
+  static_assert(kThreads / 32 == 4 * (NS / kNh), "two warps per lane quarter and 16-column group");
 };
-static_assert(K3Smem::AK - K3Smem::AW == Rec::AK - Rec::AW, "AW | AK keep the record's layout");
-static_assert(K3Smem::SLOT % 16 == 0 && K3Smem::AQ0 % 16 == 0 && K3Smem::U0 % 16 == 0,
-              "bulk-copy destinations and operand tiles are 16-byte aligned");
-static_assert(K3Smem::AQ0 >= 1024, "the A_qk tile descriptor starts 1 KB early inside shared memory");
-static_assert(K3Smem::BYTES <= 226 * 1024, "fits one CTA per SM");
 
 // The chain operands of chunk cidx: three bulk copies (AW | AK, this CTA's
 // slice of U~, Gamma_L) on one barrier.
+template <int NS>
 __device__ __forceinline__ void k3_load_chain(const ChunkParams& p, uint8_t* slot, uint64_t* bar,
                                               int64_t cidx, int h, int n0) {
+  using C = K3Cfg<NS>;
   const uint8_t* rec = reinterpret_cast<const uint8_t*>(p.inter) + ((size_t)cidx * p.H + h) * Rec::BYTES;
-  mbar_arrive_expect_tx(bar, K3Smem::TX);
-  bulk_g2s(slot + K3Smem::AW, rec + Rec::AW, K3Smem::TILES, bar);
-  bulk_g2s(slot + K3Smem::UT, rec + Rec::UT + (n0 / 4) * 64 * 16, 64 * kNs * 4, bar);
-  bulk_g2s(slot + K3Smem::GL, rec + Rec::GL, 128 * 4, bar);
+  mbar_arrive_expect_tx(bar, C::TX);
+  bulk_g2s(slot + C::AW, rec + Rec::AW, C::TILES, bar);
+  bulk_g2s(slot + C::UT, rec + Rec::UT + (n0 / 4) * 64 * 16, 64 * NS * 4, bar);
+  bulk_g2s(slot + C::GL, rec + Rec::GL, 128 * 4, bar);
 }
 
 // The A_qk tile of chunk cidx.
 __device__ __forceinline__ void k3_load_aq(const ChunkParams& p, uint8_t* dst, uint64_t* bar,
                                            int64_t cidx, int h) {
   const uint8_t* rec = reinterpret_cast<const uint8_t*>(p.inter) + ((size_t)cidx * p.H + h) * Rec::BYTES;
-  mbar_arrive_expect_tx(bar, K3Smem::AQ_BYTES);
-  bulk_g2s(dst, rec + Rec::AQ, K3Smem::AQ_BYTES, bar);
+  mbar_arrive_expect_tx(bar, kAqBytes);
+  bulk_g2s(dst, rec + Rec::AQ, kAqBytes, bar);
 }
 
 // This thread's 16 columns of a hi | lo accumulator pair, summed: v[n] =
-// column (h16 + n) + column (32 + h16 + n) of one TMEM lane.
+// column (h16 + n) + column (NS + h16 + n) of one TMEM lane.
+template <int NS>
 __device__ __forceinline__ void tmem_ld_sum(uint32_t taddr, int h16, float* v) {
   float b[kNh];
   tmem_ld16(taddr + h16, v);
-  tmem_ld16(taddr + kNs + h16, b);
+  tmem_ld16(taddr + NS + h16, b);
   tmem_ld_wait();
 #pragma unroll
   for (int n = 0; n < kNh; ++n) v[n] += b[n];
@@ -159,10 +170,11 @@ __device__ __forceinline__ GateRow load_gate_row(const ChunkParams& p, const Chu
 // o rows of one chunk from lanes 64-127 of an output accumulator: row i, this
 // thread's 16 columns (none in the first pass of the segment scan), times
 // the output gate's factors gf when there is a gate
+template <int NS>
 __device__ __forceinline__ void store_output(const ChunkParams& p, const Chunk& ch, uint32_t d1,
                                              int h16, int i, int h, int n0, const GateF& gf) {
   float d[kNh];
-  tmem_ld_sum(d1, h16, d);
+  tmem_ld_sum<NS>(d1, h16, d);
   if (i < ch.len && p.k3_mode != kScanPass1) {
     const float scale = p.scale;
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o);
@@ -182,6 +194,7 @@ __device__ __forceinline__ void store_output(const ChunkParams& p, const Chunk& 
 
 // The state write-back of one TMEM lane (key channel c), this thread's 16
 // columns: the bf16 operand [hi | lo] of v, and Sa <- gl v, Sb <- 0.
+template <int NS>
 __device__ __forceinline__ void write_state(uint8_t* sop, uint32_t ds, int c, int h16, const float* v,
                                             float gl) {
 #pragma unroll
@@ -189,7 +202,7 @@ __device__ __forceinline__ void write_state(uint8_t* sop, uint32_t ds, int c, in
     uint4 hi, lo;
     split8(v + 8 * m, hi, lo);
     *reinterpret_cast<uint4*>(sop + mnmajor_off(h16 + 8 * m, c, kSopSbo)) = hi;
-    *reinterpret_cast<uint4*>(sop + mnmajor_off(kNs + h16 + 8 * m, c, kSopSbo)) = lo;
+    *reinterpret_cast<uint4*>(sop + mnmajor_off(NS + h16 + 8 * m, c, kSopSbo)) = lo;
   }
   float s[kNh], z[kNh];
 #pragma unroll
@@ -198,28 +211,31 @@ __device__ __forceinline__ void write_state(uint8_t* sop, uint32_t ds, int c, in
     z[n] = 0.f;
   }
   tmem_st16(ds + h16, s);
-  tmem_st16(ds + kNs + h16, z);
+  tmem_st16(ds + NS + h16, z);
   tmem_st_wait();
 }
 
-// kPoll: the instantiation for wait limits under kPollLimitNs (the give-up test)
-template <bool kPoll>
-__global__ void __launch_bounds__(kThreads, 1)
+// kPoll: the instantiation for wait limits under kPollLimitNs (the give-up
+// test); NS: the state columns of a CTA (K3Cfg)
+template <bool kPoll, int NS>
+__global__ void __launch_bounds__(K3Cfg<NS>::kThreads, 1)
 tc_inter(ChunkParams p) {
+  using C = K3Cfg<NS>;
+  constexpr int kNs = NS, kNop = C::kNop;
   extern __shared__ __align__(1024) uint8_t sm[];
-  __shared__ __align__(8) uint64_t bar_full[K3Smem::kSlots];
-  __shared__ __align__(8) uint64_t bar_aq[K3Smem::kAqSlots];
+  __shared__ __align__(8) uint64_t bar_full[C::kSlots];
+  __shared__ __align__(8) uint64_t bar_aq[C::kAqSlots];
   __shared__ __align__(8) uint64_t bar_mma1;     // MMA 1
   __shared__ __align__(8) uint64_t bar_mma2;     // MMA 2 (state chain)
   __shared__ __align__(8) uint64_t bar_mma3[2];  // MMA 3 of even / odd chunks (output path)
   __shared__ __align__(8) uint64_t bar_drain;    // every MMA, on the error path
   __shared__ uint32_t tmem_base;
 
-  const int s = blockIdx.x, h = blockIdx.y, n0 = (blockIdx.z & 3) * kNs;
-  // first pass of the segment scan: CTAs z >= 4 carry the transition map
-  // (identity state, U~ = 0), the others the state offset (zero state)
+  const int s = blockIdx.x, h = blockIdx.y, n0 = (int)(blockIdx.z % C::kSlices) * kNs;
+  // first pass of the segment scan: CTAs z >= kSlices carry the transition
+  // map (identity state, U~ = 0), the others the state offset (zero state)
   const bool pass1 = p.k3_mode == kScanPass1;
-  const bool trans = pass1 && blockIdx.z >= 4;
+  const bool trans = pass1 && blockIdx.z >= C::kSlices;
   const int H = p.H, tid = threadIdx.x, warp = tid >> 5;
   const int64_t c_begin = p.seq_chunk_begin[s], c_end = p.seq_chunk_begin[s + 1];
   if (c_end > c_begin && p.meta->total_chunks == 0) return;  // chunk table overflowed
@@ -230,12 +246,12 @@ tc_inter(ChunkParams p) {
   const int h16 = (warp >> 2) * kNh;
   const int c = tid & 127;
   const bool u_warp = quarter < 2;  // warps 0, 1, 4, 5: lanes 0-63 (W rows, U)
-  uint8_t* SOP = sm + K3Smem::SOP;
+  uint8_t* SOP = sm + C::SOP;
 
-  if (warp == 0) tmem_alloc(&tmem_base, kTmemCols);
+  if (warp == 0) tmem_alloc(&tmem_base, C::kTmemCols);
   if (tid == 0) {
-    for (int i = 0; i < K3Smem::kSlots; ++i) mbar_init(&bar_full[i], 1);
-    for (int i = 0; i < K3Smem::kAqSlots; ++i) mbar_init(&bar_aq[i], 1);
+    for (int i = 0; i < C::kSlots; ++i) mbar_init(&bar_full[i], 1);
+    for (int i = 0; i < C::kAqSlots; ++i) mbar_init(&bar_aq[i], 1);
     mbar_init(&bar_mma1, 1);
     mbar_init(&bar_mma2, 1);
     mbar_init(&bar_mma3[0], 1);
@@ -253,15 +269,15 @@ tc_inter(ChunkParams p) {
   // output accumulator of chunk j (this warp's lanes): [W;Qp] S_j, then
   // + A_qk U in lanes 64-127
   auto d1_of = [&](int64_t j) { return tmem + (uint32_t)(j % 3) * kNop; };
-  auto slot_of = [&](int64_t j) { return sm + (uint32_t)(j % K3Smem::kSlots) * K3Smem::SLOT; };
+  auto slot_of = [&](int64_t j) { return sm + (uint32_t)(j % C::kSlots) * C::SLOT; };
   auto aq_of = [&](int64_t j) {
-    return sm + K3Smem::AQ0 + (uint32_t)(j % K3Smem::kAqSlots) * K3Smem::AQ_BYTES;
+    return sm + C::AQ0 + (uint32_t)(j % C::kAqSlots) * kAqBytes;
   };
-  auto u_of = [&](int64_t j) { return sm + K3Smem::U0 + (uint32_t)(j & 1) * K3Smem::U_BYTES; };
+  auto u_of = [&](int64_t j) { return sm + C::U0 + (uint32_t)(j & 1) * C::U_BYTES; };
   // (the drain of the error path waits with the long limit)
   auto wait_chain = [&](int64_t j, bool drain) {
-    uint64_t* bar = &bar_full[j % K3Smem::kSlots];
-    const uint32_t par = (uint32_t)((j / K3Smem::kSlots) & 1);
+    uint64_t* bar = &bar_full[j % C::kSlots];
+    const uint32_t par = (uint32_t)((j / C::kSlots) & 1);
     return drain ? mbar_wait(bar, par, kWaitLimitNs) : mbar_wait_t<kPoll>(bar, par, p.wait_ns);
   };
 
@@ -270,10 +286,10 @@ tc_inter(ChunkParams p) {
   // can let copies in flight land.
   int64_t chain_issued = 0, chain_waited = 0, aq_issued = 0, aq_waited = 0;
   if (tid == kLoadThread)
-    for (; chain_issued < K3Smem::kSlots && chain_issued < nchunks; ++chain_issued)
-      k3_load_chain(p, slot_of(chain_issued), &bar_full[chain_issued], c_begin + chain_issued, h, n0);
+    for (; chain_issued < C::kSlots && chain_issued < nchunks; ++chain_issued)
+      k3_load_chain<NS>(p, slot_of(chain_issued), &bar_full[chain_issued], c_begin + chain_issued, h, n0);
   if (tid == kOutThread)
-    for (; aq_issued < K3Smem::kAqSlots && aq_issued < nchunks; ++aq_issued)
+    for (; aq_issued < C::kAqSlots && aq_issued < nchunks; ++aq_issued)
       k3_load_aq(p, aq_of(aq_issued), &bar_aq[aq_issued], c_begin + aq_issued, h);
 
   bool ok = true;
@@ -301,9 +317,9 @@ tc_inter(ChunkParams p) {
     if (nchunks > 0) {
       okl = wait_chain(0, false);
       if (okl) chain_waited = 1;  // a copy still in flight is left to the drain
-      gl = reinterpret_cast<const float*>(slot_of(0) + K3Smem::GL)[c];
+      gl = reinterpret_cast<const float*>(slot_of(0) + C::GL)[c];
     }
-    write_state(SOP, DS, c, h16, v, gl);
+    write_state<NS>(SOP, DS, c, h16, v, gl);
   }
 
   const uint32_t id = idesc_bf16(128, kNop, 0, 1);     // B operands MN-major
@@ -311,7 +327,7 @@ tc_inter(ChunkParams p) {
   // MMA 3 of chunk j, thread 64: wait for its A_qk tile, then
   // D1[j % 3] += A_qk [U_hi | U_lo].  False if the tile never came.
   auto mma3 = [&](int64_t j) -> bool {
-    if (!mbar_wait_t<kPoll>(&bar_aq[j % K3Smem::kAqSlots], (uint32_t)((j / K3Smem::kAqSlots) & 1), p.wait_ns))
+    if (!mbar_wait_t<kPoll>(&bar_aq[j % C::kAqSlots], (uint32_t)((j / C::kAqSlots) & 1), p.wait_ns))
       return false;
     aq_waited = j + 1;
     const uint32_t a = smem_u32(aq_of(j)) - 1024, ub = smem_u32(u_of(j));
@@ -348,7 +364,7 @@ tc_inter(ChunkParams p) {
     if (tid == kMmaThread) {
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        mma_bf16(d1_of(it), sdesc(smem_u32(slot + K3Smem::AW) + k * 2 * 128 * 16, 128 * 16, 128),
+        mma_bf16(d1_of(it), sdesc(smem_u32(slot + C::AW) + k * 2 * 128 * 16, 128 * 16, 128),
                  sdesc(smem_u32(SOP) + k * 256, 128, kSopSbo), id, k > 0);
       mma_commit(&bar_mma1);
     }
@@ -357,16 +373,17 @@ tc_inter(ChunkParams p) {
       if (it >= 2) {
         okl = okl && wait_mma3(it - 2);
         fence_after_sync();
-        if (okl) store_output(p, prev2, d1_of(it - 2) + lane_off, h16, c - 64, h, n0, gfac);
+        if (okl) store_output<NS>(p, prev2, d1_of(it - 2) + lane_off, h16, c - 64, h, n0, gfac);
         // ... its A_qk tile takes chunk it+1 ...
         if (tid == kOutThread && okl && it + 1 < nchunks && aq_issued == it + 1) {
-          k3_load_aq(p, aq_of(it + 1), &bar_aq[(it + 1) % K3Smem::kAqSlots], c_begin + it + 1, h);
+          k3_load_aq(p, aq_of(it + 1), &bar_aq[(it + 1) % C::kAqSlots], c_begin + it + 1, h);
           aq_issued = it + 2;
         }
       }
-      // ... the slot of chunk it-1 (MMA 2 done) takes chunk it+2 ...
-      if (tid == kLoadThread && okl && it >= 1 && it + 2 < nchunks) {
-        k3_load_chain(p, slot_of(it + 2), &bar_full[(it + 2) % K3Smem::kSlots], c_begin + it + 2, h, n0);
+      // ... with a 3-slot ring the slot of chunk it-1 (MMA 2 done) takes
+      // chunk it+2 here, off the chain ...
+      if (C::kSlots == 3 && tid == kLoadThread && okl && it >= 1 && it + 2 < nchunks) {
+        k3_load_chain<NS>(p, slot_of(it + 2), &bar_full[(it + 2) % C::kSlots], c_begin + it + 2, h, n0);
         chain_issued = it + 3;
       }
       // ... and the output product of chunk it-1 runs once MMA 1 is done; the
@@ -388,8 +405,8 @@ tc_inter(ChunkParams p) {
       fence_after_sync();
       const int i = c;
       float d[kNh];
-      tmem_ld_sum(d1_of(it) + lane_off, h16, d);
-      const float* ut = reinterpret_cast<const float*>(slot + K3Smem::UT);
+      tmem_ld_sum<NS>(d1_of(it) + lane_off, h16, d);
+      const float* ut = reinterpret_cast<const float*>(slot + C::UT);
       const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int m = 0; m < kNh / 8; ++m) {
@@ -405,13 +422,13 @@ tc_inter(ChunkParams p) {
         *reinterpret_cast<uint4*>(uop + mnmajor_off(kNs + e, i, kUopSbo)) = lo;
       }
       fence_async_smem();
-      asm volatile("bar.sync %0, 128;" ::"n"(kUBarrier) : "memory");
+      asm volatile("bar.sync %0, %1;" ::"n"(kUBarrier), "n"(C::kUThreads) : "memory");
       // MMA 2, the state chain: [Sa | Sb] += Kr^T [U_hi | U_lo]
       if (tid == kMmaThread) {
         const uint32_t ub = smem_u32(uop);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_bf16(DS - lane_off, sdesc(smem_u32(slot + K3Smem::AK) + k * 256, 128, Rec::kAkSbo),
+          mma_bf16(DS - lane_off, sdesc(smem_u32(slot + C::AK) + k * 256, 128, Rec::kAkSbo),
                    sdesc(ub + k * 256, 128, kUopSbo), id_ak, 1);
         mma_commit(&bar_mma2);
       }
@@ -421,9 +438,15 @@ tc_inter(ChunkParams p) {
     okl = okl && mbar_wait_t<kPoll>(&bar_mma2, ph2, p.wait_ns);
     ph2 ^= 1;
     fence_after_sync();
+    // with a 2-slot ring, this chunk's slot takes chunk it+2 as soon as MMA 2
+    // has read it (MMA 1 and the U warps before it): a step of lead
+    if (C::kSlots == 2 && tid == kLoadThread && okl && it + 2 < nchunks) {
+      k3_load_chain<NS>(p, slot, &bar_full[it % C::kSlots], c_begin + it + 2, h, n0);
+      chain_issued = it + 3;
+    }
     {
       float v[kNh];
-      tmem_ld_sum(DS, h16, v);
+      tmem_ld_sum<NS>(DS, h16, v);
       if (ch.snap_slot >= 0 && p.snapshots && !pass1 && row_live) {
         float* dst = p.snapshots + ((size_t)ch.snap_slot * H + h) * DK * DV + (size_t)c * DV + n0 + h16;
 #pragma unroll
@@ -434,9 +457,9 @@ tc_inter(ChunkParams p) {
       if (it + 1 < nchunks) {
         okl = okl && wait_chain(it + 1, false);
         if (okl) chain_waited = it + 2;
-        gl = reinterpret_cast<const float*>(slot_of(it + 1) + K3Smem::GL)[c];
+        gl = reinterpret_cast<const float*>(slot_of(it + 1) + C::GL)[c];
       }
-      write_state(SOP, DS, c, h16, v, gl);
+      write_state<NS>(SOP, DS, c, h16, v, gl);
     }
     prev2 = prev1;
     prev1 = ch;
@@ -451,12 +474,12 @@ tc_inter(ChunkParams p) {
       if (nchunks >= 2) {
         okl = okl && wait_mma3(nchunks - 2);
         fence_after_sync();
-        if (okl) store_output(p, prev2, d1_of(nchunks - 2) + lane_off, h16, c - 64, h, n0, gfac);
+        if (okl) store_output<NS>(p, prev2, d1_of(nchunks - 2) + lane_off, h16, c - 64, h, n0, gfac);
       }
       if (p.out_gate) gfac = gate_factors(p, graw);  // chunk n-1's row
       okl = okl && wait_mma3(nchunks - 1);
       fence_after_sync();
-      if (okl) store_output(p, prev1, d1_of(nchunks - 1) + lane_off, h16, c - 64, h, n0, gfac);
+      if (okl) store_output<NS>(p, prev1, d1_of(nchunks - 1) + lane_off, h16, c - 64, h, n0, gfac);
     }
   }
   fence_before_sync();
@@ -465,7 +488,7 @@ tc_inter(ChunkParams p) {
   float* const fin = trans ? p.trans : p.final_state;
   if (ok && fin) {
     float v[kNh];
-    tmem_ld_sum(DS, h16, v);  // warp-collective: outside the row test
+    tmem_ld_sum<NS>(DS, h16, v);  // warp-collective: outside the row test
     float* dst = fin + sbase + (size_t)c * DV + n0 + h16;
     if (row_live)
 #pragma unroll
@@ -480,27 +503,40 @@ tc_inter(ChunkParams p) {
       for (int64_t j = chain_waited; j < chain_issued; ++j) wait_chain(j, true);
     if (tid == kOutThread)
       for (int64_t j = aq_waited; j < aq_issued; ++j)
-        mbar_wait(&bar_aq[j % K3Smem::kAqSlots], (uint32_t)((j / K3Smem::kAqSlots) & 1), kWaitLimitNs);
+        mbar_wait(&bar_aq[j % C::kAqSlots], (uint32_t)((j / C::kAqSlots) & 1), kWaitLimitNs);
     if (tid == kMmaThread || tid == kOutThread) mma_commit(&bar_drain);
     if (tid == kMmaThread) mbar_wait(&bar_drain, 0, kWaitLimitNs);
   }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 0) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-// tc_inter with the wait mode its limit asks for
-cudaError_t run_inter(const ChunkParams& p, dim3 grid, cudaStream_t stream) {
+// tc_inter with the wait mode its limit asks for, over grid (gx, gy, zmul x
+// the head's column slices)
+template <int NS>
+cudaError_t run_inter_ns(const ChunkParams& p, unsigned gx, unsigned gy, unsigned zmul, cudaStream_t stream) {
+  using C = K3Cfg<NS>;
   const bool poll = p.wait_ns < kPollLimitNs;
-  cudaError_t e = cudaFuncSetAttribute(poll ? tc_inter<true> : tc_inter<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K3Smem::BYTES);
+  auto kernel = poll ? tc_inter<true, NS> : tc_inter<false, NS>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::BYTES);
   if (e != cudaSuccess) return e;
-  if (poll)
-    tc_inter<true><<<grid, kThreads, K3Smem::BYTES, stream>>>(p);
-  else
-    tc_inter<false><<<grid, kThreads, K3Smem::BYTES, stream>>>(p);
+  kernel<<<dim3(gx, gy, zmul * (unsigned)(p.dv / NS)), C::kThreads, C::BYTES, stream>>>(p);
   return cudaGetLastError();
+}
+// 32 state columns per CTA while those CTAs all fit the GPU at once (a chain
+// step of a 32-column CTA is shorter), else 64 where the value columns come
+// in 64s (half the CTAs, each at a longer step: less time in all once the
+// CTAs run in waves)
+cudaError_t run_inter(const ChunkParams& p, unsigned gx, unsigned gy, unsigned zmul, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t ctas32 = (int64_t)gx * gy * zmul * (p.dv / 32);
+  return (p.dv % 64 == 0 && ctas32 > sms) ? run_inter_ns<64>(p, gx, gy, zmul, stream)
+                                          : run_inter_ns<32>(p, gx, gy, zmul, stream);
 }
 
 }  // namespace
@@ -518,20 +554,22 @@ cudaError_t launch_tc_prefill(const ChunkParams& p, cudaStream_t stream, cudaEve
     e = cudaEventRecord(mid, stream);
     if (e != cudaSuccess) return e;
   }
-  return run_inter(p, dim3((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)(p.dv / kNs)), stream);
+  return run_inter(p, (unsigned)p.num_seqs, (unsigned)p.H, 1, stream);
 }
 
 namespace {
 
 using namespace tcp;
 
+constexpr int kCombineNs = 32;  // state columns per CTA of the combine
+
 // inits[0] = S0 (or zeros); inits[s+1] = A_s inits[s] + B_s.  One CTA per
 // (head, 32-column slice); thread t owns row t / 2 and 16 columns.  The
 // slice of the running state sits in shared memory; A_s rows are read
 // straight from global memory (L2), 4 floats at a time.
 __global__ void __launch_bounds__(256) scan_combine(ScanBuffers sb, int P, int H) {
-  __shared__ __align__(16) float S[kD * kNs];
-  const int h = blockIdx.x, n0 = blockIdx.y * kNs;
+  __shared__ __align__(16) float S[kD * kCombineNs];
+  const int h = blockIdx.x, n0 = blockIdx.y * kCombineNs;
   const int r = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * 16;
   const size_t mat = (size_t)kD * kD;
   float acc[16];
@@ -545,7 +583,7 @@ __global__ void __launch_bounds__(256) scan_combine(ScanBuffers sb, int P, int H
 #pragma unroll
     for (int n = 0; n < 16; n += 4) {
       *reinterpret_cast<float4*>(out + n) = make_float4(acc[n], acc[n + 1], acc[n + 2], acc[n + 3]);
-      *reinterpret_cast<float4*>(S + r * kNs + c0 + n) = make_float4(acc[n], acc[n + 1], acc[n + 2], acc[n + 3]);
+      *reinterpret_cast<float4*>(S + r * kCombineNs + c0 + n) = make_float4(acc[n], acc[n + 1], acc[n + 2], acc[n + 3]);
     }
     if (s + 1 >= P) break;
     __syncthreads();
@@ -558,7 +596,7 @@ __global__ void __launch_bounds__(256) scan_combine(ScanBuffers sb, int P, int H
       const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const float* srow = S + (k + kk) * kNs + c0;
+        const float* srow = S + (k + kk) * kCombineNs + c0;
 #pragma unroll
         for (int n = 0; n < 16; n += 4) {
           const float4 x = *reinterpret_cast<const float4*>(srow + n);
@@ -612,9 +650,9 @@ cudaError_t launch_tc_prefill_scan(const ChunkParams& p, const ScanBuffers& sb, 
   p1.final_state = sb.B;
   p1.trans = sb.A;
   p1.snapshots = nullptr;
-  e = run_inter(p1, dim3((unsigned)p.num_seqs, (unsigned)p.H, 2 * (unsigned)(kD / kNs)), stream);
+  e = run_inter(p1, (unsigned)p.num_seqs, (unsigned)p.H, 2, stream);
   if (e != cudaSuccess) return e;
-  scan_combine<<<dim3((unsigned)p.H, (unsigned)(kD / kNs)), 256, 0, stream>>>(sb, p.num_seqs, p.H);
+  scan_combine<<<dim3((unsigned)p.H, (unsigned)(kD / kCombineNs)), 256, 0, stream>>>(sb, p.num_seqs, p.H);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // pass 2: every segment from its true initial state
@@ -623,7 +661,7 @@ cudaError_t launch_tc_prefill_scan(const ChunkParams& p, const ScanBuffers& sb, 
   p2.initial_state = sb.inits;
   p2.final_state = sb.finals;
   p2.trans = nullptr;
-  e = run_inter(p2, dim3((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)(kD / kNs)), stream);
+  e = run_inter(p2, (unsigned)p.num_seqs, (unsigned)p.H, 1, stream);
   if (e != cudaSuccess || !sb.final_state) return e;
   return cudaMemcpyAsync(sb.final_state, sb.finals + (size_t)(p.num_seqs - 1) * p.H * kD * kD,
                          (size_t)p.H * kD * kD * sizeof(float), cudaMemcpyDeviceToDevice, stream);

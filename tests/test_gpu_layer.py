@@ -141,6 +141,21 @@ def test_prefill_conv_variants_tc(width, silu, windows, gate_mode, head_gate):
     check(p, ref, "bf16", f"W={width} silu={silu} win={windows} gate={gate_mode} hg={head_gate}")
 
 
+@pytest.mark.parametrize("gate_mode", ["channel", "head"])
+def test_layer_steps_on_64_column_ctas(gate_mode):
+    """The convolution and the output gate with enough sequences and heads
+    that the inter-chunk kernel runs 64 state columns per CTA (its 32-column
+    CTAs would exceed the SM count): the gate's factors are applied by the
+    output rows of a 64-column CTA."""
+    lens = [5, 70, 129, 64, 1, 2, 200, 33, 90, 3]
+    H = 4
+    assert len(lens) * H * 4 > torch.cuda.get_device_properties(0).multi_processor_count
+    inp, li = case(lens, H, 128, 128, "bf16", seed=330, width=3, gate_mode=gate_mode)
+    p = gpu_prefill(inp, li, True, True)
+    ref = oracle_prefill(inp, li, True, True, "bf16")
+    check(p, ref, "bf16", f"64-column CTAs gate={gate_mode}")
+
+
 def test_output_gate_on_padded_heads():
     """bf16 heads of 64 channels run on the tensor-core kernels zero-padded
     to 128; the output gate (per channel and per head) rides on their store

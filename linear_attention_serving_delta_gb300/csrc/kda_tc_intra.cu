@@ -478,9 +478,13 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
   // the pipeline: chunk entries of the current and the next item; the first
   // item's rows are staged here (groups A and B), each later item's during
   // the item before it
+  // (chunk-table entries are read two items ahead of their first use, the
+  // L2 prefetch of the next item's rows: a global load's latency is hidden)
   ItemChunk ch = item_chunk<kConv>(p, item / H);  // entries past the table's end have len 0
   ItemChunk ch_next =
       item + stride < n_items ? item_chunk<kConv>(p, (item + stride) / H) : ItemChunk{0, 0, 0};
+  ItemChunk ch_next2 =
+      item + 2 * stride < n_items ? item_chunk<kConv>(p, (item + 2 * stride) / H) : ItemChunk{0, 0, 0};
   {
     const int h0 = (int)(item % H);
     if (tid == 0) {
@@ -634,7 +638,9 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
         nrm[128 + hc * 64 + i0 + r] = sk;
       }
     }
-    if (tid < 64) beta[tid] = tid < len ? beta_of(bcur) : 0.f;
+    // beta = sigmoid(b) with the fast exponential and division (it enters
+    // T diag(beta), which is rounded to bf16)
+    if (tid < 64) beta[tid] = tid < len ? __fdividef(1.f, 1.f + __expf(-bcur)) : 0.f;
     // the previous item's record copies must have read A1 before it is rewritten
     if (copy_group(tid) >= 0) bulk_wait_read_all();
     ok = __syncthreads_and(ok);
@@ -646,8 +652,10 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
       break;
     }
     if (tid < 64) {
-      inv_q[tid] = inv_norm_of(nrm[tid] + nrm[64 + tid]);
-      inv_k[tid] = inv_norm_of(nrm[128 + tid] + nrm[192 + tid]);
+      // 1 / max(|x|, 1e-6) = rsqrt(max(|x|^2, 1e-12)), with the hardware
+      // reciprocal square root (the operands it scales are rounded to bf16)
+      inv_q[tid] = rsqrtf(fmaxf(nrm[tid] + nrm[64 + tid], 1e-12f));
+      inv_k[tid] = rsqrtf(fmaxf(nrm[128 + tid] + nrm[192 + tid], 1e-12f));
     }
     // ---- V into B2 MN-major rows 128..255 (every raw row has been read:
     // the staging is free): the raw 16 bytes are one core-matrix row
@@ -921,8 +929,9 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
       bulk_commit();
     }
     ch = ch_next;
-    ch_next = item + 2 * stride < n_items ? item_chunk<kConv>(p, (item + 2 * stride) / H)
-                                          : ItemChunk{0, 0, 0};
+    ch_next = ch_next2;
+    ch_next2 = item + 3 * stride < n_items ? item_chunk<kConv>(p, (item + 3 * stride) / H)
+                                           : ItemChunk{0, 0, 0};
   }
   // no staging copy and no MMA is left in flight when the CTA exits (these
   // waits keep the long limit whatever the caller chose for the others)

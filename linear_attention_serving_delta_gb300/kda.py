@@ -737,12 +737,12 @@ def prefill_cached(cache: PrefixCache, pool, tokens, q, k, v, g, b, *, interval=
     rel = torch.tensor([x - p for x in absolute], dtype=torch.int64)
     cu_b = torch.tensor([0, len(absolute)], dtype=torch.int64)
     hcu = torch.tensor([0, T - p], dtype=torch.int64)
-    pr = Prefill(q[p:], k[p:], v[p:], g[p:], b[p:], hcu.to(dev),
-                 scale=scale, initial_state=pool[row:row + 1] if p > 0 else None,
-                 boundary_pos=rel.to(dev), cu_boundaries=cu_b.to(dev),
-                 host_cu_seqlens=hcu, host_boundary_pos=rel, host_cu_boundaries=cu_b,
-                 snapshot_pool=pool, snapshot_slot_map=torch.from_numpy(rows).to(dev))
     try:
+        pr = Prefill(q[p:], k[p:], v[p:], g[p:], b[p:], hcu.to(dev),
+                     scale=scale, initial_state=pool[row:row + 1] if p > 0 else None,
+                     boundary_pos=rel.to(dev), cu_boundaries=cu_b.to(dev),
+                     host_cu_seqlens=hcu, host_boundary_pos=rel, host_cu_boundaries=cu_b,
+                     snapshot_pool=pool, snapshot_slot_map=torch.from_numpy(rows).to(dev))
         pr.run(stream)
     except Exception:
         cache.forget(rows)  # the rows were never written: no lookup may resume from them

@@ -121,3 +121,19 @@ def test_forget_frees_rows_of_a_failed_prefill(kda):
         c.forget([4])                                        # outside the pool
     with pytest.raises(ValueError):
         c.forget([-2])
+
+
+def test_prefill_cached_forgets_rows_when_the_call_fails(kda):
+    """prefill_cached reserves rows before it builds and launches the prefill;
+    when that raises (here: host tensors, refused by the binding before any
+    launch), the reservation is dropped again, so the cache holds no entry
+    for states that were never written."""
+    import torch
+    c = kda.PrefixCache(8)
+    T, H, d = 300, 2, 16
+    x = torch.zeros(T, H, d)
+    pool = torch.zeros(8, H, d, d)
+    with pytest.raises(ValueError):
+        kda.prefill_cached(c, pool, toks(T, 21), x, x, x, x, torch.zeros(T, H), interval=128)
+    assert c.entries() == 0
+    assert c.lookup(toks(T, 21)) == (0, -1)

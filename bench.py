@@ -305,10 +305,10 @@ def bench_layer_steps(torch, kda, W, dev, steps=10):
 def bench_wide_heads(torch, kda, W, dev, steps=5):
     """Head sizes other than 128 (bf16, fp32 state).  64 channels: a prefill
     of one 8192-token sequence with 32 heads, on the tensor-core kernels
-    zero-padded to 128.  256 channels, on the CUDA-core path: a prefill of one
-    8192-token sequence with 16 heads and a decode step of 64 rows x 16 heads
-    (256 KB of state per head, read and written once: 2.15 GB a step).  L2
-    flushed before every call."""
+    zero-padded to 128, and a decode step of 1024 rows x 32 heads.  256
+    channels: a prefill of one 8192-token sequence with 16 heads (CUDA-core
+    path) and a decode step of 64 rows x 16 heads (256 KB of state per head,
+    read and written once: 2.15 GB a step).  L2 flushed before every call."""
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
     def timed(fn):
@@ -354,8 +354,9 @@ def bench_wide_heads(torch, kda, W, dev, steps=5):
     t_dec = timed(lambda: kda.kda_decode_step(*x, state, o))
     state_bytes = 2 * 64 * 16 * 256 * 256 * 4
     return {"workload": "bf16; dk = dv = 64: prefill of one 8192-token sequence x 32 heads "
-                        "(tensor cores, zero-padded); dk = dv = 256: prefill of one 8192-token "
-                        "sequence x 16 heads, decode of 64 rows x 16 heads (CUDA cores)",
+                        "(tensor cores, zero-padded), decode of 1024 rows x 32 heads (ring, 4 heads "
+                        "an item); dk = dv = 256: prefill of one 8192-token sequence x 16 heads "
+                        "(CUDA cores), decode of 64 rows x 16 heads (ring, 256 x 64 slices)",
             "d64_prefill_ms": t64, "d64_prefill_tokens_per_s": 8192 / (t64 * 1e-3),
             "d64_decode_workload": "1024 rows x 32 heads of 64 x 64 fp32 state (1.07 GB a step)",
             "d64_decode_us": t_d64, "d64_decode_state_gbs": 2 * 1024 * 32 * 64 * 64 * 4 / (t_d64 * 1e-6) / 1e9,

@@ -263,14 +263,21 @@ struct RingSlice {
   static constexpr int DVS = DV < CAP ? DV : CAP;
   static constexpr int NS = DV / DVS;  // slices per head
 };
-template <typename TIn, bool kConv, int DK, int DV>
+// G heads per item: consecutive heads of one row are adjacent in the pool
+// and in q, k, g, v, so a slot of G small heads (G x 16 or 32 KB) is filled
+// by the same few copies as one large head, and an item's fixed costs are
+// shared by G heads.  8 / G compute warps per head.
+template <typename TIn, bool kConv, int DK, int DV, int G = 1>
 struct Ring {
   static constexpr int DVS = RingSlice<DK, DV>::DVS, NS = RingSlice<DK, DV>::NS;
   static_assert((DK == 64 || DK == 128 || DK == 256) && (DVS == 64 || DVS == 128) && DK * DVS <= 128 * 128,
                 "ring head sizes");
-  static constexpr int RPW = DK / 8, CPL = DVS / 32;
-  static constexpr uint32_t STATE = DK * DVS * 4;
-  static constexpr uint32_t RK = DK * sizeof(TIn), RV = DVS * sizeof(TIn);  // a q / k / g row, a v slice
+  static_assert(G == 1 || (NS == 1 && !kConv && G * DK * DVS <= 128 * 128 && (G == 2 || G == 4)),
+                "several heads per item: unsliced heads, no convolution, at most 64 KB of state");
+  static constexpr int WH = 8 / G;                   // compute warps per head
+  static constexpr int RPW = DK / WH, CPL = DVS / 32;
+  static constexpr uint32_t STATE = G * DK * DVS * 4;
+  static constexpr uint32_t RK = G * DK * sizeof(TIn), RV = G * DVS * sizeof(TIn);  // q / k / g rows, v
   static constexpr uint32_t QO = STATE, KO = QO + RK, GO = KO + RK, VO = GO + RK;
   static constexpr uint32_t RW = RK > RV ? RK : RV;
   static constexpr uint32_t WIN = VO + RV;  // window row m of tensor t at WIN + (3 m + t) RW
@@ -337,23 +344,33 @@ __device__ __forceinline__ void tma_state_store(const CUtensorMap* m, int x, int
                : "memory");
 }
 
-// An item: (row, head, slice z) with the slices of one head adjacent
+// An item: (row, first head h, slice z) with the slices of one head
+// adjacent; with G heads per item (NS = 1), heads h .. h + G - 1
 struct RingItem {
   int row, h, z;
 };
-template <int NS>
+template <int NS, int G = 1>
 __device__ __forceinline__ RingItem ring_item(int64_t item, int H) {
+  if (G > 1) {
+    const int hg = H / G;
+    return RingItem{(int)(item / hg), (int)(item % hg) * G, 0};
+  }
   const int64_t rh = item / NS;
   return RingItem{(int)(rh / H), (int)(rh % H), (int)(item % NS)};
 }
+// index of (row, head h + gi) in a [B, H] tensor (b, g with a gate per head)
+template <int NS, int G = 1>
+__device__ __forceinline__ int64_t ring_rowhead(int64_t item, int gi) {
+  return (item / NS) * G + gi;
+}
 
-template <typename TIn, bool kConv, int DK, int DV>
+template <typename TIn, bool kConv, int DK, int DV, int G>
 __device__ __forceinline__ void ring_issue(const kda_decode_args& a, const kda_layer_args& l, uint8_t* stage,
                                            uint64_t* bar, int32_t* valid_flag, int64_t item,
                                            const CUtensorMap* smap) {
-  using R = Ring<TIn, kConv, DK, DV>;
+  using R = Ring<TIn, kConv, DK, DV, G>;
   const int H = a.num_heads;
-  const RingItem it = ring_item<R::NS>(item, H);
+  const RingItem it = ring_item<R::NS, G>(item, H);
   const int row = it.row, h = it.h;
   const int slot = a.state_slots ? a.state_slots[row] : row;
   const bool valid = slot >= 0 && slot < a.num_slots;
@@ -393,11 +410,11 @@ __device__ __forceinline__ void ring_issue(const kda_decode_args& a, const kda_l
 // test).  kConv: the short convolution (window rows in the slot).
 // smap: the pool as [slots H DK][DV] fp32 rows with a box of DVS columns x
 // DK rows (used when a head is cut into slices)
-template <typename TIn, bool kPoll, bool kConv, int DK, int DV>
-__global__ void __launch_bounds__(kRingAllThreads, (DK * DV <= 64 * 64) ? 2 : 1)
+template <typename TIn, bool kPoll, bool kConv, int DK, int DV, int G>
+__global__ void __launch_bounds__(kRingAllThreads, (G * DK * DV <= 64 * 64) ? 2 : 1)
 decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l, const __grid_constant__ CUtensorMap smap) {
-  using R = Ring<TIn, kConv, DK, DV>;
-  constexpr int kStages = R::STAGES, RPW = R::RPW, CPL = R::CPL, DVS = R::DVS, NS = R::NS;
+  using R = Ring<TIn, kConv, DK, DV, G>;
+  constexpr int kStages = R::STAGES, RPW = R::RPW, CPL = R::CPL, DVS = R::DVS, NS = R::NS, WH = R::WH;
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ __align__(8) uint64_t full[kStages];  // slot loaded
   __shared__ __align__(8) uint64_t done[kStages];  // slot's state updated by warps 0-7
@@ -425,8 +442,8 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l, const __
     if (lane == 0) {
       int64_t issued = 0;  // items whose slot copies were issued
       for (; issued < kStages && issued < n_local; ++issued)
-        ring_issue<TIn, kConv, DK, DV>(a, l, sm + issued * R::STAGE, &full[issued], &valid_flag[issued],
-                                       first + issued * stride, &smap);
+        ring_issue<TIn, kConv, DK, DV, G>(a, l, sm + issued * R::STAGE, &full[issued], &valid_flag[issued],
+                                          first + issued * stride, &smap);
       for (int64_t k = 0; k < n_local; ++k) {
         const int st = (int)(k % kStages);
         uint8_t* stage = sm + st * R::STAGE;
@@ -440,7 +457,7 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l, const __
         }
         const int64_t item = first + k * stride;
         if (valid_flag[st]) {
-          const RingItem it = ring_item<NS>(item, H);
+          const RingItem it = ring_item<NS, G>(item, H);
           const int slot = a.state_slots ? a.state_slots[it.row] : it.row;
           if (NS > 1)
             tma_state_store(&smap, it.z * DVS, (slot * H + it.h) * DK, stage);
@@ -450,7 +467,8 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l, const __
           tc::bulk_wait_read_all();
         }
         if (k + kStages < n_local) {
-          ring_issue<TIn, kConv, DK, DV>(a, l, stage, &full[st], &valid_flag[st], item + kStages * stride, &smap);
+          ring_issue<TIn, kConv, DK, DV, G>(a, l, stage, &full[st], &valid_flag[st], item + kStages * stride,
+                                            &smap);
           issued = k + kStages + 1;
         }
       }
@@ -459,9 +477,12 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l, const __
     return;
   }
 
-  // ---- compute warps 0-7; warp w owns key channels (rows) w + 8 i, i < RPW
+  // ---- compute warps 0-7: warp w works on head gi = w / WH of the item and
+  // owns its key channels (rows) lw + WH i, i < RPW (lw = w % WH)
+  const int gi = warp / WH, lw = warp % WH;
   const TIn* gb = static_cast<const TIn*>(a.b);
-  float b_next = n_local > 0 ? ld_in(gb, first / NS) : 0.f;  // b [B, H]: one per (row, head)
+  // b [B, H]: one per (row, head)
+  float b_next = n_local > 0 ? ld_in(gb, ring_rowhead<NS, G>(first, gi)) : 0.f;
   for (int64_t k = 0; k < n_local; ++k) {
     const int st = (int)(k % kStages);
     uint8_t* stage = sm + st * R::STAGE;
@@ -470,7 +491,7 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l, const __
     bool ok = tc::mbar_wait_t<kPoll>(&full[st], (uint32_t)((k / kStages) & 1), lim);
     const bool valid = valid_flag[st] != 0;
     const float b_cur = b_next;
-    if (k + 1 < n_local) b_next = ld_in(gb, (item + stride) / NS);
+    if (k + 1 < n_local) b_next = ld_in(gb, ring_rowhead<NS, G>(item + stride, gi));
     if (!valid) {  // uniform: nothing to compute, the slot is handed back
       mbar_arrive(&done[st]);
       if (!bar_and(kComputeBarrier, kRingThreads, ok)) {
@@ -479,25 +500,27 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l, const __
       }
       continue;
     }
-    const TIn* rq = reinterpret_cast<const TIn*>(stage + R::QO);
-    const TIn* rk = reinterpret_cast<const TIn*>(stage + R::KO);
-    const TIn* rg = reinterpret_cast<const TIn*>(stage + R::GO);
-    const TIn* rv = reinterpret_cast<const TIn*>(stage + R::VO);
-    // this warp's RPW rows: lane i < RPW holds raw q, k and alpha of row warp + 8 i
+    // this warp's head's rows of q, k, g, v in the slot
+    const TIn* rq = reinterpret_cast<const TIn*>(stage + R::QO) + gi * DK;
+    const TIn* rk = reinterpret_cast<const TIn*>(stage + R::KO) + gi * DK;
+    const TIn* rg = reinterpret_cast<const TIn*>(stage + R::GO) + gi * DK;
+    const TIn* rv = reinterpret_cast<const TIn*>(stage + R::VO) + gi * DVS;
+    // this warp's RPW rows: lane i < RPW holds raw q, k and alpha of row lw + WH i
     float xq = 0.f, xk = 0.f, xa = 0.f;
     // with the convolution: window row m of tensor t in the slot (0 without one)
     auto wrow = [&](int t, int m, int c) {
       return l.conv_in[t] ? ld_in(reinterpret_cast<const TIn*>(stage + R::WIN + (3 * m + t) * R::RW), c) : 0.f;
     };
-    const RingItem it = ring_item<NS>(item, H);
+    const RingItem it = ring_item<NS, G>(item, H);
     int slot = 0;
     if (kConv) slot = a.state_slots ? a.state_slots[it.row] : it.row;
     const int hh = it.h;
     if (lane < RPW) {
-      const int r = warp + 8 * lane;
+      const int r = lw + WH * lane;
       xq = ld_in(rq, r);
       xk = ld_in(rk, r);
-      xa = expf(log_alpha_of(a.gate_per_head ? ld_in(static_cast<const TIn*>(a.g), item / NS) : ld_in(rg, r)));
+      xa = expf(log_alpha_of(a.gate_per_head ? ld_in(static_cast<const TIn*>(a.g), ring_rowhead<NS, G>(item, gi))
+                                             : ld_in(rg, r)));
       if (kConv) {
         auto pq = [&](int m) { return wrow(0, m, r); };
         auto pk = [&](int m) { return wrow(1, m, r); };
@@ -512,13 +535,13 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l, const __
       if (lane == 0) *reinterpret_cast<float4*>(&part[buf][warp][0]) = make_float4(sq, sk, sqk, 0.f);
     }
     // retention and the two reductions over this warp's rows (raw q, k)
-    const float* S = reinterpret_cast<const float*>(stage);
+    const float* S = reinterpret_cast<const float*>(stage) + gi * DK * DVS;
     float s[RPW][CPL], pp[CPL], po[CPL];
 #pragma unroll
     for (int j = 0; j < CPL; ++j) pp[j] = po[j] = 0.f;
 #pragma unroll
     for (int i = 0; i < RPW; ++i) {
-      const int r = warp + 8 * i;
+      const int r = lw + WH * i;
       ld_cols<CPL>(S + r * DVS + CPL * lane, s[i]);
       const float a_r = __shfl_sync(0xffffffffu, xa, i), k_r = __shfl_sync(0xffffffffu, xk, i),
                   q_r = __shfl_sync(0xffffffffu, xq, i);
@@ -535,9 +558,10 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l, const __
       if (tid == 0 && a.status) atomicOr(a.status, kFlagTimeout);
       break;
     }
+    // the partial sums of this head's warps
     float sq = 0.f, sk = 0.f, sqk = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
+    for (int w = gi * WH; w < gi * WH + WH; ++w) {
       const float4 x = *reinterpret_cast<const float4*>(&part[buf][w][0]);
       sq += x.x; sk += x.y; sqk += x.z;
     }
@@ -546,7 +570,7 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l, const __
 #pragma unroll
     for (int j = 0; j < CPL; ++j) p[j] = oq[j] = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
+    for (int w = gi * WH; w < gi * WH + WH; ++w) {
       float x[CPL], y[CPL];
       ld_cols<CPL>(&red_p[buf][w][CPL * lane], x);
       ld_cols<CPL>(&red_o[buf][w][CPL * lane], y);
@@ -571,10 +595,10 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l, const __
     }
     // the updated state into the slot (each thread its own rows), then the
     // producer sends it back
-    float* Ss = reinterpret_cast<float*>(stage);
+    float* Ss = reinterpret_cast<float*>(stage) + gi * DK * DVS;
 #pragma unroll
     for (int i = 0; i < RPW; ++i) {
-      const int r = warp + 8 * i;
+      const int r = lw + WH * i;
       const float k_r = ik * __shfl_sync(0xffffffffu, xk, i);
 #pragma unroll
       for (int j = 0; j < CPL; ++j) s[i][j] += k_r * u[j];
@@ -582,9 +606,9 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l, const __
     }
     tc::fence_async_smem();
     mbar_arrive(&done[st]);
-    if (warp == 0) {
+    if (lw == 0) {  // one warp per head writes its o
       const float scl = a.scale;
-      const int row = it.row, h = it.h;
+      const int row = it.row, h = it.h + gi;
       TIn* o = static_cast<TIn*>(a.o);
       const int64_t ob = ((int64_t)row * H + h) * DV + it.z * DVS + CPL * lane;
 #pragma unroll
@@ -609,20 +633,20 @@ bool encode_state_map(CUtensorMap* m, const kda_decode_args& a) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename TIn, bool kConv, int DK, int DV>
+template <typename TIn, bool kConv, int DK, int DV, int G = 1>
 cudaError_t launch_ring(const kda_decode_args& a, const kda_layer_args& l, cudaStream_t stream) {
-  using R = Ring<TIn, kConv, DK, DV>;
+  using R = Ring<TIn, kConv, DK, DV, G>;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool poll = a.wait_limit_ns > 0 && (uint64_t)a.wait_limit_ns < tc::kPollLimitNs;
-  auto kernel = poll ? decode_ring<TIn, true, kConv, DK, DV> : decode_ring<TIn, false, kConv, DK, DV>;
+  auto kernel = poll ? decode_ring<TIn, true, kConv, DK, DV, G> : decode_ring<TIn, false, kConv, DK, DV, G>;
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)R::BYTES);
   if (e != cudaSuccess) return e;
   CUtensorMap smap{};
   if (R::NS > 1 && !encode_state_map<DK, DV>(&smap, a)) return cudaErrorInvalidValue;
-  const int64_t n_items = (int64_t)a.batch * a.num_heads * R::NS, slots = (int64_t)sms * R::CTAS;
+  const int64_t n_items = (int64_t)a.batch * a.num_heads * R::NS / G, slots = (int64_t)sms * R::CTAS;
   const int64_t grid = n_items < slots ? n_items : slots;
   kernel<<<(unsigned)grid, kRingAllThreads, R::BYTES, stream>>>(a, n_items, l, smap);
   return cudaGetLastError();
@@ -647,6 +671,12 @@ cudaError_t launch_t(const kda_decode_args& a, const kda_layer_args& l, cudaStre
                    al16(l.conv_in[2])))) {
       if constexpr (sizeof(TIn) == 2 && NS == 1 && DK <= 128)
         if (conv) return launch_ring<TIn, true, DK, DV>(a, l, stream);
+      // small heads: several per item (up to 64 KB of state), when the head
+      // count divides into groups of that size
+      if constexpr (NS == 1 && 4 * DK * DV <= 128 * 128)
+        if (a.num_heads % 4 == 0) return launch_ring<TIn, false, DK, DV, 4>(a, l, stream);
+      if constexpr (NS == 1 && 2 * DK * DV <= 128 * 128)
+        if (a.num_heads % 2 == 0) return launch_ring<TIn, false, DK, DV, 2>(a, l, stream);
       return launch_ring<TIn, false, DK, DV>(a, l, stream);
     }
   }

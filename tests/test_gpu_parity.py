@@ -173,6 +173,39 @@ def test_decode_full_size(oracle_mod):
     assert rel(host(state), ref_state) <= 1e-5
 
 
+@pytest.mark.parametrize("dk,dv,H,gate_per_head", [(64, 64, 4, False), (64, 64, 8, True), (64, 128, 6, False),
+                                                   (128, 64, 2, True), (64, 64, 6, False)])
+def test_decode_several_heads_per_item(dk, dv, H, gate_per_head, oracle_mod):
+    """Small heads share a ring item (several consecutive heads of a row, up
+    to 64 KB of state: 4 of 64 x 64, 2 of 64 x 128 or 128 x 64) when the
+    head count divides into such groups (H = 6 at 64 x 64 takes pairs).
+    Four steps with slot indirection and a skipped row, against the oracle;
+    o per (row, head) too."""
+    B = 7
+    dw = W.DecodeWorkload("group", B, H, dk, dv, 4, 501 + dk + dv + H)
+    inp = W.decode_inputs(dw)
+    state = inp["state"].cuda().contiguous()
+    ref_state = host(inp["state"]).astype(np.float64)
+    slots = torch.tensor([3, 0, -1, 6, 1, 5, 2], dtype=torch.int32)
+    units = [((r, h), (r, h)) for r in range(B) for h in range(H) if r != 2]
+    for step in range(dw.steps):
+        x = {n: inp[n][step].contiguous() for n in "qkvgb"}
+        gx = x["g"][:, :, 0].contiguous() if gate_per_head else x["g"]
+        gref = gx[:, :, None].expand(x["g"].shape) if gate_per_head else x["g"]
+        o = torch.zeros(B, H, dv, dtype=x["q"].dtype, device="cuda")
+        kda.kda_decode_step(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), gx.cuda(), x["b"].cuda(), state, o,
+                            state_slots=slots.cuda(), scale=0.9)
+        ro = oracle_mod.decode(host(x["q"]), host(x["k"]), host(x["v"]), host(gref), host(x["b"]), ref_state,
+                               slots=slots.numpy(), scale=0.9)
+        torch.cuda.synchronize()
+        assert rel(host(o), ro) <= TOL["bf16"]
+        e, at = worst_unit(host(o), ro, units)
+        assert e <= UNIT_FACTOR * TOL["bf16"], f"step {step}: worst (row, head) {at} {e:.3e}"
+        assert np.all(host(o)[2] == 0)
+    assert rel(host(state), ref_state) <= 1e-5
+    np.testing.assert_array_equal(host(state)[4], host(inp["state"])[4])  # slot 4 unused
+
+
 @pytest.mark.slow
 def test_decode_full_size_1000_steps(oracle_mod):
     """The batched decode workload as the benchmark runs it: 256 sequences x 32

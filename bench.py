@@ -257,6 +257,35 @@ def bench_gate_per_head(torch, kda, W, dev, steps=10):
             "ms_per_step": t, "tokens_per_s": T / (t * 1e-3), "steps": steps}
 
 
+def bench_fused(torch, kda, W, dev, steps=10):
+    """prefill_8k on the fused schedule (KDA_SCHEDULE_FUSED: the intra-chunk
+    pipelines and the inter-chunk chains in one kernel, the records read
+    back from L2), the same inputs and results as the default separate
+    kernels.  L2 flushed before every call."""
+    w = W.WORKLOADS[PREFILL_WL]
+    inp = W.prefill_inputs(w, device=dev, gen_device=dev)
+    p = kda.Prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["b"], inp["cu_seqlens"],
+                    host_cu_seqlens=inp["cu_seqlens"].cpu(), schedule=kda.SCHEDULE_FUSED)
+    path = kda.kda_prefill_schedule(p.args)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        p.run()
+    ms = []
+    for _ in range(steps):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        p.run()
+        e1.record()
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    assert p.device_status() == 0
+    t = sum(ms) / len(ms)
+    T = sum(inp["lens"])
+    return {"workload": w.description + ", fused schedule", "path": path,
+            "ms_per_step": t, "tokens_per_s": T / (t * 1e-3), "steps": steps}
+
+
 def bench_layer_steps(torch, kda, W, dev, steps=10):
     """prefill_8k with the layer steps around the recurrence: the short
     convolution (4 taps, SiLU) on q, k, v inside the intra-chunk kernel, with
@@ -572,6 +601,9 @@ def gpu_arm(a):
     if a.layer_only:
         print(json.dumps(bench_layer_steps(torch, kda, W, dev, steps=a.steps)))
         return
+    if a.fused_only:
+        print(json.dumps(bench_fused(torch, kda, W, dev, steps=a.steps)))
+        return
     if a.wide_only:
         print(json.dumps(bench_wide_heads(torch, kda, W, dev, steps=a.steps)))
         return
@@ -601,6 +633,7 @@ def gpu_arm(a):
     m1 = bench_1m(torch, kda, W, dev) if rank == 0 and not a.no_1m else None
     vl = bench_varlen(torch, kda, W, dev) if rank == 0 else None
     gph = bench_gate_per_head(torch, kda, W, dev) if rank == 0 else None
+    fus = bench_fused(torch, kda, W, dev) if rank == 0 else None
     lay = bench_layer_steps(torch, kda, W, dev) if rank == 0 else None
     wide = bench_wide_heads(torch, kda, W, dev) if rank == 0 else None
     if rank != 0:
@@ -676,6 +709,9 @@ def gpu_arm(a):
         "prefill_varlen": {"tokens": vl["tokens"], "ms": r3(vl["ms_per_step"]),
                            "tokens_per_s": r3(vl["tokens_per_s"]), "snapshots": vl["snapshots"]},
         "prefill_gate_per_head": {"ms": r3(gph["ms_per_step"]), "tokens_per_s": r3(gph["tokens_per_s"])},
+        "prefill_fused": {"ms": r3(fus["ms_per_step"]), "tokens_per_s": r3(fus["tokens_per_s"]),
+                          "fused_path": fus["path"] == kda.PATH_FUSED,
+                          "vs_separate": r3(step_ms / fus["ms_per_step"])},
         "prefill_layer_steps": {"ms": r3(lay["ms_per_step"]), "tokens_per_s": r3(lay["tokens_per_s"]),
                                 "kernels_ms": {k: r3(v) for k, v in lay["kernels_ms"].items()}},
         "wide_heads": {k: (r3(v) if isinstance(v, float) else v) for k, v in wide.items()
@@ -758,6 +794,8 @@ def main():
                     help="time the prefill workload alone (for profiler captures)")
     ap.add_argument("--layer-only", action="store_true",
                     help="time the prefill with the layer steps alone (for profiler captures)")
+    ap.add_argument("--fused-only", action="store_true",
+                    help="time the prefill on the fused schedule alone (for profiler captures)")
     ap.add_argument("--wide-only", action="store_true",
                     help="time the 256-channel heads alone")
     ap.add_argument("--decode-only", action="store_true",

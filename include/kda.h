@@ -183,7 +183,17 @@ typedef struct {
   const kda_layer_args* layer; /* host pointer, or NULL: the short convolution and
                                   output gate (above); read during the call only.
                                   Windows are [N, conv_width - 1, H, d]          */
+  int32_t schedule;            /* KDA_SCHEDULE_AUTO (0) or KDA_SCHEDULE_SEPARATE
+                                  (1): the intra-chunk and inter-chunk kernels one
+                                  after the other; KDA_SCHEDULE_FUSED (2): the
+                                  fused kernel where it applies (see below), else
+                                  the two kernels.  All give the same results, bit
+                                  for bit                                       */
 } kda_prefill_args;
+
+#define KDA_SCHEDULE_AUTO 0
+#define KDA_SCHEDULE_SEPARATE 1
+#define KDA_SCHEDULE_FUSED 2
 
 /*
  * Segment scan.  The inter-chunk recurrence of one sequence is a chain over
@@ -202,6 +212,34 @@ typedef struct {
  * with P >= 3 segments of >= 16 chunks each.  The results match the unsplit
  * chain to rounding (fp32 state combine), not bit for bit.
  */
+
+/*
+ * Fused prefill (schedule = KDA_SCHEDULE_FUSED).  On the tensor-core path the
+ * intra-chunk step (K2) and the inter-chunk chains (K3) run as one kernel of
+ * two CTAs per SM: a CTA either runs the chain of one (sequence, head,
+ * 32-column slice of the state) or a pipeline of (chunk, head) items taken in
+ * chunk order.  Each record is published once written; a chain copies it as
+ * soon as it sees it, from L2, so the records are read back from L2 rather
+ * than HBM and the chains run while the items are made.  Pipelines never wait
+ * for chains and the chains are placed after the pipelines they read, so no
+ * wait depends on the CTAs being resident together.  It applies without the
+ * segment scan when the chains (num_seqs x num_heads x dv / 32) are at most
+ * as many as the SMs.  A chain waits for a record at most the longer of
+ * wait_limit_ns and 1 s.  Measured on GB300 it is slower than the two kernels
+ * (a chain step takes about twice as long on an SM shared with another CTA
+ * as on an SM of its own), so the automatic choice does not take it.  With
+ * phase_events, the intra-chunk phase holds the fused kernel and the
+ * inter-chunk phase only what follows it.
+ */
+
+/* The path kda_prefill takes for these arguments on a GPU with sm_count SMs
+ * (0: the current device, which must then be present).  Host-side fields
+ * only; -1 for invalid arguments or a failed device query. */
+#define KDA_PATH_CUDA_CORES 0    /* fp32 CUDA-core kernels                  */
+#define KDA_PATH_SEPARATE 1      /* tensor cores, K2 then K3                 */
+#define KDA_PATH_FUSED 2         /* tensor cores, the fused kernel           */
+#define KDA_PATH_SEGMENT_SCAN 3  /* tensor cores, the segment scan           */
+int32_t kda_prefill_schedule(const kda_prefill_args* args, int32_t sm_count);
 
 /* Number of timed phases of kda_prefill (see phase_events). */
 #define KDA_PREFILL_PHASES 3

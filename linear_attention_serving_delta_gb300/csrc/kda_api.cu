@@ -108,11 +108,29 @@ kda_status_t validate_prefill(const kda_prefill_args* a) {
   if (!a->snapshot_slot_map && a->snapshot_map_len != 0) return KDA_ERR_INVALID_ARG;
   if (a->wait_limit_ns < 0) return KDA_ERR_INVALID_ARG;
   if (a->gate_per_head != 0 && a->gate_per_head != 1) return KDA_ERR_INVALID_ARG;
+  if (a->schedule != KDA_SCHEDULE_AUTO && a->schedule != KDA_SCHEDULE_SEPARATE &&
+      a->schedule != KDA_SCHEDULE_FUSED)
+    return KDA_ERR_INVALID_ARG;
   kda_status_t ls = validate_layer(a->layer, a->num_seqs, a->num_heads, a->dk, a->dv, elem_bytes(a->in_dtype));
   if (ls != KDA_OK) return ls;
   // sizes whose products must stay inside the index types used by the kernels
   if (a->total_tokens > ((int64_t)1 << 40)) return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
+}
+
+// The fused tensor-core prefill applies to these arguments when its chains
+// (one per sequence, head and 32-column slice) are at most as many as the
+// SMs: each takes half an SM beside an item CTA.  Host-side fields only, and
+// the SM count.
+bool fused_shape(const kda_prefill_args* a) {
+  return use_tensor_cores(a) && scan_segments_of(a) == 1 && a->dv % fused_chain_columns() == 0 &&
+         a->total_tokens > 0;
+}
+int64_t fused_chains(const kda_prefill_args* a) {
+  return (int64_t)a->num_seqs * a->num_heads * (a->dv / fused_chain_columns());
+}
+bool fused_fits(const kda_prefill_args* a, int sms) {
+  return a->schedule == KDA_SCHEDULE_FUSED && fused_shape(a) && fused_chains(a) <= sms;
 }
 
 WsLayout prefill_layout(const kda_prefill_args* a) {
@@ -139,6 +157,8 @@ WsLayout prefill_layout(const kda_prefill_args* a) {
   L.seq_aux = take(sizeof(int64_t) * 3 * N);  // seq_len [N] + seq_bnd [2N]
   L.chunks = take(sizeof(Chunk) * (size_t)L.max_chunks);
   L.inter = take(L.rec_bytes * (size_t)L.max_chunks * (size_t)a->num_heads);
+  if (fused_shape(a) && a->schedule == KDA_SCHEDULE_FUSED)
+    L.rec_ready = take(sizeof(uint32_t) * (size_t)L.max_chunks * a->num_heads);
   L.scan_P = P;
   if (P > 1) {
     const size_t mats = (size_t)P * a->num_heads * a->dk * a->dv * sizeof(float);
@@ -164,6 +184,21 @@ extern "C" {
 size_t kda_prefill_workspace_size(const kda_prefill_args* args) {
   if (validate_prefill(args) != KDA_OK) return 0;
   return prefill_layout(args).total;
+}
+
+int32_t kda_prefill_schedule(const kda_prefill_args* a, int32_t sm_count) {
+  if (validate_prefill(a) != KDA_OK || sm_count < 0) return -1;
+  if (!use_tensor_cores(a)) return KDA_PATH_CUDA_CORES;
+  if (scan_segments_of(a) > 1) return KDA_PATH_SEGMENT_SCAN;
+  bool device_ok = true;
+  if (sm_count == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return -1;
+    device_ok = fused_supported(dev);
+  }
+  return device_ok && fused_fits(a, sm_count) ? KDA_PATH_FUSED : KDA_PATH_SEPARATE;
 }
 
 kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, void* stream_) {
@@ -255,9 +290,21 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
     sb.s0 = a->initial_state;
     sb.final_state = a->final_state;
     e = launch_tc_prefill_scan(cp, sb, stream, ev ? ev[2] : nullptr);
+  } else if (use_tensor_cores(a)) {
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    if (fused_fits(a, sms) && fused_supported(dev)) {
+      cp.rec_ready = reinterpret_cast<uint32_t*>(w + L.rec_ready);
+      e = cudaMemsetAsync(cp.rec_ready, 0, sizeof(uint32_t) * (size_t)L.max_chunks * a->num_heads, stream);
+      if (e == cudaSuccess) e = launch_tc_fused(cp, (int32_t)fused_chains(a), 2 * sms, stream);
+      if (e == cudaSuccess && ev) e = cudaEventRecord(ev[2], stream);
+    } else {
+      e = launch_tc_prefill(cp, stream, ev ? ev[2] : nullptr);
+    }
   } else {
-    e = use_tensor_cores(a) ? launch_tc_prefill(cp, stream, ev ? ev[2] : nullptr)
-                            : launch_simt_prefill(cp, a->in_dtype, stream, ev ? ev[2] : nullptr);
+    e = launch_simt_prefill(cp, a->in_dtype, stream, ev ? ev[2] : nullptr);
   }
   if (e == cudaSuccess && a->layer && a->layer->conv_width > 1) {
     const void* x[3] = {a->q, a->k, a->v};

@@ -133,6 +133,9 @@ struct WsLayout {
   // segment scan: segment count (1 = off) and its buffers
   int32_t scan_P = 1;
   size_t scan_cu = 0, scan_A = 0, scan_B = 0, scan_inits = 0, scan_finals = 0;
+  // fused tensor-core prefill: a flag per record (where the arguments can
+  // take it)
+  size_t rec_ready = 0;
 };
 
 }  // namespace kda

@@ -79,6 +79,9 @@ struct ChunkParams {
   int32_t conv_one_seq;
   const void* out_gate;     // [T][H][dv], or [T][H] with out_gate_per_head
   int32_t out_gate_per_head;
+  // the fused tensor-core prefill: a flag per record [max_chunks][H], zero
+  // at the launch, set once the record is complete (null otherwise)
+  uint32_t* rec_ready;
 };
 constexpr int32_t kScanPass1 = 1;
 
@@ -101,6 +104,14 @@ cudaError_t launch_simt_prefill(const ChunkParams& p, kda_dtype_t dt, cudaStream
 extern const bool kHaveTensorCorePath;
 size_t tc_record_bytes();
 cudaError_t launch_tc_prefill(const ChunkParams& p, cudaStream_t stream, cudaEvent_t mid);
+// The fused tensor-core prefill (kda_tc_fused.cu): one launch of `grid`
+// CTAs (two per SM), the last n_chain of them the chains of the (sequence,
+// head, fused_chain_columns()-column slice) triples in that order, the
+// others the intra-chunk item pipelines; p.rec_ready set and zero.
+// fused_supported: the device holds two of its CTAs per SM.
+int fused_chain_columns();
+bool fused_supported(int device);
+cudaError_t launch_tc_fused(const ChunkParams& p, int32_t n_chain, int32_t grid, cudaStream_t stream);
 // The segment scan over P chunk-aligned segments of one sequence (planned as
 // P sequences in `p`): K2 once, K3 pass 1 (state offsets B and transition
 // maps A of every segment, in parallel), the combine (inits[s+1] = A_s

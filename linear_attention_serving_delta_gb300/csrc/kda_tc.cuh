@@ -95,6 +95,42 @@ __device__ __forceinline__ void fence_after_sync() {
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// the same between the generic and the async proxy for global memory
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// orders this thread's earlier memory accesses before its later ones for
+// every thread of the GPU
+__device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Barrier of a group of 256 threads, warp-aligned: barrier `id` of the CTA
+// with a count of 256 (id 0 when the group is the whole CTA, else a named
+// barrier of its own), with the and / or reductions of __syncthreads_and /
+// __syncthreads_or.
+struct PipeSync {
+  uint32_t id;
+  __device__ __forceinline__ void sync() const { asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory"); }
+  __device__ __forceinline__ bool all(bool v) const {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id)
+        : "memory");
+    return r != 0;
+  }
+  __device__ __forceinline__ bool any(bool v) const {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id)
+        : "memory");
+    return r != 0;
+  }
+};
 
 // 32 lanes x 16 columns of 32-bit data from TMEM: thread i of the warp gets
 // columns [col, col+16) of lane (lane_base + i).  Followed by tmem_ld_wait().
@@ -230,6 +266,30 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 }
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
+
+// 32-bit counters in global memory shared between CTAs (gpu scope)
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* a) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t* a, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_relaxed_add_u32(uint32_t* a, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+// Waits until *a >= target, polling with short sleeps, for at most limit_ns
+// of wall time; false on expiry.
+__device__ __forceinline__ bool wait_at_least(const uint32_t* a, uint32_t target, uint64_t limit_ns) {
+  if (ld_acquire_u32(a) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (ld_acquire_u32(a) >= target) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
 
 }  // namespace tc
 }  // namespace kda

@@ -27,6 +27,9 @@ KDA_OK = 0
 KDA_F32, KDA_BF16 = 0, 1
 CHUNK = 64
 PREFILL_PHASES = 3  # chunk planning, intra-chunk, inter-chunk
+SCHEDULE_AUTO, SCHEDULE_SEPARATE, SCHEDULE_FUSED = 0, 1, 2  # kda_prefill_args.schedule
+# kda_prefill_schedule: the path a prefill takes
+PATH_CUDA_CORES, PATH_SEPARATE, PATH_FUSED, PATH_SEGMENT_SCAN = 0, 1, 2, 3
 _STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED",
                  3: "KDA_ERR_WORKSPACE", 4: "KDA_ERR_CUDA", 5: "KDA_ERR_TIMEOUT",
                  6: "KDA_ERR_DEVICE_DATA"}
@@ -36,7 +39,7 @@ EXPORTED = ("kda_prefill_workspace_size", "kda_prefill", "kda_prefill_noalloc",
             "kda_prefix_cache_create", "kda_prefix_cache_destroy", "kda_prefix_cache_entries",
             "kda_prefix_cache_lookup", "kda_prefix_cache_reserve",
             "kda_prefill_device_status", "kda_snapshot_plan", "kda_decode_step", "kda_prep",
-            "kda_status_string", "kda_version")
+            "kda_status_string", "kda_version", "kda_prefill_schedule")
 NOALLOC_SCRATCH_BYTES = 64 << 20  # fixed workspace behind kda_prefill_noalloc
 
 
@@ -68,7 +71,7 @@ class PrefillArgs(ctypes.Structure):
                 ("num_snapshots", c_i64), ("phase_events", c_vp), ("scan_segments", c_i32),
                 ("snapshot_slot_map", c_vp), ("snapshot_map_len", c_i64),
                 ("wait_limit_ns", c_i64), ("gate_per_head", c_i32),
-                ("layer", ctypes.POINTER(LayerArgs))]
+                ("layer", ctypes.POINTER(LayerArgs)), ("schedule", c_i32)]
 
 
 class PrefillHostArgs(ctypes.Structure):
@@ -111,6 +114,8 @@ def lib() -> ctypes.CDLL:
             L = ctypes.CDLL(LIB_PATH)
             L.kda_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs)]
             L.kda_prefill_workspace_size.restype = ctypes.c_size_t
+            L.kda_prefill_schedule.argtypes = [ctypes.POINTER(PrefillArgs), c_i32]
+            L.kda_prefill_schedule.restype = c_i32
             L.kda_prefill.argtypes = [ctypes.POINTER(PrefillArgs), c_vp, ctypes.c_size_t, c_vp]
             L.kda_prefill.restype = ctypes.c_int
             L.kda_prefill_host_workspace_size.argtypes = [ctypes.POINTER(PrefillHostArgs)]
@@ -262,7 +267,7 @@ def make_prefill_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=
                       final_state=None, snapshot_interval=0, boundary_pos=None,
                       cu_boundaries=None, cu_snapshots=None, snapshots=None,
                       scan_segments=0, snapshot_slot_map=None, wait_limit_ns=0,
-                      layer: LayerArgs | None = None) -> PrefillArgs:
+                      layer: LayerArgs | None = None, schedule=SCHEDULE_AUTO) -> PrefillArgs:
     T, H, dk, dv, N = _check_shapes(q, k, v, g, b, cu_seqlens, o, initial_state, final_state)
     dt = q.dtype
     if snapshots is not None and (snapshots.dim() != 4 or tuple(snapshots.shape[1:]) != (H, dk, dv)):
@@ -295,12 +300,19 @@ def make_prefill_args(q, k, v, g, b, cu_seqlens, o, *, scale=1.0, initial_state=
     a.gate_per_head = 1 if g.dim() == 2 else 0
     if layer is not None:
         a.layer = ctypes.pointer(layer)  # the pointer object keeps `layer` alive
+    a.schedule = int(schedule)
     return a
 
 
 # ----------------------------------------------------------------- the C entry points
 def kda_prefill_workspace_size(args: PrefillArgs) -> int:
     return int(lib().kda_prefill_workspace_size(ctypes.byref(args)))
+
+
+def kda_prefill_schedule(args: PrefillArgs, sm_count: int = 0) -> int:
+    """The path kda_prefill takes for ``args`` on a GPU with ``sm_count`` SMs
+    (0: the current device); one of the PATH_* values, -1 if invalid."""
+    return int(lib().kda_prefill_schedule(ctypes.byref(args), int(sm_count)))
 
 
 def kda_prefill(args: PrefillArgs, workspace: torch.Tensor, stream=None) -> None:
@@ -497,7 +509,7 @@ class Prefill:
                  want_final=True, host_cu_seqlens=None, host_boundary_pos=None,
                  host_cu_boundaries=None, o=None, scan_segments=0, snapshot_pool=None,
                  snapshot_slot_map=None, wait_limit_ns=0, conv_weights=None, conv_silu=False,
-                 conv_window=None, conv_window_out=None, out_gate=None):
+                 conv_window=None, conv_window_out=None, out_gate=None, schedule=SCHEDULE_AUTO):
         """The layer steps: conv_weights (wq, wk, wv) float32 [W, H, d] turn on
         the short convolution, with each sequence's window before the call in
         conv_window ((q, k, v) [N, W-1, H, d], None = zeros); conv_window_out
@@ -547,7 +559,7 @@ class Prefill:
             cu_snapshots=self.cu_snapshots, snapshots=self.snapshots,
             scan_segments=scan_segments,
             snapshot_slot_map=snapshot_slot_map if self.snapshots is not None else None,
-            wait_limit_ns=wait_limit_ns, layer=self.layer)
+            wait_limit_ns=wait_limit_ns, layer=self.layer, schedule=schedule)
         nbytes = kda_prefill_workspace_size(self.args)
         if nbytes == 0:
             raise ValueError("kda_prefill_workspace_size rejected the arguments")

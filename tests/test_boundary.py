@@ -64,6 +64,13 @@ int main(void) {
   printf("const.KDA_CONV_MAX %d\n", KDA_CONV_MAX);
   printf("const.KDA_CHUNK %d\n", KDA_CHUNK);
   printf("const.KDA_PREFILL_PHASES %d\n", KDA_PREFILL_PHASES);
+  printf("const.KDA_SCHEDULE_AUTO %d\n", KDA_SCHEDULE_AUTO);
+  printf("const.KDA_SCHEDULE_SEPARATE %d\n", KDA_SCHEDULE_SEPARATE);
+  printf("const.KDA_SCHEDULE_FUSED %d\n", KDA_SCHEDULE_FUSED);
+  printf("const.KDA_PATH_CUDA_CORES %d\n", KDA_PATH_CUDA_CORES);
+  printf("const.KDA_PATH_SEPARATE %d\n", KDA_PATH_SEPARATE);
+  printf("const.KDA_PATH_FUSED %d\n", KDA_PATH_FUSED);
+  printf("const.KDA_PATH_SEGMENT_SCAN %d\n", KDA_PATH_SEGMENT_SCAN);
   F(kda_layer_args, conv_silu) F(kda_layer_args, conv_w) F(kda_layer_args, conv_in)
   F(kda_layer_args, conv_out) F(kda_layer_args, out_gate) F(kda_layer_args, out_gate_per_head)
   F(kda_prefill_args, layer) F(kda_decode_args, layer) F(kda_prep_args, layer)
@@ -77,7 +84,7 @@ int main(void) {
   F(kda_prefill_args, snapshots) F(kda_prefill_args, num_snapshots)
   F(kda_prefill_args, phase_events) F(kda_prefill_args, scan_segments)
   F(kda_prefill_args, snapshot_slot_map) F(kda_prefill_args, wait_limit_ns)
-  F(kda_prefill_args, gate_per_head) F(kda_decode_args, gate_per_head)
+  F(kda_prefill_args, gate_per_head) F(kda_prefill_args, schedule) F(kda_decode_args, gate_per_head)
   F(kda_prep_args, gate_per_head) F(kda_prefill_host_args, gate_per_head)
   F(kda_decode_args, scale) F(kda_decode_args, q) F(kda_decode_args, state_slots)
   F(kda_decode_args, o) F(kda_decode_args, wait_limit_ns) F(kda_decode_args, status)
@@ -95,7 +102,11 @@ int main(void) {
                "kda_prep_args": kda.PrepArgs, "kda_prefill_host_args": kda.PrefillHostArgs,
                "kda_layer_args": kda.LayerArgs}
     consts = {"KDA_CONV_MAX": kda.CONV_MAX, "KDA_CHUNK": kda.CHUNK,
-              "KDA_PREFILL_PHASES": kda.PREFILL_PHASES}
+              "KDA_PREFILL_PHASES": kda.PREFILL_PHASES,
+              "KDA_SCHEDULE_AUTO": kda.SCHEDULE_AUTO, "KDA_SCHEDULE_SEPARATE": kda.SCHEDULE_SEPARATE,
+              "KDA_SCHEDULE_FUSED": kda.SCHEDULE_FUSED,
+              "KDA_PATH_CUDA_CORES": kda.PATH_CUDA_CORES, "KDA_PATH_SEPARATE": kda.PATH_SEPARATE,
+              "KDA_PATH_FUSED": kda.PATH_FUSED, "KDA_PATH_SEGMENT_SCAN": kda.PATH_SEGMENT_SCAN}
     for key, val in got.items():
         if key.startswith("const."):
             assert consts[key[6:]] == int(val), key
@@ -139,10 +150,21 @@ def test_workspace_size_and_validation(kda):
     # bf16 heads of 64 channels take the tensor-core path (zero-padded to 128:
     # its 90,624-byte record per chunk-head), fp32 ones the CUDA-core path
     # (82,176 bytes): 2 chunk-table entries (64 tokens + one per sequence) x 2 heads
-    tcp = _args(kda, in_dtype=kda.KDA_BF16, dk=64, dv=64)
+    tcp = _args(kda, in_dtype=kda.KDA_BF16, dk=64, dv=64, schedule=kda.SCHEDULE_SEPARATE)
     cup = _args(kda, dk=64, dv=64)
     assert (L.kda_prefill_workspace_size(ctypes.byref(tcp)) -
             L.kda_prefill_workspace_size(ctypes.byref(cup))) == 2 * 2 * (90624 - 82176)
+    # the fused kernel reads the same record array; only its flags are added
+    # (2 chunk-table entries x 2 heads, one 256-byte block), the automatic
+    # choice is the separate kernels, and an unknown schedule is rejected
+    fused = _args(kda, in_dtype=kda.KDA_BF16, dk=64, dv=64, schedule=kda.SCHEDULE_FUSED)
+    auto = _args(kda, in_dtype=kda.KDA_BF16, dk=64, dv=64)
+    assert (L.kda_prefill_workspace_size(ctypes.byref(fused)) -
+            L.kda_prefill_workspace_size(ctypes.byref(tcp))) == 256
+    assert L.kda_prefill_workspace_size(ctypes.byref(auto)) == L.kda_prefill_workspace_size(ctypes.byref(tcp))
+    a = _args(kda, schedule=3)
+    assert L.kda_prefill_workspace_size(ctypes.byref(a)) == 0
+    assert L.kda_prefill(ctypes.byref(a), 0x4000, 1 << 30, None) == 1
     # heads of 256 channels are taken (the CUDA-core path's blocked kernel)
     wide = _args(kda, dk=256, dv=256)
     assert L.kda_prefill_workspace_size(ctypes.byref(wide)) > ws
@@ -171,6 +193,35 @@ def test_workspace_size_and_validation(kda):
     assert L.kda_prefill_workspace_size(ctypes.byref(_args(kda, scan_segments=4))) == ws
     assert L.kda_prefill(None, 0x4000, ws, None) == 1
     assert kda.kda_status_string(3).startswith("workspace")
+
+
+def test_prefill_schedule(kda):
+    """The path a prefill takes (kda_prefill_schedule, host logic only, for a
+    given SM count): the separate tensor-core kernels by default; with
+    schedule = FUSED the fused kernel where its chains (sequences x heads x
+    dv / 32) are at most as many as the SMs; the segment scan and the fp32
+    CUDA-core path where they apply."""
+    L = kda.lib()
+    bf = dict(in_dtype=kda.KDA_BF16, dk=128, dv=128)
+    fu = dict(schedule=kda.SCHEDULE_FUSED)
+
+    def path(sms=152, **over):
+        return L.kda_prefill_schedule(ctypes.byref(_args(kda, **over)), sms)
+
+    assert path(num_heads=32, total_tokens=8192, **bf) == kda.PATH_SEPARATE       # the default
+    assert path(num_heads=32, total_tokens=8192, schedule=kda.SCHEDULE_SEPARATE, **bf) == kda.PATH_SEPARATE
+    assert path(num_heads=32, total_tokens=8192, **fu, **bf) == kda.PATH_FUSED    # 128 chains
+    assert path(num_heads=38, total_tokens=8192, **fu, **bf) == kda.PATH_FUSED    # 152 chains
+    assert path(num_heads=39, total_tokens=8192, **fu, **bf) == kda.PATH_SEPARATE  # 156 chains
+    assert path(sms=100, num_heads=32, total_tokens=8192, **fu, **bf) == kda.PATH_SEPARATE
+    assert path(num_seqs=8, num_heads=32, total_tokens=8192, **fu, **bf) == kda.PATH_SEPARATE
+    assert path(num_heads=32, total_tokens=8192, in_dtype=kda.KDA_BF16, dk=64, dv=64, **fu) == kda.PATH_FUSED
+    assert path(num_heads=32, total_tokens=8192, in_dtype=kda.KDA_BF16, dk=128, dv=32, **fu) == kda.PATH_FUSED
+    assert path(num_heads=32, total_tokens=0, **fu, **bf) == kda.PATH_SEPARATE    # nothing to fuse
+    assert path(num_heads=32, total_tokens=8192, **fu) == kda.PATH_CUDA_CORES     # fp32
+    assert path(num_heads=2, total_tokens=65536, **fu, **bf) == kda.PATH_SEGMENT_SCAN
+    assert path(num_heads=2, total_tokens=65536, scan_segments=1, **fu, **bf) == kda.PATH_FUSED
+    assert path(num_seqs=0) == -1 and path(sms=-1) == -1
 
 
 def test_layer_args_validation(kda):

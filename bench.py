@@ -53,10 +53,12 @@ DECODE_STATE_BYTES_PER_HEAD = 2 * 128 * 128 * 4                # read + write fp
 # sources each kernel is built from: a profile summary counts only while
 # these files hash to the value recorded in it
 KERNEL_SOURCES = {
-    "tc_intra": ["kda_tc_intra.cu", "kda_tc_common.cuh", "kda_tc.cuh", "kda_internal.cuh",
-                 "kda_common.cuh"],
-    "tc_inter": ["kda_tc_inter.cu", "kda_tc_common.cuh", "kda_tc.cuh", "kda_internal.cuh",
-                 "kda_common.cuh"],
+    "tc_intra": ["kda_tc_intra.cu", "kda_tc_intra.cuh", "kda_tc_handoff.cuh", "kda_tc_common.cuh",
+                 "kda_tc.cuh", "kda_internal.cuh", "kda_common.cuh"],
+    "tc_inter": ["kda_tc_inter.cu", "kda_tc_inter.cuh", "kda_tc_handoff.cuh", "kda_tc_common.cuh",
+                 "kda_tc.cuh", "kda_internal.cuh", "kda_common.cuh"],
+    "tc_fused": ["kda_tc_fused.cu", "kda_tc_intra.cuh", "kda_tc_inter.cuh", "kda_tc_handoff.cuh",
+                 "kda_tc_common.cuh", "kda_tc.cuh", "kda_internal.cuh", "kda_common.cuh"],
     "decode_ring": ["kda_decode.cu", "kda_tc.cuh", "kda_internal.cuh", "kda_common.cuh"],
     "prep_vec": ["kda_prep.cu", "kda_internal.cuh", "kda_common.cuh"],
     "plan_kernel": ["kda_plan.cu", "kda_internal.cuh", "kda_common.cuh"],

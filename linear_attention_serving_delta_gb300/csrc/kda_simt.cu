@@ -15,9 +15,15 @@
 //
 // obtained by expanding the token recurrence (delta rule with a diagonal
 // gate, "From KV Cache to Depth Attention", Technical Details) inside the
-// chunk.  This path keeps everything in fp32 and forms exp(G_i - G_j)
-// directly, so it has no exponent-range limit; it serves fp32 inputs and
-// head sizes other than 128.
+// chunk.  This path keeps everything in fp32; it serves fp32 inputs and head
+// sizes other than 128.  A_kk and A_qk are products of factors with a
+// per-channel reference s (an integer number of nats, so G - s is exact):
+// Kp = k^ e^(G - s), Qp = q^ e^(G - s), Kn = k^ e^(s - G), so that
+// exp(G_i - G_j) = e^(G_i - s) e^(s - G_j) with both factors in fp32 range.
+// s = 0 while a channel's chunk decay G_L stays above -kRefNats, else
+// round(G_L / 2); a chunk (or block of channels) whose G_L falls below
+// -kMaxNats in some channel forms exp(G_i - G_j) directly instead, so the
+// path has no exponent-range limit.
 //
 // K2 (intra) runs one CTA per (chunk, head) and writes a SimtRec per pair;
 // K3 (inter) runs one CTA per (sequence, head, value-column slice) and walks
@@ -28,6 +34,80 @@ namespace kda {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr float kRefNats = 80.f;   // e^-80 and e^80 are inside the fp32 range
+constexpr float kMaxNats = 170.f;  // e^(+-85) are too
+
+// The per-channel references of a block of nb channels from its running
+// log-decay G ([64][ld], rows past the chunk carrying G_{L-1}): s[c], and
+// whether some channel is past kMaxNats (the direct form is then taken).
+// Every thread of the CTA calls it; the result is the same for all.
+__device__ __forceinline__ bool channel_refs(const float* G, int ld, int nb, float* sref) {
+  bool direct = false;
+  for (int c = threadIdx.x; c < nb; c += kThreads) {
+    const float gl = G[(kChunk - 1) * ld + c];
+    sref[c] = gl >= -kRefNats ? 0.f : rintf(0.5f * gl);
+    direct |= gl < -kMaxNats;
+  }
+  return __syncthreads_or(direct);
+}
+
+// In place over a block of nb channels: X (q^) <- Qp, Kb (k^) <- Kp and
+// G <- Kn, with the references sref.
+__device__ __forceinline__ void factor_block(float* X, float* Kb, float* G, int ld, int nb, const float* sref) {
+  for (int idx = threadIdx.x; idx < kChunk * nb; idx += kThreads) {
+    const int i = idx / nb, c = idx - i * nb;
+    const float e = G[i * ld + c] - sref[c];
+    const float ep = expf(e), en = expf(-e), k = Kb[i * ld + c];
+    X[i * ld + c] *= ep;
+    Kb[i * ld + c] = k * ep;
+    G[i * ld + c] = k * en;
+  }
+}
+
+// A[i][j] += beta_i (Kp Kn^T)[i][j] for j < i and AQ[i][j] += (Qp Kn^T)[i][j]
+// for j <= i, rows i < len, over nb channels; thread t takes rows
+// 4 (t / 16) .. +3 and columns 4 (t % 16) .. +3 (tiles above the diagonal
+// are zero and skipped).
+__device__ __forceinline__ void accumulate_products(const float* Qp, const float* Kp, const float* Kn, int ld,
+                                                    int nb, int len, const float* beta, float* A, float* AQ) {
+  const int I = threadIdx.x >> 4, J = threadIdx.x & 15;
+  if (J > I) return;
+  float akk[4][4], aqk[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) akk[r][t] = aqk[r][t] = 0.f;
+  const float* kp = Kp + 4 * I * ld;
+  const float* qp = Qp + 4 * I * ld;
+  const float* kn = Kn + 4 * J * ld;
+  for (int c = 0; c < nb; ++c) {
+    float a[4], q[4], b[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      a[r] = kp[r * ld + c];
+      q[r] = qp[r * ld + c];
+      b[r] = kn[r * ld + c];
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        akk[r][t] += a[r] * b[t];
+        aqk[r][t] += q[r] * b[t];
+      }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = 4 * I + r;
+    if (i >= len) continue;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int j = 4 * J + t;
+      if (j < i) A[i * kChunk + j] += beta[i] * akk[r][t];
+      if (j <= i) AQ[i * kChunk + j] += aqk[r][t];
+    }
+  }
+}
 
 // Tensor t (0 q, 1 k, 2 v; head size d) at token i of chunk ch, channel col,
 // after the short convolution when there is one:
@@ -78,6 +158,7 @@ simt_intra(ChunkParams p) {
   float* A = V + kChunk * dv;       // [64][64]
   float* Tm = A + kChunk * kChunk;  // [64][64]
   float* beta = Tm + kChunk * kChunk;  // [64]
+  float* sref = beta + kChunk;          // [dk] per-channel references
 
   const TIn* q = static_cast<const TIn*>(p.q);
   const TIn* k = static_cast<const TIn*>(p.k);
@@ -131,21 +212,41 @@ simt_intra(ChunkParams p) {
   __syncthreads();
 
   float* rec = p.inter + ((size_t)c * H + h) * p.rec_floats;
-  // A_kk (into A) and A_qk (into the record)
-  for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-    const int i = idx >> 6, j = idx & 63;
-    float akk = 0.f, aqk = 0.f;
-    if (j <= i && i < len) {
-      for (int col = 0; col < dk; ++col) {
-        const float d = expf(G[i * ld + col] - G[j * ld + col]);
-        const float kj = kh[j * ld + col] * d;
-        akk += kh[i * ld + col] * kj;
-        aqk += qh[i * ld + col] * kj;
+  // the record's Q^ o Gamma, K^ o Gamma_L / Gamma and Gamma_L, and
+  // K^ o Gamma (into EG) for W
+  const float* GLrow = G + (kChunk - 1) * ld;  // padded rows carry G_{L-1} forward
+  for (int idx = tid; idx < kChunk * dk; idx += kThreads) {
+    const int i = idx / dk, col = idx - i * dk;
+    const float eg = EG[i * ld + col], kv = kh[i * ld + col];
+    rec[SimtRec::qg(dk) + idx] = qh[i * ld + col] * eg;
+    rec[SimtRec::kr(dk) + idx] = kv * expf(GLrow[col] - G[i * ld + col]);
+    EG[i * ld + col] = kv * eg;
+  }
+  for (int col = tid; col < dk; col += kThreads) rec[SimtRec::gl(dk, dv) + col] = expf(GLrow[col]);
+  // A_kk (into A) and A_qk (into the record, by way of Tm)
+  if (!channel_refs(G, ld, dk, sref)) {
+    factor_block(qh, kh, G, ld, dk, sref);  // qh, kh, G <- Qp, Kp, Kn
+    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) A[idx] = Tm[idx] = 0.f;
+    __syncthreads();
+    accumulate_products(qh, kh, G, ld, dk, len, beta, A, Tm);
+    __syncthreads();
+    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) rec[SimtRec::aqk(dk) + idx] = Tm[idx];
+  } else {
+    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
+      const int i = idx >> 6, j = idx & 63;
+      float akk = 0.f, aqk = 0.f;
+      if (j <= i && i < len) {
+        for (int col = 0; col < dk; ++col) {
+          const float d = expf(G[i * ld + col] - G[j * ld + col]);
+          const float kj = kh[j * ld + col] * d;
+          akk += kh[i * ld + col] * kj;
+          aqk += qh[i * ld + col] * kj;
+        }
+        akk = j < i ? beta[i] * akk : 0.f;
       }
-      akk = j < i ? beta[i] * akk : 0.f;
+      A[idx] = akk;
+      rec[SimtRec::aqk(dk) + idx] = aqk;
     }
-    A[idx] = akk;
-    rec[SimtRec::aqk(dk) + idx] = aqk;
   }
   __syncthreads();
 
@@ -171,15 +272,12 @@ simt_intra(ChunkParams p) {
   for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) Tm[idx] *= beta[idx & 63];
   __syncthreads();
 
-  const float* GLrow = G + (kChunk - 1) * ld;  // padded rows carry G_{L-1} forward
+  // W = T diag(beta) (K^ o Gamma), K^ o Gamma held in EG
   for (int idx = tid; idx < kChunk * dk; idx += kThreads) {
     const int i = idx / dk, col = idx - i * dk;
     float w = 0.f;
-    for (int m = 0; m <= i; ++m)
-      w += Tm[i * kChunk + m] * kh[m * ld + col] * EG[m * ld + col];
+    for (int m = 0; m <= i; ++m) w += Tm[i * kChunk + m] * EG[m * ld + col];
     rec[SimtRec::w(dk) + idx] = w;
-    rec[SimtRec::qg(dk) + idx] = qh[i * ld + col] * EG[i * ld + col];
-    rec[SimtRec::kr(dk) + idx] = kh[i * ld + col] * expf(GLrow[col] - G[i * ld + col]);
   }
   for (int idx = tid; idx < kChunk * dv; idx += kThreads) {
     const int i = idx / dv, col = idx - i * dv;
@@ -187,7 +285,6 @@ simt_intra(ChunkParams p) {
     for (int m = 0; m <= i; ++m) u += Tm[i * kChunk + m] * V[m * dv + col];
     rec[SimtRec::ut(dk) + idx] = u;
   }
-  for (int col = tid; col < dk; col += kThreads) rec[SimtRec::gl(dk, dv) + col] = expf(GLrow[col]);
 }
 
 // Heads wider than 128 channels (dk or dv = 256): the same chunk algebra with
@@ -222,6 +319,7 @@ simt_intra_blocked(ChunkParams p) {
   float* beta = Tm + kChunk * kChunk;  // [64]
   float* invq = beta + kChunk;       // [64]
   float* invk = invq + kChunk;       // [64]
+  float* sref = invk + kChunk;       // [kCB] per-channel references of a block
 
   const TIn* q = static_cast<const TIn*>(p.q);
   const TIn* k = static_cast<const TIn*>(p.k);
@@ -275,10 +373,18 @@ simt_intra_blocked(ChunkParams p) {
     __syncthreads();
   };
 
-  // pass 2: A_kk and A_qk, summed over the key blocks
+  // pass 2: A_kk and A_qk, summed over the key blocks (each block takes the
+  // factored products, or the direct form if its decay is past the range)
   for (int c0 = 0; c0 < dk; c0 += kCB) {
     const int nb = dk - c0 < kCB ? dk - c0 : kCB;
     load_key_block(c0, nb);
+    if (!channel_refs(G, kLd, nb, sref)) {
+      factor_block(X, Kb, G, kLd, nb, sref);  // X, Kb, G <- Qp, Kp, Kn
+      __syncthreads();
+      accumulate_products(X, Kb, G, kLd, nb, len, beta, A, AQ);
+      __syncthreads();
+      continue;
+    }
     for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
       const int i = idx >> 6, j = idx & 63;
       if (j <= i && i < len) {
@@ -318,16 +424,23 @@ simt_intra_blocked(ChunkParams p) {
     const int nb = dk - c0 < kCB ? dk - c0 : kCB;
     load_key_block(c0, nb);
     const float* GL = G + (kChunk - 1) * kLd;
+    // Q^ o Gamma and K^ o Gamma_L / Gamma to the record, K^ o Gamma into X
+    for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
+      const int i = idx / nb, col = idx - i * nb;
+      const float eg = expf(G[i * kLd + col]), kv = Kb[i * kLd + col];
+      const size_t o = (size_t)i * dk + c0 + col;
+      rec[SimtRec::qg(dk) + o] = X[i * kLd + col] * eg;
+      rec[SimtRec::kr(dk) + o] = kv * expf(GL[col] - G[i * kLd + col]);
+      X[i * kLd + col] = kv * eg;
+    }
+    for (int col = tid; col < nb; col += kThreads) rec[SimtRec::gl(dk, dv) + c0 + col] = expf(GL[col]);
+    __syncthreads();
     for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
       const int i = idx / nb, col = idx - i * nb;
       float w = 0.f;
-      for (int m = 0; m <= i; ++m) w += Tm[i * kChunk + m] * Kb[m * kLd + col] * expf(G[m * kLd + col]);
-      const size_t o = (size_t)i * dk + c0 + col;
-      rec[SimtRec::w(dk) + o] = w;
-      rec[SimtRec::qg(dk) + o] = X[i * kLd + col] * expf(G[i * kLd + col]);
-      rec[SimtRec::kr(dk) + o] = Kb[i * kLd + col] * expf(GL[col] - G[i * kLd + col]);
+      for (int m = 0; m <= i; ++m) w += Tm[i * kChunk + m] * X[m * kLd + col];
+      rec[SimtRec::w(dk) + (size_t)i * dk + c0 + col] = w;
     }
-    for (int col = tid; col < nb; col += kThreads) rec[SimtRec::gl(dk, dv) + c0 + col] = expf(GL[col]);
     __syncthreads();
   }
   // U~ = T diag(beta) V per value block
@@ -511,8 +624,9 @@ cudaError_t launch_simt_t(const ChunkParams& p, cudaStream_t stream, cudaEvent_t
   // take the blocked kernel
   const bool blocked = p.dk > kCB || p.dv > kCB;
   const size_t smem_intra =
-      blocked ? sizeof(float) * (3 * (size_t)kChunk * (kCB + 1) + 3 * kChunk * kChunk + 3 * kChunk)
-              : sizeof(float) * (4 * (size_t)kChunk * (p.dk + 1) + (size_t)kChunk * p.dv + 2 * kChunk * kChunk + kChunk);
+      blocked ? sizeof(float) * (3 * (size_t)kChunk * (kCB + 1) + 3 * kChunk * kChunk + 3 * kChunk + kCB)
+              : sizeof(float) * (4 * (size_t)kChunk * (p.dk + 1) + (size_t)kChunk * p.dv + 2 * kChunk * kChunk + kChunk +
+                                 p.dk);
   auto intra = blocked ? simt_intra_blocked<TIn> : simt_intra<TIn>;
   cudaError_t e = cudaFuncSetAttribute(intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_intra);
   if (e != cudaSuccess) return e;

@@ -34,6 +34,19 @@ namespace kda {
 namespace {
 
 constexpr int kThreads = 256;
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned), and
+// its groups
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 constexpr float kRefNats = 80.f;   // e^-80 and e^80 are inside the fp32 range
 constexpr float kMaxNats = 170.f;  // e^(+-85) are too
 
@@ -62,6 +75,69 @@ __device__ __forceinline__ void factor_block(float* X, float* Kb, float* G, int 
     Kb[i * ld + c] = k * ep;
     G[i * ld + c] = k * en;
   }
+}
+
+// T = (I + A)^{-1} for strictly lower-triangular A (64 x 64, row-major),
+// by blocks (all 256 threads): the four 16 x 16 diagonal blocks by forward
+// substitution (a thread per column, 16 steps), then within each 32 x 32
+// half T10 = -T11 A10 T00, then T[32:64, 0:32] = -T_hi A T_lo, each product
+// as fp32 dot products.  X: scratch of 1024 floats.
+__device__ __noinline__ void simt_inverse(const float* __restrict__ A, float* __restrict__ T,
+                                          float* __restrict__ X) {
+  const int tid = threadIdx.x;
+  if (tid < kChunk) {
+    const int d = tid >> 4, jj = tid & 15, j = 16 * d + jj;
+    float col[16];
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) {
+      const float* ar = A + (16 * d + ii) * kChunk + 16 * d;
+      float acc = ii == jj ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < ii; ++m) acc -= ar[m] * col[m];
+      col[ii] = acc;
+    }
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) T[(16 * d + ii) * kChunk + j] = col[ii];
+  } else {
+    // the blocks above the diagonal are zero
+    for (int idx = tid - kChunk; idx < 6 * 256; idx += kThreads - kChunk) {
+      const int t = idx >> 8, e = idx & 255;
+      const int bi = t < 3 ? 0 : (t < 5 ? 1 : 2);
+      const int bj = t < 3 ? t + 1 : (t < 5 ? t - 1 : 3);
+      T[(16 * bi + (e >> 4)) * kChunk + 16 * bj + (e & 15)] = 0.f;
+    }
+  }
+  __syncthreads();
+  // level 1: half P = e / 256; X1 = A10 T00, then T10 = -T11 X1
+  for (int e = tid; e < 512; e += kThreads) {
+    const int P = e >> 8, r = (e >> 4) & 15, c = e & 15, r0 = 32 * P + 16, c0 = 32 * P;
+    float acc = 0.f;
+    for (int m = 0; m < 16; ++m) acc += A[(r0 + r) * kChunk + c0 + m] * T[(c0 + m) * kChunk + c0 + c];
+    X[e] = acc;
+  }
+  __syncthreads();
+  for (int e = tid; e < 512; e += kThreads) {
+    const int P = e >> 8, r = (e >> 4) & 15, c = e & 15, r0 = 32 * P + 16, c0 = 32 * P;
+    float acc = 0.f;
+    for (int m = 0; m <= r; ++m) acc += T[(r0 + r) * kChunk + r0 + m] * X[(P << 8) + (m << 4) + c];
+    T[(r0 + r) * kChunk + c0 + c] = -acc;
+  }
+  __syncthreads();
+  // level 2: X = A[32:64, 0:32] T[0:32, 0:32], then T[32:64, 0:32] = -T[32:64, 32:64] X
+  for (int e = tid; e < 1024; e += kThreads) {
+    const int r = e >> 5, c = e & 31;
+    float acc = 0.f;
+    for (int m = c & ~15; m < 32; ++m) acc += A[(32 + r) * kChunk + m] * T[m * kChunk + c];
+    X[e] = acc;
+  }
+  __syncthreads();
+  for (int e = tid; e < 1024; e += kThreads) {
+    const int r = e >> 5, c = e & 31;
+    float acc = 0.f;
+    for (int m = 0; m <= r; ++m) acc += T[(32 + r) * kChunk + 32 + m] * X[(m << 5) + c];
+    T[(32 + r) * kChunk + c] = -acc;
+  }
+  __syncthreads();
 }
 
 // A[i][j] += beta_i (Kp Kn^T)[i][j] for j < i and AQ[i][j] += (Qp Kn^T)[i][j]
@@ -166,6 +242,7 @@ simt_intra(ChunkParams p) {
   const TIn* g = static_cast<const TIn*>(p.g);
   const TIn* b = static_cast<const TIn*>(p.b);
 
+#pragma unroll 4
   for (int idx = tid; idx < kChunk * dk; idx += kThreads) {
     const int i = idx / dk, col = idx - i * dk;
     float xq = 0.f, xk = 0.f, la = 0.f;
@@ -179,6 +256,7 @@ simt_intra(ChunkParams p) {
     kh[i * ld + col] = xk;
     G[i * ld + col] = la;
   }
+#pragma unroll 4
   for (int idx = tid; idx < kChunk * dv; idx += kThreads) {
     const int i = idx / dv, col = idx - i * dv;
     V[idx] = i < len ? conv_input(p, 2, v, dv, ch, i, h, col) : 0.f;
@@ -250,24 +328,8 @@ simt_intra(ChunkParams p) {
   }
   __syncthreads();
 
-  // T = (I + A_kk)^{-1}, unit lower triangular: forward substitution, one
-  // thread per column
-  if (tid < kChunk) {
-    const int j = tid;
-    for (int i = 0; i < kChunk; ++i) {
-      float t;
-      if (i < j) {
-        t = 0.f;
-      } else if (i == j) {
-        t = 1.f;
-      } else {
-        t = 0.f;
-        for (int m = j; m < i; ++m) t -= A[i * kChunk + m] * Tm[m * kChunk + j];
-      }
-      Tm[i * kChunk + j] = t;
-    }
-  }
-  __syncthreads();
+  // T = (I + A_kk)^{-1}, unit lower triangular (q^ rows are free: scratch)
+  simt_inverse(A, Tm, qh);
   // fold beta into the columns: Tb = T diag(beta)
   for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) Tm[idx] *= beta[idx & 63];
   __syncthreads();
@@ -331,6 +393,7 @@ simt_intra_blocked(ChunkParams p) {
   for (int i = warp; i < kChunk; i += kThreads / 32) {
     float sq = 0.f, sk = 0.f;
     if (i < len)
+#pragma unroll 4
       for (int col = lane; col < dk; col += 32) {
         const float xq = conv_input(p, 0, q, dk, ch, i, h, col), xk = conv_input(p, 1, k, dk, ch, i, h, col);
         sq += xq * xq;
@@ -349,6 +412,7 @@ simt_intra_blocked(ChunkParams p) {
 
   // one key block [c0, c0 + nb) of q^, k^ and the running log-decay G
   auto load_key_block = [&](int c0, int nb) {
+#pragma unroll 4
     for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
       const int i = idx / nb, col = idx - i * nb;
       float xq = 0.f, xk = 0.f, la = 0.f;
@@ -404,18 +468,10 @@ simt_intra_blocked(ChunkParams p) {
   float* rec = p.inter + ((size_t)c * H + h) * p.rec_floats;
   for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) rec[SimtRec::aqk(dk) + idx] = AQ[idx];
 
-  // T = (I + A_kk)^{-1} by forward substitution (a thread per column), then
+  // T = (I + A_kk)^{-1} (A_qk is in the record: its tile is scratch), then
   // T diag(beta)
-  if (tid < kChunk) {
-    const int j = tid;
-    for (int i = 0; i < kChunk; ++i) {
-      float t = i == j ? 1.f : 0.f;
-      if (i > j)
-        for (int m = j; m < i; ++m) t -= A[i * kChunk + m] * Tm[m * kChunk + j];
-      Tm[i * kChunk + j] = t;
-    }
-  }
   __syncthreads();
+  simt_inverse(A, Tm, AQ);
   for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) Tm[idx] *= beta[idx & 63];
   __syncthreads();
 
@@ -446,6 +502,7 @@ simt_intra_blocked(ChunkParams p) {
   // U~ = T diag(beta) V per value block
   for (int v0 = 0; v0 < dv; v0 += kCB) {
     const int nb = dv - v0 < kCB ? dv - v0 : kCB;
+#pragma unroll 4
     for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
       const int i = idx / nb, col = idx - i * nb;
       X[i * kLd + col] = i < len ? conv_input(p, 2, v, dv, ch, i, h, v0 + col) : 0.f;
@@ -464,8 +521,9 @@ simt_intra_blocked(ChunkParams p) {
 // K3 on CUDA cores: one CTA per (sequence, head, NS-column slice of S),
 // walking the sequence's chunks with its slice of S in shared memory.  Per
 // chunk the record's W, Q^ o Gamma and K^ o Gamma_L / Gamma are staged in
-// shared memory one after another (16-byte loads, rows padded by 4 floats)
-// and each thread works on a register tile: token rows i0 .. i0 + RPT - 1 of
+// shared memory by asynchronous 16-byte copies, each one stage ahead of its
+// use, in two alternating buffers (rows padded by 4 floats), and each thread
+// works on a register tile: token rows i0 .. i0 + RPT - 1 of
 // a column pair for U = U~ - W S and O = scale ((Q^ o Gamma) S + A_qk U),
 // and key rows r0 .. r0 + SR - 1 of the same column pair for
 // S <- Diag(Gamma_L) S + KR^T U (written in place: each thread reads and
@@ -486,9 +544,9 @@ simt_inter(ChunkParams p) {
   const int xs = dk + 4;                  // padded row stride of the staged rows
   float* S = sm;                          // [dk][NS]
   float* U = S + dk * NS;                 // [64][NS]
-  float* X = U + kChunk * NS;             // [64][dk + 4]: W, then Q^ o Gamma, then KR
-  float* AQ = X + kChunk * xs;            // [64][64]
-  float* GLs = AQ + kChunk * kChunk;      // [dk]
+  float* Xb = U + kChunk * NS;            // two [64][dk + 4]: W / Q^ o Gamma / KR, in turn
+  float* AQb = Xb + 2 * kChunk * xs;      // two [64][64]: A_qk
+  float* GLb = AQb + 2 * kChunk * kChunk; // two [dk]: Gamma_L
   const int cp = tid % NCP, rg = tid / NCP;
   const int c0 = 2 * cp, i0 = rg * RPT;
   const int SR = (dk + RG - 1) / RG, r0 = rg * SR;
@@ -498,16 +556,30 @@ simt_inter(ChunkParams p) {
     const int r = idx / NS, n = idx - r * NS;
     S[idx] = p.initial_state ? p.initial_state[sbase + (size_t)r * dv + n0 + n] : 0.f;
   }
-  auto stage_rows = [&](const float* src) {
+  // The record's rows go to shared memory by asynchronous 16-byte copies,
+  // one stage ahead: W (with A_qk and Gamma_L) of chunk c+1 while chunk c
+  // forms O, Q^ o Gamma while it forms U, KR while it forms O.  The two row
+  // buffers alternate: chunk c's W and KR in buffer c % 2, its Q^ o Gamma
+  // and the next chunk's W in the other.
+  auto rec_of = [&](int64_t c) { return p.inter + ((size_t)c * H + h) * p.rec_floats; };
+  auto issue_rows = [&](float* dst, const float* src) {
     const int q4 = dk / 4;
     for (int idx = tid; idx < kChunk * q4; idx += kThreads) {
       const int i = idx / q4, c4 = idx - i * q4;
-      *reinterpret_cast<float4*>(X + i * xs + 4 * c4) =
-          *reinterpret_cast<const float4*>(src + (size_t)i * dk + 4 * c4);
+      cp_async16(dst + i * xs + 4 * c4, src + (size_t)i * dk + 4 * c4);
     }
   };
+  auto issue_w = [&](int64_t c, int buf) {
+    const float* rec = rec_of(c);
+    issue_rows(Xb + buf * kChunk * xs, rec + SimtRec::w(dk));
+    for (int idx = tid; idx < kChunk * kChunk / 4; idx += kThreads)
+      cp_async16(AQb + buf * kChunk * kChunk + 4 * idx, rec + SimtRec::aqk(dk) + 4 * idx);
+    for (int idx = tid; idx < dk / 4; idx += kThreads)
+      cp_async16(GLb + buf * dk + 4 * idx, rec + SimtRec::gl(dk, dv) + 4 * idx);
+    cp_async_commit();
+  };
   // acc[ii] += X[i0 + ii] . S[:, c0 .. c0 + 1]
-  auto rows_times_state = [&](float (*acc)[2]) {
+  auto rows_times_state = [&](const float* X, float (*acc)[2]) {
     for (int r = 0; r < dk; ++r) {
       const float2 sv = *reinterpret_cast<const float2*>(S + r * NS + c0);
 #pragma unroll
@@ -520,35 +592,43 @@ simt_inter(ChunkParams p) {
   };
   TIn* o = static_cast<TIn*>(p.o);
   const TIn* og = static_cast<const TIn*>(p.out_gate);
+  if (c_end > c_begin) issue_w(c_begin, 0);
   for (int64_t c = c_begin; c < c_end; ++c) {
+    const int par = (int)((c - c_begin) & 1);
+    float* Xw = Xb + par * kChunk * xs;        // W, then KR
+    float* Xq = Xb + (1 - par) * kChunk * xs;  // Q^ o Gamma, then the next W
+    const float* AQ = AQb + par * kChunk * kChunk;
+    const float* GLs = GLb + par * dk;
     const Chunk ch = p.chunks[c];
-    const float* rec = p.inter + ((size_t)c * H + h) * p.rec_floats;
-    const float* UT = rec + SimtRec::ut(dk);
-    // W, A_qk and Gamma_L in; S is complete (previous chunk's update)
-    stage_rows(rec + SimtRec::w(dk));
-    for (int idx = tid; idx < kChunk * kChunk / 4; idx += kThreads)
-      reinterpret_cast<float4*>(AQ)[idx] = reinterpret_cast<const float4*>(rec + SimtRec::aqk(dk))[idx];
-    for (int r = tid; r < dk; r += kThreads) GLs[r] = rec[SimtRec::gl(dk, dv) + r];
+    const float* rec = rec_of(c);
+    issue_rows(Xq, rec + SimtRec::qg(dk));
+    cp_async_commit();
+    float2 ut[RPT];
+#pragma unroll
+    for (int ii = 0; ii < RPT; ++ii)
+      ut[ii] = *reinterpret_cast<const float2*>(rec + SimtRec::ut(dk) + (size_t)(i0 + ii) * dv + n0 + c0);
+    cp_async_wait<1>();  // W, A_qk, Gamma_L
     __syncthreads();
     // U = U~ - W S
     {
       float a[RPT][2] = {};
-      rows_times_state(a);
+      rows_times_state(Xw, a);
 #pragma unroll
       for (int ii = 0; ii < RPT; ++ii) {
         const int i = i0 + ii;
-        const float2 ut = *reinterpret_cast<const float2*>(UT + (size_t)i * dv + n0 + c0);
-        U[i * NS + c0] = ut.x - a[ii][0];
-        U[i * NS + c0 + 1] = ut.y - a[ii][1];
+        U[i * NS + c0] = ut[ii].x - a[ii][0];
+        U[i * NS + c0 + 1] = ut[ii].y - a[ii][1];
       }
     }
     __syncthreads();  // U complete, W read
-    stage_rows(rec + SimtRec::qg(dk));
+    issue_rows(Xw, rec + SimtRec::kr(dk));
+    cp_async_commit();
+    cp_async_wait<1>();  // Q^ o Gamma
     __syncthreads();
     // O = scale ((Q^ o Gamma) S + A_qk U), A_qk masked j <= i
     {
       float a[RPT][2] = {};
-      rows_times_state(a);
+      rows_times_state(Xq, a);
 #pragma unroll
       for (int ii = 0; ii < RPT; ++ii) {
         const int i = i0 + ii;
@@ -570,7 +650,12 @@ simt_inter(ChunkParams p) {
       }
     }
     __syncthreads();  // Q^ o Gamma and S read
-    stage_rows(rec + SimtRec::kr(dk));
+    if (c + 1 < c_end) {
+      issue_w(c + 1, 1 - par);
+      cp_async_wait<1>();  // KR
+    } else {
+      cp_async_wait<0>();
+    }
     __syncthreads();
     // S <- Diag(Gamma_L) S + KR^T U on this thread's key rows
     {
@@ -584,7 +669,7 @@ simt_inter(ChunkParams p) {
       }
       for (int i = 0; i < kChunk; ++i) {
         const float2 u = *reinterpret_cast<const float2*>(U + i * NS + c0);
-        const float* xr = X + i * xs + r0;
+        const float* xr = Xw + i * xs + r0;
 #pragma unroll
         for (int rr = 0; rr < kMaxSR; ++rr)
           if (rr < SR && r0 + rr < dk) {
@@ -642,7 +727,7 @@ cudaError_t launch_simt_t(const ChunkParams& p, cudaStream_t stream, cudaEvent_t
   }
   const int ns = p.dv < 32 ? p.dv : 32;  // 16 or 32 value columns per CTA
   const size_t smem_inter = sizeof(float) * ((size_t)p.dk * ns + (size_t)kChunk * ns +
-                                             (size_t)kChunk * (p.dk + 4) + kChunk * kChunk + p.dk);
+                                             2 * (size_t)kChunk * (p.dk + 4) + 2 * kChunk * kChunk + 2 * (size_t)p.dk);
   auto inter = ns == 32 ? simt_inter<TIn, 32> : simt_inter<TIn, 16>;
   e = cudaFuncSetAttribute(inter, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_inter);
   if (e != cudaSuccess) return e;

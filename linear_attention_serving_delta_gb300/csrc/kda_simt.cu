@@ -212,6 +212,34 @@ __device__ float conv_input(const ChunkParams& p, int t, const TIn* x, int d, co
   return round_in<TIn>(acc);
 }
 
+// 8 consecutive elements x[e .. e+7] as floats, one 16-byte load (bf16) or
+// two (fp32); e a multiple of 8, x 16-byte aligned
+__device__ __forceinline__ void ld8(const __nv_bfloat16* x, int64_t e, float* out) {
+  const uint4 u = *reinterpret_cast<const uint4*>(x + e);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    out[2 * t] = __uint_as_float(w[t] << 16);
+    out[2 * t + 1] = __uint_as_float(w[t] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void ld8(const float* x, int64_t e, float* out) {
+  const float4 a = *reinterpret_cast<const float4*>(x + e), b = *reinterpret_cast<const float4*>(x + e + 4);
+  out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+  out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+}
+__device__ __forceinline__ bool aligned16_dev(const void* x) {
+  return (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+}
+// The rows of q, k, v, g can be read 8 channels at a time: no convolution
+// (it reads other rows), 16-byte aligned tensors (head sizes are multiples
+// of 8)
+template <typename TIn>
+__device__ __forceinline__ bool vector_rows(const ChunkParams& p) {
+  return p.conv_width == 0 && aligned16_dev(p.q) && aligned16_dev(p.k) && aligned16_dev(p.v) &&
+         (p.gate_per_head || aligned16_dev(p.g));
+}
+
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads)
 simt_intra(ChunkParams p) {
@@ -242,24 +270,70 @@ simt_intra(ChunkParams p) {
   const TIn* g = static_cast<const TIn*>(p.g);
   const TIn* b = static_cast<const TIn*>(p.b);
 
-#pragma unroll 4
-  for (int idx = tid; idx < kChunk * dk; idx += kThreads) {
-    const int i = idx / dk, col = idx - i * dk;
-    float xq = 0.f, xk = 0.f, la = 0.f;
-    if (i < len) {
-      const int64_t e = ((ch.tok0 + i) * H + h) * dk + col;
-      xq = conv_input(p, 0, q, dk, ch, i, h, col);
-      xk = conv_input(p, 1, k, dk, ch, i, h, col);
-      la = log_alpha_of(ld_in(g, p.gate_per_head ? (ch.tok0 + i) * H + h : e));
+  if (vector_rows<TIn>(p)) {
+    // 8 channels a thread and load
+    const int dk8 = dk / 8, dv8 = dv / 8;
+#pragma unroll 2
+    for (int idx = tid; idx < kChunk * dk8; idx += kThreads) {
+      const int i = idx / dk8, c0 = 8 * (idx - i * dk8);
+      float xq[8], xk[8], la[8];
+      if (i < len) {
+        const int64_t e = ((ch.tok0 + i) * H + h) * dk + c0;
+        ld8(q, e, xq);
+        ld8(k, e, xk);
+        if (p.gate_per_head) {
+          const float l = log_alpha_of(ld_in(g, (ch.tok0 + i) * H + h));
+#pragma unroll
+          for (int t = 0; t < 8; ++t) la[t] = l;
+        } else {
+          ld8(g, e, la);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) la[t] = log_alpha_of(la[t]);
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) xq[t] = xk[t] = la[t] = 0.f;
+      }
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        qh[i * ld + c0 + t] = xq[t];
+        kh[i * ld + c0 + t] = xk[t];
+        G[i * ld + c0 + t] = la[t];
+      }
     }
-    qh[i * ld + col] = xq;
-    kh[i * ld + col] = xk;
-    G[i * ld + col] = la;
-  }
+#pragma unroll 2
+    for (int idx = tid; idx < kChunk * dv8; idx += kThreads) {
+      const int i = idx / dv8, c0 = 8 * (idx - i * dv8);
+      float xv[8];
+      if (i < len) {
+        ld8(v, ((ch.tok0 + i) * H + h) * dv + c0, xv);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) xv[t] = 0.f;
+      }
+#pragma unroll
+      for (int t = 0; t < 8; ++t) V[i * dv + c0 + t] = xv[t];
+    }
+  } else {
 #pragma unroll 4
-  for (int idx = tid; idx < kChunk * dv; idx += kThreads) {
-    const int i = idx / dv, col = idx - i * dv;
-    V[idx] = i < len ? conv_input(p, 2, v, dv, ch, i, h, col) : 0.f;
+    for (int idx = tid; idx < kChunk * dk; idx += kThreads) {
+      const int i = idx / dk, col = idx - i * dk;
+      float xq = 0.f, xk = 0.f, la = 0.f;
+      if (i < len) {
+        const int64_t e = ((ch.tok0 + i) * H + h) * dk + col;
+        xq = conv_input(p, 0, q, dk, ch, i, h, col);
+        xk = conv_input(p, 1, k, dk, ch, i, h, col);
+        la = log_alpha_of(ld_in(g, p.gate_per_head ? (ch.tok0 + i) * H + h : e));
+      }
+      qh[i * ld + col] = xq;
+      kh[i * ld + col] = xk;
+      G[i * ld + col] = la;
+    }
+#pragma unroll 4
+    for (int idx = tid; idx < kChunk * dv; idx += kThreads) {
+      const int i = idx / dv, col = idx - i * dv;
+      V[idx] = i < len ? conv_input(p, 2, v, dv, ch, i, h, col) : 0.f;
+    }
   }
   if (tid < kChunk) beta[tid] = tid < len ? beta_of(ld_in(b, (ch.tok0 + tid) * H + h)) : 0.f;
   __syncthreads();
@@ -390,9 +464,22 @@ simt_intra_blocked(ChunkParams p) {
   const TIn* b = static_cast<const TIn*>(p.b);
 
   // pass 1: inverse norms of the (convolved) q and k rows, one warp per token
+  const bool vec = vector_rows<TIn>(p);
   for (int i = warp; i < kChunk; i += kThreads / 32) {
     float sq = 0.f, sk = 0.f;
-    if (i < len)
+    if (i < len && vec) {
+      for (int c0 = 8 * lane; c0 < dk; c0 += 256) {
+        float xq[8], xk[8];
+        const int64_t e = ((ch.tok0 + i) * H + h) * dk + c0;
+        ld8(q, e, xq);
+        ld8(k, e, xk);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          sq += xq[t] * xq[t];
+          sk += xk[t] * xk[t];
+        }
+      }
+    } else if (i < len)
 #pragma unroll 4
       for (int col = lane; col < dk; col += 32) {
         const float xq = conv_input(p, 0, q, dk, ch, i, h, col), xk = conv_input(p, 1, k, dk, ch, i, h, col);
@@ -412,19 +499,52 @@ simt_intra_blocked(ChunkParams p) {
 
   // one key block [c0, c0 + nb) of q^, k^ and the running log-decay G
   auto load_key_block = [&](int c0, int nb) {
-#pragma unroll 4
-    for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
-      const int i = idx / nb, col = idx - i * nb;
-      float xq = 0.f, xk = 0.f, la = 0.f;
-      if (i < len) {
-        xq = conv_input(p, 0, q, dk, ch, i, h, c0 + col) * invq[i];
-        xk = conv_input(p, 1, k, dk, ch, i, h, c0 + col) * invk[i];
-        const int64_t e = ((ch.tok0 + i) * H + h) * dk + c0 + col;
-        la = log_alpha_of(ld_in(g, p.gate_per_head ? (ch.tok0 + i) * H + h : e));
+    if (vec) {
+      const int nb8 = nb / 8;
+#pragma unroll 2
+      for (int idx = tid; idx < kChunk * nb8; idx += kThreads) {
+        const int i = idx / nb8, cc = 8 * (idx - i * nb8);
+        float xq[8], xk[8], la[8];
+        if (i < len) {
+          const int64_t e = ((ch.tok0 + i) * H + h) * dk + c0 + cc;
+          ld8(q, e, xq);
+          ld8(k, e, xk);
+          if (p.gate_per_head) {
+            const float l = log_alpha_of(ld_in(g, (ch.tok0 + i) * H + h));
+#pragma unroll
+            for (int t = 0; t < 8; ++t) la[t] = l;
+          } else {
+            ld8(g, e, la);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) la[t] = log_alpha_of(la[t]);
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) xq[t] = xk[t] = la[t] = 0.f;
+        }
+        const float iq = i < len ? invq[i] : 0.f, ik = i < len ? invk[i] : 0.f;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          X[i * kLd + cc + t] = xq[t] * iq;
+          Kb[i * kLd + cc + t] = xk[t] * ik;
+          G[i * kLd + cc + t] = la[t];
+        }
       }
-      X[i * kLd + col] = xq;
-      Kb[i * kLd + col] = xk;
-      G[i * kLd + col] = la;
+    } else {
+#pragma unroll 4
+      for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
+        const int i = idx / nb, col = idx - i * nb;
+        float xq = 0.f, xk = 0.f, la = 0.f;
+        if (i < len) {
+          xq = conv_input(p, 0, q, dk, ch, i, h, c0 + col) * invq[i];
+          xk = conv_input(p, 1, k, dk, ch, i, h, c0 + col) * invk[i];
+          const int64_t e = ((ch.tok0 + i) * H + h) * dk + c0 + col;
+          la = log_alpha_of(ld_in(g, p.gate_per_head ? (ch.tok0 + i) * H + h : e));
+        }
+        X[i * kLd + col] = xq;
+        Kb[i * kLd + col] = xk;
+        G[i * kLd + col] = la;
+      }
     }
     __syncthreads();
     for (int col = tid; col < nb; col += kThreads) {  // rows past len carry G_{L-1}
@@ -502,10 +622,27 @@ simt_intra_blocked(ChunkParams p) {
   // U~ = T diag(beta) V per value block
   for (int v0 = 0; v0 < dv; v0 += kCB) {
     const int nb = dv - v0 < kCB ? dv - v0 : kCB;
+    if (vec) {
+      const int nb8 = nb / 8;
+#pragma unroll 2
+      for (int idx = tid; idx < kChunk * nb8; idx += kThreads) {
+        const int i = idx / nb8, cc = 8 * (idx - i * nb8);
+        float xv[8];
+        if (i < len) {
+          ld8(v, ((ch.tok0 + i) * H + h) * dv + v0 + cc, xv);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) xv[t] = 0.f;
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) X[i * kLd + cc + t] = xv[t];
+      }
+    } else {
 #pragma unroll 4
-    for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
-      const int i = idx / nb, col = idx - i * nb;
-      X[i * kLd + col] = i < len ? conv_input(p, 2, v, dv, ch, i, h, v0 + col) : 0.f;
+      for (int idx = tid; idx < kChunk * nb; idx += kThreads) {
+        const int i = idx / nb, col = idx - i * nb;
+        X[i * kLd + col] = i < len ? conv_input(p, 2, v, dv, ch, i, h, v0 + col) : 0.f;
+      }
     }
     __syncthreads();
     for (int idx = tid; idx < kChunk * nb; idx += kThreads) {

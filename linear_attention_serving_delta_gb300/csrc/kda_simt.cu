@@ -669,10 +669,8 @@ template <typename TIn, int NS>
 __global__ void __launch_bounds__(kThreads)
 simt_inter(ChunkParams p) {
   extern __shared__ float sm[];
-  constexpr int NCP = NS / 2;         // column pairs
-  constexpr int RG = kThreads / NCP;  // row groups
-  constexpr int RPT = kChunk / RG;    // token rows per thread
-  constexpr int kMaxSR = 16;          // key rows per thread (dk <= 256)
+  constexpr int NO = NS / 8;          // column octets
+  constexpr int kMaxRB = 4;           // key rows per thread (dk <= 256)
   const int s = blockIdx.x, h = blockIdx.y, n0 = blockIdx.z * NS;
   const int H = p.H, dk = p.dk, dv = p.dv, tid = threadIdx.x;
   const int64_t c_begin = p.seq_chunk_begin[s], c_end = p.seq_chunk_begin[s + 1];
@@ -684,9 +682,14 @@ simt_inter(ChunkParams p) {
   float* Xb = U + kChunk * NS;            // two [64][dk + 4]: W / Q^ o Gamma / KR, in turn
   float* AQb = Xb + 2 * kChunk * xs;      // two [64][64]: A_qk
   float* GLb = AQb + 2 * kChunk * kChunk; // two [dk]: Gamma_L
-  const int cp = tid % NCP, rg = tid / NCP;
-  const int c0 = 2 * cp, i0 = rg * RPT;
-  const int SR = (dk + RG - 1) / RG, r0 = rg * SR;
+  // U and O: token row ti, columns c0 .. c0 + 7 (threads past 64 NO idle);
+  // the state update: key rows r0 .. r0 + RB - 1, the same columns
+  const int cg = tid % NO, c0 = 8 * cg;
+  const int ti = tid / NO;
+  const bool row_thread = ti < kChunk;
+  const int RB = dk * NO >= kThreads ? dk * NO / kThreads : 1;
+  const int r0 = (tid / NO) * RB;
+  const bool key_thread = r0 < dk;
 
   const size_t sbase = ((size_t)s * H + h) * dk * dv;
   for (int idx = tid; idx < dk * NS; idx += kThreads) {
@@ -715,16 +718,15 @@ simt_inter(ChunkParams p) {
       cp_async16(GLb + buf * dk + 4 * idx, rec + SimtRec::gl(dk, dv) + 4 * idx);
     cp_async_commit();
   };
-  // acc[ii] += X[i0 + ii] . S[:, c0 .. c0 + 1]
-  auto rows_times_state = [&](const float* X, float (*acc)[2]) {
+  // acc[t] += X[ti] . S[:, c0 + t]
+  auto row_times_state = [&](const float* X, float* acc) {
+    const float* xr = X + ti * xs;
     for (int r = 0; r < dk; ++r) {
-      const float2 sv = *reinterpret_cast<const float2*>(S + r * NS + c0);
-#pragma unroll
-      for (int ii = 0; ii < RPT; ++ii) {
-        const float x = X[(i0 + ii) * xs + r];
-        acc[ii][0] += x * sv.x;
-        acc[ii][1] += x * sv.y;
-      }
+      const float4 sa = *reinterpret_cast<const float4*>(S + r * NS + c0);
+      const float4 sb = *reinterpret_cast<const float4*>(S + r * NS + c0 + 4);
+      const float x = xr[r];
+      acc[0] += x * sa.x; acc[1] += x * sa.y; acc[2] += x * sa.z; acc[3] += x * sa.w;
+      acc[4] += x * sb.x; acc[5] += x * sb.y; acc[6] += x * sb.z; acc[7] += x * sb.w;
     }
   };
   TIn* o = static_cast<TIn*>(p.o);
@@ -740,22 +742,22 @@ simt_inter(ChunkParams p) {
     const float* rec = rec_of(c);
     issue_rows(Xq, rec + SimtRec::qg(dk));
     cp_async_commit();
-    float2 ut[RPT];
-#pragma unroll
-    for (int ii = 0; ii < RPT; ++ii)
-      ut[ii] = *reinterpret_cast<const float2*>(rec + SimtRec::ut(dk) + (size_t)(i0 + ii) * dv + n0 + c0);
+    float4 uta = make_float4(0.f, 0.f, 0.f, 0.f), utb = uta;
+    if (row_thread) {
+      const float* ut = rec + SimtRec::ut(dk) + (size_t)ti * dv + n0 + c0;
+      uta = *reinterpret_cast<const float4*>(ut);
+      utb = *reinterpret_cast<const float4*>(ut + 4);
+    }
     cp_async_wait<1>();  // W, A_qk, Gamma_L
     __syncthreads();
     // U = U~ - W S
-    {
-      float a[RPT][2] = {};
-      rows_times_state(Xw, a);
-#pragma unroll
-      for (int ii = 0; ii < RPT; ++ii) {
-        const int i = i0 + ii;
-        U[i * NS + c0] = ut[ii].x - a[ii][0];
-        U[i * NS + c0 + 1] = ut[ii].y - a[ii][1];
-      }
+    if (row_thread) {
+      float a[8] = {};
+      row_times_state(Xw, a);
+      *reinterpret_cast<float4*>(U + ti * NS + c0) =
+          make_float4(uta.x - a[0], uta.y - a[1], uta.z - a[2], uta.w - a[3]);
+      *reinterpret_cast<float4*>(U + ti * NS + c0 + 4) =
+          make_float4(utb.x - a[4], utb.y - a[5], utb.z - a[6], utb.w - a[7]);
     }
     __syncthreads();  // U complete, W read
     issue_rows(Xw, rec + SimtRec::kr(dk));
@@ -763,26 +765,24 @@ simt_inter(ChunkParams p) {
     cp_async_wait<1>();  // Q^ o Gamma
     __syncthreads();
     // O = scale ((Q^ o Gamma) S + A_qk U), A_qk masked j <= i
-    {
-      float a[RPT][2] = {};
-      rows_times_state(Xq, a);
+    if (row_thread) {
+      float a[8] = {};
+      row_times_state(Xq, a);
+      const int i = ti;
+      for (int j = 0; j <= i; ++j) {
+        const float aq = AQ[i * kChunk + j];
+        const float4 ua = *reinterpret_cast<const float4*>(U + j * NS + c0);
+        const float4 ub = *reinterpret_cast<const float4*>(U + j * NS + c0 + 4);
+        a[0] += aq * ua.x; a[1] += aq * ua.y; a[2] += aq * ua.z; a[3] += aq * ua.w;
+        a[4] += aq * ub.x; a[5] += aq * ub.y; a[6] += aq * ub.z; a[7] += aq * ub.w;
+      }
+      if (i < ch.len) {
 #pragma unroll
-      for (int ii = 0; ii < RPT; ++ii) {
-        const int i = i0 + ii;
-        for (int j = 0; j <= i; ++j) {
-          const float aq = AQ[i * kChunk + j];
-          const float2 u = *reinterpret_cast<const float2*>(U + j * NS + c0);
-          a[ii][0] += aq * u.x;
-          a[ii][1] += aq * u.y;
-        }
-        if (i < ch.len) {
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int64_t oi = ((ch.tok0 + i) * H + h) * dv + n0 + c0 + t;
-            float val = p.scale * a[ii][t];
-            if (og) val *= out_gate_of(ld_in(og, p.out_gate_per_head ? (ch.tok0 + i) * H + h : oi));
-            st_out(o, oi, val);
-          }
+        for (int t = 0; t < 8; ++t) {
+          const int64_t oi = ((ch.tok0 + i) * H + h) * dv + n0 + c0 + t;
+          float val = p.scale * a[t];
+          if (og) val *= out_gate_of(ld_in(og, p.out_gate_per_head ? (ch.tok0 + i) * H + h : oi));
+          st_out(o, oi, val);
         }
       }
     }
@@ -795,31 +795,38 @@ simt_inter(ChunkParams p) {
     }
     __syncthreads();
     // S <- Diag(Gamma_L) S + KR^T U on this thread's key rows
-    {
-      float b[kMaxSR][2];
+    if (key_thread) {
+      float b[kMaxRB][8];
 #pragma unroll
-      for (int rr = 0; rr < kMaxSR; ++rr) {
+      for (int rr = 0; rr < kMaxRB; ++rr) {
         const int r = r0 + rr;
-        const bool live = rr < SR && r < dk;
-        b[rr][0] = live ? GLs[r] * S[r * NS + c0] : 0.f;
-        b[rr][1] = live ? GLs[r] * S[r * NS + c0 + 1] : 0.f;
+        const bool live = rr < RB;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) b[rr][t] = live ? GLs[r] * S[r * NS + c0 + t] : 0.f;
       }
       for (int i = 0; i < kChunk; ++i) {
-        const float2 u = *reinterpret_cast<const float2*>(U + i * NS + c0);
-        const float* xr = Xw + i * xs + r0;
+        const float4 ua = *reinterpret_cast<const float4*>(U + i * NS + c0);
+        const float4 ub = *reinterpret_cast<const float4*>(U + i * NS + c0 + 4);
+        const float u[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+        float x[kMaxRB];
+        if (RB == 4) {
+          const float4 xv = *reinterpret_cast<const float4*>(Xw + i * xs + r0);
+          x[0] = xv.x; x[1] = xv.y; x[2] = xv.z; x[3] = xv.w;
+        } else {
 #pragma unroll
-        for (int rr = 0; rr < kMaxSR; ++rr)
-          if (rr < SR && r0 + rr < dk) {
-            const float x = xr[rr];
-            b[rr][0] += x * u.x;
-            b[rr][1] += x * u.y;
-          }
+          for (int rr = 0; rr < kMaxRB; ++rr) x[rr] = rr < RB ? Xw[i * xs + r0 + rr] : 0.f;
+        }
+#pragma unroll
+        for (int rr = 0; rr < kMaxRB; ++rr)
+#pragma unroll
+          for (int t = 0; t < 8; ++t) b[rr][t] += x[rr] * u[t];
       }
 #pragma unroll
-      for (int rr = 0; rr < kMaxSR; ++rr)
-        if (rr < SR && r0 + rr < dk) {
-          S[(r0 + rr) * NS + c0] = b[rr][0];
-          S[(r0 + rr) * NS + c0 + 1] = b[rr][1];
+      for (int rr = 0; rr < kMaxRB; ++rr)
+        if (rr < RB) {
+          *reinterpret_cast<float4*>(S + (r0 + rr) * NS + c0) = make_float4(b[rr][0], b[rr][1], b[rr][2], b[rr][3]);
+          *reinterpret_cast<float4*>(S + (r0 + rr) * NS + c0 + 4) =
+              make_float4(b[rr][4], b[rr][5], b[rr][6], b[rr][7]);
         }
     }
     __syncthreads();

@@ -203,13 +203,15 @@ __device__ __forceinline__ GateRow load_gate_row(const ChunkParams& p, const Chu
 
 // o rows of one chunk from lanes 64-127 of an output accumulator: row i, this
 // thread's 16 columns (none in the first pass of the segment scan), times
-// the output gate's factors gf when there is a gate
+// the output gate's factors gf when there is a gate.  The TMEM read is
+// warp-collective: every lane takes it; only lanes whose waits succeeded
+// (`live`) store.
 template <int NS>
 __device__ __forceinline__ void store_output(const ChunkParams& p, const Chunk& ch, uint32_t d1,
-                                             int h16, int i, int h, int n0, const GateF& gf) {
+                                             int h16, int i, int h, int n0, const GateF& gf, bool live) {
   float d[kNh];
   tmem_ld_sum<NS>(d1, h16, d);
-  if (i < ch.len && p.k3_mode != kScanPass1) {
+  if (live && i < ch.len && p.k3_mode != kScanPass1) {
     const float scale = p.scale;
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o);
     const int64_t row = (ch.tok0 + i) * p.H + h;
@@ -489,7 +491,7 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
       if (it >= 2) {
         okl = okl && wait_mma3(it - 2);
         fence_after_sync();
-        if (okl) store_output<NS>(p, prev2, d1_of(it - 2) + lane_off, h16, c - 64, h, n0, gfac);
+        store_output<NS>(p, prev2, d1_of(it - 2) + lane_off, h16, c - 64, h, n0, gfac, okl);
         // ... its A_qk tile takes chunk it+1 (with two tiles, chunk it, whose
         // slot held chunk it-2's) ...
         constexpr int kAqLead = C::kAqSlots - 2;
@@ -611,12 +613,12 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
       if (nchunks >= 2) {
         okl = okl && wait_mma3(nchunks - 2);
         fence_after_sync();
-        if (okl) store_output<NS>(p, prev2, d1_of(nchunks - 2) + lane_off, h16, c - 64, h, n0, gfac);
+        store_output<NS>(p, prev2, d1_of(nchunks - 2) + lane_off, h16, c - 64, h, n0, gfac, okl);
       }
       if (p.out_gate) gfac = gate_factors(p, graw);  // chunk n-1's row
       okl = okl && wait_mma3(nchunks - 1);
       fence_after_sync();
-      if (okl) store_output<NS>(p, prev1, d1_of(nchunks - 1) + lane_off, h16, c - 64, h, n0, gfac);
+      store_output<NS>(p, prev1, d1_of(nchunks - 1) + lane_off, h16, c - 64, h, n0, gfac, okl);
     }
   }
   fence_before_sync();

@@ -166,11 +166,41 @@ def flush_l2(buf):
 
 
 def bench_prefill(torch, kda, W, steps, warmup, dev):
+    """prefill_8k.  The step: the library's own choice of schedule (the
+    overlapped kernels for this one sequence), timed with events around the
+    call only, so that nothing sits between its launches.  Then the same
+    call on the separate kernels with the phase events between them: the
+    per-kernel times of the intra-chunk and inter-chunk kernels.  L2 flushed
+    before every call."""
     w = W.WORKLOADS[PREFILL_WL]
     inp = W.prefill_inputs(w, device=dev, gen_device=dev)
     T = sum(inp["lens"])
-    p = kda.Prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["b"], inp["cu_seqlens"],
-                    host_cu_seqlens=inp["cu_seqlens"].cpu())
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > L2 (129 MB)
+
+    def make(schedule):
+        return kda.Prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["b"], inp["cu_seqlens"],
+                           host_cu_seqlens=inp["cu_seqlens"].cpu(), schedule=schedule)
+
+    p = make(kda.SCHEDULE_AUTO)
+    path = kda.kda_prefill_schedule(p.args)
+    for _ in range(warmup):
+        flush_l2(flush)
+        p.run()
+    torch.cuda.synchronize()
+    step_ms = []
+    for _ in range(steps):
+        flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        p.run(stream)
+        e1.record(stream)
+        e1.synchronize()
+        step_ms.append(e0.elapsed_time(e1))
+    torch.cuda.synchronize()
+    assert p.device_status() == 0
+
+    sep = make(kda.SCHEDULE_SEPARATE)
     nph = kda.PREFILL_PHASES
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)]
     for e in ev:  # torch creates the cudaEvent_t on first record
@@ -178,27 +208,25 @@ def bench_prefill(torch, kda, W, steps, warmup, dev):
     torch.cuda.synchronize()
     assert all(e.cuda_event for e in ev)
     ev_handles = (kda.c_vp * (nph + 1))(*[e.cuda_event for e in ev])
-    stream = torch.cuda.current_stream()
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > L2 (129 MB)
-    for _ in range(warmup):
+    for _ in range(3):
         flush_l2(flush)
-        p.run()
+        sep.run()
     torch.cuda.synchronize()
-    p.args.phase_events = kda.ctypes.cast(ev_handles, kda.c_vp)
-    step_ms, phase_ms = [], [[] for _ in range(nph)]
+    sep.args.phase_events = kda.ctypes.cast(ev_handles, kda.c_vp)
+    sep_ms, phase_ms = [], [[] for _ in range(nph)]
     for _ in range(steps):
         flush_l2(flush)
-        p.run(stream)
+        sep.run(stream)
         ev[-1].synchronize()
-        step_ms.append(ev[0].elapsed_time(ev[-1]))
+        sep_ms.append(ev[0].elapsed_time(ev[-1]))
         for i in range(nph):
             phase_ms[i].append(ev[i].elapsed_time(ev[i + 1]))
-    p.args.phase_events = None
+    sep.args.phase_events = None
     torch.cuda.synchronize()
-    assert p.device_status() == 0
+    assert sep.device_status() == 0
     n_chunks = (T + 63) // 64
-    return dict(T=T, H=w.H, step_ms=step_ms, phase_ms=phase_ms, n_chunks=n_chunks,
-                launches_per_step=3, workload=w)
+    return dict(T=T, H=w.H, step_ms=step_ms, phase_ms=phase_ms, n_chunks=n_chunks, path=path,
+                separate_step_ms=sep_ms, launches_per_step=3, workload=w)
 
 
 def bench_prep(torch, kda, W, dev, reps=10):
@@ -286,6 +314,38 @@ def bench_fused(torch, kda, W, dev, steps=10):
     T = sum(inp["lens"])
     return {"workload": w.description + ", fused schedule", "path": path,
             "ms_per_step": t, "tokens_per_s": T / (t * 1e-3), "steps": steps}
+
+
+def bench_overlap(torch, kda, W, dev, steps=10):
+    """One 8192-token sequence of 16 heads (dk = dv = 128), where the
+    automatic choice overlaps the intra-chunk kernel's last items with the
+    inter-chunk chains (64 chains of 32 state columns leave 88 SMs to it),
+    against the separate kernels on the same inputs.  L2 flushed before every
+    call."""
+    w = W.PrefillWorkload("prefill_8k_h16", None, 1, 16, 128, 128, "bf16", 11, len_range=(1, 1))
+    inp = W.prefill_inputs(w, lens=[8192], device=dev, gen_device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    out = {"workload": "one 8192-token sequence x 16 heads, dk = dv = 128, bf16"}
+    for name, sch in (("separate", kda.SCHEDULE_SEPARATE), ("auto", kda.SCHEDULE_AUTO)):
+        p = kda.Prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["b"], inp["cu_seqlens"],
+                        host_cu_seqlens=inp["cu_seqlens"].cpu(), schedule=sch)
+        for _ in range(3):
+            flush_l2(flush)
+            p.run()
+        ms = []
+        for _ in range(steps):
+            flush_l2(flush)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            p.run()
+            e1.record()
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        assert p.device_status() == 0
+        out[name + "_ms"] = sum(ms) / len(ms)
+        out[name + "_path"] = kda.kda_prefill_schedule(p.args)
+    out["tokens_per_s"] = 8192 / (out["auto_ms"] * 1e-3)
+    return out
 
 
 def bench_layer_steps(torch, kda, W, dev, steps=10):
@@ -622,7 +682,9 @@ def gpu_arm(a):
         barrier()
         if a.prefill_only:
             print(json.dumps({"prefill_ms_per_step": sum(pre["step_ms"]) / len(pre["step_ms"]),
-                              "phase_ms": [sum(x) / len(x) for x in pre["phase_ms"]]}))
+                              "path": pre["path"],
+                              "separate_ms_per_step": sum(pre["separate_step_ms"]) / len(pre["separate_step_ms"]),
+                              "separate_phase_ms": [sum(x) / len(x) for x in pre["phase_ms"]]}))
             return
         dec = bench_decode(torch, kda, W, a.decode_steps, max(3, a.warmup), dev)
         barrier()
@@ -636,6 +698,7 @@ def gpu_arm(a):
     vl = bench_varlen(torch, kda, W, dev) if rank == 0 else None
     gph = bench_gate_per_head(torch, kda, W, dev) if rank == 0 else None
     fus = bench_fused(torch, kda, W, dev) if rank == 0 else None
+    ovl = bench_overlap(torch, kda, W, dev) if rank == 0 else None
     lay = bench_layer_steps(torch, kda, W, dev) if rank == 0 else None
     wide = bench_wide_heads(torch, kda, W, dev) if rank == 0 else None
     if rank != 0:
@@ -645,6 +708,7 @@ def gpu_arm(a):
     T, H = pre["T"], pre["H"]
     value = whole_job_tokens_per_s(world, T, step_ms)
     ph = [sum(x) / len(x) for x in pre["phase_ms"]]
+    sep_ms = sum(pre["separate_step_ms"]) / len(pre["separate_step_ms"])
     names = ["plan", "intra_chunk", "inter_chunk"]
     chunk_heads = pre["n_chunks"] * H
     r3 = lambda x: float(f"{x:.4g}")
@@ -652,6 +716,7 @@ def gpu_arm(a):
     inter_tflops = INTER_FLOP_PER_CHUNK_HEAD * chunk_heads / (ph[2] * 1e-3) / 1e12
     intra_gbs = INTRA_BYTES_PER_CHUNK_HEAD * chunk_heads / (ph[1] * 1e-3) / 1e9
     prefill_gbs = PREFILL_BYTES_PER_TOKEN_HEAD * T * H / (step_ms * 1e-3) / 1e9
+    # per-kernel times: the separate kernels, one after the other
     kernels = {
         "plan": {"ms": r3(ph[0])},
         "intra_chunk": {"ms": r3(ph[1]), "tflops": r3(intra_tflops),
@@ -700,6 +765,9 @@ def gpu_arm(a):
                 "ms_per_step": r3(e2e["ms_per_step"])},
         "gpu_launches": pre["launches_per_step"] * a.steps + dec["steps"],
         "clocks": clk.summary(),
+        "prefill_schedule": {"path": {kda.PATH_OVERLAP: "overlapped", kda.PATH_SEPARATE: "separate",
+                                      kda.PATH_FUSED: "fused"}.get(pre["path"], str(pre["path"])),
+                             "separate_ms": r3(sep_ms), "vs_separate": r3(sep_ms / step_ms)},
         "kernels": kernels,
         "decode": {"us_per_step": r3(dec_ms * 1e3), "state_gbs": r3(dec_gbs),
                    "tokens_per_s": r3(world * dec["batch"] / (dec_ms * 1e-3)),
@@ -713,7 +781,11 @@ def gpu_arm(a):
         "prefill_gate_per_head": {"ms": r3(gph["ms_per_step"]), "tokens_per_s": r3(gph["tokens_per_s"])},
         "prefill_fused": {"ms": r3(fus["ms_per_step"]), "tokens_per_s": r3(fus["tokens_per_s"]),
                           "fused_path": fus["path"] == kda.PATH_FUSED,
-                          "vs_separate": r3(step_ms / fus["ms_per_step"])},
+                          "vs_separate": r3(sep_ms / fus["ms_per_step"])},
+        "prefill_overlap_h16": {"separate_ms": r3(ovl["separate_ms"]), "ms": r3(ovl["auto_ms"]),
+                                "overlapped": ovl["auto_path"] == kda.PATH_OVERLAP,
+                                "tokens_per_s": r3(ovl["tokens_per_s"]),
+                                "vs_separate": r3(ovl["separate_ms"] / ovl["auto_ms"])},
         "prefill_layer_steps": {"ms": r3(lay["ms_per_step"]), "tokens_per_s": r3(lay["tokens_per_s"]),
                                 "kernels_ms": {k: r3(v) for k, v in lay["kernels_ms"].items()}},
         "wide_heads": {k: (r3(v) if isinstance(v, float) else v) for k, v in wide.items()

@@ -183,17 +183,21 @@ typedef struct {
   const kda_layer_args* layer; /* host pointer, or NULL: the short convolution and
                                   output gate (above); read during the call only.
                                   Windows are [N, conv_width - 1, H, d]          */
-  int32_t schedule;            /* KDA_SCHEDULE_AUTO (0) or KDA_SCHEDULE_SEPARATE
-                                  (1): the intra-chunk and inter-chunk kernels one
-                                  after the other; KDA_SCHEDULE_FUSED (2): the
-                                  fused kernel where it applies (see below), else
-                                  the two kernels.  All give the same results, bit
-                                  for bit                                       */
+  int32_t schedule;            /* KDA_SCHEDULE_SEPARATE (1): the intra-chunk and
+                                  inter-chunk kernels one after the other;
+                                  KDA_SCHEDULE_FUSED (2): the fused kernel where it
+                                  applies (see below), else the two kernels;
+                                  KDA_SCHEDULE_OVERLAP (3): the overlapped kernels
+                                  where they apply (see below), else the two
+                                  kernels; KDA_SCHEDULE_AUTO (0): the overlapped
+                                  kernels where they apply, else the two kernels.
+                                  All give the same results, bit for bit        */
 } kda_prefill_args;
 
 #define KDA_SCHEDULE_AUTO 0
 #define KDA_SCHEDULE_SEPARATE 1
 #define KDA_SCHEDULE_FUSED 2
+#define KDA_SCHEDULE_OVERLAP 3
 
 /*
  * Segment scan.  The inter-chunk recurrence of one sequence is a chain over
@@ -232,6 +236,24 @@ typedef struct {
  * inter-chunk phase only what follows it.
  */
 
+/*
+ * Overlapped prefill (schedule = KDA_SCHEDULE_OVERLAP or AUTO).  On the
+ * tensor-core path the intra-chunk kernel (K2) takes its (chunk, head) items
+ * in chunk order from a counter on every SM until most are taken; then its
+ * CTAs leave every SM but a few, which make the remaining records.  The
+ * inter-chunk kernel (K3) is launched as K2's programmatic dependent: its
+ * chains (one per head and 32-column slice of the state, each on an SM of
+ * its own) start on the SMs K2 leaves, and read each record once K2 has
+ * published it, while the last ones are still being made.  A chain needs
+ * the record of chunk j only j chain steps after it starts, so the chains
+ * no longer wait for the last item.  It applies on the tensor-core path
+ * without the segment scan, to one sequence whose chains
+ * (num_heads x dv / 32) leave at least 8 SMs for K2, with a wait limit of
+ * 0 or at least 100 us.  A chain waits for a record at most the longer of
+ * wait_limit_ns and 1 s.  With phase_events, the intra-chunk phase holds
+ * both kernels.
+ */
+
 /* The path kda_prefill takes for these arguments on a GPU with sm_count SMs
  * (0: the current device, which must then be present).  Host-side fields
  * only; -1 for invalid arguments or a failed device query. */
@@ -239,6 +261,7 @@ typedef struct {
 #define KDA_PATH_SEPARATE 1      /* tensor cores, K2 then K3                 */
 #define KDA_PATH_FUSED 2         /* tensor cores, the fused kernel           */
 #define KDA_PATH_SEGMENT_SCAN 3  /* tensor cores, the segment scan           */
+#define KDA_PATH_OVERLAP 4       /* tensor cores, K2 and K3 overlapped       */
 int32_t kda_prefill_schedule(const kda_prefill_args* args, int32_t sm_count);
 
 /* Number of timed phases of kda_prefill (see phase_events). */

@@ -109,7 +109,7 @@ kda_status_t validate_prefill(const kda_prefill_args* a) {
   if (a->wait_limit_ns < 0) return KDA_ERR_INVALID_ARG;
   if (a->gate_per_head != 0 && a->gate_per_head != 1) return KDA_ERR_INVALID_ARG;
   if (a->schedule != KDA_SCHEDULE_AUTO && a->schedule != KDA_SCHEDULE_SEPARATE &&
-      a->schedule != KDA_SCHEDULE_FUSED)
+      a->schedule != KDA_SCHEDULE_FUSED && a->schedule != KDA_SCHEDULE_OVERLAP)
     return KDA_ERR_INVALID_ARG;
   kda_status_t ls = validate_layer(a->layer, a->num_seqs, a->num_heads, a->dk, a->dv, elem_bytes(a->in_dtype));
   if (ls != KDA_OK) return ls;
@@ -131,6 +131,49 @@ int64_t fused_chains(const kda_prefill_args* a) {
 }
 bool fused_fits(const kda_prefill_args* a, int sms) {
   return a->schedule == KDA_SCHEDULE_FUSED && fused_shape(a) && fused_chains(a) <= sms;
+}
+
+// The overlapped tensor-core prefill (kda_tc_overlap.cu) applies to one
+// sequence without the segment scan, with normal wait limits (the give-up
+// test's short limits take the separate kernels).  Host-side fields only.
+bool overlap_shape(const kda_prefill_args* a) {
+  return use_tensor_cores(a) && scan_segments_of(a) == 1 && a->num_seqs == 1 && a->dv % 32 == 0 &&
+         a->total_tokens > 0 && (a->wait_limit_ns == 0 || a->wait_limit_ns >= 100000) &&
+         (a->schedule == KDA_SCHEDULE_AUTO || a->schedule == KDA_SCHEDULE_OVERLAP);
+}
+int64_t overlap_chains(const kda_prefill_args* a) {
+  return (int64_t)a->num_seqs * a->num_heads * (a->dv / 32);
+}
+// Where it is taken on a GPU of `sms` SMs: its chains (one per head and
+// 32-column slice of the state, an SM each) take at most half the SMs, so
+// that the SMs left to the intra-chunk kernel make the last records about as
+// fast as the chains read them; the automatic choice also wants at least
+// kOvlMinChains of them.  Measured on GB300 (one sequence, bf16, L2
+// flushed): 64 chains (32 heads of 64 channels, 16 heads of 128, 8192 and
+// 65536 tokens) 1.12-1.21x the separate kernels; 32 chains 0.99-1.0x;
+// 96 and 128 chains 0.93-0.99x (24-56 SMs left make the last records too
+// slowly).
+constexpr int64_t kOvlMinChains = 40;
+bool overlap_fits(const kda_prefill_args* a, int sms) {
+  const int64_t n = overlap_chains(a);
+  return overlap_shape(a) && 2 * n <= sms && (a->schedule == KDA_SCHEDULE_OVERLAP || n >= kOvlMinChains);
+}
+
+// The split of the overlapped prefill: the intra-chunk CTAs that leave stop
+// taking items once this many are taken.  The staying SMs (2 CTAs each) then
+// make the remaining items while the chains run.  A chain step takes about
+// kOvlStepPerItem of an intra-chunk item's time in one CTA (measured on
+// GB300: 12.2 us an item at two CTAs per SM, 1.44 us a chain step), so R
+// remaining items keep ahead of the chains when R <= 2 stay x chunks x
+// kOvlStepPerItem; a margin below that.
+constexpr double kOvlStepPerItem = 0.118;
+constexpr double kOvlMargin = 0.85;
+int64_t overlap_split(const kda_prefill_args* a, int32_t stay_sms) {
+  const int64_t chunks = (a->total_tokens + kChunk - 1) / kChunk + a->num_boundaries;
+  const double ratio = kOvlStepPerItem * kOvlMargin;
+  const int64_t rest = (int64_t)(ratio * 2.0 * stay_sms * (double)chunks);
+  const int64_t items = chunks * a->num_heads;
+  return items > rest ? items - rest : 0;
 }
 
 WsLayout prefill_layout(const kda_prefill_args* a) {
@@ -159,6 +202,13 @@ WsLayout prefill_layout(const kda_prefill_args* a) {
   L.inter = take(L.rec_bytes * (size_t)L.max_chunks * (size_t)a->num_heads);
   if (fused_shape(a) && a->schedule == KDA_SCHEDULE_FUSED)
     L.rec_ready = take(sizeof(uint32_t) * (size_t)L.max_chunks * a->num_heads);
+  if (overlap_shape(a)) {
+    // the counters, then the record flags: one region the planning kernel
+    // clears (a multiple of 16 bytes)
+    L.ovl = take(sizeof(OverlapCounters));
+    L.rec_ready = take(sizeof(uint32_t) * (size_t)L.max_chunks * a->num_heads);
+    L.ovl_words = (off - L.ovl) / sizeof(uint32_t);
+  }
   L.scan_P = P;
   if (P > 1) {
     const size_t mats = (size_t)P * a->num_heads * a->dk * a->dv * sizeof(float);
@@ -198,6 +248,7 @@ int32_t kda_prefill_schedule(const kda_prefill_args* a, int32_t sm_count) {
       return -1;
     device_ok = fused_supported(dev);
   }
+  if (overlap_fits(a, sm_count)) return KDA_PATH_OVERLAP;
   return device_ok && fused_fits(a, sm_count) ? KDA_PATH_FUSED : KDA_PATH_SEPARATE;
 }
 
@@ -233,6 +284,20 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
   pp.seq_len = reinterpret_cast<int64_t*>(w + L.seq_aux);
   pp.seq_bnd = pp.seq_len + a->num_seqs;
   pp.chunks = reinterpret_cast<Chunk*>(w + L.chunks);
+
+  // the path on the tensor cores (no device query for the other paths)
+  int dev = 0, sms = 0;
+  bool overlap = false;
+  if (P == 1 && use_tensor_cores(a)) {
+    cudaError_t qe = cudaGetDevice(&dev);
+    if (qe == cudaSuccess) qe = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (qe != cudaSuccess) return KDA_ERR_CUDA;
+    overlap = overlap_fits(a, sms);
+  }
+  if (overlap) {
+    pp.zero_words = reinterpret_cast<uint32_t*>(w + L.ovl);
+    pp.n_zero_words = L.ovl_words;
+  }
 
   cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(a->phase_events);
   auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
@@ -290,11 +355,14 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
     sb.s0 = a->initial_state;
     sb.final_state = a->final_state;
     e = launch_tc_prefill_scan(cp, sb, stream, ev ? ev[2] : nullptr);
+  } else if (overlap) {
+    cp.rec_ready = reinterpret_cast<uint32_t*>(w + L.rec_ready);
+    cp.ovl = reinterpret_cast<OverlapCounters*>(w + L.ovl);
+    cp.ovl_stay_sms = sms - (int32_t)overlap_chains(a);
+    cp.ovl_split = overlap_split(a, cp.ovl_stay_sms);
+    e = launch_tc_overlap(cp, stream);
+    if (e == cudaSuccess && ev) e = cudaEventRecord(ev[2], stream);
   } else if (use_tensor_cores(a)) {
-    int dev = 0, sms = 0;
-    e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return KDA_ERR_CUDA;
     if (fused_fits(a, sms) && fused_supported(dev)) {
       cp.rec_ready = reinterpret_cast<uint32_t*>(w + L.rec_ready);
       e = cudaMemsetAsync(cp.rec_ready, 0, sizeof(uint32_t) * (size_t)L.max_chunks * a->num_heads, stream);

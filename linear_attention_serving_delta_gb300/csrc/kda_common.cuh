@@ -43,6 +43,17 @@ struct PlanMeta {
   int64_t pad[3];
 };
 
+// Programmatic dependent launch (griddepcontrol, sm_90 and later).  A
+// kernel launched as the programmatic dependent of the kernel before it on
+// the stream may start once every CTA of that kernel has signalled
+// (pdl_launch_dependents) or exited; at pdl_wait it waits until that kernel
+// has completed and its memory operations are visible.  Both are no-ops for
+// a kernel launched the ordinary way or without such a dependent.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ input access
 template <typename T>
 __device__ __forceinline__ float ld_in(const T* p, int64_t i);
@@ -133,9 +144,12 @@ struct WsLayout {
   // segment scan: segment count (1 = off) and its buffers
   int32_t scan_P = 1;
   size_t scan_cu = 0, scan_A = 0, scan_B = 0, scan_inits = 0, scan_finals = 0;
-  // fused tensor-core prefill: a flag per record (where the arguments can
-  // take it)
+  // fused and overlapped tensor-core prefill: a flag per record (where the
+  // arguments can take it); (overlapped) its counters, right before the
+  // flags, and the words of both, which the planning kernel clears
   size_t rec_ready = 0;
+  size_t ovl = 0;
+  int64_t ovl_words = 0;
 };
 
 }  // namespace kda

@@ -38,6 +38,22 @@ struct PlanParams {
   int32_t* bnd_nonaligned;  // [num_boundaries + N]
   int32_t* bnd_nonmult;     // [num_boundaries + N]
   Chunk* chunks;            // [max_chunks]
+  // words the planning kernel clears before anything else (the overlapped
+  // schedule's record flags and counters), or null
+  uint32_t* zero_words;
+  int64_t n_zero_words;
+};
+
+// Counters of the overlapped tensor-core prefill, in the workspace, cleared
+// by the planning kernel.  SMs are keyed by their id modulo kOvlSmKeys (two
+// SMs that share a key share a role, which changes no result).
+constexpr int kOvlSmKeys = 512;
+struct OverlapCounters {
+  unsigned long long next_item;  // items taken so far
+  uint32_t stay_sms;             // SMs elected to stay
+  uint32_t pad;
+  uint32_t arrived[kOvlSmKeys];  // intra-chunk CTAs started on the SM
+  uint32_t role[kOvlSmKeys];     // 0 undecided, 1 leaves at the split, 2 stays
 };
 
 // Everything the intra-chunk and inter-chunk kernels read.
@@ -79,10 +95,18 @@ struct ChunkParams {
   int32_t conv_one_seq;
   const void* out_gate;     // [T][H][dv], or [T][H] with out_gate_per_head
   int32_t out_gate_per_head;
-  // the fused tensor-core prefill: a flag per record [max_chunks][H], zero
-  // at the launch, set once the record is complete (null otherwise)
+  // the fused and the overlapped tensor-core prefill: a flag per record
+  // [max_chunks][H], zero at the launch, set once the record is complete
+  // (null otherwise)
   uint32_t* rec_ready;
+  // the overlapped tensor-core prefill (OverlapCounters, zero at the launch):
+  // the intra-chunk CTAs on ovl_stay_sms SMs take items until none is left,
+  // the others only while fewer than ovl_split have been taken
+  OverlapCounters* ovl;
+  int32_t ovl_stay_sms;
+  int64_t ovl_split;
 };
+
 constexpr int32_t kScanPass1 = 1;
 
 // The window of each sequence after the call (kda_layer_args::conv_out):
@@ -112,6 +136,14 @@ cudaError_t launch_tc_prefill(const ChunkParams& p, cudaStream_t stream, cudaEve
 int fused_chain_columns();
 bool fused_supported(int device);
 cudaError_t launch_tc_fused(const ChunkParams& p, int32_t n_chain, int32_t grid, cudaStream_t stream);
+// The overlapped tensor-core prefill (kda_tc_overlap.cu): the intra-chunk
+// kernel and then the inter-chunk kernel launched as its programmatic
+// dependent, the chains starting on the SMs the intra-chunk CTAs leave at
+// the split while p.ovl_stay_sms SMs make the last records; p.rec_ready and
+// p.ovl set and zero (cleared by the planning kernel launched before).
+// overlap_chain_columns: the state columns of a chain CTA.
+int overlap_chain_columns();
+cudaError_t launch_tc_overlap(const ChunkParams& p, cudaStream_t stream);
 // The segment scan over P chunk-aligned segments of one sequence (planned as
 // P sequences in `p`): K2 once, K3 pass 1 (state offsets B and transition
 // maps A of every segment, in parallel), the combine (inits[s+1] = A_s

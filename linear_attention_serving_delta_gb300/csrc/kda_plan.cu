@@ -186,18 +186,25 @@ __device__ void fill_segment(const PlanParams& p, int64_t gidx, int32_t& bad) {
   }
 }
 
-// One CTA: clears the status word, plans the sequences, writes every chunk
-// entry, and marks the unused tail of the table (len = 0) so that the
-// per-chunk kernels can read their entry without consulting the totals.
+// One CTA: clears the status word (and the words of zero_words), plans the
+// sequences, writes every chunk entry, and marks the unused tail of the table
+// (len = 0) so that the per-chunk kernels can read their entry without
+// consulting the totals.  The intra-chunk kernel after it may be launched as
+// its programmatic dependent: it is let start at once, and it waits for this
+// kernel's results before it reads them.
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(PlanParams p) {
   __shared__ int64_t sh[kPlanThreads];
   __shared__ int32_t shf;
   const int tid = threadIdx.x;
+  pdl_launch_dependents();
   if (tid == 0) {
     *p.status = 0;
     shf = 0;
   }
+  // (a multiple of 4 words, 16-byte aligned)
+  for (int64_t i = tid; i < p.n_zero_words / 4; i += kPlanThreads)
+    reinterpret_cast<uint4*>(p.zero_words)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   int32_t flags = 0;
   plan_sequences(p, sh, flags);

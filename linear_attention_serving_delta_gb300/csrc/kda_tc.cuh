@@ -273,6 +273,11 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* a) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
   return v;
 }
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* a) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_release_u32(uint32_t* a, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
 }

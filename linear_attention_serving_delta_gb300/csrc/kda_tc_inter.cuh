@@ -261,6 +261,10 @@ struct K3Bars {
   uint64_t mma3[2];  // MMA 3 of even / odd chunks (output path)
   uint64_t drain;    // every MMA, on the error path
   uint32_t tmem_base;
+  // (kFused) the records of the chain's first `pub` chunks are published,
+  // as thread kLoadThread found them; read by thread kOutThread after a
+  // CTA barrier
+  int64_t pub;
 };
 
 // The chain of (sequence s, head h, column slice z % kSlices) on a whole CTA
@@ -289,8 +293,16 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
   const bool pass1 = p.k3_mode == kScanPass1;
   const bool trans = pass1 && z >= C::kSlices;
   const int H = p.H, tid = threadIdx.x, warp = tid >> 5;
-  const int64_t c_begin = p.seq_chunk_begin[s], c_end = p.seq_chunk_begin[s + 1];
-  if (c_end > c_begin && p.meta->total_chunks == 0) return;  // chunk table overflowed
+  // (kFused, one operand ring: the overlapped schedule) this CTA started as
+  // the programmatic dependent of the intra-chunk kernel, without waiting for
+  // it; what it reads of the planning kernel's outputs was complete before
+  // any intra-chunk CTA signalled (each waited for the planning kernel
+  // first).  The scalars are read through L2.
+  constexpr bool kOvl = kFused && !kSplit;
+  const int64_t c_begin = kOvl ? __ldcg(p.seq_chunk_begin + s) : p.seq_chunk_begin[s];
+  const int64_t c_end = kOvl ? __ldcg(p.seq_chunk_begin + s + 1) : p.seq_chunk_begin[s + 1];
+  const int64_t total_chunks = kOvl ? __ldcg(&p.meta->total_chunks) : p.meta->total_chunks;
+  if (c_end > c_begin && total_chunks == 0) return;  // chunk table overflowed
   const int64_t nchunks = c_end - c_begin;
 
   // TMEM lane quarter of this warp, its 16 columns, its key channel / token row
@@ -356,19 +368,47 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
   bool okl = true;  // this thread's own waits succeeded
   // (kFused) record j is published, as seen by this thread (an acquire,
   // then a proxy fence before the copies that read it): 1 yes, 0 not yet
-  // (`now` false: no wait), -1 the wait gave up.  `seen` spares a second
-  // look at a record the thread has seen.
-  int64_t seen = -1;
+  // (`now` false: no wait), -1 the wait gave up.  The records of chunks
+  // below `pub` are known published.  Thread kLoadThread, finding record j
+  // not known, reads the flags of up to kScanAhead chunks from `pub` on at
+  // once (relaxed loads in flight together) and takes the published ones in
+  // order with one acquire fence: an acquire load per record would hold its
+  // warp, which also takes part in every chain step, for a round trip to L2
+  // each time.  It leaves `pub` in shared memory, where thread kOutThread
+  // takes it after the next CTA barrier.
+  constexpr int kScanAhead = 16;
+  int64_t pub = 0;
+  if (kFused && tid == kLoadThread) bars.pub = 0;
   auto ready = [&](int64_t j, bool now) -> int {
     if constexpr (kFused) {
-      if (j <= seen) return 1;
-      if (now) {
-        if (!rec_wait_published(p, c_begin + j, h)) return -1;
-      } else {
-        if (!rec_published(p, c_begin + j, h)) return 0;
-        fence_proxy_async_global();
+      if (j < pub) return 1;
+      if (tid == kLoadThread && !now) {
+        // batches of kScanAhead flags, while a whole batch is published
+        int64_t q = pub;
+        for (;;) {
+          uint32_t f[kScanAhead];
+#pragma unroll
+          for (int k = 0; k < kScanAhead; ++k)
+            f[k] = q + k < nchunks ? ld_relaxed_u32(rec_flag(p, c_begin + q + k, h)) : 0u;
+          int n = 0;
+          while (n < kScanAhead && f[n] != 0u) ++n;
+          q += n;
+          if (n < kScanAhead) break;
+        }
+        if (q > pub) {
+          fence_gpu();  // with the relaxed loads that saw the flags: an acquire
+          fence_proxy_async_global();
+          pub = q;
+          *reinterpret_cast<volatile int64_t*>(&bars.pub) = pub;
+        }
+        return j < pub ? 1 : 0;
       }
-      seen = j;
+      if (!now) return 0;
+      if (!rec_wait_published(p, c_begin + j, h)) return -1;
+      if (j == pub) {
+        pub = j + 1;
+        if (tid == kLoadThread) *reinterpret_cast<volatile int64_t*>(&bars.pub) = pub;
+      }
     }
     return 1;
   };
@@ -405,7 +445,7 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
   }
   if (tid == kOutThread)
     for (int64_t j = 0; okl && j < C::kAqSlots && j < nchunks && aq_issued == j; ++j)
-      okl = issue_aq(j, false);
+      okl = issue_aq(j, kFused && j == 0);
   // initial state: the operand holds S_0, TMEM Gamma_L(0) S_0.  States are
   // [dk][dv] in global memory; a head narrower than 128 channels (dk or dv =
   // 64) runs zero-padded: key rows c >= dk hold zeros and are never written,
@@ -476,6 +516,13 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
     ok = __syncthreads_and(okl);
     fence_after_sync();
     if (!ok) break;
+    if (kFused && tid == kOutThread) {
+      const int64_t q = *reinterpret_cast<volatile int64_t*>(&bars.pub);
+      if (q > pub) {
+        pub = q;
+        fence_proxy_async_global();  // before its copies read those records
+      }
+    }
     // (kFused, kSplit) a first look at chunk it+1's record, early: its part
     // A can then go in as soon as MMA 1 has read AW
     if (kFused && kSplit && tid == kLoadThread && okl && it + 1 < nchunks) ready(it + 1, false);
@@ -495,16 +542,40 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
         // ... its A_qk tile takes chunk it+1 (with two tiles, chunk it, whose
         // slot held chunk it-2's) ...
         constexpr int kAqLead = C::kAqSlots - 2;
-        if (tid == kOutThread && okl && it + kAqLead < nchunks && aq_issued == it + kAqLead)
-          okl = issue_aq(it + kAqLead, false);
+        if constexpr (kFused && !kSplit) {
+          // (records that come late) every tile not yet copied whose slot is
+          // free, in order, as far as their records are published
+          if (tid == kOutThread)
+            while (okl && aq_issued <= it + kAqLead && aq_issued < nchunks) {
+              const int64_t j = aq_issued;
+              okl = issue_aq(j, false);
+              if (aq_issued == j) break;
+            }
+        } else {
+          if (tid == kOutThread && okl && it + kAqLead < nchunks && aq_issued == it + kAqLead)
+            okl = issue_aq(it + kAqLead, false);
+        }
       }
       // ... with a 3-slot ring the slot of chunk it-1 (MMA 2 done) takes
       // chunk it+2 here, off the chain ...
-      if (C::kSlots == 3 && tid == kLoadThread && okl && it >= 1 && it + 2 < nchunks) okl = issue_chain(it + 2, true);
+      if constexpr (kFused && C::kSlots == 3) {
+        // (records that come late) every chunk not yet copied whose slot is
+        // free (up to chunk it+2), in order, as far as their records are
+        // published; one still missing is copied, waiting, in the write-back
+        // of the step before it is needed
+        if (tid == kLoadThread && it >= 1)
+          while (okl && chain_issued <= it + 2 && chain_issued < nchunks) {
+            const int64_t j = chain_issued;
+            okl = issue_chain(j, false);
+            if (chain_issued == j) break;
+          }
+      } else {
+        if (C::kSlots == 3 && tid == kLoadThread && okl && it >= 1 && it + 2 < nchunks) okl = issue_chain(it + 2, true);
+      }
       // ... (kSplit) part A of chunk it+1 goes in once MMA 1 has read AW
       // (kFused: if its record was seen above) ...
       if (kSplit && tid == kLoadThread && okl && it + 1 < nchunks && chain_issued == it + 1 &&
-          (!kFused || seen >= it + 1)) {
+          (!kFused || pub > it + 1)) {
         okl = mbar_wait_t<kPoll>(&bar_mma1, ph1, p.wait_ns);
         if (okl) okl = issue_chain(it + 1, false);
       }

@@ -439,6 +439,12 @@ struct IntraBars {
   // complete but not yet published (or null)
   uint32_t* cur;
   uint32_t* pend;
+  // (items taken from the shared counter) the pipeline's coming items: item
+  // n + k of the pipeline (k = 1..3 ahead of item n) in entry (n + k) % 4;
+  // thread 0 takes item n + 3 during item n.  `stopped`: a pipeline that
+  // leaves at the split has taken its last item
+  int64_t ahead[4];
+  int32_t stopped;
 };
 __device__ __forceinline__ void init_intra_bars(IntraBars* b) {
   mbar_init(&b->mma, 1);
@@ -447,11 +453,15 @@ __device__ __forceinline__ void init_intra_bars(IntraBars* b) {
   mbar_init(&b->drain, 1);
   mbar_init_fence();
   b->pend = nullptr;
+  b->stopped = 0;
 }
 
 // One item pipeline: 256 threads (tid 0..255) on Smem::BYTES of shared
 // memory at sm, 256 TMEM columns at tmem, synchronised by bs; it takes the
-// items first, first + stride, ... below n_items.
+// items first, first + stride, ... below n_items (or, with items taken from
+// the overlapped schedule's counter, those it takes there; `stay`: it takes
+// items until none is left, else only while fewer than p.ovl_split have
+// been taken).
 struct IntraPipe {
   uint8_t* sm;
   IntraBars* bars;
@@ -459,7 +469,20 @@ struct IntraPipe {
   int tid;
   PipeSync bs;
   int64_t first, stride, n_items;
+  bool stay;
 };
+
+// (thread 0, overlapped schedule) the next item of this pipeline from the
+// shared counter, or INT64_MAX for none.  Items are taken in index order,
+// that is in chunk order, the order in which the chains read them.  A
+// pipeline that leaves at the split takes no more items once it has taken
+// one at or past the split (which it still makes).
+__device__ __forceinline__ int64_t take_item(const ChunkParams& p, const IntraPipe& x) {
+  if (x.bars->stopped) return INT64_MAX;
+  const unsigned long long i = atomicAdd(&p.ovl->next_item, 1ull);
+  if (!x.stay && i >= (unsigned long long)p.ovl_split) x.bars->stopped = 1;
+  return i < (unsigned long long)x.n_items ? (int64_t)i : INT64_MAX;
+}
 
 // The items of one pipeline.  The next item's rows are prefetched into L2 at
 // the top of an item and staged by bulk copies as soon as their tiles are
@@ -471,7 +494,10 @@ struct IntraPipe {
 // kFused: the chains of the fused kernel read the records as they come: the
 // record of each item is published (kda_tc_handoff.cuh) once its copies
 // have landed, at a barrier of the pipeline's next item (or after its last).
-template <bool kPoll, bool kHeadGate, bool kConv, bool kFused>
+// kTake: the items come from the overlapped schedule's counter (take_item)
+// instead of a stride; each is known three items ahead of its turn, as the
+// prefetches need.
+template <bool kPoll, bool kHeadGate, bool kConv, bool kFused, bool kTake = false>
 __device__ __forceinline__ void intra_items(const ChunkParams& p, const RowMaps& maps, const IntraPipe& x) {
   uint8_t* const sm = x.sm;
   uint64_t& bar_mma = x.bars->mma;
@@ -512,11 +538,24 @@ __device__ __forceinline__ void intra_items(const ChunkParams& p, const RowMaps&
   // the item before it
   // (chunk-table entries are read two items ahead of their first use, the
   // L2 prefetch of the next item's rows: a global load's latency is hidden)
+  // the pipeline's item k ahead of its n-th (INT64_MAX or past n_items: none)
+  int64_t* const ahead = x.bars->ahead;
+  auto item_ahead = [&](uint32_t n, int k) -> int64_t {
+    return kTake ? ahead[(n + k) & 3] : item + k * stride;
+  };
+  if constexpr (kTake) {
+    if (tid == 0) {
+      item = take_item(p, x);
+      for (int k = 1; k <= 2; ++k) ahead[k] = take_item(p, x);
+      ahead[0] = item;
+    }
+    bs.sync();
+    item = ahead[0];
+    if (item >= n_items) return;  // (uniform) nothing left: no staging was issued
+  }
   ItemChunk ch = item_chunk<kConv>(p, item / H);  // entries past the table's end have len 0
-  ItemChunk ch_next =
-      item + stride < n_items ? item_chunk<kConv>(p, (item + stride) / H) : ItemChunk{0, 0, 0};
-  ItemChunk ch_next2 =
-      item + 2 * stride < n_items ? item_chunk<kConv>(p, (item + 2 * stride) / H) : ItemChunk{0, 0, 0};
+  ItemChunk ch_next = item_ahead(0, 1) < n_items ? item_chunk<kConv>(p, item_ahead(0, 1) / H) : ItemChunk{0, 0, 0};
+  ItemChunk ch_next2 = item_ahead(0, 2) < n_items ? item_chunk<kConv>(p, item_ahead(0, 2) / H) : ItemChunk{0, 0, 0};
   {
     const int h0 = (int)(item % H);
     if (tid == 0) {
@@ -536,18 +575,21 @@ __device__ __forceinline__ void intra_items(const ChunkParams& p, const RowMaps&
   const uint32_t tmem = x.tmem;
   bool ok = true;
 
-  for (; item < n_items; item += stride) {
+  uint32_t nth = 0;  // (kTake) the pipeline's count of items so far
+  for (; item < n_items;) {
     const int h = (int)(item % H);
     const int64_t cidx = item / H;
     const int len = ch.len;
+
     // past the end of the chunk table (uniform across the CTA); every later
     // item of this CTA is past it too
     if (len == 0) break;
     uint8_t* rec = reinterpret_cast<uint8_t*>(p.inter) + ((size_t)cidx * H + h) * Rec::BYTES;
     if (kFused && tid == 0) x.bars->cur = rec_flag(p, cidx, h);
-    const bool has_next = item + stride < n_items;
+    const int64_t item1 = item_ahead(nth, 1);
+    const bool has_next = item1 < n_items;
     const ItemChunk chn = ch_next;
-    const int hn = (int)((item + stride) % H);
+    const int hn = has_next ? (int)(item1 % H) : 0;
     const float bcur = bnext;
     // the next item's rows into L2 now, so that their staging copies hit L2
     if (has_next && tid < 4 && !(kHeadGate && tid == 0))
@@ -821,6 +863,10 @@ __device__ __forceinline__ void intra_items(const ChunkParams& p, const RowMaps&
       bulk_commit();
     }
     // ---- MMA 1: [A_kk ; A_qk] = [Kp ; Qp] Kn^T   (M=128, N=64, K=128)
+    // (kTake) the item three ahead is taken while MMA 1 runs (the atomic's
+    // round trip overlaps the wait) and written for the other threads, who
+    // read it after this item's last barrier
+    int64_t taken = 0;
     if (tid == 0) {
       const uint32_t id = idesc_bf16(128, 64);
 #pragma unroll
@@ -828,10 +874,12 @@ __device__ __forceinline__ void intra_items(const ChunkParams& p, const RowMaps&
         mma_bf16(tmem, sdesc(smem_u32(A1) + s * 2 * kA1Lbo, kA1Lbo, 128),
                  sdesc(smem_u32(B1) + s * 2 * kB1Lbo, kB1Lbo, 128), id, s > 0);
       mma_commit(&bar_mma);
+      if (kTake) taken = take_item(p, x);
     }
     // the A_kk tile is rewritten below: the AK copies must have read it
     if (copy_group(tid) >= 0) bulk_wait_read_all();
     ok = bs.all(mbar_wait_t<kPoll>(&bar_mma, 0, p.wait_ns));
+    if (kTake && tid == 0) ahead[(nth + 3) & 3] = taken;
     fence_after_sync();
     if (!ok) break;
     if (rescale) {
@@ -979,10 +1027,12 @@ __device__ __forceinline__ void intra_items(const ChunkParams& p, const RowMaps&
       bulk_commit();
     }
     if (kFused && tid == 0) x.bars->pend = x.bars->cur;
+    const int64_t item3 = item_ahead(nth, 3);
     ch = ch_next;
     ch_next = ch_next2;
-    ch_next2 = item + 3 * stride < n_items ? item_chunk<kConv>(p, (item + 3 * stride) / H)
-                                           : ItemChunk{0, 0, 0};
+    ch_next2 = item3 < n_items ? item_chunk<kConv>(p, item3 / H) : ItemChunk{0, 0, 0};
+    item = item1;
+    ++nth;
   }
   // no staging copy and no MMA is left in flight when the CTA exits (these
   // waits keep the long limit whatever the caller chose for the others)

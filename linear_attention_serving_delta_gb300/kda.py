@@ -27,9 +27,9 @@ KDA_OK = 0
 KDA_F32, KDA_BF16 = 0, 1
 CHUNK = 64
 PREFILL_PHASES = 3  # chunk planning, intra-chunk, inter-chunk
-SCHEDULE_AUTO, SCHEDULE_SEPARATE, SCHEDULE_FUSED = 0, 1, 2  # kda_prefill_args.schedule
+SCHEDULE_AUTO, SCHEDULE_SEPARATE, SCHEDULE_FUSED, SCHEDULE_OVERLAP = 0, 1, 2, 3  # kda_prefill_args.schedule
 # kda_prefill_schedule: the path a prefill takes
-PATH_CUDA_CORES, PATH_SEPARATE, PATH_FUSED, PATH_SEGMENT_SCAN = 0, 1, 2, 3
+PATH_CUDA_CORES, PATH_SEPARATE, PATH_FUSED, PATH_SEGMENT_SCAN, PATH_OVERLAP = 0, 1, 2, 3, 4
 _STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED",
                  3: "KDA_ERR_WORKSPACE", 4: "KDA_ERR_CUDA", 5: "KDA_ERR_TIMEOUT",
                  6: "KDA_ERR_DEVICE_DATA"}

@@ -67,6 +67,8 @@ int main(void) {
   printf("const.KDA_SCHEDULE_AUTO %d\n", KDA_SCHEDULE_AUTO);
   printf("const.KDA_SCHEDULE_SEPARATE %d\n", KDA_SCHEDULE_SEPARATE);
   printf("const.KDA_SCHEDULE_FUSED %d\n", KDA_SCHEDULE_FUSED);
+  printf("const.KDA_SCHEDULE_OVERLAP %d\n", KDA_SCHEDULE_OVERLAP);
+  printf("const.KDA_PATH_OVERLAP %d\n", KDA_PATH_OVERLAP);
   printf("const.KDA_PATH_CUDA_CORES %d\n", KDA_PATH_CUDA_CORES);
   printf("const.KDA_PATH_SEPARATE %d\n", KDA_PATH_SEPARATE);
   printf("const.KDA_PATH_FUSED %d\n", KDA_PATH_FUSED);
@@ -104,7 +106,8 @@ int main(void) {
     consts = {"KDA_CONV_MAX": kda.CONV_MAX, "KDA_CHUNK": kda.CHUNK,
               "KDA_PREFILL_PHASES": kda.PREFILL_PHASES,
               "KDA_SCHEDULE_AUTO": kda.SCHEDULE_AUTO, "KDA_SCHEDULE_SEPARATE": kda.SCHEDULE_SEPARATE,
-              "KDA_SCHEDULE_FUSED": kda.SCHEDULE_FUSED,
+              "KDA_SCHEDULE_FUSED": kda.SCHEDULE_FUSED, "KDA_SCHEDULE_OVERLAP": kda.SCHEDULE_OVERLAP,
+              "KDA_PATH_OVERLAP": kda.PATH_OVERLAP,
               "KDA_PATH_CUDA_CORES": kda.PATH_CUDA_CORES, "KDA_PATH_SEPARATE": kda.PATH_SEPARATE,
               "KDA_PATH_FUSED": kda.PATH_FUSED, "KDA_PATH_SEGMENT_SCAN": kda.PATH_SEGMENT_SCAN}
     for key, val in got.items():
@@ -155,14 +158,23 @@ def test_workspace_size_and_validation(kda):
     assert (L.kda_prefill_workspace_size(ctypes.byref(tcp)) -
             L.kda_prefill_workspace_size(ctypes.byref(cup))) == 2 * 2 * (90624 - 82176)
     # the fused kernel reads the same record array; only its flags are added
-    # (2 chunk-table entries x 2 heads, one 256-byte block), the automatic
-    # choice is the separate kernels, and an unknown schedule is rejected
+    # (2 chunk-table entries x 2 heads, one 256-byte block); the overlapped
+    # kernels (the automatic choice for one sequence) add the flags and their
+    # counters (8 + 8 + 2 x 512 x 4 bytes, in 256-byte blocks); with several
+    # sequences nothing is added; an unknown schedule is rejected
     fused = _args(kda, in_dtype=kda.KDA_BF16, dk=64, dv=64, schedule=kda.SCHEDULE_FUSED)
     auto = _args(kda, in_dtype=kda.KDA_BF16, dk=64, dv=64)
+    ovl = _args(kda, in_dtype=kda.KDA_BF16, dk=64, dv=64, schedule=kda.SCHEDULE_OVERLAP)
     assert (L.kda_prefill_workspace_size(ctypes.byref(fused)) -
             L.kda_prefill_workspace_size(ctypes.byref(tcp))) == 256
-    assert L.kda_prefill_workspace_size(ctypes.byref(auto)) == L.kda_prefill_workspace_size(ctypes.byref(tcp))
-    a = _args(kda, schedule=3)
+    counters = -(-(16 + 2 * 512 * 4) // 256) * 256
+    for a in (auto, ovl):
+        assert (L.kda_prefill_workspace_size(ctypes.byref(a)) -
+                L.kda_prefill_workspace_size(ctypes.byref(tcp))) == 256 + counters
+    two = dict(in_dtype=kda.KDA_BF16, dk=64, dv=64, num_seqs=2)
+    assert (L.kda_prefill_workspace_size(ctypes.byref(_args(kda, **two))) ==
+            L.kda_prefill_workspace_size(ctypes.byref(_args(kda, schedule=kda.SCHEDULE_SEPARATE, **two))))
+    a = _args(kda, schedule=4)
     assert L.kda_prefill_workspace_size(ctypes.byref(a)) == 0
     assert L.kda_prefill(ctypes.byref(a), 0x4000, 1 << 30, None) == 1
     # heads of 256 channels are taken (the CUDA-core path's blocked kernel)
@@ -197,18 +209,37 @@ def test_workspace_size_and_validation(kda):
 
 def test_prefill_schedule(kda):
     """The path a prefill takes (kda_prefill_schedule, host logic only, for a
-    given SM count): the separate tensor-core kernels by default; with
-    schedule = FUSED the fused kernel where its chains (sequences x heads x
-    dv / 32) are at most as many as the SMs; the segment scan and the fp32
-    CUDA-core path where they apply."""
+    given SM count): by default the overlapped tensor-core kernels for one
+    sequence whose chains (heads x dv / 32) number 40 to half the SMs (with
+    schedule = OVERLAP any number up to half the SMs), else the separate
+    kernels; with schedule = FUSED the fused kernel where its chains
+    (sequences x heads x dv / 32) are at most as many as the SMs; the segment
+    scan and the fp32 CUDA-core path where they apply."""
     L = kda.lib()
     bf = dict(in_dtype=kda.KDA_BF16, dk=128, dv=128)
     fu = dict(schedule=kda.SCHEDULE_FUSED)
+    ov = dict(schedule=kda.SCHEDULE_OVERLAP)
 
     def path(sms=152, **over):
         return L.kda_prefill_schedule(ctypes.byref(_args(kda, **over)), sms)
 
-    assert path(num_heads=32, total_tokens=8192, **bf) == kda.PATH_SEPARATE       # the default
+    assert path(num_heads=32, total_tokens=8192, **bf) == kda.PATH_SEPARATE       # 128 chains
+    assert path(num_heads=32, total_tokens=8192, **ov, **bf) == kda.PATH_SEPARATE
+    assert path(num_heads=16, total_tokens=8192, **bf) == kda.PATH_OVERLAP        # 64 chains
+    assert path(num_heads=19, total_tokens=8192, **bf) == kda.PATH_OVERLAP        # 76 chains
+    assert path(num_heads=20, total_tokens=8192, **bf) == kda.PATH_SEPARATE       # 80 chains
+    assert path(num_heads=10, total_tokens=8192, **bf) == kda.PATH_OVERLAP        # 40 chains
+    assert path(num_heads=8, total_tokens=8192, **bf) == kda.PATH_SEPARATE        # 32 chains
+    assert path(num_heads=8, total_tokens=8192, **ov, **bf) == kda.PATH_OVERLAP
+    assert path(sms=128, num_heads=16, total_tokens=8192, **bf) == kda.PATH_OVERLAP
+    assert path(sms=127, num_heads=16, total_tokens=8192, **bf) == kda.PATH_SEPARATE
+    assert path(num_seqs=2, num_heads=8, total_tokens=8192, **bf) == kda.PATH_SEPARATE
+    assert path(num_heads=16, total_tokens=8192, wait_limit_ns=1000, **bf) == kda.PATH_SEPARATE
+    assert path(num_heads=16, total_tokens=8192, wait_limit_ns=100000, **bf) == kda.PATH_OVERLAP
+    assert path(num_heads=16, total_tokens=0, **bf) == kda.PATH_SEPARATE          # nothing to overlap
+    assert path(num_heads=32, total_tokens=8192, in_dtype=kda.KDA_BF16, dk=64, dv=64) == kda.PATH_OVERLAP
+    assert path(num_heads=2, total_tokens=65536, **bf) == kda.PATH_SEGMENT_SCAN
+    assert path(num_heads=2, total_tokens=65536, scan_segments=1, **ov, **bf) == kda.PATH_OVERLAP
     assert path(num_heads=32, total_tokens=8192, schedule=kda.SCHEDULE_SEPARATE, **bf) == kda.PATH_SEPARATE
     assert path(num_heads=32, total_tokens=8192, **fu, **bf) == kda.PATH_FUSED    # 128 chains
     assert path(num_heads=38, total_tokens=8192, **fu, **bf) == kda.PATH_FUSED    # 152 chains

@@ -118,6 +118,27 @@ cudaError_t launch_conv_windows(const kda_layer_args& l, int32_t num_seqs, int32
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 
+// A launch as the programmatic dependent of the kernel before it on the
+// stream (programmatic stream serialization): its CTAs may start once every
+// CTA of that kernel has signalled (pdl_launch_dependents) or exited, and it
+// waits for that kernel's results at pdl_wait.  `dependent` false: an
+// ordinary launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_maybe_dependent(bool dependent, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                   cudaStream_t stream, const Args&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // fp32 CUDA-core path (any supported dk, dv; f32 or bf16 inputs)
 // `mid` (may be null) is recorded on the stream between the intra-chunk and
 // the inter-chunk kernels.

@@ -38,22 +38,35 @@ __device__ __forceinline__ int64_t upper_bound_i64(const int64_t* a, int64_t lo,
   return lo;
 }
 
-// Block-wide exclusive scan of one value per thread; `total` receives the sum.
+// Block-wide exclusive scan of one value per thread; `total` receives the
+// sum.  A shuffle scan inside each warp, the warps' sums scanned by warp 0
+// through shared memory (sh: one entry per warp), two barriers.
 __device__ int64_t block_exclusive_scan(int64_t x, int64_t* sh, int64_t& total) {
-  const int tid = threadIdx.x;
-  sh[tid] = x;
-  __syncthreads();
-  for (int off = 1; off < kPlanThreads; off <<= 1) {
-    int64_t y = tid >= off ? sh[tid - off] : 0;
-    __syncthreads();
-    sh[tid] += y;
-    __syncthreads();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int64_t incl = x;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
   }
-  const int64_t incl = sh[tid];
-  total = sh[kPlanThreads - 1];
+  if (lane == 31) sh[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = sh[lane];  // kPlanThreads / 32 == 32 warps
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    sh[lane] = w;  // inclusive sums of the warps
+  }
+  __syncthreads();
+  const int64_t before = warp > 0 ? sh[warp - 1] : 0;
+  total = sh[kPlanThreads / 32 - 1];
   __syncthreads();  // every thread has read before sh is reused
-  return incl - x;
+  return before + incl - x;
 }
+static_assert(kPlanThreads == 32 * 32, "the scan has one warp sum per lane of warp 0");
 
 // Per-sequence validation, counts and prefix sums (whole block).
 __device__ void plan_sequences(const PlanParams& p, int64_t* sh, int32_t& flags) {

@@ -118,7 +118,8 @@ __device__ __forceinline__ float gate_fast(float r) {
   return r >= 0.f ? 1.f - t : t;
 }
 
-cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream);
+// dependent: launched as the programmatic dependent of the planning kernel
+cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream, bool dependent = false);
 
 }  // namespace tcp
 }  // namespace kda

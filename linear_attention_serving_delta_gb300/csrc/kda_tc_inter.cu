@@ -12,33 +12,39 @@ template <bool kPoll, int NS>
 __global__ void __launch_bounds__(K3Cfg<NS>::kThreads, 1) tc_inter(ChunkParams p) {
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ K3Bars<NS> bars;
+  // (launched as the intra-chunk kernel's programmatic dependent) its
+  // records are read from here on
+  pdl_wait();
   inter_chain<kPoll, NS, false>(p, (int)blockIdx.x, (int)blockIdx.y, (int)blockIdx.z, sm, bars);
 }
 
 // tc_inter with the wait mode its limit asks for, over grid (gx, gy, zmul x
 // the head's column slices)
 template <int NS>
-cudaError_t run_inter_ns(const ChunkParams& p, unsigned gx, unsigned gy, unsigned zmul, cudaStream_t stream) {
+cudaError_t run_inter_ns(const ChunkParams& p, unsigned gx, unsigned gy, unsigned zmul, cudaStream_t stream,
+                         bool dependent) {
   using C = K3Cfg<NS>;
   const bool poll = p.wait_ns < kPollLimitNs;
   auto kernel = poll ? tc_inter<true, NS> : tc_inter<false, NS>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::BYTES);
   if (e != cudaSuccess) return e;
-  kernel<<<dim3(gx, gy, zmul * (unsigned)(p.dv / NS)), C::kThreads, C::BYTES, stream>>>(p);
-  return cudaGetLastError();
+  return launch_maybe_dependent(dependent, kernel, dim3(gx, gy, zmul * (unsigned)(p.dv / NS)), dim3(C::kThreads),
+                                (size_t)C::BYTES, stream, p);
 }
 // 32 state columns per CTA while those CTAs all fit the GPU at once (a chain
 // step of a 32-column CTA is shorter), else 64 where the value columns come
 // in 64s (half the CTAs, each at a longer step: less time in all once the
 // CTAs run in waves)
-cudaError_t run_inter(const ChunkParams& p, unsigned gx, unsigned gy, unsigned zmul, cudaStream_t stream) {
+// dependent: launched as the programmatic dependent of the intra-chunk kernel
+cudaError_t run_inter(const ChunkParams& p, unsigned gx, unsigned gy, unsigned zmul, cudaStream_t stream,
+                      bool dependent = false) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int64_t ctas32 = (int64_t)gx * gy * zmul * (p.dv / 32);
-  return (p.dv % 64 == 0 && ctas32 > sms) ? run_inter_ns<64>(p, gx, gy, zmul, stream)
-                                          : run_inter_ns<32>(p, gx, gy, zmul, stream);
+  return (p.dv % 64 == 0 && ctas32 > sms) ? run_inter_ns<64>(p, gx, gy, zmul, stream, dependent)
+                                          : run_inter_ns<32>(p, gx, gy, zmul, stream, dependent);
 }
 
 }  // namespace
@@ -48,15 +54,18 @@ const bool kHaveTensorCorePath = true;
 
 size_t tc_record_bytes() { return tcp::Rec::BYTES; }
 
+// The intra-chunk kernel as the planning kernel's programmatic dependent,
+// and the inter-chunk kernel as its (unless `mid` sits between them): each
+// starts its set-up while the kernel before it finishes.
 cudaError_t launch_tc_prefill(const ChunkParams& p, cudaStream_t stream, cudaEvent_t mid) {
   using namespace tcp;
-  cudaError_t e = launch_intra(p, stream);
+  cudaError_t e = launch_intra(p, stream, true);
   if (e != cudaSuccess) return e;
   if (mid) {
     e = cudaEventRecord(mid, stream);
     if (e != cudaSuccess) return e;
   }
-  return run_inter(p, (unsigned)p.num_seqs, (unsigned)p.H, 1, stream);
+  return run_inter(p, (unsigned)p.num_seqs, (unsigned)p.H, 1, stream, mid == nullptr);
 }
 
 namespace {

@@ -18,6 +18,11 @@ tc_intra(ChunkParams p, int64_t n_items, const __grid_constant__ RowMaps maps) {
   const int tid = threadIdx.x;
   if (tid < 32) tmem_alloc(&tmem_base, 256);
   if (tid == 0) init_intra_bars(&bars);
+  // (launched as the planning kernel's programmatic dependent) its chunk
+  // table is read from here on; the inter-chunk kernel may then be launched
+  // (its CTAs wait for this kernel's completion before they read)
+  pdl_wait();
+  pdl_launch_dependents();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
@@ -47,7 +52,7 @@ EncodeTiledFn encode_tiled() {
 
 namespace tcp {
 
-cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream) {
+cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream, bool dependent) {
   const bool head = p.gate_per_head != 0, conv = p.conv_width > 0;
   // (the convolution has no polling instance: its waits keep the suspending
   // form, which honours the limit too, only less promptly)
@@ -65,8 +70,8 @@ cudaError_t launch_intra(const ChunkParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int64_t n_items = p.max_chunks * (int64_t)p.H;
   const int64_t grid = n_items < 2 * (int64_t)sms ? n_items : 2 * (int64_t)sms;
-  kernel<<<(unsigned)grid, kThreads, Smem::BYTES, stream>>>(p, n_items, maps);
-  return cudaGetLastError();
+  return launch_maybe_dependent(dependent, kernel, dim3((unsigned)grid), dim3(kThreads), (size_t)Smem::BYTES,
+                                stream, p, n_items, maps);
 }
 
 }  // namespace tcp

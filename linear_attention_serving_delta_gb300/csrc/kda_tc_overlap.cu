@@ -86,24 +86,6 @@ __global__ void __launch_bounds__(OvlChainCfg::kThreads, 1) tc_inter_ovl(ChunkPa
   pdl_wait();
 }
 
-// a launch that may start before the kernel before it on the stream has
-// completed (programmatic stream serialization)
-template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                             const Args&... args) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
 }  // namespace
 }  // namespace tcp
 
@@ -129,10 +111,12 @@ cudaError_t launch_tc_overlap(const ChunkParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int64_t n_items = p.max_chunks * (int64_t)p.H;
   const int64_t grid = n_items < 2 * (int64_t)sms ? n_items : 2 * (int64_t)sms;
-  e = launch_dependent(k2, dim3((unsigned)grid), dim3(kThreads), (size_t)Smem::BYTES, stream, p, n_items, maps);
+  e = launch_maybe_dependent(true, k2, dim3((unsigned)grid), dim3(kThreads), (size_t)Smem::BYTES, stream, p,
+                             n_items, maps);
   if (e != cudaSuccess) return e;
-  return launch_dependent(tc_inter_ovl, dim3((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)(p.dv / kOvlNs)),
-                          dim3(OvlChainCfg::kThreads), (size_t)OvlChainCfg::BYTES, stream, p);
+  return launch_maybe_dependent(true, tc_inter_ovl,
+                                dim3((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)(p.dv / kOvlNs)),
+                                dim3(OvlChainCfg::kThreads), (size_t)OvlChainCfg::BYTES, stream, p);
 }
 
 }  // namespace kda

@@ -288,6 +288,20 @@ def test_prefill_ragged_varlen(dtype, dk, dv):
     assert_close(gpu, ref, TOL[dtype], f"{dtype} {dk}x{dv}", lens=lens)
 
 
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("f32", 32)])
+def test_prefill_many_sequences(dtype, d):
+    """1100 sequences of 0 to 40 tokens (some empty), with initial states and
+    snapshots every 64 tokens: the planning kernel's prefix sums over the
+    sequences span many warps and two passes of its 1024-thread block."""
+    rng = np.random.default_rng(77)
+    lens = [int(x) for x in rng.integers(0, 41, size=1100)]
+    lens[5] = lens[1023] = lens[1024] = 0
+    lens[1099] = 130
+    inp = make_inputs(lens, 2, d, d, dtype, 31, s0_std=0.02)
+    gpu, ref = run_both(inp, dtype, interval=64)
+    assert_close(gpu, ref, TOL[dtype], f"{dtype} many sequences", lens=lens)
+
+
 def sm_count():
     return torch.cuda.get_device_properties(0).multi_processor_count
 

@@ -57,6 +57,10 @@ KERNEL_SOURCES = {
                  "kda_tc.cuh", "kda_internal.cuh", "kda_common.cuh"],
     "tc_inter": ["kda_tc_inter.cu", "kda_tc_inter.cuh", "kda_tc_handoff.cuh", "kda_tc_common.cuh",
                  "kda_tc.cuh", "kda_internal.cuh", "kda_common.cuh"],
+    "tc_intra_ovl": ["kda_tc_overlap.cu", "kda_tc_intra.cuh", "kda_tc_inter.cuh", "kda_tc_handoff.cuh",
+                     "kda_tc_common.cuh", "kda_tc.cuh", "kda_internal.cuh", "kda_common.cuh"],
+    "tc_inter_ovl": ["kda_tc_overlap.cu", "kda_tc_intra.cuh", "kda_tc_inter.cuh", "kda_tc_handoff.cuh",
+                     "kda_tc_common.cuh", "kda_tc.cuh", "kda_internal.cuh", "kda_common.cuh"],
     "tc_fused": ["kda_tc_fused.cu", "kda_tc_intra.cuh", "kda_tc_inter.cuh", "kda_tc_handoff.cuh",
                  "kda_tc_common.cuh", "kda_tc.cuh", "kda_internal.cuh", "kda_common.cuh"],
     "decode_ring": ["kda_decode.cu", "kda_tc.cuh", "kda_internal.cuh", "kda_common.cuh"],
@@ -666,6 +670,9 @@ def gpu_arm(a):
     if a.fused_only:
         print(json.dumps(bench_fused(torch, kda, W, dev, steps=a.steps)))
         return
+    if a.overlap_only:
+        print(json.dumps(bench_overlap(torch, kda, W, dev, steps=a.steps)))
+        return
     if a.wide_only:
         print(json.dumps(bench_wide_heads(torch, kda, W, dev, steps=a.steps)))
         return
@@ -862,6 +869,8 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--overlap-only", action="store_true",
+                    help="only the 16-head prefill, separate and overlapped kernels (profiling)")
     ap.add_argument("--no-1m", action="store_true",
                     help="skip the million-token configuration (~100 GB of device memory)")
     ap.add_argument("--prefill-only", action="store_true",

@@ -9,8 +9,10 @@
 // fp32 block is its hi half next to its lo half (x = hi + lo to about
 // 2^-16), so one instruction multiplies both.  A tcgen05.mma costs about the
 // same for any N <= 64, so this doubles the precision of the state and U
-// operands for free.  The state is kept as two accumulators S = Sa + Sb (Sa
-// takes the hi products, Sb the lo products).
+// operands for free.  Each thread keeps its 16 state values in fp32
+// registers; MMA 2 writes the chunk's increment into two fresh accumulators
+// [Da | Db] (the hi and the lo products), and the write-back forms
+// S_{j+1} = Gamma_L(j) S_j + Da + Db.
 //
 // Two warps share each TMEM lane quarter (warps w and w+4), each taking 16 of
 // the 32 columns.  Step j of the walk, with S = S_j (the state entering
@@ -20,9 +22,9 @@
 //                  thread 64 then issues MMA 3 of chunk j-1 (M=128, N=64,
 //                  K=64): D1[(j-1) % 3][64..127] += A_qk [U_hi | U_lo]
 //   warps 0,1,4,5: U = U~ - W S_j as bf16 hi | lo, then thread 0 issues
-//                  MMA 2 (M=128, N=64, K=64): [Sa | Sb] += Kr^T [U_hi | U_lo]
-//   all:           S_{j+1} = Sa + Sb: the bf16 operand, a snapshot if chunk j
-//                  ends at one, and Sa <- Gamma_L(j+1) S_{j+1}, Sb <- 0
+//                  MMA 2 (M=128, N=64, K=64): [Da | Db] = Kr^T [U_hi | U_lo]
+//   all:           S_{j+1} = Gamma_L(j) S_j + Da + Db in registers: the bf16
+//                  operand, and a snapshot if chunk j ends at one
 // The chunk-to-chunk chain is MMA 1 -> U -> MMA 2 -> state write-back; the
 // output product, its store and the copies run beside it.  Records are
 // prefetched two chunks ahead with bulk copies (TMA engine).  TMEM holds
@@ -228,11 +230,10 @@ __device__ __forceinline__ void store_output(const ChunkParams& p, const Chunk& 
   }
 }
 
-// The state write-back of one TMEM lane (key channel c), this thread's 16
-// columns: the bf16 operand [hi | lo] of v, and Sa <- gl v, Sb <- 0.
+// The state operand of one key channel c, this thread's 16 columns: the
+// bf16 [hi | lo] pair of v.
 template <int NS>
-__device__ __forceinline__ void write_state(uint8_t* sop, uint32_t ds, int c, int h16, const float* v,
-                                            float gl) {
+__device__ __forceinline__ void write_operand(uint8_t* sop, int c, int h16, const float* v) {
 #pragma unroll
   for (int m = 0; m < kNh / 8; ++m) {
     uint4 hi, lo;
@@ -240,15 +241,6 @@ __device__ __forceinline__ void write_state(uint8_t* sop, uint32_t ds, int c, in
     *reinterpret_cast<uint4*>(sop + mnmajor_off(h16 + 8 * m, c, kSopSbo)) = hi;
     *reinterpret_cast<uint4*>(sop + mnmajor_off(NS + h16 + 8 * m, c, kSopSbo)) = lo;
   }
-  float s[kNh], z[kNh];
-#pragma unroll
-  for (int n = 0; n < kNh; ++n) {
-    s[n] = gl * v[n];
-    z[n] = 0.f;
-  }
-  tmem_st16(ds + h16, s);
-  tmem_st16(ds + NS + h16, z);
-  tmem_st_wait();
 }
 
 // The mbarriers of a chain CTA and its TMEM address
@@ -329,7 +321,7 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
   fence_after_sync();
   const uint32_t tmem = tmem_base;
   const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-  const uint32_t DS = tmem + 3 * kNop + lane_off;  // [Sa | Sb], lane = key channel
+  const uint32_t DS = tmem + 3 * kNop + lane_off;  // [Da | Db], lane = key channel
   // output accumulator of chunk j (this warp's lanes): [W;Qp] S_j, then
   // + A_qk U in lanes 64-127
   auto d1_of = [&](int64_t j) { return tmem + (uint32_t)(j % 3) * kNop; };
@@ -453,6 +445,7 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
   const int DK = p.dk, DV = p.dv;
   const bool row_live = c < DK;
   const size_t sbase = ((size_t)s * H + h) * DK * DV;
+  float sreg[kNh];  // this thread's 16 state values (key channel c), fp32
   {
     float v[kNh];
 #pragma unroll
@@ -465,13 +458,9 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
     if (trans)
 #pragma unroll
       for (int n = 0; n < kNh; ++n) v[n] = c == n0 + h16 + n ? 1.f : 0.f;
-    float gl = 1.f;
-    if (nchunks > 0) {
-      okl = okl && wait_chain(0, false);
-      if (okl) chain_waited = 1;  // a copy still in flight is left to the drain
-      gl = reinterpret_cast<const float*>(slot_of(0) + C::GL)[c];
-    }
-    write_state<NS>(SOP, DS, c, h16, v, gl);
+#pragma unroll
+    for (int n = 0; n < kNh; ++n) sreg[n] = v[n];
+    write_operand<NS>(SOP, c, h16, v);
   }
 
   const uint32_t id = idesc_bf16(128, kNop, 0, 1);     // B operands MN-major
@@ -509,8 +498,15 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
     uint8_t* uop = u_of(it);
     const Chunk ch = next;  // chunk entries are read one step ahead
     if (it + 1 < nchunks) next = p.chunks[c_begin + it + 1];
-    // the state operand and TMEM state of this step are written; this
-    // slot's copies have landed (waited during the previous write-back)
+    // this chunk's operands (kFused: copied now if their record came late;
+    // kSplit: part B too) have landed; Gamma_L(it) is read before any copy
+    // can take the slot (kSplit: part A of chunk it+1, during this step)
+    if (kFused && tid == kLoadThread && okl && chain_issued == it) okl = issue_chain(it, true);
+    if (kSplit && tid == kLoadThread && okl && b_issued == it) okl = issue_b(it, true);
+    okl = okl && wait_chain(it, false);
+    if (okl) chain_waited = it + 1;  // a copy still in flight is left to the drain
+    const float gl_cur = reinterpret_cast<const float*>(slot_of(it) + C::GL)[c];
+    // the state operand of this step is written
     fence_async_smem();
     fence_before_sync();
     ok = __syncthreads_and(okl);
@@ -620,25 +616,26 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
       }
       fence_async_smem();
       asm volatile("bar.sync %0, %1;" ::"n"(kUBarrier), "n"(C::kUThreads) : "memory");
-      // MMA 2, the state chain: [Sa | Sb] += Kr^T [U_hi | U_lo]
+      // MMA 2, the state chain: [Da | Db] = Kr^T [U_hi | U_lo]
       if (tid == kMmaThread) {
         const uint32_t ub = smem_u32(uop);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_bf16(DS - lane_off, sdesc(smem_u32(slot + C::AK) + k * 256, 128, Rec::kAkSbo),
-                   sdesc(ub + k * 256, 128, kUopSbo), id_ak, 1);
+                   sdesc(ub + k * 256, 128, kUopSbo), id_ak, k > 0);
         mma_commit(&bar_mma2);
       }
     }
     ph1 ^= 1;
-    // the state write-back: S_{j+1} = Sa + Sb
+    // the state write-back: S_{j+1} = Gamma_L(j) S_j + Da + Db
     okl = okl && mbar_wait_t<kPoll>(&bar_mma2, ph2, p.wait_ns);
     ph2 ^= 1;
     fence_after_sync();
     // with a 2-slot ring, this chunk's slot takes chunk it+2 as soon as MMA 2
-    // has read it (MMA 1 and the U warps before it): a step of lead.  (kFused)
-    // only if its record is already published; else it is copied before the
-    // wait for it in the next step's write-back.
+    // has read it (MMA 1 and the U warps before it; Gamma_L was read at the
+    // step's top): a step of lead.  (kFused) only if its record is already
+    // published; else it is copied before the wait for it at the top of its
+    // step.
     if (C::kSlots == 2 && tid == kLoadThread && okl && it + 2 < nchunks && chain_issued == it + 2)
       okl = issue_chain(it + 2, false);
     // (kSplit) part B of chunk it+1 goes in now that MMA 2 has read AK and
@@ -655,21 +652,18 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
     {
       float v[kNh];
       tmem_ld_sum<NS>(DS, h16, v);
+#pragma unroll
+      for (int n = 0; n < kNh; ++n) {
+        v[n] = fmaf(gl_cur, sreg[n], v[n]);
+        sreg[n] = v[n];
+      }
       if (ch.snap_slot >= 0 && p.snapshots && !pass1 && row_live) {
         float* dst = p.snapshots + ((size_t)ch.snap_slot * H + h) * DK * DV + (size_t)c * DV + n0 + h16;
 #pragma unroll
         for (int n = 0; n < kNh; n += 4)
           *reinterpret_cast<float4*>(dst + n) = make_float4(v[n], v[n + 1], v[n + 2], v[n + 3]);
       }
-      float gl = 1.f;  // the last chunk leaves S_n itself in TMEM
-      if (it + 1 < nchunks) {
-        if (kFused && tid == kLoadThread && okl && chain_issued == it + 1) okl = issue_chain(it + 1, true);
-        if (kSplit && tid == kLoadThread && okl && b_issued == it + 1) okl = issue_b(it + 1, true);
-        okl = okl && wait_chain(it + 1, false);
-        if (okl) chain_waited = it + 2;
-        gl = reinterpret_cast<const float*>(slot_of(it + 1) + C::GL)[c];
-      }
-      write_state<NS>(SOP, DS, c, h16, v, gl);
+      write_operand<NS>(SOP, c, h16, v);
     }
     prev2 = prev1;
     prev1 = ch;
@@ -696,14 +690,11 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
   ok = __syncthreads_and(ok && okl);
   fence_after_sync();
   float* const fin = trans ? p.trans : p.final_state;
-  if (ok && fin) {
-    float v[kNh];
-    tmem_ld_sum<NS>(DS, h16, v);  // warp-collective: outside the row test
+  if (ok && fin && row_live) {
     float* dst = fin + sbase + (size_t)c * DV + n0 + h16;
-    if (row_live)
 #pragma unroll
-      for (int n = 0; n < kNh; n += 4)
-        *reinterpret_cast<float4*>(dst + n) = make_float4(v[n], v[n + 1], v[n + 2], v[n + 3]);
+    for (int n = 0; n < kNh; n += 4)
+      *reinterpret_cast<float4*>(dst + n) = make_float4(sreg[n], sreg[n + 1], sreg[n + 2], sreg[n + 3]);
   }
   if (!ok) {
     // let the copies and MMAs still in flight finish (each wait bounded)

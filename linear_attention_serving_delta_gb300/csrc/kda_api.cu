@@ -198,6 +198,7 @@ WsLayout prefill_layout(const kda_prefill_args* a) {
   L.bnd_nonaligned = take(sizeof(int32_t) * (nb + N + 1));
   L.bnd_nonmult = take(sizeof(int32_t) * (nb + N + 1));
   L.seq_aux = take(sizeof(int64_t) * 3 * N);  // seq_len [N] + seq_bnd [2N]
+  L.seq_order = take(sizeof(int32_t) * N);
   L.chunks = take(sizeof(Chunk) * (size_t)L.max_chunks);
   L.inter = take(L.rec_bytes * (size_t)L.max_chunks * (size_t)a->num_heads);
   if (fused_shape(a) && a->schedule == KDA_SCHEDULE_FUSED)
@@ -283,6 +284,9 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
   pp.bnd_nonmult = reinterpret_cast<int32_t*>(w + L.bnd_nonmult);
   pp.seq_len = reinterpret_cast<int64_t*>(w + L.seq_aux);
   pp.seq_bnd = pp.seq_len + a->num_seqs;
+  // the chains of long sequences first, where several sequences' chains
+  // share the GPU (the plain tensor-core and CUDA-core prefill)
+  if (P == 1 && a->num_seqs > 1) pp.seq_order = reinterpret_cast<int32_t*>(w + L.seq_order);
   pp.chunks = reinterpret_cast<Chunk*>(w + L.chunks);
 
   // the path on the tensor cores (no device query for the other paths)
@@ -330,6 +334,7 @@ kda_status_t kda_prefill(const kda_prefill_args* a, void* ws, size_t ws_bytes, v
   cp.status = pp.status;
   cp.meta = pp.meta;
   cp.seq_chunk_begin = pp.seq_chunk_begin;
+  cp.seq_order = pp.seq_order;
   cp.chunks = pp.chunks;
   cp.inter = reinterpret_cast<float*>(w + L.inter);
   cp.rec_floats = L.rec_bytes / sizeof(float);

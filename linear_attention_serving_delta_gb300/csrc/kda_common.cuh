@@ -148,6 +148,7 @@ struct WsLayout {
   // arguments can take it); (overlapped) its counters, right before the
   // flags, and the words of both, which the planning kernel clears
   size_t rec_ready = 0;
+  size_t seq_order = 0;
   size_t ovl = 0;
   int64_t ovl_words = 0;
 };

@@ -38,6 +38,9 @@ struct PlanParams {
   int32_t* bnd_nonaligned;  // [num_boundaries + N]
   int32_t* bnd_nonmult;     // [num_boundaries + N]
   Chunk* chunks;            // [max_chunks]
+  // (or null) the sequences by chunk count, longest first (ties by index):
+  // the inter-chunk kernels start the chains of long sequences first
+  int32_t* seq_order;       // [N]
   // words the planning kernel clears before anything else (the overlapped
   // schedule's record flags and counters), or null
   uint32_t* zero_words;
@@ -76,6 +79,10 @@ struct ChunkParams {
   const PlanMeta* meta;
   const int64_t* seq_chunk_begin;
   const Chunk* chunks;
+  // (or null) the sequences longest first (PlanParams::seq_order): the
+  // inter-chunk kernels take their CTAs' sequences in that order, so that
+  // the chains that run longest start in the first wave
+  const int32_t* seq_order;
   float* inter;     // [max_chunks][H] records
   size_t rec_floats;
   // segment scan (tensor-core path): mode kScanPass1 runs grid z = 0..3 from

@@ -231,6 +231,32 @@ plan_kernel(PlanParams p) {
   empty.snap_slot = -1;
   for (int64_t ci = total + tid; ci < p.max_chunks; ci += kPlanThreads) p.chunks[ci] = empty;
   if (flags) atomicOr(&shf, flags);
+  // the sequences by chunk count, longest first: thread s finds the rank of
+  // sequence s among the counts in shared memory (up to kPlanThreads
+  // sequences; more keep their own order)
+  if (p.seq_order) {
+    int32_t* cnt = reinterpret_cast<int32_t*>(sh);
+    const int32_t N = p.num_seqs;
+    if (N <= kPlanThreads) {
+      int32_t mine = 0;
+      if (tid < N) {
+        const int64_t n = p.seq_chunk_begin[tid + 1] - p.seq_chunk_begin[tid];
+        mine = n < INT32_MAX ? (int32_t)n : INT32_MAX;
+        cnt[tid] = mine;
+      }
+      __syncthreads();
+      if (tid < N) {
+        int32_t rank = 0;
+        for (int32_t t = 0; t < N; ++t) {
+          const int32_t o = cnt[t];
+          rank += (o > mine || (o == mine && t < tid)) ? 1 : 0;
+        }
+        p.seq_order[rank] = tid;
+      }
+    } else {
+      for (int32_t s = tid; s < N; s += kPlanThreads) p.seq_order[s] = s;
+    }
+  }
   __syncthreads();
   if (tid == 0 && shf) atomicOr(p.status, shf);
 }

@@ -671,7 +671,17 @@ simt_inter(ChunkParams p) {
   extern __shared__ float sm[];
   constexpr int NO = NS / 8;          // column octets
   constexpr int kMaxRB = 4;           // key rows per thread (dk <= 256)
-  const int s = blockIdx.x, h = blockIdx.y, n0 = blockIdx.z * NS;
+  // CTAs start in the order of their linear index: with seq_order, the
+  // sequences longest first, each with all its heads and column slices
+  int s = blockIdx.x, h = blockIdx.y, zs = blockIdx.z;
+  if (p.seq_order) {
+    const unsigned lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    const unsigned per = gridDim.y * gridDim.z, r = lin % per;
+    s = p.seq_order[lin / per];
+    h = (int)(r / gridDim.z);
+    zs = (int)(r % gridDim.z);
+  }
+  const int n0 = zs * NS;
   const int H = p.H, dk = p.dk, dv = p.dv, tid = threadIdx.x;
   const int64_t c_begin = p.seq_chunk_begin[s], c_end = p.seq_chunk_begin[s + 1];
   if (c_end > c_begin && p.meta->total_chunks == 0) return;  // chunk table overflowed

@@ -15,7 +15,17 @@ __global__ void __launch_bounds__(K3Cfg<NS>::kThreads, 1) tc_inter(ChunkParams p
   // (launched as the intra-chunk kernel's programmatic dependent) its
   // records are read from here on
   pdl_wait();
-  inter_chain<kPoll, NS, false>(p, (int)blockIdx.x, (int)blockIdx.y, (int)blockIdx.z, sm, bars);
+  int s = (int)blockIdx.x, h = (int)blockIdx.y, z = (int)blockIdx.z;
+  if (p.seq_order) {
+    // CTAs start in the order of their linear index: the sequences longest
+    // first, each with all its heads and column slices
+    const unsigned lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    const unsigned per = gridDim.y * gridDim.z, r = lin % per;
+    s = p.seq_order[lin / per];
+    h = (int)(r / gridDim.z);
+    z = (int)(r % gridDim.z);
+  }
+  inter_chain<kPoll, NS, false>(p, s, h, z, sm, bars);
 }
 
 // tc_inter with the wait mode its limit asks for, over grid (gx, gy, zmul x

@@ -431,6 +431,9 @@ __device__ __forceinline__ void inter_chain(const ChunkParams& p, int s, int h, 
     return true;
   };
   if (tid == kLoadThread) {
+    // (kFused) the first scan of the flags before any copy is issued: its
+    // acquire fence then waits behind none
+    if (kFused && nchunks > 0) ready(0, false);
     for (int64_t j = 0; okl && j < C::kSlots && j < nchunks && chain_issued == j; ++j)
       okl = issue_chain(j, j == 0);
     if (kSplit && okl && nchunks > 0) okl = issue_b(0, true);

@@ -434,6 +434,12 @@ decode_ring(kda_decode_args a, int64_t n_items, const kda_layer_args l, const __
     }
     tc::mbar_init_fence();
   }
+  // (launched as the programmatic dependent of the kernel before it, the
+  // previous decode step on the same pool as a rule) nothing it wrote is
+  // read before this point; the next step may be launched now (its CTAs
+  // take the SMs this one leaves and wait there likewise)
+  pdl_wait();
+  pdl_launch_dependents();
   __syncthreads();
 
   const uint64_t lim = a.wait_limit_ns > 0 ? (uint64_t)a.wait_limit_ns : tc::kWaitLimitNs;
@@ -648,8 +654,8 @@ cudaError_t launch_ring(const kda_decode_args& a, const kda_layer_args& l, cudaS
   if (R::NS > 1 && !encode_state_map<DK, DV>(&smap, a)) return cudaErrorInvalidValue;
   const int64_t n_items = (int64_t)a.batch * a.num_heads * R::NS / G, slots = (int64_t)sms * R::CTAS;
   const int64_t grid = n_items < slots ? n_items : slots;
-  kernel<<<(unsigned)grid, kRingAllThreads, R::BYTES, stream>>>(a, n_items, l, smap);
-  return cudaGetLastError();
+  return launch_maybe_dependent(true, kernel, dim3((unsigned)grid), dim3(kRingAllThreads), (size_t)R::BYTES,
+                                stream, a, n_items, l, smap);
 }
 
 template <typename TIn, int DK, int DV>

@@ -223,8 +223,8 @@ typedef struct {
  * two CTAs per SM: a CTA either runs the chain of one (sequence, head,
  * 32-column slice of the state) or a pipeline of (chunk, head) items taken in
  * chunk order.  Each record is published once written; a chain copies it as
- * soon as it sees it, from L2, so the records are read back from L2 rather
- * than HBM and the chains run while the items are made.  Pipelines never wait
+ * soon as it sees it, so the chains run while the items are made (and read
+ * the records from L2 while they keep up).  Pipelines never wait
  * for chains and the chains are placed after the pipelines they read, so no
  * wait depends on the CTAs being resident together.  It applies without the
  * segment scan when the chains (num_seqs x num_heads x dv / 32) are at most

@@ -208,6 +208,7 @@ __device__ void fill_segment(const PlanParams& p, int64_t gidx, int32_t& bad) {
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(PlanParams p) {
   __shared__ int64_t sh[kPlanThreads];
+  __shared__ int32_t cnt[kPlanThreads];  // chunk counts of the sequences (their order)
   __shared__ int32_t shf;
   const int tid = threadIdx.x;
   pdl_launch_dependents();
@@ -235,7 +236,6 @@ plan_kernel(PlanParams p) {
   // sequence s among the counts in shared memory (up to kPlanThreads
   // sequences; more keep their own order)
   if (p.seq_order) {
-    int32_t* cnt = reinterpret_cast<int32_t*>(sh);
     const int32_t N = p.num_seqs;
     if (N <= kPlanThreads) {
       int32_t mine = 0;

@@ -31,7 +31,6 @@ namespace {
 constexpr int kOvlNs = 32;  // state columns of a chain CTA
 using OvlChainCfg = K3Cfg<kOvlNs, false>;
 
-
 // (thread 0 of a K2 CTA) whether this CTA stays for the items past the
 // split.  The first K2 CTA to start on an SM decides for the SM: it stays
 // if fewer than ovl_stay_sms SMs have been elected.  A later one follows
